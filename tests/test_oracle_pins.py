@@ -1,0 +1,432 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each check takes the implementation under test as an argument, so the
+mutation tests at the bottom can run the same checks on deliberately broken
+copies of oracle functions (planted here on the CPU) and show that each
+plausible mistake is caught.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+from scipy.special import logsumexp
+
+import oracle
+from oracle import decode as od
+from synthetic import make_tiny_sequence, workload
+
+RNG = np.random.default_rng(12345)
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ rounding
+def check_round_bf16(fn):
+    # fp32-representable values: RNE fp64->bf16 equals torch's fp32->bf16 RNE
+    x32 = torch.randn(20000, dtype=torch.float32) * torch.exp(torch.randn(20000) * 8)
+    ref = x32.to(torch.bfloat16).to(torch.float64).numpy()
+    got = fn(x32.to(torch.float64).numpy())
+    assert np.array_equal(got, ref)
+    # exact ties go to the even neighbour; one fp64 ulp past a tie goes away from zero
+    one_plus_half = 1.0 + 2.0 ** -8  # halfway between 1 and 1 + 2^-7
+    assert fn(np.array([one_plus_half]))[0] == 1.0
+    three_half = 1.0 + 3 * 2.0 ** -8  # halfway between 1+2^-7 (odd) and 1+2^-6 (even)
+    assert fn(np.array([three_half]))[0] == 1.0 + 2.0 ** -6
+    assert fn(np.array([np.nextafter(one_plus_half, 2.0)]))[0] == 1.0 + 2.0 ** -7
+    assert fn(np.array([-np.nextafter(one_plus_half, 2.0)]))[0] == -(1.0 + 2.0 ** -7)
+    # values that fp32 rounding would tie but fp64 does not (no double rounding)
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert fn(np.array([v]))[0] == 1.0 + 2.0 ** -7
+    assert fn(np.array([0.0]))[0] == 0.0
+    assert np.isinf(fn(np.array([3.5e38]))[0])
+
+
+def test_round_bf16():
+    check_round_bf16(oracle.round_bf16)
+
+
+def test_round_to_f32_matches_numpy_cast():
+    x = RNG.standard_normal(1000)
+    assert np.array_equal(oracle.round_to(x, "f32"), x.astype(np.float32).astype(np.float64))
+    assert np.array_equal(oracle.round_to(x, "f64"), x)
+
+
+# ---------------------------------------------------------------------- RoPE
+def check_rope(rotate_fn, inv_freq_fn):
+    d, base = 64, 10000.0
+    theta = inv_freq_fn(d, base)
+    assert theta.shape == (d // 2,)
+    assert theta[0] == 1.0
+    # geometric progression with ratio base^(-2/d), last term base^(-(d-2)/d)
+    ratio = theta[1:] / theta[:-1]
+    assert np.allclose(ratio, math.exp(-2.0 / d * math.log(base)), rtol=1e-13, atol=0)
+    assert math.isclose(theta[-1], math.exp(-(d - 2) / d * math.log(base)), rel_tol=1e-13)
+    x = RNG.standard_normal((3, d))
+    # position 0 is the identity
+    assert np.array_equal(rotate_fn(x, 0, base), x)
+    for pos in (1, 7, 4095, 131071):
+        y = rotate_fn(x, pos, base)
+        # complex form: (x0 + i x1) * exp(i pos theta) for each adjacent pair
+        z = (x[:, 0::2] + 1j * x[:, 1::2]) * np.exp(1j * pos * theta)
+        assert np.allclose(y[:, 0::2], z.real, rtol=0, atol=1e-12)
+        assert np.allclose(y[:, 1::2], z.imag, rtol=0, atol=1e-12)
+        # every pair keeps its norm
+        assert np.allclose(np.hypot(y[:, 0::2], y[:, 1::2]), np.hypot(x[:, 0::2], x[:, 1::2]), atol=1e-12)
+    # scores depend only on the position difference
+    q, k = RNG.standard_normal(d), RNG.standard_normal(d)
+    for m, n, shift in ((5, 2, 100), (17, 17, 3), (1000, 3, 7)):
+        a = rotate_fn(q, m, base) @ rotate_fn(k, n, base)
+        b = rotate_fn(q, m + shift, base) @ rotate_fn(k, n + shift, base)
+        assert abs(a - b) < 1e-11
+    # rotations compose: R(a) R(b) = R(a + b)
+    assert np.allclose(rotate_fn(rotate_fn(x, 3, base), 5, base), rotate_fn(x, 8, base), atol=1e-12)
+    # direction: position 1 turns (1, 0) of pair 0 to (cos 1, sin 1)
+    e = np.zeros(d)
+    e[0] = 1.0
+    r = rotate_fn(e, 1, base)
+    assert math.isclose(r[0], math.cos(1.0), abs_tol=1e-15) and math.isclose(r[1], math.sin(1.0), abs_tol=1e-15)
+
+
+def test_rope():
+    check_rope(oracle.rope_rotate, oracle.rope_inv_freq)
+
+
+# ----------------------------------------------------------------- attention
+def _sdpa(q_rot, K, V, scale):
+    """torch scaled_dot_product_attention, fp64 on CPU, GQA enabled (library routine)."""
+    q = torch.from_numpy(q_rot)[None, :, None, :]
+    k = torch.from_numpy(K)[None]
+    v = torch.from_numpy(V)[None]
+    return F.scaled_dot_product_attention(q, k, v, scale=scale, enable_gqa=True)[0, :, 0, :].numpy()
+
+
+def check_gqa(attn_fn):
+    for h_q, h_kv, L, d in ((8, 2, 37, 64), (4, 4, 5, 32), (32, 1, 64, 128), (6, 3, 1, 16), (12, 4, 100, 64)):
+        q = RNG.standard_normal((h_q, d))
+        K = RNG.standard_normal((h_kv, L, d))
+        V = RNG.standard_normal((h_kv, L, d))
+        scale = 1.0 / math.sqrt(d)
+        out, lse = attn_fn(q, K, V, scale)
+        assert np.allclose(out, _sdpa(q, K, V, scale), rtol=0, atol=1e-12)
+        G = h_q // h_kv
+        for h in range(h_q):
+            s = K[h // G] @ q[h] * scale
+            assert abs(lse[h] - logsumexp(s)) < 1e-12
+
+
+def test_gqa_matches_library_sdpa():
+    check_gqa(oracle.gqa_attention)
+
+
+def test_gqa_special_cases():
+    d = 64
+    # L = 1: the single value is the output, exactly
+    q = RNG.standard_normal((4, d))
+    K = RNG.standard_normal((2, 1, d))
+    V = RNG.standard_normal((2, 1, d))
+    out, lse = oracle.gqa_attention(q, K, V, 0.125)
+    assert np.array_equal(out, np.repeat(V[:, 0], 2, axis=0))
+    # q = 0: uniform weights, output is the mean of V
+    K = RNG.standard_normal((2, 50, d))
+    V = RNG.standard_normal((2, 50, d))
+    out, lse = oracle.gqa_attention(np.zeros((4, d)), K, V, 0.125)
+    assert np.allclose(out, np.repeat(V.mean(axis=1), 2, axis=0), atol=1e-14)
+    assert np.allclose(lse, math.log(50), atol=1e-14)
+    # rows of the attention matrix sum to 1
+    q = RNG.standard_normal((8, d))
+    _, _, w = oracle.gqa_attention(q, K, V, 0.125, return_weights=True)
+    assert np.all(w >= 0) and np.max(np.abs(w.sum(axis=1) - 1.0)) <= 1e-12
+    # heads sharing a KV head but with different queries give different outputs
+    out, _ = oracle.gqa_attention(q, K, V, 0.125)
+    assert not np.allclose(out[0], out[1])
+
+
+def test_gqa_reduces_to_mha_and_mqa():
+    d, L = 64, 33
+    q = RNG.standard_normal((8, d))
+    K = RNG.standard_normal((8, L, d))
+    V = RNG.standard_normal((8, L, d))
+    assert np.allclose(oracle.gqa_attention(q, K, V, 0.125)[0], oracle.mha_attention(q, K, V, 0.125), atol=1e-13)
+    assert np.allclose(oracle.gqa_attention(q, K[:1], V[:1], 0.125)[0], oracle.mqa_attention(q, K[0], V[0], 0.125),
+                       atol=1e-13)
+    # the MHA / MQA routines themselves against the library
+    assert np.allclose(oracle.mha_attention(q, K, V, 0.125), _sdpa(q, K, V, 0.125), atol=1e-12)
+    assert np.allclose(oracle.mqa_attention(q, K[0], V[0], 0.125), _sdpa(q, K[:1], V[:1], 0.125), atol=1e-12)
+
+
+def test_causal_attention_matches_library():
+    h_q, h_kv, n, d = 8, 2, 23, 32
+    Q = RNG.standard_normal((h_q, n, d))
+    K = RNG.standard_normal((h_kv, n, d))
+    V = RNG.standard_normal((h_kv, n, d))
+    ref = F.scaled_dot_product_attention(torch.from_numpy(Q)[None], torch.from_numpy(K)[None],
+                                         torch.from_numpy(V)[None], is_causal=True, scale=0.3,
+                                         enable_gqa=True)[0].numpy()
+    assert np.allclose(oracle.causal_attention(Q, K, V, 0.3), ref, atol=1e-12)
+
+
+def check_split_combine(partial_fn, combine_fn):
+    h_q, h_kv, L, d = 8, 2, 300, 64
+    q = RNG.standard_normal((h_q, d))
+    K = RNG.standard_normal((h_kv, L, d))
+    V = RNG.standard_normal((h_kv, L, d))
+    full, full_lse = oracle.gqa_attention(q, K, V, 0.125)
+    for bounds in ([0, 300], [0, 64, 300], [0, 1, 2, 299, 300], [0, 100, 100, 250, 300, 300]):
+        parts = [partial_fn(q, K, V, 0.125, a, b) for a, b in zip(bounds[:-1], bounds[1:])]
+        out, lse = combine_fn(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        assert np.allclose(out, full, atol=1e-13)
+        assert np.allclose(lse, full_lse, atol=1e-13)
+
+
+def test_split_combine_is_exact():
+    check_split_combine(oracle.attention_partial, oracle.lse_combine)
+
+
+def test_empty_partial():
+    o, lse = oracle.attention_partial(np.ones((2, 8)), np.ones((1, 4, 8)), np.ones((1, 4, 8)), 1.0, 3, 3)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+# ------------------------------------------------------------- paged layout
+def test_page_slots_match_printed_example(golden_dir):
+    ex = _load(golden_dir, "paged_example.json")
+    for t, page, off in ex["slots"]:
+        assert oracle.page_slot(ex["block_table"], t, ex["page_size"]) == (page, off)
+    n_blocks = -(-ex["length"] // ex["page_size"])
+    assert n_blocks == len(ex["block_table"])
+    assert ex["length"] - (n_blocks - 1) * ex["page_size"] == ex["last_block_filled"]
+    assert n_blocks * ex["page_size"] - ex["length"] <= ex["max_waste_tokens"]
+
+
+def _contiguous_to_paged(K, lens, page_size, rng):
+    """Scatter a contiguous cache into a shuffled pool through a block table."""
+    B, h_kv, cap, d = K.shape
+    npages = [-(-int(L) // page_size) for L in lens]
+    total = sum(npages) + 3
+    perm = rng.permutation(total)
+    table = -np.ones((B, max(npages) + 2), dtype=np.int64)
+    pool = rng.standard_normal((total, h_kv, page_size, d))  # junk in unused rows
+    off = 0
+    for b in range(B):
+        for i in range(npages[b]):
+            page = perm[off + i]
+            table[b, i] = page
+            lo, hi = i * page_size, min((i + 1) * page_size, cap)
+            pool[page, :, : hi - lo, :] = K[b, :, lo:hi, :]
+        off += npages[b]
+    return pool, table
+
+
+def test_paged_equals_contiguous():
+    rng = np.random.default_rng(7)
+    B, h_q, h_kv, d, ps = 3, 8, 2, 64, 16
+    lens = np.array([1, 40, 64])
+    cap = 64
+    Kc = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    Vc = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    q = oracle.round_bf16(rng.standard_normal((B, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    rc = oracle.decode_step_contiguous(Kc, Vc, q, k, v, lens, 10000.0, 0.125, "bf16")
+    pk, table = _contiguous_to_paged(Kc, lens, ps, np.random.default_rng(1))
+    pv, _ = _contiguous_to_paged(Vc, lens, ps, np.random.default_rng(1))
+    rp = oracle.decode_step_paged(pk, pv, table, q, k, v, lens, ps, 10000.0, 0.125, "bf16")
+    assert np.array_equal(rp["out"], rc["out"])
+    assert np.array_equal(rp["lse"], rc["lse"])
+    for b in range(B):
+        L = int(lens[b])
+        assert np.array_equal(oracle.gather_paged(rp["k_pool"], table[b], L, ps), rc["k_cache"][b, :, :L])
+        assert np.array_equal(oracle.gather_paged(rp["v_pool"], table[b], L, ps), rc["v_cache"][b, :, :L])
+
+
+def test_append_writes_only_the_new_slot():
+    rng = np.random.default_rng(3)
+    B, h_q, h_kv, d, cap = 2, 4, 2, 32, 10
+    Kc = rng.standard_normal((B, h_kv, cap, d))
+    Vc = rng.standard_normal((B, h_kv, cap, d))
+    q, k, v = rng.standard_normal((B, h_q, d)), rng.standard_normal((B, h_kv, d)), rng.standard_normal((B, h_kv, d))
+    lens = np.array([4, 10])
+    r = oracle.decode_step_contiguous(Kc, Vc, q, k, v, lens, 10000.0, 0.2, "f64")
+    changed = np.argwhere(np.any(r["v_cache"] != Vc, axis=-1))
+    assert sorted(map(tuple, changed)) == [(b, h, int(lens[b]) - 1) for b in range(B) for h in range(h_kv)]
+    assert np.array_equal(np.any(r["k_cache"] != Kc, axis=-1), np.any(r["v_cache"] != Vc, axis=-1))
+    assert np.array_equal(r["v_cache"][0, :, 3], v[0])
+
+
+def test_decode_unit_equals_full_step():
+    rng = np.random.default_rng(11)
+    B, h_q, h_kv, d, cap = 2, 8, 2, 64, 70
+    Kc = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    Vc = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    q = oracle.round_bf16(rng.standard_normal((B, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    lens = np.array([70, 33])
+    r = oracle.decode_step_contiguous(Kc, Vc, q, k, v, lens, 10000.0, 0.125, "bf16")
+    G = h_q // h_kv
+    for b in range(B):
+        for j in range(h_kv):
+            out, lse, ks = oracle.decode_unit(q[b, j * G:(j + 1) * G], k[b, j], v[b, j], Kc[b, j], Vc[b, j],
+                                              lens[b], 10000.0, 0.125, "bf16")
+            assert np.array_equal(out, r["out"][b, j * G:(j + 1) * G])
+            assert np.array_equal(ks, r["k_cache"][b, j, lens[b] - 1])
+
+
+# ---------------------------------------------- cached == uncached, counts
+@pytest.mark.parametrize("evals", [16, 64])
+def test_cached_equals_recomputation_and_projection_counts(golden_dir, evals):
+    gold = {c["evals"]: c for c in _load(golden_dir, "projection_counts.json")["cases"]}[evals]
+    w = workload("tiny")
+    seq = make_tiny_sequence(w, prompt_len=gold["prompt_len"], decode_evals=evals)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    outs, lses, n_cached, written = oracle.run_cached_sequence(seq.q, seq.k, seq.v, seq.prompt_len, evals,
+                                                               w.rope_base, scale, "f64")
+    ref, last_rows, n_uncached = oracle.run_uncached_sequence(seq.q, seq.k, seq.v, seq.prompt_len, evals,
+                                                              w.rope_base, scale)
+    # the pages' printed counts, and the closed form printed beside them
+    assert (n_uncached, n_cached) == (gold["no_cache"], gold["with_cache"])
+    assert oracle.projection_counts_closed_form(gold["prompt_len"], evals) == (gold["no_cache"], gold["with_cache"])
+    if "ratio" in gold:
+        assert round(n_uncached / n_cached, 1) == gold["ratio"]
+    else:
+        assert round(n_uncached / n_cached) == gold["ratio_approx"]
+    # cached decode equals brute-force recomputation under the causal mask
+    assert np.max(np.abs(outs - ref)) <= 1e-12
+    # ... and every earlier cached output equals the matching row of the final causal pass
+    n = seq.prompt_len + evals - 1
+    for i, p in enumerate(range(seq.prompt_len - 1, n)):
+        assert np.max(np.abs(outs[i] - last_rows[:, :, p, :])) <= 1e-12
+    # the cache holds 2 * T * H_kv * d scalars per layer (T = stored positions)
+    assert int(written.sum()) // w.batch == oracle.layer_cache_scalars(n, w.h_kv, w.head_dim)
+
+
+def test_decode_step_matches_recomputation():
+    """One decode step over a cache built from the first n-1 positions equals
+    the last row of full causal recomputation over all n positions."""
+    w = workload("tiny")
+    seq = make_tiny_sequence(w)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    n = seq.prompt_len + seq.decode_evals - 1
+    q = seq.q.double().numpy()
+    k = seq.k.double().numpy()
+    v = seq.v.double().numpy()
+    K = np.zeros((w.batch, w.h_kv, n, w.head_dim))
+    V = np.zeros_like(K)
+    for p in range(n - 1):
+        K[:, :, p] = np.stack([oracle.rope_rotate(k[p, b], p, w.rope_base) for b in range(w.batch)])
+        V[:, :, p] = v[p]
+    r = oracle.decode_step_contiguous(K, V, q[n - 1], k[n - 1], v[n - 1], np.full(w.batch, n), w.rope_base, scale,
+                                      "f64")
+    _, last_rows, _ = oracle.run_uncached_sequence(seq.q, seq.k, seq.v, seq.prompt_len, seq.decode_evals,
+                                                   w.rope_base, scale)
+    assert np.max(np.abs(r["out"] - last_rows[:, :, n - 1, :])) <= 1e-12
+
+
+# ------------------------------------------------------------ byte figures
+UNITS = {"GB": 1e9, "TB": 1e12, "MiB": 2.0 ** 20, "GiB": 2.0 ** 30, "KiB": 2.0 ** 10}
+
+
+def test_kv_bytes_match_printed_figures(golden_dir):
+    g = _load(golden_dir, "kv_bytes.json")
+    for c in g["per_token"]:
+        got = oracle.kv_bytes_per_token(c["layers"], c["kv_heads"], c["head_dim"], c["bytes"])
+        if "exact" in c:
+            assert got == c["exact"], c["source"]
+        else:
+            assert round(got / UNITS[c["unit"]], c["decimals"]) == c["rounded"], c["source"]
+    for c in g["totals"]:
+        got = oracle.kv_cache_bytes(c["layers"], c["kv_heads"], c["head_dim"], c["bytes"], c["seq_len"], c["batch"])
+        assert round(got / UNITS[c["unit"]], c["decimals"]) == c["rounded"], c["source"]
+    for c in g["bounds"]:
+        got = oracle.kv_cache_bytes(c["layers"], c["kv_heads"], c["head_dim"], c["bytes"], c["seq_len"], c["batch"])
+        if "greater_than" in c:
+            assert got > c["greater_than"], c["source"]
+        else:
+            assert abs(got / c["about"] - 1) <= c["rel_tol"], c["source"]
+
+
+def test_layer_scalars_grow_with_kv_heads():
+    # halving H_kv halves the stored scalars at fixed T and d
+    assert oracle.layer_cache_scalars(100, 8, 128) == 2 * oracle.layer_cache_scalars(100, 4, 128)
+    assert oracle.layer_cache_scalars(100, 8, 128) * 2 == oracle.kv_bytes_per_token(1, 8, 128, 2) * 100
+
+
+# -------------------------------------------- planted mistakes are caught
+def _fails(check, *impls):
+    try:
+        check(*impls)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_planted_mistakes_are_caught():
+    def rope_sign_flipped(x, pos, base):
+        return od.rope_rotate(x, -pos, base)
+
+    def rope_half_split(x, pos, base):
+        x = np.asarray(x, dtype=np.float64)
+        d = x.shape[-1]
+        ang = pos * od.rope_inv_freq(d, base)
+        c, s = np.cos(ang), np.sin(ang)
+        a, b = x[..., : d // 2], x[..., d // 2:]
+        return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
+
+    def inv_freq_wrong_exponent(d, base):
+        return np.power(base, -np.arange(d // 2) / d)
+
+    assert _fails(check_rope, rope_sign_flipped, od.rope_inv_freq)
+    assert _fails(check_rope, rope_half_split, od.rope_inv_freq)
+    assert _fails(check_rope, od.rope_rotate, inv_freq_wrong_exponent)
+
+    def gqa_modulo_group(q, K, V, scale):
+        h_q, h_kv = q.shape[0], K.shape[0]
+        out = np.empty_like(q)
+        lse = np.empty(h_q)
+        for h in range(h_q):
+            o, l = od.gqa_attention(q[h:h + 1], K[h % h_kv][None], V[h % h_kv][None], scale)
+            out[h], lse[h] = o[0], l[0]
+        return out, lse
+
+    def gqa_no_scale(q, K, V, scale):
+        return od.gqa_attention(q, K, V, 1.0)
+
+    def gqa_k_for_v(q, K, V, scale):
+        return od.gqa_attention(q, K, K, scale)
+
+    assert _fails(check_gqa, gqa_modulo_group)
+    assert _fails(check_gqa, gqa_no_scale)
+    assert _fails(check_gqa, gqa_k_for_v)
+
+    def combine_unweighted(o, lse):
+        return o.mean(axis=0), lse.max(axis=0)
+
+    def partial_off_by_one(q, K, V, scale, t0, t1):
+        return od.attention_partial(q, K, V, scale, t0, max(t0, t1 - 1)) if t1 - t0 > 1 else \
+            od.attention_partial(q, K, V, scale, t0, t1)
+
+    assert _fails(check_split_combine, od.attention_partial, combine_unweighted)
+    assert _fails(check_split_combine, partial_off_by_one, od.lse_combine)
+
+    def round_truncating(x):
+        x = np.asarray(x, np.float64)
+        _, e = np.frexp(x)
+        q = np.maximum(e.astype(np.int64) - 8, -133)
+        return np.ldexp(np.trunc(np.ldexp(x, -q)), q)
+
+    def round_half_up(x):
+        x = np.asarray(x, np.float64)
+        _, e = np.frexp(x)
+        q = np.maximum(e.astype(np.int64) - 8, -133)
+        return np.ldexp(np.floor(np.ldexp(x, -q) + 0.5), q)
+
+    assert _fails(check_round_bf16, round_truncating)
+    assert _fails(check_round_bf16, round_half_up)
