@@ -1,0 +1,204 @@
+/*
+ * mqa_decode.h -- C ABI of the GB300 decode-step attention library
+ * (libmqa_decode.so, sm_103a).
+ *
+ * One autoregressive decode step of grouped-query attention over a KV cache:
+ *
+ *   1. kv_append_rope        RoPE on the new token's q and k; append the
+ *                            rotated k and the v into the cache.
+ *   2. gqa_decode_attention  O_h = softmax(Q_h K_g(h)^T / sqrt(d)) V_g(h),
+ *                            g(h) = floor(h / G), G = H_q / H_kv, over every
+ *                            cached token of the sequence.
+ *   3. splitkv_combine       log-sum-exp merge of split-KV partial results
+ *                            (called by 2 itself when it splits).
+ *
+ * Sources: "Grouped-query attention: berbagi KV head di antara grup query"
+ * (nalar.dev), section "Jumlah head menentukan batas grup" (G, g(h), A_h,
+ * O_h) and "GQA berada di antara MHA dan MQA" (H_kv = H_q is MHA, H_kv = 1
+ * is MQA); "KV Cache" explainer (lensaml.com), Langkah 3 (cache pair
+ * [batch, kv_heads, tokens, head_dim], one slice written per decode step,
+ * keys rotated by position once and stored rotated); "KV Cache 최적화 심층
+ * 분석" (youngju.dev), class PagedKVCache (block = pos / block_size,
+ * offset = pos % block_size); "Arsitektur Inferensi LLM" (tveniu.com),
+ * section 4 PagedAttention (16-token blocks behind a page table) and section
+ * 5 FlashAttention (online softmax, no score matrix in HBM).
+ *
+ * Conventions for every call
+ *  - All pointers to tensors are DEVICE pointers unless stated otherwise;
+ *    the layout struct itself is a HOST pointer, read during the call only.
+ *  - The caller owns every buffer. The library never allocates device memory,
+ *    never synchronises, and keeps no pointer after a call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously; a host-side status says only that the
+ *    arguments were accepted and the launches were enqueued.
+ *  - Argument errors are found on the host and returned BEFORE anything is
+ *    launched (MQA_ERR_INVALID_ARG / MQA_ERR_UNSUPPORTED). Errors that only
+ *    the data can show (a position, length or block-table entry out of
+ *    range) are found on the device: the kernel ORs an MQA_DEVERR_* bit into
+ *    the caller's `err_word` (device int32, zeroed by the caller) and skips
+ *    that sequence's work; it never traps.
+ *  - Tensors are dense row-major with the stated shapes; every base pointer
+ *    must be 16-byte aligned.
+ */
+#ifndef MQA_DECODE_H
+#define MQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MQA_API __attribute__((visibility("default")))
+#else
+#define MQA_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* mqa_stream_t; /* same type as cudaStream_t */
+
+typedef enum mqa_status {
+  MQA_OK = 0,
+  MQA_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned pointer */
+  MQA_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, dtype, variant */
+  MQA_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+  MQA_ERR_WORKSPACE = 4    /* workspace missing or smaller than needed */
+} mqa_status;
+
+typedef enum mqa_dtype { MQA_BF16 = 0, MQA_F32 = 1 } mqa_dtype;
+
+/* Which decode-attention kernel to run (gqa_decode_attention `variant`). */
+typedef enum mqa_variant {
+  MQA_VARIANT_AUTO = 0,        /* tensor cores for a bf16 cache, else CUDA cores */
+  MQA_VARIANT_CUDA_CORE = 1,   /* fp32 FMA on CUDA cores; bf16 and f32 caches */
+  MQA_VARIANT_TENSOR_CORE = 2  /* bf16 tensor-core MMA; bf16 cache only */
+} mqa_variant;
+
+/* Bits a kernel ORs into the caller's device error word. */
+#define MQA_DEVERR_POS_RANGE 0x1u  /* append position < 0, >= capacity, or past the block table */
+#define MQA_DEVERR_PAGE_RANGE 0x2u /* a block-table entry in use lies outside [0, num_pages) */
+#define MQA_DEVERR_SEQ_LEN 0x4u    /* seq_len < 1, > capacity, > max_seq_len or past the block table */
+#define MQA_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel ran out (the result is invalid) */
+
+/*
+ * Where the KV cache of one layer lives.
+ *
+ * Contiguous (paged == 0): k_cache and v_cache are each
+ *     [batch, h_kv, capacity, head_dim]   (the pages' [batch, kv_heads, tokens, head_dim])
+ * Paged (paged == 1): k_cache and v_cache are each a page pool
+ *     [num_pages, h_kv, page_size, head_dim]
+ *   and block_table is a device int32 [batch, max_pages_per_seq]: token t of
+ *   sequence b lives in page block_table[b * max_pages_per_seq + t / page_size]
+ *   at row t % page_size. Entries past a sequence's last page are not read.
+ *   Several sequences may share a page (read path only).
+ *
+ * cache_dtype applies to both caches and to q_new / k_new / v_new.
+ * Requirements: h_q % h_kv == 0; head_dim in {64, 128}; batch >= 1;
+ * page_size a power of two in [16, 256] (paged).
+ */
+typedef struct mqa_kv_layout {
+  int32_t cache_dtype; /* mqa_dtype */
+  int32_t batch;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t head_dim;
+  int32_t paged;
+  void* k_cache;
+  void* v_cache;
+  int64_t capacity; /* contiguous: tokens per (sequence, kv head) row; unused when paged */
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t max_pages_per_seq;
+  int32_t reserved;
+  const int32_t* block_table;
+} mqa_kv_layout;
+
+/*
+ * kv_append_rope -- steps 1-2 of the decode step for every sequence b:
+ * p = pos[b] (the new token's 0-based position = its sequence length after
+ * the append minus one).
+ *   q_rot[b, h, :]  = RoPE(q_new[b, h, :], p)               (fp32 out)
+ *   cache K at (b, j, p) = round(RoPE(k_new[b, j, :], p))   (cache dtype)
+ *   cache V at (b, j, p) = v_new[b, j, :]                   (bit copy)
+ * RoPE rotates adjacent pairs (x[2i], x[2i+1]) by angle p * theta_i,
+ * theta_i = rope_base^(-2i/head_dim): (x cos - y sin, x sin + y cos). The
+ * angle and the key's rotation are evaluated in fp64 and the key is rounded
+ * once (nearest, ties to even) to the cache dtype; the query is rotated in
+ * fp32. ("KV Cache" explainer, Langkah 3: each key is rotated by its
+ * position once and stored rotated; only the newest token is projected.)
+ *
+ * q_new [batch, h_q, head_dim], k_new / v_new [batch, h_kv, head_dim]
+ * (cache dtype), pos [batch] int32, q_rot [batch, h_q, head_dim] fp32 output.
+ * A paged layout needs the page of position p already in the block table.
+ * A sequence whose p or page is out of range sets MQA_DEVERR_POS_RANGE /
+ * MQA_DEVERR_PAGE_RANGE and its cache is left untouched (q_rot is written).
+ */
+MQA_API mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                          const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word,
+                          mqa_stream_t stream);
+
+/*
+ * gqa_decode_attention -- step 3: for every sequence b and query head h,
+ *   O[b, h, :] = sum_t softmax_t(scale * q_rot[b, h, :] . K[b, g(h), t, :]) V[b, g(h), t, :]
+ * over tokens t in [0, seq_lens[b]), g(h) = floor(h / (h_q / h_kv)).
+ * Each kernel block streams the K/V tiles of one (sequence, kv head) token
+ * range from HBM once and serves all G query heads of the group from that
+ * load, with an fp32 online softmax (FlashAttention's running max and sum,
+ * "Arsitektur Inferensi LLM", section 5).
+ *
+ * q_rot       [batch, h_q, head_dim] fp32 (output of kv_append_rope)
+ * seq_lens    [batch] int32 device, lengths after the append (>= 1)
+ * max_seq_len host upper bound of every seq_lens[b]; sizes the grid and the split
+ * scale       score scale, normally 1/sqrt(head_dim)
+ * num_splits  1 = no split; > 1 = split the token axis into that many equal
+ *             chunks (rounded up to 64 tokens) and merge them with
+ *             splitkv_combine; 0 = let the library choose (mqa_choose_splits)
+ * out         [batch, h_q, head_dim] in out_dtype (mqa_dtype)
+ * lse_out     optional [batch, h_q] fp32: natural-log sum of exp(scaled score)
+ * workspace   device scratch of at least mqa_workspace_size(...) bytes when the
+ *             call splits (may be NULL when it does not); 256-byte aligned
+ * variant     mqa_variant
+ * A sequence with an out-of-range length or block-table entry sets its
+ * MQA_DEVERR_* bit; its output rows are then unspecified.
+ */
+MQA_API mqa_status gqa_decode_attention(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens,
+                                int32_t max_seq_len, float scale, int32_t num_splits, void* out,
+                                int32_t out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                                int32_t variant, int32_t* err_word, mqa_stream_t stream);
+
+/*
+ * splitkv_combine -- merge per-split results of disjoint token ranges:
+ *   LSE = log sum_s exp(lse_part[b, h, s]),
+ *   out[b, h, :] = sum_s exp(lse_part[b, h, s] - LSE) * o_part[b, h, s, :].
+ * o_part [batch, h_q, num_splits, head_dim] fp32 holds each split's
+ * NORMALISED output; lse_part [batch, h_q, num_splits] fp32 its natural-log
+ * sum of exp(score). A split with no tokens has lse = -inf and is ignored;
+ * at least one split per row must be non-empty. out is [batch, h_q,
+ * head_dim] in out_dtype; lse_out (optional) [batch, h_q] fp32.
+ */
+MQA_API mqa_status splitkv_combine(const float* o_part, const float* lse_part, int32_t batch, int32_t h_q,
+                           int32_t num_splits, int32_t head_dim, void* out, int32_t out_dtype, float* lse_out,
+                           mqa_stream_t stream);
+
+/* Split count gqa_decode_attention uses for num_splits = 0 on the current device
+ * (>= 1), or -1 if the layout is invalid. */
+MQA_API int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant);
+
+/* Workspace bytes gqa_decode_attention needs for this layout, bound and split
+ * count (num_splits = 0: the count mqa_choose_splits returns); 0 when the call
+ * does not split. */
+MQA_API size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t num_splits, int32_t variant);
+
+/* Static description of a status code. */
+MQA_API const char* mqa_status_string(mqa_status status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+MQA_API const char* mqa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQA_DECODE_H */

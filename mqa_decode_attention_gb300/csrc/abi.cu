@@ -1,0 +1,374 @@
+// The C ABI of libmqa_decode.so (declared in include/mqa_decode.h):
+// host-side argument checks, split choice, TMA descriptor encoding, launches.
+// Nothing here allocates device memory or synchronises.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mqa_decode.h"
+#include "launch.h"
+
+namespace {
+
+using namespace mqa;
+
+thread_local char g_cuda_error[256] = "";
+
+mqa_status fail_cuda(cudaError_t e) {
+  snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return MQA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
+
+
+mqa_status check_layout(const mqa_kv_layout* L) {
+  if (L == nullptr) return MQA_ERR_INVALID_ARG;
+  if (L->cache_dtype != MQA_BF16 && L->cache_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  if (L->batch < 1 || L->h_q < 1 || L->h_kv < 1 || L->h_q % L->h_kv != 0) return MQA_ERR_INVALID_ARG;
+  if (L->head_dim != 64 && L->head_dim != 128) return MQA_ERR_UNSUPPORTED;
+  if (L->k_cache == nullptr || L->v_cache == nullptr) return MQA_ERR_INVALID_ARG;
+  if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16)) return MQA_ERR_INVALID_ARG;
+  if (L->paged != 0 && L->paged != 1) return MQA_ERR_INVALID_ARG;
+  if (!L->paged) {
+    if (L->capacity < 1 || L->capacity > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
+  } else {
+    if (L->page_size < 16 || L->page_size > 256 || !is_pow2(L->page_size)) return MQA_ERR_UNSUPPORTED;
+    if (L->num_pages < 1 || L->max_pages_per_seq < 1 || L->block_table == nullptr) return MQA_ERR_INVALID_ARG;
+    if (!aligned(L->block_table, 4)) return MQA_ERR_INVALID_ARG;
+    if (static_cast<long long>(L->max_pages_per_seq) * L->page_size > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
+  }
+  return MQA_OK;
+}
+
+long long token_limit(const mqa_kv_layout* L) {
+  return L->paged ? static_cast<long long>(L->max_pages_per_seq) * L->page_size : L->capacity;
+}
+
+int resolve_variant(const mqa_kv_layout* L, int variant) {
+  if (variant == MQA_VARIANT_AUTO) return L->cache_dtype == MQA_BF16 ? MQA_VARIANT_TENSOR_CORE : MQA_VARIANT_CUDA_CORE;
+  return variant;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_per_sm = 0;
+  int threads_per_sm = 0;
+};
+
+DeviceInfo device_info(int dev) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = cache[dev & 63];
+  if (d.sms == 0) {
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&d.threads_per_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+    if (d.sms <= 0) d.sms = 1;
+  }
+  return d;
+}
+
+KernelShape decode_shape(const mqa_kv_layout* L, int variant) {
+  const int G = L->h_q / L->h_kv;
+  if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G);
+  return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
+}
+
+int head_blocks(const mqa_kv_layout* L, const KernelShape& ks) {
+  const int G = L->h_q / L->h_kv;
+  return (G + ks.heads_per_cta - 1) / ks.heads_per_cta;
+}
+
+// Token-axis split count. Blocks of one (sequence, kv head) are independent,
+// so the only reasons to split are (a) too few units to keep every SM
+// streaming, and (b) long sequences whose blocks would finish late (the
+// device-side lengths may vary up to max_seq_len), which chunks of a bounded
+// size avoid.
+int choose_splits(const mqa_kv_layout* L, int max_len, int variant) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const DeviceInfo di = device_info(dev);
+  const KernelShape ks = decode_shape(L, variant);
+  const int by_smem = ks.smem_bytes > 0 ? di.smem_per_sm / (ks.smem_bytes + 1024) : 8;
+  const int by_threads = di.threads_per_sm / ks.threads;
+  const int per_sm = std::max(1, std::min(by_smem, by_threads));
+  const long long slots = static_cast<long long>(di.sms) * per_sm;
+  const long long units = static_cast<long long>(L->batch) * L->h_kv * head_blocks(L, ks);
+  const int tiles = (max_len + kTile - 1) / kTile;
+  int s = 1;
+  if (units < slots) s = static_cast<int>((slots + units - 1) / units);
+  if (L->paged) {
+    // bound the work of one block so that late long sequences do not leave a tail
+    const int cap_tiles = 32;  // 2048 tokens
+    s = std::max(s, (tiles + cap_tiles - 1) / cap_tiles);
+  }
+  return std::max(1, std::min(s, tiles));
+}
+
+// Effective split count and chunk for a requested count.
+void split_plan(int requested, int max_len, int* splits, int* chunk) {
+  const int per = (max_len + requested - 1) / requested;
+  const int c = ((per + kTile - 1) / kTile) * kTile;
+  *chunk = c;
+  *splits = (max_len + c - 1) / c;
+}
+
+size_t partial_bytes(const mqa_kv_layout* L, int splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(L->batch) * L->h_q;
+  const size_t o_bytes = ((rows * splits * L->head_dim * 4) + 255) / 256 * 256;
+  return o_bytes + rows * splits * 4;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 64-column (128-byte) swizzled boxes of kTile rows, or of one page when
+// pages are shorter than a tile.
+bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t D = L->head_dim;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  cuuint32_t rank;
+  if (!L->paged) {
+    rank = 3;
+    dims[0] = D;
+    dims[1] = static_cast<cuuint64_t>(L->capacity);
+    dims[2] = static_cast<cuuint64_t>(L->batch) * L->h_kv;
+    strides[0] = D * 2;
+    strides[1] = static_cast<cuuint64_t>(L->capacity) * D * 2;
+    box[0] = 64;
+    box[1] = kTile;
+    box[2] = 1;
+  } else {
+    rank = 4;
+    dims[0] = D;
+    dims[1] = static_cast<cuuint64_t>(L->page_size);
+    dims[2] = static_cast<cuuint64_t>(L->h_kv);
+    dims[3] = static_cast<cuuint64_t>(L->num_pages);
+    strides[0] = D * 2;
+    strides[1] = static_cast<cuuint64_t>(L->page_size) * D * 2;
+    strides[2] = static_cast<cuuint64_t>(L->h_kv) * L->page_size * D * 2;
+    box[0] = 64;
+    box[1] = static_cast<cuuint32_t>(L->page_size < kTile ? L->page_size : kTile);
+    box[2] = 1;
+    box[3] = 1;
+  }
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mqa_status_string(mqa_status s) {
+  switch (s) {
+    case MQA_OK: return "ok";
+    case MQA_ERR_INVALID_ARG: return "invalid argument";
+    case MQA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MQA_ERR_CUDA: return "CUDA error";
+    case MQA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* mqa_last_cuda_error(void) { return g_cuda_error; }
+
+mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                          const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word,
+                          mqa_stream_t stream) {
+  const mqa_status st = check_layout(layout);
+  if (st != MQA_OK) return st;
+  if (!q_new || !k_new || !v_new || !pos || !q_rot || !err_word) return MQA_ERR_INVALID_ARG;
+  if (!aligned(q_new, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q_rot, 16) ||
+      !aligned(pos, 4) || !aligned(err_word, 4))
+    return MQA_ERR_INVALID_ARG;
+  if (!(rope_base > 0.0) || !std::isfinite(rope_base)) return MQA_ERR_INVALID_ARG;
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = layout->batch;
+  p.h_q = layout->h_q;
+  p.h_kv = layout->h_kv;
+  p.head_dim = layout->head_dim;
+  p.cache_dtype = layout->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.paged = layout->paged;
+  p.q_new = q_new;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.pos = pos;
+  p.k_cache = layout->k_cache;
+  p.v_cache = layout->v_cache;
+  p.capacity = layout->capacity;
+  p.page_size = layout->page_size;
+  p.num_pages = layout->num_pages;
+  p.max_pages = layout->max_pages_per_seq;
+  p.block_table = layout->block_table;
+  p.q_rot = q_rot;
+  p.err = err_word;
+  for (int i = 0; i < layout->head_dim / 2; ++i)
+    p.theta[i] = std::pow(rope_base, -2.0 * static_cast<double>(i) / static_cast<double>(layout->head_dim));
+  const cudaError_t e = launch_append_rope(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  const cudaError_t e2 = cudaGetLastError();
+  return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+}
+
+int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant) {
+  if (check_layout(layout) != MQA_OK || max_seq_len < 1 || max_seq_len > token_limit(layout)) return -1;
+  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return -1;
+  return choose_splits(layout, max_seq_len, resolve_variant(layout, variant));
+}
+
+size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t num_splits, int32_t variant) {
+  if (check_layout(layout) != MQA_OK || max_seq_len < 1 || max_seq_len > token_limit(layout) || num_splits < 0)
+    return 0;
+  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return 0;
+  const int v = resolve_variant(layout, variant);
+  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+  int splits, chunk;
+  split_plan(req, max_seq_len, &splits, &chunk);
+  return partial_bytes(layout, splits);
+}
+
+mqa_status splitkv_combine(const float* o_part, const float* lse_part, int32_t batch, int32_t h_q,
+                           int32_t num_splits, int32_t head_dim, void* out, int32_t out_dtype, float* lse_out,
+                           mqa_stream_t stream) {
+  if (!o_part || !lse_part || !out) return MQA_ERR_INVALID_ARG;
+  if (batch < 1 || h_q < 1 || num_splits < 1 || head_dim < 1) return MQA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MQA_ERR_UNSUPPORTED;
+  if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  if (!aligned(o_part, 4) || !aligned(lse_part, 4) || !aligned(out, 4) || (lse_out && !aligned(lse_out, 4)))
+    return MQA_ERR_INVALID_ARG;
+  CombineParams c;
+  c.o_part = o_part;
+  c.lse_part = lse_part;
+  c.rows = batch * h_q;
+  c.num_splits = num_splits;
+  c.head_dim = head_dim;
+  c.out = out;
+  c.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  c.lse_out = lse_out;
+  const cudaError_t e = launch_combine(c, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  const cudaError_t e2 = cudaGetLastError();
+  return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+}
+
+mqa_status gqa_decode_attention(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens,
+                                int32_t max_seq_len, float scale, int32_t num_splits, void* out,
+                                int32_t out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                                int32_t variant, int32_t* err_word, mqa_stream_t stream) {
+  const mqa_status st = check_layout(layout);
+  if (st != MQA_OK) return st;
+  if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
+  if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
+      (lse_out && !aligned(lse_out, 4)))
+    return MQA_ERR_INVALID_ARG;
+  if (max_seq_len < 1 || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || num_splits < 0) return MQA_ERR_INVALID_ARG;
+  if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return MQA_ERR_INVALID_ARG;
+  const int v = resolve_variant(layout, variant);
+  if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype != MQA_BF16) return MQA_ERR_UNSUPPORTED;
+
+  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+  int splits, chunk;
+  split_plan(req, max_seq_len, &splits, &chunk);
+  const size_t need = partial_bytes(layout, splits);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need) return MQA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return MQA_ERR_INVALID_ARG;
+  }
+
+  const KernelShape ks = decode_shape(layout, v);
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = layout->batch;
+  p.h_q = layout->h_q;
+  p.h_kv = layout->h_kv;
+  p.group = layout->h_q / layout->h_kv;
+  p.head_dim = layout->head_dim;
+  p.cache_dtype = layout->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.paged = layout->paged;
+  p.k_cache = layout->k_cache;
+  p.v_cache = layout->v_cache;
+  p.capacity = layout->capacity;
+  p.page_size = layout->page_size;
+  p.num_pages = layout->num_pages;
+  p.max_pages = layout->max_pages_per_seq;
+  p.block_table = layout->block_table;
+  p.q_rot = q_rot;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_splits = splits;
+  p.chunk = chunk;
+  p.head_blocks = head_blocks(layout, ks);
+  p.out = out;
+  p.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.lse_out = lse_out;
+  p.err = err_word;
+  if (splits > 1) {
+    const size_t rows = static_cast<size_t>(layout->batch) * layout->h_q;
+    const size_t o_bytes = ((rows * splits * layout->head_dim * 4) + 255) / 256 * 256;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + o_bytes);
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (v == MQA_VARIANT_TENSOR_CORE) {
+    CUtensorMap tk, tv;
+    if (!make_tensor_map(&tk, layout->k_cache, layout) || !make_tensor_map(&tv, layout->v_cache, layout)) {
+      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+      return MQA_ERR_CUDA;
+    }
+    e = launch_decode_mma(p, tk, tv, s);
+  } else {
+    e = launch_decode_fma(p, s);
+  }
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (splits > 1) {
+    CombineParams c;
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.rows = layout->batch * layout->h_q;
+    c.num_splits = splits;
+    c.head_dim = layout->head_dim;
+    c.out = out;
+    c.out_dtype = p.out_dtype;
+    c.lse_out = lse_out;
+    e = launch_combine(c, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  const cudaError_t e2 = cudaGetLastError();
+  return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+}
+
+}  // extern "C"

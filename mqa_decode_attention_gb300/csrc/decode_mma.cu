@@ -1,0 +1,448 @@
+// gqa_decode_attention on tensor cores, bf16 cache.
+//
+// Same result as the CUDA-core kernel, O_h = softmax(scale * q_h K_j^T) V_j
+// for the query heads h of kv head j ("Grouped-query attention" page,
+// equations for A_h and O_h), with an online softmax ("Arsitektur Inferensi
+// LLM", section 5: running max and sum, no score matrix in HBM).
+//
+// The G query heads of a group are the rows of the MMA A operand (padded to
+// 16 per head block), so one K/V tile in shared memory serves every head of
+// the group:  S = Q K^T  (m16 x n8 x k16 steps over head_dim), then
+// O += P V with P rounded to bf16 (the fp32 softmax state stays in registers).
+//
+// Block = 4 consumer warps per head block of 16 heads + 1 producer warp. The
+// producer streams 64-token K and V tiles with TMA tensor copies
+// (cp.async.bulk.tensor, 128-byte swizzle, one mbarrier pair per stage);
+// a paged cache is gathered page by page through the block table. Consumer
+// warp w reads tokens [16 (w % 4), 16 (w % 4) + 16) of every tile with
+// ldmatrix (the swizzle keeps the 8 rows of each 8x8 matrix in distinct
+// banks), runs its own online softmax over its tokens, and the 4 warps of a
+// head block merge once at the end.
+#include <cuda_bf16.h>
+
+#include "../../include/mqa_decode.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+#ifndef MQA_MMA_STAGES_D128
+#define MQA_MMA_STAGES_D128 3
+#endif
+#ifndef MQA_MMA_STAGES_D64
+#define MQA_MMA_STAGES_D64 4
+#endif
+
+namespace mqa {
+namespace {
+
+template <int D, int HB, int STAGES>
+struct MmaCfg {
+  static constexpr int kConsumerWarps = 4 * HB;
+  static constexpr int kConsumerThreads = 32 * kConsumerWarps;
+  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int kHalfBytes = kTile * 128;             // 64 rows x 64 bf16 (one swizzle span)
+  static constexpr int kTileBytes = (D / 64) * kHalfBytes;    // a K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kMergeStride = D + 8;                  // floats per merged row
+  static constexpr int kMergeBytes = kConsumerWarps * 16 * (kMergeStride + 2) * 4;
+  static constexpr int kBodyBytes = (STAGES * kStageBytes > kMergeBytes) ? STAGES * kStageBytes : kMergeBytes;
+  static constexpr int kSmemBytes = kBodyBytes + 2 * STAGES * 8 + 1024;  // + alignment slack
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+};
+
+// Shared-memory byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r
+// under the 128-byte swizzle TMA applied: chunk (c mod 8) of a 128-byte row
+// is stored at position (c mod 8) xor (r mod 8); D = 128 keeps its two
+// 64-column halves in separate spans.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <int D, int HB, int STAGES>
+__global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                      const DecodeParams p) {
+  using C = MmaCfg<D, HB, STAGES>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBodyBytes);
+  uint64_t* empty = full + STAGES;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.num_splits;
+  int cta = blockIdx.x;
+  const int split = cta % S;
+  cta /= S;
+  const int hsb = cta % p.head_blocks;
+  cta /= p.head_blocks;
+  const int j = cta % p.h_kv;
+  const int b = cta / p.h_kv;
+  const int G = p.group;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), C::kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == C::kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  __syncthreads();
+  grid_dependency_wait();
+  // Lengths are read only after the preceding grid is complete and visible.
+  long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;
+  if (limit > p.max_seq_len) limit = p.max_seq_len;
+  int L = p.seq_lens[b];
+  if (L < 1 || L > limit) {
+    if (threadIdx.x == 0 && split == 0 && hsb == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
+    L = L < 0 ? 0 : static_cast<int>(L > limit ? limit : L);
+  }
+  const int t_begin = split * p.chunk;
+  const int t_end = min(L, t_begin + p.chunk);
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
+
+
+  if (warp == C::kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const int ps = p.page_size;
+    const int rpc = ps < kTile ? ps : kTile;  // tile rows per paged copy
+    const int32_t* trow = p.block_table + static_cast<long long>(b) * p.max_pages;
+    const int n_pages_seq = p.paged ? (L + ps - 1) / ps : 0;
+    int wbase = p.paged ? t_begin / ps : 0;  // logical page window [wbase, wbase + 32)
+    int wcur = -1, wnxt = -1;
+    if (p.paged) {
+      wcur = (wbase + lane < n_pages_seq) ? __ldg(trow + wbase + lane) : -1;
+      wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
+    }
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int stage = it % STAGES;
+      if (it >= STAGES) {
+        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
+          if (lane == 0) {
+            s_abort = 1;
+            atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
+          }
+          break;
+        }
+      }
+      if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+      const int t0 = t_begin + it * kTile;
+      const uint32_t kdst = smem_u32(smem + stage * C::kStageBytes);
+      const uint32_t vdst = kdst + C::kTileBytes;
+      const uint32_t fb = smem_u32(&full[stage]);
+      if (!p.paged) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          const int row = b * p.h_kv + j;
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_load_3d(kdst + hf * C::kHalfBytes, &tmap_k, 64 * hf, t0, row, fb);
+            tma_load_3d(vdst + hf * C::kHalfBytes, &tmap_v, 64 * hf, t0, row, fb);
+          }
+        }
+      } else {
+        // Every copy is issued whole: rows past the sequence read a page that
+        // is still in bounds (or, for a bad table entry, the TMA fill value),
+        // and the consumers mask those rows.
+        int pg[kTile / 16];
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k) {
+          pg[k] = -1;
+          if (k * rpc < kTile) {
+            int lp = (t0 + k * rpc) / ps;
+            if (lp >= n_pages_seq) lp = n_pages_seq - 1;
+            while (lp >= wbase + 32) {  // warp-uniform window advance
+              wbase += 32;
+              wcur = wnxt;
+              wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
+            }
+            pg[k] = __shfl_sync(0xffffffffu, wcur, lp - wbase);
+            if ((pg[k] < 0 || pg[k] >= p.num_pages) && lane == 0)
+              atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
+          }
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k) {
+            if (k * rpc >= kTile) break;
+            const int r = (t0 + k * rpc) % ps;
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf) {
+              tma_load_4d(kdst + hf * C::kHalfBytes + k * rpc * 128, &tmap_k, 64 * hf, r, j, pg[k], fb);
+              tma_load_4d(vdst + hf * C::kHalfBytes + k * rpc * 128, &tmap_v, 64 * hf, r, j, pg[k], fb);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      issued = it + 1;
+    }
+    if (*reinterpret_cast<volatile int*>(&s_abort)) {
+      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+        (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int hb = warp >> 2;           // head block within this CTA
+  const int ws = warp & 3;            // token slice of each tile
+  const int head0 = (hsb * HB + hb) * 16;  // first head (within the group) of this warp's rows
+  const int rows_valid = G - head0;   // rows >= this are padding
+  const int r0 = lane >> 2;           // fragment rows r0 and r0 + 8
+  const int c2 = (lane & 3) * 2;      // fragment column pair
+
+  // Q as the A operand: rows = heads, k = head_dim, pre-scaled into the log2 domain
+  uint32_t qa[D / 16][4];
+  {
+    const float* q = p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
+    const float sc = p.scale_log2;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        const int row = r0 + ((part & 1) ? 8 : 0);
+        const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
+        float2 v = make_float2(0.f, 0.f);
+        if (row < rows_valid) v = *reinterpret_cast<const float2*>(q + row * D + col);
+        qa[ks][part] = pack_bf16x2(v.x * sc, v.y * sc);
+      }
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  bool ok = true;
+  const int trow0 = ws * 16;  // first tile row of this warp
+  for (int it = 0; it < n_tiles; ++it) {
+    const int stage = it % STAGES;
+    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
+      if (lane == 0) {
+        s_abort = 1;
+        atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
+      }
+      ok = false;
+      break;
+    }
+    const uint32_t kb = smem_u32(smem + stage * C::kStageBytes);
+    const uint32_t vb = kb + C::kTileBytes;
+    const int n_valid = t_end - (t_begin + it * kTile + trow0);  // valid rows of this warp's 16
+
+    if (n_valid < 16) {
+      // Rows past the range may hold anything (even NaN bit patterns); zero
+      // their V so that P = 0 contributes exactly nothing.
+      const int first = n_valid < 0 ? 0 : n_valid;
+      unsigned char* vrow = smem + stage * C::kStageBytes + C::kTileBytes;
+      for (int idx = lane; idx < (16 - first) * (D / 8); idx += 32) {
+        const int r = trow0 + first + idx / (D / 8);
+        const int c = idx % (D / 8);
+        *reinterpret_cast<uint4*>(vrow + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+
+    if (n_valid > 0) {
+      // ---- S = Q K^T over this warp's 16 tokens (two n8 tiles)
+      float s[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 32; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int row = trow0 + nt * 8 + (lane & 7);
+          const int c = kk * 4 + (lane >> 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + swz(row, c), b0, b1, b2, b3);
+          mma_bf16_16816(s[nt], qa[2 * kk], b0, b1);
+          mma_bf16_16816(s[nt], qa[2 * kk + 1], b2, b3);
+        }
+      }
+      // ---- mask, online softmax (rows r0 and r0 + 8)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (nt * 8 + c2 + e >= n_valid) {
+            s[nt][e] = -INFINITY;
+            s[nt][2 + e] = -INFINITY;
+          }
+        }
+      }
+      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // mn is finite: every warp slice with n_valid > 0 has at least one valid token
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float pr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        pr[nt][0] = exp2f(s[nt][0] - mn0);
+        pr[nt][1] = exp2f(s[nt][1] - mn0);
+        pr[nt][2] = exp2f(s[nt][2] - mn1);
+        pr[nt][3] = exp2f(s[nt][3] - mn1);
+      }
+      l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+      l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
+      // ---- O += P V (P as the A operand straight from the S fragments)
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+      pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+      pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+      pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+#pragma unroll
+      for (int dn = 0; dn < D / 16; ++dn) {
+        const int row = trow0 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int c = dn * 2 + (lane >> 4);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vb + swz(row, c), v0, v1, v2, v3);
+        mma_bf16_16816(o[2 * dn], pa, v0, v1);
+        mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+  }
+
+  // ------------------------------------------- merge the 4 token slices
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  named_bar_sync(1, C::kConsumerThreads);
+  if (*reinterpret_cast<volatile int*>(&s_abort) || !ok) return;
+  float* mo = reinterpret_cast<float*>(smem);            // [warps][16][stride]
+  float* mm = mo + C::kConsumerWarps * 16 * C::kMergeStride;  // [warps][16]
+  float* ml = mm + C::kConsumerWarps * 16;                     // [warps][16]
+  {
+    float* mine = mo + warp * 16 * C::kMergeStride;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      *reinterpret_cast<float2*>(mine + r0 * C::kMergeStride + n * 8 + c2) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(mine + (r0 + 8) * C::kMergeStride + n * 8 + c2) = make_float2(o[n][2], o[n][3]);
+    }
+    if ((lane & 3) == 0) {
+      mm[warp * 16 + r0] = m0;
+      mm[warp * 16 + r0 + 8] = m1;
+      ml[warp * 16 + r0] = l0;
+      ml[warp * 16 + r0 + 8] = l1;
+    }
+  }
+  named_bar_sync(1, C::kConsumerThreads);
+
+  const bool split_out = S > 1;
+  const int tid = threadIdx.x;
+  for (int hbi = 0; hbi < HB; ++hbi) {
+    const int hh0 = (hsb * HB + hbi) * 16;
+    const int n_rows = min(16, G - hh0);
+    for (int idx = tid; idx < n_rows * D; idx += C::kConsumerThreads) {
+      const int r = idx / D, d = idx - r * D;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mm[(hbi * 4 + w) * 16 + r]);
+      float num = 0.f, den = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int ww = hbi * 4 + w;
+          const float wt = exp2f(mm[ww * 16 + r] - mx);
+          num = fmaf(wt, mo[(ww * 16 + r) * C::kMergeStride + d], num);
+          den = fmaf(wt, ml[ww * 16 + r], den);
+        }
+      }
+      const float ov = den > 0.f ? num / den : 0.f;
+      const float lse = den > 0.f ? (mx + log2f(den)) * 0.69314718055994530942f : -INFINITY;
+      const long long grow = static_cast<long long>(b) * p.h_q + j * G + hh0 + r;
+      if (split_out) {
+        p.o_part[(grow * S + split) * D + d] = ov;
+        if (d == 0) p.lse_part[grow * S + split] = lse;
+      } else {
+        if (p.out_dtype == kDtypeBf16)
+          static_cast<__nv_bfloat16*>(p.out)[grow * D + d] = __float2bfloat16_rn(ov);
+        else
+          static_cast<float*>(p.out)[grow * D + d] = ov;
+        if (d == 0 && p.lse_out != nullptr) p.lse_out[grow] = lse;
+      }
+    }
+  }
+}
+
+template <int D, int HB>
+constexpr int mma_stages() {
+  return D == 128 ? MQA_MMA_STAGES_D128 : MQA_MMA_STAGES_D64;
+}
+
+template <int D, int HB>
+cudaError_t launch_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  constexpr int ST = mma_stages<D, HB>();
+  using C = MmaCfg<D, HB, ST>;
+  auto kern = decode_mma_kernel<D, HB, ST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.h_kv * p.head_blocks * p.num_splits);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+int mma_hb(int group) { return group > 16 ? 2 : 1; }
+
+}  // namespace
+
+KernelShape decode_mma_shape(int head_dim, int group) {
+  const int hb = mma_hb(group);
+  if (head_dim == 128) {
+    if (hb == 2) {
+      using C = MmaCfg<128, 2, mma_stages<128, 2>()>;
+      return {C::kThreads, C::kSmemBytes, 32};
+    }
+    using C = MmaCfg<128, 1, mma_stages<128, 1>()>;
+    return {C::kThreads, C::kSmemBytes, 16};
+  }
+  if (hb == 2) {
+    using C = MmaCfg<64, 2, mma_stages<64, 2>()>;
+    return {C::kThreads, C::kSmemBytes, 32};
+  }
+  using C = MmaCfg<64, 1, mma_stages<64, 1>()>;
+  return {C::kThreads, C::kSmemBytes, 16};
+}
+
+cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              cudaStream_t stream) {
+  const int hb = mma_hb(p.group);
+  if (p.head_dim == 128) return hb == 2 ? launch_mma_t<128, 2>(p, tk, tv, stream) : launch_mma_t<128, 1>(p, tk, tv, stream);
+  return hb == 2 ? launch_mma_t<64, 2>(p, tk, tv, stream) : launch_mma_t<64, 1>(p, tk, tv, stream);
+}
+
+}  // namespace mqa

@@ -1,0 +1,82 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mqa {
+
+constexpr int kTile = 64;          // tokens per pipeline stage of the decode kernels
+constexpr int kMaxHalfDim = 64;    // RoPE frequencies held in the append kernel's parameters
+constexpr int kDtypeBf16 = 0;
+constexpr int kDtypeF32 = 1;
+
+struct AppendParams {
+  int batch, h_q, h_kv, head_dim, cache_dtype, paged;
+  const void* q_new;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* pos;
+  void* k_cache;
+  void* v_cache;
+  long long capacity;
+  int page_size, num_pages, max_pages;
+  const int32_t* block_table;
+  float* q_rot;
+  int32_t* err;
+  double theta[kMaxHalfDim];  // RoPE inverse frequencies base^(-2i/d)
+};
+
+struct DecodeParams {
+  int batch, h_q, h_kv, group, head_dim, cache_dtype, paged;
+  const void* k_cache;
+  const void* v_cache;
+  long long capacity;
+  int page_size, num_pages, max_pages;
+  const int32_t* block_table;
+  const float* q_rot;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  float scale_log2;  // score scale times log2(e): scores live in the log2 domain
+  int num_splits;    // token-axis splits per (sequence, kv head); 1 = write `out` directly
+  int chunk;         // tokens per split, a multiple of kTile
+  int head_blocks;   // blocks of query heads a (sequence, kv head) is cut into
+  void* out;
+  int out_dtype;
+  float* lse_out;
+  float* o_part;     // [batch, h_q, num_splits, head_dim] when num_splits > 1
+  float* lse_part;   // [batch, h_q, num_splits]
+  int32_t* err;
+};
+
+struct CombineParams {
+  const float* o_part;
+  const float* lse_part;
+  int rows;  // batch * h_q
+  int num_splits, head_dim;
+  void* out;
+  int out_dtype;
+  float* lse_out;
+};
+
+// Kernel shapes the host needs for grids, split heuristics and workspace.
+struct KernelShape {
+  int threads;
+  int smem_bytes;
+  int heads_per_cta;  // query heads one block serves
+};
+
+KernelShape append_rope_shape();
+cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream);
+
+KernelShape decode_fma_shape(int cache_dtype, int head_dim, int group);
+cudaError_t launch_decode_fma(const DecodeParams& p, cudaStream_t stream);
+
+KernelShape decode_mma_shape(int head_dim, int group);
+cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                              cudaStream_t stream);
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+}  // namespace mqa

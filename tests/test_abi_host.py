@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function the header declares, and rejects bad arguments before it
+touches CUDA."""
+
+import ctypes
+
+import pytest
+
+from mqa_decode_attention_gb300 import _abi
+
+FAKE = 0x10000  # 16-byte-aligned stand-in pointer; never dereferenced (calls fail validation first)
+
+
+@pytest.fixture(scope="module")
+def lib(built_lib):
+    return _abi.load()
+
+
+def _layout(**kw):
+    base = dict(cache_dtype=_abi.MQA_BF16, batch=2, h_q=8, h_kv=2, head_dim=128, paged=0, k_cache=FAKE,
+                v_cache=FAKE + 4096, capacity=256, page_size=0, num_pages=0, max_pages_per_seq=0, reserved=0,
+                block_table=None)
+    base.update(kw)
+    return _abi.KVLayout(**base)
+
+
+def test_exports_every_declared_function(lib):
+    names = _abi.header_functions()
+    assert {"kv_append_rope", "gqa_decode_attention", "splitkv_combine"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.mqa_status_string(code)
+    assert lib.mqa_status_string(0) == b"ok"
+
+
+def _append(lib, lay, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, pos=FAKE, base=10000.0, q_rot=FAKE, err=FAKE)
+    args.update(kw)
+    return lib.kv_append_rope(ctypes.byref(lay) if lay is not None else None, args["q"], args["k"], args["v"],
+                              args["pos"], args["base"], args["q_rot"], args["err"], None)
+
+
+def test_append_rejects_bad_arguments(lib):
+    assert _append(lib, None) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(h_q=6, h_kv=4)) == _abi.MQA_ERR_INVALID_ARG  # h_q % h_kv != 0
+    assert _append(lib, _layout(head_dim=96)) == _abi.MQA_ERR_UNSUPPORTED
+    assert _append(lib, _layout(cache_dtype=7)) == _abi.MQA_ERR_UNSUPPORTED
+    assert _append(lib, _layout(k_cache=None)) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(k_cache=FAKE + 8)) == _abi.MQA_ERR_INVALID_ARG  # misaligned
+    assert _append(lib, _layout(capacity=0)) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(), pos=None) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(), base=-1.0) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(), base=float("nan")) == _abi.MQA_ERR_INVALID_ARG
+    # paged: page size must be a power of two in [16, 256], table present
+    assert _append(lib, _layout(paged=1, page_size=24, num_pages=4, max_pages_per_seq=2, block_table=FAKE)) == \
+        _abi.MQA_ERR_UNSUPPORTED
+    assert _append(lib, _layout(paged=1, page_size=16, num_pages=4, max_pages_per_seq=2, block_table=None)) == \
+        _abi.MQA_ERR_INVALID_ARG
+
+
+def _attn(lib, lay, **kw):
+    a = dict(q_rot=FAKE, lens=FAKE, max_len=100, scale=0.1, splits=1, out=FAKE, out_dtype=_abi.MQA_BF16,
+             lse=None, ws=None, ws_bytes=0, variant=0, err=FAKE)
+    a.update(kw)
+    return lib.gqa_decode_attention(ctypes.byref(lay), a["q_rot"], a["lens"], a["max_len"], a["scale"], a["splits"],
+                                    a["out"], a["out_dtype"], a["lse"], a["ws"], a["ws_bytes"], a["variant"],
+                                    a["err"], None)
+
+
+def test_attention_rejects_bad_arguments(lib):
+    lay = _layout()
+    assert _attn(lib, lay, max_len=0) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, lay, max_len=257) == _abi.MQA_ERR_INVALID_ARG  # beyond capacity
+    assert _attn(lib, lay, scale=float("inf")) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, lay, splits=-1) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, lay, out_dtype=5) == _abi.MQA_ERR_UNSUPPORTED
+    assert _attn(lib, lay, variant=9) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, lay, out=None) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, lay, err=None) == _abi.MQA_ERR_INVALID_ARG
+    # tensor cores need a bf16 cache
+    assert _attn(lib, _layout(cache_dtype=_abi.MQA_F32), variant=_abi.MQA_VARIANT_TENSOR_CORE) == \
+        _abi.MQA_ERR_UNSUPPORTED
+    # a split run needs its workspace
+    assert _attn(lib, lay, splits=4) == _abi.MQA_ERR_WORKSPACE
+    assert _attn(lib, lay, splits=4, ws=FAKE, ws_bytes=16) == _abi.MQA_ERR_WORKSPACE
+
+
+def test_combine_rejects_bad_arguments(lib):
+    assert lib.splitkv_combine(None, FAKE, 1, 1, 1, 128, FAKE, 0, None, None) == _abi.MQA_ERR_INVALID_ARG
+    assert lib.splitkv_combine(FAKE, FAKE, 0, 1, 1, 128, FAKE, 0, None, None) == _abi.MQA_ERR_INVALID_ARG
+    assert lib.splitkv_combine(FAKE, FAKE, 1, 1, 1, 96, FAKE, 0, None, None) == _abi.MQA_ERR_UNSUPPORTED
+    assert lib.splitkv_combine(FAKE, FAKE, 1, 1, 1, 128, FAKE, 3, None, None) == _abi.MQA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,hq,d,max_len,splits,expect_splits", [
+    (2, 8, 128, 256, 1, 1), (2, 8, 128, 256, 4, 4), (4, 32, 128, 131072, 64, 64), (1, 4, 64, 300, 7, 5),
+    (3, 8, 64, 65, 2, 2), (3, 8, 64, 64, 2, 1),
+])
+def test_workspace_size_matches_split_plan(lib, B, hq, d, max_len, splits, expect_splits):
+    """Explicit split counts are rounded to 64-token chunks: chunk =
+    ceil(ceil(L/S)/64)*64, effective splits = ceil(L/chunk); the workspace holds
+    fp32 partial outputs [B, H_q, S, d] (padded to 256 bytes) and fp32 lse [B, H_q, S]."""
+    lay = _layout(batch=B, h_q=hq, h_kv=hq // 4 or 1, head_dim=d, capacity=max(max_len, 1))
+    got = lib.mqa_workspace_size(ctypes.byref(lay), max_len, splits, 0)
+    if expect_splits == 1:
+        assert got == 0
+    else:
+        o = (B * hq * expect_splits * d * 4 + 255) // 256 * 256
+        assert got == o + B * hq * expect_splits * 4
+
+
+def test_invalid_layout_queries(lib):
+    assert lib.mqa_choose_splits(None, 10, 0) == -1
+    assert lib.mqa_choose_splits(ctypes.byref(_layout(h_kv=3)), 10, 0) == -1
+    assert lib.mqa_workspace_size(ctypes.byref(_layout()), 0, 1, 0) == 0
