@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: one JSON line.
+
+A step is one pass of the whole decode hot path over one batch: kv_append_rope
+(RoPE + append of the new token) and gqa_decode_attention (attention over the
+cache, plus the split combine when it splits), all through the C ABI.
+The default workload is the Llama-style GQA decode step (batch 32, 32 query
+heads, 8 KV heads, head_dim 128, 4096-token bf16 cache, RoPE base 10000).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``value`` is the achieved HBM throughput of the step in GB/s (algorithmic
+bytes / device time, summed over ranks); ``ms_per_step`` gives the step time.
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path). ``--impl reference`` times the fp64 CPU oracle on the host
+cores instead, one (sequence, kv head) unit of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# The oracle legs run single-threaded: pin BLAS before numpy loads.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from synthetic import make_contiguous_case, make_paged_case, workload  # noqa: E402
+
+METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 GPU"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "gqa4k"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["decode_mma.cu", "ptx.cuh", "launch.h"]
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mqa_decode_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload_name)
+        if e and e.get("source_sha") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def step_bytes(w, lens, out_esize):
+    """Algorithmic bytes of one step: every cached K/V byte read once (including
+    the new token), q_new read, out written, k_new/v_new read and their slot
+    written, and (paged) the block-table entries used."""
+    es = w.esize
+    kv = 2 * int(lens.sum()) * w.h_kv * w.head_dim * es
+    q = w.batch * w.h_q * w.head_dim * es
+    out = w.batch * w.h_q * w.head_dim * out_esize
+    append = 2 * 2 * w.batch * w.h_kv * w.head_dim * es
+    table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
+    return kv + q + out + append + table
+
+
+def attention_bytes(w, lens, out_esize):
+    """Algorithmic bytes of one gqa_decode_attention launch: K/V of every token,
+    q_rot (fp32) read, out written, block-table entries (paged)."""
+    kv = 2 * int(lens.sum()) * w.h_kv * w.head_dim * w.esize
+    q = w.batch * w.h_q * w.head_dim * 4
+    out = w.batch * w.h_q * w.head_dim * out_esize
+    table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
+    return kv + q + out + table
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, sampled every 100 ms in a thread."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sel = [p for t, p in self.samples if t0 <= t <= t1]
+        if not sel:
+            sel = [p for _, p in self.samples[-5:]]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in sel if num(p[1]) is not None]
+        mx = [num(p[2]) for p in sel if num(p[2]) is not None]
+        pw = [num(p[3]) for p in sel if num(p[3]) is not None]
+        reasons = sorted({name for p in sel for name, v in zip(self.NAMES, p[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sel), "power_w_max": max(pw) if pw else None}
+
+
+def gpu_index_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ----------------------------------------------------------- inputs / oracle
+def build_case(w, device):
+    if w.paged:
+        return make_paged_case(w, device)
+    return make_contiguous_case(w, device)
+
+
+def unit_inputs(w, case, units):
+    """CPU copies of the inputs of (b, j) units, taken before any step runs."""
+    G = w.group
+    out = []
+    lens = case.seq_lens.cpu()
+    for b, j in units:
+        L = int(lens[b])
+        if w.paged:
+            n = (L + w.page_size - 1) // w.page_size
+            pages = case.block_table[b, :n].long()
+            K = case.k_pool[pages, j].reshape(-1, w.head_dim)[:L].cpu()
+            V = case.v_pool[pages, j].reshape(-1, w.head_dim)[:L].cpu()
+        else:
+            K = case.k_cache[b, j, :L].cpu()
+            V = case.v_cache[b, j, :L].cpu()
+        out.append(dict(b=b, j=j, L=L, q=case.q_new[b, j * G:(j + 1) * G].cpu(), k=case.k_new[b, j].cpu(),
+                        v=case.v_new[b, j].cpu(), K=K, V=V))
+    return out
+
+
+def unit_bytes(w, L, out_esize):
+    es = w.esize
+    return (2 * L * w.head_dim * es + w.group * w.head_dim * (es + out_esize) + 4 * w.head_dim * es)
+
+
+def run_oracle_units(w, inputs, budget_s: float, min_units: int = 2):
+    """Time oracle.decode_unit over the units, cycling through them, until the
+    budget is spent. Returns the first result of each unit and the totals."""
+    import oracle  # test infrastructure: the CPU-baseline leg only
+
+    scale = 1.0 / math.sqrt(w.head_dim)
+    results = {}
+    done = 0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        u = inputs[i % len(inputs)]
+        o, lse, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype)
+        results.setdefault(i % len(inputs), (u, o))
+        done += 1
+        i += 1
+        if done >= min_units and time.perf_counter() - t0 > budget_s:
+            break
+    return list(results.values()), done, time.perf_counter() - t0
+
+
+# --------------------------------------------------------------- our arm
+def bench_ours(args):
+    import mqa_decode_attention_gb300 as m
+    import numpy as np
+
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = workload(args.workload)
+    if args.splits is not None:
+        w = w.with_(num_splits=args.splits)
+    case = build_case(w, dev)
+    lens_cpu = case.seq_lens.cpu()
+    max_len = int(lens_cpu.max())
+    if w.paged:
+        lay = m.layout_paged(case.k_pool, case.v_pool, case.block_table, w.h_q)
+    else:
+        lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q)
+    variant = args.variant
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=w.num_splits, variant=variant, device=dev)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    splits_used = w.num_splits if w.num_splits > 0 else m.choose_splits(lay, max_len, variant)
+    out_es = bufs.out.element_size()
+    sbytes = step_bytes(w, lens_cpu, out_es)
+    abytes = attention_bytes(w, lens_cpu, out_es)
+    stream = torch.cuda.current_stream()
+
+    # CPU-baseline units (rank 0, N = 1), copied before any step touches the cache
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    units = []
+    if do_cpu:
+        g = torch.Generator().manual_seed(w.seed)
+        perm = torch.randperm(w.batch * w.h_kv, generator=g).tolist()
+        units = unit_inputs(w, case, [(u // w.h_kv, u % w.h_kv) for u in perm[:args.cpu_units or len(perm)]])
+
+    def append():
+        m.kv_append_rope(lay, case.q_new, case.k_new, case.v_new, case.pos, w.rope_base, bufs.q_rot, bufs.err, stream)
+
+    def attend():
+        m.gqa_decode_attention(lay, bufs.q_rot, case.seq_lens, max_len, scale, w.num_splits, bufs.out, bufs.lse,
+                               bufs.workspace, variant, bufs.err, stream)
+
+    def step():
+        m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs, w.rope_base,
+                      scale, w.num_splits, variant, stream)
+
+    launches_per_step = 2 + (1 if splits_used > 1 else 0)
+
+    # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
+    sampler = ClockSampler(gpu_index_for(local))
+    t_warm = time.monotonic()
+    n_warm = 0
+    while n_warm < args.warmup or time.monotonic() - t_warm < 1.0:
+        step()
+        n_warm += 1
+        if n_warm % 256 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    t_clock0 = time.monotonic() - 0.5
+
+    # timed region: K steps through mqa_decode_step, events at both ends
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    K = args.steps
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(K):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_clock1 = time.monotonic()
+    total_ms = t_start.elapsed_time(t_end)
+
+    # per-kernel durations: K more steps as separate calls with an event
+    # around each launch (the fused call admits no event between its launches)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        ev_s[i].record(stream)
+        append()
+        ev_m[i].record(stream)
+        attend()
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    append_ms = statistics.fmean(ev_s[i].elapsed_time(ev_m[i]) for i in range(K))
+    attn_ms = statistics.fmean(ev_m[i].elapsed_time(ev_e[i]) for i in range(K))
+    err_word = int(bufs.err.item())
+    if err_word != 0:
+        raise RuntimeError(f"device error word {err_word:#x} after the timed steps")
+
+    max_ms = total_ms
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        max_ms = float(t.item())
+    ms_per_step = max_ms / K
+    value = world * sbytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end: pinned host inputs copied in, output copied out, every step
+    host_in = [x.cpu().pin_memory() for x in (case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens)]
+    dev_in = [case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens]
+    host_out = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    for _ in range(3):
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        host_out.copy_(bufs.out, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        host_out.copy_(bufs.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * sbytes / (e2e_ms / K * 1e-3) / 1e9
+
+    peak, peak_src = measured_peak()
+    achieved = abytes / (attn_ms * 1e-3) / 1e9
+    kernel_name = "decode_mma_kernel" if (variant in (0, 2) and w.dtype == "bf16") else "decode_fma_kernel"
+    traffic = ncu_traffic(args.workload) if kernel_name == "decode_mma_kernel" else None
+    clocks = sampler.summary(t_clock0, t_clock1)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v and cache; no dataset)",
+        "config": {
+            "workload": (f"{w.name}: batch {w.batch}, H_q {w.h_q}, H_kv {w.h_kv}, head_dim {w.head_dim}, "
+                         + (f"paged {w.page_size}-token pages, lengths U[{w.len_lo},{w.len_hi}]" if w.paged
+                            else f"contiguous {w.dtype} cache of {w.seq_len} tokens/seq") + ", RoPE base 10000"),
+            "batch_per_gpu": w.batch,
+            "tokens_per_step_per_gpu": int(lens_cpu.sum()),
+            "num_splits": splits_used,
+            "variant": {0: "auto", 1: "cuda_core", 2: "tensor_core"}[variant],
+            "bytes_per_step_per_gpu": sbytes,
+            "l2": "inputs larger than L2 (no flush): %.0f MB streamed per step vs 129 MB L2" % (sbytes / 1e6),
+            "parallelism": f"dp{world}" if world > 1 else "single",
+        },
+        "kernels_ms": {"kv_append_rope": round(append_ms, 6), "gqa_decode_attention": round(attn_ms, 6),
+                       "how": "second pass of K steps, separate calls, CUDA events around each launch"},
+        "roofline": {
+            "bound": "hbm",
+            "kernel": kernel_name + (" + combine_kernel" if splits_used > 1 else ""),
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": abytes,
+            "peak_source": peak_src,
+            "frac_of_8000": round(achieved / 8000.0, 4),
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / K, 6)},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+    }
+
+    if do_cpu:
+        results, n_done, secs = run_oracle_units(w, units, args.cpu_seconds)
+        by_unit = {(u["b"], u["j"]): u for u, _ in results}
+        done = sum(unit_bytes(w, units[i % len(units)]["L"], out_es) for i in range(n_done))
+        out_host = bufs.out.float().cpu().numpy()
+        G = w.group
+        errs = [float(np.max(np.abs(out_host[u["b"], u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
+        line["cpu_baseline"] = {
+            "value": round(done / secs / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_done} (sequence, kv head) units of the step ({len(by_unit)} distinct of "
+                      f"{w.batch * w.h_kv}), fp64 numpy, single thread, {secs:.1f} s",
+            "ms_per_step_extrapolated": round(secs / n_done * w.batch * w.h_kv * 1e3, 1),
+        }
+        line["parity_sample"] = {"units": len(results), "max_abs_err": max(errs), "tolerance": 2e-2}
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm
+def bench_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workload(args.workload)
+    case = build_case(w, "cpu")
+    lens = case.seq_lens
+    n_units = w.batch * w.h_kv
+    order = [(u // w.h_kv, u % w.h_kv) for u in range(n_units)]
+    out_es = w.esize
+
+    def one(i):
+        u = unit_inputs(w, case, [order[i % n_units]])
+        return u
+
+    import oracle  # the reference arm is the oracle
+
+    scale = 1.0 / math.sqrt(w.head_dim)
+    inputs = [one(i)[0] for i in range(min(n_units, args.warmup + args.steps))]
+
+    def run(i):
+        u = inputs[i % len(inputs)]
+        oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype)
+        return unit_bytes(w, u["L"], out_es)
+
+    for i in range(args.warmup):
+        run(i)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        done += run(args.warmup + i)
+    secs = time.perf_counter() - t0
+    value = done / secs / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "impl": "reference",
+        "config": {"workload": w.name, "batch_per_gpu": w.batch, "tokens_per_step_per_gpu": int(lens.sum()),
+                   "step": "one (sequence, kv head) unit of the workload per step, cycling over the units"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} units of {n_units}, fp64 numpy, single thread"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--splits", type=int, default=None, help="override the workload's split count (0 = auto)")
+    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-units", type=int, default=0, help="distinct units in the CPU sample (0 = all)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

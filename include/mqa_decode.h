@@ -182,6 +182,24 @@ MQA_API mqa_status splitkv_combine(const float* o_part, const float* lse_part, i
                            int32_t num_splits, int32_t head_dim, void* out, int32_t out_dtype, float* lse_out,
                            mqa_stream_t stream);
 
+/*
+ * mqa_decode_step -- the whole decode step in one call: kv_append_rope, then
+ * gqa_decode_attention (and the combine when it splits), on one stream. The
+ * arguments mean what they mean in those two calls; q_rot is the caller's
+ * fp32 [batch, h_q, head_dim] scratch that carries the rotated query from the
+ * first launch to the second. Every argument of both calls is checked before
+ * the first launch. Because the attention launch directly follows the append
+ * launch, it is allowed to start while the append is still running: it
+ * streams every cached row except the appended one, the lengths and the
+ * block table early, and waits for the append before it reads q_rot or the
+ * new token's row.
+ */
+MQA_API mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const void* k_new,
+                                   const void* v_new, const int32_t* pos, const int32_t* seq_lens,
+                                   int32_t max_seq_len, double rope_base, float scale, int32_t num_splits,
+                                   float* q_rot, void* out, int32_t out_dtype, float* lse_out, void* workspace,
+                                   size_t workspace_bytes, int32_t variant, int32_t* err_word, mqa_stream_t stream);
+
 /* Split count gqa_decode_attention uses for num_splits = 0 on the current device
  * (>= 1), or -1 if the layout is invalid. */
 MQA_API int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant);

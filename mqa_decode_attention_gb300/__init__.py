@@ -170,12 +170,17 @@ class DecodeBuffers:
 def decode_step(layout: KVLayout, q_new, k_new, v_new, pos, seq_lens, max_seq_len: int, bufs: DecodeBuffers,
                 rope_base: float = 10000.0, scale: float | None = None, num_splits: int = 0,
                 variant: int = MQA_VARIANT_AUTO, stream=None) -> torch.Tensor:
-    """One decode step: append with RoPE at ``pos`` (= seq_lens - 1), then
-    attention over ``seq_lens`` tokens (and the combine when it splits).
-    Returns ``bufs.out``."""
+    """One decode step through ``mqa_decode_step``: append with RoPE at ``pos``
+    (= seq_lens - 1), then attention over ``seq_lens`` tokens (and the combine
+    when it splits). Returns ``bufs.out``."""
     if scale is None:
         scale = 1.0 / math.sqrt(layout.head_dim)
-    kv_append_rope(layout, q_new, k_new, v_new, pos, rope_base, bufs.q_rot, bufs.err, stream)
-    gqa_decode_attention(layout, bufs.q_rot, seq_lens, max_seq_len, scale, num_splits, bufs.out, bufs.lse,
-                         bufs.workspace, variant, bufs.err, stream)
+    ws = bufs.workspace
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = library().mqa_decode_step(ctypes.byref(layout), _ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(pos),
+                                   _ptr(seq_lens), int(max_seq_len), float(rope_base), float(scale), int(num_splits),
+                                   _ptr(bufs.q_rot), _ptr(bufs.out), _dtype_code(bufs.out.dtype), _ptr(bufs.lse),
+                                   _ptr(ws), ws_bytes, int(variant), _ptr(bufs.err), _stream(stream))
+    if st != 0:
+        raise MqaError("mqa_decode_step", st)
     return bufs.out

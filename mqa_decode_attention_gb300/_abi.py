@@ -61,6 +61,11 @@ _PROTOTYPES = {
          ctypes.c_size_t, c_i32, c_vp, c_vp],
     ),
     "splitkv_combine": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp]),
+    "mqa_decode_step": (
+        c_i32,
+        [ctypes.POINTER(KVLayout), c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, ctypes.c_double, ctypes.c_float, c_i32, c_vp,
+         c_vp, c_i32, c_vp, c_vp, ctypes.c_size_t, c_i32, c_vp, c_vp],
+    ),
     "mqa_choose_splits": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32]),
     "mqa_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32]),
     "mqa_status_string": (ctypes.c_char_p, [c_i32]),

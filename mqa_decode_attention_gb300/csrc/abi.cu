@@ -89,10 +89,12 @@ int head_blocks(const mqa_kv_layout* L, const KernelShape& ks) {
 }
 
 // Token-axis split count. Blocks of one (sequence, kv head) are independent,
-// so the only reasons to split are (a) too few units to keep every SM
-// streaming, and (b) long sequences whose blocks would finish late (the
-// device-side lengths may vary up to max_seq_len), which chunks of a bounded
-// size avoid.
+// so the only reasons to split are (a) too few units to fill the GPU in one
+// wave, and (b) device-side lengths that may vary up to max_seq_len, where
+// bounded chunks keep long sequences from finishing last. Measured on GB300:
+// a single wave of equal blocks streams best (more, smaller blocks add
+// partial-output traffic and a second wave), and 4096-token chunks balance a
+// paged batch of lengths spread over [128, 16384].
 int choose_splits(const mqa_kv_layout* L, int max_len, int variant) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -100,16 +102,17 @@ int choose_splits(const mqa_kv_layout* L, int max_len, int variant) {
   const KernelShape ks = decode_shape(L, variant);
   const int by_smem = ks.smem_bytes > 0 ? di.smem_per_sm / (ks.smem_bytes + 1024) : 8;
   const int by_threads = di.threads_per_sm / ks.threads;
-  const int per_sm = std::max(1, std::min(by_smem, by_threads));
+  int per_sm = std::max(1, std::min(by_smem, by_threads));
+  if (ks.max_ctas_per_sm > 0) per_sm = std::min(per_sm, ks.max_ctas_per_sm);
   const long long slots = static_cast<long long>(di.sms) * per_sm;
   const long long units = static_cast<long long>(L->batch) * L->h_kv * head_blocks(L, ks);
   const int tiles = (max_len + kTile - 1) / kTile;
   int s = 1;
-  if (units < slots) s = static_cast<int>((slots + units - 1) / units);
   if (L->paged) {
-    // bound the work of one block so that late long sequences do not leave a tail
-    const int cap_tiles = 32;  // 2048 tokens
-    s = std::max(s, (tiles + cap_tiles - 1) / cap_tiles);
+    const int chunk_tiles = 64;  // 4096 tokens
+    s = (tiles + chunk_tiles - 1) / chunk_tiles;
+  } else if (units < slots) {
+    s = static_cast<int>(slots / units);  // at most one wave
   }
   return std::max(1, std::min(s, tiles));
 }
@@ -184,26 +187,8 @@ bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L) {
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* mqa_status_string(mqa_status s) {
-  switch (s) {
-    case MQA_OK: return "ok";
-    case MQA_ERR_INVALID_ARG: return "invalid argument";
-    case MQA_ERR_UNSUPPORTED: return "unsupported configuration";
-    case MQA_ERR_CUDA: return "CUDA error";
-    case MQA_ERR_WORKSPACE: return "workspace missing or too small";
-  }
-  return "unknown status";
-}
-
-const char* mqa_last_cuda_error(void) { return g_cuda_error; }
-
-mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
-                          const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word,
-                          mqa_stream_t stream) {
+mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                       const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word, mqa_stream_t stream) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
   if (!q_new || !k_new || !v_new || !pos || !q_rot || !err_word) return MQA_ERR_INVALID_ARG;
@@ -238,6 +223,120 @@ mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new, const 
   if (e != cudaSuccess) return fail_cuda(e);
   const cudaError_t e2 = cudaGetLastError();
   return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+}
+
+mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens, int32_t max_seq_len,
+                          float scale, int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
+                          void* workspace, size_t workspace_bytes, int32_t variant, int32_t* err_word,
+                          mqa_stream_t stream, int early) {
+  const mqa_status st = check_layout(layout);
+  if (st != MQA_OK) return st;
+  if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
+  if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
+      (lse_out && !aligned(lse_out, 4)))
+    return MQA_ERR_INVALID_ARG;
+  if (max_seq_len < 1 || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || num_splits < 0) return MQA_ERR_INVALID_ARG;
+  if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return MQA_ERR_INVALID_ARG;
+  const int v = resolve_variant(layout, variant);
+  if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype != MQA_BF16) return MQA_ERR_UNSUPPORTED;
+
+  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+  int splits, chunk;
+  split_plan(req, max_seq_len, &splits, &chunk);
+  const size_t need = partial_bytes(layout, splits);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need) return MQA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return MQA_ERR_INVALID_ARG;
+  }
+
+  const KernelShape ks = decode_shape(layout, v);
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = layout->batch;
+  p.h_q = layout->h_q;
+  p.h_kv = layout->h_kv;
+  p.group = layout->h_q / layout->h_kv;
+  p.head_dim = layout->head_dim;
+  p.cache_dtype = layout->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.paged = layout->paged;
+  p.k_cache = layout->k_cache;
+  p.v_cache = layout->v_cache;
+  p.capacity = layout->capacity;
+  p.page_size = layout->page_size;
+  p.num_pages = layout->num_pages;
+  p.max_pages = layout->max_pages_per_seq;
+  p.block_table = layout->block_table;
+  p.q_rot = q_rot;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_splits = splits;
+  p.chunk = chunk;
+  p.head_blocks = head_blocks(layout, ks);
+  p.early = early;
+  p.out = out;
+  p.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.lse_out = lse_out;
+  p.err = err_word;
+  if (splits > 1) {
+    const size_t rows = static_cast<size_t>(layout->batch) * layout->h_q;
+    const size_t o_bytes = ((rows * splits * layout->head_dim * 4) + 255) / 256 * 256;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + o_bytes);
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (v == MQA_VARIANT_TENSOR_CORE) {
+    CUtensorMap tk, tv;
+    if (!make_tensor_map(&tk, layout->k_cache, layout) || !make_tensor_map(&tv, layout->v_cache, layout)) {
+      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+      return MQA_ERR_CUDA;
+    }
+    e = launch_decode_mma(p, tk, tv, s);
+  } else {
+    e = launch_decode_fma(p, s);
+  }
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (splits > 1) {
+    CombineParams c;
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.rows = layout->batch * layout->h_q;
+    c.num_splits = splits;
+    c.head_dim = layout->head_dim;
+    c.out = out;
+    c.out_dtype = p.out_dtype;
+    c.lse_out = lse_out;
+    e = launch_combine(c, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  const cudaError_t e2 = cudaGetLastError();
+  return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mqa_status_string(mqa_status s) {
+  switch (s) {
+    case MQA_OK: return "ok";
+    case MQA_ERR_INVALID_ARG: return "invalid argument";
+    case MQA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MQA_ERR_CUDA: return "CUDA error";
+    case MQA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* mqa_last_cuda_error(void) { return g_cuda_error; }
+
+mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                          const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word,
+                          mqa_stream_t stream) {
+  return append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream);
 }
 
 int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant) {
@@ -285,90 +384,35 @@ mqa_status gqa_decode_attention(const mqa_kv_layout* layout, const float* q_rot,
                                 int32_t max_seq_len, float scale, int32_t num_splits, void* out,
                                 int32_t out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
                                 int32_t variant, int32_t* err_word, mqa_stream_t stream) {
+  return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out, workspace,
+                        workspace_bytes, variant, err_word, stream, /*early=*/0);
+}
+
+mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                           const int32_t* pos, const int32_t* seq_lens, int32_t max_seq_len, double rope_base,
+                           float scale, int32_t num_splits, float* q_rot, void* out, int32_t out_dtype,
+                           float* lse_out, void* workspace, size_t workspace_bytes, int32_t variant,
+                           int32_t* err_word, mqa_stream_t stream) {
+  // Check the attention's arguments too before anything is launched.
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
-  if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
-      (lse_out && !aligned(lse_out, 4)))
+  if (!seq_lens || !out || max_seq_len < 1 || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE || num_splits < 0)
     return MQA_ERR_INVALID_ARG;
-  if (max_seq_len < 1 || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || num_splits < 0) return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
-  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return MQA_ERR_INVALID_ARG;
   const int v = resolve_variant(layout, variant);
   if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype != MQA_BF16) return MQA_ERR_UNSUPPORTED;
-
-  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
-  int splits, chunk;
-  split_plan(req, max_seq_len, &splits, &chunk);
-  const size_t need = partial_bytes(layout, splits);
-  if (need > 0) {
-    if (workspace == nullptr || workspace_bytes < need) return MQA_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return MQA_ERR_INVALID_ARG;
+  {
+    const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+    int splits, chunk;
+    split_plan(req, max_seq_len, &splits, &chunk);
+    const size_t need = partial_bytes(layout, splits);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MQA_ERR_WORKSPACE;
   }
-
-  const KernelShape ks = decode_shape(layout, v);
-  DecodeParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.batch = layout->batch;
-  p.h_q = layout->h_q;
-  p.h_kv = layout->h_kv;
-  p.group = layout->h_q / layout->h_kv;
-  p.head_dim = layout->head_dim;
-  p.cache_dtype = layout->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
-  p.paged = layout->paged;
-  p.k_cache = layout->k_cache;
-  p.v_cache = layout->v_cache;
-  p.capacity = layout->capacity;
-  p.page_size = layout->page_size;
-  p.num_pages = layout->num_pages;
-  p.max_pages = layout->max_pages_per_seq;
-  p.block_table = layout->block_table;
-  p.q_rot = q_rot;
-  p.seq_lens = seq_lens;
-  p.max_seq_len = max_seq_len;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.num_splits = splits;
-  p.chunk = chunk;
-  p.head_blocks = head_blocks(layout, ks);
-  p.out = out;
-  p.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
-  p.lse_out = lse_out;
-  p.err = err_word;
-  if (splits > 1) {
-    const size_t rows = static_cast<size_t>(layout->batch) * layout->h_q;
-    const size_t o_bytes = ((rows * splits * layout->head_dim * 4) + 255) / 256 * 256;
-    p.o_part = static_cast<float*>(workspace);
-    p.lse_part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + o_bytes);
-  }
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (v == MQA_VARIANT_TENSOR_CORE) {
-    CUtensorMap tk, tv;
-    if (!make_tensor_map(&tk, layout->k_cache, layout) || !make_tensor_map(&tv, layout->v_cache, layout)) {
-      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
-      return MQA_ERR_CUDA;
-    }
-    e = launch_decode_mma(p, tk, tv, s);
-  } else {
-    e = launch_decode_fma(p, s);
-  }
-  if (e != cudaSuccess) return fail_cuda(e);
-  if (splits > 1) {
-    CombineParams c;
-    c.o_part = p.o_part;
-    c.lse_part = p.lse_part;
-    c.rows = layout->batch * layout->h_q;
-    c.num_splits = splits;
-    c.head_dim = layout->head_dim;
-    c.out = out;
-    c.out_dtype = p.out_dtype;
-    c.lse_out = lse_out;
-    e = launch_combine(c, s);
-    if (e != cudaSuccess) return fail_cuda(e);
-  }
-  const cudaError_t e2 = cudaGetLastError();
-  return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+  const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream);
+  if (a != MQA_OK) return a;
+  return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out, workspace,
+                        workspace_bytes, variant, err_word, stream, /*early=*/1);
 }
 
 }  // extern "C"

@@ -7,11 +7,13 @@
 // rotated. Paged slot: "KV Cache 최적화 심층 분석" (youngju.dev), class
 // PagedKVCache (block pos / block_size, row pos % block_size).
 //
-// One block per sequence. The d/2 angles pos * theta_i are formed and their
-// sine and cosine taken in fp64 once per sequence, shared by all heads. The
-// key is rotated in fp64 with explicit round-to-nearest products (no fused
-// multiply-add), then rounded once to the cache dtype; the query is rotated
-// in fp32 and written as fp32.
+// Blocks cover (sequence, chunk of heads); q heads come first, then k/v
+// heads. Each block forms the d/2 angles pos * theta_i in fp64, reduces them
+// to [-pi, pi] by Cody-Waite additive range reduction (2 pi split into three
+// doubles, products folded in with fused multiply-adds) and takes their sine
+// and cosine in fp64. The key is rotated in fp64 with explicit
+// round-to-nearest products (no fused multiply-add), then rounded once to the
+// cache dtype; the query is rotated in fp32 and written as fp32.
 #include <cuda_bf16.h>
 
 #include "../../include/mqa_decode.h"
@@ -22,6 +24,23 @@ namespace mqa {
 namespace {
 
 constexpr int kAppendThreads = 256;
+constexpr int kHeadsPerBlock = 8;
+
+// 2 pi = kTwoPi1 + kTwoPi2 + kTwoPi3 (leading double, then the next two
+// 53-bit pieces of the remainder).
+constexpr double kTwoPi1 = 6.283185307179586232;
+constexpr double kTwoPi2 = 2.4492935982947063545e-16;
+constexpr double kTwoPi3 = -5.9895396194366793e-33;
+constexpr double kInvTwoPi = 0.15915494309189533577;
+
+// x - k 2 pi with k = nearest integer to x / (2 pi); |x| < 2^40 here.
+__device__ __forceinline__ double reduce_two_pi(double x) {
+  const double k = rint(x * kInvTwoPi);
+  double r = fma(-k, kTwoPi1, x);
+  r = fma(-k, kTwoPi2, r);
+  r = fma(-k, kTwoPi3, r);
+  return r;
+}
 
 template <typename T>
 struct Elem;
@@ -63,27 +82,31 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   __shared__ int s_ok;
 
   // Let a dependent decode launch start its prologue; it waits for this grid
-  // before it reads q_rot or the cache.
+  // before it reads q_rot or the appended slot.
   grid_dependents_launch();
 
   const int b = blockIdx.x;
   const int D = p.head_dim;
   const int half = D >> 1;
   const int pos = p.pos[b];
+  const int h_begin = blockIdx.y * kHeadsPerBlock;  // in [0, h_q + h_kv)
+  const int h_end = min(h_begin + kHeadsPerBlock, p.h_q + p.h_kv);
+  const bool has_kv = h_end > p.h_q;
 
   if (threadIdx.x < half) {
     double sn, cs;
-    sincos(static_cast<double>(pos) * p.theta[threadIdx.x], &sn, &cs);
+    sincos(reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]), &sn, &cs);
     s_cos[threadIdx.x] = cs;
     s_sin[threadIdx.x] = sn;
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && has_kv) {
     int ok = 1;
     long long row = 0, stride = 0;
+    const bool report = h_begin <= p.h_q;  // one block per sequence reports
     if (!p.paged) {
       if (pos < 0 || pos >= p.capacity) {
         ok = 0;
-        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+        if (report) atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
       } else {
         row = (static_cast<long long>(b) * p.h_kv * p.capacity + pos) * D;
         stride = p.capacity * D;
@@ -92,12 +115,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
       const int lp = pos >= 0 ? pos / p.page_size : -1;
       if (pos < 0 || lp >= p.max_pages) {
         ok = 0;
-        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+        if (report) atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
       } else {
         const int page = p.block_table[static_cast<long long>(b) * p.max_pages + lp];
         if (page < 0 || page >= p.num_pages) {
           ok = 0;
-          atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
+          if (report) atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
         } else {
           row = (static_cast<long long>(page) * p.h_kv * p.page_size + (pos % p.page_size)) * D;
           stride = static_cast<long long>(p.page_size) * D;
@@ -110,25 +133,32 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
   __syncthreads();
 
-  // q: fp32 rotation, fp32 output
-  const T* q = static_cast<const T*>(p.q_new) + static_cast<long long>(b) * p.h_q * D;
-  float* qr = p.q_rot + static_cast<long long>(b) * p.h_q * D;
-  for (int idx = threadIdx.x; idx < p.h_q * half; idx += kAppendThreads) {
-    const int h = idx / half, i = idx - h * half;
-    const float2 x = Elem<T>::load2(q + h * D + 2 * i);
-    const float c = static_cast<float>(s_cos[i]), s = static_cast<float>(s_sin[i]);
-    *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
+  // q heads of this block: fp32 rotation, fp32 output
+  const int q_end = min(h_end, p.h_q);
+  if (h_begin < q_end) {
+    const T* q = static_cast<const T*>(p.q_new) + static_cast<long long>(b) * p.h_q * D;
+    float* qr = p.q_rot + static_cast<long long>(b) * p.h_q * D;
+    const int n = (q_end - h_begin) * half;
+    for (int idx = threadIdx.x; idx < n; idx += kAppendThreads) {
+      const int h = h_begin + idx / half, i = idx % half;
+      const float2 x = Elem<T>::load2(q + h * D + 2 * i);
+      const float c = static_cast<float>(s_cos[i]), s = static_cast<float>(s_sin[i]);
+      *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
+    }
   }
-  if (!s_ok) return;
+  if (!has_kv || !s_ok) return;
 
-  // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
+  // kv heads of this block: k in fp64 with one rounding to the cache dtype; v bit copy
+  const int j_begin = max(h_begin, p.h_q) - p.h_q;
+  const int j_end = h_end - p.h_q;
   const T* k = static_cast<const T*>(p.k_new) + static_cast<long long>(b) * p.h_kv * D;
   const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(b) * p.h_kv * D;
   T* kc = static_cast<T*>(p.k_cache) + s_row;
   T* vc = static_cast<T*>(p.v_cache) + s_row;
   const long long stride = s_stride;
-  for (int idx = threadIdx.x; idx < p.h_kv * half; idx += kAppendThreads) {
-    const int h = idx / half, i = idx - h * half;
+  const int n = (j_end - j_begin) * half;
+  for (int idx = threadIdx.x; idx < n; idx += kAppendThreads) {
+    const int h = j_begin + idx / half, i = idx % half;
     const float2 x = Elem<T>::load2(k + h * D + 2 * i);
     const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
     const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
@@ -140,11 +170,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 
 }  // namespace
 
-KernelShape append_rope_shape() { return {kAppendThreads, 0, 0}; }
+KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.batch);
+  cfg.gridDim = dim3(p.batch, (p.h_q + p.h_kv + kHeadsPerBlock - 1) / kHeadsPerBlock);
   cfg.blockDim = dim3(kAppendThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -421,7 +421,7 @@ template <typename T, int D, int HBLK>
 KernelShape shape_t() {
   constexpr int ST = fma_stages<T, D, HBLK>();
   using C = FmaCfg<T, D, HBLK, ST>;
-  return {C::kThreads, C::kSmemBytes, HBLK};
+  return {C::kThreads, C::kSmemBytes, HBLK, 0};
 }
 
 template <int HBLK>

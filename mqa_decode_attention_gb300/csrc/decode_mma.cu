@@ -93,8 +93,12 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     prefetch_tensormap(&tmap_v);
   }
   __syncthreads();
-  grid_dependency_wait();
-  // Lengths are read only after the preceding grid is complete and visible.
+  // Unless the preceding launch is known to be the append kernel, wait for it
+  // before reading anything. After the append kernel, the lengths, the block
+  // table and every cached row except the new token's are already final, so
+  // the producer streams them early and only the tile holding the new token
+  // (and the consumers, which need q_rot) wait.
+  if (!p.early) grid_dependency_wait();
   long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;
   if (limit > p.max_seq_len) limit = p.max_seq_len;
   int L = p.seq_lens[b];
@@ -120,6 +124,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
     }
     int issued = 0;
+    bool waited = !p.early;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
@@ -133,6 +138,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       }
       if (*reinterpret_cast<volatile int*>(&s_abort)) break;
       const int t0 = t_begin + it * kTile;
+      if (!waited && L - 1 < t0 + kTile) {  // this tile holds the appended token
+        grid_dependency_wait();
+        waited = true;
+      }
       const uint32_t kdst = smem_u32(smem + stage * C::kStageBytes);
       const uint32_t vdst = kdst + C::kTileBytes;
       const uint32_t fb = smem_u32(&full[stage]);
@@ -200,6 +209,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   const int c2 = (lane & 3) * 2;      // fragment column pair
 
   // Q as the A operand: rows = heads, k = head_dim, pre-scaled into the log2 domain
+  if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
   uint32_t qa[D / 16][4];
   {
     const float* q = p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
@@ -425,17 +435,17 @@ KernelShape decode_mma_shape(int head_dim, int group) {
   if (head_dim == 128) {
     if (hb == 2) {
       using C = MmaCfg<128, 2, mma_stages<128, 2>()>;
-      return {C::kThreads, C::kSmemBytes, 32};
+      return {C::kThreads, C::kSmemBytes, 32, 1};
     }
     using C = MmaCfg<128, 1, mma_stages<128, 1>()>;
-    return {C::kThreads, C::kSmemBytes, 16};
+    return {C::kThreads, C::kSmemBytes, 16, 0};
   }
   if (hb == 2) {
     using C = MmaCfg<64, 2, mma_stages<64, 2>()>;
-    return {C::kThreads, C::kSmemBytes, 32};
+    return {C::kThreads, C::kSmemBytes, 32, 1};
   }
   using C = MmaCfg<64, 1, mma_stages<64, 1>()>;
-  return {C::kThreads, C::kSmemBytes, 16};
+  return {C::kThreads, C::kSmemBytes, 16, 0};
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -42,6 +42,7 @@ struct DecodeParams {
   int num_splits;    // token-axis splits per (sequence, kv head); 1 = write `out` directly
   int chunk;         // tokens per split, a multiple of kTile
   int head_blocks;   // blocks of query heads a (sequence, kv head) is cut into
+  int early;         // 1: the preceding launch is the append kernel; stream K/V before waiting for it
   void* out;
   int out_dtype;
   float* lse_out;
@@ -65,6 +66,7 @@ struct KernelShape {
   int threads;
   int smem_bytes;
   int heads_per_cta;  // query heads one block serves
+  int max_ctas_per_sm;  // > 0: blocks per SM beyond this slow the kernel down (measured)
 };
 
 KernelShape append_rope_shape();

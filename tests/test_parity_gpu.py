@@ -357,3 +357,35 @@ def test_full_size_paged_sampled(m):
         got_k = _np(pc.k_pool[page, j, p % w.page_size])
         want_k = r["k_pool"][int(rank[p // w.page_size]), 0, p % w.page_size]
         assert np.all(np.abs(got_k - want_k) <= ulp_bf16(want_k))
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("paged", [False, True])
+def test_fused_step_equals_separate_calls(m, variant, paged):
+    """mqa_decode_step (append, then attention started early) gives exactly the
+    result of kv_append_rope followed by gqa_decode_attention."""
+    w = workload("paged" if paged else "gqa4k").with_(batch=3, h_q=16, h_kv=4, seed=44)
+    lens = torch.tensor([700, 1, 129], dtype=torch.int32)
+    outs = []
+    for fused in (True, False):
+        if paged:
+            c = make_paged_case(w, "cpu", seq_lens=lens)
+            kc, vc, bt = c.k_pool.to(DEV), c.v_pool.to(DEV), c.block_table.to(DEV)
+            lay = m.layout_paged(kc, vc, bt, w.h_q)
+        else:
+            c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=704)
+            kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+            lay = m.layout_contiguous(kc, vc, w.h_q)
+        bufs = m.DecodeBuffers.allocate(lay, 700, num_splits=3, variant=variant, device=DEV)
+        args = (c.q_new.to(DEV), c.k_new.to(DEV), c.v_new.to(DEV), c.pos.to(DEV), c.seq_lens.to(DEV))
+        if fused:
+            m.decode_step(lay, *args, 700, bufs, w.rope_base, 0.1, num_splits=3, variant=variant)
+        else:
+            m.kv_append_rope(lay, args[0], args[1], args[2], args[3], w.rope_base, bufs.q_rot, bufs.err)
+            m.gqa_decode_attention(lay, bufs.q_rot, args[4], 700, 0.1, 3, bufs.out, bufs.lse, bufs.workspace,
+                                   variant, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        outs.append((bufs.out.clone(), bufs.lse.clone(), kc.clone(), vc.clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
