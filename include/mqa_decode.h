@@ -200,6 +200,35 @@ MQA_API mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_ne
                                    float* q_rot, void* out, int32_t out_dtype, float* lse_out, void* workspace,
                                    size_t workspace_bytes, int32_t variant, int32_t* err_word, mqa_stream_t stream);
 
+/*
+ * gqa_decode_attention_noalloc -- gqa_decode_attention for callers that cannot
+ * allocate device memory (the pages have no counterpart of this call).
+ *
+ * A split run needs scratch for its per-split partial results; normally the
+ * caller allocates it and passes it as `workspace`. Callers that own no
+ * device allocator -- for instance a plugin loaded into a process whose
+ * framework has reserved the device memory for its own pool, or a serving
+ * loop that must not take cudaMalloc's implicit device synchronisation --
+ * use this call instead: the scratch is a fixed 32 MiB array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. The call itself allocates nothing and frees nothing.
+ *
+ * Arguments as in gqa_decode_attention, without workspace. Returns
+ * MQA_ERR_WORKSPACE when mqa_workspace_size(layout, max_seq_len, num_splits,
+ * variant) exceeds 32 MiB.
+ * The first call on a device looks up the scratch's device address with that
+ * device current; make that first call before any stream capture.
+ * All calls share the one scratch array and it keeps the last call's
+ * contents; nothing in it needs clearing, since every call rewrites each
+ * partial result it reads. Calls whose work overlaps on the GPU (two streams,
+ * or two host threads on different streams) race on the scratch and must be
+ * serialised by the caller.
+ */
+MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, const float* q_rot,
+                                                const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                                int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
+                                                int32_t variant, int32_t* err_word, mqa_stream_t stream);
+
 /* Split count gqa_decode_attention uses for num_splits = 0 on the current device
  * (>= 1), or -1 if the layout is invalid. */
 MQA_API int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant);
