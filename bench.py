@@ -244,6 +244,8 @@ def bench_ours(args):
     w = workload(args.workload)
     if args.splits is not None:
         w = w.with_(num_splits=args.splits)
+    if args.batch:
+        w = w.with_(batch=args.batch)
     case = build_case(w, dev)
     lens_cpu = case.seq_lens.cpu()
     max_len = int(lens_cpu.max())
@@ -285,7 +287,7 @@ def bench_ours(args):
     sampler = ClockSampler(gpu_index_for(local))
     t_warm = time.monotonic()
     n_warm = 0
-    while n_warm < args.warmup or time.monotonic() - t_warm < 1.0:
+    while n_warm < args.warmup or time.monotonic() - t_warm < args.warm_seconds:
         step()
         n_warm += 1
         if n_warm % 256 == 0:
@@ -499,6 +501,9 @@ def main():
     ap.add_argument("--splits", type=int, default=None, help="override the workload's split count (0 = auto)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--warm-seconds", type=float, default=1.0,
+                    help="minimum warm-up time, so the clock sampler sees the load (0 for profiler runs)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-units", type=int, default=0, help="distinct units in the CPU sample (0 = all)")
     args = ap.parse_args()

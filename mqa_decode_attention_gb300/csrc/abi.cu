@@ -146,40 +146,67 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 64-column (128-byte) swizzled boxes of kTile rows, or of one page when
-// pages are shorter than a tile.
-bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L) {
+// TMA descriptors for the tensor-core path: 128-byte swizzled boxes of
+// 64 columns, kTile rows (contiguous) or one page (paged, pages shorter than
+// a tile). With `merged`, head_dim 128 is described as 64 columns x 2 halves
+// where the half dimension has the smaller stride (128 bytes) than the row
+// (256 bytes): one box then carries both halves of its rows and lands in
+// shared memory as two 64-column spans, so a tile needs half as many copies.
+bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool merged) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t D = L->head_dim;
-  cuuint64_t dims[4];
-  cuuint64_t strides[3];
-  cuuint32_t box[4];
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const cuuint64_t row_bytes = D * 2;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const cuuint32_t rows = static_cast<cuuint32_t>(L->paged ? (L->page_size < kTile ? L->page_size : kTile) : kTile);
+  const cuuint64_t outer_rows = L->paged ? static_cast<cuuint64_t>(L->page_size) : static_cast<cuuint64_t>(L->capacity);
   cuuint32_t rank;
-  if (!L->paged) {
-    rank = 3;
-    dims[0] = D;
-    dims[1] = static_cast<cuuint64_t>(L->capacity);
-    dims[2] = static_cast<cuuint64_t>(L->batch) * L->h_kv;
-    strides[0] = D * 2;
-    strides[1] = static_cast<cuuint64_t>(L->capacity) * D * 2;
+  if (merged) {
+    dims[0] = 64;
+    dims[1] = outer_rows;
+    dims[2] = D / 64;
+    strides[0] = row_bytes;
+    strides[1] = 128;
     box[0] = 64;
-    box[1] = kTile;
-    box[2] = 1;
+    box[1] = rows;
+    box[2] = static_cast<cuuint32_t>(D / 64);
+    if (!L->paged) {
+      rank = 4;
+      dims[3] = static_cast<cuuint64_t>(L->batch) * L->h_kv;
+      strides[2] = static_cast<cuuint64_t>(L->capacity) * row_bytes;
+      box[3] = 1;
+    } else {
+      rank = 5;
+      dims[3] = static_cast<cuuint64_t>(L->h_kv);
+      dims[4] = static_cast<cuuint64_t>(L->num_pages);
+      strides[2] = static_cast<cuuint64_t>(L->page_size) * row_bytes;
+      strides[3] = static_cast<cuuint64_t>(L->h_kv) * L->page_size * row_bytes;
+      box[3] = 1;
+      box[4] = 1;
+    }
   } else {
-    rank = 4;
     dims[0] = D;
-    dims[1] = static_cast<cuuint64_t>(L->page_size);
-    dims[2] = static_cast<cuuint64_t>(L->h_kv);
-    dims[3] = static_cast<cuuint64_t>(L->num_pages);
-    strides[0] = D * 2;
-    strides[1] = static_cast<cuuint64_t>(L->page_size) * D * 2;
-    strides[2] = static_cast<cuuint64_t>(L->h_kv) * L->page_size * D * 2;
+    dims[1] = outer_rows;
+    strides[0] = row_bytes;
     box[0] = 64;
-    box[1] = static_cast<cuuint32_t>(L->page_size < kTile ? L->page_size : kTile);
-    box[2] = 1;
-    box[3] = 1;
+    box[1] = rows;
+    if (!L->paged) {
+      rank = 3;
+      dims[2] = static_cast<cuuint64_t>(L->batch) * L->h_kv;
+      strides[1] = static_cast<cuuint64_t>(L->capacity) * row_bytes;
+      box[2] = 1;
+    } else {
+      rank = 4;
+      dims[2] = static_cast<cuuint64_t>(L->h_kv);
+      dims[3] = static_cast<cuuint64_t>(L->num_pages);
+      strides[1] = static_cast<cuuint64_t>(L->page_size) * row_bytes;
+      strides[2] = static_cast<cuuint64_t>(L->h_kv) * L->page_size * row_bytes;
+      box[2] = 1;
+      box[3] = 1;
+    }
   }
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -290,7 +317,10 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   cudaError_t e;
   if (v == MQA_VARIANT_TENSOR_CORE) {
     CUtensorMap tk, tv;
-    if (!make_tensor_map(&tk, layout->k_cache, layout) || !make_tensor_map(&tv, layout->v_cache, layout)) {
+    p.merged_halves = layout->head_dim == 128 && make_tensor_map(&tk, layout->k_cache, layout, true) &&
+                      make_tensor_map(&tv, layout->v_cache, layout, true);
+    if (!p.merged_halves &&
+        (!make_tensor_map(&tk, layout->k_cache, layout, false) || !make_tensor_map(&tv, layout->v_cache, layout, false))) {
       snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
       return MQA_ERR_CUDA;
     }

@@ -7,13 +7,16 @@
 // rotated. Paged slot: "KV Cache 최적화 심층 분석" (youngju.dev), class
 // PagedKVCache (block pos / block_size, row pos % block_size).
 //
-// Blocks cover (sequence, chunk of heads); q heads come first, then k/v
-// heads. Each block forms the d/2 angles pos * theta_i in fp64, reduces them
-// to [-pi, pi] by Cody-Waite additive range reduction (2 pi split into three
-// doubles, products folded in with fused multiply-adds) and takes their sine
-// and cosine in fp64. The key is rotated in fp64 with explicit
-// round-to-nearest products (no fused multiply-add), then rounded once to the
-// cache dtype; the query is rotated in fp32 and written as fp32.
+// Blocks cover (sequence, chunk of heads): first the query-head blocks (up to
+// 8 heads each), then the kv-head blocks (2 heads each, so the fp64 key
+// rotation is spread over many SMs). Every thread issues its global loads
+// before the trigonometry so the two latencies overlap. Each block forms the
+// d/2 angles pos * theta_i in fp64, reduces them to [-pi, pi] by Cody-Waite
+// additive range reduction (2 pi split into three doubles, products folded in
+// with fused multiply-adds) and takes their sine and cosine in fp64. The key
+// is rotated in fp64 with explicit round-to-nearest products (no fused
+// multiply-add), then rounded once to the cache dtype; the query is rotated
+// in fp32 and written as fp32.
 #include <cuda_bf16.h>
 
 #include "../../include/mqa_decode.h"
@@ -24,7 +27,8 @@ namespace mqa {
 namespace {
 
 constexpr int kAppendThreads = 256;
-constexpr int kHeadsPerBlock = 8;
+constexpr int kQHeadsPerBlock = 8;   // 8 heads x 64 pairs = 2 pairs per thread at d = 128
+constexpr int kKvHeadsPerBlock = 2;  // 2 heads x 64 pairs <= one pair per thread
 
 // 2 pi = kTwoPi1 + kTwoPi2 + kTwoPi3 (leading double, then the next two
 // 53-bit pieces of the remainder).
@@ -88,10 +92,26 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   const int b = blockIdx.x;
   const int D = p.head_dim;
   const int half = D >> 1;
+  const int n_qblocks = (p.h_q + kQHeadsPerBlock - 1) / kQHeadsPerBlock;
+  const bool kv_block = static_cast<int>(blockIdx.y) >= n_qblocks;
   const int pos = p.pos[b];
-  const int h_begin = blockIdx.y * kHeadsPerBlock;  // in [0, h_q + h_kv)
-  const int h_end = min(h_begin + kHeadsPerBlock, p.h_q + p.h_kv);
-  const bool has_kv = h_end > p.h_q;
+
+  // Issue this thread's loads first (at most 2 pairs per thread).
+  int h_begin, h_end;
+  if (!kv_block) {
+    h_begin = blockIdx.y * kQHeadsPerBlock;
+    h_end = min(h_begin + kQHeadsPerBlock, p.h_q);
+  } else {
+    h_begin = (blockIdx.y - n_qblocks) * kKvHeadsPerBlock;
+    h_end = min(h_begin + kKvHeadsPerBlock, p.h_kv);
+  }
+  const int n_pairs = (h_end - h_begin) * half;
+  const T* src = kv_block ? static_cast<const T*>(p.k_new) + static_cast<long long>(b) * p.h_kv * D
+                          : static_cast<const T*>(p.q_new) + static_cast<long long>(b) * p.h_q * D;
+  float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+  const int i0 = threadIdx.x, i1 = threadIdx.x + kAppendThreads;
+  if (i0 < n_pairs) x0 = Elem<T>::load2(src + (h_begin + i0 / half) * D + 2 * (i0 % half));
+  if (i1 < n_pairs) x1 = Elem<T>::load2(src + (h_begin + i1 / half) * D + 2 * (i1 % half));
 
   if (threadIdx.x < half) {
     double sn, cs;
@@ -99,10 +119,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
     s_cos[threadIdx.x] = cs;
     s_sin[threadIdx.x] = sn;
   }
-  if (threadIdx.x == 0 && has_kv) {
+  if (threadIdx.x == 0 && kv_block) {
     int ok = 1;
     long long row = 0, stride = 0;
-    const bool report = h_begin <= p.h_q;  // one block per sequence reports
+    const bool report = h_begin == 0;  // one block per sequence reports
     if (!p.paged) {
       if (pos < 0 || pos >= p.capacity) {
         ok = 0;
@@ -133,33 +153,33 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
   __syncthreads();
 
-  // q heads of this block: fp32 rotation, fp32 output
-  const int q_end = min(h_end, p.h_q);
-  if (h_begin < q_end) {
-    const T* q = static_cast<const T*>(p.q_new) + static_cast<long long>(b) * p.h_q * D;
+  if (!kv_block) {
+    // q: fp32 rotation, fp32 output
     float* qr = p.q_rot + static_cast<long long>(b) * p.h_q * D;
-    const int n = (q_end - h_begin) * half;
-    for (int idx = threadIdx.x; idx < n; idx += kAppendThreads) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int idx = u == 0 ? i0 : i1;
+      if (idx >= n_pairs) continue;
+      const float2 x = u == 0 ? x0 : x1;
       const int h = h_begin + idx / half, i = idx % half;
-      const float2 x = Elem<T>::load2(q + h * D + 2 * i);
       const float c = static_cast<float>(s_cos[i]), s = static_cast<float>(s_sin[i]);
       *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
     }
+    return;
   }
-  if (!has_kv || !s_ok) return;
+  if (!s_ok) return;
 
-  // kv heads of this block: k in fp64 with one rounding to the cache dtype; v bit copy
-  const int j_begin = max(h_begin, p.h_q) - p.h_q;
-  const int j_end = h_end - p.h_q;
-  const T* k = static_cast<const T*>(p.k_new) + static_cast<long long>(b) * p.h_kv * D;
+  // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
   const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(b) * p.h_kv * D;
   T* kc = static_cast<T*>(p.k_cache) + s_row;
   T* vc = static_cast<T*>(p.v_cache) + s_row;
   const long long stride = s_stride;
-  const int n = (j_end - j_begin) * half;
-  for (int idx = threadIdx.x; idx < n; idx += kAppendThreads) {
-    const int h = j_begin + idx / half, i = idx % half;
-    const float2 x = Elem<T>::load2(k + h * D + 2 * i);
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int idx = u == 0 ? i0 : i1;
+    if (idx >= n_pairs) continue;
+    const float2 x = u == 0 ? x0 : x1;
+    const int h = h_begin + idx / half, i = idx % half;
     const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
     const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
     const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
@@ -174,7 +194,8 @@ KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.batch, (p.h_q + p.h_kv + kHeadsPerBlock - 1) / kHeadsPerBlock);
+  cfg.gridDim = dim3(p.batch, (p.h_q + kQHeadsPerBlock - 1) / kQHeadsPerBlock +
+                                  (p.h_kv + kKvHeadsPerBlock - 1) / kKvHeadsPerBlock);
   cfg.blockDim = dim3(kAppendThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

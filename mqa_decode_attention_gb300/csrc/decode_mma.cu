@@ -31,6 +31,7 @@
 #define MQA_MMA_STAGES_D64 4
 #endif
 
+
 namespace mqa {
 namespace {
 
@@ -49,12 +50,16 @@ struct MmaCfg {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
-// Shared-memory byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r
-// under the 128-byte swizzle TMA applied: chunk (c mod 8) of a 128-byte row
-// is stored at position (c mod 8) xor (r mod 8); D = 128 keeps its two
-// 64-column halves in separate spans.
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+// Shared-memory byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r.
+// A tile is stored as blocks of `1 << lg_rpb` rows (one TMA box: a page, or
+// the whole 64-row tile); inside a block each 64-column half is a span of
+// 128-byte rows, and TMA's 128-byte swizzle put chunk (c mod 8) of row r at
+// position (c mod 8) xor (r mod 8). Blocks and spans start on 1 KB
+// boundaries, so the 8 rows an ldmatrix reads land in 8 distinct bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c, int lg_rpb) {
+  const int blk = r >> lg_rpb, rin = r & ((1 << lg_rpb) - 1);
+  return ((blk * (D / 64) + (c >> 3)) << (lg_rpb + 7)) + rin * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 template <int D, int HB, int STAGES>
@@ -149,10 +154,15 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, C::kStageBytes);
           const int row = b * p.h_kv + j;
+          if (p.merged_halves) {  // one box: both halves of 64 rows
+            tma_load_4d(kdst, &tmap_k, 0, t0, 0, row, fb);
+            tma_load_4d(vdst, &tmap_v, 0, t0, 0, row, fb);
+          } else {
 #pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf) {
-            tma_load_3d(kdst + hf * C::kHalfBytes, &tmap_k, 64 * hf, t0, row, fb);
-            tma_load_3d(vdst + hf * C::kHalfBytes, &tmap_v, 64 * hf, t0, row, fb);
+            for (int hf = 0; hf < D / 64; ++hf) {
+              tma_load_3d(kdst + hf * C::kHalfBytes, &tmap_k, 64 * hf, t0, row, fb);
+              tma_load_3d(vdst + hf * C::kHalfBytes, &tmap_v, 64 * hf, t0, row, fb);
+            }
           }
         }
       } else {
@@ -182,10 +192,16 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
           for (int k = 0; k < kTile / 16; ++k) {
             if (k * rpc >= kTile) break;
             const int r = (t0 + k * rpc) % ps;
+            if (p.merged_halves) {  // one box per page: both halves of rpc rows
+              const uint32_t off = k * rpc * 128 * (D / 64);
+              tma_load_5d(kdst + off, &tmap_k, 0, r, 0, j, pg[k], fb);
+              tma_load_5d(vdst + off, &tmap_v, 0, r, 0, j, pg[k], fb);
+            } else {
 #pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf) {
-              tma_load_4d(kdst + hf * C::kHalfBytes + k * rpc * 128, &tmap_k, 64 * hf, r, j, pg[k], fb);
-              tma_load_4d(vdst + hf * C::kHalfBytes + k * rpc * 128, &tmap_v, 64 * hf, r, j, pg[k], fb);
+              for (int hf = 0; hf < D / 64; ++hf) {
+                tma_load_4d(kdst + hf * C::kHalfBytes + k * rpc * 128, &tmap_k, 64 * hf, r, j, pg[k], fb);
+                tma_load_4d(vdst + hf * C::kHalfBytes + k * rpc * 128, &tmap_v, 64 * hf, r, j, pg[k], fb);
+              }
             }
           }
         }
@@ -234,6 +250,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
 
   bool ok = true;
   const int trow0 = ws * 16;  // first tile row of this warp
+  // rows per TMA box in shared memory: a page when each box holds one page's
+  // two halves, else the whole tile
+  const int rpb = (p.paged && p.merged_halves && p.page_size < kTile) ? p.page_size : kTile;
+  const int lg_rpb = 31 - __clz(rpb);
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it % STAGES;
     if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
@@ -256,7 +276,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       for (int idx = lane; idx < (16 - first) * (D / 8); idx += 32) {
         const int r = trow0 + first + idx / (D / 8);
         const int c = idx % (D / 8);
-        *reinterpret_cast<uint4*>(vrow + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(vrow + swz<D>(r, c, lg_rpb)) = make_uint4(0u, 0u, 0u, 0u);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -274,7 +294,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
           const int row = trow0 + nt * 8 + (lane & 7);
           const int c = kk * 4 + (lane >> 3);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + swz(row, c), b0, b1, b2, b3);
+          ldsm_x4(kb + swz<D>(row, c, lg_rpb), b0, b1, b2, b3);
           mma_bf16_16816(s[nt], qa[2 * kk], b0, b1);
           mma_bf16_16816(s[nt], qa[2 * kk + 1], b2, b3);
         }
@@ -329,7 +349,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
         const int row = trow0 + ((lane >> 3) & 1) * 8 + (lane & 7);
         const int c = dn * 2 + (lane >> 4);
         uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vb + swz(row, c), v0, v1, v2, v3);
+        ldsm_x4_trans(vb + swz<D>(row, c, lg_rpb), v0, v1, v2, v3);
         mma_bf16_16816(o[2 * dn], pa, v0, v1);
         mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
       }

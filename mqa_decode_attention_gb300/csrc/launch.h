@@ -43,6 +43,7 @@ struct DecodeParams {
   int chunk;         // tokens per split, a multiple of kTile
   int head_blocks;   // blocks of query heads a (sequence, kv head) is cut into
   int early;         // 1: the preceding launch is the append kernel; stream K/V before waiting for it
+  int merged_halves; // tensor-core path: one TMA box carries both 64-column halves of a row block
   void* out;
   int out_dtype;
   float* lse_out;
