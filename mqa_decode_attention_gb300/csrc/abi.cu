@@ -152,7 +152,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // where the half dimension has the smaller stride (128 bytes) than the row
 // (256 bytes): one box then carries both halves of its rows and lands in
 // shared memory as two 64-column spans, so a tile needs half as many copies.
-bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool merged) {
+// `heads` > 1 (paged, merged only): a box also spans that many consecutive kv
+// heads of one page, which are contiguous in the pool.
+bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool merged, int heads = 1) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t D = L->head_dim;
@@ -184,7 +186,7 @@ bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool 
       dims[4] = static_cast<cuuint64_t>(L->num_pages);
       strides[2] = static_cast<cuuint64_t>(L->page_size) * row_bytes;
       strides[3] = static_cast<cuuint64_t>(L->h_kv) * L->page_size * row_bytes;
-      box[3] = 1;
+      box[3] = static_cast<cuuint32_t>(heads);
       box[4] = 1;
     }
   } else {
@@ -317,6 +319,17 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   cudaError_t e;
   if (v == MQA_VARIANT_TENSOR_CORE) {
     CUtensorMap tk, tv;
+    // Paged 16-token pages: blocks over groups of kv heads, one box per page
+    // and head group (long contiguous runs of the pool).
+    const int hg = decode_mma_heads_group(p);
+    if (hg > 0 && make_tensor_map(&tk, layout->k_cache, layout, true, hg) &&
+        make_tensor_map(&tv, layout->v_cache, layout, true, hg)) {
+      p.merged_halves = 1;
+      p.head_blocks = 1;
+      e = launch_decode_mma_heads(p, hg, tk, tv, s);
+      if (e != cudaSuccess) return fail_cuda(e);
+      goto combine;
+    }
     p.merged_halves = layout->head_dim == 128 && make_tensor_map(&tk, layout->k_cache, layout, true) &&
                       make_tensor_map(&tv, layout->v_cache, layout, true);
     if (!p.merged_halves &&
@@ -329,6 +342,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     e = launch_decode_fma(p, s);
   }
   if (e != cudaSuccess) return fail_cuda(e);
+combine:
   if (splits > 1) {
     CombineParams c;
     c.o_part = p.o_part;

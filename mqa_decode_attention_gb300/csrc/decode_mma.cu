@@ -22,6 +22,7 @@
 
 #include "../../include/mqa_decode.h"
 #include "launch.h"
+#include "mma_warp.cuh"
 #include "ptx.cuh"
 
 #ifndef MQA_MMA_STAGES_D128
@@ -49,18 +50,6 @@ struct MmaCfg {
   static constexpr int kSmemBytes = kBodyBytes + 2 * STAGES * 8 + 1024;  // + alignment slack
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
-
-// Shared-memory byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r.
-// A tile is stored as blocks of `1 << lg_rpb` rows (one TMA box: a page, or
-// the whole 64-row tile); inside a block each 64-column half is a span of
-// 128-byte rows, and TMA's 128-byte swizzle put chunk (c mod 8) of row r at
-// position (c mod 8) xor (r mod 8). Blocks and spans start on 1 KB
-// boundaries, so the 8 rows an ldmatrix reads land in 8 distinct bank groups.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c, int lg_rpb) {
-  const int blk = r >> lg_rpb, rin = r & ((1 << lg_rpb) - 1);
-  return ((blk * (D / 64) + (c >> 3)) << (lg_rpb + 7)) + rin * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
 
 template <int D, int HB, int STAGES>
 __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
@@ -220,33 +209,12 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   const int hb = warp >> 2;           // head block within this CTA
   const int ws = warp & 3;            // token slice of each tile
   const int head0 = (hsb * HB + hb) * 16;  // first head (within the group) of this warp's rows
-  const int rows_valid = G - head0;   // rows >= this are padding
   const int r0 = lane >> 2;           // fragment rows r0 and r0 + 8
   const int c2 = (lane & 3) * 2;      // fragment column pair
 
-  // Q as the A operand: rows = heads, k = head_dim, pre-scaled into the log2 domain
   if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
-  uint32_t qa[D / 16][4];
-  {
-    const float* q = p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
-    const float sc = p.scale_log2;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        const int row = r0 + ((part & 1) ? 8 : 0);
-        const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
-        float2 v = make_float2(0.f, 0.f);
-        if (row < rows_valid) v = *reinterpret_cast<const float2*>(q + row * D + col);
-        qa[ks][part] = pack_bf16x2(v.x * sc, v.y * sc);
-      }
-    }
-  }
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  WarpAttn<D> wa;
+  wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
 
   bool ok = true;
   const int trow0 = ws * 16;  // first tile row of this warp
@@ -264,105 +232,17 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       ok = false;
       break;
     }
-    const uint32_t kb = smem_u32(smem + stage * C::kStageBytes);
-    const uint32_t vb = kb + C::kTileBytes;
     const int n_valid = t_end - (t_begin + it * kTile + trow0);  // valid rows of this warp's 16
-
-    if (n_valid < 16) {
-      // Rows past the range may hold anything (even NaN bit patterns); zero
-      // their V so that P = 0 contributes exactly nothing.
-      const int first = n_valid < 0 ? 0 : n_valid;
-      unsigned char* vrow = smem + stage * C::kStageBytes + C::kTileBytes;
-      for (int idx = lane; idx < (16 - first) * (D / 8); idx += 32) {
-        const int r = trow0 + first + idx / (D / 8);
-        const int c = idx % (D / 8);
-        *reinterpret_cast<uint4*>(vrow + swz<D>(r, c, lg_rpb)) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-    }
-
     if (n_valid > 0) {
-      // ---- S = Q K^T over this warp's 16 tokens (two n8 tiles)
-      float s[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < D / 32; ++kk) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int row = trow0 + nt * 8 + (lane & 7);
-          const int c = kk * 4 + (lane >> 3);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + swz<D>(row, c, lg_rpb), b0, b1, b2, b3);
-          mma_bf16_16816(s[nt], qa[2 * kk], b0, b1);
-          mma_bf16_16816(s[nt], qa[2 * kk + 1], b2, b3);
-        }
-      }
-      // ---- mask, online softmax (rows r0 and r0 + 8)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if (nt * 8 + c2 + e >= n_valid) {
-            s[nt][e] = -INFINITY;
-            s[nt][2 + e] = -INFINITY;
-          }
-        }
-      }
-      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      // mn is finite: every warp slice with n_valid > 0 has at least one valid token
-      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float pr[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        pr[nt][0] = exp2f(s[nt][0] - mn0);
-        pr[nt][1] = exp2f(s[nt][1] - mn0);
-        pr[nt][2] = exp2f(s[nt][2] - mn1);
-        pr[nt][3] = exp2f(s[nt][3] - mn1);
-      }
-      l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-      l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= a0;
-        o[n][1] *= a0;
-        o[n][2] *= a1;
-        o[n][3] *= a1;
-      }
-      // ---- O += P V (P as the A operand straight from the S fragments)
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-      pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-      pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-      pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-#pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        const int row = trow0 + ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int c = dn * 2 + (lane >> 4);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vb + swz<D>(row, c, lg_rpb), v0, v1, v2, v3);
-        mma_bf16_16816(o[2 * dn], pa, v0, v1);
-        mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
-      }
+      unsigned char* ktile = smem + stage * C::kStageBytes;
+      wa.step(smem_u32(ktile), smem_u32(ktile + C::kTileBytes), ktile + C::kTileBytes, trow0,
+              n_valid < 16 ? n_valid : 16, lg_rpb, lane);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }
-
+  wa.finish_sums();
   // ------------------------------------------- merge the 4 token slices
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   named_bar_sync(1, C::kConsumerThreads);
   if (*reinterpret_cast<volatile int*>(&s_abort) || !ok) return;
   float* mo = reinterpret_cast<float*>(smem);            // [warps][16][stride]
@@ -372,14 +252,15 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     float* mine = mo + warp * 16 * C::kMergeStride;
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
-      *reinterpret_cast<float2*>(mine + r0 * C::kMergeStride + n * 8 + c2) = make_float2(o[n][0], o[n][1]);
-      *reinterpret_cast<float2*>(mine + (r0 + 8) * C::kMergeStride + n * 8 + c2) = make_float2(o[n][2], o[n][3]);
+      *reinterpret_cast<float2*>(mine + r0 * C::kMergeStride + n * 8 + c2) = make_float2(wa.o[n][0], wa.o[n][1]);
+      *reinterpret_cast<float2*>(mine + (r0 + 8) * C::kMergeStride + n * 8 + c2) =
+          make_float2(wa.o[n][2], wa.o[n][3]);
     }
     if ((lane & 3) == 0) {
-      mm[warp * 16 + r0] = m0;
-      mm[warp * 16 + r0 + 8] = m1;
-      ml[warp * 16 + r0] = l0;
-      ml[warp * 16 + r0 + 8] = l1;
+      mm[warp * 16 + r0] = wa.m0;
+      mm[warp * 16 + r0 + 8] = wa.m1;
+      ml[warp * 16 + r0] = wa.l0;
+      ml[warp * 16 + r0 + 8] = wa.l1;
     }
   }
   named_bar_sync(1, C::kConsumerThreads);

@@ -80,6 +80,13 @@ KernelShape decode_mma_shape(int head_dim, int group);
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                               cudaStream_t stream);
 
+// Paged 16-token pages, head_dim 128, G <= 16: kv heads per block of the
+// head-slice kernel (4 or 2), or 0 when it does not apply.
+int decode_mma_heads_group(const DecodeParams& p);
+KernelShape decode_mma_heads_shape(int heads_per_block);
+cudaError_t launch_decode_mma_heads(const DecodeParams& p, int heads_per_block, const CUtensorMap& tmap_k,
+                                    const CUtensorMap& tmap_v, cudaStream_t stream);
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 }  // namespace mqa

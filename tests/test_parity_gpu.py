@@ -116,8 +116,15 @@ def test_contiguous_matches_oracle(m, variant, shape, splits):
 
 @pytest.mark.parametrize("variant", ["tc", "cc"])
 @pytest.mark.parametrize("page_size", [16, 32, 64, 128])
-def test_paged_matches_oracle(m, variant, page_size):
-    w = workload("paged").with_(batch=5, h_q=16, h_kv=2, page_size=page_size, len_lo=1, len_hi=700, seed=9)
+@pytest.mark.parametrize("heads", [(16, 2), (32, 8), (12, 3), (64, 2)], ids=lambda h: f"q{h[0]}kv{h[1]}")
+def test_paged_matches_oracle(m, variant, page_size, heads):
+    """Covers the head-group paged kernel (16-token pages, kv heads in groups of
+    2 or 4, G <= 16) and the per-head kernel (other page sizes, odd kv head
+    counts, G > 16)."""
+    if heads != (16, 2) and page_size not in (16, 64):
+        pytest.skip("page-size sweep runs on the first head layout")
+    w = workload("paged").with_(batch=5, h_q=heads[0], h_kv=heads[1], page_size=page_size, len_lo=1, len_hi=700,
+                                seed=9)
     lens = torch.tensor([1, 16, 17, 700, 333], dtype=torch.int32)
     pc = make_paged_case(w, "cpu", seq_lens=lens, spare_pages=3)
     ref = oracle.decode_step_paged(pc.k_pool, pc.v_pool, pc.block_table, pc.q_new, pc.k_new, pc.v_new,
