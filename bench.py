@@ -44,7 +44,7 @@ METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 G
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "gqa4k"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_mma.cu", "ptx.cuh", "launch.h"]
+KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "mma_warp.cuh", "ptx.cuh", "launch.h"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -53,6 +53,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_gbs(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank streams its own batch's bytes each step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
 def measured_peak():
@@ -331,13 +348,8 @@ def bench_ours(args):
     if err_word != 0:
         raise RuntimeError(f"device error word {err_word:#x} after the timed steps")
 
-    max_ms = total_ms
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        max_ms = float(t.item())
-    ms_per_step = max_ms / K
-    value = world * sbytes / (ms_per_step * 1e-3) / 1e9
+    ms_per_step = max_over_ranks(total_ms, world) / K
+    value = throughput_gbs(world, sbytes, ms_per_step)
 
     # end to end: pinned host inputs copied in, output copied out, every step
     host_in = [x.cpu().pin_memory() for x in (case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens)]
@@ -363,17 +375,17 @@ def bench_ours(args):
         host_out.copy_(bufs.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * sbytes / (e2e_ms / K * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = throughput_gbs(world, sbytes, e2e_ms / K)
 
     peak, peak_src = measured_peak()
     achieved = abytes / (attn_ms * 1e-3) / 1e9
-    kernel_name = "decode_mma_kernel" if (variant in (0, 2) and w.dtype == "bf16") else "decode_fma_kernel"
-    traffic = ncu_traffic(args.workload) if kernel_name == "decode_mma_kernel" else None
+    if variant in (0, 2) and w.dtype == "bf16":
+        heads_kernel = w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
+        kernel_name = "decode_mma_heads_kernel" if heads_kernel else "decode_mma_kernel"
+    else:
+        kernel_name = "decode_fma_kernel"
+    traffic = ncu_traffic(args.workload) if kernel_name.startswith("decode_mma") else None
     clocks = sampler.summary(t_clock0, t_clock1)
 
     line = {
