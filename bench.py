@@ -298,7 +298,8 @@ def bench_ours(args):
         m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs, w.rope_base,
                       scale, w.num_splits, variant, stream)
 
-    launches_per_step = 2 + (1 if splits_used > 1 else 0)
+    fused = variant in (0, 2) and w.dtype == "bf16" and w.group <= 32  # append done inside the decode kernel
+    launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
     sampler = ClockSampler(gpu_index_for(local))
@@ -329,21 +330,30 @@ def bench_ours(args):
     t_clock1 = time.monotonic()
     total_ms = t_start.elapsed_time(t_end)
 
-    # per-kernel durations: K more steps as separate calls with an event
-    # around each launch (the fused call admits no event between its launches)
+    # per-launch durations: K more steps, an event on each side of every call.
+    # When the step is a single launch (tensor cores, no split) this is that
+    # kernel's own duration; with a split it also holds the combine.
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for i in range(K):
         ev_s[i].record(stream)
-        append()
-        ev_m[i].record(stream)
-        attend()
+        step()
         ev_e[i].record(stream)
     torch.cuda.synchronize()
     sampler.stop()
-    append_ms = statistics.fmean(ev_s[i].elapsed_time(ev_m[i]) for i in range(K))
-    attn_ms = statistics.fmean(ev_m[i].elapsed_time(ev_e[i]) for i in range(K))
+    step_call_ms = statistics.fmean(ev_s[i].elapsed_time(ev_e[i]) for i in range(K))
+    # the standalone calls, for reference (not part of the step)
+    n_alone = min(K, 500)
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(3 * n_alone)]
+    for i in range(n_alone):
+        ea[3 * i].record(stream)
+        append()
+        ea[3 * i + 1].record(stream)
+        attend()
+        ea[3 * i + 2].record(stream)
+    torch.cuda.synchronize()
+    append_ms = statistics.fmean(ea[3 * i].elapsed_time(ea[3 * i + 1]) for i in range(n_alone))
+    attn_ms = statistics.fmean(ea[3 * i + 1].elapsed_time(ea[3 * i + 2]) for i in range(n_alone))
     err_word = int(bufs.err.item())
     if err_word != 0:
         raise RuntimeError(f"device error word {err_word:#x} after the timed steps")
@@ -379,12 +389,26 @@ def bench_ours(args):
     e2e_value = throughput_gbs(world, sbytes, e2e_ms / K)
 
     peak, peak_src = measured_peak()
-    achieved = abytes / (attn_ms * 1e-3) / 1e9
     if variant in (0, 2) and w.dtype == "bf16":
         heads_kernel = w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
         kernel_name = "decode_mma_heads_kernel" if heads_kernel else "decode_mma_kernel"
     else:
         kernel_name = "decode_fma_kernel"
+    if fused and splits_used == 1:
+        # the step is this one launch: its average duration over the timed
+        # region is the step time, and it moves the whole step's bytes
+        roof_bytes, roof_ms = sbytes, ms_per_step
+        roof_kernel = kernel_name + " (append fused)"
+        roof_time = "timed region: K back-to-back launches of this kernel, CUDA events at both ends"
+    elif fused:
+        roof_bytes, roof_ms = sbytes, step_call_ms
+        roof_kernel = kernel_name + " (append fused) + combine_kernel"
+        roof_time = "events around each step call (decode + combine launches)"
+    else:
+        roof_bytes, roof_ms = abytes, attn_ms
+        roof_kernel = kernel_name + (" + combine_kernel" if splits_used > 1 else "")
+        roof_time = "events around each standalone gqa_decode_attention call"
+    achieved = roof_bytes / (roof_ms * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload) if kernel_name.startswith("decode_mma") else None
     clocks = sampler.summary(t_clock0, t_clock1)
 
@@ -414,17 +438,21 @@ def bench_ours(args):
             "l2": "inputs larger than L2 (no flush): %.0f MB streamed per step vs 129 MB L2" % (sbytes / 1e6),
             "parallelism": f"dp{world}" if world > 1 else "single",
         },
-        "kernels_ms": {"kv_append_rope": round(append_ms, 6), "gqa_decode_attention": round(attn_ms, 6),
-                       "how": "second pass of K steps, separate calls, CUDA events around each launch"},
+        "kernels_ms": {"mqa_decode_step": round(step_call_ms, 6),
+                       "standalone_kv_append_rope": round(append_ms, 6),
+                       "standalone_gqa_decode_attention": round(attn_ms, 6),
+                       "how": "CUDA events around each call on the launching stream, second pass of the same steps"},
         "roofline": {
             "bound": "hbm",
-            "kernel": kernel_name + (" + combine_kernel" if splits_used > 1 else ""),
+            "kernel": roof_kernel,
             "achieved": round(achieved, 2),
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": abytes,
+            "algorithmic_bytes_per_launch": roof_bytes,
+            "duration_ms": round(roof_ms, 6),
+            "duration_from": roof_time,
             "peak_source": peak_src,
             "frac_of_8000": round(achieved / 8000.0, 4),
         },

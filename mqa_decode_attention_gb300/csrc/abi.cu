@@ -216,8 +216,13 @@ bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool 
   return r == CUDA_SUCCESS;
 }
 
-mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
-                       const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word, mqa_stream_t stream) {
+void fill_theta(double* theta, int head_dim, double base) {
+  for (int i = 0; i < head_dim / 2; ++i)
+    theta[i] = std::pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(head_dim));
+}
+
+mqa_status check_append_args(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                             const int32_t* pos, double rope_base, const float* q_rot, const int32_t* err_word) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
   if (!q_new || !k_new || !v_new || !pos || !q_rot || !err_word) return MQA_ERR_INVALID_ARG;
@@ -225,6 +230,13 @@ mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const voi
       !aligned(pos, 4) || !aligned(err_word, 4))
     return MQA_ERR_INVALID_ARG;
   if (!(rope_base > 0.0) || !std::isfinite(rope_base)) return MQA_ERR_INVALID_ARG;
+  return MQA_OK;
+}
+
+mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                       const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word, mqa_stream_t stream) {
+  const mqa_status st = check_append_args(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word);
+  if (st != MQA_OK) return st;
   AppendParams p;
   std::memset(&p, 0, sizeof(p));
   p.batch = layout->batch;
@@ -246,18 +258,36 @@ mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const voi
   p.block_table = layout->block_table;
   p.q_rot = q_rot;
   p.err = err_word;
-  for (int i = 0; i < layout->head_dim / 2; ++i)
-    p.theta[i] = std::pow(rope_base, -2.0 * static_cast<double>(i) / static_cast<double>(layout->head_dim));
+  fill_theta(p.theta, layout->head_dim, rope_base);
   const cudaError_t e = launch_append_rope(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   const cudaError_t e2 = cudaGetLastError();
   return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
 }
 
+// The raw new-token query and its positions, when the attention launch
+// directly follows the append launch (fused step): the tensor-core kernels
+// then rotate q themselves instead of waiting for q_rot.
+struct RopeArgs {
+  const void* q_new;
+  const int32_t* pos;
+  double rope_base;
+  int fuse_append;  // 1: no append launch precedes; the decode kernel appends k_new / v_new itself
+  const void* k_new;
+  const void* v_new;
+  float* q_rot;
+};
+
+// The tensor-core kernels can take the append over when one block sees all
+// query heads of its kv head (G <= 32).
+bool fusable(const mqa_kv_layout* L, int variant) {
+  return variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16 && L->h_q / L->h_kv <= 32;
+}
+
 mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens, int32_t max_seq_len,
                           float scale, int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
                           void* workspace, size_t workspace_bytes, int32_t variant, int32_t* err_word,
-                          mqa_stream_t stream, int early) {
+                          mqa_stream_t stream, int early, const RopeArgs* rope) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
   if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
@@ -305,6 +335,19 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.chunk = chunk;
   p.head_blocks = head_blocks(layout, ks);
   p.early = early;
+  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE) {
+    p.rope_q = 1;
+    p.q_new = rope->q_new;
+    p.pos = rope->pos;
+    fill_theta(p.theta, layout->head_dim, rope->rope_base);
+    if (rope->fuse_append) {
+      p.fuse_append = 1;
+      p.early = 0;  // nothing of this step precedes the launch
+      p.k_new = rope->k_new;
+      p.v_new = rope->v_new;
+      p.q_rot_out = rope->q_rot;
+    }
+  }
   p.out = out;
   p.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
   p.lse_out = lse_out;
@@ -429,7 +472,7 @@ mqa_status gqa_decode_attention(const mqa_kv_layout* layout, const float* q_rot,
                                 int32_t out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
                                 int32_t variant, int32_t* err_word, mqa_stream_t stream) {
   return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out, workspace,
-                        workspace_bytes, variant, err_word, stream, /*early=*/0);
+                        workspace_bytes, variant, err_word, stream, /*early=*/0, /*rope=*/nullptr);
 }
 
 mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
@@ -453,10 +496,19 @@ mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const
     const size_t need = partial_bytes(layout, splits);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MQA_ERR_WORKSPACE;
   }
+  const mqa_status ca = check_append_args(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word);
+  if (ca != MQA_OK) return ca;
+  if (fusable(layout, v)) {
+    // one launch: the attention kernel appends the new token itself
+    const RopeArgs rope{q_new, pos, rope_base, 1, k_new, v_new, q_rot};
+    return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out,
+                          workspace, workspace_bytes, variant, err_word, stream, /*early=*/0, &rope);
+  }
   const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream);
   if (a != MQA_OK) return a;
+  const RopeArgs rope{q_new, pos, rope_base, 0, nullptr, nullptr, nullptr};
   return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out, workspace,
-                        workspace_bytes, variant, err_word, stream, /*early=*/1);
+                        workspace_bytes, variant, err_word, stream, /*early=*/1, &rope);
 }
 
 }  // extern "C"

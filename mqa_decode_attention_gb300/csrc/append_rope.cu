@@ -22,6 +22,7 @@
 #include "../../include/mqa_decode.h"
 #include "launch.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace mqa {
 namespace {
@@ -29,22 +30,6 @@ namespace {
 constexpr int kAppendThreads = 256;
 constexpr int kQHeadsPerBlock = 8;   // 8 heads x 64 pairs = 2 pairs per thread at d = 128
 constexpr int kKvHeadsPerBlock = 2;  // 2 heads x 64 pairs <= one pair per thread
-
-// 2 pi = kTwoPi1 + kTwoPi2 + kTwoPi3 (leading double, then the next two
-// 53-bit pieces of the remainder).
-constexpr double kTwoPi1 = 6.283185307179586232;
-constexpr double kTwoPi2 = 2.4492935982947063545e-16;
-constexpr double kTwoPi3 = -5.9895396194366793e-33;
-constexpr double kInvTwoPi = 0.15915494309189533577;
-
-// x - k 2 pi with k = nearest integer to x / (2 pi); |x| < 2^40 here.
-__device__ __forceinline__ double reduce_two_pi(double x) {
-  const double k = rint(x * kInvTwoPi);
-  double r = fma(-k, kTwoPi1, x);
-  r = fma(-k, kTwoPi2, r);
-  r = fma(-k, kTwoPi3, r);
-  return r;
-}
 
 template <typename T>
 struct Elem;
@@ -114,8 +99,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   if (i1 < n_pairs) x1 = Elem<T>::load2(src + (h_begin + i1 / half) * D + 2 * (i1 % half));
 
   if (threadIdx.x < half) {
-    double sn, cs;
-    sincos(reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]), &sn, &cs);
+    double cs, sn;
+    rope_cos_sin(pos, p.theta[threadIdx.x], &cs, &sn);
     s_cos[threadIdx.x] = cs;
     s_sin[threadIdx.x] = sn;
   }

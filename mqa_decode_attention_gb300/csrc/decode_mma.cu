@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     }
     int issued = 0;
     bool waited = !p.early;
+    const int apos = p.fuse_append ? p.pos[b] : 0;
+    const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos, p.chunk, S);
+    bool appended = !awaits;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
@@ -135,6 +138,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       if (!waited && L - 1 < t0 + kTile) {  // this tile holds the appended token
         grid_dependency_wait();
         waited = true;
+      }
+      if (!appended && apos < t0 + kTile) {  // this block wrote that row itself: wait for it
+        named_bar_sync(3, D / 2 + 32);
+        appended = true;
       }
       const uint32_t kdst = smem_u32(smem + stage * C::kStageBytes);
       const uint32_t vdst = kdst + C::kTileBytes;
@@ -198,6 +205,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       __syncwarp();
       issued = it + 1;
     }
+    if (!appended) named_bar_sync(3, D / 2 + 32);  // pair the writers' arrival
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
@@ -212,9 +220,20 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   const int r0 = lane >> 2;           // fragment rows r0 and r0 + 8
   const int c2 = (lane & 3) * 2;      // fragment column pair
 
-  if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
   WarpAttn<D> wa;
-  wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
+  if (p.rope_q) {
+    // rotate q_new here: nothing the consumers read comes from the append kernel
+    __shared__ float s_cs[D];
+    const int pos = p.pos[b];
+    const bool writer = p.fuse_append && hsb == 0 && split == append_split(pos, p.chunk, S);
+    rope_table<D>(s_cs, p, b, pos, threadIdx.x, 2, C::kConsumerThreads, j, writer ? 1 : 0, 3);
+    const long long qoff = (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
+    wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G - head0, s_cs, p.scale_log2, lane,
+                 (p.fuse_append && split == 0 && ws == 0) ? p.q_rot_out + qoff : nullptr);
+  } else {
+    if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
+    wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
+  }
 
   bool ok = true;
   const int trow0 = ws * 16;  // first tile row of this warp

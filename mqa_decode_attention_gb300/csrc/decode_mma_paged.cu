@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
     int wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
     int issued = 0;
     bool waited = !p.early;
+    const int apos = p.fuse_append ? p.pos[b] : 0;
+    bool appended = !(p.fuse_append && split == append_split(apos, p.chunk, S));
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
@@ -114,6 +116,10 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
       if (!waited && L - 1 < t0 + kPage) {  // this page holds the appended token
         grid_dependency_wait();
         waited = true;
+      }
+      if (!appended && apos < t0 + kPage) {  // this block wrote that row itself: wait for it
+        named_bar_sync(3, D / 2 + 32);
+        appended = true;
       }
       const int lp = t0 / kPage;  // < n_pages_seq since t0 < t_end <= L
       while (lp >= wbase + 32) {  // warp-uniform window advance
@@ -134,6 +140,7 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
       __syncwarp();
       issued = it + 1;
     }
+    if (!appended) named_bar_sync(3, D / 2 + 32);  // pair the writers' arrival
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
@@ -144,9 +151,20 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
   // -------------------------------------------------------------- consumers
   const int j = jg * HG + warp;  // this warp's kv head
   const int r0 = lane >> 2, c2 = (lane & 3) * 2;
-  if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
   WarpAttn<D> wa;
-  wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G) * D, G, p.scale_log2, lane);
+  if (p.rope_q) {
+    // rotate q_new here: nothing the consumers read comes from the append kernel
+    __shared__ float s_cs[D];
+    const int pos = p.pos[b];
+    const bool writer = p.fuse_append && split == append_split(pos, p.chunk, S);
+    rope_table<D>(s_cs, p, b, pos, threadIdx.x, 2, C::kConsumerWarps * 32, jg * HG, writer ? HG : 0, 3);
+    const long long qoff = (static_cast<long long>(b) * p.h_q + j * G) * D;
+    wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G, s_cs, p.scale_log2, lane,
+                 (p.fuse_append && split == 0) ? p.q_rot_out + qoff : nullptr);
+  } else {
+    if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
+    wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G) * D, G, p.scale_log2, lane);
+  }
 
   bool ok = true;
   for (int it = 0; it < n_tiles; ++it) {

@@ -44,6 +44,14 @@ struct DecodeParams {
   int head_blocks;   // blocks of query heads a (sequence, kv head) is cut into
   int early;         // 1: the preceding launch is the append kernel; stream K/V before waiting for it
   int merged_halves; // tensor-core path: one TMA box carries both 64-column halves of a row block
+  int rope_q;        // 1: rotate q_new (bf16) in the kernel instead of reading q_rot (fused step)
+  int fuse_append;   // 1: the kernel also performs the append of the new token (single-launch step)
+  const void* q_new;
+  const void* k_new;
+  const void* v_new;
+  float* q_rot_out;  // fused step: where the kernel stores RoPE(q_new)
+  const int32_t* pos;
+  double theta[kMaxHalfDim];  // RoPE inverse frequencies, used when rope_q
   void* out;
   int out_dtype;
   float* lse_out;

@@ -14,6 +14,7 @@
 
 #include "launch.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace mqa {
 
@@ -27,6 +28,83 @@ template <int D>
 __device__ __forceinline__ uint32_t swz(int r, int c, int lg_rpb) {
   const int blk = r >> lg_rpb, rin = r & ((1 << lg_rpb) - 1);
   return ((blk * (D / 64) + (c >> 3)) << (lg_rpb + 7)) + rin * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// Element offset of the cache row (sequence b, kv head j, token pos), or -1
+// (with the matching error bit when `report`) if pos or its page is out of
+// range. Same checks as the append kernel.
+__device__ __forceinline__ long long cache_row(const DecodeParams& p, int b, int j, int pos, bool report) {
+  if (!p.paged) {
+    if (pos < 0 || pos >= p.capacity) {
+      if (report) atomicOr(p.err, 0x1);  // MQA_DEVERR_POS_RANGE
+      return -1;
+    }
+    return ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + pos) * p.head_dim;
+  }
+  const int lp = pos >= 0 ? pos / p.page_size : -1;
+  if (pos < 0 || lp >= p.max_pages) {
+    if (report) atomicOr(p.err, 0x1);  // MQA_DEVERR_POS_RANGE
+    return -1;
+  }
+  const int page = p.block_table[static_cast<long long>(b) * p.max_pages + lp];
+  if (page < 0 || page >= p.num_pages) {
+    if (report) atomicOr(p.err, 0x2);  // MQA_DEVERR_PAGE_RANGE
+    return -1;
+  }
+  return ((static_cast<long long>(page) * p.h_kv + j) * p.page_size + pos % p.page_size) * p.head_dim;
+}
+
+// Split whose block performs the fused append of sequence b's new token:
+// the one whose token range holds pos, else split 0.
+__device__ __forceinline__ int append_split(int pos, int chunk, int splits) {
+  return (pos >= 0 && pos / chunk < splits) ? pos / chunk : 0;
+}
+
+// Fill cs[0 .. D/2) with cos and cs[D/2 .. D) with sin of pos * theta_i for
+// rotating the query in fp32: the angle is formed and reduced in fp64, then
+// its fp32 sine/cosine taken. Called by all `count` consumer threads; the
+// first D/2 compute. With `append_heads` > 0 those threads also perform the
+// append of the new token for kv heads j0 .. j0 + append_heads - 1 exactly as
+// the append kernel does (fp64 sine/cosine, k rotated in fp64 with
+// round-to-nearest products and one rounding to bf16; v copied), fence the
+// rows for the block's own TMA loads and signal the producer on named barrier
+// `append_bar` (D/2 + 32 threads).
+template <int D>
+__device__ __forceinline__ void rope_table(float* cs, const DecodeParams& p, int b, int pos, int tid, int bar,
+                                           int count, int j0, int append_heads, int append_bar) {
+  if (tid < D / 2) {
+    const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[tid]);
+    float sf, cf;
+    sincosf(static_cast<float>(ang), &sf, &cf);
+    cs[tid] = cf;
+    cs[D / 2 + tid] = sf;
+    if (append_heads > 0) {
+      double c, s;
+      sincos(ang, &s, &c);
+      for (int h = 0; h < append_heads; ++h) {
+        const int j = j0 + h;
+        const long long row = cache_row(p, b, j, pos, tid == 0 && h == 0);
+        if (row < 0) continue;
+        const long long src = (static_cast<long long>(b) * p.h_kv + j) * D + 2 * tid;
+        const uint32_t kraw = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
+        const double x = bf16lo_to_f32(kraw), y = bf16hi_to_f32(kraw);
+        const double xr = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
+        const double yr = __dadd_rn(__dmul_rn(x, s), __dmul_rn(y, c));
+        __nv_bfloat162 kv;
+        kv.x = __double2bfloat16(xr);
+        kv.y = __double2bfloat16(yr);
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + row + 2 * tid;
+        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + row + 2 * tid;
+        *reinterpret_cast<__nv_bfloat162*>(kc) = kv;
+        *reinterpret_cast<uint32_t*>(vc) =
+            *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
+      }
+      // the rows are read back by this block's TMA (async proxy)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      asm volatile("bar.arrive %0, %1;" ::"r"(append_bar), "r"(D / 2 + 32) : "memory");
+    }
+  }
+  named_bar_sync(bar, count);
 }
 
 template <int D>
@@ -142,6 +220,35 @@ struct WarpAttn {
       mma_bf16_16816(o[2 * dn], pa, v0, v1);
       mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
     }
+  }
+
+  // Same as init, but rotates the raw bf16 query q_new first: pair i of a row
+  // turns by the angle whose fp32 cosine / sine are cs[i] / cs[D/2 + i], as the
+  // append kernel does for q_rot.
+  __device__ __forceinline__ void init_rope(const __nv_bfloat16* q, int rows_valid, const float* cs,
+                                            float scale_log2, int lane, float* q_rot_out) {
+    const int r0 = lane >> 2, c2 = (lane & 3) * 2;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        const int row = r0 + ((part & 1) ? 8 : 0);
+        const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
+        float2 v = make_float2(0.f, 0.f);
+        if (row < rows_valid) {
+          const uint32_t raw = *reinterpret_cast<const uint32_t*>(q + row * D + col);
+          const float x = bf16lo_to_f32(raw), y = bf16hi_to_f32(raw);
+          const float c = cs[col >> 1], s = cs[D / 2 + (col >> 1)];
+          v = make_float2(x * c - y * s, x * s + y * c);
+          if (q_rot_out != nullptr) *reinterpret_cast<float2*>(q_rot_out + row * D + col) = v;
+        }
+        qa[ks][part] = pack_bf16x2(v.x * scale_log2, v.y * scale_log2);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
   }
 
   // Sum the lane-partial row sums over the 4 lanes that share a row.

@@ -393,6 +393,11 @@ def test_fused_step_equals_separate_calls(m, variant, paged):
                                    variant, bufs.err)
         torch.cuda.synchronize()
         assert int(bufs.err.item()) == 0
-        outs.append((bufs.out.clone(), bufs.lse.clone(), kc.clone(), vc.clone()))
-    for a, b in zip(outs[0], outs[1]):
-        assert torch.equal(a, b)
+        outs.append((bufs.out.clone(), bufs.lse.clone(), kc.clone(), vc.clone(), bufs.q_rot.clone()))
+    # the fused step appends and rotates q inside the tensor-core kernel (same
+    # formulas as the append kernel): the cache is bit-identical, q_rot and the
+    # outputs agree to fp32 / bf16 rounding
+    assert (outs[0][0].float() - outs[1][0].float()).abs().max().item() <= 1e-2
+    assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-3
+    assert torch.equal(outs[0][2], outs[1][2]) and torch.equal(outs[0][3], outs[1][3])
+    assert (outs[0][4] - outs[1][4]).abs().max().item() <= 1e-5 * (1 + outs[1][4].abs().max().item())
