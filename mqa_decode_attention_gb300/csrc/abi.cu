@@ -281,7 +281,8 @@ struct RopeArgs {
 // The tensor-core kernels can take the append over when one block sees all
 // query heads of its kv head (G <= 32).
 bool fusable(const mqa_kv_layout* L, int variant) {
-  return variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16 && L->h_q / L->h_kv <= 32;
+  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16) return false;
+  return head_blocks(L, decode_shape(L, variant)) == 1;
 }
 
 mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens, int32_t max_seq_len,

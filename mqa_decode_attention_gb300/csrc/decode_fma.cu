@@ -112,10 +112,10 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_splits;
   int cta = blockIdx.x;
-  const int split = cta % S;
-  cta /= S;
   const int hsb = cta % p.head_blocks;
   cta /= p.head_blocks;
+  const int split = cta % S;
+  cta /= S;
   const int j = cta % p.h_kv;
   const int b = cta / p.h_kv;
   const int G = p.group;

@@ -65,11 +65,13 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_splits;
+  // head blocks of one (sequence, kv head, split) are adjacent, so blocks that
+  // read the same K/V tiles run together and share them through L2
   int cta = blockIdx.x;
-  const int split = cta % S;
-  cta /= S;
   const int hsb = cta % p.head_blocks;
   cta /= p.head_blocks;
+  const int split = cta % S;
+  cta /= S;
   const int j = cta % p.h_kv;
   const int b = cta / p.h_kv;
   const int G = p.group;
@@ -346,7 +348,10 @@ cudaError_t launch_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUt
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-int mma_hb(int group) { return group > 16 ? 2 : 1; }
+#ifndef MQA_MMA_MAX_HB
+#define MQA_MMA_MAX_HB 2
+#endif
+int mma_hb(int group) { return (group > 16 && MQA_MMA_MAX_HB >= 2) ? 2 : 1; }
 
 }  // namespace
 

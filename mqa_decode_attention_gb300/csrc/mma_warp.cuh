@@ -150,10 +150,14 @@ struct WarpAttn {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
-    // ---- S = Q K^T over 16 tokens (two n8 tiles)
-    float s[2][4];
+    // ---- S = Q K^T over 16 tokens (two n8 tiles); even and odd k-steps
+    // accumulate separately so four independent MMA chains are in flight
+    float s[2][4], s2[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+    }
 #pragma unroll
     for (int kk = 0; kk < D / 32; ++kk) {
 #pragma unroll
@@ -163,8 +167,13 @@ struct WarpAttn {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + swz<D>(row, c, lg_rpb), b0, b1, b2, b3);
         mma_bf16_16816(s[nt], qa[2 * kk], b0, b1);
-        mma_bf16_16816(s[nt], qa[2 * kk + 1], b2, b3);
+        mma_bf16_16816(s2[nt], qa[2 * kk + 1], b2, b3);
       }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
     }
     // ---- mask, online softmax (rows r0 and r0 + 8)
 #pragma unroll
@@ -185,25 +194,29 @@ struct WarpAttn {
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     // mn is finite: at least one of the 16 tokens is valid
-    const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+    const bool moved = (mn0 != m0) || (mn1 != m1);
+    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
     m0 = mn0;
     m1 = mn1;
     float pr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = exp2f(s[nt][0] - mn0);
-      pr[nt][1] = exp2f(s[nt][1] - mn0);
-      pr[nt][2] = exp2f(s[nt][2] - mn1);
-      pr[nt][3] = exp2f(s[nt][3] - mn1);
+      pr[nt][0] = fast_exp2(s[nt][0] - mn0);
+      pr[nt][1] = fast_exp2(s[nt][1] - mn0);
+      pr[nt][2] = fast_exp2(s[nt][2] - mn1);
+      pr[nt][3] = fast_exp2(s[nt][3] - mn1);
     }
     l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
     l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+    // rescale the accumulators only when some row's running max moved
+    if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= a0;
-      o[n][1] *= a0;
-      o[n][2] *= a1;
-      o[n][3] *= a1;
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
     }
     // ---- O += P V
     uint32_t pa[4];
