@@ -105,22 +105,28 @@ def ncu_traffic(workload_name: str):
     return None
 
 
-def step_bytes(w, lens, out_esize):
-    """Algorithmic bytes of one step: every cached K/V byte read once (including
-    the new token), q_new read, out written, k_new/v_new read and their slot
-    written, and (paged) the block-table entries used."""
+def attended(lens, window: int):
+    """Tokens each sequence's query reads: all L, or the last `window`."""
+    return lens.clamp(max=window) if window > 0 else lens
+
+
+def step_bytes(w, lens, out_esize, window: int = 0):
+    """Algorithmic bytes of one step: every attended K/V byte read once
+    (including the new token), q_new read, out written, k_new/v_new read and
+    their slot written, and (paged) the block-table entries used."""
     es = w.esize
-    kv = 2 * int(lens.sum()) * w.h_kv * w.head_dim * es
+    kv = 2 * int(attended(lens, window).sum()) * w.h_kv * w.head_dim * es
     q = w.batch * w.h_q * w.head_dim * es
     out = w.batch * w.h_q * w.head_dim * out_esize
     append = 2 * 2 * w.batch * w.h_kv * w.head_dim * es
-    table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
+    table = 4 * int(((attended(lens, window) + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
     return kv + q + out + append + table
 
 
-def attention_bytes(w, lens, out_esize):
-    """Algorithmic bytes of one gqa_decode_attention launch: K/V of every token,
-    q_rot (fp32) read, out written, block-table entries (paged)."""
+def attention_bytes(w, lens, out_esize, window: int = 0):
+    """Algorithmic bytes of one gqa_decode_attention launch: K/V of every
+    attended token, q_rot (fp32) read, out written, block-table entries (paged)."""
+    lens = attended(lens, window)
     kv = 2 * int(lens.sum()) * w.h_kv * w.head_dim * w.esize
     q = w.batch * w.h_q * w.head_dim * 4
     out = w.batch * w.h_q * w.head_dim * out_esize
@@ -224,7 +230,7 @@ def unit_bytes(w, L, out_esize):
     return (2 * L * w.head_dim * es + w.group * w.head_dim * (es + out_esize) + 4 * w.head_dim * es)
 
 
-def run_oracle_units(w, inputs, budget_s: float, min_units: int = 2):
+def run_oracle_units(w, inputs, budget_s: float, min_units: int = 2, window: int = 0):
     """Time oracle.decode_unit over the units, cycling through them, until the
     budget is spent. Returns the first result of each unit and the totals."""
     import oracle  # test infrastructure: the CPU-baseline leg only
@@ -236,7 +242,8 @@ def run_oracle_units(w, inputs, budget_s: float, min_units: int = 2):
     i = 0
     while True:
         u = inputs[i % len(inputs)]
-        o, lse, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype)
+        o, lse, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype,
+                                       window=window)
         results.setdefault(i % len(inputs), (u, o))
         done += 1
         i += 1
@@ -267,16 +274,16 @@ def bench_ours(args):
     lens_cpu = case.seq_lens.cpu()
     max_len = int(lens_cpu.max())
     if w.paged:
-        lay = m.layout_paged(case.k_pool, case.v_pool, case.block_table, w.h_q)
+        lay = m.layout_paged(case.k_pool, case.v_pool, case.block_table, w.h_q, window=args.window)
     else:
-        lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q)
+        lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q, window=args.window)
     variant = args.variant
     bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=w.num_splits, variant=variant, device=dev)
     scale = 1.0 / math.sqrt(w.head_dim)
     splits_used = w.num_splits if w.num_splits > 0 else m.choose_splits(lay, max_len, variant)
     out_es = bufs.out.element_size()
-    sbytes = step_bytes(w, lens_cpu, out_es)
-    abytes = attention_bytes(w, lens_cpu, out_es)
+    sbytes = step_bytes(w, lens_cpu, out_es, args.window)
+    abytes = attention_bytes(w, lens_cpu, out_es, args.window)
     stream = torch.cuda.current_stream()
 
     # CPU-baseline units (rank 0, N = 1), copied before any step touches the cache
@@ -433,6 +440,7 @@ def bench_ours(args):
             "batch_per_gpu": w.batch,
             "tokens_per_step_per_gpu": int(lens_cpu.sum()),
             "num_splits": splits_used,
+            "window": args.window,
             "variant": {0: "auto", 1: "cuda_core", 2: "tensor_core"}[variant],
             "bytes_per_step_per_gpu": sbytes,
             "l2": "inputs larger than L2 (no flush): %.0f MB streamed per step vs 129 MB L2" % (sbytes / 1e6),
@@ -463,9 +471,10 @@ def bench_ours(args):
     }
 
     if do_cpu:
-        results, n_done, secs = run_oracle_units(w, units, args.cpu_seconds)
+        results, n_done, secs = run_oracle_units(w, units, args.cpu_seconds, window=args.window)
         by_unit = {(u["b"], u["j"]): u for u, _ in results}
-        done = sum(unit_bytes(w, units[i % len(units)]["L"], out_es) for i in range(n_done))
+        done = sum(unit_bytes(w, min(units[i % len(units)]["L"], args.window or 1 << 30), out_es)
+                   for i in range(n_done))
         out_host = bufs.out.float().cpu().numpy()
         G = w.group
         errs = [float(np.max(np.abs(out_host[u["b"], u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
@@ -544,6 +553,7 @@ def main():
     ap.add_argument("--warm-seconds", type=float, default=1.0,
                     help="minimum warm-up time, so the clock sampler sees the load (0 for profiler runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (smaller profiling cases)")
+    ap.add_argument("--window", type=int, default=0, help="sliding window: attend to the last W tokens (0 = all)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-units", type=int, default=0, help="distinct units in the CPU sample (0 = all)")
     args = ap.parse_args()

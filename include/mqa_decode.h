@@ -97,6 +97,12 @@ typedef enum mqa_variant {
  * cache_dtype applies to both caches and to q_new / k_new / v_new.
  * Requirements: h_q % h_kv == 0; head_dim in {64, 128}; batch >= 1;
  * page_size a power of two in [16, 256] (paged).
+ *
+ * window: 0 = the attention reads every cached token [0, L); W > 0 = a
+ * sliding window: only the last W tokens [max(0, L - W), L) are read
+ * ("KV Cache 최적화 심층 분석", SlidingWindowAttention keeps the cache's last
+ * window_size tokens). Rows and pages wholly before the window are never
+ * read, so a paged cache may release them (table entries -1).
  */
 typedef struct mqa_kv_layout {
   int32_t cache_dtype; /* mqa_dtype */
@@ -111,7 +117,7 @@ typedef struct mqa_kv_layout {
   int32_t page_size;
   int32_t num_pages;
   int32_t max_pages_per_seq;
-  int32_t reserved;
+  int32_t window; /* 0: full context; W > 0: sliding window of the last W tokens */
   const int32_t* block_table;
 } mqa_kv_layout;
 
@@ -142,7 +148,8 @@ MQA_API mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new
 /*
  * gqa_decode_attention -- step 3: for every sequence b and query head h,
  *   O[b, h, :] = sum_t softmax_t(scale * q_rot[b, h, :] . K[b, g(h), t, :]) V[b, g(h), t, :]
- * over tokens t in [0, seq_lens[b]), g(h) = floor(h / (h_q / h_kv)).
+ * over tokens t in [0, seq_lens[b]) (with layout->window = W > 0: t in
+ * [max(0, seq_lens[b] - W), seq_lens[b])), g(h) = floor(h / (h_q / h_kv)).
  * Each kernel block streams the K/V tiles of one (sequence, kv head) token
  * range from HBM once and serves all G query heads of the group from that
  * load, with an fp32 online softmax (FlashAttention's running max and sum,

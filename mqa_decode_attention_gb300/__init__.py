@@ -85,24 +85,27 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def layout_contiguous(k_cache: torch.Tensor, v_cache: torch.Tensor, h_q: int) -> KVLayout:
-    """Layout of a contiguous cache pair, each [batch, h_kv, capacity, head_dim]."""
+def layout_contiguous(k_cache: torch.Tensor, v_cache: torch.Tensor, h_q: int, window: int = 0) -> KVLayout:
+    """Layout of a contiguous cache pair, each [batch, h_kv, capacity, head_dim];
+    window > 0 restricts the attention to the last `window` tokens."""
     assert k_cache.shape == v_cache.shape and k_cache.dim() == 4
     assert k_cache.is_contiguous() and v_cache.is_contiguous()
     B, h_kv, cap, d = k_cache.shape
     return KVLayout(_dtype_code(k_cache.dtype), B, h_q, h_kv, d, 0, k_cache.data_ptr(), v_cache.data_ptr(), cap,
-                    0, 0, 0, 0, None)
+                    0, 0, 0, window, None)
 
 
-def layout_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor, h_q: int) -> KVLayout:
+def layout_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor, h_q: int,
+                 window: int = 0) -> KVLayout:
     """Layout of a paged pool pair, each [num_pages, h_kv, page_size, head_dim],
-    with an int32 block table [batch, max_pages_per_seq]."""
+    with an int32 block table [batch, max_pages_per_seq]; window > 0 restricts
+    the attention to the last `window` tokens."""
     assert k_pool.shape == v_pool.shape and k_pool.dim() == 4
     assert block_table.dtype == torch.int32 and block_table.is_contiguous()
     n, h_kv, ps, d = k_pool.shape
     B, mp = block_table.shape
     return KVLayout(_dtype_code(k_pool.dtype), B, h_q, h_kv, d, 1, k_pool.data_ptr(), v_pool.data_ptr(), 0, ps, n,
-                    mp, 0, block_table.data_ptr())
+                    mp, window, block_table.data_ptr())
 
 
 def kv_append_rope(layout: KVLayout, q_new, k_new, v_new, pos, rope_base: float, q_rot, err, stream=None) -> None:

@@ -48,7 +48,7 @@ class KVLayout(ctypes.Structure):
         ("page_size", c_i32),
         ("num_pages", c_i32),
         ("max_pages_per_seq", c_i32),
-        ("reserved", c_i32),
+        ("window", c_i32),
         ("block_table", c_vp),
     ]
 

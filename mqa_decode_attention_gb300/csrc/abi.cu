@@ -37,6 +37,7 @@ mqa_status check_layout(const mqa_kv_layout* L) {
   if (L->k_cache == nullptr || L->v_cache == nullptr) return MQA_ERR_INVALID_ARG;
   if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16)) return MQA_ERR_INVALID_ARG;
   if (L->paged != 0 && L->paged != 1) return MQA_ERR_INVALID_ARG;
+  if (L->window < 0) return MQA_ERR_INVALID_ARG;
   if (!L->paged) {
     if (L->capacity < 1 || L->capacity > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
   } else {
@@ -88,6 +89,13 @@ int head_blocks(const mqa_kv_layout* L, const KernelShape& ks) {
   return (G + ks.heads_per_cta - 1) / ks.heads_per_cta;
 }
 
+// Tokens one (sequence, kv head) may need read: the bound, or with a sliding
+// window W the window plus the alignment of its start down to a tile.
+int read_span(const mqa_kv_layout* L, int max_len) {
+  if (L->window > 0 && L->window + kTile < max_len) return L->window + kTile;
+  return max_len;
+}
+
 // Token-axis split count. Blocks of one (sequence, kv head) are independent,
 // so the only reasons to split are (a) too few units to fill the GPU in one
 // wave, and (b) device-side lengths that may vary up to max_seq_len, where
@@ -95,7 +103,8 @@ int head_blocks(const mqa_kv_layout* L, const KernelShape& ks) {
 // a single wave of equal blocks streams best (more, smaller blocks add
 // partial-output traffic and a second wave), and 4096-token chunks balance a
 // paged batch of lengths spread over [128, 16384].
-int choose_splits(const mqa_kv_layout* L, int max_len, int variant) {
+int choose_splits(const mqa_kv_layout* L, int max_len_in, int variant) {
+  const int max_len = read_span(L, max_len_in);
   int dev = 0;
   cudaGetDevice(&dev);
   const DeviceInfo di = device_info(dev);
@@ -109,7 +118,7 @@ int choose_splits(const mqa_kv_layout* L, int max_len, int variant) {
   const int tiles = (max_len + kTile - 1) / kTile;
   int s = 1;
   if (L->paged) {
-    const int chunk_tiles = 64;  // 4096 tokens
+    const int chunk_tiles = 65;  // 4096 tokens, plus one tile for a window's unaligned start
     s = (tiles + chunk_tiles - 1) / chunk_tiles;
   } else if (units < slots) {
     s = static_cast<int>(slots / units);  // at most one wave
@@ -304,7 +313,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
 
   const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
   int splits, chunk;
-  split_plan(req, max_seq_len, &splits, &chunk);
+  split_plan(req, read_span(layout, max_seq_len), &splits, &chunk);
   const size_t need = partial_bytes(layout, splits);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return MQA_ERR_WORKSPACE;
@@ -335,6 +344,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.num_splits = splits;
   p.chunk = chunk;
   p.head_blocks = head_blocks(layout, ks);
+  p.window = layout->window;
   p.early = early;
   if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE) {
     p.rope_q = 1;
@@ -440,7 +450,7 @@ size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int3
   const int v = resolve_variant(layout, variant);
   const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
   int splits, chunk;
-  split_plan(req, max_seq_len, &splits, &chunk);
+  split_plan(req, read_span(layout, max_seq_len), &splits, &chunk);
   return partial_bytes(layout, splits);
 }
 
@@ -493,7 +503,7 @@ mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const
   {
     const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
     int splits, chunk;
-    split_plan(req, max_seq_len, &splits, &chunk);
+    split_plan(req, read_span(layout, max_seq_len), &splits, &chunk);
     const size_t need = partial_bytes(layout, splits);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MQA_ERR_WORKSPACE;
   }

@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
     if (threadIdx.x == 0 && split == 0 && hsb == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
     L = L < 0 ? 0 : static_cast<int>(L > limit ? limit : L);
   }
-  const int t_begin = split * p.chunk;
+  // sliding window: tokens [t_lo, L); splits start at t_lo rounded down to a tile
+  const int t_lo = p.window > 0 ? max(0, L - p.window) : 0;
+  const int t_begin = (t_lo / kTile) * kTile + split * p.chunk;
   const int t_end = min(L, t_begin + p.chunk);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
 
@@ -155,6 +157,8 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
     PageWindow win;
     const int ps = p.page_size;
     if (p.paged) win.init(p.block_table + static_cast<long long>(b) * p.max_pages, (L + ps - 1) / ps, t_begin / ps, lane);
+    // (pages before the window are skipped below; the window may start past
+    //  t_begin, and win.page only moves forward)
     int issued = 0;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k) {
           pg[k] = -1;
-          if (k < pieces) {
+          if (k < pieces && t0 + (k + 1) * rpc > t_lo) {  // pieces wholly before the window are not read
             const int t = t0 + k * rpc;
             pg[k] = win.page(t / ps, lane);
             if (pg[k] < 0 || pg[k] >= p.num_pages) {
@@ -263,6 +267,7 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
     const unsigned char* ktile = smem + stage * C::kStageBytes;
     const unsigned char* vtile = ktile + C::kTileBytes;
     const int nrow = min(kTile, t_end - (t_begin + it * kTile));
+    const int lo_row = t_lo - (t_begin + it * kTile);  // rows before it are outside the window
 
     float s[C::kTPG][HBLK];
 #pragma unroll
@@ -289,7 +294,8 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
       for (int h = 0; h < HBLK; ++h) {
 #pragma unroll
         for (int off = 1; off < C::kLPT; off <<= 1) s[k][h] += __shfl_xor_sync(0xffffffffu, s[k][h], off);
-        if (gi + k * C::kGroups >= nrow) s[k][h] = -INFINITY;
+        const int row = gi + k * C::kGroups;
+        if (row >= nrow || row < lo_row) s[k][h] = -INFINITY;
       }
     }
     float base[HBLK];
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
 #pragma unroll
     for (int k = 0; k < C::kTPG; ++k) {
       const int row = gi + k * C::kGroups;
-      if (row < nrow) {
+      if (row < nrow && row >= lo_row) {
         float vv[C::kEPL];
 #pragma unroll
         for (int v = 0; v < C::kVPL; ++v) {

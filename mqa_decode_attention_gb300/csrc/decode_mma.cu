@@ -102,7 +102,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     if (threadIdx.x == 0 && split == 0 && hsb == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
     L = L < 0 ? 0 : static_cast<int>(L > limit ? limit : L);
   }
-  const int t_begin = split * p.chunk;
+  // sliding window: tokens [t_lo, L); splits start at t_lo rounded down to a tile
+  const int t_lo = p.window > 0 ? max(0, L - p.window) : 0;
+  const int t_base = (t_lo / kTile) * kTile;
+  const int t_begin = t_base + split * p.chunk;
   const int t_end = min(L, t_begin + p.chunk);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
 
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     int issued = 0;
     bool waited = !p.early;
     const int apos = p.fuse_append ? p.pos[b] : 0;
-    const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos, p.chunk, S);
+    const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos - t_base, p.chunk, S);
     bool appended = !awaits;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
           pg[k] = -1;
           if (k * rpc < kTile) {
             int lp = (t0 + k * rpc) / ps;
+            if (t0 + k * rpc + rpc <= t_lo) lp = t_lo / ps;  // wholly before the window: never read a released page
             if (lp >= n_pages_seq) lp = n_pages_seq - 1;
             while (lp >= wbase + 32) {  // warp-uniform window advance
               wbase += 32;
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     // rotate q_new here: nothing the consumers read comes from the append kernel
     __shared__ float s_cs[D];
     const int pos = p.pos[b];
-    const bool writer = p.fuse_append && hsb == 0 && split == append_split(pos, p.chunk, S);
+    const bool writer = p.fuse_append && hsb == 0 && split == append_split(pos - t_base, p.chunk, S);
     rope_table<D>(s_cs, p, b, pos, threadIdx.x, 2, C::kConsumerThreads, j, writer ? 1 : 0, 3);
     const long long qoff = (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
     wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G - head0, s_cs, p.scale_log2, lane,
@@ -253,11 +257,11 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       ok = false;
       break;
     }
-    const int n_valid = t_end - (t_begin + it * kTile + trow0);  // valid rows of this warp's 16
-    if (n_valid > 0) {
+    const int tt = t_begin + it * kTile + trow0;  // token of this warp's first row
+    const int lo = max(0, t_lo - tt), hi = min(16, t_end - tt);
+    if (lo < hi) {
       unsigned char* ktile = smem + stage * C::kStageBytes;
-      wa.step(smem_u32(ktile), smem_u32(ktile + C::kTileBytes), ktile + C::kTileBytes, trow0,
-              n_valid < 16 ? n_valid : 16, lg_rpb, lane);
+      wa.step(smem_u32(ktile), smem_u32(ktile + C::kTileBytes), ktile + C::kTileBytes, trow0, lo, hi, lg_rpb, lane);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));

@@ -85,7 +85,10 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
     if (threadIdx.x == 0 && split == 0 && jg == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
     L = L < 0 ? 0 : static_cast<int>(L > limit ? limit : L);
   }
-  const int t_begin = split * p.chunk;
+  // sliding window: tokens [t_lo, L); splits start at t_lo's page
+  const int t_lo = p.window > 0 ? max(0, L - p.window) : 0;
+  const int t_base = (t_lo / kPage) * kPage;
+  const int t_begin = t_base + split * p.chunk;
   const int t_end = min(L, t_begin + p.chunk);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kPage - 1) / kPage : 0;
 
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
     int issued = 0;
     bool waited = !p.early;
     const int apos = p.fuse_append ? p.pos[b] : 0;
-    bool appended = !(p.fuse_append && split == append_split(apos, p.chunk, S));
+    bool appended = !(p.fuse_append && split == append_split(apos - t_base, p.chunk, S));
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
     // rotate q_new here: nothing the consumers read comes from the append kernel
     __shared__ float s_cs[D];
     const int pos = p.pos[b];
-    const bool writer = p.fuse_append && split == append_split(pos, p.chunk, S);
+    const bool writer = p.fuse_append && split == append_split(pos - t_base, p.chunk, S);
     rope_table<D>(s_cs, p, b, pos, threadIdx.x, 2, C::kConsumerWarps * 32, jg * HG, writer ? HG : 0, 3);
     const long long qoff = (static_cast<long long>(b) * p.h_q + j * G) * D;
     wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G, s_cs, p.scale_log2, lane,
@@ -177,10 +180,11 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
       ok = false;
       break;
     }
-    const int n_valid = t_end - (t_begin + it * kPage);  // >= 1
+    const int t0 = t_begin + it * kPage;
+    const int lo = max(0, t_lo - t0), hi = min(kPage, t_end - t0);  // lo < hi: the page holds a window token
     unsigned char* kt = smem + stage * C::kStageBytes + warp * C::kHeadBytes;
     unsigned char* vt = kt + C::kBoxBytes;
-    wa.step(smem_u32(kt), smem_u32(vt), vt, 0, n_valid < kPage ? n_valid : kPage, 4, lane);
+    wa.step(smem_u32(kt), smem_u32(vt), vt, 0, lo, hi, 4, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }

@@ -42,6 +42,7 @@ struct DecodeParams {
   int num_splits;    // token-axis splits per (sequence, kv head); 1 = write `out` directly
   int chunk;         // tokens per split, a multiple of kTile
   int head_blocks;   // blocks of query heads a (sequence, kv head) is cut into
+  int window;        // 0: all tokens; W > 0: only tokens [max(0, L - W), L)
   int early;         // 1: the preceding launch is the append kernel; stream K/V before waiting for it
   int merged_halves; // tensor-core path: one TMA box carries both 64-column halves of a row block
   int rope_q;        // 1: rotate q_new (bf16) in the kernel instead of reading q_rot (fused step)

@@ -135,17 +135,20 @@ struct WarpAttn {
   }
 
   // Rows [trow0, trow0 + 16) of the K / V tiles at shared addresses kb / vb;
-  // only the first n_valid of them are real tokens (1 <= n_valid). vtile is the
-  // generic pointer of the V tile: rows past n_valid may hold anything (even
-  // NaN bit patterns) and are zeroed so that P = 0 contributes exactly nothing.
-  __device__ __forceinline__ void step(uint32_t kb, uint32_t vb, unsigned char* vtile, int trow0, int n_valid,
+  // only rows lo .. hi-1 of these 16 are real tokens (0 <= lo < hi <= 16).
+  // vtile is the generic pointer of the V tile: the other rows may hold
+  // anything (even NaN bit patterns) and are zeroed so that P = 0 contributes
+  // exactly nothing.
+  __device__ __forceinline__ void step(uint32_t kb, uint32_t vb, unsigned char* vtile, int trow0, int lo, int hi,
                                        int lg_rpb, int lane) {
     const int c2 = (lane & 3) * 2;
-    if (n_valid < 16) {
-      for (int idx = lane; idx < (16 - n_valid) * (D / 8); idx += 32) {
-        const int r = trow0 + n_valid + idx / (D / 8);
+    if (lo > 0 || hi < 16) {
+      const int n_bad = 16 - (hi - lo);
+      for (int idx = lane; idx < n_bad * (D / 8); idx += 32) {
+        int r = idx / (D / 8);
+        r = r < lo ? r : r + (hi - lo);  // rows [0, lo) then [hi, 16)
         const int c = idx % (D / 8);
-        *reinterpret_cast<uint4*>(vtile + swz<D>(r, c, lg_rpb)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(vtile + swz<D>(trow0 + r, c, lg_rpb)) = make_uint4(0u, 0u, 0u, 0u);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -180,7 +183,8 @@ struct WarpAttn {
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        if (nt * 8 + c2 + e >= n_valid) {
+        const int r = nt * 8 + c2 + e;
+        if (r < lo || r >= hi) {
           s[nt][e] = -INFINITY;
           s[nt][2 + e] = -INFINITY;
         }
@@ -193,7 +197,7 @@ struct WarpAttn {
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    // mn is finite: at least one of the 16 tokens is valid
+    // mn is finite: at least one of the 16 tokens is valid (lo < hi)
     const bool moved = (mn0 != m0) || (mn1 != m1);
     const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
     m0 = mn0;

@@ -30,6 +30,7 @@ from .decode import (
     round_to,
     run_cached_sequence,
     run_uncached_sequence,
+    window_start,
 )
 from .accounting import (
     kv_bytes_per_token,

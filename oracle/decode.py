@@ -182,6 +182,15 @@ def mqa_attention(q_rot, K1, V1, scale: float) -> np.ndarray:
     return w @ np.asarray(V1, F64)
 
 
+def window_start(length: int, window: int) -> int:
+    """First token a query at position length-1 attends to: 0 for full
+    attention (window 0), else max(0, length - window) -- the last `window`
+    cached tokens, its own included ("KV Cache 최적화 심층 분석",
+    SlidingWindowAttention: after the concatenation the cache keeps only its
+    last window_size tokens)."""
+    return 0 if window <= 0 else max(0, length - window)
+
+
 def attention_partial(q_rot, K, V, scale: float, t0: int, t1: int):
     """Attention restricted to tokens [t0, t1): normalised partial output and its
     log-sum-exp; an empty range gives output 0 and lse = -inf."""
@@ -239,7 +248,7 @@ def _f64(t) -> np.ndarray:
 
 
 def decode_step_contiguous(k_cache, v_cache, q_new, k_new, v_new, seq_lens, rope_base: float,
-                           scale: float, cache_dtype: str):
+                           scale: float, cache_dtype: str, window: int = 0):
     """One decode step over a contiguous cache [B, H_kv, capacity, d].
 
     For each sequence b with length L_b (after append), p = L_b - 1:
@@ -262,12 +271,13 @@ def decode_step_contiguous(k_cache, v_cache, q_new, k_new, v_new, seq_lens, rope
         q_rot[b] = rope_rotate(q_new[b], p, rope_base)
         k_stored = round_to(rope_rotate(k_new[b], p, rope_base), cache_dtype)
         append_contiguous(K, V, b, p, k_stored, v_new[b])
-        out[b], lse[b] = gqa_attention(q_rot[b], K[b, :, :L], V[b, :, :L], scale)
+        t0 = window_start(L, window)
+        out[b], lse[b] = gqa_attention(q_rot[b], K[b, :, t0:L], V[b, :, t0:L], scale)
     return {"out": out, "lse": lse, "q_rot": q_rot, "k_cache": K, "v_cache": V}
 
 
 def decode_step_paged(k_pool, v_pool, block_table, q_new, k_new, v_new, seq_lens, page_size: int,
-                      rope_base: float, scale: float, cache_dtype: str):
+                      rope_base: float, scale: float, cache_dtype: str, window: int = 0):
     """One decode step over a paged pool [num_pages, H_kv, page_size, d] with a
     block table [B, max_pages]; same steps as the contiguous form, with the slot
     of token p at (table[b][p // page_size], p % page_size)."""
@@ -286,14 +296,15 @@ def decode_step_paged(k_pool, v_pool, block_table, q_new, k_new, v_new, seq_lens
         q_rot[b] = rope_rotate(q_new[b], p, rope_base)
         k_stored = round_to(rope_rotate(k_new[b], p, rope_base), cache_dtype)
         append_paged(K, V, table[b], page_size, p, k_stored, v_new[b])
-        Kb = gather_paged(K, table[b], L, page_size)
-        Vb = gather_paged(V, table[b], L, page_size)
+        t0 = window_start(L, window)
+        Kb = gather_paged(K, table[b], L, page_size)[:, t0:]
+        Vb = gather_paged(V, table[b], L, page_size)[:, t0:]
         out[b], lse[b] = gqa_attention(q_rot[b], Kb, Vb, scale)
     return {"out": out, "lse": lse, "q_rot": q_rot, "k_pool": K, "v_pool": V}
 
 
 def decode_unit(q_group, k_row, v_row, K_unit, V_unit, seq_len: int, rope_base: float, scale: float,
-                cache_dtype: str):
+                cache_dtype: str, window: int = 0):
     """The decode step for ONE (sequence, KV head) unit, for sampled checks at
     full size: q_group [G, d] are the query heads of the group, k_row / v_row
     [d] the new token's key / value for this KV head, K_unit / V_unit [>= L, d]
@@ -307,7 +318,8 @@ def decode_unit(q_group, k_row, v_row, K_unit, V_unit, seq_len: int, rope_base: 
     V = _f64(V_unit)[:L].copy()
     K[p] = k_stored
     V[p] = _f64(v_row)
-    out, lse = gqa_attention(q_rot, K[None], V[None], scale)
+    t0 = window_start(L, window)
+    out, lse = gqa_attention(q_rot, K[None, t0:], V[None, t0:], scale)
     return out, lse, k_stored
 
 

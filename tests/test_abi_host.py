@@ -18,7 +18,7 @@ def lib(built_lib):
 
 def _layout(**kw):
     base = dict(cache_dtype=_abi.MQA_BF16, batch=2, h_q=8, h_kv=2, head_dim=128, paged=0, k_cache=FAKE,
-                v_cache=FAKE + 4096, capacity=256, page_size=0, num_pages=0, max_pages_per_seq=0, reserved=0,
+                v_cache=FAKE + 4096, capacity=256, page_size=0, num_pages=0, max_pages_per_seq=0, window=0,
                 block_table=None)
     base.update(kw)
     return _abi.KVLayout(**base)
@@ -80,6 +80,7 @@ def test_attention_rejects_bad_arguments(lib):
     assert _attn(lib, lay, out_dtype=5) == _abi.MQA_ERR_UNSUPPORTED
     assert _attn(lib, lay, variant=9) == _abi.MQA_ERR_INVALID_ARG
     assert _attn(lib, lay, out=None) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, _layout(window=-1)) == _abi.MQA_ERR_INVALID_ARG
     assert _attn(lib, lay, err=None) == _abi.MQA_ERR_INVALID_ARG
     # tensor cores need a bf16 cache
     assert _attn(lib, _layout(cache_dtype=_abi.MQA_F32), variant=_abi.MQA_VARIANT_TENSOR_CORE) == \

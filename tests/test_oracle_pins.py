@@ -430,3 +430,50 @@ def test_planted_mistakes_are_caught():
 
     assert _fails(check_round_bf16, round_truncating)
     assert _fails(check_round_bf16, round_half_up)
+
+
+# ------------------------------------------------------- sliding window
+def test_sliding_window_decode_pins():
+    """Sliding-window decode (youngju.dev SlidingWindowAttention: the cache keeps
+    its last window_size tokens): window 1 attends to the new token alone, a
+    window >= L is full attention, and every step of a sequence equals the last
+    row of causal attention under a band mask (keys j with i - W < j <= i),
+    computed by the library routine SDPA with an explicit boolean mask."""
+    rng = np.random.default_rng(21)
+    B, h_q, h_kv, d, cap = 2, 8, 2, 32, 50
+    K = rng.standard_normal((B, h_kv, cap, d))
+    V = rng.standard_normal((B, h_kv, cap, d))
+    q, k, v = rng.standard_normal((B, h_q, d)), rng.standard_normal((B, h_kv, d)), rng.standard_normal((B, h_kv, d))
+    lens = np.array([50, 7])
+    one = oracle.decode_step_contiguous(K, V, q, k, v, lens, 10000.0, 0.2, "f64", window=1)
+    assert np.array_equal(one["out"], np.repeat(v, h_q // h_kv, axis=1))
+    full = oracle.decode_step_contiguous(K, V, q, k, v, lens, 10000.0, 0.2, "f64")
+    wide = oracle.decode_step_contiguous(K, V, q, k, v, lens, 10000.0, 0.2, "f64", window=64)
+    assert np.array_equal(full["out"], wide["out"])
+    assert oracle.window_start(10, 0) == 0 and oracle.window_start(10, 4) == 6 and oracle.window_start(3, 4) == 0
+
+    # band-masked causal attention over a whole sequence, every row
+    n, W = 23, 5
+    Qs = rng.standard_normal((h_q, n, d))
+    Ks = rng.standard_normal((h_kv, n, d))
+    Vs = rng.standard_normal((h_kv, n, d))
+    i = np.arange(n)[:, None]
+    jj = np.arange(n)[None, :]
+    band = torch.from_numpy((jj <= i) & (jj > i - W))
+    ref = F.scaled_dot_product_attention(torch.from_numpy(Qs)[None], torch.from_numpy(Ks)[None],
+                                         torch.from_numpy(Vs)[None], attn_mask=band, scale=0.3,
+                                         enable_gqa=True)[0].numpy()
+    for row in range(n):
+        t0 = oracle.window_start(row + 1, W)
+        o, _ = oracle.gqa_attention(Qs[:, row], Ks[:, t0:row + 1], Vs[:, t0:row + 1], 0.3)
+        assert np.allclose(o, ref[:, row], atol=1e-12)
+
+    # paged with a window equals contiguous with the same window
+    Kc = oracle.round_bf16(rng.standard_normal((B, h_kv, 64, d)))
+    Vc = oracle.round_bf16(rng.standard_normal((B, h_kv, 64, d)))
+    lens = np.array([64, 40])
+    rc = oracle.decode_step_contiguous(Kc, Vc, q, k, v, lens, 10000.0, 0.2, "bf16", window=19)
+    pk, table = _contiguous_to_paged(Kc, lens, 16, np.random.default_rng(5))
+    pv, _ = _contiguous_to_paged(Vc, lens, 16, np.random.default_rng(5))
+    rp = oracle.decode_step_paged(pk, pv, table, q, k, v, lens, 16, 10000.0, 0.2, "bf16", window=19)
+    assert np.array_equal(rp["out"], rc["out"])

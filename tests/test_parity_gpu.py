@@ -401,3 +401,77 @@ def test_fused_step_equals_separate_calls(m, variant, paged):
     assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-3
     assert torch.equal(outs[0][2], outs[1][2]) and torch.equal(outs[0][3], outs[1][3])
     assert (outs[0][4] - outs[1][4]).abs().max().item() <= 1e-5 * (1 + outs[1][4].abs().max().item())
+
+
+# ---------------------------------------------------------- sliding window
+@pytest.mark.parametrize("variant", [2, 1])
+@pytest.mark.parametrize("window", [1, 7, 16, 17, 100, 1000])
+def test_sliding_window_contiguous(m, variant, window):
+    w = workload("gqa4k").with_(batch=3, h_q=16, h_kv=4, seed=61)
+    lens = torch.tensor([700, 65, 3], dtype=torch.int32)
+    c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=704)
+    ref = oracle.decode_step_contiguous(c.k_cache, c.v_cache, c.q_new, c.k_new, c.v_new, c.seq_lens, w.rope_base,
+                                        1.0 / math.sqrt(w.head_dim), "bf16", window=window)
+    for splits in (1, 3, 0):
+        kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+        lay = m.layout_contiguous(kc, vc, w.h_q, window=window)
+        bufs = m.DecodeBuffers.allocate(lay, 700, num_splits=splits, variant=variant, device=DEV)
+        m.decode_step(lay, c.q_new.to(DEV), c.k_new.to(DEV), c.v_new.to(DEV), c.pos.to(DEV), c.seq_lens.to(DEV),
+                      700, bufs, w.rope_base, 1.0 / math.sqrt(w.head_dim), num_splits=splits, variant=variant)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        assert np.max(np.abs(_np(bufs.out) - ref["out"])) <= BF16_TOL, (splits, window)
+        assert np.max(np.abs(_np(bufs.lse) - ref["lse"])) <= BF16_TOL
+
+
+@pytest.mark.parametrize("variant", [2, 1])
+@pytest.mark.parametrize("h_kv", [4, 3])
+@pytest.mark.parametrize("window", [1, 15, 16, 33, 300])
+def test_sliding_window_paged_with_released_pages(m, variant, h_kv, window):
+    """Pages wholly before the window are released (table entry -1): no error,
+    and the result equals the oracle's windowed attention."""
+    w = workload("paged").with_(batch=4, h_q=4 * h_kv, h_kv=h_kv, seed=62)
+    lens = torch.tensor([700, 64, 17, 1], dtype=torch.int32)
+    pc = make_paged_case(w, "cpu", seq_lens=lens)
+    ref = oracle.decode_step_paged(pc.k_pool, pc.v_pool, pc.block_table, pc.q_new, pc.k_new, pc.v_new, pc.seq_lens,
+                                   pc.page_size, w.rope_base, 1.0 / math.sqrt(w.head_dim), "bf16", window=window)
+    table = pc.block_table.clone()
+    for b in range(w.batch):
+        t_lo = max(0, int(lens[b]) - window)
+        table[b, :t_lo // pc.page_size] = -1
+    for splits in (1, 3, 0):
+        kp, vp, bt = pc.k_pool.to(DEV), pc.v_pool.to(DEV), table.to(DEV)
+        lay = m.layout_paged(kp, vp, bt, w.h_q, window=window)
+        bufs = m.DecodeBuffers.allocate(lay, 700, num_splits=splits, variant=variant, device=DEV)
+        m.decode_step(lay, pc.q_new.to(DEV), pc.k_new.to(DEV), pc.v_new.to(DEV), pc.pos.to(DEV),
+                      pc.seq_lens.to(DEV), 700, bufs, w.rope_base, 1.0 / math.sqrt(w.head_dim), num_splits=splits,
+                      variant=variant)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0, (splits, int(bufs.err.item()))
+        assert np.max(np.abs(_np(bufs.out) - ref["out"])) <= BF16_TOL, (splits, window)
+
+
+def test_sliding_window_full_size_long(m):
+    """131072-token sequences with a 4096-token window (Mistral's W): sampled
+    units against the oracle."""
+    w = workload("long")
+    W = 4096
+    c = make_contiguous_case(w, DEV)
+    L = w.seq_len
+    G = w.group
+    units = [(0, 0), (3, 7), (2, 4)]
+    saved = {(b, j): (c.k_cache[b, j, L - W:L].cpu(), c.v_cache[b, j, L - W:L].cpu()) for b, j in units}
+    lay = m.layout_contiguous(c.k_cache, c.v_cache, w.h_q, window=W)
+    bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, device=DEV)
+    m.decode_step(lay, c.q_new, c.k_new, c.v_new, c.pos, c.seq_lens, L, bufs, w.rope_base,
+                  1.0 / math.sqrt(w.head_dim), num_splits=0)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    q_new, k_new, v_new = c.q_new.cpu(), c.k_new.cpu(), c.v_new.cpu()
+    for (b, j), (Ku, Vu) in saved.items():
+        # the unit seen from the window's start: positions keep their absolute values
+        ro, rl, _ = oracle.decode_unit(q_new[b, j * G:(j + 1) * G], k_new[b, j], v_new[b, j],
+                                       torch.cat([torch.zeros(L - W, w.head_dim, dtype=Ku.dtype), Ku]),
+                                       torch.cat([torch.zeros(L - W, w.head_dim, dtype=Vu.dtype), Vu]), L,
+                                       w.rope_base, 1.0 / math.sqrt(w.head_dim), "bf16", window=W)
+        assert np.max(np.abs(_np(bufs.out[b, j * G:(j + 1) * G]) - ro)) <= BF16_TOL
