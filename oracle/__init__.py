@@ -17,6 +17,9 @@ from .decode import (
     causal_attention,
     decode_step_contiguous,
     decode_step_paged,
+    decode_step_u8,
+    dequantize_u8,
+    quantize_u8,
     decode_unit,
     gather_paged,
     gqa_attention,

@@ -79,6 +79,30 @@ def round_to(x, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
+# --------------------------------------------------------- uint8 KV cache
+def quantize_u8(x):
+    """Asymmetric uint8 quantisation of each row of the last axis, the pages'
+    QuantizedKVCache ("KV Cache 최적화 심층 분석", youngju.dev):
+    scale = (max - min) / 255, zero_point = round(-min / scale) clamped to
+    [0, 255], code = round(x / scale + zero_point) clamped to [0, 255] (round
+    half to even, as torch.round). Reading: the arithmetic is float32, in that
+    operation order, and a constant row (max == min) takes scale 1.
+    Returns (codes uint8 [..., d], scale float32 [...], zero_point float32 [...])."""
+    x = np.asarray(x, dtype=np.float32)
+    mn = x.min(axis=-1)
+    mx = x.max(axis=-1)
+    scale = ((mx - mn) / np.float32(255.0)).astype(np.float32)
+    scale = np.where(scale == 0, np.float32(1.0), scale).astype(np.float32)
+    zp = np.clip(np.rint((-mn) / scale), 0, 255).astype(np.float32)
+    codes = np.clip(np.rint(x / scale[..., None] + zp[..., None]), 0, 255).astype(np.uint8)
+    return codes, scale, zp
+
+
+def dequantize_u8(codes, scale, zp):
+    """(code - zero_point) * scale, exactly (float64)."""
+    return (np.asarray(codes, F64) - np.asarray(zp, F64)[..., None]) * np.asarray(scale, F64)[..., None]
+
+
 # -------------------------------------------------------------------- RoPE
 def rope_inv_freq(head_dim: int, base: float) -> np.ndarray:
     """theta_i = base^(-2i/d), i = 0 .. d/2-1 (reading; the pages give no formula)."""
@@ -301,6 +325,51 @@ def decode_step_paged(k_pool, v_pool, block_table, q_new, k_new, v_new, seq_lens
         Vb = gather_paged(V, table[b], L, page_size)[:, t0:]
         out[b], lse[b] = gqa_attention(q_rot[b], Kb, Vb, scale)
     return {"out": out, "lse": lse, "q_rot": q_rot, "k_pool": K, "v_pool": V}
+
+
+def decode_step_u8(k_codes, k_sz, v_codes, v_sz, q_new, k_new, v_new, seq_lens, rope_base: float, scale: float,
+                   block_table=None, page_size: int = 0, window: int = 0):
+    """One decode step over a uint8 cache (contiguous [B, H_kv, capacity, d]
+    codes with (scale, zero_point) pairs [B, H_kv, capacity, 2], or paged
+    [num_pages, H_kv, page_size, d] with a block table). The new token's key
+    is rotated in fp64, rounded to fp32 and quantised; its value (bf16 input)
+    is quantised; the attention reads the dequantised cache.
+    Returns dict(out, lse, q_rot, k_codes, k_sz, v_codes, v_sz) with updated copies."""
+    Kc, Vc = np.array(k_codes, copy=True), np.array(v_codes, copy=True)
+    Ks, Vs = np.array(k_sz, dtype=np.float32, copy=True), np.array(v_sz, dtype=np.float32, copy=True)
+    q_new, k_new, v_new = _f64(q_new), _f64(k_new), _f64(v_new)
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    table = None if block_table is None else np.asarray(_f64(block_table), dtype=np.int64)
+    B, h_q, d = q_new.shape
+    out = np.empty((B, h_q, d), F64)
+    lse = np.empty((B, h_q), F64)
+    q_rot = np.empty((B, h_q, d), F64)
+    for b in range(B):
+        L = int(lens[b])
+        p = L - 1
+        q_rot[b] = rope_rotate(q_new[b], p, rope_base)
+        kq, ks, kz = quantize_u8(rope_rotate(k_new[b], p, rope_base))
+        vq, vs, vz = quantize_u8(v_new[b])
+        if table is None:
+            Kc[b, :, p], Vc[b, :, p] = kq, vq
+            Ks[b, :, p] = np.stack([ks, kz], -1)
+            Vs[b, :, p] = np.stack([vs, vz], -1)
+            Kd = dequantize_u8(Kc[b, :, :L], Ks[b, :, :L, 0], Ks[b, :, :L, 1])
+            Vd = dequantize_u8(Vc[b, :, :L], Vs[b, :, :L, 0], Vs[b, :, :L, 1])
+        else:
+            page, off = page_slot(table[b], p, page_size)
+            Kc[page, :, off], Vc[page, :, off] = kq, vq
+            Ks[page, :, off] = np.stack([ks, kz], -1)
+            Vs[page, :, off] = np.stack([vs, vz], -1)
+            kcode = gather_paged(Kc, table[b], L, page_size)
+            vcode = gather_paged(Vc, table[b], L, page_size)
+            ksz = gather_paged(Ks, table[b], L, page_size)
+            vsz = gather_paged(Vs, table[b], L, page_size)
+            Kd = dequantize_u8(kcode, ksz[..., 0], ksz[..., 1])
+            Vd = dequantize_u8(vcode, vsz[..., 0], vsz[..., 1])
+        t0 = window_start(L, window)
+        out[b], lse[b] = gqa_attention(q_rot[b], Kd[:, t0:], Vd[:, t0:], scale)
+    return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "k_sz": Ks, "v_codes": Vc, "v_sz": Vs}
 
 
 def decode_unit(q_group, k_row, v_row, K_unit, V_unit, seq_len: int, rope_base: float, scale: float,

@@ -11,7 +11,9 @@ from .generate import (
     ContiguousCase,
     PagedCase,
     TinySequence,
+    U8Cache,
     make_contiguous_case,
+    make_u8_cache,
     make_paged_case,
     make_tiny_sequence,
     normal,
@@ -25,7 +27,9 @@ __all__ = [
     "ContiguousCase",
     "PagedCase",
     "TinySequence",
+    "U8Cache",
     "make_contiguous_case",
+    "make_u8_cache",
     "make_paged_case",
     "make_tiny_sequence",
     "normal",

@@ -140,3 +140,33 @@ def make_tiny_sequence(w: Workload, prompt_len: int | None = None, decode_evals:
     k = normal((n, w.batch, w.h_kv, w.head_dim), w.seed, S_K, w.dtype)
     v = normal((n, w.batch, w.h_kv, w.head_dim), w.seed, S_V, w.dtype)
     return TinySequence(q, k, v, p, t)
+
+
+@dataclass
+class U8Cache:
+    """A uint8 cache drawn directly: codes uniform on [0, 255], scale and
+    zero point as a quantised N(0,1) row would have them (scale about
+    6 / 255, zero point about 128), one pair per (token, kv head)."""
+
+    k_codes: torch.Tensor
+    k_sz: torch.Tensor  # float32 [..., 2] (scale, zero_point)
+    v_codes: torch.Tensor
+    v_sz: torch.Tensor
+
+
+S_KQ, S_VQ, S_KS, S_VS = 8, 9, 10, 11
+
+
+def make_u8_cache(shape_rows, head_dim: int, seed: int, device="cpu") -> U8Cache:
+    """shape_rows: the leading shape of the cache rows ([B, H_kv, capacity] or
+    [num_pages, H_kv, page_size])."""
+    out = []
+    for sc, ss in ((S_KQ, S_KS), (S_VQ, S_VS)):
+        g = _generator(seed, sc, device)
+        codes = torch.randint(0, 256, tuple(shape_rows) + (head_dim,), generator=g, device=device,
+                              dtype=torch.int32).to(torch.uint8)
+        g2 = _generator(seed, ss, device)
+        scale = (5.0 + 2.0 * torch.rand(tuple(shape_rows), generator=g2, device=device)) / 255.0
+        zp = torch.randint(100, 156, tuple(shape_rows), generator=g2, device=device).to(torch.float32)
+        out += [codes, torch.stack([scale.to(torch.float32), zp], dim=-1).contiguous()]
+    return U8Cache(*out)

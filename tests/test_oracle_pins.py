@@ -477,3 +477,65 @@ def test_sliding_window_decode_pins():
     pv, _ = _contiguous_to_paged(Vc, lens, 16, np.random.default_rng(5))
     rp = oracle.decode_step_paged(pk, pv, table, q, k, v, lens, 16, 10000.0, 0.2, "bf16", window=19)
     assert np.array_equal(rp["out"], rc["out"])
+
+
+# ---------------------------------------------------------- uint8 cache
+def test_u8_quantisation_pins():
+    """QuantizedKVCache (youngju.dev): codes in [0, 255]; the round trip is
+    within half a step (scale / 2) of the input; values already on the grid
+    come back exactly; the row min and max land on codes 0 and 255 when the
+    zero point needs no clamping; a constant row takes scale 1."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((50, 128)).astype(np.float32) * rng.uniform(0.1, 10, (50, 1)).astype(np.float32)
+    codes, scale, zp = oracle.quantize_u8(x)
+    assert codes.dtype == np.uint8 and scale.dtype == np.float32
+    back = oracle.dequantize_u8(codes, scale, zp)
+    assert np.all(np.abs(back - x) <= scale[:, None].astype(np.float64) * (0.5 + 1e-5) + 1e-7)
+    # grid values survive exactly
+    s = np.float32(0.03125)
+    grid = ((rng.integers(0, 256, (4, 64)) - 100) * s).astype(np.float32)
+    grid[:, 0] = -100 * s
+    grid[:, 1] = 155 * s
+    c2, s2, z2 = oracle.quantize_u8(grid)
+    assert np.all(s2 == s) and np.all(z2 == 100)
+    assert np.array_equal(oracle.dequantize_u8(c2, s2, z2), grid.astype(np.float64))
+    assert np.all(c2[:, 0] == 0) and np.all(c2[:, 1] == 255)
+    # constant row
+    c3, s3, z3 = oracle.quantize_u8(np.full((1, 8), 0.5, np.float32))
+    assert s3[0] == 1.0 and np.all(oracle.dequantize_u8(c3, s3, z3) == 0.0)
+
+
+def test_u8_decode_step_pins():
+    """The uint8 step equals the bf16-free definition: attention over the
+    dequantised cache, with the new token quantised by quantize_u8; paged
+    equals contiguous on the same logical data."""
+    rng = np.random.default_rng(32)
+    B, h_q, h_kv, d, cap = 2, 8, 2, 64, 48
+    kc = rng.integers(0, 256, (B, h_kv, cap, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, (B, h_kv, cap, d)).astype(np.uint8)
+    ks = np.stack([rng.uniform(0.01, 0.03, (B, h_kv, cap)), rng.integers(100, 156, (B, h_kv, cap))], -1)
+    vs = np.stack([rng.uniform(0.01, 0.03, (B, h_kv, cap)), rng.integers(100, 156, (B, h_kv, cap))], -1)
+    ks, vs = ks.astype(np.float32), vs.astype(np.float32)
+    q = oracle.round_bf16(rng.standard_normal((B, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    lens = np.array([48, 20])
+    r = oracle.decode_step_u8(kc, ks, vc, vs, q, k, v, lens, 10000.0, 0.125)
+    for b in range(B):
+        L = int(lens[b])
+        Kd = oracle.dequantize_u8(r["k_codes"][b, :, :L], r["k_sz"][b, :, :L, 0], r["k_sz"][b, :, :L, 1])
+        Vd = oracle.dequantize_u8(r["v_codes"][b, :, :L], r["v_sz"][b, :, :L, 0], r["v_sz"][b, :, :L, 1])
+        out, _ = oracle.gqa_attention(oracle.rope_rotate(q[b], L - 1, 10000.0), Kd, Vd, 0.125)
+        assert np.array_equal(out, r["out"][b])
+        kq, kss, kz = oracle.quantize_u8(oracle.rope_rotate(k[b], L - 1, 10000.0))
+        assert np.array_equal(r["k_codes"][b, :, L - 1], kq)
+        # only the new slot changed
+        assert np.array_equal(np.delete(r["k_codes"][b], L - 1, axis=1), np.delete(kc[b], L - 1, axis=1))
+    # paged == contiguous
+    pk, table = _contiguous_to_paged(kc, lens, 16, np.random.default_rng(2))
+    pv, _ = _contiguous_to_paged(vc, lens, 16, np.random.default_rng(2))
+    pks, _ = _contiguous_to_paged(ks, lens, 16, np.random.default_rng(2))
+    pvs, _ = _contiguous_to_paged(vs, lens, 16, np.random.default_rng(2))
+    rp = oracle.decode_step_u8(pk.astype(np.uint8), pks, pv.astype(np.uint8), pvs, q, k, v, lens, 10000.0, 0.125,
+                               block_table=table, page_size=16)
+    assert np.array_equal(rp["out"], r["out"])
