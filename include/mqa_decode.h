@@ -67,7 +67,11 @@ typedef enum mqa_status {
   MQA_ERR_WORKSPACE = 4    /* workspace missing or smaller than needed */
 } mqa_status;
 
-typedef enum mqa_dtype { MQA_BF16 = 0, MQA_F32 = 1 } mqa_dtype;
+typedef enum mqa_dtype {
+  MQA_BF16 = 0,
+  MQA_F32 = 1,
+  MQA_U8 = 2 /* cache only: uint8 codes + (scale, zero point) per cached (token, kv head); q/k/v new in bf16 */
+} mqa_dtype;
 
 /* Which decode-attention kernel to run (gqa_decode_attention `variant`). */
 typedef enum mqa_variant {
@@ -81,6 +85,7 @@ typedef enum mqa_variant {
 #define MQA_DEVERR_PAGE_RANGE 0x2u /* a block-table entry in use lies outside [0, num_pages) */
 #define MQA_DEVERR_SEQ_LEN 0x4u    /* seq_len < 1, > capacity, > max_seq_len or past the block table */
 #define MQA_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel ran out (the result is invalid) */
+#define MQA_DEVERR_U8_SCALE 0x10u  /* MQA_U8: a V scale above 1023 was read; those output rows are invalid */
 
 /*
  * Where the KV cache of one layer lives.
@@ -97,6 +102,18 @@ typedef enum mqa_variant {
  * cache_dtype applies to both caches and to q_new / k_new / v_new.
  * Requirements: h_q % h_kv == 0; head_dim in {64, 128}; batch >= 1;
  * page_size a power of two in [16, 256] (paged).
+ *
+ * MQA_U8 cache ("KV Cache 최적화 심층 분석", QuantizedKVCache): each cached
+ * (token, kv head) row of head_dim values is stored as uint8 codes with a
+ * float32 (scale, zero_point) pair in k_scale_zero / v_scale_zero
+ * ([batch, h_kv, capacity, 2] contiguous, [num_pages, h_kv, page_size, 2]
+ * paged); the value is (code - zero_point) * scale. kv_append_rope quantises
+ * the new row: scale = (max - min) / 255 (1 if max == min), zero_point =
+ * round(-min / scale) clamped to [0, 255], code = round(x / scale +
+ * zero_point) clamped to [0, 255], in float32, rounding half to even; the
+ * key is quantised after its fp64 rotation, rounded to float32. q_new,
+ * k_new and v_new are bf16. Attention over a MQA_U8 cache runs on tensor
+ * cores only.
  *
  * window: 0 = the attention reads every cached token [0, L); W > 0 = a
  * sliding window: only the last W tokens [max(0, L - W), L) are read
@@ -119,6 +136,8 @@ typedef struct mqa_kv_layout {
   int32_t max_pages_per_seq;
   int32_t window; /* 0: full context; W > 0: sliding window of the last W tokens */
   const int32_t* block_table;
+  void* k_scale_zero; /* MQA_U8 only: float32 (scale, zero_point) per cached row of K */
+  void* v_scale_zero; /* MQA_U8 only: same for V */
 } mqa_kv_layout;
 
 /*

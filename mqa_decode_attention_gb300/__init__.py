@@ -24,7 +24,9 @@ from ._abi import (
     MQA_DEVERR_POS_RANGE,
     MQA_DEVERR_SEQ_LEN,
     MQA_DEVERR_TIMEOUT,
+    MQA_DEVERR_U8_SCALE,
     MQA_F32,
+    MQA_U8,
     MQA_VARIANT_AUTO,
     MQA_VARIANT_CUDA_CORE,
     MQA_VARIANT_TENSOR_CORE,
@@ -50,6 +52,8 @@ __all__ = [
     "MQA_DEVERR_PAGE_RANGE",
     "MQA_DEVERR_SEQ_LEN",
     "MQA_DEVERR_TIMEOUT",
+    "MQA_DEVERR_U8_SCALE",
+    "MQA_U8",
 ]
 
 
@@ -72,6 +76,8 @@ def _dtype_code(dt: torch.dtype) -> int:
         return MQA_BF16
     if dt == torch.float32:
         return MQA_F32
+    if dt == torch.uint8:
+        return MQA_U8
     raise TypeError(f"unsupported dtype {dt}")
 
 
@@ -85,19 +91,24 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def layout_contiguous(k_cache: torch.Tensor, v_cache: torch.Tensor, h_q: int, window: int = 0) -> KVLayout:
-    """Layout of a contiguous cache pair, each [batch, h_kv, capacity, head_dim];
-    window > 0 restricts the attention to the last `window` tokens."""
+def layout_contiguous(k_cache: torch.Tensor, v_cache: torch.Tensor, h_q: int, window: int = 0,
+                      k_scale_zero: torch.Tensor | None = None, v_scale_zero: torch.Tensor | None = None) -> KVLayout:
+    """Layout of a contiguous cache pair, each [batch, h_kv, capacity, head_dim]
+    (bf16, fp32, or uint8 codes with float32 [batch, h_kv, capacity, 2] scale /
+    zero-point pairs); window > 0 restricts the attention to the last `window`
+    tokens."""
     assert k_cache.shape == v_cache.shape and k_cache.dim() == 4
     assert k_cache.is_contiguous() and v_cache.is_contiguous()
     B, h_kv, cap, d = k_cache.shape
     return KVLayout(_dtype_code(k_cache.dtype), B, h_q, h_kv, d, 0, k_cache.data_ptr(), v_cache.data_ptr(), cap,
-                    0, 0, 0, window, None)
+                    0, 0, 0, window, None, _ptr(k_scale_zero), _ptr(v_scale_zero))
 
 
 def layout_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor, h_q: int,
-                 window: int = 0) -> KVLayout:
-    """Layout of a paged pool pair, each [num_pages, h_kv, page_size, head_dim],
+                 window: int = 0, k_scale_zero: torch.Tensor | None = None,
+                 v_scale_zero: torch.Tensor | None = None) -> KVLayout:
+    """Layout of a paged pool pair, each [num_pages, h_kv, page_size, head_dim]
+    (uint8 pools take [num_pages, h_kv, page_size, 2] scale / zero-point pairs),
     with an int32 block table [batch, max_pages_per_seq]; window > 0 restricts
     the attention to the last `window` tokens."""
     assert k_pool.shape == v_pool.shape and k_pool.dim() == 4
@@ -105,7 +116,7 @@ def layout_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.
     n, h_kv, ps, d = k_pool.shape
     B, mp = block_table.shape
     return KVLayout(_dtype_code(k_pool.dtype), B, h_q, h_kv, d, 1, k_pool.data_ptr(), v_pool.data_ptr(), 0, ps, n,
-                    mp, window, block_table.data_ptr())
+                    mp, window, block_table.data_ptr(), _ptr(k_scale_zero), _ptr(v_scale_zero))
 
 
 def kv_append_rope(layout: KVLayout, q_new, k_new, v_new, pos, rope_base: float, q_rot, err, stream=None) -> None:
@@ -159,7 +170,7 @@ class DecodeBuffers:
                  out_dtype: torch.dtype | None = None, device="cuda") -> "DecodeBuffers":
         B, hq, d = layout.batch, layout.h_q, layout.head_dim
         if out_dtype is None:
-            out_dtype = torch.bfloat16 if layout.cache_dtype == MQA_BF16 else torch.float32
+            out_dtype = torch.float32 if layout.cache_dtype == MQA_F32 else torch.bfloat16
         ws = workspace_size(layout, max_seq_len, num_splits, variant)
         return DecodeBuffers(
             q_rot=torch.empty(B, hq, d, dtype=torch.float32, device=device),

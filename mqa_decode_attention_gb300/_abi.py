@@ -18,6 +18,7 @@ MQA_ERR_WORKSPACE = 4
 
 MQA_BF16 = 0
 MQA_F32 = 1
+MQA_U8 = 2
 
 MQA_VARIANT_AUTO = 0
 MQA_VARIANT_CUDA_CORE = 1
@@ -27,6 +28,7 @@ MQA_DEVERR_POS_RANGE = 0x1
 MQA_DEVERR_PAGE_RANGE = 0x2
 MQA_DEVERR_SEQ_LEN = 0x4
 MQA_DEVERR_TIMEOUT = 0x8
+MQA_DEVERR_U8_SCALE = 0x10
 
 c_i32 = ctypes.c_int32
 c_vp = ctypes.c_void_p
@@ -50,6 +52,8 @@ class KVLayout(ctypes.Structure):
         ("max_pages_per_seq", c_i32),
         ("window", c_i32),
         ("block_table", c_vp),
+        ("k_scale_zero", c_vp),
+        ("v_scale_zero", c_vp),
     ]
 
 

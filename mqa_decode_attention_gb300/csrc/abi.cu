@@ -31,7 +31,14 @@ bool is_pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
 
 mqa_status check_layout(const mqa_kv_layout* L) {
   if (L == nullptr) return MQA_ERR_INVALID_ARG;
-  if (L->cache_dtype != MQA_BF16 && L->cache_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  if (L->cache_dtype != MQA_BF16 && L->cache_dtype != MQA_F32 && L->cache_dtype != MQA_U8)
+    return MQA_ERR_UNSUPPORTED;
+  if (L->cache_dtype == MQA_U8) {
+    if (L->k_scale_zero == nullptr || L->v_scale_zero == nullptr) return MQA_ERR_INVALID_ARG;
+    if (!aligned(L->k_scale_zero, 16) || !aligned(L->v_scale_zero, 16)) return MQA_ERR_INVALID_ARG;
+    // the (scale, zero) rows of a kv head are copied by TMA: 16-byte strides
+    if (!L->paged && L->capacity % 2 != 0) return MQA_ERR_UNSUPPORTED;
+  }
   if (L->batch < 1 || L->h_q < 1 || L->h_kv < 1 || L->h_q % L->h_kv != 0) return MQA_ERR_INVALID_ARG;
   if (L->head_dim != 64 && L->head_dim != 128) return MQA_ERR_UNSUPPORTED;
   if (L->k_cache == nullptr || L->v_cache == nullptr) return MQA_ERR_INVALID_ARG;
@@ -54,8 +61,19 @@ long long token_limit(const mqa_kv_layout* L) {
 }
 
 int resolve_variant(const mqa_kv_layout* L, int variant) {
-  if (variant == MQA_VARIANT_AUTO) return L->cache_dtype == MQA_BF16 ? MQA_VARIANT_TENSOR_CORE : MQA_VARIANT_CUDA_CORE;
+  if (variant == MQA_VARIANT_AUTO) return L->cache_dtype == MQA_F32 ? MQA_VARIANT_CUDA_CORE : MQA_VARIANT_TENSOR_CORE;
   return variant;
+}
+
+// Which cache dtypes a kernel family reads: tensor cores bf16 and uint8,
+// CUDA cores bf16 and fp32.
+bool variant_supports(int variant, int cache_dtype) {
+  if (variant == MQA_VARIANT_TENSOR_CORE) return cache_dtype == MQA_BF16 || cache_dtype == MQA_U8;
+  return cache_dtype == MQA_BF16 || cache_dtype == MQA_F32;
+}
+
+int dtype_code(int cache_dtype) {
+  return cache_dtype == MQA_BF16 ? kDtypeBf16 : (cache_dtype == MQA_F32 ? kDtypeF32 : kDtypeU8);
 }
 
 struct DeviceInfo {
@@ -80,6 +98,7 @@ DeviceInfo device_info(int dev) {
 
 KernelShape decode_shape(const mqa_kv_layout* L, int variant) {
   const int G = L->h_q / L->h_kv;
+  if (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_U8) return decode_u8_shape(L->head_dim, G);
   if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
 }
@@ -225,6 +244,78 @@ bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool 
   return r == CUDA_SUCCESS;
 }
 
+// TMA descriptors of a uint8 cache: maps[0], maps[1] the K / V codes (boxes
+// of head_dim x `rows` rows x `heads` kv heads; 128-byte swizzle for 128-byte
+// rows, 64-byte swizzle for 64-byte rows), maps[2], maps[3] their (scale,
+// zero) rows as float32 runs of 2 x `rows` values per head. `heads` > 1 only
+// for paged pools, where the heads of one page are consecutive.
+bool make_u8_maps(CUtensorMap* maps, const mqa_kv_layout* L, int rows_in, int heads) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t D = L->head_dim;
+  const cuuint32_t rows = static_cast<cuuint32_t>(rows_in);
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  void* codes[2] = {L->k_cache, L->v_cache};
+  void* sz[2] = {L->k_scale_zero, L->v_scale_zero};
+  for (int i = 0; i < 2; ++i) {
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    cuuint32_t rank;
+    dims[0] = D;
+    box[0] = static_cast<cuuint32_t>(D);
+    box[1] = rows;
+    strides[0] = D;
+    if (!L->paged) {
+      rank = 3;
+      dims[1] = static_cast<cuuint64_t>(L->capacity);
+      dims[2] = static_cast<cuuint64_t>(L->batch) * L->h_kv;
+      strides[1] = static_cast<cuuint64_t>(L->capacity) * D;
+      box[2] = 1;
+    } else {
+      rank = 4;
+      dims[1] = static_cast<cuuint64_t>(L->page_size);
+      dims[2] = static_cast<cuuint64_t>(L->h_kv);
+      dims[3] = static_cast<cuuint64_t>(L->num_pages);
+      strides[1] = static_cast<cuuint64_t>(L->page_size) * D;
+      strides[2] = static_cast<cuuint64_t>(L->h_kv) * L->page_size * D;
+      box[2] = static_cast<cuuint32_t>(heads);
+      box[3] = 1;
+    }
+    if (fn(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, codes[i], dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  for (int i = 0; i < 2; ++i) {
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    cuuint32_t rank;
+    box[0] = 2 * rows;
+    if (!L->paged) {
+      rank = 2;
+      dims[0] = 2 * static_cast<cuuint64_t>(L->capacity);
+      dims[1] = static_cast<cuuint64_t>(L->batch) * L->h_kv;
+      strides[0] = 2 * static_cast<cuuint64_t>(L->capacity) * 4;
+      box[1] = 1;
+    } else {
+      rank = 3;
+      dims[0] = 2 * static_cast<cuuint64_t>(L->page_size);
+      dims[1] = static_cast<cuuint64_t>(L->h_kv);
+      dims[2] = static_cast<cuuint64_t>(L->num_pages);
+      strides[0] = 2 * static_cast<cuuint64_t>(L->page_size) * 4;
+      strides[1] = static_cast<cuuint64_t>(L->h_kv) * strides[0];
+      box[1] = static_cast<cuuint32_t>(heads);
+      box[2] = 1;
+    }
+    if (fn(&maps[2 + i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, sz[i], dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 void fill_theta(double* theta, int head_dim, double base) {
   for (int i = 0; i < head_dim / 2; ++i)
     theta[i] = std::pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(head_dim));
@@ -252,8 +343,10 @@ mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const voi
   p.h_q = layout->h_q;
   p.h_kv = layout->h_kv;
   p.head_dim = layout->head_dim;
-  p.cache_dtype = layout->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.cache_dtype = dtype_code(layout->cache_dtype);
   p.paged = layout->paged;
+  p.k_sz = static_cast<float2*>(layout->k_scale_zero);
+  p.v_sz = static_cast<float2*>(layout->v_scale_zero);
   p.q_new = q_new;
   p.k_new = k_new;
   p.v_new = v_new;
@@ -309,7 +402,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return MQA_ERR_INVALID_ARG;
   const int v = resolve_variant(layout, variant);
-  if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype != MQA_BF16) return MQA_ERR_UNSUPPORTED;
+  if (!variant_supports(v, layout->cache_dtype)) return MQA_ERR_UNSUPPORTED;
 
   const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
   int splits, chunk;
@@ -328,9 +421,11 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.h_kv = layout->h_kv;
   p.group = layout->h_q / layout->h_kv;
   p.head_dim = layout->head_dim;
-  p.cache_dtype = layout->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.cache_dtype = dtype_code(layout->cache_dtype);
   p.paged = layout->paged;
   p.k_cache = layout->k_cache;
+  p.k_sz = static_cast<const float2*>(layout->k_scale_zero);
+  p.v_sz = static_cast<const float2*>(layout->v_scale_zero);
   p.v_cache = layout->v_cache;
   p.capacity = layout->capacity;
   p.page_size = layout->page_size;
@@ -346,7 +441,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.head_blocks = head_blocks(layout, ks);
   p.window = layout->window;
   p.early = early;
-  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE) {
+  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_BF16) {
     p.rope_q = 1;
     p.q_new = rope->q_new;
     p.pos = rope->pos;
@@ -371,7 +466,18 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   }
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (v == MQA_VARIANT_TENSOR_CORE) {
+  if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_U8) {
+    CUtensorMap maps[4];
+    // Paged 16- / 32-token pages: blocks over groups of kv heads, one box per
+    // page and head group (long contiguous runs of the pool).
+    const int hg = decode_u8_heads_group(p);
+    const int rows = hg > 0 ? layout->page_size : (layout->paged && layout->page_size < kTile ? layout->page_size : kTile);
+    if (!make_u8_maps(maps, layout, rows, hg > 0 ? hg : 1)) {
+      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+      return MQA_ERR_CUDA;
+    }
+    e = hg > 0 ? launch_decode_u8_heads(p, hg, maps, s) : launch_decode_u8(p, maps, s);
+  } else if (v == MQA_VARIANT_TENSOR_CORE) {
     CUtensorMap tk, tv;
     // Paged 16-token pages: blocks over groups of kv heads, one box per page
     // and head group (long contiguous runs of the pool).
@@ -499,7 +605,7 @@ mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const
     return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   const int v = resolve_variant(layout, variant);
-  if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype != MQA_BF16) return MQA_ERR_UNSUPPORTED;
+  if (!variant_supports(v, layout->cache_dtype)) return MQA_ERR_UNSUPPORTED;
   {
     const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
     int splits, chunk;

@@ -63,9 +63,24 @@ struct Elem<float> {
   }
 };
 
-template <typename T>
+// uint8 quantisation of one (token, kv head) row in float32, in the order
+// scale = (max - min) / 255 (1 if 0), zero = rint(-min / scale) clamped,
+// code = rint(x / scale + zero) clamped (rint: nearest, ties to even).
+__device__ __forceinline__ float2 u8_params(float mn, float mx) {
+  float sc = __fdiv_rn(__fsub_rn(mx, mn), 255.0f);
+  if (sc == 0.0f) sc = 1.0f;
+  const float zp = fminf(fmaxf(rintf(__fdiv_rn(-mn, sc)), 0.0f), 255.0f);
+  return make_float2(sc, zp);
+}
+
+__device__ __forceinline__ uint32_t u8_code(float x, float2 sz) {
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(__fadd_rn(__fdiv_rn(x, sz.x), sz.y)), 0.0f), 255.0f));
+}
+
+template <typename T, bool QU8>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const AppendParams p) {
   __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];
+  __shared__ float s_red[kAppendThreads / 32][4];  // uint8 cache: per-warp k/v min and max
   __shared__ long long s_row;     // element offset of the slot row of kv head 0
   __shared__ long long s_stride;  // element distance between kv heads at that slot
   __shared__ int s_ok;
@@ -154,6 +169,57 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
   if (!s_ok) return;
 
+  if constexpr (QU8) {
+    // k: fp64 rotation rounded to fp32, then both rows quantised; one pair per thread
+    const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(b) * p.h_kv * D;
+    const bool act = i0 < n_pairs;
+    const int hl = act ? i0 / half : 0, i = i0 % half;
+    float kx = 0.f, ky = 0.f, vx = 0.f, vy = 0.f;
+    if (act) {
+      const double xd = x0.x, yd = x0.y, c = s_cos[i], s = s_sin[i];
+      kx = __double2float_rn(__dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s)));
+      ky = __double2float_rn(__dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c)));
+      const float2 vv = Elem<T>::load2(v + (h_begin + hl) * D + 2 * i);
+      vx = vv.x;
+      vy = vv.y;
+    }
+    float r[4] = {act ? fminf(kx, ky) : INFINITY, act ? fmaxf(kx, ky) : -INFINITY,
+                  act ? fminf(vx, vy) : INFINITY, act ? fmaxf(vx, vy) : -INFINITY};
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {  // a warp never spans two heads (half is 32 or 64)
+      r[0] = fminf(r[0], __shfl_xor_sync(0xffffffffu, r[0], off));
+      r[1] = fmaxf(r[1], __shfl_xor_sync(0xffffffffu, r[1], off));
+      r[2] = fminf(r[2], __shfl_xor_sync(0xffffffffu, r[2], off));
+      r[3] = fmaxf(r[3], __shfl_xor_sync(0xffffffffu, r[3], off));
+    }
+    if ((threadIdx.x & 31) == 0) {
+      s_red[threadIdx.x >> 5][0] = r[0];
+      s_red[threadIdx.x >> 5][1] = r[1];
+      s_red[threadIdx.x >> 5][2] = r[2];
+      s_red[threadIdx.x >> 5][3] = r[3];
+    }
+    __syncthreads();
+    if (!act) return;
+    float kmn = INFINITY, kmx = -INFINITY, vmn = INFINITY, vmx = -INFINITY;
+    for (int w = hl * half / 32; w < (hl + 1) * half / 32; ++w) {
+      kmn = fminf(kmn, s_red[w][0]);
+      kmx = fmaxf(kmx, s_red[w][1]);
+      vmn = fminf(vmn, s_red[w][2]);
+      vmx = fmaxf(vmx, s_red[w][3]);
+    }
+    const float2 ksz = u8_params(kmn, kmx), vsz = u8_params(vmn, vmx);
+    const long long row = s_row + static_cast<long long>(h_begin + hl) * s_stride;  // element offset of the row
+    uint8_t* kc = static_cast<uint8_t*>(p.k_cache) + row;
+    uint8_t* vc = static_cast<uint8_t*>(p.v_cache) + row;
+    *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(u8_code(kx, ksz) | (u8_code(ky, ksz) << 8));
+    *reinterpret_cast<uint16_t*>(vc + 2 * i) = static_cast<uint16_t>(u8_code(vx, vsz) | (u8_code(vy, vsz) << 8));
+    if (i == 0) {
+      p.k_sz[row / D] = ksz;
+      p.v_sz[row / D] = vsz;
+    }
+    return;
+  }
+
   // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
   const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(b) * p.h_kv * D;
   T* kc = static_cast<T*>(p.k_cache) + s_row;
@@ -184,8 +250,9 @@ cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kAppendThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  if (p.cache_dtype == kDtypeBf16) return cudaLaunchKernelEx(&cfg, append_rope_kernel<__nv_bfloat16>, p);
-  return cudaLaunchKernelEx(&cfg, append_rope_kernel<float>, p);
+  if (p.cache_dtype == kDtypeU8) return cudaLaunchKernelEx(&cfg, append_rope_kernel<__nv_bfloat16, true>, p);
+  if (p.cache_dtype == kDtypeBf16) return cudaLaunchKernelEx(&cfg, append_rope_kernel<__nv_bfloat16, false>, p);
+  return cudaLaunchKernelEx(&cfg, append_rope_kernel<float, false>, p);
 }
 
 }  // namespace mqa

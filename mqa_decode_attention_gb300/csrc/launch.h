@@ -11,6 +11,7 @@ constexpr int kTile = 64;          // tokens per pipeline stage of the decode ke
 constexpr int kMaxHalfDim = 64;    // RoPE frequencies held in the append kernel's parameters
 constexpr int kDtypeBf16 = 0;
 constexpr int kDtypeF32 = 1;
+constexpr int kDtypeU8 = 2;  // cache only: uint8 codes + float2 (scale, zero point) per row
 
 struct AppendParams {
   int batch, h_q, h_kv, head_dim, cache_dtype, paged;
@@ -25,6 +26,8 @@ struct AppendParams {
   const int32_t* block_table;
   float* q_rot;
   int32_t* err;
+  float2* k_sz;  // uint8 cache: (scale, zero point) per row
+  float2* v_sz;
   double theta[kMaxHalfDim];  // RoPE inverse frequencies base^(-2i/d)
 };
 
@@ -35,6 +38,8 @@ struct DecodeParams {
   long long capacity;
   int page_size, num_pages, max_pages;
   const int32_t* block_table;
+  const float2* k_sz;  // uint8 cache: (scale, zero point) per row
+  const float2* v_sz;
   const float* q_rot;
   const int32_t* seq_lens;
   int max_seq_len;
@@ -95,6 +100,15 @@ int decode_mma_heads_group(const DecodeParams& p);
 KernelShape decode_mma_heads_shape(int heads_per_block);
 cudaError_t launch_decode_mma_heads(const DecodeParams& p, int heads_per_block, const CUtensorMap& tmap_k,
                                     const CUtensorMap& tmap_v, cudaStream_t stream);
+
+// uint8 cache (codes + per-row scale and zero point), tensor cores; maps =
+// {K codes, V codes, K (scale, zero), V (scale, zero)}.
+KernelShape decode_u8_shape(int head_dim, int group);
+cudaError_t launch_decode_u8(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream);
+// Paged 16- or 32-token pages, G <= 16: kv heads per block of the head-group
+// uint8 kernel (4 or 2), or 0 when it does not apply. Its maps box `hg` heads.
+int decode_u8_heads_group(const DecodeParams& p);
+cudaError_t launch_decode_u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 

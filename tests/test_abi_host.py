@@ -82,12 +82,28 @@ def test_attention_rejects_bad_arguments(lib):
     assert _attn(lib, lay, out=None) == _abi.MQA_ERR_INVALID_ARG
     assert _attn(lib, _layout(window=-1)) == _abi.MQA_ERR_INVALID_ARG
     assert _attn(lib, lay, err=None) == _abi.MQA_ERR_INVALID_ARG
-    # tensor cores need a bf16 cache
+    # tensor cores read bf16 or uint8 caches, CUDA cores bf16 or fp32
     assert _attn(lib, _layout(cache_dtype=_abi.MQA_F32), variant=_abi.MQA_VARIANT_TENSOR_CORE) == \
         _abi.MQA_ERR_UNSUPPORTED
     # a split run needs its workspace
     assert _attn(lib, lay, splits=4) == _abi.MQA_ERR_WORKSPACE
     assert _attn(lib, lay, splits=4, ws=FAKE, ws_bytes=16) == _abi.MQA_ERR_WORKSPACE
+
+
+def test_u8_layout_checks(lib):
+    """A uint8 cache needs its (scale, zero) arrays, 16-byte aligned, an even
+    capacity (the pairs of a kv head are copied with 16-byte strides), and the
+    tensor-core kernel."""
+    ok = dict(cache_dtype=_abi.MQA_U8, k_scale_zero=FAKE + 8192, v_scale_zero=FAKE + 12288)
+    assert _append(lib, _layout(cache_dtype=_abi.MQA_U8)) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(**dict(ok, k_scale_zero=FAKE + 8))) == _abi.MQA_ERR_INVALID_ARG
+    assert _append(lib, _layout(**dict(ok, capacity=255))) == _abi.MQA_ERR_UNSUPPORTED
+    assert _attn(lib, _layout(**dict(ok, v_scale_zero=None))) == _abi.MQA_ERR_INVALID_ARG
+    assert _attn(lib, _layout(**ok), variant=_abi.MQA_VARIANT_CUDA_CORE) == _abi.MQA_ERR_UNSUPPORTED
+    # paged pools have no capacity constraint
+    assert _attn(lib, _layout(**dict(ok, paged=1, capacity=0, page_size=16, num_pages=4, max_pages_per_seq=2,
+                                     block_table=FAKE)), max_len=32, variant=_abi.MQA_VARIANT_CUDA_CORE) == \
+        _abi.MQA_ERR_UNSUPPORTED
 
 
 def test_combine_rejects_bad_arguments(lib):

@@ -1,0 +1,218 @@
+"""GPU parity of the uint8 KV cache (MQA_U8) against the fp64 oracle.
+
+The oracle quantises the new token's rotated key and its value in float32 (the
+pages' QuantizedKVCache) and attends over the dequantised cache in fp64. The
+append is integer / byte work and must match exactly: codes, scale and zero
+point of the appended rows, and nothing else in the caches changes. Outputs
+are bf16, max |err| <= 2e-2 like the bf16 cache path.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import make_contiguous_case, make_paged_case, make_u8_cache, workload
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-2
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def m(built_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mqa_decode_attention_gb300 as mod
+
+    mod.library()
+    return mod
+
+
+def _np(t):
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def _contiguous(w, lens, cap, seed):
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=cap)
+    u = make_u8_cache((w.batch, w.h_kv, cap), w.head_dim, seed)
+    return c, u
+
+
+def _paged(w, lens, seed):
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=2)
+    u = make_u8_cache((pc.num_pages, w.h_kv, pc.page_size), w.head_dim, seed)
+    return pc, u
+
+
+def run_u8(m, w, case, u, paged, splits=0, window=0, table=None, max_len=None):
+    kc, vc = u.k_codes.to(DEV), u.v_codes.to(DEV)
+    ks, vs = u.k_sz.to(DEV), u.v_sz.to(DEV)
+    if paged:
+        bt = (case.block_table if table is None else table).to(DEV)
+        lay = m.layout_paged(kc, vc, bt, w.h_q, window=window, k_scale_zero=ks, v_scale_zero=vs)
+    else:
+        lay = m.layout_contiguous(kc, vc, w.h_q, window=window, k_scale_zero=ks, v_scale_zero=vs)
+    max_len = int(case.seq_lens.max()) if max_len is None else max_len
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=splits, device=DEV)
+    m.decode_step(lay, case.q_new.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV), case.pos.to(DEV),
+                  case.seq_lens.to(DEV), max_len, bufs, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                  num_splits=splits)
+    torch.cuda.synchronize()
+    return dict(out=_np(bufs.out), lse=_np(bufs.lse), q_rot=_np(bufs.q_rot), err=int(bufs.err.item()),
+                k_codes=kc.cpu().numpy(), v_codes=vc.cpu().numpy(), k_sz=ks.cpu().numpy(), v_sz=vs.cpu().numpy())
+
+
+def _oracle(w, case, u, paged, window=0):
+    if paged:
+        return oracle.decode_step_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, case.q_new, case.k_new, case.v_new,
+                                     case.seq_lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                     block_table=case.block_table,
+                                     page_size=case.page_size, window=window)
+    return oracle.decode_step_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, case.q_new, case.k_new, case.v_new,
+                                 case.seq_lens, w.rope_base, 1.0 / math.sqrt(w.head_dim), window=window)
+
+
+def check_u8_append(got, ref):
+    """Codes and (scale, zero) pairs equal the oracle's everywhere: the appended
+    rows bit for bit, every other row untouched."""
+    for key in ("k_codes", "v_codes"):
+        bad = np.argwhere(got[key] != ref[key])
+        assert bad.size == 0, (key, bad[:5])
+    for key in ("k_sz", "v_sz"):
+        assert np.array_equal(got[key].view(np.uint32), np.asarray(ref[key], np.float32).view(np.uint32)), key
+
+
+SHAPES = [
+    # B, h_q, h_kv, d, lens, capacity
+    (2, 32, 8, 128, [1000, 257], 1000),      # G=4, ragged tail
+    (3, 8, 8, 128, [64, 1, 129], 130),       # MHA
+    (1, 16, 1, 128, [777], 778),             # MQA, G=16
+    (2, 64, 2, 128, [300, 45], 300),         # G=32: two head blocks in one CTA
+    (1, 96, 1, 64, [200], 200),              # G=96: several head super-blocks, d=64
+    (2, 12, 3, 64, [513, 64], 514),          # d=64, G=4
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}d{s[3]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_u8_contiguous_matches_oracle(m, shape, splits):
+    B, hq, hkv, d, lens, cap = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, head_dim=d, seed=300 + hq + d)
+    c, u = _contiguous(w, lens, cap, seed=7 + d)
+    ref = _oracle(w, c, u, paged=False)
+    got = run_u8(m, w, c, u, paged=False, splits=splits)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
+    check_u8_append(got, ref)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("heads", [(16, 2, 128), (32, 8, 128), (12, 3, 128), (64, 2, 128), (16, 4, 64)],
+                         ids=lambda h: f"q{h[0]}kv{h[1]}d{h[2]}")
+def test_u8_paged_matches_oracle(m, page_size, heads):
+    """16- and 32-token pages with G <= 16 and an even kv head count run the
+    head-group kernel (groups of 4 or 2 kv heads per block); the rest the
+    token-slice kernel."""
+    w = workload("paged").with_(batch=5, h_q=heads[0], h_kv=heads[1], head_dim=heads[2], page_size=page_size,
+                                len_lo=1, len_hi=700, seed=19)
+    pc, u = _paged(w, [1, 16, 17, 700, 333], seed=23)
+    ref = _oracle(w, pc, u, paged=True)
+    for splits in (1, 3, 0):
+        got = run_u8(m, w, pc, u, paged=True, splits=splits)
+        assert got["err"] == 0
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, splits
+        assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+        check_u8_append(got, ref)
+
+
+@pytest.mark.parametrize("window", [1, 16, 17, 100, 1000])
+def test_u8_sliding_window(m, window):
+    w = workload("gqa4k").with_(batch=3, h_q=16, h_kv=4, seed=71)
+    c, u = _contiguous(w, [700, 65, 3], 704, seed=5)
+    ref = _oracle(w, c, u, paged=False, window=window)
+    for splits in (1, 0):
+        got = run_u8(m, w, c, u, paged=False, splits=splits, window=window, max_len=700)
+        assert got["err"] == 0
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
+    wp = workload("paged").with_(batch=4, h_q=16, h_kv=4, seed=72)
+    pc, up = _paged(wp, [700, 64, 17, 1], seed=6)
+    refp = _oracle(wp, pc, up, paged=True, window=window)
+    table = pc.block_table.clone()
+    for b, L in enumerate([700, 64, 17, 1]):
+        table[b, :max(0, L - window) // pc.page_size] = -1  # released pages before the window
+    got = run_u8(m, wp, pc, up, paged=True, splits=0, window=window, table=table, max_len=700)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - refp["out"])) <= BF16_TOL, window
+
+
+def test_u8_quantised_values_match_dequantised_input(m):
+    """A cache built by quantising N(0,1) rows with the oracle's quantiser:
+    the GPU result equals attention over the dequantised values."""
+    w = workload("gqa4k").with_(batch=2, h_q=8, h_kv=2, seed=73)
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor([500, 77], dtype=torch.int32), capacity=500)
+    kq, ks, kz = oracle.quantize_u8(c.k_cache.float().numpy())
+    vq, vs, vz = oracle.quantize_u8(c.v_cache.float().numpy())
+
+    class U:
+        k_codes = torch.from_numpy(kq)
+        v_codes = torch.from_numpy(vq)
+        k_sz = torch.from_numpy(np.stack([ks, kz], -1).astype(np.float32))
+        v_sz = torch.from_numpy(np.stack([vs, vz], -1).astype(np.float32))
+
+    ref = _oracle(w, c, U, paged=False)
+    got = run_u8(m, w, c, U, paged=False)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
+    check_u8_append(got, ref)
+
+
+def test_u8_large_v_scale_sets_error(m):
+    """A V scale beyond what the kernel's fp16 P' holds is reported, not
+    silently wrong."""
+    w = workload("gqa4k").with_(batch=1, h_q=8, h_kv=2, seed=74)
+    c, u = _contiguous(w, [100], 100, seed=8)
+    u.v_sz[0, 1, 10, 0] = 2000.0
+    got = run_u8(m, w, c, u, paged=False, splits=1)
+    assert got["err"] & m.MQA_DEVERR_U8_SCALE
+
+
+def test_u8_full_size_sampled(m):
+    """The 4096-token GQA workload (batch 32, 32 query / 8 kv heads) over a
+    uint8 cache: three (sequence, kv head) units against the oracle."""
+    w = workload("gqa4k")
+    L = w.seq_len
+    c = make_contiguous_case(w, DEV)
+    u = make_u8_cache((w.batch, w.h_kv, L), w.head_dim, 9, device=DEV)
+    units = [(0, 0), (w.batch - 1, w.h_kv - 1), (13, 5)]
+    saved = {(b, j): (u.k_codes[b, j].cpu(), u.k_sz[b, j].cpu(), u.v_codes[b, j].cpu(), u.v_sz[b, j].cpu())
+             for b, j in units}
+    lay = m.layout_contiguous(u.k_codes, u.v_codes, w.h_q, k_scale_zero=u.k_sz, v_scale_zero=u.v_sz)
+    bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, device=DEV)
+    m.decode_step(lay, c.q_new, c.k_new, c.v_new, c.pos, c.seq_lens, L, bufs, w.rope_base,
+                  1.0 / math.sqrt(w.head_dim), num_splits=0)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    G = w.group
+    for b, j in units:
+        kc, ks, vc, vs = saved[(b, j)]
+        sub = workload("gqa4k").with_(batch=1, h_q=G, h_kv=1)
+
+        class Case:
+            q_new = c.q_new[b:b + 1, j * G:(j + 1) * G].cpu()
+            k_new = c.k_new[b:b + 1, j:j + 1].cpu()
+            v_new = c.v_new[b:b + 1, j:j + 1].cpu()
+            seq_lens = torch.tensor([L], dtype=torch.int32)
+
+        class Unit:
+            k_codes, k_sz, v_codes, v_sz = kc[None, None], ks[None, None], vc[None, None], vs[None, None]
+
+        ref = _oracle(sub, Case, Unit, paged=False)
+        got = _np(bufs.out[b, j * G:(j + 1) * G])
+        assert np.max(np.abs(got - ref["out"][0])) <= BF16_TOL, (b, j)
+        assert np.array_equal(u.k_codes[b, j, L - 1].cpu().numpy(), ref["k_codes"][0, 0, L - 1])
