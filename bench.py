@@ -8,12 +8,15 @@ The default workload is the Llama-style GQA decode step (batch 32, 32 query
 heads, 8 KV heads, head_dim 128, 4096-token bf16 cache, RoPE base 10000).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--cache native|u8] [--window W]
 
 ``value`` is the achieved HBM throughput of the step in GB/s (algorithmic
 bytes / device time, summed over ranks); ``ms_per_step`` gives the step time.
 Under torchrun each rank runs its own batch (weak scaling, no collective on
 the data path). ``--impl reference`` times the fp64 CPU oracle on the host
 cores instead, one (sequence, kv head) unit of the same workload per step.
+``--cache u8`` runs the same workload over a uint8 cache (codes plus a float32
+(scale, zero point) pair per cached row, as the pages' QuantizedKVCache).
 """
 
 from __future__ import annotations
@@ -38,13 +41,13 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from synthetic import make_contiguous_case, make_paged_case, workload  # noqa: E402
+from synthetic import make_contiguous_case, make_paged_case, make_u8_cache, workload  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 GPU"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "gqa4k"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "mma_warp.cuh", "ptx.cuh", "launch.h"]
+KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "mma_warp.cuh", "ptx.cuh", "launch.h"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -110,24 +113,30 @@ def attended(lens, window: int):
     return lens.clamp(max=window) if window > 0 else lens
 
 
-def step_bytes(w, lens, out_esize, window: int = 0):
+def row_bytes(w, cache: str) -> int:
+    """Bytes of one cached (token, kv head) row of K (or V): head_dim values,
+    or head_dim uint8 codes plus the float32 (scale, zero point) pair."""
+    return w.head_dim + 8 if cache == "u8" else w.head_dim * w.esize
+
+
+def step_bytes(w, lens, out_esize, window: int = 0, cache: str = "native"):
     """Algorithmic bytes of one step: every attended K/V byte read once
     (including the new token), q_new read, out written, k_new/v_new read and
     their slot written, and (paged) the block-table entries used."""
-    es = w.esize
-    kv = 2 * int(attended(lens, window).sum()) * w.h_kv * w.head_dim * es
+    es = w.esize  # q_new / k_new / v_new
+    kv = 2 * int(attended(lens, window).sum()) * w.h_kv * row_bytes(w, cache)
     q = w.batch * w.h_q * w.head_dim * es
     out = w.batch * w.h_q * w.head_dim * out_esize
-    append = 2 * 2 * w.batch * w.h_kv * w.head_dim * es
+    append = 2 * w.batch * w.h_kv * (w.head_dim * es + row_bytes(w, cache))
     table = 4 * int(((attended(lens, window) + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
     return kv + q + out + append + table
 
 
-def attention_bytes(w, lens, out_esize, window: int = 0):
+def attention_bytes(w, lens, out_esize, window: int = 0, cache: str = "native"):
     """Algorithmic bytes of one gqa_decode_attention launch: K/V of every
     attended token, q_rot (fp32) read, out written, block-table entries (paged)."""
     lens = attended(lens, window)
-    kv = 2 * int(lens.sum()) * w.h_kv * w.head_dim * w.esize
+    kv = 2 * int(lens.sum()) * w.h_kv * row_bytes(w, cache)
     q = w.batch * w.h_q * w.head_dim * 4
     out = w.batch * w.h_q * w.head_dim * out_esize
     table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
@@ -199,10 +208,33 @@ def gpu_index_for(local_rank: int) -> str:
 
 
 # ----------------------------------------------------------- inputs / oracle
-def build_case(w, device):
+U8_SEED = 77
+
+
+def build_case(w, device, cache: str = "native"):
+    """The workload's seeded inputs. With cache "u8" the K/V caches are
+    replaced by uint8 codes and (scale, zero point) pairs of the same rows
+    (attributes u8 = synthetic.U8Cache)."""
+    case = make_paged_case(w, device) if w.paged else make_contiguous_case(w, device)
+    case.u8 = None
+    if cache == "u8":
+        if w.paged:
+            rows = (case.num_pages, w.h_kv, case.page_size)
+            case.k_pool = case.v_pool = None
+        else:
+            rows = (w.batch, w.h_kv, case.capacity)
+            case.k_cache = case.v_cache = None
+        case.u8 = make_u8_cache(rows, w.head_dim, U8_SEED, device=device)
+    return case
+
+
+def _rows(w, case, cache_t, b, j, L):
+    """Rows [0, L) of kv head j of sequence b from a cache tensor."""
     if w.paged:
-        return make_paged_case(w, device)
-    return make_contiguous_case(w, device)
+        n = (L + w.page_size - 1) // w.page_size
+        pages = case.block_table[b, :n].long()
+        return cache_t[pages, j].reshape(-1, *cache_t.shape[3:])[:L].cpu()
+    return cache_t[b, j, :L].cpu()
 
 
 def unit_inputs(w, case, units):
@@ -212,38 +244,51 @@ def unit_inputs(w, case, units):
     lens = case.seq_lens.cpu()
     for b, j in units:
         L = int(lens[b])
-        if w.paged:
-            n = (L + w.page_size - 1) // w.page_size
-            pages = case.block_table[b, :n].long()
-            K = case.k_pool[pages, j].reshape(-1, w.head_dim)[:L].cpu()
-            V = case.v_pool[pages, j].reshape(-1, w.head_dim)[:L].cpu()
+        u = dict(b=b, j=j, L=L, q=case.q_new[b, j * G:(j + 1) * G].cpu(), k=case.k_new[b, j].cpu(),
+                 v=case.v_new[b, j].cpu())
+        if case.u8 is not None:
+            c = case.u8
+            u.update(Kc=_rows(w, case, c.k_codes, b, j, L), Ks=_rows(w, case, c.k_sz, b, j, L),
+                     Vc=_rows(w, case, c.v_codes, b, j, L), Vs=_rows(w, case, c.v_sz, b, j, L))
         else:
-            K = case.k_cache[b, j, :L].cpu()
-            V = case.v_cache[b, j, :L].cpu()
-        out.append(dict(b=b, j=j, L=L, q=case.q_new[b, j * G:(j + 1) * G].cpu(), k=case.k_new[b, j].cpu(),
-                        v=case.v_new[b, j].cpu(), K=K, V=V))
+            kc, vc = (case.k_pool, case.v_pool) if w.paged else (case.k_cache, case.v_cache)
+            u.update(K=_rows(w, case, kc, b, j, L), V=_rows(w, case, vc, b, j, L))
+        out.append(u)
     return out
 
 
-def unit_bytes(w, L, out_esize):
+def unit_bytes(w, L, out_esize, cache: str = "native"):
     es = w.esize
-    return (2 * L * w.head_dim * es + w.group * w.head_dim * (es + out_esize) + 4 * w.head_dim * es)
+    return (2 * L * row_bytes(w, cache) + w.group * w.head_dim * (es + out_esize)
+            + 2 * (w.head_dim * es + row_bytes(w, cache)))
+
+
+def oracle_unit(w, u, window: int = 0):
+    """The oracle's decode step for one (sequence, kv head) unit: its output rows."""
+    import oracle  # test infrastructure: the CPU-baseline and reference legs only
+
+    scale = 1.0 / math.sqrt(w.head_dim)
+    if "Kc" in u:
+        L = u["L"]
+        r = oracle.decode_step_u8(u["Kc"][None, None], u["Ks"][None, None], u["Vc"][None, None], u["Vs"][None, None],
+                                  u["q"][None], u["k"][None, None], u["v"][None, None], [L], w.rope_base, scale,
+                                  window=window)
+        return r["out"][0]
+    o, _, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype,
+                                 window=window)
+    return o
 
 
 def run_oracle_units(w, inputs, budget_s: float, min_units: int = 2, window: int = 0):
-    """Time oracle.decode_unit over the units, cycling through them, until the
-    budget is spent. Returns the first result of each unit and the totals."""
-    import oracle  # test infrastructure: the CPU-baseline leg only
-
-    scale = 1.0 / math.sqrt(w.head_dim)
+    """Time the oracle's decode step over the units, cycling through them,
+    until the budget is spent. Returns the first result of each unit and the totals."""
     results = {}
     done = 0
     t0 = time.perf_counter()
     i = 0
     while True:
         u = inputs[i % len(inputs)]
-        o, lse, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype,
-                                       window=window)
+        o = oracle_unit(w, u, window)
         results.setdefault(i % len(inputs), (u, o))
         done += 1
         i += 1
@@ -270,10 +315,19 @@ def bench_ours(args):
         w = w.with_(num_splits=args.splits)
     if args.batch:
         w = w.with_(batch=args.batch)
-    case = build_case(w, dev)
+    u8 = args.cache == "u8"
+    case = build_case(w, dev, args.cache)
     lens_cpu = case.seq_lens.cpu()
     max_len = int(lens_cpu.max())
-    if w.paged:
+    if u8:
+        c = case.u8
+        if w.paged:
+            lay = m.layout_paged(c.k_codes, c.v_codes, case.block_table, w.h_q, window=args.window,
+                                 k_scale_zero=c.k_sz, v_scale_zero=c.v_sz)
+        else:
+            lay = m.layout_contiguous(c.k_codes, c.v_codes, w.h_q, window=args.window, k_scale_zero=c.k_sz,
+                                      v_scale_zero=c.v_sz)
+    elif w.paged:
         lay = m.layout_paged(case.k_pool, case.v_pool, case.block_table, w.h_q, window=args.window)
     else:
         lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q, window=args.window)
@@ -282,8 +336,8 @@ def bench_ours(args):
     scale = 1.0 / math.sqrt(w.head_dim)
     splits_used = w.num_splits if w.num_splits > 0 else m.choose_splits(lay, max_len, variant)
     out_es = bufs.out.element_size()
-    sbytes = step_bytes(w, lens_cpu, out_es, args.window)
-    abytes = attention_bytes(w, lens_cpu, out_es, args.window)
+    sbytes = step_bytes(w, lens_cpu, out_es, args.window, args.cache)
+    abytes = attention_bytes(w, lens_cpu, out_es, args.window, args.cache)
     stream = torch.cuda.current_stream()
 
     # CPU-baseline units (rank 0, N = 1), copied before any step touches the cache
@@ -305,7 +359,7 @@ def bench_ours(args):
         m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs, w.rope_base,
                       scale, w.num_splits, variant, stream)
 
-    fused = variant in (0, 2) and w.dtype == "bf16" and w.group <= 32  # append done inside the decode kernel
+    fused = not u8 and variant in (0, 2) and w.dtype == "bf16" and w.group <= 32  # append inside the decode kernel
     launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
@@ -396,7 +450,10 @@ def bench_ours(args):
     e2e_value = throughput_gbs(world, sbytes, e2e_ms / K)
 
     peak, peak_src = measured_peak()
-    if variant in (0, 2) and w.dtype == "bf16":
+    if u8:
+        heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
+        kernel_name = "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel"
+    elif variant in (0, 2) and w.dtype == "bf16":
         heads_kernel = w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
         kernel_name = "decode_mma_heads_kernel" if heads_kernel else "decode_mma_kernel"
     else:
@@ -416,7 +473,8 @@ def bench_ours(args):
         roof_kernel = kernel_name + (" + combine_kernel" if splits_used > 1 else "")
         roof_time = "events around each standalone gqa_decode_attention call"
     achieved = roof_bytes / (roof_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload) if kernel_name.startswith("decode_mma") else None
+    traffic = (ncu_traffic(args.workload + ("_u8" if u8 else "")) if kernel_name.startswith(("decode_mma", "decode_u8"))
+               else None)
     clocks = sampler.summary(t_clock0, t_clock1)
 
     line = {
@@ -431,12 +489,16 @@ def bench_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
-        "data": "synthetic (seeded N(0,1) bf16 q/k/v and cache; no dataset)",
+        "dtype": "u8" if u8 else w.dtype,
+        "data": ("synthetic (seeded N(0,1) bf16 q/k/v; uint8 cache codes U[0,255], scales ~6/255, zero points "
+                 "U[100,155]; no dataset)" if u8 else "synthetic (seeded N(0,1) bf16 q/k/v and cache; no dataset)"),
         "config": {
             "workload": (f"{w.name}: batch {w.batch}, H_q {w.h_q}, H_kv {w.h_kv}, head_dim {w.head_dim}, "
                          + (f"paged {w.page_size}-token pages, lengths U[{w.len_lo},{w.len_hi}]" if w.paged
-                            else f"contiguous {w.dtype} cache of {w.seq_len} tokens/seq") + ", RoPE base 10000"),
+                            else f"contiguous {'uint8' if u8 else w.dtype} cache of {w.seq_len} tokens/seq")
+                         + (", uint8 cache codes + float32 (scale, zero point) per row" if u8 else "")
+                         + ", RoPE base 10000"),
+            "cache": "u8" if u8 else w.dtype,
             "batch_per_gpu": w.batch,
             "tokens_per_step_per_gpu": int(lens_cpu.sum()),
             "num_splits": splits_used,
@@ -473,7 +535,7 @@ def bench_ours(args):
     if do_cpu:
         results, n_done, secs = run_oracle_units(w, units, args.cpu_seconds, window=args.window)
         by_unit = {(u["b"], u["j"]): u for u, _ in results}
-        done = sum(unit_bytes(w, min(units[i % len(units)]["L"], args.window or 1 << 30), out_es)
+        done = sum(unit_bytes(w, min(units[i % len(units)]["L"], args.window or 1 << 30), out_es, args.cache)
                    for i in range(n_done))
         out_host = bufs.out.float().cpu().numpy()
         G = w.group
@@ -498,25 +560,22 @@ def bench_reference(args):
     if rank != 0:
         return
     w = workload(args.workload)
-    case = build_case(w, "cpu")
+    case = build_case(w, "cpu", args.cache)
     lens = case.seq_lens
     n_units = w.batch * w.h_kv
     order = [(u // w.h_kv, u % w.h_kv) for u in range(n_units)]
-    out_es = w.esize
+    out_es = 4 if w.dtype == "f32" else 2
 
     def one(i):
         u = unit_inputs(w, case, [order[i % n_units]])
         return u
 
-    import oracle  # the reference arm is the oracle
-
-    scale = 1.0 / math.sqrt(w.head_dim)
     inputs = [one(i)[0] for i in range(min(n_units, args.warmup + args.steps))]
 
     def run(i):
         u = inputs[i % len(inputs)]
-        oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype)
-        return unit_bytes(w, u["L"], out_es)
+        oracle_unit(w, u, args.window)
+        return unit_bytes(w, min(u["L"], args.window or 1 << 30), out_es, args.cache)
 
     for i in range(args.warmup):
         run(i)
@@ -531,7 +590,8 @@ def bench_reference(args):
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
         "impl": "reference",
-        "config": {"workload": w.name, "batch_per_gpu": w.batch, "tokens_per_step_per_gpu": int(lens.sum()),
+        "config": {"workload": w.name, "cache": args.cache if args.cache == "u8" else w.dtype, "window": args.window,
+                   "batch_per_gpu": w.batch, "tokens_per_step_per_gpu": int(lens.sum()),
                    "step": "one (sequence, kv head) unit of the workload per step, cycling over the units"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} units of {n_units}, fp64 numpy, single thread"},
@@ -554,6 +614,8 @@ def main():
                     help="minimum warm-up time, so the clock sampler sees the load (0 for profiler runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--window", type=int, default=0, help="sliding window: attend to the last W tokens (0 = all)")
+    ap.add_argument("--cache", choices=["native", "u8"], default="native",
+                    help="cache type: the workload's own (bf16 / fp32) or uint8 codes with per-row scale / zero point")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-units", type=int, default=0, help="distinct units in the CPU sample (0 = all)")
     args = ap.parse_args()

@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "../../include/mqa_decode.h"
 #include "launch.h"
 #include "ptx.cuh"
@@ -605,10 +607,24 @@ cudaError_t launch_u8_t(const DecodeParams& p, const CUtensorMap* maps, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], p);
 }
 
+// Blocks per SM as the occupancy calculator sees them (registers bound the
+// 288-thread blocks to one); 0 if there is no device to ask.
 template <int D, int HB>
 KernelShape shape_t() {
   using C = U8Cfg<D, HB, U8Stages<D>::value>;
-  return {C::kThreads, C::kSmemBytes, 16 * HB, 0};
+  static std::atomic<int> occ{-1};
+  int n = occ.load(std::memory_order_relaxed);
+  if (n < 0) {
+    auto kern = decode_u8_kernel<D, HB, U8Stages<D>::value>;
+    n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmemBytes) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();  // the failed query's own error, not left for the next launch check
+    }
+    occ.store(n, std::memory_order_relaxed);
+  }
+  return {C::kThreads, C::kSmemBytes, 16 * HB, n};
 }
 
 // ---------------------------------------------------------------------------
