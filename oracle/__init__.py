@@ -16,6 +16,7 @@ from .decode import (
     attention_partial,
     causal_attention,
     decode_step_contiguous,
+    decode_step_multi,
     decode_step_paged,
     decode_step_u8,
     dequantize_u8,
@@ -36,6 +37,7 @@ from .decode import (
     window_start,
 )
 from .accounting import (
+    expected_tokens_per_verify,
     kv_bytes_per_token,
     kv_cache_bytes,
     layer_cache_scalars,

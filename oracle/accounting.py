@@ -10,6 +10,10 @@ TEST INFRASTRUCTURE (see oracle/decode.py): used by the oracle's pins only.
     bytes_per_element; total = bytes per token x seq_len x batch.
   * "KV Cache" explainer (lensaml.com), Langkah 5 and FAQ: the same product,
     cache per token = 2 x layers x kv_heads x head_dim x bytes.
+  * "Arsitektur Inferensi LLM ..." (tveniu.com), section 7 (speculative
+    decoding): with per-draft acceptance rate alpha and gamma drafted
+    tokens, one verification pass yields (1 - alpha^(gamma+1)) / (1 - alpha)
+    tokens in expectation (3.69 for alpha = 0.8, gamma = 5).
   * fahmindra.github.io bab 2.5.1: the formula's factors l (layers),
     u (batch), n (heads), b (head size), z (sequence length), a first 2 for
     K and V and a second 2 for 16-bit bytes (the formula itself was lost in
@@ -40,3 +44,14 @@ def projection_counts_closed_form(prompt_len: int, evals: int) -> tuple[int, int
     explainer, Langkah 2): T*P + T(T-1)/2 versus P + T - 1."""
     p, t = prompt_len, evals
     return t * p + t * (t - 1) // 2, p + t - 1
+
+
+def expected_tokens_per_verify(alpha: float, gamma: int) -> float:
+    """Expected tokens one verification pass yields ("Arsitektur Inferensi
+    LLM", section 7): the accepted prefix of the gamma drafts plus the one
+    token the target model supplies, each draft accepted with probability
+    alpha while all before it were: sum_{k=0..gamma} alpha^k
+    = (1 - alpha^(gamma+1)) / (1 - alpha)."""
+    if alpha == 1.0:
+        return float(gamma + 1)
+    return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)

@@ -372,6 +372,55 @@ def decode_step_u8(k_codes, k_sz, v_codes, v_sz, q_new, k_new, v_new, seq_lens, 
     return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "k_sz": Ks, "v_codes": Vc, "v_sz": Vs}
 
 
+def decode_step_multi(k_cache, v_cache, q_new, k_new, v_new, seq_lens, rope_base: float, scale: float,
+                      cache_dtype: str, block_table=None, page_size: int = 0, window: int = 0):
+    """n new tokens per sequence in one pass: the target-model verification of
+    speculative decoding ("Arsitektur Inferensi LLM", section 7), where the
+    drafted tokens are checked in parallel and the result must equal decoding
+    them one at a time.
+
+    q_new [B, n, H_q, d], k_new / v_new [B, n, H_kv, d]; seq_lens = L_b after
+    the append, so new token i of sequence b sits at position p = L_b - n + i.
+    Each new token's q and k are rotated by p, its k (rounded to the cache
+    dtype) and v stored at p (contiguous cache [B, H_kv, capacity, d], or a
+    paged pool through block_table); query i then attends to the tokens
+    [window_start(p + 1, W), p + 1) of the updated cache: causal within the
+    new tokens.
+    Returns dict(out [B,n,H_q,d], lse [B,n,H_q], q_rot [B,n,H_q,d], k_cache,
+    v_cache) with the caches as updated copies.
+    """
+    K = _f64(k_cache).copy()
+    V = _f64(v_cache).copy()
+    q_new, k_new, v_new = _f64(q_new), _f64(k_new), _f64(v_new)
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    table = None if block_table is None else np.asarray(_f64(block_table), dtype=np.int64)
+    B, n, h_q, d = q_new.shape
+    out = np.empty((B, n, h_q, d), F64)
+    lse = np.empty((B, n, h_q), F64)
+    q_rot = np.empty((B, n, h_q, d), F64)
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(n):
+            p = L - n + i
+            q_rot[b, i] = rope_rotate(q_new[b, i], p, rope_base)
+            k_stored = round_to(rope_rotate(k_new[b, i], p, rope_base), cache_dtype)
+            if table is None:
+                append_contiguous(K, V, b, p, k_stored, v_new[b, i])
+            else:
+                append_paged(K, V, table[b], page_size, p, k_stored, v_new[b, i])
+        if table is None:
+            Kb, Vb = K[b, :, :L], V[b, :, :L]
+        else:
+            Kb, Vb = gather_paged(K, table[b], L, page_size), gather_paged(V, table[b], L, page_size)
+        for i in range(n):
+            p = L - n + i
+            t0 = window_start(p + 1, window)
+            out[b, i], lse[b, i] = gqa_attention(q_rot[b, i], Kb[:, t0:p + 1], Vb[:, t0:p + 1], scale)
+    res = {"out": out, "lse": lse, "q_rot": q_rot}
+    res.update({"k_cache": K, "v_cache": V} if table is None else {"k_pool": K, "v_pool": V})
+    return res
+
+
 def decode_unit(q_group, k_row, v_row, K_unit, V_unit, seq_len: int, rope_base: float, scale: float,
                 cache_dtype: str, window: int = 0):
     """The decode step for ONE (sequence, KV head) unit, for sampled checks at

@@ -539,3 +539,133 @@ def test_u8_decode_step_pins():
     rp = oracle.decode_step_u8(pk.astype(np.uint8), pks, pv.astype(np.uint8), pvs, q, k, v, lens, 10000.0, 0.125,
                                block_table=table, page_size=16)
     assert np.array_equal(rp["out"], r["out"])
+
+
+# ------------------------------------------- multi-token (verify) decode
+def _multi_variant(K, V, q, k, v, lens, base, scale, dtype, rot_of, end_of):
+    """A restatement of the multi-token step with the RoPE position of new
+    token i and the end of its key range as parameters, to plant mistakes in.
+    New token i is stored at slot L - n + i."""
+    K, V = np.array(K, np.float64), np.array(V, np.float64)
+    B, n, h_q, d = q.shape
+    out = np.empty((B, n, h_q, d))
+    lse = np.empty((B, n, h_q))
+    qr = np.empty((B, n, h_q, d))
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(n):
+            r = rot_of(L, n, i)
+            qr[b, i] = oracle.rope_rotate(q[b, i], r, base)
+            K[b, :, L - n + i] = oracle.round_to(oracle.rope_rotate(k[b, i], r, base), dtype)
+            V[b, :, L - n + i] = v[b, i]
+        for i in range(n):
+            e = end_of(L, n, i)
+            out[b, i], lse[b, i] = oracle.gqa_attention(qr[b, i], K[b, :, :e], V[b, :, :e], scale)
+    return {"out": out, "lse": lse, "q_rot": qr, "k_cache": K, "v_cache": V}
+
+
+def check_multi_step(fn):
+    """n new tokens in one pass equal n single-token steps taken in order (the
+    verification of drafted tokens is lossless, tveniu.com section 7), for the
+    outputs, the log-sum-exps, q_rot and the updated caches, with and without a
+    sliding window."""
+    rng = np.random.default_rng(41)
+    B, h_q, h_kv, d, cap, n = 2, 8, 2, 32, 40, 5
+    K0 = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    V0 = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    q = oracle.round_bf16(rng.standard_normal((B, n, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    lens = np.array([40, 7])
+    for window in (0, 3):
+        r = fn(K0, V0, q, k, v, lens, 10000.0, 0.17, "bf16", window=window)
+        K, V = K0.copy(), V0.copy()
+        for i in range(n):
+            s = oracle.decode_step_contiguous(K, V, q[:, i], k[:, i], v[:, i], lens - n + i + 1, 10000.0, 0.17,
+                                              "bf16", window=window)
+            K, V = s["k_cache"], s["v_cache"]
+            assert np.max(np.abs(s["out"] - r["out"][:, i])) <= 1e-12
+            assert np.max(np.abs(s["lse"] - r["lse"][:, i])) <= 1e-12
+            assert np.array_equal(s["q_rot"], r["q_rot"][:, i])
+        assert np.array_equal(K, r["k_cache"]) and np.array_equal(V, r["v_cache"])
+
+
+def test_multi_token_decode_pins(golden_dir):
+    check_multi_step(oracle.decode_step_multi)
+    # n = 1 is the single-token step
+    rng = np.random.default_rng(43)
+    K0 = oracle.round_bf16(rng.standard_normal((2, 2, 30, 16)))
+    V0 = oracle.round_bf16(rng.standard_normal((2, 2, 30, 16)))
+    q = oracle.round_bf16(rng.standard_normal((2, 1, 4, 16)))
+    k = oracle.round_bf16(rng.standard_normal((2, 1, 2, 16)))
+    v = oracle.round_bf16(rng.standard_normal((2, 1, 2, 16)))
+    lens = np.array([30, 9])
+    r1 = oracle.decode_step_multi(K0, V0, q, k, v, lens, 500.0, 0.25, "bf16")
+    s1 = oracle.decode_step_contiguous(K0, V0, q[:, 0], k[:, 0], v[:, 0], lens, 500.0, 0.25, "bf16")
+    assert np.array_equal(r1["out"][:, 0], s1["out"]) and np.array_equal(r1["k_cache"], s1["k_cache"])
+    # the n new tokens of one pass equal the last n rows of full causal recomputation
+    w = workload("tiny")
+    seq = make_tiny_sequence(w)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    N = seq.prompt_len + seq.decode_evals - 1
+    n = 6
+    qa, ka, va = (t.double().numpy() for t in (seq.q, seq.k, seq.v))
+    K = np.zeros((w.batch, w.h_kv, N, w.head_dim))
+    V = np.zeros_like(K)
+    for p in range(N - n):
+        K[:, :, p] = np.stack([oracle.rope_rotate(ka[p, b], p, w.rope_base) for b in range(w.batch)])
+        V[:, :, p] = va[p]
+    tail = lambda x: np.transpose(x[N - n:N], (1, 0, 2, 3))  # [n, B, ...] -> [B, n, ...]
+    r = oracle.decode_step_multi(K, V, tail(qa), tail(ka), tail(va), np.full(w.batch, N), w.rope_base, scale, "f64")
+    _, last_rows, _ = oracle.run_uncached_sequence(seq.q, seq.k, seq.v, seq.prompt_len, seq.decode_evals,
+                                                   w.rope_base, scale)
+    for i in range(n):
+        assert np.max(np.abs(r["out"][:, i] - last_rows[:, :, N - n + i, :])) <= 1e-12
+    # paged equals contiguous on the same logical data
+    rng = np.random.default_rng(44)
+    B, h_kv, cap, d, n = 3, 2, 50, 16, 4
+    Kc = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    Vc = oracle.round_bf16(rng.standard_normal((B, h_kv, cap, d)))
+    q = oracle.round_bf16(rng.standard_normal((B, n, 8, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    lens = np.array([50, 4, 17])
+    rc = oracle.decode_step_multi(Kc, Vc, q, k, v, lens, 10000.0, 0.25, "bf16")
+    pk, table = _contiguous_to_paged(Kc, lens, 16, np.random.default_rng(5))
+    pv, _ = _contiguous_to_paged(Vc, lens, 16, np.random.default_rng(5))
+    rp = oracle.decode_step_multi(pk, pv, q, k, v, lens, 10000.0, 0.25, "bf16", block_table=table, page_size=16)
+    assert np.array_equal(rp["out"], rc["out"]) and np.array_equal(rp["lse"], rc["lse"])
+    # the pages' expected tokens per verification pass
+    g = _load(golden_dir, "speculative.json")
+    for c in g["cases"]:
+        got = oracle.expected_tokens_per_verify(c["alpha"], c["gamma"])
+        assert round(got, c["digits"]) == c["value"]
+        # brute force over accept / reject patterns: the pass yields the accepted
+        # prefix of the drafts plus one token from the target model
+        a, gam = c["alpha"], c["gamma"]
+        expect = 0.0
+        for pattern in range(2 ** gam):
+            accepts = [(pattern >> t) & 1 for t in range(gam)]
+            prob = np.prod([a if x else 1 - a for x in accepts])
+            prefix = next((t for t, x in enumerate(accepts) if not x), gam)
+            expect += prob * (prefix + 1)
+        assert abs(expect - got) <= 1e-12
+    assert oracle.expected_tokens_per_verify(1.0, 5) == 6.0
+    assert abs(oracle.expected_tokens_per_verify(0.0, 5) - 1.0) <= 1e-15
+
+
+def test_multi_token_planted_mistakes_are_caught():
+    def planted(rot_of, end_of):
+        def fn(K, V, q, k, v, lens, base, scale, dtype, window=0):
+            if window:  # the variants carry no window: the windowed half of the check uses the oracle
+                return oracle.decode_step_multi(K, V, q, k, v, lens, base, scale, dtype, window=window)
+            return _multi_variant(K, V, q, k, v, lens, base, scale, dtype, rot_of, end_of)
+        return fn
+
+    pos = lambda L, n, i: L - n + i
+    end = lambda L, n, i: L - n + i + 1
+    assert not _fails(check_multi_step, planted(pos, end))  # the restatement itself passes
+    assert _fails(check_multi_step, planted(pos, lambda L, n, i: L))  # no causal mask among the new tokens
+    assert _fails(check_multi_step, planted(pos, lambda L, n, i: min(L, L - n + i + 2)))  # sees the next draft
+    assert _fails(check_multi_step, planted(lambda L, n, i: L - 1, end))  # every new token rotated by L - 1
+    assert _fails(check_multi_step, planted(lambda L, n, i: L - n + i + 1, end))  # rotation one position late
