@@ -214,9 +214,12 @@ MQA_API mqa_status splitkv_combine(const float* o_part, const float* lse_part, i
  * arguments mean what they mean in those two calls; q_rot is the caller's
  * fp32 [batch, h_q, head_dim] scratch that carries the rotated query from the
  * first launch to the second. Every argument of both calls is checked before
- * the first launch. Because the attention launch directly follows the append
- * launch, it is allowed to start while the append is still running: it
- * streams every cached row except the appended one, the lengths and the
+ * the first launch. On the tensor-core path with a bf16 cache and at most 32
+ * query heads per kv head the step is ONE launch: the attention kernel
+ * rotates q and k_new itself, writes the new token's slot and q_rot, and then
+ * reads that slot back. Otherwise the attention launch directly follows the
+ * append launch and is allowed to start while the append is still running:
+ * it streams every cached row except the appended one, the lengths and the
  * block table early, and waits for the append before it reads q_rot or the
  * new token's row.
  */
@@ -254,6 +257,49 @@ MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, con
                                                 const int32_t* seq_lens, int32_t max_seq_len, float scale,
                                                 int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
                                                 int32_t variant, int32_t* err_word, mqa_stream_t stream);
+
+/*
+ * Multi-token decode: n_new query tokens per sequence in one pass -- the
+ * target model's verification of drafted tokens in speculative decoding
+ * ("Arsitektur Inferensi LLM", section 7: the gamma drafted tokens are
+ * checked in parallel, and the result must equal decoding them one by one).
+ *
+ * kv_append_rope_multi: q_new [batch, n_new, h_q, head_dim], k_new / v_new
+ *   [batch, n_new, h_kv, head_dim] (cache dtype); new token i of sequence b
+ *   is rotated by and stored at position pos[b] + i; q_rot [batch, n_new, h_q,
+ *   head_dim] fp32 output. Same arithmetic and device errors as kv_append_rope.
+ * gqa_decode_attention_multi: seq_lens[b] = length after the append; query
+ *   token i of sequence b (position L - n_new + i) attends to the tokens
+ *   [0, L - n_new + i] (with a window W: the last W of them) -- causal among
+ *   the new tokens. out [batch, n_new, h_q, head_dim], lse_out [batch, n_new,
+ *   h_q]. max_seq_len >= n_new; a sequence with L < n_new sets
+ *   MQA_DEVERR_SEQ_LEN. The (token, query head) pairs of a kv head are the
+ *   rows of one MMA tile set, so the K/V bytes are read once for all n_new
+ *   tokens.
+ * mqa_decode_step_multi: the two calls on one stream, pos[b] = L - n_new.
+ * 1 <= n_new <= 32. n_new > 1 runs on tensor cores over a bf16 cache only
+ * (MQA_ERR_UNSUPPORTED otherwise); n_new = 1 is exactly the single-token call.
+ */
+MQA_API mqa_status kv_append_rope_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new,
+                                        const void* k_new, const void* v_new, const int32_t* pos, double rope_base,
+                                        float* q_rot, int32_t* err_word, mqa_stream_t stream);
+MQA_API mqa_status gqa_decode_attention_multi(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,
+                                              const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                              int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
+                                              void* workspace, size_t workspace_bytes, int32_t variant,
+                                              int32_t* err_word, mqa_stream_t stream);
+MQA_API mqa_status mqa_decode_step_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new,
+                                         const void* k_new, const void* v_new, const int32_t* pos,
+                                         const int32_t* seq_lens, int32_t max_seq_len, double rope_base, float scale,
+                                         int32_t num_splits, float* q_rot, void* out, int32_t out_dtype,
+                                         float* lse_out, void* workspace, size_t workspace_bytes, int32_t variant,
+                                         int32_t* err_word, mqa_stream_t stream);
+/* Split count / workspace bytes of gqa_decode_attention_multi (as the
+ * single-token queries below; -1 / 0 for invalid arguments). */
+MQA_API int32_t mqa_choose_splits_multi(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len,
+                                        int32_t variant);
+MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len,
+                                        int32_t num_splits, int32_t variant);
 
 /* Split count gqa_decode_attention uses for num_splits = 0 on the current device
  * (>= 1), or -1 if the layout is invalid. */

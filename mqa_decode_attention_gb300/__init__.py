@@ -44,6 +44,9 @@ __all__ = [
     "choose_splits",
     "workspace_size",
     "decode_step",
+    "decode_step_multi",
+    "kv_append_rope_multi",
+    "gqa_decode_attention_multi",
     "library",
     "MQA_VARIANT_AUTO",
     "MQA_VARIANT_CUDA_CORE",
@@ -147,12 +150,38 @@ def splitkv_combine(o_part, lse_part, out, lse_out=None, stream=None) -> None:
         raise MqaError("splitkv_combine", st)
 
 
-def choose_splits(layout: KVLayout, max_seq_len: int, variant: int = MQA_VARIANT_AUTO) -> int:
-    return int(library().mqa_choose_splits(ctypes.byref(layout), int(max_seq_len), int(variant)))
+def kv_append_rope_multi(layout: KVLayout, n_new: int, q_new, k_new, v_new, pos, rope_base: float, q_rot, err,
+                         stream=None) -> None:
+    """Append n_new tokens per sequence: q_new [B, n, H_q, d], k_new / v_new
+    [B, n, H_kv, d]; token i at position pos[b] + i."""
+    st = library().kv_append_rope_multi(ctypes.byref(layout), int(n_new), _ptr(q_new), _ptr(k_new), _ptr(v_new),
+                                        _ptr(pos), float(rope_base), _ptr(q_rot), _ptr(err), _stream(stream))
+    if st != 0:
+        raise MqaError("kv_append_rope_multi", st)
 
 
-def workspace_size(layout: KVLayout, max_seq_len: int, num_splits: int, variant: int = MQA_VARIANT_AUTO) -> int:
-    return int(library().mqa_workspace_size(ctypes.byref(layout), int(max_seq_len), int(num_splits), int(variant)))
+def gqa_decode_attention_multi(layout: KVLayout, n_new: int, q_rot, seq_lens, max_seq_len: int, scale: float,
+                               num_splits: int, out, lse_out=None, workspace=None, variant: int = MQA_VARIANT_AUTO,
+                               err=None, stream=None) -> None:
+    """Attention of the last n_new tokens of each sequence, causal among them:
+    q_rot [B, n, H_q, d] fp32, out [B, n, H_q, d]."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = library().gqa_decode_attention_multi(ctypes.byref(layout), int(n_new), _ptr(q_rot), _ptr(seq_lens),
+                                              int(max_seq_len), float(scale), int(num_splits), _ptr(out),
+                                              _dtype_code(out.dtype), _ptr(lse_out), _ptr(workspace), ws_bytes,
+                                              int(variant), _ptr(err), _stream(stream))
+    if st != 0:
+        raise MqaError("gqa_decode_attention_multi", st)
+
+
+def choose_splits(layout: KVLayout, max_seq_len: int, variant: int = MQA_VARIANT_AUTO, n_new: int = 1) -> int:
+    return int(library().mqa_choose_splits_multi(ctypes.byref(layout), int(n_new), int(max_seq_len), int(variant)))
+
+
+def workspace_size(layout: KVLayout, max_seq_len: int, num_splits: int, variant: int = MQA_VARIANT_AUTO,
+                   n_new: int = 1) -> int:
+    return int(library().mqa_workspace_size_multi(ctypes.byref(layout), int(n_new), int(max_seq_len),
+                                                  int(num_splits), int(variant)))
 
 
 @dataclass
@@ -167,15 +196,18 @@ class DecodeBuffers:
 
     @staticmethod
     def allocate(layout: KVLayout, max_seq_len: int, num_splits: int = 0, variant: int = MQA_VARIANT_AUTO,
-                 out_dtype: torch.dtype | None = None, device="cuda") -> "DecodeBuffers":
+                 out_dtype: torch.dtype | None = None, device="cuda", n_new: int = 1) -> "DecodeBuffers":
+        """Buffers for n_new query tokens per sequence: [B, H_q, d] (n_new = 1)
+        or [B, n_new, H_q, d]."""
         B, hq, d = layout.batch, layout.h_q, layout.head_dim
         if out_dtype is None:
             out_dtype = torch.float32 if layout.cache_dtype == MQA_F32 else torch.bfloat16
-        ws = workspace_size(layout, max_seq_len, num_splits, variant)
+        ws = workspace_size(layout, max_seq_len, num_splits, variant, n_new)
+        rows = (B, hq) if n_new == 1 else (B, n_new, hq)
         return DecodeBuffers(
-            q_rot=torch.empty(B, hq, d, dtype=torch.float32, device=device),
-            out=torch.empty(B, hq, d, dtype=out_dtype, device=device),
-            lse=torch.empty(B, hq, dtype=torch.float32, device=device),
+            q_rot=torch.empty(*rows, d, dtype=torch.float32, device=device),
+            out=torch.empty(*rows, d, dtype=out_dtype, device=device),
+            lse=torch.empty(*rows, dtype=torch.float32, device=device),
             workspace=torch.empty(ws, dtype=torch.uint8, device=device) if ws > 0 else None,
             err=torch.zeros(1, dtype=torch.int32, device=device),
         )
@@ -197,4 +229,26 @@ def decode_step(layout: KVLayout, q_new, k_new, v_new, pos, seq_lens, max_seq_le
                                    _ptr(ws), ws_bytes, int(variant), _ptr(bufs.err), _stream(stream))
     if st != 0:
         raise MqaError("mqa_decode_step", st)
+    return bufs.out
+
+
+def decode_step_multi(layout: KVLayout, n_new: int, q_new, k_new, v_new, pos, seq_lens, max_seq_len: int,
+                      bufs: DecodeBuffers, rope_base: float = 10000.0, scale: float | None = None,
+                      num_splits: int = 0, variant: int = MQA_VARIANT_AUTO, stream=None) -> torch.Tensor:
+    """n_new new tokens per sequence through ``mqa_decode_step_multi`` (the
+    verification pass of speculative decoding): tokens appended with RoPE at
+    ``pos`` .. ``pos + n_new - 1`` (pos = seq_lens - n_new), then each attends
+    causally. q_new [B, n, H_q, d], k_new / v_new [B, n, H_kv, d]; buffers from
+    ``DecodeBuffers.allocate(..., n_new=n_new)``. Returns ``bufs.out``."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(layout.head_dim)
+    ws = bufs.workspace
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = library().mqa_decode_step_multi(ctypes.byref(layout), int(n_new), _ptr(q_new), _ptr(k_new), _ptr(v_new),
+                                         _ptr(pos), _ptr(seq_lens), int(max_seq_len), float(rope_base), float(scale),
+                                         int(num_splits), _ptr(bufs.q_rot), _ptr(bufs.out),
+                                         _dtype_code(bufs.out.dtype), _ptr(bufs.lse), _ptr(ws), ws_bytes,
+                                         int(variant), _ptr(bufs.err), _stream(stream))
+    if st != 0:
+        raise MqaError("mqa_decode_step_multi", st)
     return bufs.out

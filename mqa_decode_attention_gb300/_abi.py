@@ -70,6 +70,20 @@ _PROTOTYPES = {
         [ctypes.POINTER(KVLayout), c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, ctypes.c_double, ctypes.c_float, c_i32, c_vp,
          c_vp, c_i32, c_vp, c_vp, ctypes.c_size_t, c_i32, c_vp, c_vp],
     ),
+    "kv_append_rope_multi": (
+        c_i32, [ctypes.POINTER(KVLayout), c_i32, c_vp, c_vp, c_vp, c_vp, ctypes.c_double, c_vp, c_vp, c_vp]),
+    "gqa_decode_attention_multi": (
+        c_i32,
+        [ctypes.POINTER(KVLayout), c_i32, c_vp, c_vp, c_i32, ctypes.c_float, c_i32, c_vp, c_i32, c_vp, c_vp,
+         ctypes.c_size_t, c_i32, c_vp, c_vp],
+    ),
+    "mqa_decode_step_multi": (
+        c_i32,
+        [ctypes.POINTER(KVLayout), c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, ctypes.c_double, ctypes.c_float, c_i32,
+         c_vp, c_vp, c_i32, c_vp, c_vp, ctypes.c_size_t, c_i32, c_vp, c_vp],
+    ),
+    "mqa_choose_splits_multi": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32]),
+    "mqa_workspace_size_multi": (ctypes.c_size_t, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32, c_i32]),
     "mqa_choose_splits": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32]),
     "mqa_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32]),
     "mqa_status_string": (ctypes.c_char_p, [c_i32]),

@@ -96,22 +96,30 @@ DeviceInfo device_info(int dev) {
   return d;
 }
 
-KernelShape decode_shape(const mqa_kv_layout* L, int variant) {
+// n_new: query tokens per sequence; a kv head then has G x n_new query rows.
+KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
   const int G = L->h_q / L->h_kv;
   if (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_U8) return decode_u8_shape(L->head_dim, G);
-  if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G);
+  if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G * n_new);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
 }
 
-int head_blocks(const mqa_kv_layout* L, const KernelShape& ks) {
-  const int G = L->h_q / L->h_kv;
-  return (G + ks.heads_per_cta - 1) / ks.heads_per_cta;
+int head_blocks(const mqa_kv_layout* L, const KernelShape& ks, int n_new = 1) {
+  const int rows = (L->h_q / L->h_kv) * n_new;
+  return (rows + ks.heads_per_cta - 1) / ks.heads_per_cta;
+}
+
+constexpr int kMaxNewTokens = 32;
+
+// Multi-token decode runs on the bf16 tensor-core kernel only.
+bool multi_supported(const mqa_kv_layout* L, int variant, int n_new) {
+  return n_new == 1 || (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16);
 }
 
 // Tokens one (sequence, kv head) may need read: the bound, or with a sliding
 // window W the window plus the alignment of its start down to a tile.
-int read_span(const mqa_kv_layout* L, int max_len) {
-  if (L->window > 0 && L->window + kTile < max_len) return L->window + kTile;
+int read_span(const mqa_kv_layout* L, int max_len, int n_new = 1) {
+  if (L->window > 0 && L->window + kTile + n_new - 1 < max_len) return L->window + kTile + n_new - 1;
   return max_len;
 }
 
@@ -122,18 +130,18 @@ int read_span(const mqa_kv_layout* L, int max_len) {
 // a single wave of equal blocks streams best (more, smaller blocks add
 // partial-output traffic and a second wave), and 4096-token chunks balance a
 // paged batch of lengths spread over [128, 16384].
-int choose_splits(const mqa_kv_layout* L, int max_len_in, int variant) {
+int choose_splits(const mqa_kv_layout* L, int max_len_in, int variant, int n_new = 1) {
   const int max_len = read_span(L, max_len_in);
   int dev = 0;
   cudaGetDevice(&dev);
   const DeviceInfo di = device_info(dev);
-  const KernelShape ks = decode_shape(L, variant);
+  const KernelShape ks = decode_shape(L, variant, n_new);
   const int by_smem = ks.smem_bytes > 0 ? di.smem_per_sm / (ks.smem_bytes + 1024) : 8;
   const int by_threads = di.threads_per_sm / ks.threads;
   int per_sm = std::max(1, std::min(by_smem, by_threads));
   if (ks.max_ctas_per_sm > 0) per_sm = std::min(per_sm, ks.max_ctas_per_sm);
   const long long slots = static_cast<long long>(di.sms) * per_sm;
-  const long long units = static_cast<long long>(L->batch) * L->h_kv * head_blocks(L, ks);
+  const long long units = static_cast<long long>(L->batch) * L->h_kv * head_blocks(L, ks, n_new);
   const int tiles = (max_len + kTile - 1) / kTile;
   int s = 1;
   if (L->paged) {
@@ -153,9 +161,9 @@ void split_plan(int requested, int max_len, int* splits, int* chunk) {
   *splits = (max_len + c - 1) / c;
 }
 
-size_t partial_bytes(const mqa_kv_layout* L, int splits) {
+size_t partial_bytes(const mqa_kv_layout* L, int splits, int n_new = 1) {
   if (splits <= 1) return 0;
-  const size_t rows = static_cast<size_t>(L->batch) * L->h_q;
+  const size_t rows = static_cast<size_t>(L->batch) * n_new * L->h_q;
   const size_t o_bytes = ((rows * splits * L->head_dim * 4) + 255) / 256 * 256;
   return o_bytes + rows * splits * 4;
 }
@@ -334,11 +342,14 @@ mqa_status check_append_args(const mqa_kv_layout* layout, const void* q_new, con
 }
 
 mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
-                       const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word, mqa_stream_t stream) {
+                       const int32_t* pos, double rope_base, float* q_rot, int32_t* err_word, mqa_stream_t stream,
+                       int n_new = 1) {
   const mqa_status st = check_append_args(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word);
   if (st != MQA_OK) return st;
+  if (n_new < 1 || n_new > kMaxNewTokens) return MQA_ERR_INVALID_ARG;
   AppendParams p;
   std::memset(&p, 0, sizeof(p));
+  p.n_new = n_new;
   p.batch = layout->batch;
   p.h_q = layout->h_q;
   p.h_kv = layout->h_kv;
@@ -390,32 +401,34 @@ bool fusable(const mqa_kv_layout* L, int variant) {
 mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens, int32_t max_seq_len,
                           float scale, int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
                           void* workspace, size_t workspace_bytes, int32_t variant, int32_t* err_word,
-                          mqa_stream_t stream, int early, const RopeArgs* rope) {
+                          mqa_stream_t stream, int early, const RopeArgs* rope, int n_new = 1) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
+  if (n_new < 1 || n_new > kMaxNewTokens) return MQA_ERR_INVALID_ARG;
   if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
   if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
       (lse_out && !aligned(lse_out, 4)))
     return MQA_ERR_INVALID_ARG;
-  if (max_seq_len < 1 || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || num_splits < 0) return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return MQA_ERR_INVALID_ARG;
   const int v = resolve_variant(layout, variant);
-  if (!variant_supports(v, layout->cache_dtype)) return MQA_ERR_UNSUPPORTED;
+  if (!variant_supports(v, layout->cache_dtype) || !multi_supported(layout, v, n_new)) return MQA_ERR_UNSUPPORTED;
 
-  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v, n_new) : num_splits;
   int splits, chunk;
-  split_plan(req, read_span(layout, max_seq_len), &splits, &chunk);
-  const size_t need = partial_bytes(layout, splits);
+  split_plan(req, read_span(layout, max_seq_len, n_new), &splits, &chunk);
+  const size_t need = partial_bytes(layout, splits, n_new);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return MQA_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return MQA_ERR_INVALID_ARG;
   }
 
-  const KernelShape ks = decode_shape(layout, v);
+  const KernelShape ks = decode_shape(layout, v, n_new);
   DecodeParams p;
   std::memset(&p, 0, sizeof(p));
+  p.n_new = n_new;
   p.batch = layout->batch;
   p.h_q = layout->h_q;
   p.h_kv = layout->h_kv;
@@ -438,10 +451,10 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_splits = splits;
   p.chunk = chunk;
-  p.head_blocks = head_blocks(layout, ks);
+  p.head_blocks = head_blocks(layout, ks, n_new);
   p.window = layout->window;
   p.early = early;
-  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_BF16) {
+  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_BF16 && n_new == 1) {
     p.rope_q = 1;
     p.q_new = rope->q_new;
     p.pos = rope->pos;
@@ -459,7 +472,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.lse_out = lse_out;
   p.err = err_word;
   if (splits > 1) {
-    const size_t rows = static_cast<size_t>(layout->batch) * layout->h_q;
+    const size_t rows = static_cast<size_t>(layout->batch) * n_new * layout->h_q;
     const size_t o_bytes = ((rows * splits * layout->head_dim * 4) + 255) / 256 * 256;
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + o_bytes);
@@ -507,7 +520,7 @@ combine:
     CombineParams c;
     c.o_part = p.o_part;
     c.lse_part = p.lse_part;
-    c.rows = layout->batch * layout->h_q;
+    c.rows = layout->batch * n_new * layout->h_q;
     c.num_splits = splits;
     c.head_dim = layout->head_dim;
     c.out = out;
@@ -543,21 +556,32 @@ mqa_status kv_append_rope(const mqa_kv_layout* layout, const void* q_new, const 
   return append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream);
 }
 
-int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant) {
+int32_t mqa_choose_splits_multi(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len, int32_t variant) {
   if (check_layout(layout) != MQA_OK || max_seq_len < 1 || max_seq_len > token_limit(layout)) return -1;
   if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return -1;
-  return choose_splits(layout, max_seq_len, resolve_variant(layout, variant));
+  if (n_new < 1 || n_new > kMaxNewTokens || max_seq_len < n_new) return -1;
+  return choose_splits(layout, max_seq_len, resolve_variant(layout, variant), n_new);
 }
 
-size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t num_splits, int32_t variant) {
+int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t variant) {
+  return mqa_choose_splits_multi(layout, 1, max_seq_len, variant);
+}
+
+size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len, int32_t num_splits,
+                                int32_t variant) {
   if (check_layout(layout) != MQA_OK || max_seq_len < 1 || max_seq_len > token_limit(layout) || num_splits < 0)
     return 0;
   if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return 0;
+  if (n_new < 1 || n_new > kMaxNewTokens || max_seq_len < n_new) return 0;
   const int v = resolve_variant(layout, variant);
-  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v, n_new) : num_splits;
   int splits, chunk;
-  split_plan(req, read_span(layout, max_seq_len), &splits, &chunk);
-  return partial_bytes(layout, splits);
+  split_plan(req, read_span(layout, max_seq_len, n_new), &splits, &chunk);
+  return partial_bytes(layout, splits, n_new);
+}
+
+size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t num_splits, int32_t variant) {
+  return mqa_workspace_size_multi(layout, 1, max_seq_len, num_splits, variant);
 }
 
 mqa_status splitkv_combine(const float* o_part, const float* lse_part, int32_t batch, int32_t h_q,
@@ -592,40 +616,81 @@ mqa_status gqa_decode_attention(const mqa_kv_layout* layout, const float* q_rot,
                         workspace_bytes, variant, err_word, stream, /*early=*/0, /*rope=*/nullptr);
 }
 
-mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
-                           const int32_t* pos, const int32_t* seq_lens, int32_t max_seq_len, double rope_base,
-                           float scale, int32_t num_splits, float* q_rot, void* out, int32_t out_dtype,
-                           float* lse_out, void* workspace, size_t workspace_bytes, int32_t variant,
-                           int32_t* err_word, mqa_stream_t stream) {
+mqa_status kv_append_rope_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new, const void* k_new,
+                                const void* v_new, const int32_t* pos, double rope_base, float* q_rot,
+                                int32_t* err_word, mqa_stream_t stream) {
+  return append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);
+}
+
+mqa_status gqa_decode_attention_multi(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,
+                                      const int32_t* seq_lens, int32_t max_seq_len, float scale, int32_t num_splits,
+                                      void* out, int32_t out_dtype, float* lse_out, void* workspace,
+                                      size_t workspace_bytes, int32_t variant, int32_t* err_word,
+                                      mqa_stream_t stream) {
+  return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out, workspace,
+                        workspace_bytes, variant, err_word, stream, /*early=*/0, /*rope=*/nullptr, n_new);
+}
+
+}  // extern "C"
+
+namespace {
+
+mqa_status step_impl(const mqa_kv_layout* layout, int n_new, const void* q_new, const void* k_new, const void* v_new,
+                     const int32_t* pos, const int32_t* seq_lens, int32_t max_seq_len, double rope_base, float scale,
+                     int32_t num_splits, float* q_rot, void* out, int32_t out_dtype, float* lse_out, void* workspace,
+                     size_t workspace_bytes, int32_t variant, int32_t* err_word, mqa_stream_t stream) {
   // Check the attention's arguments too before anything is launched.
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if (!seq_lens || !out || max_seq_len < 1 || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (n_new < 1 || n_new > kMaxNewTokens) return MQA_ERR_INVALID_ARG;
+  if (!seq_lens || !out || max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
   if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE || num_splits < 0)
     return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   const int v = resolve_variant(layout, variant);
-  if (!variant_supports(v, layout->cache_dtype)) return MQA_ERR_UNSUPPORTED;
+  if (!variant_supports(v, layout->cache_dtype) || !multi_supported(layout, v, n_new)) return MQA_ERR_UNSUPPORTED;
   {
-    const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v) : num_splits;
+    const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v, n_new) : num_splits;
     int splits, chunk;
-    split_plan(req, read_span(layout, max_seq_len), &splits, &chunk);
-    const size_t need = partial_bytes(layout, splits);
+    split_plan(req, read_span(layout, max_seq_len, n_new), &splits, &chunk);
+    const size_t need = partial_bytes(layout, splits, n_new);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MQA_ERR_WORKSPACE;
   }
   const mqa_status ca = check_append_args(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word);
   if (ca != MQA_OK) return ca;
-  if (fusable(layout, v)) {
+  if (n_new == 1 && fusable(layout, v)) {
     // one launch: the attention kernel appends the new token itself
     const RopeArgs rope{q_new, pos, rope_base, 1, k_new, v_new, q_rot};
     return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out,
                           workspace, workspace_bytes, variant, err_word, stream, /*early=*/0, &rope);
   }
-  const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream);
+  const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);
   if (a != MQA_OK) return a;
   const RopeArgs rope{q_new, pos, rope_base, 0, nullptr, nullptr, nullptr};
   return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out, workspace,
-                        workspace_bytes, variant, err_word, stream, /*early=*/1, &rope);
+                        workspace_bytes, variant, err_word, stream, /*early=*/1, &rope, n_new);
+}
+
+}  // namespace
+
+extern "C" {
+
+mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const void* k_new, const void* v_new,
+                           const int32_t* pos, const int32_t* seq_lens, int32_t max_seq_len, double rope_base,
+                           float scale, int32_t num_splits, float* q_rot, void* out, int32_t out_dtype,
+                           float* lse_out, void* workspace, size_t workspace_bytes, int32_t variant,
+                           int32_t* err_word, mqa_stream_t stream) {
+  return step_impl(layout, 1, q_new, k_new, v_new, pos, seq_lens, max_seq_len, rope_base, scale, num_splits, q_rot,
+                   out, out_dtype, lse_out, workspace, workspace_bytes, variant, err_word, stream);
+}
+
+mqa_status mqa_decode_step_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new, const void* k_new,
+                                 const void* v_new, const int32_t* pos, const int32_t* seq_lens, int32_t max_seq_len,
+                                 double rope_base, float scale, int32_t num_splits, float* q_rot, void* out,
+                                 int32_t out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                                 int32_t variant, int32_t* err_word, mqa_stream_t stream) {
+  return step_impl(layout, n_new, q_new, k_new, v_new, pos, seq_lens, max_seq_len, rope_base, scale, num_splits,
+                   q_rot, out, out_dtype, lse_out, workspace, workspace_bytes, variant, err_word, stream);
 }
 
 }  // extern "C"

@@ -89,12 +89,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   // before it reads q_rot or the appended slot.
   grid_dependents_launch();
 
-  const int b = blockIdx.x;
+  const int bt = blockIdx.x;  // (sequence, new token) = b * n_new + token
+  const int b = bt / p.n_new;
   const int D = p.head_dim;
   const int half = D >> 1;
   const int n_qblocks = (p.h_q + kQHeadsPerBlock - 1) / kQHeadsPerBlock;
   const bool kv_block = static_cast<int>(blockIdx.y) >= n_qblocks;
-  const int pos = p.pos[b];
+  const int pos = p.pos[b] + (bt - b * p.n_new);
 
   // Issue this thread's loads first (at most 2 pairs per thread).
   int h_begin, h_end;
@@ -106,8 +107,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
     h_end = min(h_begin + kKvHeadsPerBlock, p.h_kv);
   }
   const int n_pairs = (h_end - h_begin) * half;
-  const T* src = kv_block ? static_cast<const T*>(p.k_new) + static_cast<long long>(b) * p.h_kv * D
-                          : static_cast<const T*>(p.q_new) + static_cast<long long>(b) * p.h_q * D;
+  const T* src = kv_block ? static_cast<const T*>(p.k_new) + static_cast<long long>(bt) * p.h_kv * D
+                          : static_cast<const T*>(p.q_new) + static_cast<long long>(bt) * p.h_q * D;
   float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
   const int i0 = threadIdx.x, i1 = threadIdx.x + kAppendThreads;
   if (i0 < n_pairs) x0 = Elem<T>::load2(src + (h_begin + i0 / half) * D + 2 * (i0 % half));
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 
   if (!kv_block) {
     // q: fp32 rotation, fp32 output
-    float* qr = p.q_rot + static_cast<long long>(b) * p.h_q * D;
+    float* qr = p.q_rot + static_cast<long long>(bt) * p.h_q * D;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int idx = u == 0 ? i0 : i1;
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 
   if constexpr (QU8) {
     // k: fp64 rotation rounded to fp32, then both rows quantised; one pair per thread
-    const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(b) * p.h_kv * D;
+    const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
     const bool act = i0 < n_pairs;
     const int hl = act ? i0 / half : 0, i = i0 % half;
     float kx = 0.f, ky = 0.f, vx = 0.f, vy = 0.f;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
 
   // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
-  const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(b) * p.h_kv * D;
+  const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
   T* kc = static_cast<T*>(p.k_cache) + s_row;
   T* vc = static_cast<T*>(p.v_cache) + s_row;
   const long long stride = s_stride;
@@ -245,7 +246,7 @@ KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.batch, (p.h_q + kQHeadsPerBlock - 1) / kQHeadsPerBlock +
+  cfg.gridDim = dim3(p.batch * p.n_new, (p.h_q + kQHeadsPerBlock - 1) / kQHeadsPerBlock +
                                   (p.h_kv + kKvHeadsPerBlock - 1) / kKvHeadsPerBlock);
   cfg.blockDim = dim3(kAppendThreads);
   cfg.dynamicSmemBytes = 0;

@@ -51,7 +51,10 @@ struct MmaCfg {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
-template <int D, int HB, int STAGES>
+// MULTI: n_new > 1 query tokens per sequence (the verification pass of
+// speculative decoding): the rows of a kv head are (new token i, query head
+// h) pairs, row = i G + h, and row i sees tokens [.., L - n + i] only.
+template <int D, int HB, int STAGES, bool MULTI>
 __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const DecodeParams p) {
@@ -75,6 +78,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   const int j = cta % p.h_kv;
   const int b = cta / p.h_kv;
   const int G = p.group;
+  const int nq = MULTI ? p.n_new : 1;  // new tokens (query rows per head) of each sequence
+  const int R = G * nq;                // query rows of this kv head
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -98,12 +103,13 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;
   if (limit > p.max_seq_len) limit = p.max_seq_len;
   int L = p.seq_lens[b];
-  if (L < 1 || L > limit) {
+  if (L < nq || L > limit) {
     if (threadIdx.x == 0 && split == 0 && hsb == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
-    L = L < 0 ? 0 : static_cast<int>(L > limit ? limit : L);
+    L = L < nq ? (L < 0 ? 0 : L) : static_cast<int>(limit);
   }
-  // sliding window: tokens [t_lo, L); splits start at t_lo rounded down to a tile
-  const int t_lo = p.window > 0 ? max(0, L - p.window) : 0;
+  // sliding window: tokens [t_lo, L) (t_lo of the first new token, the lowest);
+  // splits start at t_lo rounded down to a tile
+  const int t_lo = p.window > 0 ? max(0, L - nq + 1 - p.window) : 0;
   const int t_base = (t_lo / kTile) * kTile;
   const int t_begin = t_base + split * p.chunk;
   const int t_end = min(L, t_begin + p.chunk);
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       }
       if (*reinterpret_cast<volatile int*>(&s_abort)) break;
       const int t0 = t_begin + it * kTile;
-      if (!waited && L - 1 < t0 + kTile) {  // this tile holds the appended token
+      if (!waited && L - nq < t0 + kTile) {  // this tile holds an appended token
         grid_dependency_wait();
         waited = true;
       }
@@ -236,9 +242,27 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     const long long qoff = (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
     wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G - head0, s_cs, p.scale_log2, lane,
                  (p.fuse_append && split == 0 && ws == 0) ? p.q_rot_out + qoff : nullptr);
+  } else if (MULTI) {
+    if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
+    auto qrow = [&](int r) -> const float* {
+      if (r >= R) return nullptr;
+      const int i = r / G;
+      return p.q_rot + ((static_cast<long long>(b) * nq + i) * p.h_q + j * G + (r - i * G)) * D;
+    };
+    wa.init2(qrow(head0 + r0), qrow(head0 + r0 + 8), p.scale_log2, lane);
   } else {
     if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
     wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
+  }
+  // MULTI: the key range [ka, ke) of this lane's rows r0 and r0 + 8 (row of
+  // new token i: ends after position L - nq + i; a window of W before that)
+  int ka0 = 0, ke0 = L, ka1 = 0, ke1 = L;
+  if (MULTI) {
+    const int i0 = min(head0 + r0, R - 1) / G, i1 = min(head0 + r0 + 8, R - 1) / G;
+    ke0 = L - nq + i0 + 1;
+    ke1 = L - nq + i1 + 1;
+    ka0 = p.window > 0 ? max(0, ke0 - p.window) : 0;
+    ka1 = p.window > 0 ? max(0, ke1 - p.window) : 0;
   }
 
   bool ok = true;
@@ -261,7 +285,14 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     const int lo = max(0, t_lo - tt), hi = min(16, t_end - tt);
     if (lo < hi) {
       unsigned char* ktile = smem + stage * C::kStageBytes;
-      wa.step(smem_u32(ktile), smem_u32(ktile + C::kTileBytes), ktile + C::kTileBytes, trow0, lo, hi, lg_rpb, lane);
+      if constexpr (MULTI) {
+        wa.template step<true>(smem_u32(ktile), smem_u32(ktile + C::kTileBytes), ktile + C::kTileBytes, trow0, lo,
+                               hi, lg_rpb, lane, max(0, ka0 - tt), min(16, min(ke0, t_end) - tt), max(0, ka1 - tt),
+                               min(16, min(ke1, t_end) - tt));
+      } else {
+        wa.step(smem_u32(ktile), smem_u32(ktile + C::kTileBytes), ktile + C::kTileBytes, trow0, lo, hi, lg_rpb,
+                lane);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
@@ -294,7 +325,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   const int tid = threadIdx.x;
   for (int hbi = 0; hbi < HB; ++hbi) {
     const int hh0 = (hsb * HB + hbi) * 16;
-    const int n_rows = min(16, G - hh0);
+    const int n_rows = min(16, R - hh0);
     for (int idx = tid; idx < n_rows * D; idx += C::kConsumerThreads) {
       const int r = idx / D, d = idx - r * D;
       float mx = -INFINITY;
@@ -312,7 +343,11 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       }
       const float ov = den > 0.f ? num / den : 0.f;
       const float lse = den > 0.f ? (mx + log2f(den)) * 0.69314718055994530942f : -INFINITY;
-      const long long grow = static_cast<long long>(b) * p.h_q + j * G + hh0 + r;
+      long long grow = static_cast<long long>(b) * p.h_q + j * G + hh0 + r;  // output row [B, (n,) H_q]
+      if (MULTI) {
+        const int i = (hh0 + r) / G;
+        grow = (static_cast<long long>(b) * nq + i) * p.h_q + j * G + (hh0 + r - i * G);
+      }
       if (split_out) {
         p.o_part[(grow * S + split) * D + d] = ov;
         if (d == 0) p.lse_part[grow * S + split] = lse;
@@ -332,11 +367,11 @@ constexpr int mma_stages() {
   return D == 128 ? MQA_MMA_STAGES_D128 : MQA_MMA_STAGES_D64;
 }
 
-template <int D, int HB>
+template <int D, int HB, bool MULTI>
 cudaError_t launch_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   constexpr int ST = mma_stages<D, HB>();
   using C = MmaCfg<D, HB, ST>;
-  auto kern = decode_mma_kernel<D, HB, ST>;
+  auto kern = decode_mma_kernel<D, HB, ST, MULTI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -355,12 +390,20 @@ cudaError_t launch_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUt
 #ifndef MQA_MMA_MAX_HB
 #define MQA_MMA_MAX_HB 2
 #endif
-int mma_hb(int group) { return (group > 16 && MQA_MMA_MAX_HB >= 2) ? 2 : 1; }
+int mma_hb(int rows) { return (rows > 16 && MQA_MMA_MAX_HB >= 2) ? 2 : 1; }
+
+template <bool MULTI>
+cudaError_t launch_mma_m(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  const int hb = mma_hb(p.group * (MULTI ? p.n_new : 1));
+  if (p.head_dim == 128)
+    return hb == 2 ? launch_mma_t<128, 2, MULTI>(p, tk, tv, stream) : launch_mma_t<128, 1, MULTI>(p, tk, tv, stream);
+  return hb == 2 ? launch_mma_t<64, 2, MULTI>(p, tk, tv, stream) : launch_mma_t<64, 1, MULTI>(p, tk, tv, stream);
+}
 
 }  // namespace
 
-KernelShape decode_mma_shape(int head_dim, int group) {
-  const int hb = mma_hb(group);
+KernelShape decode_mma_shape(int head_dim, int rows) {
+  const int hb = mma_hb(rows);
   if (head_dim == 128) {
     if (hb == 2) {
       using C = MmaCfg<128, 2, mma_stages<128, 2>()>;
@@ -379,9 +422,7 @@ KernelShape decode_mma_shape(int head_dim, int group) {
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                               cudaStream_t stream) {
-  const int hb = mma_hb(p.group);
-  if (p.head_dim == 128) return hb == 2 ? launch_mma_t<128, 2>(p, tk, tv, stream) : launch_mma_t<128, 1>(p, tk, tv, stream);
-  return hb == 2 ? launch_mma_t<64, 2>(p, tk, tv, stream) : launch_mma_t<64, 1>(p, tk, tv, stream);
+  return p.n_new > 1 ? launch_mma_m<true>(p, tk, tv, stream) : launch_mma_m<false>(p, tk, tv, stream);
 }
 
 }  // namespace mqa

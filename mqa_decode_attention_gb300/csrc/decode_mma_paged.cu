@@ -253,7 +253,7 @@ cudaError_t launch_heads_t(const DecodeParams& p, const CUtensorMap& tk, const C
 }  // namespace
 
 int decode_mma_heads_group(const DecodeParams& p) {
-  if (!p.paged || p.page_size != kPage || p.head_dim != 128 || p.group > 16) return 0;
+  if (!p.paged || p.page_size != kPage || p.head_dim != 128 || p.group > 16 || p.n_new > 1) return 0;
   if (p.h_kv % 4 == 0) return 4;
   if (p.h_kv % 2 == 0) return 2;
   return 0;

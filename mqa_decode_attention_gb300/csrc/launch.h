@@ -15,6 +15,7 @@ constexpr int kDtypeU8 = 2;  // cache only: uint8 codes + float2 (scale, zero po
 
 struct AppendParams {
   int batch, h_q, h_kv, head_dim, cache_dtype, paged;
+  int n_new;  // new tokens per sequence: token i at position pos[b] + i; q/k/v_new, q_rot [B, n_new, H, d]
   const void* q_new;
   const void* k_new;
   const void* v_new;
@@ -33,6 +34,7 @@ struct AppendParams {
 
 struct DecodeParams {
   int batch, h_q, h_kv, group, head_dim, cache_dtype, paged;
+  int n_new;  // query tokens per sequence (the last n_new of its L); rows of a kv head = group * n_new
   const void* k_cache;
   const void* v_cache;
   long long capacity;
@@ -90,7 +92,8 @@ cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream);
 KernelShape decode_fma_shape(int cache_dtype, int head_dim, int group);
 cudaError_t launch_decode_fma(const DecodeParams& p, cudaStream_t stream);
 
-KernelShape decode_mma_shape(int head_dim, int group);
+// rows = query rows per kv head (group x new tokens)
+KernelShape decode_mma_shape(int head_dim, int rows);
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                               cudaStream_t stream);
 

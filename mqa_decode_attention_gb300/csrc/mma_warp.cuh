@@ -116,15 +116,23 @@ struct WarpAttn {
   // q points at row 0 of this warp's 16 query heads ([16][D] fp32, row stride D);
   // rows >= rows_valid are padding and read as zero.
   __device__ __forceinline__ void init(const float* q, int rows_valid, float scale_log2, int lane) {
-    const int r0 = lane >> 2, c2 = (lane & 3) * 2;
+    const int r0 = lane >> 2;
+    init2(r0 < rows_valid ? q + r0 * D : nullptr, r0 + 8 < rows_valid ? q + (r0 + 8) * D : nullptr, scale_log2,
+          lane);
+  }
+
+  // The same with the lane's two rows given directly: q0 is row r0 = lane / 4
+  // of the warp's 16, q1 row r0 + 8 (each fp32 [D], or null for padding).
+  __device__ __forceinline__ void init2(const float* q0, const float* q1, float scale_log2, int lane) {
+    const int c2 = (lane & 3) * 2;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
       for (int part = 0; part < 4; ++part) {
-        const int row = r0 + ((part & 1) ? 8 : 0);
+        const float* q = (part & 1) ? q1 : q0;
         const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
         float2 v = make_float2(0.f, 0.f);
-        if (row < rows_valid) v = *reinterpret_cast<const float2*>(q + row * D + col);
+        if (q != nullptr) v = *reinterpret_cast<const float2*>(q + col);
         qa[ks][part] = pack_bf16x2(v.x * scale_log2, v.y * scale_log2);
       }
     }
@@ -138,9 +146,16 @@ struct WarpAttn {
   // only rows lo .. hi-1 of these 16 are real tokens (0 <= lo < hi <= 16).
   // vtile is the generic pointer of the V tile: the other rows may hold
   // anything (even NaN bit patterns) and are zeroed so that P = 0 contributes
-  // exactly nothing.
+  // exactly nothing. With PER_ROW, the query rows r0 and r0 + 8 of this lane
+  // see only tokens [lo0, hi0) and [lo1, hi1) of the 16 (inside [lo, hi));
+  // a row may then see none of them, and the softmax update stays finite.
+  template <bool PER_ROW = false>
   __device__ __forceinline__ void step(uint32_t kb, uint32_t vb, unsigned char* vtile, int trow0, int lo, int hi,
-                                       int lg_rpb, int lane) {
+                                       int lg_rpb, int lane, int lo0 = 0, int hi0 = 0, int lo1 = 0, int hi1 = 0) {
+    if constexpr (!PER_ROW) {
+      lo0 = lo1 = lo;
+      hi0 = hi1 = hi;
+    }
     const int c2 = (lane & 3) * 2;
     if (lo > 0 || hi < 16) {
       const int n_bad = 16 - (hi - lo);
@@ -184,10 +199,8 @@ struct WarpAttn {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r = nt * 8 + c2 + e;
-        if (r < lo || r >= hi) {
-          s[nt][e] = -INFINITY;
-          s[nt][2 + e] = -INFINITY;
-        }
+        if (r < lo0 || r >= hi0) s[nt][e] = -INFINITY;
+        if (r < lo1 || r >= hi1) s[nt][2 + e] = -INFINITY;
       }
     }
     float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
@@ -197,18 +210,22 @@ struct WarpAttn {
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    // mn is finite: at least one of the 16 tokens is valid (lo < hi)
+    // Without PER_ROW, mn is finite: at least one of the 16 tokens is valid
+    // (lo < hi). With it, a row that has seen no token yet keeps -inf, and
+    // its exponentials use 0 in place of the max (2^-inf = 0, no inf - inf).
     const bool moved = (mn0 != m0) || (mn1 != m1);
-    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+    const float e0 = (PER_ROW && mn0 == -INFINITY) ? 0.f : mn0;
+    const float e1 = (PER_ROW && mn1 == -INFINITY) ? 0.f : mn1;
+    const float a0 = fast_exp2(m0 - e0), a1 = fast_exp2(m1 - e1);
     m0 = mn0;
     m1 = mn1;
     float pr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = fast_exp2(s[nt][0] - mn0);
-      pr[nt][1] = fast_exp2(s[nt][1] - mn0);
-      pr[nt][2] = fast_exp2(s[nt][2] - mn1);
-      pr[nt][3] = fast_exp2(s[nt][3] - mn1);
+      pr[nt][0] = fast_exp2(s[nt][0] - e0);
+      pr[nt][1] = fast_exp2(s[nt][1] - e0);
+      pr[nt][2] = fast_exp2(s[nt][2] - e1);
+      pr[nt][3] = fast_exp2(s[nt][3] - e1);
     }
     l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
     l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
