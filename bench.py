@@ -41,7 +41,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from synthetic import make_contiguous_case, make_paged_case, make_u8_cache, workload  # noqa: E402
+from synthetic import make_contiguous_case, make_paged_case, make_u8_cache, normal, workload  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 GPU"
 UNIT = "GB/s"
@@ -108,9 +108,10 @@ def ncu_traffic(workload_name: str):
     return None
 
 
-def attended(lens, window: int):
-    """Tokens each sequence's query reads: all L, or the last `window`."""
-    return lens.clamp(max=window) if window > 0 else lens
+def attended(lens, window: int, n_new: int = 1):
+    """Tokens each sequence's queries read: all L, or with a window the last
+    `window` tokens of each of its n_new queries (their union)."""
+    return lens.clamp(max=window + n_new - 1) if window > 0 else lens
 
 
 def row_bytes(w, cache: str) -> int:
@@ -119,26 +120,28 @@ def row_bytes(w, cache: str) -> int:
     return w.head_dim + 8 if cache == "u8" else w.head_dim * w.esize
 
 
-def step_bytes(w, lens, out_esize, window: int = 0, cache: str = "native"):
+def step_bytes(w, lens, out_esize, window: int = 0, cache: str = "native", n_new: int = 1):
     """Algorithmic bytes of one step: every attended K/V byte read once
-    (including the new token), q_new read, out written, k_new/v_new read and
-    their slot written, and (paged) the block-table entries used."""
+    (including the new tokens; once for all n_new queries of a sequence),
+    q_new read, out written, k_new/v_new read and their slots written, and
+    (paged) the block-table entries used."""
     es = w.esize  # q_new / k_new / v_new
-    kv = 2 * int(attended(lens, window).sum()) * w.h_kv * row_bytes(w, cache)
-    q = w.batch * w.h_q * w.head_dim * es
-    out = w.batch * w.h_q * w.head_dim * out_esize
-    append = 2 * w.batch * w.h_kv * (w.head_dim * es + row_bytes(w, cache))
-    table = 4 * int(((attended(lens, window) + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
+    att = attended(lens, window, n_new)
+    kv = 2 * int(att.sum()) * w.h_kv * row_bytes(w, cache)
+    q = n_new * w.batch * w.h_q * w.head_dim * es
+    out = n_new * w.batch * w.h_q * w.head_dim * out_esize
+    append = 2 * n_new * w.batch * w.h_kv * (w.head_dim * es + row_bytes(w, cache))
+    table = 4 * int(((att + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
     return kv + q + out + append + table
 
 
-def attention_bytes(w, lens, out_esize, window: int = 0, cache: str = "native"):
+def attention_bytes(w, lens, out_esize, window: int = 0, cache: str = "native", n_new: int = 1):
     """Algorithmic bytes of one gqa_decode_attention launch: K/V of every
     attended token, q_rot (fp32) read, out written, block-table entries (paged)."""
-    lens = attended(lens, window)
+    lens = attended(lens, window, n_new)
     kv = 2 * int(lens.sum()) * w.h_kv * row_bytes(w, cache)
-    q = w.batch * w.h_q * w.head_dim * 4
-    out = w.batch * w.h_q * w.head_dim * out_esize
+    q = n_new * w.batch * w.h_q * w.head_dim * 4
+    out = n_new * w.batch * w.h_q * w.head_dim * out_esize
     table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.paged else 0
     return kv + q + out + table
 
@@ -211,12 +214,22 @@ def gpu_index_for(local_rank: int) -> str:
 U8_SEED = 77
 
 
-def build_case(w, device, cache: str = "native"):
+S_QM, S_KM, S_VM = 21, 22, 23  # seeded streams of multi-token q, k, v
+
+
+def build_case(w, device, cache: str = "native", n_new: int = 1):
     """The workload's seeded inputs. With cache "u8" the K/V caches are
     replaced by uint8 codes and (scale, zero point) pairs of the same rows
-    (attributes u8 = synthetic.U8Cache)."""
+    (attributes u8 = synthetic.U8Cache). With n_new > 1 the new tokens are
+    [B, n_new, H, d] and pos = seq_lens - n_new."""
     case = make_paged_case(w, device) if w.paged else make_contiguous_case(w, device)
     case.u8 = None
+    case.n_new = n_new
+    if n_new > 1:
+        case.q_new = normal((w.batch, n_new, w.h_q, w.head_dim), w.seed, S_QM, w.dtype, device)
+        case.k_new = normal((w.batch, n_new, w.h_kv, w.head_dim), w.seed, S_KM, w.dtype, device)
+        case.v_new = normal((w.batch, n_new, w.h_kv, w.head_dim), w.seed, S_VM, w.dtype, device)
+        case.pos = (case.seq_lens - n_new).to(torch.int32)
     if cache == "u8":
         if w.paged:
             rows = (case.num_pages, w.h_kv, case.page_size)
@@ -244,8 +257,12 @@ def unit_inputs(w, case, units):
     lens = case.seq_lens.cpu()
     for b, j in units:
         L = int(lens[b])
-        u = dict(b=b, j=j, L=L, q=case.q_new[b, j * G:(j + 1) * G].cpu(), k=case.k_new[b, j].cpu(),
-                 v=case.v_new[b, j].cpu())
+        if case.n_new > 1:  # [n, G, d] queries, [n, d] k / v of the unit
+            u = dict(b=b, j=j, L=L, q=case.q_new[b, :, j * G:(j + 1) * G].cpu(), k=case.k_new[b, :, j].cpu(),
+                     v=case.v_new[b, :, j].cpu(), n=case.n_new)
+        else:
+            u = dict(b=b, j=j, L=L, q=case.q_new[b, j * G:(j + 1) * G].cpu(), k=case.k_new[b, j].cpu(),
+                     v=case.v_new[b, j].cpu(), n=1)
         if case.u8 is not None:
             c = case.u8
             u.update(Kc=_rows(w, case, c.k_codes, b, j, L), Ks=_rows(w, case, c.k_sz, b, j, L),
@@ -257,10 +274,10 @@ def unit_inputs(w, case, units):
     return out
 
 
-def unit_bytes(w, L, out_esize, cache: str = "native"):
+def unit_bytes(w, L, out_esize, cache: str = "native", n_new: int = 1):
     es = w.esize
-    return (2 * L * row_bytes(w, cache) + w.group * w.head_dim * (es + out_esize)
-            + 2 * (w.head_dim * es + row_bytes(w, cache)))
+    return (2 * L * row_bytes(w, cache) + n_new * w.group * w.head_dim * (es + out_esize)
+            + 2 * n_new * (w.head_dim * es + row_bytes(w, cache)))
 
 
 def oracle_unit(w, u, window: int = 0):
@@ -273,6 +290,10 @@ def oracle_unit(w, u, window: int = 0):
         r = oracle.decode_step_u8(u["Kc"][None, None], u["Ks"][None, None], u["Vc"][None, None], u["Vs"][None, None],
                                   u["q"][None], u["k"][None, None], u["v"][None, None], [L], w.rope_base, scale,
                                   window=window)
+        return r["out"][0]
+    if u["n"] > 1:
+        r = oracle.decode_step_multi(u["K"][None, None], u["V"][None, None], u["q"][None], u["k"][None, :, None],
+                                     u["v"][None, :, None], [u["L"]], w.rope_base, scale, w.dtype, window=window)
         return r["out"][0]
     o, _, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype,
                                  window=window)
@@ -316,7 +337,8 @@ def bench_ours(args):
     if args.batch:
         w = w.with_(batch=args.batch)
     u8 = args.cache == "u8"
-    case = build_case(w, dev, args.cache)
+    nn = args.n_new
+    case = build_case(w, dev, args.cache, nn)
     lens_cpu = case.seq_lens.cpu()
     max_len = int(lens_cpu.max())
     if u8:
@@ -332,12 +354,12 @@ def bench_ours(args):
     else:
         lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q, window=args.window)
     variant = args.variant
-    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=w.num_splits, variant=variant, device=dev)
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=w.num_splits, variant=variant, device=dev, n_new=nn)
     scale = 1.0 / math.sqrt(w.head_dim)
-    splits_used = w.num_splits if w.num_splits > 0 else m.choose_splits(lay, max_len, variant)
+    splits_used = w.num_splits if w.num_splits > 0 else m.choose_splits(lay, max_len, variant, nn)
     out_es = bufs.out.element_size()
-    sbytes = step_bytes(w, lens_cpu, out_es, args.window, args.cache)
-    abytes = attention_bytes(w, lens_cpu, out_es, args.window, args.cache)
+    sbytes = step_bytes(w, lens_cpu, out_es, args.window, args.cache, nn)
+    abytes = attention_bytes(w, lens_cpu, out_es, args.window, args.cache, nn)
     stream = torch.cuda.current_stream()
 
     # CPU-baseline units (rank 0, N = 1), copied before any step touches the cache
@@ -349,17 +371,23 @@ def bench_ours(args):
         units = unit_inputs(w, case, [(u // w.h_kv, u % w.h_kv) for u in perm[:args.cpu_units or len(perm)]])
 
     def append():
-        m.kv_append_rope(lay, case.q_new, case.k_new, case.v_new, case.pos, w.rope_base, bufs.q_rot, bufs.err, stream)
+        m.kv_append_rope_multi(lay, nn, case.q_new, case.k_new, case.v_new, case.pos, w.rope_base, bufs.q_rot,
+                               bufs.err, stream)
 
     def attend():
-        m.gqa_decode_attention(lay, bufs.q_rot, case.seq_lens, max_len, scale, w.num_splits, bufs.out, bufs.lse,
-                               bufs.workspace, variant, bufs.err, stream)
+        m.gqa_decode_attention_multi(lay, nn, bufs.q_rot, case.seq_lens, max_len, scale, w.num_splits, bufs.out,
+                                     bufs.lse, bufs.workspace, variant, bufs.err, stream)
 
     def step():
-        m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs, w.rope_base,
-                      scale, w.num_splits, variant, stream)
+        if nn > 1:
+            m.decode_step_multi(lay, nn, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs,
+                                w.rope_base, scale, w.num_splits, variant, stream)
+        else:
+            m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs,
+                          w.rope_base, scale, w.num_splits, variant, stream)
 
-    fused = not u8 and variant in (0, 2) and w.dtype == "bf16" and w.group <= 32  # append inside the decode kernel
+    # append inside the decode kernel
+    fused = not u8 and nn == 1 and variant in (0, 2) and w.dtype == "bf16" and w.group <= 32
     launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
@@ -454,7 +482,8 @@ def bench_ours(args):
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
         kernel_name = "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel"
     elif variant in (0, 2) and w.dtype == "bf16":
-        heads_kernel = w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
+        heads_kernel = (w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
+                        and nn == 1)
         kernel_name = "decode_mma_heads_kernel" if heads_kernel else "decode_mma_kernel"
     else:
         kernel_name = "decode_fma_kernel"
@@ -497,8 +526,11 @@ def bench_ours(args):
                          + (f"paged {w.page_size}-token pages, lengths U[{w.len_lo},{w.len_hi}]" if w.paged
                             else f"contiguous {'uint8' if u8 else w.dtype} cache of {w.seq_len} tokens/seq")
                          + (", uint8 cache codes + float32 (scale, zero point) per row" if u8 else "")
+                         + (f", {nn} new tokens per sequence verified in one pass (causal among them)"
+                            if nn > 1 else "")
                          + ", RoPE base 10000"),
             "cache": "u8" if u8 else w.dtype,
+            "n_new": nn,
             "batch_per_gpu": w.batch,
             "tokens_per_step_per_gpu": int(lens_cpu.sum()),
             "num_splits": splits_used,
@@ -535,11 +567,14 @@ def bench_ours(args):
     if do_cpu:
         results, n_done, secs = run_oracle_units(w, units, args.cpu_seconds, window=args.window)
         by_unit = {(u["b"], u["j"]): u for u, _ in results}
-        done = sum(unit_bytes(w, min(units[i % len(units)]["L"], args.window or 1 << 30), out_es, args.cache)
-                   for i in range(n_done))
+        span = (args.window + nn - 1) if args.window else 1 << 30
+        done = sum(unit_bytes(w, min(units[i % len(units)]["L"], span), out_es, args.cache, nn) for i in range(n_done))
         out_host = bufs.out.float().cpu().numpy()
         G = w.group
-        errs = [float(np.max(np.abs(out_host[u["b"], u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
+        if nn > 1:
+            errs = [float(np.max(np.abs(out_host[u["b"], :, u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
+        else:
+            errs = [float(np.max(np.abs(out_host[u["b"], u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
         line["cpu_baseline"] = {
             "value": round(done / secs / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n_done} (sequence, kv head) units of the step ({len(by_unit)} distinct of "
@@ -560,7 +595,7 @@ def bench_reference(args):
     if rank != 0:
         return
     w = workload(args.workload)
-    case = build_case(w, "cpu", args.cache)
+    case = build_case(w, "cpu", args.cache, args.n_new)
     lens = case.seq_lens
     n_units = w.batch * w.h_kv
     order = [(u // w.h_kv, u % w.h_kv) for u in range(n_units)]
@@ -575,7 +610,8 @@ def bench_reference(args):
     def run(i):
         u = inputs[i % len(inputs)]
         oracle_unit(w, u, args.window)
-        return unit_bytes(w, min(u["L"], args.window or 1 << 30), out_es, args.cache)
+        span = (args.window + args.n_new - 1) if args.window else 1 << 30
+        return unit_bytes(w, min(u["L"], span), out_es, args.cache, args.n_new)
 
     for i in range(args.warmup):
         run(i)
@@ -591,6 +627,7 @@ def bench_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
         "impl": "reference",
         "config": {"workload": w.name, "cache": args.cache if args.cache == "u8" else w.dtype, "window": args.window,
+                   "n_new": args.n_new,
                    "batch_per_gpu": w.batch, "tokens_per_step_per_gpu": int(lens.sum()),
                    "step": "one (sequence, kv head) unit of the workload per step, cycling over the units"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -614,6 +651,8 @@ def main():
                     help="minimum warm-up time, so the clock sampler sees the load (0 for profiler runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--window", type=int, default=0, help="sliding window: attend to the last W tokens (0 = all)")
+    ap.add_argument("--n-new", type=int, default=1,
+                    help="new tokens per sequence (the verification pass of speculative decoding)")
     ap.add_argument("--cache", choices=["native", "u8"], default="native",
                     help="cache type: the workload's own (bf16 / fp32) or uint8 codes with per-row scale / zero point")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
