@@ -277,8 +277,10 @@ MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, con
  *   rows of one MMA tile set, so the K/V bytes are read once for all n_new
  *   tokens.
  * mqa_decode_step_multi: the two calls on one stream, pos[b] = L - n_new.
- * 1 <= n_new <= 32. n_new > 1 runs on tensor cores over a bf16 cache only
- * (MQA_ERR_UNSUPPORTED otherwise); n_new = 1 is exactly the single-token call.
+ * 1 <= n_new <= 32 for the attention (kv_append_rope_multi takes any n_new;
+ * longer runs of new tokens go to gqa_prefill_attention). n_new > 1 runs on
+ * tensor cores over a bf16 cache only (MQA_ERR_UNSUPPORTED otherwise); n_new
+ * = 1 is exactly the single-token call.
  */
 MQA_API mqa_status kv_append_rope_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new,
                                         const void* k_new, const void* v_new, const int32_t* pos, double rope_base,
@@ -300,6 +302,34 @@ MQA_API int32_t mqa_choose_splits_multi(const mqa_kv_layout* layout, int32_t n_n
                                         int32_t variant);
 MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len,
                                         int32_t num_splits, int32_t variant);
+
+/*
+ * Prefill: the prompt's n_new tokens of every sequence appended and attended
+ * causally in one pass ("KV Cache" explainer, Langkah 1 and 4: the prompt's
+ * keys and values are computed in one pass and stored; prefill is
+ * compute-bound). The arithmetic is that of the multi-token calls above --
+ * query token i of sequence b (position L - n_new + i) attends to the keys
+ * [0, L - n_new + i] (or the last W of them) -- on the tensor-memory tensor
+ * cores (tcgen05): one block per (sequence, query head, 128 tokens), S and O
+ * accumulated in tensor memory.
+ *
+ * gqa_prefill_attention: q_rot [batch, n_new, h_q, 128] fp32 (from
+ *   kv_append_rope_multi), seq_lens[b] = L after the append (>= n_new; L > n_new
+ *   means a cached prefix of L - n_new tokens), out [batch, n_new, h_q, 128],
+ *   lse_out optional [batch, n_new, h_q].
+ * mqa_prefill_step: kv_append_rope_multi (pos[b] = L - n_new), then
+ *   gqa_prefill_attention, on one stream.
+ * Contiguous bf16 cache with head_dim 128 only (MQA_ERR_UNSUPPORTED
+ * otherwise); no workspace. A bounded wait that runs out sets
+ * MQA_DEVERR_TIMEOUT and every later block of the launch returns at once.
+ */
+MQA_API mqa_status gqa_prefill_attention(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,
+                                         const int32_t* seq_lens, int32_t max_seq_len, float scale, void* out,
+                                         int32_t out_dtype, float* lse_out, int32_t* err_word, mqa_stream_t stream);
+MQA_API mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const void* q_new, const void* k_new,
+                                    const void* v_new, const int32_t* pos, const int32_t* seq_lens,
+                                    int32_t max_seq_len, double rope_base, float scale, float* q_rot, void* out,
+                                    int32_t out_dtype, float* lse_out, int32_t* err_word, mqa_stream_t stream);
 
 /* Split count gqa_decode_attention uses for num_splits = 0 on the current device
  * (>= 1), or -1 if the layout is invalid. */

@@ -47,6 +47,8 @@ __all__ = [
     "decode_step_multi",
     "kv_append_rope_multi",
     "gqa_decode_attention_multi",
+    "gqa_prefill_attention",
+    "prefill_step",
     "library",
     "MQA_VARIANT_AUTO",
     "MQA_VARIANT_CUDA_CORE",
@@ -251,4 +253,32 @@ def decode_step_multi(layout: KVLayout, n_new: int, q_new, k_new, v_new, pos, se
                                          int(variant), _ptr(bufs.err), _stream(stream))
     if st != 0:
         raise MqaError("mqa_decode_step_multi", st)
+    return bufs.out
+
+
+def gqa_prefill_attention(layout: KVLayout, n_new: int, q_rot, seq_lens, max_seq_len: int, scale: float, out,
+                          lse_out=None, err=None, stream=None) -> None:
+    """Causal attention of the last n_new tokens of every sequence on the
+    tensor-memory tensor cores: q_rot [B, n, H_q, 128] fp32, out [B, n, H_q, 128]."""
+    st = library().gqa_prefill_attention(ctypes.byref(layout), int(n_new), _ptr(q_rot), _ptr(seq_lens),
+                                         int(max_seq_len), float(scale), _ptr(out), _dtype_code(out.dtype),
+                                         _ptr(lse_out), _ptr(err), _stream(stream))
+    if st != 0:
+        raise MqaError("gqa_prefill_attention", st)
+
+
+def prefill_step(layout: KVLayout, n_new: int, q_new, k_new, v_new, pos, seq_lens, max_seq_len: int,
+                 bufs: DecodeBuffers, rope_base: float = 10000.0, scale: float | None = None,
+                 stream=None) -> torch.Tensor:
+    """The prompt's n_new tokens through ``mqa_prefill_step``: appended with RoPE
+    at pos .. pos + n_new - 1 (pos = seq_lens - n_new), then causal attention.
+    Buffers from ``DecodeBuffers.allocate(..., n_new=n_new, num_splits=1)``."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(layout.head_dim)
+    st = library().mqa_prefill_step(ctypes.byref(layout), int(n_new), _ptr(q_new), _ptr(k_new), _ptr(v_new),
+                                    _ptr(pos), _ptr(seq_lens), int(max_seq_len), float(rope_base), float(scale),
+                                    _ptr(bufs.q_rot), _ptr(bufs.out), _dtype_code(bufs.out.dtype), _ptr(bufs.lse),
+                                    _ptr(bufs.err), _stream(stream))
+    if st != 0:
+        raise MqaError("mqa_prefill_step", st)
     return bufs.out

@@ -82,6 +82,13 @@ _PROTOTYPES = {
         [ctypes.POINTER(KVLayout), c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, ctypes.c_double, ctypes.c_float, c_i32,
          c_vp, c_vp, c_i32, c_vp, c_vp, ctypes.c_size_t, c_i32, c_vp, c_vp],
     ),
+    "gqa_prefill_attention": (
+        c_i32, [ctypes.POINTER(KVLayout), c_i32, c_vp, c_vp, c_i32, ctypes.c_float, c_vp, c_i32, c_vp, c_vp, c_vp]),
+    "mqa_prefill_step": (
+        c_i32,
+        [ctypes.POINTER(KVLayout), c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, ctypes.c_double, ctypes.c_float, c_vp,
+         c_vp, c_i32, c_vp, c_vp, c_vp],
+    ),
     "mqa_choose_splits_multi": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32]),
     "mqa_workspace_size_multi": (ctypes.c_size_t, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32, c_i32]),
     "mqa_choose_splits": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32]),

@@ -190,7 +190,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // shared memory as two 64-column spans, so a tile needs half as many copies.
 // `heads` > 1 (paged, merged only): a box also spans that many consecutive kv
 // heads of one page, which are contiguous in the pool.
-bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool merged, int heads = 1) {
+bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool merged, int heads = 1,
+                     int box_rows = 0) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t D = L->head_dim;
@@ -199,7 +200,9 @@ bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool 
   cuuint64_t strides[4];
   cuuint32_t box[5];
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  const cuuint32_t rows = static_cast<cuuint32_t>(L->paged ? (L->page_size < kTile ? L->page_size : kTile) : kTile);
+  const cuuint32_t rows = box_rows > 0 ? static_cast<cuuint32_t>(box_rows)
+                                       : static_cast<cuuint32_t>(L->paged ? (L->page_size < kTile ? L->page_size : kTile)
+                                                                          : kTile);
   const cuuint64_t outer_rows = L->paged ? static_cast<cuuint64_t>(L->page_size) : static_cast<cuuint64_t>(L->capacity);
   cuuint32_t rank;
   if (merged) {
@@ -346,7 +349,7 @@ mqa_status append_impl(const mqa_kv_layout* layout, const void* q_new, const voi
                        int n_new = 1) {
   const mqa_status st = check_append_args(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word);
   if (st != MQA_OK) return st;
-  if (n_new < 1 || n_new > kMaxNewTokens) return MQA_ERR_INVALID_ARG;
+  if (n_new < 1 || static_cast<long long>(layout->batch) * n_new > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
   AppendParams p;
   std::memset(&p, 0, sizeof(p));
   p.n_new = n_new;
@@ -533,9 +536,79 @@ combine:
   return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
 }
 
+// Causal attention of the last n_new tokens of every sequence on tcgen05
+// (prefill): contiguous bf16 cache, head_dim 128.
+mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_rot, const int32_t* seq_lens,
+                        int32_t max_seq_len, float scale, void* out, int32_t out_dtype, float* lse_out,
+                        int32_t* err_word, mqa_stream_t stream) {
+  const mqa_status st = check_layout(layout);
+  if (st != MQA_OK) return st;
+  if (layout->cache_dtype != MQA_BF16 || layout->paged || layout->head_dim != 128) return MQA_ERR_UNSUPPORTED;
+  if (n_new < 1 || static_cast<long long>(layout->batch) * n_new > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
+  if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
+  if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
+      (lse_out && !aligned(lse_out, 4)))
+    return MQA_ERR_INVALID_ARG;
+  if (max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MQA_ERR_INVALID_ARG;
+  if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  const long long blocks = static_cast<long long>(layout->batch) * layout->h_q * ((n_new + 127) / 128);
+  if (blocks > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = layout->batch;
+  p.h_q = layout->h_q;
+  p.h_kv = layout->h_kv;
+  p.group = layout->h_q / layout->h_kv;
+  p.n_new = n_new;
+  p.k_cache = layout->k_cache;
+  p.v_cache = layout->v_cache;
+  p.capacity = layout->capacity;
+  p.max_seq_len = max_seq_len;
+  p.seq_lens = seq_lens;
+  p.q_rot = q_rot;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = layout->window;
+  p.out = out;
+  p.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
+  p.lse_out = lse_out;
+  p.err = err_word;
+  CUtensorMap tk, tv;
+  if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
+      !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {
+    snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+    return MQA_ERR_CUDA;
+  }
+  const cudaError_t e = launch_prefill(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  const cudaError_t e2 = cudaGetLastError();
+  return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);
+}
+
 }  // namespace
 
 extern "C" {
+
+mqa_status gqa_prefill_attention(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,
+                                 const int32_t* seq_lens, int32_t max_seq_len, float scale, void* out,
+                                 int32_t out_dtype, float* lse_out, int32_t* err_word, mqa_stream_t stream) {
+  return prefill_impl(layout, n_new, q_rot, seq_lens, max_seq_len, scale, out, out_dtype, lse_out, err_word, stream);
+}
+
+mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const void* q_new, const void* k_new,
+                            const void* v_new, const int32_t* pos, const int32_t* seq_lens, int32_t max_seq_len,
+                            double rope_base, float scale, float* q_rot, void* out, int32_t out_dtype,
+                            float* lse_out, int32_t* err_word, mqa_stream_t stream) {
+  // the attention's own checks first, so nothing is launched for a call that fails
+  const mqa_status st = check_layout(layout);
+  if (st != MQA_OK) return st;
+  if (layout->cache_dtype != MQA_BF16 || layout->paged || layout->head_dim != 128) return MQA_ERR_UNSUPPORTED;
+  if (!seq_lens || !out || max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
+  if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
+  const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);
+  if (a != MQA_OK) return a;
+  return prefill_impl(layout, n_new, q_rot, seq_lens, max_seq_len, scale, out, out_dtype, lse_out, err_word, stream);
+}
 
 const char* mqa_status_string(mqa_status s) {
   switch (s) {

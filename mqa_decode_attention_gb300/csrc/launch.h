@@ -68,6 +68,24 @@ struct DecodeParams {
   int32_t* err;
 };
 
+// Causal attention of the last n_new tokens of each sequence on tcgen05
+// (prefill): contiguous bf16 cache, head_dim 128.
+struct PrefillParams {
+  int batch, h_q, h_kv, group, n_new;
+  const void* k_cache;
+  const void* v_cache;
+  long long capacity;
+  int max_seq_len;
+  const int32_t* seq_lens;
+  const float* q_rot;  // [B, n_new, H_q, 128] fp32
+  float scale_log2;
+  int window;
+  void* out;  // [B, n_new, H_q, 128]
+  int out_dtype;
+  float* lse_out;  // [B, n_new, H_q] or null
+  int32_t* err;
+};
+
 struct CombineParams {
   const float* o_part;
   const float* lse_part;
@@ -114,5 +132,10 @@ int decode_u8_heads_group(const DecodeParams& p);
 cudaError_t launch_decode_u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+// tmap_k / tmap_v: the merged-halves bf16 maps with 128-row boxes.
+KernelShape prefill_shape();
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                           cudaStream_t stream);
 
 }  // namespace mqa

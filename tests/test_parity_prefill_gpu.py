@@ -1,0 +1,173 @@
+"""GPU parity of prefill (the prompt's tokens appended and attended causally
+in one pass, on the tcgen05 tensor cores) against the fp64 oracle's
+``decode_step_multi`` -- prefill is the multi-token step with n = prompt
+length.
+
+Tolerances: bf16 outputs and lse max |err| <= 2e-2, fp32 outputs <= 2e-2
+(the scores and P pass through bf16 on the tensor cores); the appended cache
+rows are placement-exact (V byte copies, K within one bf16 ulp).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import make_contiguous_case, make_paged_case, normal, workload
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+DEV = "cuda"
+S_QM, S_KM, S_VM = 21, 22, 23
+
+
+@pytest.fixture(scope="module")
+def m(built_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mqa_decode_attention_gb300 as mod
+
+    mod.library()
+    return mod
+
+
+def _np(t):
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def new_tokens(w, n, device="cpu"):
+    q = normal((w.batch, n, w.h_q, w.head_dim), w.seed, S_QM, w.dtype, device)
+    k = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_KM, w.dtype, device)
+    v = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_VM, w.dtype, device)
+    return q, k, v
+
+
+def ulp_bf16(x):
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def run_prefill(m, w, n, case, q, k, v, lens, window=0, out_dtype=None):
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    lay = m.layout_contiguous(kc, vc, w.h_q, window=window)
+    lens_d = torch.as_tensor(lens, dtype=torch.int32).to(DEV)
+    max_len = int(max(lens))
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=1, device=DEV, n_new=n, out_dtype=out_dtype)
+    pos = (lens_d - n).to(torch.int32)
+    m.prefill_step(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), pos, lens_d, max_len, bufs, w.rope_base,
+                   1.0 / math.sqrt(w.head_dim))
+    torch.cuda.synchronize()
+    B, hq = w.batch, w.h_q  # single-token buffers are [B, H_q, ...]: view them as [B, 1, H_q, ...]
+    return dict(out=_np(bufs.out).reshape(B, n, hq, -1), lse=_np(bufs.lse).reshape(B, n, hq), k=kc.cpu(),
+                v=vc.cpu(), err=int(bufs.err.item()))
+
+
+CASES = [
+    # B, h_q, h_kv, n (prompt), prefix, capacity
+    (2, 8, 2, 1, 0, 8),
+    (2, 8, 2, 5, 0, 8),
+    (2, 8, 2, 127, 0, 130),
+    (1, 8, 2, 128, 0, 128),
+    (2, 8, 2, 129, 0, 140),
+    (2, 8, 2, 300, 0, 300),
+    (2, 8, 2, 200, 57, 260),   # cached prefix of 57 tokens
+    (1, 4, 4, 150, 300, 450),  # MHA, prefix longer than the prompt
+    (1, 16, 1, 140, 10, 150),  # MQA
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}q{c[1]}kv{c[2]}n{c[3]}pre{c[4]}")
+def test_prefill_matches_oracle(m, case):
+    B, hq, hkv, n, pre, cap = case
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=500 + n + pre + hq)
+    lens = [pre + n] * B
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=cap)
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16")
+    got = run_prefill(m, w, n, c, q, k, v, lens)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= TOL
+    # appended rows: V byte copies, K within one bf16 ulp, nothing else touched
+    bk, ak = _np(c.k_cache), _np(got["k"])
+    assert np.array_equal(np.any(ak != bk, axis=-1), np.any(ref["k_cache"] != bk, axis=-1))
+    assert np.all(np.abs(ak - ref["k_cache"]) <= ulp_bf16(ref["k_cache"]) + 1e-30)
+    assert np.array_equal(_np(got["v"]), ref["v_cache"])
+
+
+@pytest.mark.parametrize("window", [1, 64, 200])
+def test_prefill_sliding_window(m, window):
+    w = workload("gqa4k").with_(batch=2, h_q=8, h_kv=2, seed=611)
+    n, pre = 300, 40
+    lens = [pre + n] * 2
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=340)
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", window=window)
+    got = run_prefill(m, w, n, c, q, k, v, lens, window=window)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= TOL, window
+
+
+def test_prefill_f32_output_and_unequal_rows(m):
+    """fp32 output; two sequences of different lengths (the prefix differs)."""
+    w = workload("gqa4k").with_(batch=2, h_q=8, h_kv=2, seed=612)
+    n = 130
+    lens = [n + 3, n + 200]
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=340)
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16")
+    got = run_prefill(m, w, n, c, q, k, v, lens, out_dtype=torch.float32)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
+
+
+def test_prefill_errors_and_refusals(m):
+    w = workload("gqa4k").with_(batch=2, h_q=8, h_kv=2, seed=613)
+    n = 64
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor([64, 64], dtype=torch.int32), capacity=64)
+    kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+    lay = m.layout_contiguous(kc, vc, w.h_q)
+    q_rot = torch.zeros(2, n, 8, 128, device=DEV)
+    out = torch.empty(2, n, 8, 128, dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.gqa_prefill_attention(lay, n, q_rot, torch.tensor([64, 10], dtype=torch.int32, device=DEV), 64, 0.1, out,
+                            err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & m.MQA_DEVERR_SEQ_LEN
+    wp = workload("paged").with_(batch=1, h_q=8, h_kv=2, seed=614)
+    pc = make_paged_case(wp, "cpu", seq_lens=torch.tensor([64], dtype=torch.int32))
+    bt = pc.block_table.to(DEV)
+    lay_p = m.layout_paged(pc.k_pool.to(DEV), pc.v_pool.to(DEV), bt, 8)
+    with pytest.raises(m.MqaError):  # paged pools: decode and multi-token calls only
+        m.gqa_prefill_attention(lay_p, n, q_rot[:1], torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1,
+                                out[:1], err=err)
+
+
+def test_prefill_full_size_sampled(m):
+    """4 sequences of 2048 prompt tokens, 32 query / 8 kv heads: two
+    (sequence, kv head) units against the oracle, every row of their groups."""
+    w = workload("gqa4k").with_(batch=4, seed=615)
+    n = 2048
+    lens = [n] * w.batch
+    c = make_contiguous_case(w, DEV, seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=n)
+    q, k, v = new_tokens(w, n, DEV)
+    lay = m.layout_contiguous(c.k_cache, c.v_cache, w.h_q)
+    bufs = m.DecodeBuffers.allocate(lay, n, num_splits=1, device=DEV, n_new=n)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    m.prefill_step(lay, n, q, k, v, lens_d - n, lens_d, n, bufs, w.rope_base)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    G = w.group
+    for b, j in [(0, 0), (3, 5)]:
+        Kz = torch.zeros(1, 1, n, w.head_dim, dtype=torch.bfloat16)
+        ref = oracle.decode_step_multi(Kz, Kz, q[b:b + 1, :, j * G:(j + 1) * G].cpu(), k[b:b + 1, :, j:j + 1].cpu(),
+                                       v[b:b + 1, :, j:j + 1].cpu(), [n], w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                       "bf16")
+        got = _np(bufs.out[b, :, j * G:(j + 1) * G])
+        assert np.max(np.abs(got - ref["out"][0])) <= TOL, (b, j)
