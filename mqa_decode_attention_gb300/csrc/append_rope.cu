@@ -240,12 +240,98 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
 }
 
+// Many new tokens per sequence (prefill): one block per (sequence, token)
+// that forms the token's d/2 fp64 sines and cosines once and rotates every
+// query and kv head of it, with the arithmetic of append_rope_kernel (the
+// per-head-block grid would evaluate the same fp64 table once per head block).
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(const AppendParams p) {
+  __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];
+  __shared__ long long s_row, s_stride;
+  __shared__ int s_ok;
+  grid_dependents_launch();
+  const int bt = blockIdx.x;
+  const int b = bt / p.n_new;
+  const int D = p.head_dim, half = D >> 1;
+  const int pos = p.pos[b] + (bt - b * p.n_new);
+  if (threadIdx.x < half) {
+    double cs, sn;
+    rope_cos_sin(pos, p.theta[threadIdx.x], &cs, &sn);
+    s_cos[threadIdx.x] = cs;
+    s_sin[threadIdx.x] = sn;
+  }
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    long long row = 0, stride = 0;
+    if (!p.paged) {
+      if (pos < 0 || pos >= p.capacity) {
+        ok = 0;
+        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+      } else {
+        row = (static_cast<long long>(b) * p.h_kv * p.capacity + pos) * D;
+        stride = p.capacity * D;
+      }
+    } else {
+      const int lp = pos >= 0 ? pos / p.page_size : -1;
+      if (pos < 0 || lp >= p.max_pages) {
+        ok = 0;
+        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+      } else {
+        const int page = p.block_table[static_cast<long long>(b) * p.max_pages + lp];
+        if (page < 0 || page >= p.num_pages) {
+          ok = 0;
+          atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
+        } else {
+          row = (static_cast<long long>(page) * p.h_kv * p.page_size + (pos % p.page_size)) * D;
+          stride = static_cast<long long>(p.page_size) * D;
+        }
+      }
+    }
+    s_ok = ok;
+    s_row = row;
+    s_stride = stride;
+  }
+  __syncthreads();
+  // q: fp32 rotation, fp32 output
+  const T* qs = static_cast<const T*>(p.q_new) + static_cast<long long>(bt) * p.h_q * D;
+  float* qr = p.q_rot + static_cast<long long>(bt) * p.h_q * D;
+  for (int idx = threadIdx.x; idx < p.h_q * half; idx += kAppendThreads) {
+    const int h = idx / half, i = idx - h * half;
+    const float2 x = Elem<T>::load2(qs + h * D + 2 * i);
+    const float c = static_cast<float>(s_cos[i]), s = static_cast<float>(s_sin[i]);
+    *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
+  }
+  if (!s_ok) return;
+  // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
+  const T* ks = static_cast<const T*>(p.k_new) + static_cast<long long>(bt) * p.h_kv * D;
+  const T* vs = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
+  T* kc = static_cast<T*>(p.k_cache) + s_row;
+  T* vc = static_cast<T*>(p.v_cache) + s_row;
+  for (int idx = threadIdx.x; idx < p.h_kv * half; idx += kAppendThreads) {
+    const int h = idx / half, i = idx - h * half;
+    const float2 x = Elem<T>::load2(ks + h * D + 2 * i);
+    const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
+    const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
+    const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
+    Elem<T>::store2_from_f64(kc + h * s_stride + 2 * i, xr, yr);
+    Elem<T>::copy2(vc + h * s_stride + 2 * i, vs + h * D + 2 * i);
+  }
+}
+
 }  // namespace
 
 KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
+  if (p.cache_dtype != kDtypeU8 && static_cast<long long>(p.batch) * p.n_new >= 1024) {
+    // enough tokens to fill the GPU with one block each
+    cfg.gridDim = dim3(p.batch * p.n_new);
+    cfg.blockDim = dim3(kAppendThreads);
+    cfg.stream = stream;
+    if (p.cache_dtype == kDtypeBf16) return cudaLaunchKernelEx(&cfg, append_rope_tokens_kernel<__nv_bfloat16>, p);
+    return cudaLaunchKernelEx(&cfg, append_rope_tokens_kernel<float>, p);
+  }
   cfg.gridDim = dim3(p.batch * p.n_new, (p.h_q + kQHeadsPerBlock - 1) / kQHeadsPerBlock +
                                   (p.h_kv + kKvHeadsPerBlock - 1) / kKvHeadsPerBlock);
   cfg.blockDim = dim3(kAppendThreads);

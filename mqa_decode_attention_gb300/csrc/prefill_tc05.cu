@@ -248,6 +248,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kSFree + sb));
       // keys of this tile outside [ka, pos] are masked
       const int key0 = (kt0 + it) * kBN;
+      if (key0 + kBN > L && key0 + r >= L) {
+        // cache rows past the sequence may hold anything (NaN bit patterns
+        // included); P = 0 there, and 0 * NaN would still poison O: zero the
+        // V row of this thread's key (V of the stage landed with K, before S)
+        unsigned char* vrow = smem + kStageOff + (it % kStages) * 2 * kTileBytes + kTileBytes + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       if (key0 < ka || key0 + kBN - 1 > pos) {
 #pragma unroll
         for (int c = 0; c < kBN; ++c)

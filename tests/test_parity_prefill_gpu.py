@@ -171,3 +171,20 @@ def test_prefill_full_size_sampled(m):
                                        "bf16")
         got = _np(bufs.out[b, :, j * G:(j + 1) * G])
         assert np.max(np.abs(got - ref["out"][0])) <= TOL, (b, j)
+
+
+def test_prefill_ignores_garbage_past_the_sequence(m):
+    """Cache rows at or past L hold NaN: the masked keys contribute nothing."""
+    w = workload("gqa4k").with_(batch=2, h_q=8, h_kv=2, seed=616)
+    n = 100
+    lens = [n, n]
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=256)
+    c.k_cache[:, :, n:] = float("nan")
+    c.v_cache[:, :, n:] = float("nan")
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(c.k_cache[:, :, :n], c.v_cache[:, :, :n], q, k, v, lens, w.rope_base,
+                                   1.0 / math.sqrt(w.head_dim), "bf16")
+    got = run_prefill(m, w, n, c, q, k, v, lens)
+    assert got["err"] == 0
+    assert np.all(np.isfinite(got["out"]))
+    assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
