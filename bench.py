@@ -589,6 +589,101 @@ def bench_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------------------ prefill leg
+PREFILL_METRIC = "prefill causal attention TFLOP/s (fraction of GB300 bf16 peak) at 1 GPU"
+
+
+def prefill_flops(w, n):
+    """Algorithmic FLOPs of causal attention over n new tokens per sequence
+    (no prefix): query i scores and mixes i + 1 keys, 4 d FLOPs per (head, key)."""
+    return 4 * w.head_dim * w.h_q * w.batch * n * (n + 1) // 2
+
+
+def bench_prefill(args):
+    """The prompt's tokens appended and attended causally in one pass
+    (mqa_prefill_step): time per step and the attention kernel's TFLOP/s."""
+    import mqa_decode_attention_gb300 as m
+
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = args.prefill
+    w = workload(args.workload).with_(batch=args.batch or 8)
+    case = make_contiguous_case(w, dev, seq_lens=torch.full((w.batch,), n, dtype=torch.int32), capacity=n)
+    q = normal((w.batch, n, w.h_q, w.head_dim), w.seed, S_QM, w.dtype, dev)
+    k = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_KM, w.dtype, dev)
+    v = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_VM, w.dtype, dev)
+    lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q)
+    bufs = m.DecodeBuffers.allocate(lay, n, num_splits=1, device=dev, n_new=n)
+    lens = case.seq_lens
+    pos = (lens - n).to(torch.int32)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.prefill_step(lay, n, q, k, v, pos, lens, n, bufs, w.rope_base, scale, stream)
+
+    sampler = ClockSampler(gpu_index_for(local))
+    t_warm = time.monotonic()
+    n_warm = 0
+    while n_warm < args.warmup or time.monotonic() - t_warm < args.warm_seconds:
+        step()
+        n_warm += 1
+    torch.cuda.synchronize()
+    t_clock0 = time.monotonic() - 0.5
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / K
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    for i in range(K):
+        ev[2 * i].record(stream)
+        m.gqa_prefill_attention(lay, n, bufs.q_rot, lens, n, scale, bufs.out, bufs.lse, bufs.err, stream)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    t_clock1 = time.monotonic()
+    sampler.stop()
+    attn_ms = statistics.fmean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(K))
+    if int(bufs.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(bufs.err.item()):#x}")
+    flops = prefill_flops(w, n)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": round(flops / (ms_step * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v; empty cache before the prompt)",
+        "config": {"workload": f"prefill: batch {w.batch}, {n}-token prompts, H_q {w.h_q}, H_kv {w.h_kv}, "
+                               f"head_dim {w.head_dim}, causal, RoPE base 10000",
+                   "flops_per_step": flops},
+        "kernels_ms": {"mqa_prefill_step": round(ms_step, 6), "standalone_gqa_prefill_attention": round(attn_ms, 6)},
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)" if peaks else "fallback"},
+        "gpu_launches": 2 * K,
+        "clocks": sampler.summary(t_clock0, t_clock1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------- reference arm
 def bench_reference(args):
     world, rank, _ = dist_env()
@@ -651,6 +746,8 @@ def main():
                     help="minimum warm-up time, so the clock sampler sees the load (0 for profiler runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--window", type=int, default=0, help="sliding window: attend to the last W tokens (0 = all)")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="time prefill of this many prompt tokens per sequence instead of a decode step")
     ap.add_argument("--n-new", type=int, default=1,
                     help="new tokens per sequence (the verification pass of speculative decoding)")
     ap.add_argument("--cache", choices=["native", "u8"], default="native",
@@ -662,6 +759,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         bench_reference(args)
+    elif args.prefill:
+        bench_prefill(args)
     else:
         bench_ours(args)
 

@@ -38,8 +38,8 @@ constexpr int kThreads = 192;
 constexpr int kTileBytes = kBN * kD * 2;                 // 32 KB: [2 halves][128 rows][128 B]
 constexpr int kQOff = 0;
 constexpr int kStageOff = kTileBytes;                    // stages: K then V
-constexpr int kPOff = kStageOff + kStages * 2 * kTileBytes;
-constexpr int kBarOff = kPOff + kTileBytes;
+constexpr int kPOff = kStageOff + kStages * 2 * kTileBytes;  // two P buffers
+constexpr int kBarOff = kPOff + 2 * kTileBytes;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;                      // S0, S1, O (+ unused)
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -47,7 +47,7 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // mbarriers (8 bytes each) at kBarOff
 enum Bar {
-  kQReady = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kODone = 10, kDrain = 11, kNBars = 12
+  kQReady = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kODone = 11, kDrain = 13, kNBars = 14
 };
 
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
@@ -108,8 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kSFree + s), 4);
     }
-    mbar_init(bar(kPFull), 4);
-    mbar_init(bar(kODone), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kPFull + s), 4);
+      mbar_init(bar(kODone + s), 1);
+    }
     mbar_init(bar(kDrain), 1);
     fence_mbar_init();
   }
@@ -173,17 +175,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_pv = [&](int it) -> bool {
-        const int s = it % kStages;
-        if (!mbar_wait(bar(kPFull), it & 1)) return false;
+        const int s = it % kStages, pb = it & 1;
+        if (!mbar_wait(bar(kPFull + pb), (it >> 1) & 1)) return false;
         tc05::fence_after_sync();
         const uint32_t v_s = sbase + kStageOff + s * 2 * kTileBytes + kTileBytes;
+        const uint32_t pp = p_s + pb * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc05::mma_bf16(tmem + kColO, tc05::smem_desc_sw128(p_s + off, 16, 1024),
+          tc05::mma_bf16(tmem + kColO, tc05::smem_desc_sw128(pp + off, 16, 1024),
                          tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, it > 0 || ks > 0);
         }
-        tc05::commit(bar(kODone));
+        tc05::commit(bar(kODone + pb));
         tc05::commit(bar(kKvEmpty + s));
         return true;
       };
@@ -235,14 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc05::fence_after_sync();
       float s[kBN];
+      // four loads in flight, one wait
+      tc05::ld_32x32b_x32(tmem + lane_base + kColS + sb * 128 + 0, *reinterpret_cast<float(*)[32]>(&s[0]));
+      tc05::ld_32x32b_x32(tmem + lane_base + kColS + sb * 128 + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+      tc05::ld_32x32b_x32(tmem + lane_base + kColS + sb * 128 + 64, *reinterpret_cast<float(*)[32]>(&s[64]));
+      tc05::ld_32x32b_x32(tmem + lane_base + kColS + sb * 128 + 96, *reinterpret_cast<float(*)[32]>(&s[96]));
+      tc05::wait_ld();
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        float v[32];
-        tc05::ld_32x32b_x32(tmem + lane_base + kColS + sb * 128 + c * 32, v);
-        tc05::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-      }
+      for (int c = 0; c < kBN; c += 32) tc05::reg_fence(*reinterpret_cast<float(*)[32]>(&s[c]));
       tc05::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kSFree + sb));
@@ -264,56 +267,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (key0 + c < ka || key0 + c > pos) s[c] = -INFINITY;
       }
-      float mt = s[0];
+      float mx8[8];  // eight independent chains
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // a new reference maximum only when the row's maximum grew by more than 2^8
       const bool grow = mt > m_ref + kRescaleLog2 || (m_ref == -INFINITY && mt != -INFINITY);
       const float m_new = grow ? mt : m_ref;
-      if (it > 0) {  // PV of the previous tile must be done: O is stable and P is free
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone), (it - 1) & 1) && !stop());
+      if (it > 0 && __any_sync(0xffffffffu, grow && m_ref != -INFINITY)) {
+        // O is rescaled: PV of the previous tile must be done first
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + ((it - 1) & 1)), ((it - 1) >> 1) & 1) && !stop());
         if (!ok) break;
         tc05::fence_after_sync();
-        if (__any_sync(0xffffffffu, grow && m_ref != -INFINITY)) {
-          const float alpha = (grow && m_ref != -INFINITY) ? fast_exp2(m_ref - m_new) : 1.f;
+        const float alpha = (grow && m_ref != -INFINITY) ? fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            float v[32];
-            tc05::ld_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
-            tc05::wait_ld();
+        for (int c = 0; c < kD / 32; ++c) {
+          float v[32];
+          tc05::ld_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
+          tc05::wait_ld();
+          tc05::reg_fence(v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tc05::st_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
-          }
-          tc05::wait_st();
-          l *= alpha;
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tc05::st_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
         }
+        tc05::wait_st();
+        l *= alpha;
       }
       m_ref = m_new;
       const float e = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum = 0.f;
+      float sm8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBN; c += 8) {
-        float pv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          pv[i] = fast_exp2(s[c + i] - e);
-          sum += pv[i];
+          s[c + i] = fast_exp2(s[c + i] - e);
+          sm8[i] += s[c + i];
         }
-        uint4 w;
-        w.x = pack_bf16x2(pv[0], pv[1]);
-        w.y = pack_bf16x2(pv[2], pv[3]);
-        w.z = pack_bf16x2(pv[4], pv[5]);
-        w.w = pack_bf16x2(pv[6], pv[7]);
-        *reinterpret_cast<uint4*>(smem + kPOff + sw128(r, c)) = w;
       }
-      l += sum;
+      l += ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+      // P buffer it % 2 was last read by the PV of tile it - 2
+      const int pb = it & 1;
+      if (it >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + pb), ((it - 2) >> 1) & 1) && !stop());
+        if (!ok) break;
+      }
+      unsigned char* prow = smem + kPOff + pb * kTileBytes;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 8) {
+        uint4 w;
+        w.x = pack_bf16x2(s[c], s[c + 1]);
+        w.y = pack_bf16x2(s[c + 2], s[c + 3]);
+        w.z = pack_bf16x2(s[c + 4], s[c + 5]);
+        w.w = pack_bf16x2(s[c + 6], s[c + 7]);
+        *reinterpret_cast<uint4*>(prow + sw128(r, c)) = w;
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc05::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kPFull));
+      if (lane == 0) mbar_arrive(bar(kPFull + pb));
     }
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone), (T - 1) & 1));
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + ((T - 1) & 1)), ((T - 1) >> 1) & 1));
     if (!ok) {
       if (lane == 0) fail(1);
     } else {
@@ -326,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
         tc05::ld_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
         tc05::wait_ld();
+        tc05::reg_fence(v);
         if (live) {
           if (p.out_dtype == kDtypeBf16) {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + grow_row * kD + c * 32;
