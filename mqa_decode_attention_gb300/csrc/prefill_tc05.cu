@@ -7,10 +7,12 @@
 // (token t0 + r, position p = L - n_new + t0 + r) attends to the keys
 // [max(0, p + 1 - W) if windowed else 0, p] of kv head floor(h / G). For each
 // 128-key tile of that range:
-//   S = Q K^T      tcgen05.mma M=128 N=128 K=128 (bf16 -> f32 in tensor memory)
-//   online softmax one row per thread of warps 0-3 (tcgen05.ld of the row),
-//                  P (bf16) written to shared memory
-//   O += P V       tcgen05.mma M=128 N=128 K=128, O stays in tensor memory
+//   S = Q K^T      tcgen05.mma M=128 N=128 K=128, Q and K from shared memory,
+//                  S (f32) into tensor memory
+//   online softmax one row per thread of warps 0-3 (tcgen05.ld of the row);
+//                  P (bf16) written back over its own S columns (tcgen05.st)
+//   O += P V       tcgen05.mma with A = P read from tensor memory, V from
+//                  shared memory; O stays in tensor memory
 // with the running maximum of FlashAttention ("Arsitektur Inferensi LLM",
 // section 5). S is double-buffered in tensor memory so the tensor core
 // computes S of the next tile while the softmax works on this one; O is only
@@ -18,8 +20,10 @@
 // taken against a reference at most 8 below the true maximum, so P stays
 // below 256 and the final O / l is unchanged).
 //
-// Warps: 0-3 softmax and epilogue (row = thread), 4 TMA producer (K and V
-// tiles, 2 stages), 5 MMA issue (one thread) and tensor-memory allocation.
+// Warps: 0-3 softmax and epilogue (row = thread), 4 K loader, 5 V loader
+// (TMA, 3 stages each; a K stage is released when its S is computed, a V
+// stage when its PV is), 6 MMA issue (one thread) and tensor-memory
+// allocation.
 #include <cuda_bf16.h>
 
 #include "../../include/mqa_decode.h"
@@ -33,13 +37,13 @@ namespace {
 constexpr int kD = 128;       // head_dim
 constexpr int kBM = 128;      // query rows (tokens of one head) per block
 constexpr int kBN = 128;      // keys per tile
-constexpr int kStages = 2;    // K/V tile ring
-constexpr int kThreads = 192;
+constexpr int kStages = 3;    // K tiles and V tiles in flight
+constexpr int kThreads = 224;
 constexpr int kTileBytes = kBN * kD * 2;                 // 32 KB: [2 halves][128 rows][128 B]
 constexpr int kQOff = 0;
-constexpr int kStageOff = kTileBytes;                    // stages: K then V
-constexpr int kPOff = kStageOff + kStages * 2 * kTileBytes;  // two P buffers
-constexpr int kBarOff = kPOff + 2 * kTileBytes;
+constexpr int kKOff = kTileBytes;                        // K stages
+constexpr int kVOff = kKOff + kStages * kTileBytes;      // V stages
+constexpr int kBarOff = kVOff + kStages * kTileBytes;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;                      // S0, S1, O (+ unused)
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -47,7 +51,16 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // mbarriers (8 bytes each) at kBarOff
 enum Bar {
-  kQReady = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kODone = 11, kDrain = 13, kNBars = 14
+  kQReady = 0,
+  kKFull = 1,    // [kStages]
+  kKEmpty = 4,   // [kStages]
+  kVFull = 7,    // [kStages]
+  kVEmpty = 10,  // [kStages]
+  kSFull = 13,   // [2]
+  kPFull = 15,   // [2]
+  kODone = 17,   // [2]
+  kDrain = 19,
+  kNBars = 20
 };
 
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
@@ -103,19 +116,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     mbar_init(bar(kQReady), 4);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kKvFull + s), 1);
-      mbar_init(bar(kKvEmpty + s), 1);
-      mbar_init(bar(kSFull + s), 1);
-      mbar_init(bar(kSFree + s), 4);
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kPFull + s), 4);
       mbar_init(bar(kODone + s), 1);
     }
     mbar_init(bar(kDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 6) {
     tc05::tmem_alloc(smem_u32(tslot), kTmemCols);
     tc05::tmem_relinquish();
   }
@@ -133,38 +147,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto stop = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == 4 || warp == 5) {
+    // ------------------------------------------------- K (warp 4) / V (warp 5) loaders
     if (lane == 0) {
+      const bool is_k = warp == 4;
+      const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+      const int full = is_k ? kKFull : kVFull, empty = is_k ? kKEmpty : kVEmpty;
+      const uint32_t dst0 = sbase + (is_k ? kKOff : kVOff);
       const int row = b * p.h_kv + j;
       for (int it = 0; it < T; ++it) {
         const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(bar(kKvEmpty + s), ((it - kStages) / kStages) & 1)) {
+        if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1)) {
           fail(1);
           break;
         }
         if (stop()) break;
-        const uint32_t dst = sbase + kStageOff + s * 2 * kTileBytes;
-        mbar_arrive_expect_tx(bar(kKvFull + s), 2 * kTileBytes);
-        const int key0 = (kt0 + it) * kBN;
-        tma_load_4d(dst, &tmap_k, 0, key0, 0, row, bar(kKvFull + s));
-        tma_load_4d(dst + kTileBytes, &tmap_v, 0, key0, 0, row, bar(kKvFull + s));
+        mbar_arrive_expect_tx(bar(full + s), kTileBytes);
+        tma_load_4d(dst0 + s * kTileBytes, map, 0, (kt0 + it) * kBN, 0, row, bar(full + s));
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 6) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t id_s = tc05::idesc_bf16_f32(kBM, kBN, false, false);
       const uint32_t id_o = tc05::idesc_bf16_f32(kBM, kD, false, true);
-      const uint32_t q_s = sbase + kQOff, p_s = sbase + kPOff;
+      const uint32_t q_s = sbase + kQOff;
       bool ok = mbar_wait(bar(kQReady), 0);
+      // S of tile it into buffer it % 2. That buffer last held P of tile it - 2,
+      // whose PV was issued before: MMAs of this thread execute in order.
       auto issue_s = [&](int it) -> bool {
         const int s = it % kStages, sb = it & 1;
-        if (!mbar_wait(bar(kKvFull + s), (it / kStages) & 1)) return false;
-        if (it >= 2 && !mbar_wait(bar(kSFree + sb), ((it - 2) >> 1) & 1)) return false;
+        if (!mbar_wait(bar(kKFull + s), (it / kStages) & 1)) return false;
         tc05::fence_after_sync();
-        const uint32_t k_s = sbase + kStageOff + s * 2 * kTileBytes;
+        const uint32_t k_s = sbase + kKOff + s * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -172,22 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                          tc05::smem_desc_sw128(k_s + off, 16, 1024), id_s, ks > 0);
         }
         tc05::commit(bar(kSFull + sb));
+        tc05::commit(bar(kKEmpty + s));
         return true;
       };
       auto issue_pv = [&](int it) -> bool {
         const int s = it % kStages, pb = it & 1;
         if (!mbar_wait(bar(kPFull + pb), (it >> 1) & 1)) return false;
+        if (!mbar_wait(bar(kVFull + s), (it / kStages) & 1)) return false;
         tc05::fence_after_sync();
-        const uint32_t v_s = sbase + kStageOff + s * 2 * kTileBytes + kTileBytes;
-        const uint32_t pp = p_s + pb * kTileBytes;
+        const uint32_t v_s = sbase + kVOff + s * kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc05::mma_bf16(tmem + kColO, tc05::smem_desc_sw128(pp + off, 16, 1024),
-                         tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, it > 0 || ks > 0);
-        }
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          tc05::mma_bf16_ta(tmem + kColO, tmem + kColS + pb * 128 + ks * 8,
+                            tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, it > 0 || ks > 0);
         tc05::commit(bar(kODone + pb));
-        tc05::commit(bar(kKvEmpty + s));
+        tc05::commit(bar(kVEmpty + s));
         return true;
       };
       if (ok && T > 0) ok = issue_s(0);
@@ -246,20 +261,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc05::wait_ld();
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) tc05::reg_fence(*reinterpret_cast<float(*)[32]>(&s[c]));
-      tc05::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSFree + sb));
       // keys of this tile outside [ka, pos] are masked
       const int key0 = (kt0 + it) * kBN;
-      if (key0 + kBN > L && key0 + r >= L) {
+      if (key0 + kBN > L) {
         // cache rows past the sequence may hold anything (NaN bit patterns
         // included); P = 0 there, and 0 * NaN would still poison O: zero the
-        // V row of this thread's key (V of the stage landed with K, before S)
-        unsigned char* vrow = smem + kStageOff + (it % kStages) * 2 * kTileBytes + kTileBytes + r * 128;
+        // V row of this thread's key once that tile has landed
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + it % kStages), (it / kStages) & 1));
+        if (!ok) break;
+        if (key0 + r >= L) {
+          unsigned char* vrow = smem + kVOff + (it % kStages) * kTileBytes + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
       }
       if (key0 < ka || key0 + kBN - 1 > pos) {
@@ -296,41 +313,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] *= alpha;
           tc05::st_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
         }
-        tc05::wait_st();
         l *= alpha;
       }
       m_ref = m_new;
       const float e = m_ref == -INFINITY ? 0.f : m_ref;
       float sm8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];  // P of keys 64 half .. 64 half + 63 as bf16 pairs
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          s[c + i] = fast_exp2(s[c + i] - e);
-          sm8[i] += s[c + i];
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = fast_exp2(s[64 * half + 2 * i] - e), p1 = fast_exp2(s[64 * half + 2 * i + 1] - e);
+          sm8[(2 * i) & 7] += p0;
+          sm8[(2 * i + 1) & 7] += p1;
+          pk[i] = pack_bf16x2(p0, p1);
         }
+        tc05::st_32x32b_x32_u(tmem + lane_base + kColS + sb * 128 + 32 * half, pk);
       }
       l += ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
-      // P buffer it % 2 was last read by the PV of tile it - 2
-      const int pb = it & 1;
-      if (it >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + pb), ((it - 2) >> 1) & 1) && !stop());
-        if (!ok) break;
-      }
-      unsigned char* prow = smem + kPOff + pb * kTileBytes;
-#pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
-        uint4 w;
-        w.x = pack_bf16x2(s[c], s[c + 1]);
-        w.y = pack_bf16x2(s[c + 2], s[c + 3]);
-        w.z = pack_bf16x2(s[c + 4], s[c + 5]);
-        w.w = pack_bf16x2(s[c + 6], s[c + 7]);
-        *reinterpret_cast<uint4*>(prow + sw128(r, c)) = w;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc05::wait_st();
       tc05::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kPFull + pb));
+      if (lane == 0) mbar_arrive(bar(kPFull + sb));
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + ((T - 1) & 1)), ((T - 1) >> 1) & 1));
     if (!ok) {
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: every role is done with tensor memory
   tc05::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 6) {
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       // MMAs may still be in flight after a timeout: wait (bounded) for them
       // before the columns are released
