@@ -386,8 +386,12 @@ def bench_ours(args):
             m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs,
                           w.rope_base, scale, w.num_splits, variant, stream)
 
-    # append inside the decode kernel
-    fused = not u8 and nn == 1 and variant in (0, 2) and w.dtype == "bf16" and w.group <= 32
+    # the library's routing: 32 or more query rows per kv head (G x n_new) on a
+    # contiguous bf16 cache with head_dim 128 run on the tcgen05 kernel (append
+    # a launch of its own); otherwise the warp-MMA kernel with the append inside
+    tc05 = (not u8 and variant in (0, 2) and w.dtype == "bf16" and not w.paged and w.head_dim == 128
+            and w.group * nn >= 32)
+    fused = not tc05 and not u8 and nn == 1 and variant in (0, 2) and w.dtype == "bf16" and w.group <= 32
     launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
@@ -481,6 +485,8 @@ def bench_ours(args):
     if u8:
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
         kernel_name = "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel"
+    elif tc05:
+        kernel_name = "attn_tc05_kernel"
     elif variant in (0, 2) and w.dtype == "bf16":
         heads_kernel = (w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
                         and nn == 1)
@@ -674,7 +680,7 @@ def bench_prefill(args):
                                f"head_dim {w.head_dim}, causal, RoPE base 10000",
                    "flops_per_step": flops},
         "kernels_ms": {"mqa_prefill_step": round(ms_step, 6), "standalone_gqa_prefill_attention": round(attn_ms, 6)},
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": "attn_tc05_kernel (prefill)", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)" if peaks else "fallback"},
         "gpu_launches": 2 * K,

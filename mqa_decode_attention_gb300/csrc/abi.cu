@@ -96,9 +96,20 @@ DeviceInfo device_info(int dev) {
   return d;
 }
 
+// Query rows per kv head from which the tensor-memory (tcgen05) kernel takes
+// the decode attention: 16-row mma.sync tiles run out of latency hiding there
+// (MQA's G = 32, several new tokens per sequence).
+constexpr int kTc05MinRows = 32;
+
+bool use_tc05(const mqa_kv_layout* L, int variant, int n_new) {
+  return variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16 && !L->paged && L->head_dim == 128 &&
+         (L->h_q / L->h_kv) * n_new >= kTc05MinRows;
+}
+
 // n_new: query tokens per sequence; a kv head then has G x n_new query rows.
 KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
   const int G = L->h_q / L->h_kv;
+  if (use_tc05(L, variant, n_new)) return tc05_shape();
   if (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_U8) return decode_u8_shape(L->head_dim, G);
   if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G * n_new);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
@@ -397,7 +408,7 @@ struct RopeArgs {
 // The tensor-core kernels can take the append over when one block sees all
 // query heads of its kv head (G <= 32).
 bool fusable(const mqa_kv_layout* L, int variant) {
-  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16) return false;
+  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16 || use_tc05(L, variant, 1)) return false;
   return head_blocks(L, decode_shape(L, variant)) == 1;
 }
 
@@ -482,6 +493,41 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   }
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (use_tc05(layout, v, n_new)) {
+    Tc05Params t;
+    std::memset(&t, 0, sizeof(t));
+    t.batch = layout->batch;
+    t.h_q = layout->h_q;
+    t.h_kv = layout->h_kv;
+    t.group = p.group;
+    t.n_new = n_new;
+    t.row_blocks = (p.group * n_new + 127) / 128;
+    t.num_splits = splits;
+    t.chunk = chunk;
+    t.k_cache = layout->k_cache;
+    t.v_cache = layout->v_cache;
+    t.capacity = layout->capacity;
+    t.max_seq_len = max_seq_len;
+    t.seq_lens = seq_lens;
+    t.q_rot = q_rot;
+    t.scale_log2 = p.scale_log2;
+    t.window = layout->window;
+    t.out = out;
+    t.out_dtype = p.out_dtype;
+    t.lse_out = lse_out;
+    t.o_part = p.o_part;
+    t.lse_part = p.lse_part;
+    t.err = err_word;
+    CUtensorMap tk, tv;
+    if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
+        !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {
+      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+      return MQA_ERR_CUDA;
+    }
+    e = launch_tc05_attention(t, tk, tv, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    goto combine;
+  }
   if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_U8) {
     CUtensorMap maps[4];
     // Paged 16- / 32-token pages: blocks over groups of kv heads, one box per
@@ -552,15 +598,19 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
   if (max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
-  const long long blocks = static_cast<long long>(layout->batch) * layout->h_q * ((n_new + 127) / 128);
+  const long long blocks = static_cast<long long>(layout->batch) * layout->h_kv *
+                           ((static_cast<long long>(layout->h_q / layout->h_kv) * n_new + 127) / 128);
   if (blocks > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
-  PrefillParams p;
+  Tc05Params p;
   std::memset(&p, 0, sizeof(p));
   p.batch = layout->batch;
   p.h_q = layout->h_q;
   p.h_kv = layout->h_kv;
   p.group = layout->h_q / layout->h_kv;
   p.n_new = n_new;
+  p.row_blocks = static_cast<int>((static_cast<long long>(p.group) * n_new + 127) / 128);
+  p.num_splits = 1;
+  p.chunk = ((max_seq_len + 63) / 64) * 64;
   p.k_cache = layout->k_cache;
   p.v_cache = layout->v_cache;
   p.capacity = layout->capacity;
@@ -579,7 +629,7 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
     snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
     return MQA_ERR_CUDA;
   }
-  const cudaError_t e = launch_prefill(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_tc05_attention(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   const cudaError_t e2 = cudaGetLastError();
   return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);

@@ -1,0 +1,597 @@
+// Attention of the last n_new tokens of every sequence on the 5th-generation
+// tensor cores: prefill ("KV Cache" explainer, Langkah 1 and 4: the prompt's
+// keys and values are computed in one pass and stored, and the work is
+// compute-bound), and decode steps with many query rows per kv head (MQA,
+// G = 32; several new tokens per sequence).
+//
+// The rows of kv head j are its (new token i, query head h = j G + hl) pairs,
+// row = i G + hl, in blocks of 128. Block = (sequence b, kv head j, token-axis
+// split, row block). Row (i, hl), at position p = L - n_new + i, attends to the
+// keys [max(0, p + 1 - W) if windowed else 0, p] that fall in the split's
+// range. For each 128-key tile of the block's range:
+//   S = Q K^T      tcgen05.mma M=128 N=128 K=128, Q and K from shared memory,
+//                  S (f32) into tensor memory
+//   online softmax one row per thread of warps 0-3 (tcgen05.ld of the row);
+//                  P (bf16) written back over its own S columns (tcgen05.st)
+//   O += P V       tcgen05.mma with A = P read from tensor memory, V from
+//                  shared memory; O stays in tensor memory
+// with the running maximum of FlashAttention ("Arsitektur Inferensi LLM",
+// section 5). S is double-buffered in tensor memory so the tensor core
+// computes S of the next tile while the softmax works on this one; O is only
+// rescaled when a row's maximum grows by more than 2^8 (the exponentials are
+// taken against a reference at most 8 below the true maximum, so P stays
+// below 256 and the final O / l is unchanged).
+//
+// With few rows per kv head (R <= 64: MQA's 32 query heads; a few new tokens
+// of a GQA group) the R rows are replicated PARTS = 128 / R_pad times over the
+// MMA's 128 rows and the softmax warps split every key tile: thread r (part
+// r / R_pad) keeps the online softmax of row r % R_pad over its 128 / PARTS
+// keys of each tile, its P row holds zeros over the other keys, and the
+// partial results of a row are merged (log-sum-exp weights) at the end.
+//
+// Warps: 0-3 softmax and epilogue (row = thread), 4 K loader, 5 V loader
+// (TMA, 3 stages each; a K stage is released when its S is computed, a V
+// stage when its PV is), 6 MMA issue (one thread) and tensor-memory
+// allocation.
+#include <cuda_bf16.h>
+
+#include "../../include/mqa_decode.h"
+#include "launch.h"
+#include "ptx.cuh"
+#include "tc05.cuh"
+
+namespace mqa {
+namespace {
+
+constexpr int kD = 128;       // head_dim
+constexpr int kBM = 128;      // query rows (tokens of one head) per block
+constexpr int kBN = 128;      // keys per tile
+constexpr int kStages = 3;    // K tiles and V tiles in flight
+constexpr int kThreads = 224;
+constexpr int kTileBytes = kBN * kD * 2;                 // 32 KB: [2 halves][128 rows][128 B]
+constexpr int kQOff = 0;
+constexpr int kKOff = kTileBytes;                        // K stages
+constexpr int kVOff = kKOff + kStages * kTileBytes;      // V stages
+constexpr int kBarOff = kVOff + kStages * kTileBytes;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;
+constexpr int kSBuf = 3;                                 // S / P buffers in tensor memory
+constexpr uint32_t kTmemCols = 512;                      // S0 .. S{kSBuf-1}, O
+constexpr uint32_t kColS = 0, kColO = kSBuf * 128;
+static_assert(kColO + kD <= kTmemCols, "S buffers and O exceed tensor memory");
+constexpr float kRescaleLog2 = 8.0f;
+
+// mbarriers (8 bytes each) at kBarOff
+constexpr int kQReady = 0;
+constexpr int kKFull = 1;                   // [kStages]
+constexpr int kKEmpty = kKFull + kStages;   // [kStages]
+constexpr int kVFull = kKEmpty + kStages;   // [kStages]
+constexpr int kVEmpty = kVFull + kStages;   // [kStages]
+constexpr int kSFull = kVEmpty + kStages;   // [kSBuf]
+constexpr int kPFull = kSFull + kSBuf;      // [kSBuf]
+constexpr int kODone = kPFull + kSBuf;      // [kSBuf]
+constexpr int kDrain = kODone + kSBuf;
+constexpr int kNBars = kDrain + 1;
+static_assert(kNBars * 8 + 4 <= 256, "barrier area");
+
+__device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
+  const int half = col >> 6, chunk = (col & 63) >> 3;
+  return half * 16384 + r * 128 + ((chunk ^ (r & 7)) << 4) + (col & 7) * 2;
+}
+
+__device__ __forceinline__ bool aborted(const Tc05Params& p) {
+  return (*reinterpret_cast<volatile int32_t*>(p.err) & static_cast<int>(MQA_DEVERR_TIMEOUT)) != 0;
+}
+
+template <int PARTS>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                     const Tc05Params p) {
+  constexpr int kRPad = kBM / PARTS;  // rows per part
+  constexpr int kKW = kBN / PARTS;    // keys of a tile per thread
+  extern __shared__ unsigned char smem_raw[];
+  // 1 KB aligned (128-byte swizzle atoms); offsetting the __shared__ array
+  // itself keeps accesses through `smem` in the shared state space
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNBars * 8);
+  __shared__ int s_abort, s_skip;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.group, n = p.n_new, R = G * n, S = p.num_splits;
+  // block order: sequence fastest, then kv head, split, row block (row blocks
+  // with the longest key ranges -- the last tokens -- first)
+  int cta = blockIdx.x;
+  const int b = cta % p.batch;
+  cta /= p.batch;
+  const int j = cta % p.h_kv;
+  cta /= p.h_kv;
+  const int split = cta % S;
+  const int rb = p.row_blocks - 1 - cta / S;
+  const int g0 = rb * kBM;
+  const int rows = min(kBM, R - g0);
+
+  long long limit = p.capacity < p.max_seq_len ? p.capacity : p.max_seq_len;
+  const int L = p.seq_lens[b];
+  if (L < n || L > limit) {
+    if (tid == 0 && split == 0 && rb == 0 && j == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
+    return;
+  }
+  if (tid == 0) s_skip = aborted(p) ? 1 : 0;  // an earlier block timed out: the result is invalid already
+  __syncthreads();
+  if (s_skip) return;
+  const int Lp = L - n;  // new token i sits at position Lp + i
+  const int pos_first = Lp + g0 / G, pos_last = Lp + (g0 + rows - 1) / G;
+  const int ka_first = p.window > 0 ? max(0, pos_first + 1 - p.window) : 0;
+  // the split's token range (as the other decode kernels cut it)
+  const int t_lo = p.window > 0 ? max(0, Lp + 1 - p.window) : 0;
+  const int t_begin = (t_lo / 64) * 64 + split * p.chunk;
+  const int t_end = min(L, t_begin + p.chunk);
+  const int kstart = max(t_begin, (ka_first / 64) * 64);
+  const int kend = min(t_end, pos_last + 1);
+  const int T = kend > kstart ? (kend - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
+  const bool split_out = S > 1;
+  if (T == 0) {
+    // no key of this split reaches these rows: an empty partial (weight 0 in the combine)
+    if (split_out) {
+      for (int idx = tid; idx < rows * kD; idx += kThreads) {
+        const int g = g0 + idx / kD, i = g / G;
+        const long long grow = (static_cast<long long>(b) * n + i) * p.h_q + j * G + (g - i * G);
+        p.o_part[(grow * S + split) * kD + idx % kD] = 0.f;
+        if (idx % kD == 0) p.lse_part[grow * S + split] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(bar(kQReady), 4);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+    }
+    for (int s = 0; s < kSBuf; ++s) {
+      mbar_init(bar(kSFull + s), 1);
+      mbar_init(bar(kPFull + s), 4);
+      mbar_init(bar(kODone + s), 1);
+    }
+    mbar_init(bar(kDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 6) {
+    tc05::tmem_alloc(smem_u32(tslot), kTmemCols);
+    tc05::tmem_relinquish();
+  }
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tslot);
+  const uint32_t sbase = smem_u32(smem);
+  // q_rot and the new tokens' cache rows come from the preceding append launch
+  grid_dependency_wait();
+
+  auto fail = [&](int role_lane0) {
+    if (role_lane0) {
+      s_abort = 1;
+      atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
+    }
+  };
+  auto stop = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
+
+  if (warp == 4 || warp == 5) {
+    // ------------------------------------------------- K (warp 4) / V (warp 5) loaders
+    // start once the Q rows have been requested: behind a burst of tile loads
+    // the Q reads would wait microseconds
+    named_bar_sync(2, kBM + 64);
+    if (lane == 0) {
+      const bool is_k = warp == 4;
+      const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+      const int full = is_k ? kKFull : kVFull, empty = is_k ? kKEmpty : kVEmpty;
+      const uint32_t dst0 = sbase + (is_k ? kKOff : kVOff);
+      const int row = b * p.h_kv + j;
+      for (int it = 0; it < T; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1)) {
+          fail(1);
+          break;
+        }
+        if (stop()) break;
+        mbar_arrive_expect_tx(bar(full + s), kTileBytes);
+        tma_load_4d(dst0 + s * kTileBytes, map, 0, kstart + it * kBN, 0, row, bar(full + s));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t id_s = tc05::idesc_bf16_f32(kBM, kBN, false, false);
+      const uint32_t id_o = tc05::idesc_bf16_f32(kBM, kD, false, true);
+      const uint32_t q_s = sbase + kQOff;
+      bool ok = mbar_wait(bar(kQReady), 0);
+      // S of tile it into buffer it % kSBuf. That buffer last held P of tile
+      // it - kSBuf, whose PV was issued before: MMAs of this thread execute in order.
+      auto issue_s = [&](int it) {
+        const int s = it % kStages, sb = it % kSBuf;
+        tc05::fence_after_sync();
+        const uint32_t k_s = sbase + kKOff + s * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          tc05::mma_bf16(tmem + kColS + sb * 128, tc05::smem_desc_sw128(q_s + off, 16, 1024),
+                         tc05::smem_desc_sw128(k_s + off, 16, 1024), id_s, ks > 0);
+        }
+        tc05::commit(bar(kSFull + sb));
+        tc05::commit(bar(kKEmpty + s));
+      };
+      auto issue_pv = [&](int it) {
+        const int s = it % kStages, pb = it % kSBuf;
+        tc05::fence_after_sync();
+        const uint32_t v_s = sbase + kVOff + s * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          tc05::mma_bf16_ta(tmem + kColO, tmem + kColS + pb * 128 + ks * 8,
+                            tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, it > 0 || ks > 0);
+        tc05::commit(bar(kODone + pb));
+        tc05::commit(bar(kVEmpty + s));
+      };
+      // Issue S and PV as their inputs land: S of tile ns needs its K tile and
+      // (buffer reuse) the PV of tile ns - kSBuf issued; PV of tile np needs its P
+      // and V tile. Neither waits behind the other.
+      int ns = 0, np = 0;
+      unsigned long long t_idle = global_timer_ns();
+      while (ok && np < T) {
+        bool progress = false;
+        if (ns < T && ns <= np + (kSBuf - 1) && mbar_test(bar(kKFull + ns % kStages), (ns / kStages) & 1)) {
+          issue_s(ns++);
+          progress = true;
+        }
+        if (np < ns && mbar_test(bar(kPFull + np % kSBuf), (np / kSBuf) & 1) &&
+            mbar_test(bar(kVFull + np % kStages), (np / kStages) & 1)) {
+          issue_pv(np++);
+          progress = true;
+        }
+        if (progress) {
+          t_idle = global_timer_ns();
+        } else if (stop() || global_timer_ns() - t_idle > kWaitLimitNs) {
+          ok = false;
+        } else {
+          __nanosleep(32);  // leave the issue slots to the softmax warp sharing this scheduler
+        }
+      }
+      if (!ok) fail(1);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------- softmax (row = tid)
+    const int r = tid;
+    const int part = r / kRPad, gr = r - part * kRPad;  // key slice and row of this thread
+    const bool live = gr < rows;
+    const int gi = (g0 + gr) / G;                      // new token of this row
+    const int hh = j * G + (g0 + gr - gi * G);         // its query head
+    const long long grow_row = (static_cast<long long>(b) * n + gi) * p.h_q + hh;  // output row [B, n, H_q]
+    {
+      // Q row, pre-scaled into the log2 domain, as bf16 in the swizzled tile
+      const float4* q = reinterpret_cast<const float4*>(p.q_rot + grow_row * kD);
+      float4 qv[kD / 4];  // the whole row requested at once: one memory round trip
+#pragma unroll
+      for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      // release the K / V loaders only now: behind their burst of tile
+      // requests these loads would wait microseconds
+      named_bar_arrive(2, kBM + 64);
+#pragma unroll
+      for (int c = 0; c < kD; c += 8) {
+        const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
+        uint4 v;
+        v.x = pack_bf16x2(a.x * p.scale_log2, a.y * p.scale_log2);
+        v.y = pack_bf16x2(a.z * p.scale_log2, a.w * p.scale_log2);
+        v.z = pack_bf16x2(bq.x * p.scale_log2, bq.y * p.scale_log2);
+        v.w = pack_bf16x2(bq.z * p.scale_log2, bq.w * p.scale_log2);
+        *reinterpret_cast<uint4*>(smem + kQOff + sw128(r, c)) = v;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQReady));
+    }
+    const int pos = live ? min(Lp + gi, t_end - 1) : -1;  // last key of this row in the split (none: padding)
+    const int ka = p.window > 0 ? max(0, Lp + gi + 1 - p.window) : 0;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int it = 0; it < T; ++it) {
+      const int sb = it % kSBuf;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + sb), (it / kSBuf) & 1) && !stop());
+      if (!ok) break;
+      tc05::fence_after_sync();
+      float s[kKW];
+      // this thread's keys of the tile: columns part * kKW .. + kKW (loads in flight, one wait)
+#pragma unroll
+      for (int c = 0; c < kKW; c += 32)
+        tc05::ld_32x32b_x32(tmem + lane_base + kColS + sb * 128 + part * kKW + c,
+                            *reinterpret_cast<float(*)[32]>(&s[c]));
+      tc05::wait_ld();
+#pragma unroll
+      for (int c = 0; c < kKW; c += 32) tc05::reg_fence(*reinterpret_cast<float(*)[32]>(&s[c]));
+      // keys of this tile outside [ka, pos] are masked
+      const int key0 = kstart + it * kBN;
+      if (key0 + kBN > L) {
+        // cache rows past the sequence may hold anything (NaN bit patterns
+        // included); P = 0 there, and 0 * NaN would still poison O: zero the
+        // V row of this thread's key once that tile has landed
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + it % kStages), (it / kStages) & 1));
+        if (!ok) break;
+        if (key0 + r >= L) {
+          unsigned char* vrow = smem + kVOff + (it % kStages) * kTileBytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+      }
+      const int kk0 = key0 + part * kKW;  // first key of this thread's slice
+      if (kk0 < ka || kk0 + kKW - 1 > pos) {
+#pragma unroll
+        for (int c = 0; c < kKW; ++c)
+          if (kk0 + c < ka || kk0 + c > pos) s[c] = -INFINITY;
+      }
+      float mx8[8];  // eight independent chains
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kKW; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // a new reference maximum only when the row's maximum grew by more than 2^8
+      const bool grow = mt > m_ref + kRescaleLog2 || (m_ref == -INFINITY && mt != -INFINITY);
+      const float m_new = grow ? mt : m_ref;
+      if (it > 0 && __any_sync(0xffffffffu, grow && m_ref != -INFINITY)) {
+        // O is rescaled: PV of the previous tile must be done first
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + (it - 1) % kSBuf), ((it - 1) / kSBuf) & 1) && !stop());
+        if (!ok) break;
+        tc05::fence_after_sync();
+        const float alpha = (grow && m_ref != -INFINITY) ? fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          float v[32];
+          tc05::ld_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
+          tc05::wait_ld();
+          tc05::reg_fence(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tc05::st_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
+        }
+        l *= alpha;
+      }
+      m_ref = m_new;
+      const float e = m_ref == -INFINITY ? 0.f : m_ref;
+      float sm8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // P of this thread's keys as bf16 pairs over its own S columns; the
+      // other parts' columns of this row carry zeros
+      const uint32_t prow = tmem + lane_base + kColS + sb * 128;
+      if constexpr (PARTS == 1) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = fast_exp2(s[64 * half + 2 * i] - e), p1 = fast_exp2(s[64 * half + 2 * i + 1] - e);
+            sm8[(2 * i) & 7] += p0;
+            sm8[(2 * i + 1) & 7] += p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tc05::st_32x32b_x32_u(prow + 32 * half, pk);
+        }
+      } else {
+        constexpr int kCols = kKW / 2;  // 32-bit columns of this thread's P
+        uint32_t pk[kCols];
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) {
+          const float p0 = fast_exp2(s[2 * i] - e), p1 = fast_exp2(s[2 * i + 1] - e);
+          sm8[(2 * i) & 7] += p0;
+          sm8[(2 * i + 1) & 7] += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        if constexpr (PARTS == 2) {
+          uint32_t z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0u;
+          tc05::st_32x32b_x32_u(prow + 32 * part, *reinterpret_cast<uint32_t(*)[32]>(pk));
+          tc05::st_32x32b_x32_u(prow + 32 * (1 - part), z);
+        } else {
+          uint32_t z[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            if (q4 == part)
+              tc05::st_32x32b_x16_u(prow + 16 * q4, *reinterpret_cast<uint32_t(*)[16]>(pk));
+            else
+              tc05::st_32x32b_x16_u(prow + 16 * q4, z);
+          }
+        }
+      }
+      l += ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+      tc05::wait_st();
+      tc05::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kPFull + sb));
+    }
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + (T - 1) % kSBuf), ((T - 1) / kSBuf) & 1));
+    if (!ok && lane == 0) fail(1);
+    if (ok) tc05::fence_after_sync();
+    {
+      if constexpr (PARTS == 1) {
+        if (ok) {
+        // ---- epilogue: O / l, lse = ln(sum exp(score)); a split writes its partial
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+  #pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          float v[32];
+          tc05::ld_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
+          tc05::wait_ld();
+          tc05::reg_fence(v);
+          if (live) {
+            if (split_out) {
+              float* dst = p.o_part + (grow_row * S + split) * kD + c * 32;
+  #pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv,
+                                                                  v[i + 3] * inv);
+            } else if (p.out_dtype == kDtypeBf16) {
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + grow_row * kD + c * 32;
+  #pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 w;
+                w.x = pack_bf16x2(v[i] * inv, v[i + 1] * inv);
+                w.y = pack_bf16x2(v[i + 2] * inv, v[i + 3] * inv);
+                w.z = pack_bf16x2(v[i + 4] * inv, v[i + 5] * inv);
+                w.w = pack_bf16x2(v[i + 6] * inv, v[i + 7] * inv);
+                *reinterpret_cast<uint4*>(dst + i) = w;
+              }
+            } else {
+              float* dst = static_cast<float*>(p.out) + grow_row * kD + c * 32;
+  #pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv,
+                                                                  v[i + 3] * inv);
+            }
+          }
+        }
+        const float lse = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        if (live && split_out)
+          p.lse_part[grow_row * S + split] = lse;
+        else if (live && p.lse_out != nullptr)
+          p.lse_out[grow_row] = lse;
+        }
+      } else {
+        // ---- merge the PARTS partial softmaxes of each row through shared
+        // memory (the K stages: every K tile has been consumed by now)
+        constexpr int kStride = kD + 4;
+        float* mo = reinterpret_cast<float*>(smem + kKOff);  // [128][kStride] unnormalised O
+        float* mm = mo + kBM * kStride;                        // [128] reference maxima
+        float* ml = mm + kBM;                                  // [128] sums
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            float v[32];
+            tc05::ld_32x32b_x32(tmem + lane_base + kColO + c * 32, v);
+            tc05::wait_ld();
+            tc05::reg_fence(v);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(mo + r * kStride + c * 32 + i) =
+                  make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          }
+          mm[r] = m_ref;
+          ml[r] = l;
+        }
+        // every softmax warp arrives, also after a timeout (which set s_abort first)
+        named_bar_sync(1, kBM);
+        // thread r < rows: the weight of each part in row r (its partial
+        // softmax renormalised to the row's maximum and divided by the row's
+        // total), the row's lse and output row
+        float* mw = ml + kBM;                                  // [PARTS][kRPad]
+        long long* mrow = reinterpret_cast<long long*>(mw + kBM);  // [kRPad]
+        if (r < rows && !stop()) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < PARTS; ++q) mx = fmaxf(mx, mm[q * kRPad + r]);
+          float w[PARTS], den = 0.f;
+#pragma unroll
+          for (int q = 0; q < PARTS; ++q) {
+            w[q] = mx == -INFINITY ? 0.f : exp2f(mm[q * kRPad + r] - mx);
+            den = fmaf(w[q], ml[q * kRPad + r], den);
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+          for (int q = 0; q < PARTS; ++q) mw[q * kRPad + r] = w[q] * inv;
+          const int ti = (g0 + r) / G;
+          const long long orow = (static_cast<long long>(b) * n + ti) * p.h_q + j * G + (g0 + r - ti * G);
+          mrow[r] = orow;
+          const float lse = den > 0.f ? (mx + log2f(den)) * 0.69314718055994530942f : -INFINITY;
+          if (split_out)
+            p.lse_part[orow * S + split] = lse;
+          else if (p.lse_out != nullptr)
+            p.lse_out[orow] = lse;
+        }
+        named_bar_sync(1, kBM);
+        // thread = head dim: every row's output element, rows independent
+        const int d = r;
+        if (!stop()) {
+#pragma unroll 4
+          for (int row = 0; row < rows; ++row) {
+            float ov = 0.f;
+#pragma unroll
+            for (int q = 0; q < PARTS; ++q)
+              ov = fmaf(mw[q * kRPad + row], mo[(q * kRPad + row) * kStride + d], ov);
+            const long long orow = mrow[row];
+            if (split_out) {
+              p.o_part[(orow * S + split) * kD + d] = ov;
+            } else if (p.out_dtype == kDtypeBf16) {
+              static_cast<__nv_bfloat16*>(p.out)[orow * kD + d] = __float2bfloat16_rn(ov);
+            } else {
+              static_cast<float*>(p.out)[orow * kD + d] = ov;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every role is done with tensor memory
+  tc05::fence_before_sync();
+  __syncthreads();
+  if (warp == 6) {
+    if (*reinterpret_cast<volatile int*>(&s_abort)) {
+      // MMAs may still be in flight after a timeout: wait (bounded) for them
+      // before the columns are released
+      if (lane == 0) {
+        tc05::commit(bar(kDrain));
+        (void)mbar_wait(bar(kDrain), 0);
+      }
+      __syncwarp();
+    }
+    tc05::fence_after_sync();
+    tc05::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+KernelShape tc05_shape() { return {kThreads, kSmemBytes, kBM, 1}; }
+
+template <int PARTS>
+cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  auto kern = attn_tc05_kernel<PARTS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.h_kv * p.num_splits * p.row_blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t stream) {
+  // replicate few rows over the 128 MMA rows so that all four softmax warps work
+  const long long rows = static_cast<long long>(p.group) * p.n_new;
+  if (p.row_blocks == 1 && rows <= 32) return launch_parts<4>(p, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 64) return launch_parts<2>(p, tk, tv, stream);
+  return launch_parts<1>(p, tk, tv, stream);
+}
+
+}  // namespace mqa

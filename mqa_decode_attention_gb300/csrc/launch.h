@@ -68,10 +68,14 @@ struct DecodeParams {
   int32_t* err;
 };
 
-// Causal attention of the last n_new tokens of each sequence on tcgen05
-// (prefill): contiguous bf16 cache, head_dim 128.
-struct PrefillParams {
+// Attention on tcgen05 over blocks of 128 (new token, query head) rows of
+// one kv head: prefill, MQA decode, multi-token decode. Contiguous bf16
+// cache, head_dim 128.
+struct Tc05Params {
   int batch, h_q, h_kv, group, n_new;
+  int row_blocks;  // ceil(group * n_new / 128)
+  int num_splits;  // token-axis splits; 1 = write `out` directly
+  int chunk;       // tokens per split, a multiple of 64
   const void* k_cache;
   const void* v_cache;
   long long capacity;
@@ -82,7 +86,9 @@ struct PrefillParams {
   int window;
   void* out;  // [B, n_new, H_q, 128]
   int out_dtype;
-  float* lse_out;  // [B, n_new, H_q] or null
+  float* lse_out;   // [B, n_new, H_q] or null
+  float* o_part;    // [B, n_new, H_q, num_splits, 128] when num_splits > 1
+  float* lse_part;  // [B, n_new, H_q, num_splits]
   int32_t* err;
 };
 
@@ -134,8 +140,8 @@ cudaError_t launch_decode_u8_heads(const DecodeParams& p, int hg, const CUtensor
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // tmap_k / tmap_v: the merged-halves bf16 maps with 128-row boxes.
-KernelShape prefill_shape();
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                           cudaStream_t stream);
+KernelShape tc05_shape();
+cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                  cudaStream_t stream);
 
 }  // namespace mqa
