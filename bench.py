@@ -387,11 +387,13 @@ def bench_ours(args):
                           w.rope_base, scale, w.num_splits, variant, stream)
 
     # the library's routing: 32 or more query rows per kv head (G x n_new) on a
-    # contiguous bf16 cache with head_dim 128 run on the tcgen05 kernel (append
-    # a launch of its own); otherwise the warp-MMA kernel with the append inside
+    # contiguous bf16 cache with head_dim 128 run on the tcgen05 kernel, the
+    # rest on the warp-MMA kernels; a one-token step is one launch (the append
+    # inside the attention kernel) when one block serves all of a kv head's heads
     tc05 = (not u8 and variant in (0, 2) and w.dtype == "bf16" and not w.paged and w.head_dim == 128
             and w.group * nn >= 32)
-    fused = not tc05 and not u8 and nn == 1 and variant in (0, 2) and w.dtype == "bf16" and w.group <= 32
+    fused = (not u8 and nn == 1 and variant in (0, 2) and w.dtype == "bf16"
+             and (w.group <= 128 if tc05 else w.group <= 32))
     launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)

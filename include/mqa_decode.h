@@ -214,10 +214,12 @@ MQA_API mqa_status splitkv_combine(const float* o_part, const float* lse_part, i
  * arguments mean what they mean in those two calls; q_rot is the caller's
  * fp32 [batch, h_q, head_dim] scratch that carries the rotated query from the
  * first launch to the second. Every argument of both calls is checked before
- * the first launch. On the tensor-core path with a bf16 cache and at most 32
- * query heads per kv head the step is ONE launch: the attention kernel
- * rotates q and k_new itself, writes the new token's slot and q_rot, and then
- * reads that slot back. Otherwise the attention launch directly follows the
+ * the first launch. On the tensor-core path with a bf16 cache the step is ONE
+ * launch (plus the combine when it splits) when one block serves all query
+ * heads of a kv head -- at most 32 of them on the warp-MMA kernels, 32 to 128
+ * on the tcgen05 kernel (contiguous cache, head_dim 128): the attention
+ * kernel rotates q and k_new itself, writes the new token's slot and q_rot,
+ * and then reads that slot back. Otherwise the attention launch directly follows the
  * append launch and is allowed to start while the append is still running:
  * it streams every cached row except the appended one, the lengths and the
  * block table early, and waits for the append before it reads q_rot or the

@@ -406,9 +406,11 @@ struct RopeArgs {
 };
 
 // The tensor-core kernels can take the append over when one block sees all
-// query heads of its kv head (G <= 32).
+// query heads of its kv head (warp-MMA kernels: G <= 32; tcgen05: one
+// 128-row block).
 bool fusable(const mqa_kv_layout* L, int variant) {
-  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16 || use_tc05(L, variant, 1)) return false;
+  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16) return false;
+  if (use_tc05(L, variant, 1)) return L->h_q / L->h_kv <= 128;  // one row block
   return head_blocks(L, decode_shape(L, variant)) == 1;
 }
 
@@ -518,6 +520,17 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     t.o_part = p.o_part;
     t.lse_part = p.lse_part;
     t.err = err_word;
+    t.early = early;
+    if (rope != nullptr && rope->fuse_append && n_new == 1) {
+      t.fuse = 1;
+      t.early = 0;  // nothing of this step precedes the launch
+      t.q_new = rope->q_new;
+      t.k_new = rope->k_new;
+      t.v_new = rope->v_new;
+      t.pos = rope->pos;
+      t.q_rot_out = rope->q_rot;
+      fill_theta(t.theta, layout->head_dim, rope->rope_base);
+    }
     CUtensorMap tk, tv;
     if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
         !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {
@@ -586,7 +599,7 @@ combine:
 // (prefill): contiguous bf16 cache, head_dim 128.
 mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_rot, const int32_t* seq_lens,
                         int32_t max_seq_len, float scale, void* out, int32_t out_dtype, float* lse_out,
-                        int32_t* err_word, mqa_stream_t stream) {
+                        int32_t* err_word, mqa_stream_t stream, int early) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
   if (layout->cache_dtype != MQA_BF16 || layout->paged || layout->head_dim != 128) return MQA_ERR_UNSUPPORTED;
@@ -623,6 +636,7 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
   p.out_dtype = out_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32;
   p.lse_out = lse_out;
   p.err = err_word;
+  p.early = early;
   CUtensorMap tk, tv;
   if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
       !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {
@@ -642,7 +656,8 @@ extern "C" {
 mqa_status gqa_prefill_attention(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,
                                  const int32_t* seq_lens, int32_t max_seq_len, float scale, void* out,
                                  int32_t out_dtype, float* lse_out, int32_t* err_word, mqa_stream_t stream) {
-  return prefill_impl(layout, n_new, q_rot, seq_lens, max_seq_len, scale, out, out_dtype, lse_out, err_word, stream);
+  return prefill_impl(layout, n_new, q_rot, seq_lens, max_seq_len, scale, out, out_dtype, lse_out, err_word, stream,
+                      /*early=*/0);
 }
 
 mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const void* q_new, const void* k_new,
@@ -657,7 +672,8 @@ mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const vo
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);
   if (a != MQA_OK) return a;
-  return prefill_impl(layout, n_new, q_rot, seq_lens, max_seq_len, scale, out, out_dtype, lse_out, err_word, stream);
+  return prefill_impl(layout, n_new, q_rot, seq_lens, max_seq_len, scale, out, out_dtype, lse_out, err_word, stream,
+                      /*early=*/1);
 }
 
 const char* mqa_status_string(mqa_status s) {

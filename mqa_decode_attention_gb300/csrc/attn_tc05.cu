@@ -38,6 +38,7 @@
 #include "../../include/mqa_decode.h"
 #include "launch.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 #include "tc05.cuh"
 
 namespace mqa {
@@ -70,7 +71,8 @@ constexpr int kSFull = kVEmpty + kStages;   // [kSBuf]
 constexpr int kPFull = kSFull + kSBuf;      // [kSBuf]
 constexpr int kODone = kPFull + kSBuf;      // [kSBuf]
 constexpr int kDrain = kODone + kSBuf;
-constexpr int kNBars = kDrain + 1;
+constexpr int kAppended = kDrain + 1;       // fused step: the new k / v row is in the cache
+constexpr int kNBars = kAppended + 1;
 static_assert(kNBars * 8 + 4 <= 256, "barrier area");
 
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
@@ -82,7 +84,7 @@ __device__ __forceinline__ bool aborted(const Tc05Params& p) {
   return (*reinterpret_cast<volatile int32_t*>(p.err) & static_cast<int>(MQA_DEVERR_TIMEOUT)) != 0;
 }
 
-template <int PARTS>
+template <int PARTS, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const Tc05Params p) {
@@ -112,10 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = min(kBM, R - g0);
 
   long long limit = p.capacity < p.max_seq_len ? p.capacity : p.max_seq_len;
-  const int L = p.seq_lens[b];
+  int L = p.seq_lens[b];
+  const int apos = FUSE ? p.pos[b] : 0;  // fused step: the new token's position
   if (L < n || L > limit) {
+    // reported; these rows are then unspecified, but the block still runs (a
+    // fused step's append and q_rot land as they would without the error)
     if (tid == 0 && split == 0 && rb == 0 && j == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
-    return;
+    L = L < n ? n : static_cast<int>(limit);
   }
   if (tid == 0) s_skip = aborted(p) ? 1 : 0;  // an earlier block timed out: the result is invalid already
   __syncthreads();
@@ -131,8 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kend = min(t_end, pos_last + 1);
   const int T = kend > kstart ? (kend - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
   const bool split_out = S > 1;
+  // fused step: the split whose token range holds the new token's position
+  // (else split 0) appends its k / v row
+  const int tbase = (t_lo / 64) * 64;
+  const bool writer = FUSE && split == ((apos - tbase >= 0 && (apos - tbase) / p.chunk < S) ? (apos - tbase) / p.chunk : 0);
   if (T == 0) {
     // no key of this split reaches these rows: an empty partial (weight 0 in the combine)
+    grid_dependency_wait();
     if (split_out) {
       for (int idx = tid; idx < rows * kD; idx += kThreads) {
         const int g = g0 + idx / kD, i = g / G;
@@ -159,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kODone + s), 1);
     }
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kAppended), 2);  // the two writer warps
     fence_mbar_init();
   }
   if (warp == 6) {
@@ -170,8 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc05::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tslot);
   const uint32_t sbase = smem_u32(smem);
-  // q_rot and the new tokens' cache rows come from the preceding append launch
-  grid_dependency_wait();
+  // q_rot and the new tokens' cache rows come from the preceding launch. After
+  // the append kernel (early) every other cached row is final already: the
+  // loaders stream those while it runs and wait only before a tile that holds
+  // a new token; the softmax threads wait before reading q_rot.
+  if (!p.early) grid_dependency_wait();
 
   auto fail = [&](int role_lane0) {
     if (role_lane0) {
@@ -183,24 +197,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4 || warp == 5) {
     // ------------------------------------------------- K (warp 4) / V (warp 5) loaders
-    // start once the Q rows have been requested: behind a burst of tile loads
-    // the Q reads would wait microseconds
+    const bool is_k = warp == 4;
+    const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+    const int full = is_k ? kKFull : kVFull, empty = is_k ? kKEmpty : kVEmpty;
+    const uint32_t dst0 = sbase + (is_k ? kKOff : kVOff);
+    const int row = b * p.h_kv + j;
+    auto issue = [&](int it) {
+      const int s = it % kStages;
+      mbar_arrive_expect_tx(bar(full + s), kTileBytes);
+      tma_load_4d(dst0 + s * kTileBytes, map, 0, kstart + it * kBN, 0, row, bar(full + s));
+    };
+    int it = 0;
+    if (p.early) {
+      // while the append kernel runs: the ring's first fill, tiles wholly
+      // before the new tokens
+      for (; it < T && it < kStages && kstart + (it + 1) * kBN <= Lp; ++it)
+        if (lane == 0) issue(it);
+    }
+    // the rest only once the Q rows have been requested: behind a burst of
+    // tile loads the Q reads would wait microseconds
     named_bar_sync(2, kBM + 64);
     if (lane == 0) {
-      const bool is_k = warp == 4;
-      const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-      const int full = is_k ? kKFull : kVFull, empty = is_k ? kKEmpty : kVEmpty;
-      const uint32_t dst0 = sbase + (is_k ? kKOff : kVOff);
-      const int row = b * p.h_kv + j;
-      for (int it = 0; it < T; ++it) {
+      bool waited = !p.early, appended = !writer;
+      for (; it < T; ++it) {
         const int s = it % kStages;
         if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1)) {
           fail(1);
           break;
         }
         if (stop()) break;
-        mbar_arrive_expect_tx(bar(full + s), kTileBytes);
-        tma_load_4d(dst0 + s * kTileBytes, map, 0, kstart + it * kBN, 0, row, bar(full + s));
+        if (!waited && Lp < kstart + (it + 1) * kBN) {  // this tile holds a new token's row
+          grid_dependency_wait();
+          waited = true;
+        }
+        if (!appended && apos < kstart + (it + 1) * kBN) {  // ... written by this block's softmax warps
+          if (!mbar_wait(bar(kAppended), 0)) {
+            fail(1);
+            break;
+          }
+          appended = true;
+        }
+        issue(it);
       }
     }
     __syncwarp();
@@ -273,14 +310,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hh = j * G + (g0 + gr - gi * G);         // its query head
     const long long grow_row = (static_cast<long long>(b) * n + gi) * p.h_q + hh;  // output row [B, n, H_q]
     {
-      // Q row, pre-scaled into the log2 domain, as bf16 in the swizzled tile
-      const float4* q = reinterpret_cast<const float4*>(p.q_rot + grow_row * kD);
-      float4 qv[kD / 4];  // the whole row requested at once: one memory round trip
+      // Q row, pre-scaled into the log2 domain, as bf16 in the swizzled tile.
+      // The whole row is requested at once (one memory round trip), and the
+      // K / V loaders are released only then: behind their burst of tile
+      // requests these loads would wait microseconds.
+      if (p.early) grid_dependency_wait();
+      float4 qv[kD / 4];
+      if constexpr (FUSE) {
+        // fused step: q_new (bf16) rotated here, pair i by the fp32 cosine /
+        // sine of the fp64-reduced angle pos * theta_i, as the append kernel
+        // forms q_rot
+        __shared__ float s_cs[kD];
+        const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_new) + grow_row * kD);
+        uint4 raw[kD / 8];
 #pragma unroll
-      for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-      // release the K / V loaders only now: behind their burst of tile
-      // requests these loads would wait microseconds
-      named_bar_arrive(2, kBM + 64);
+        for (int c = 0; c < kD / 8; ++c) raw[c] = live ? qn[c] : make_uint4(0u, 0u, 0u, 0u);
+        named_bar_arrive(2, kBM + 64);
+        if (tid < kD / 2) {
+          const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[tid]);
+          float sf, cf;
+          sincosf(static_cast<float>(ang), &sf, &cf);
+          s_cs[tid] = cf;
+          s_cs[kD / 2 + tid] = sf;
+        } else if (writer) {
+          // the new token's cache rows exactly as the append kernel writes
+          // them: k pair i turned in fp64 (round-to-nearest products, one
+          // rounding to bf16), v copied; a position outside the cache is
+          // reported and nothing is written
+          const int i = tid - kD / 2;
+          if (apos >= 0 && apos < p.capacity) {
+            double c, sn;
+            sincos(reduce_two_pi(static_cast<double>(apos) * p.theta[i]), &sn, &c);
+            const long long row = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD + 2 * i;
+            const long long src = (static_cast<long long>(b) * p.h_kv + j) * kD + 2 * i;
+            const uint32_t kraw = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
+            const double x = bf16lo_to_f32(kraw), y = bf16hi_to_f32(kraw);
+            __nv_bfloat162 kr;
+            kr.x = __double2bfloat16(__dsub_rn(__dmul_rn(x, c), __dmul_rn(y, sn)));
+            kr.y = __double2bfloat16(__dadd_rn(__dmul_rn(x, sn), __dmul_rn(y, c)));
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + row) = kr;
+            *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + row) =
+                *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
+          } else if (i == 0) {
+            atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+          }
+          // this block's TMA loads (async proxy) read the rows back
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kAppended));
+        }
+        named_bar_sync(3, kBM);  // the cos / sin table
+#pragma unroll
+        for (int c = 0; c < kD / 8; ++c) {
+          const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+          float rv[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pi = 4 * c + e;  // pair (2 pi, 2 pi + 1)
+            const float x = bf16lo_to_f32(w4[e]), y = bf16hi_to_f32(w4[e]);
+            const float cs = s_cs[pi], sn = s_cs[kD / 2 + pi];
+            rv[2 * e] = x * cs - y * sn;
+            rv[2 * e + 1] = x * sn + y * cs;
+          }
+          qv[2 * c] = make_float4(rv[0], rv[1], rv[2], rv[3]);
+          qv[2 * c + 1] = make_float4(rv[4], rv[5], rv[6], rv[7]);
+        }
+        if (live && part == 0 && split == 0) {  // one copy of each row to q_rot
+          float4* qo = reinterpret_cast<float4*>(p.q_rot_out + grow_row * kD);
+#pragma unroll
+          for (int c = 0; c < kD / 4; ++c) qo[c] = qv[c];
+        }
+      } else {
+        const float4* q = reinterpret_cast<const float4*>(p.q_rot + grow_row * kD);
+#pragma unroll
+        for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        named_bar_arrive(2, kBM + 64);
+      }
 #pragma unroll
       for (int c = 0; c < kD; c += 8) {
         const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
@@ -316,13 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kKW; c += 32) tc05::reg_fence(*reinterpret_cast<float(*)[32]>(&s[c]));
       // keys of this tile outside [ka, pos] are masked
       const int key0 = kstart + it * kBN;
-      if (key0 + kBN > L) {
-        // cache rows past the sequence may hold anything (NaN bit patterns
-        // included); P = 0 there, and 0 * NaN would still poison O: zero the
-        // V row of this thread's key once that tile has landed
+      if (key0 + kBN > t_end) {
+        // rows past the split may hold anything: past the sequence any bit
+        // pattern (NaN included), and the next split's first rows may be the
+        // new token's, being written by another block of a fused step. P = 0
+        // there, and 0 * NaN would still poison O: zero the V row of this
+        // thread's key once that tile has landed
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + it % kStages), (it / kStages) & 1));
         if (!ok) break;
-        if (key0 + r >= L) {
+        if (key0 + r >= t_end) {
           unsigned char* vrow = smem + kVOff + (it % kStages) * kTileBytes + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -567,9 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 KernelShape tc05_shape() { return {kThreads, kSmemBytes, kBM, 1}; }
 
-template <int PARTS>
+template <int PARTS, bool FUSE>
 cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  auto kern = attn_tc05_kernel<PARTS>;
+  auto kern = attn_tc05_kernel<PARTS, FUSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -589,9 +696,12 @@ cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tk, co
                                   cudaStream_t stream) {
   // replicate few rows over the 128 MMA rows so that all four softmax warps work
   const long long rows = static_cast<long long>(p.group) * p.n_new;
-  if (p.row_blocks == 1 && rows <= 32) return launch_parts<4>(p, tk, tv, stream);
-  if (p.row_blocks == 1 && rows <= 64) return launch_parts<2>(p, tk, tv, stream);
-  return launch_parts<1>(p, tk, tv, stream);
+  // (a fused step has one row block: p.fuse implies row_blocks == 1)
+  if (p.row_blocks == 1 && rows <= 32)
+    return p.fuse ? launch_parts<4, true>(p, tk, tv, stream) : launch_parts<4, false>(p, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 64)
+    return p.fuse ? launch_parts<2, true>(p, tk, tv, stream) : launch_parts<2, false>(p, tk, tv, stream);
+  return p.fuse ? launch_parts<1, true>(p, tk, tv, stream) : launch_parts<1, false>(p, tk, tv, stream);
 }
 
 }  // namespace mqa

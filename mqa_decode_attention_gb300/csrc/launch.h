@@ -90,6 +90,16 @@ struct Tc05Params {
   float* o_part;    // [B, n_new, H_q, num_splits, 128] when num_splits > 1
   float* lse_part;  // [B, n_new, H_q, num_splits]
   int32_t* err;
+  int early;  // 1: the preceding launch is the append kernel; stream K/V before waiting for it
+  // 1: single-launch step (one new token, one row block): the kernel rotates
+  // q_new itself and the block whose split holds pos appends the k / v row
+  int fuse;
+  const void* q_new;  // [B, H_q, 128] bf16
+  const void* k_new;  // [B, H_kv, 128] bf16
+  const void* v_new;
+  const int32_t* pos;
+  float* q_rot_out;  // RoPE(q_new) [B, H_q, 128] fp32
+  double theta[kMaxHalfDim];
 };
 
 struct CombineParams {
