@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the append kernel (early) every other cached row is final already: the
   // loaders stream those while it runs and wait only before a tile that holds
   // a new token; the softmax threads wait before reading q_rot.
+  // the combine (or the next step) may be scheduled now; it waits for this
+  // whole grid before it reads anything this grid writes
+  grid_dependents_launch();
   if (!p.early) grid_dependency_wait();
 
   auto fail = [&](int role_lane0) {

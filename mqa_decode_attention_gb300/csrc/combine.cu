@@ -69,6 +69,12 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(p.head_dim >= 128 ? 128 : 64);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
+  // resident while the decode grid finishes; griddepcontrol.wait holds it
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 

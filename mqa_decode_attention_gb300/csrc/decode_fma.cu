@@ -133,6 +133,9 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
   }
   __syncthreads();
   // q_rot and the appended slot come from the preceding append launch.
+  // the combine (or the next step) may be scheduled now; it waits for this
+  // whole grid before it reads anything this grid writes
+  grid_dependents_launch();
   grid_dependency_wait();
   // Lengths are read only after the preceding grid is complete and visible.
   long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;

@@ -99,6 +99,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   // table and every cached row except the new token's are already final, so
   // the producer streams them early and only the tile holding the new token
   // (and the consumers, which need q_rot) wait.
+  // the combine (or the next step) may be scheduled now; it waits for this
+  // whole grid before it reads anything this grid writes
+  grid_dependents_launch();
   if (!p.early) grid_dependency_wait();
   long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;
   if (limit > p.max_seq_len) limit = p.max_seq_len;

@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
   __syncthreads();
   // See decode_mma.cu: after the append kernel everything but q_rot and the
   // new token's row may be read before the dependency wait.
+  // the combine (or the next step) may be scheduled now; it waits for this
+  // whole grid before it reads anything this grid writes
+  grid_dependents_launch();
   if (!p.early) grid_dependency_wait();
   long long limit = static_cast<long long>(p.max_pages) * kPage;
   if (limit > p.max_seq_len) limit = p.max_seq_len;

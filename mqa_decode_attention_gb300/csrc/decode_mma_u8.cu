@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 
     fence_mbar_init();
   }
   __syncthreads();
+  // the combine (or the next step) may be scheduled now; it waits for this
+  // whole grid before it reads anything this grid writes
+  grid_dependents_launch();
   if (!p.early) grid_dependency_wait();
   long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;
   if (limit > p.max_seq_len) limit = p.max_seq_len;
@@ -688,6 +691,9 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES>::kThreads, HG <=
     fence_mbar_init();
   }
   __syncthreads();
+  // the combine (or the next step) may be scheduled now; it waits for this
+  // whole grid before it reads anything this grid writes
+  grid_dependents_launch();
   if (!p.early) grid_dependency_wait();
   long long limit = static_cast<long long>(p.max_pages) * PS;
   if (limit > p.max_seq_len) limit = p.max_seq_len;
