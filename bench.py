@@ -47,7 +47,8 @@ METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 G
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "gqa4k"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "mma_warp.cuh", "ptx.cuh", "launch.h"]
+KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "attn_tc05.cu", "mma_warp.cuh", "tc05.cuh",
+                  "rope.cuh", "ptx.cuh", "launch.h"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -510,7 +511,7 @@ def bench_ours(args):
         roof_kernel = kernel_name + (" + combine_kernel" if splits_used > 1 else "")
         roof_time = "events around each standalone gqa_decode_attention call"
     achieved = roof_bytes / (roof_ms * 1e-3) / 1e9
-    traffic = (ncu_traffic(args.workload + ("_u8" if u8 else "")) if kernel_name.startswith(("decode_mma", "decode_u8"))
+    traffic = (ncu_traffic(args.workload + ("_u8" if u8 else "")) if kernel_name.startswith(("decode_mma", "decode_u8", "attn_tc05"))
                else None)
     clocks = sampler.summary(t_clock0, t_clock1)
 
