@@ -18,8 +18,11 @@ from .decode import (
     decode_step_contiguous,
     decode_step_multi,
     decode_step_paged,
+    decode_step_e5m2,
     decode_step_u8,
+    dequantize_e5m2,
     dequantize_u8,
+    quantize_e5m2,
     quantize_u8,
     decode_unit,
     gather_paged,

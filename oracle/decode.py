@@ -103,6 +103,47 @@ def dequantize_u8(codes, scale, zp):
     return (np.asarray(codes, F64) - np.asarray(zp, F64)[..., None]) * np.asarray(scale, F64)[..., None]
 
 
+# ------------------------------------------------------ fp8 (e5m2) KV cache
+E5M2_MAX = 57344.0  # 1.75 * 2^15, the largest finite e5m2 value
+
+
+def quantize_e5m2(x):
+    """fp8 e5m2 codes of float64 values: the KV-cache format of the serving
+    flag `--kv-cache-dtype fp8_e5m2` in the vLLM examples ("KV Cache 최적화
+    심층 분석", youngju.dev, the deployment section; "Arsitektur Inferensi
+    LLM", tveniu.com, the vLLM configuration). e5m2 is 1 sign bit, 5 exponent
+    bits (bias 15) and 2 mantissa bits: (1 + m/4) 2^(E-15) for E in 1..30,
+    (m/4) 2^-14 for E = 0, E = 31 infinities and NaN.
+    Readings (the pages name the flag only): round to nearest, ties to even,
+    on the float64 value itself; magnitudes beyond the largest finite value
+    saturate to it; NaN maps to a NaN code. Returns uint8 codes."""
+    x = np.asarray(x, F64)
+    ax = np.abs(x)
+    _, e = np.frexp(ax)                                    # ax = m 2^e, 0.5 <= m < 1
+    q_exp = np.maximum(e.astype(np.int64) - 3, -16)        # quantum: 2 bits below the leading one, >= 2^-16
+    r = np.minimum(np.ldexp(np.rint(np.ldexp(ax, -q_exp)), q_exp), E5M2_MAX)  # np.rint: half to even
+    mr, er = np.frexp(r)
+    binade = er.astype(np.int64) - 1
+    normal = (r > 0) & (binade >= -14)
+    field = np.where(normal, binade + 15, 0)
+    mant = np.where(normal, np.ldexp(r, -binade) * 4 - 4, np.ldexp(r, 16))
+    codes = (field * 4 + np.rint(mant)).astype(np.int64)
+    codes = np.where(np.isnan(x), 0x7F, codes)
+    codes = np.where(np.signbit(x), codes | 0x80, codes)
+    return codes.astype(np.uint8)
+
+
+def dequantize_e5m2(codes):
+    """Value of each e5m2 code (float64), from the format's definition."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    field = (c >> 2) & 31
+    m = (c & 3).astype(F64)
+    val = np.where(field == 0, np.ldexp(m, -16), np.ldexp(1.0 + m / 4.0, field - 15))
+    val = np.where(field == 31, np.where(m == 0, np.inf, np.nan), val)
+    return sign * val
+
+
 # -------------------------------------------------------------------- RoPE
 def rope_inv_freq(head_dim: int, base: float) -> np.ndarray:
     """theta_i = base^(-2i/d), i = 0 .. d/2-1 (reading; the pages give no formula)."""
@@ -370,6 +411,41 @@ def decode_step_u8(k_codes, k_sz, v_codes, v_sz, q_new, k_new, v_new, seq_lens, 
         t0 = window_start(L, window)
         out[b], lse[b] = gqa_attention(q_rot[b], Kd[:, t0:], Vd[:, t0:], scale)
     return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "k_sz": Ks, "v_codes": Vc, "v_sz": Vs}
+
+
+def decode_step_e5m2(k_codes, v_codes, q_new, k_new, v_new, seq_lens, rope_base: float, scale: float,
+                     block_table=None, page_size: int = 0, window: int = 0):
+    """One decode step over an fp8 e5m2 cache (codes, contiguous [B, H_kv,
+    capacity, d] or paged [num_pages, H_kv, page_size, d] with a block table).
+    The new token's key is rotated in fp64 and rounded once to e5m2; its value
+    (bf16 input) is rounded to e5m2; the attention reads the decoded cache.
+    Returns dict(out, lse, q_rot, k_codes, v_codes) with updated copies."""
+    Kc, Vc = np.array(k_codes, dtype=np.uint8, copy=True), np.array(v_codes, dtype=np.uint8, copy=True)
+    q_new, k_new, v_new = _f64(q_new), _f64(k_new), _f64(v_new)
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    table = None if block_table is None else np.asarray(_f64(block_table), dtype=np.int64)
+    B, h_q, d = q_new.shape
+    out = np.empty((B, h_q, d), F64)
+    lse = np.empty((B, h_q), F64)
+    q_rot = np.empty((B, h_q, d), F64)
+    for b in range(B):
+        L = int(lens[b])
+        p = L - 1
+        q_rot[b] = rope_rotate(q_new[b], p, rope_base)
+        kq = quantize_e5m2(rope_rotate(k_new[b], p, rope_base))
+        vq = quantize_e5m2(v_new[b])
+        if table is None:
+            Kc[b, :, p], Vc[b, :, p] = kq, vq
+            Kd = dequantize_e5m2(Kc[b, :, :L])
+            Vd = dequantize_e5m2(Vc[b, :, :L])
+        else:
+            page, off = page_slot(table[b], p, page_size)
+            Kc[page, :, off], Vc[page, :, off] = kq, vq
+            Kd = dequantize_e5m2(gather_paged(Kc, table[b], L, page_size))
+            Vd = dequantize_e5m2(gather_paged(Vc, table[b], L, page_size))
+        t0 = window_start(L, window)
+        out[b], lse[b] = gqa_attention(q_rot[b], Kd[:, t0:], Vd[:, t0:], scale)
+    return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "v_codes": Vc}
 
 
 def decode_step_multi(k_cache, v_cache, q_new, k_new, v_new, seq_lens, rope_base: float, scale: float,

@@ -541,6 +541,67 @@ def test_u8_decode_step_pins():
     assert np.array_equal(rp["out"], r["out"])
 
 
+# ------------------------------------------------------ fp8 e5m2 cache
+def test_e5m2_format_pins():
+    """e5m2 is the high byte of an IEEE half: every code decodes to the
+    float16 whose bit pattern is code << 8 (numpy's float16, an independent
+    route); every finite code encodes back to itself; hand-worked roundings
+    (ties to even, subnormals, saturation, signed zero)."""
+    c = np.arange(256, dtype=np.uint8)
+    v = oracle.dequantize_e5m2(c)
+    half = (c.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(v), np.isnan(half))
+    assert np.array_equal(v[~np.isnan(v)], half[~np.isnan(half)])
+    fin = np.isfinite(v)
+    assert np.array_equal(oracle.quantize_e5m2(v[fin]), c[fin])
+    cases = [
+        (1.0, 0x3C), (1.25, 0x3D), (1.2, 0x3D), (1.125, 0x3C),  # 1.125: tie between 1.0 (even) and 1.25
+        (1.375, 0x3E),                                          # tie between 1.25 and 1.5 (even)
+        (-0.5, 0xB8), (57344.0, 0x7B), (61440.0, 0x7B), (1e9, 0x7B), (-1e9, 0xFB),  # saturation
+        (2.0 ** -14, 0x04), (2.0 ** -16, 0x01), (2.0 ** -17, 0x00), (3 * 2.0 ** -17, 0x02),  # subnormals, ties
+        (0.0, 0x00), (-0.0, 0x80),
+    ]
+    got = oracle.quantize_e5m2(np.array([x for x, _ in cases]))
+    assert [int(x) for x in got] == [c for _, c in cases]
+    # the rounding error stays within half a quantum (2 mantissa bits)
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-8, 8, 20000))
+    x = x[np.abs(x) < 57344]
+    back = oracle.dequantize_e5m2(oracle.quantize_e5m2(x))
+    quantum = np.ldexp(1.0, np.maximum(np.floor(np.log2(np.abs(x))).astype(int) - 2, -16))
+    assert np.all(np.abs(back - x) <= quantum / 2)
+
+
+def test_e5m2_decode_step_pins():
+    """The e5m2 step is attention over the decoded cache, with the new token
+    rotated in fp64 and rounded once to e5m2; only the new slot changes;
+    paged equals contiguous on the same logical data."""
+    rng = np.random.default_rng(42)
+    B, h_q, h_kv, d, cap = 2, 8, 2, 64, 48
+    kc = oracle.quantize_e5m2(rng.standard_normal((B, h_kv, cap, d)))
+    vc = oracle.quantize_e5m2(rng.standard_normal((B, h_kv, cap, d)))
+    q = oracle.round_bf16(rng.standard_normal((B, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    lens = np.array([48, 20])
+    r = oracle.decode_step_e5m2(kc, vc, q, k, v, lens, 10000.0, 0.125)
+    for b in range(B):
+        L = int(lens[b])
+        Kd = oracle.dequantize_e5m2(r["k_codes"][b, :, :L])
+        Vd = oracle.dequantize_e5m2(r["v_codes"][b, :, :L])
+        out, _ = oracle.gqa_attention(oracle.rope_rotate(q[b], L - 1, 10000.0), Kd, Vd, 0.125)
+        assert np.array_equal(out, r["out"][b])
+        assert np.array_equal(r["k_codes"][b, :, L - 1], oracle.quantize_e5m2(oracle.rope_rotate(k[b], L - 1, 10000.0)))
+        assert np.array_equal(r["v_codes"][b, :, L - 1], oracle.quantize_e5m2(v[b]))
+        assert np.array_equal(np.delete(r["k_codes"][b], L - 1, axis=1), np.delete(kc[b], L - 1, axis=1))
+        assert np.array_equal(np.delete(r["v_codes"][b], L - 1, axis=1), np.delete(vc[b], L - 1, axis=1))
+    pk, table = _contiguous_to_paged(kc, lens, 16, np.random.default_rng(2))
+    pv, _ = _contiguous_to_paged(vc, lens, 16, np.random.default_rng(2))
+    rp = oracle.decode_step_e5m2(pk.astype(np.uint8), pv.astype(np.uint8), q, k, v, lens, 10000.0, 0.125,
+                                 block_table=table, page_size=16)
+    assert np.array_equal(rp["out"], r["out"])
+
+
 # ------------------------------------------- multi-token (verify) decode
 def _multi_variant(K, V, q, k, v, lens, base, scale, dtype, rot_of, end_of):
     """A restatement of the multi-token step with the RoPE position of new
