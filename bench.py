@@ -8,7 +8,7 @@ The default workload is the Llama-style GQA decode step (batch 32, 32 query
 heads, 8 KV heads, head_dim 128, 4096-token bf16 cache, RoPE base 10000).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--cache native|u8] [--window W]
+                  [--workload NAME] [--cache native|u8|fp8] [--window W]
 
 ``value`` is the achieved HBM throughput of the step in GB/s (algorithmic
 bytes / device time, summed over ranks); ``ms_per_step`` gives the step time.
@@ -16,7 +16,8 @@ Under torchrun each rank runs its own batch (weak scaling, no collective on
 the data path). ``--impl reference`` times the fp64 CPU oracle on the host
 cores instead, one (sequence, kv head) unit of the same workload per step.
 ``--cache u8`` runs the same workload over a uint8 cache (codes plus a float32
-(scale, zero point) pair per cached row, as the pages' QuantizedKVCache).
+(scale, zero point) pair per cached row, as the pages' QuantizedKVCache);
+``--cache fp8`` over an fp8 e5m2 cache (one byte per element, no scale).
 """
 
 from __future__ import annotations
@@ -41,7 +42,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from synthetic import make_contiguous_case, make_paged_case, make_u8_cache, normal, workload  # noqa: E402
+from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, make_u8_cache, normal, workload  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 GPU"
 UNIT = "GB/s"
@@ -118,7 +119,9 @@ def attended(lens, window: int, n_new: int = 1):
 def row_bytes(w, cache: str) -> int:
     """Bytes of one cached (token, kv head) row of K (or V): head_dim values,
     or head_dim uint8 codes plus the float32 (scale, zero point) pair."""
-    return w.head_dim + 8 if cache == "u8" else w.head_dim * w.esize
+    if cache == "u8":
+        return w.head_dim + 8
+    return w.head_dim if cache == "fp8" else w.head_dim * w.esize
 
 
 def step_bytes(w, lens, out_esize, window: int = 0, cache: str = "native", n_new: int = 1):
@@ -221,24 +224,29 @@ S_QM, S_KM, S_VM = 21, 22, 23  # seeded streams of multi-token q, k, v
 def build_case(w, device, cache: str = "native", n_new: int = 1):
     """The workload's seeded inputs. With cache "u8" the K/V caches are
     replaced by uint8 codes and (scale, zero point) pairs of the same rows
-    (attributes u8 = synthetic.U8Cache). With n_new > 1 the new tokens are
-    [B, n_new, H, d] and pos = seq_lens - n_new."""
+    (attributes u8 = synthetic.U8Cache), with cache "fp8" by fp8 e5m2 caches
+    (attribute f8 = (K, V)). With n_new > 1 the new tokens are [B, n_new, H, d]
+    and pos = seq_lens - n_new."""
     case = make_paged_case(w, device) if w.paged else make_contiguous_case(w, device)
     case.u8 = None
+    case.f8 = None
     case.n_new = n_new
     if n_new > 1:
         case.q_new = normal((w.batch, n_new, w.h_q, w.head_dim), w.seed, S_QM, w.dtype, device)
         case.k_new = normal((w.batch, n_new, w.h_kv, w.head_dim), w.seed, S_KM, w.dtype, device)
         case.v_new = normal((w.batch, n_new, w.h_kv, w.head_dim), w.seed, S_VM, w.dtype, device)
         case.pos = (case.seq_lens - n_new).to(torch.int32)
-    if cache == "u8":
+    if cache in ("u8", "fp8"):
         if w.paged:
             rows = (case.num_pages, w.h_kv, case.page_size)
             case.k_pool = case.v_pool = None
         else:
             rows = (w.batch, w.h_kv, case.capacity)
             case.k_cache = case.v_cache = None
-        case.u8 = make_u8_cache(rows, w.head_dim, U8_SEED, device=device)
+        if cache == "u8":
+            case.u8 = make_u8_cache(rows, w.head_dim, U8_SEED, device=device)
+        else:
+            case.f8 = make_e5m2_cache(rows, w.head_dim, U8_SEED, device=device)
     return case
 
 
@@ -268,6 +276,9 @@ def unit_inputs(w, case, units):
             c = case.u8
             u.update(Kc=_rows(w, case, c.k_codes, b, j, L), Ks=_rows(w, case, c.k_sz, b, j, L),
                      Vc=_rows(w, case, c.v_codes, b, j, L), Vs=_rows(w, case, c.v_sz, b, j, L))
+        elif case.f8 is not None:
+            u.update(K8=_rows(w, case, case.f8[0].view(torch.uint8), b, j, L),
+                     V8=_rows(w, case, case.f8[1].view(torch.uint8), b, j, L))
         else:
             kc, vc = (case.k_pool, case.v_pool) if w.paged else (case.k_cache, case.v_cache)
             u.update(K=_rows(w, case, kc, b, j, L), V=_rows(w, case, vc, b, j, L))
@@ -286,6 +297,11 @@ def oracle_unit(w, u, window: int = 0):
     import oracle  # test infrastructure: the CPU-baseline and reference legs only
 
     scale = 1.0 / math.sqrt(w.head_dim)
+    if "K8" in u:
+        r = oracle.decode_step_e5m2(u["K8"][None, None].numpy(), u["V8"][None, None].numpy(), u["q"][None],
+                                    u["k"][None, None], u["v"][None, None], [u["L"]], w.rope_base, scale,
+                                    window=window)
+        return r["out"][0]
     if "Kc" in u:
         L = u["L"]
         r = oracle.decode_step_u8(u["Kc"][None, None], u["Ks"][None, None], u["Vc"][None, None], u["Vs"][None, None],
@@ -338,6 +354,8 @@ def bench_ours(args):
     if args.batch:
         w = w.with_(batch=args.batch)
     u8 = args.cache == "u8"
+    f8 = args.cache == "fp8"
+    byte = u8 or f8  # a one-byte cache: the uint8 / e5m2 kernels
     nn = args.n_new
     case = build_case(w, dev, args.cache, nn)
     lens_cpu = case.seq_lens.cpu()
@@ -350,6 +368,11 @@ def bench_ours(args):
         else:
             lay = m.layout_contiguous(c.k_codes, c.v_codes, w.h_q, window=args.window, k_scale_zero=c.k_sz,
                                       v_scale_zero=c.v_sz)
+    elif f8:
+        if w.paged:
+            lay = m.layout_paged(case.f8[0], case.f8[1], case.block_table, w.h_q, window=args.window)
+        else:
+            lay = m.layout_contiguous(case.f8[0], case.f8[1], w.h_q, window=args.window)
     elif w.paged:
         lay = m.layout_paged(case.k_pool, case.v_pool, case.block_table, w.h_q, window=args.window)
     else:
@@ -391,9 +414,9 @@ def bench_ours(args):
     # contiguous bf16 cache with head_dim 128 run on the tcgen05 kernel, the
     # rest on the warp-MMA kernels; a one-token step is one launch (the append
     # inside the attention kernel) when one block serves all of a kv head's heads
-    tc05 = (not u8 and variant in (0, 2) and w.dtype == "bf16" and not w.paged and w.head_dim == 128
+    tc05 = (not byte and variant in (0, 2) and w.dtype == "bf16" and not w.paged and w.head_dim == 128
             and w.group * nn >= 32)
-    fused = (not u8 and nn == 1 and variant in (0, 2) and w.dtype == "bf16"
+    fused = (not byte and nn == 1 and variant in (0, 2) and w.dtype == "bf16"
              and (w.group <= 128 if tc05 else w.group <= 32))
     launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
 
@@ -485,7 +508,7 @@ def bench_ours(args):
     e2e_value = throughput_gbs(world, sbytes, e2e_ms / K)
 
     peak, peak_src = measured_peak()
-    if u8:
+    if byte:
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
         kernel_name = "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel"
     elif tc05:
@@ -511,7 +534,7 @@ def bench_ours(args):
         roof_kernel = kernel_name + (" + combine_kernel" if splits_used > 1 else "")
         roof_time = "events around each standalone gqa_decode_attention call"
     achieved = roof_bytes / (roof_ms * 1e-3) / 1e9
-    traffic = (ncu_traffic(args.workload + ("_u8" if u8 else "")) if kernel_name.startswith(("decode_mma", "decode_u8", "attn_tc05"))
+    traffic = (ncu_traffic(args.workload + ("_" + args.cache if byte else "")) if kernel_name.startswith(("decode_mma", "decode_u8", "attn_tc05"))
                else None)
     clocks = sampler.summary(t_clock0, t_clock1)
 
@@ -527,18 +550,21 @@ def bench_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u8" if u8 else w.dtype,
+        "dtype": args.cache if byte else w.dtype,
         "data": ("synthetic (seeded N(0,1) bf16 q/k/v; uint8 cache codes U[0,255], scales ~6/255, zero points "
-                 "U[100,155]; no dataset)" if u8 else "synthetic (seeded N(0,1) bf16 q/k/v and cache; no dataset)"),
+                 "U[100,155]; no dataset)" if u8 else
+                 "synthetic (seeded N(0,1) bf16 q/k/v; N(0,1) cache rounded to fp8 e5m2; no dataset)" if f8 else
+                 "synthetic (seeded N(0,1) bf16 q/k/v and cache; no dataset)"),
         "config": {
             "workload": (f"{w.name}: batch {w.batch}, H_q {w.h_q}, H_kv {w.h_kv}, head_dim {w.head_dim}, "
                          + (f"paged {w.page_size}-token pages, lengths U[{w.len_lo},{w.len_hi}]" if w.paged
-                            else f"contiguous {'uint8' if u8 else w.dtype} cache of {w.seq_len} tokens/seq")
+                            else f"contiguous {'uint8' if u8 else 'fp8 e5m2' if f8 else w.dtype} cache of "
+                                 f"{w.seq_len} tokens/seq")
                          + (", uint8 cache codes + float32 (scale, zero point) per row" if u8 else "")
                          + (f", {nn} new tokens per sequence verified in one pass (causal among them)"
                             if nn > 1 else "")
                          + ", RoPE base 10000"),
-            "cache": "u8" if u8 else w.dtype,
+            "cache": args.cache if byte else w.dtype,
             "n_new": nn,
             "batch_per_gpu": w.batch,
             "tokens_per_step_per_gpu": int(lens_cpu.sum()),
@@ -730,7 +756,8 @@ def bench_reference(args):
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
         "impl": "reference",
-        "config": {"workload": w.name, "cache": args.cache if args.cache == "u8" else w.dtype, "window": args.window,
+        "config": {"workload": w.name, "cache": args.cache if args.cache in ("u8", "fp8") else w.dtype,
+                   "window": args.window,
                    "n_new": args.n_new,
                    "batch_per_gpu": w.batch, "tokens_per_step_per_gpu": int(lens.sum()),
                    "step": "one (sequence, kv head) unit of the workload per step, cycling over the units"},
@@ -759,7 +786,7 @@ def main():
                     help="time prefill of this many prompt tokens per sequence instead of a decode step")
     ap.add_argument("--n-new", type=int, default=1,
                     help="new tokens per sequence (the verification pass of speculative decoding)")
-    ap.add_argument("--cache", choices=["native", "u8"], default="native",
+    ap.add_argument("--cache", choices=["native", "u8", "fp8"], default="native",
                     help="cache type: the workload's own (bf16 / fp32) or uint8 codes with per-row scale / zero point")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-units", type=int, default=0, help="distinct units in the CPU sample (0 = all)")

@@ -70,7 +70,8 @@ typedef enum mqa_status {
 typedef enum mqa_dtype {
   MQA_BF16 = 0,
   MQA_F32 = 1,
-  MQA_U8 = 2 /* cache only: uint8 codes + (scale, zero point) per cached (token, kv head); q/k/v new in bf16 */
+  MQA_U8 = 2, /* cache only: uint8 codes + (scale, zero point) per cached (token, kv head); q/k/v new in bf16 */
+  MQA_FP8_E5M2 = 3 /* cache only: fp8 e5m2 values, one byte per element; q/k/v new in bf16 */
 } mqa_dtype;
 
 /* Which decode-attention kernel to run (gqa_decode_attention `variant`). */
@@ -114,6 +115,14 @@ typedef enum mqa_variant {
  * key is quantised after its fp64 rotation, rounded to float32. q_new,
  * k_new and v_new are bf16. Attention over a MQA_U8 cache runs on tensor
  * cores only.
+ *
+ * MQA_FP8_E5M2 cache (the fp8_e5m2 KV-cache dtype of the pages' vLLM
+ * serving examples): one byte per element, 1 sign, 5 exponent (bias 15) and
+ * 2 mantissa bits, no scale; k_scale_zero / v_scale_zero are unused.
+ * kv_append_rope rounds the new row to nearest (ties to even) -- the key
+ * once, from its fp64 rotation -- and saturates magnitudes beyond 57344 to
+ * it. q_new, k_new and v_new are bf16; attention on tensor cores only, one
+ * new token per sequence.
  *
  * window: 0 = the attention reads every cached token [0, L); W > 0 = a
  * sliding window: only the last W tokens [max(0, L - W), L) are read

@@ -27,6 +27,7 @@ from ._abi import (
     MQA_DEVERR_U8_SCALE,
     MQA_F32,
     MQA_U8,
+    MQA_FP8_E5M2,
     MQA_VARIANT_AUTO,
     MQA_VARIANT_CUDA_CORE,
     MQA_VARIANT_TENSOR_CORE,
@@ -59,6 +60,7 @@ __all__ = [
     "MQA_DEVERR_TIMEOUT",
     "MQA_DEVERR_U8_SCALE",
     "MQA_U8",
+    "MQA_FP8_E5M2",
 ]
 
 
@@ -83,6 +85,8 @@ def _dtype_code(dt: torch.dtype) -> int:
         return MQA_F32
     if dt == torch.uint8:
         return MQA_U8
+    if dt == torch.float8_e5m2:
+        return MQA_FP8_E5M2
     raise TypeError(f"unsupported dtype {dt}")
 
 
@@ -99,9 +103,9 @@ def _stream(stream) -> int | None:
 def layout_contiguous(k_cache: torch.Tensor, v_cache: torch.Tensor, h_q: int, window: int = 0,
                       k_scale_zero: torch.Tensor | None = None, v_scale_zero: torch.Tensor | None = None) -> KVLayout:
     """Layout of a contiguous cache pair, each [batch, h_kv, capacity, head_dim]
-    (bf16, fp32, or uint8 codes with float32 [batch, h_kv, capacity, 2] scale /
-    zero-point pairs); window > 0 restricts the attention to the last `window`
-    tokens."""
+    (bf16, fp32, fp8 e5m2, or uint8 codes with float32 [batch, h_kv, capacity,
+    2] scale / zero-point pairs); window > 0 restricts the attention to the
+    last `window` tokens."""
     assert k_cache.shape == v_cache.shape and k_cache.dim() == 4
     assert k_cache.is_contiguous() and v_cache.is_contiguous()
     B, h_kv, cap, d = k_cache.shape

@@ -19,6 +19,7 @@ MQA_ERR_WORKSPACE = 4
 MQA_BF16 = 0
 MQA_F32 = 1
 MQA_U8 = 2
+MQA_FP8_E5M2 = 3
 
 MQA_VARIANT_AUTO = 0
 MQA_VARIANT_CUDA_CORE = 1

@@ -31,7 +31,8 @@ bool is_pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
 
 mqa_status check_layout(const mqa_kv_layout* L) {
   if (L == nullptr) return MQA_ERR_INVALID_ARG;
-  if (L->cache_dtype != MQA_BF16 && L->cache_dtype != MQA_F32 && L->cache_dtype != MQA_U8)
+  if (L->cache_dtype != MQA_BF16 && L->cache_dtype != MQA_F32 && L->cache_dtype != MQA_U8 &&
+      L->cache_dtype != MQA_FP8_E5M2)
     return MQA_ERR_UNSUPPORTED;
   if (L->cache_dtype == MQA_U8) {
     if (L->k_scale_zero == nullptr || L->v_scale_zero == nullptr) return MQA_ERR_INVALID_ARG;
@@ -65,16 +66,25 @@ int resolve_variant(const mqa_kv_layout* L, int variant) {
   return variant;
 }
 
-// Which cache dtypes a kernel family reads: tensor cores bf16 and uint8,
-// CUDA cores bf16 and fp32.
+// Which cache dtypes a kernel family reads: tensor cores bf16, uint8 and fp8
+// e5m2, CUDA cores bf16 and fp32.
 bool variant_supports(int variant, int cache_dtype) {
-  if (variant == MQA_VARIANT_TENSOR_CORE) return cache_dtype == MQA_BF16 || cache_dtype == MQA_U8;
+  if (variant == MQA_VARIANT_TENSOR_CORE)
+    return cache_dtype == MQA_BF16 || cache_dtype == MQA_U8 || cache_dtype == MQA_FP8_E5M2;
   return cache_dtype == MQA_BF16 || cache_dtype == MQA_F32;
 }
 
 int dtype_code(int cache_dtype) {
-  return cache_dtype == MQA_BF16 ? kDtypeBf16 : (cache_dtype == MQA_F32 ? kDtypeF32 : kDtypeU8);
+  switch (cache_dtype) {
+    case MQA_BF16: return kDtypeBf16;
+    case MQA_F32: return kDtypeF32;
+    case MQA_U8: return kDtypeU8;
+    default: return kDtypeF8;
+  }
 }
+
+// one-byte caches: uint8 codes with (scale, zero) rows, or fp8 e5m2
+bool byte_cache(int cache_dtype) { return cache_dtype == MQA_U8 || cache_dtype == MQA_FP8_E5M2; }
 
 struct DeviceInfo {
   int sms = 0;
@@ -110,7 +120,8 @@ bool use_tc05(const mqa_kv_layout* L, int variant, int n_new) {
 KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
   const int G = L->h_q / L->h_kv;
   if (use_tc05(L, variant, n_new)) return tc05_shape();
-  if (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_U8) return decode_u8_shape(L->head_dim, G);
+  if (variant == MQA_VARIANT_TENSOR_CORE && byte_cache(L->cache_dtype))
+    return decode_u8_shape(L->head_dim, G, L->cache_dtype == MQA_FP8_E5M2);
   if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G * n_new);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
 }
@@ -272,6 +283,7 @@ bool make_tensor_map(CUtensorMap* map, void* base, const mqa_kv_layout* L, bool 
 // zero) rows as float32 runs of 2 x `rows` values per head. `heads` > 1 only
 // for paged pools, where the heads of one page are consecutive.
 bool make_u8_maps(CUtensorMap* maps, const mqa_kv_layout* L, int rows_in, int heads) {
+  const bool f8 = L->cache_dtype == MQA_FP8_E5M2;  // codes only: the (scale, zero) maps repeat the code maps
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t D = L->head_dim;
@@ -308,6 +320,11 @@ bool make_u8_maps(CUtensorMap* maps, const mqa_kv_layout* L, int rows_in, int he
            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
+  }
+  if (f8) {
+    maps[2] = maps[0];
+    maps[3] = maps[1];
+    return true;
   }
   for (int i = 0; i < 2; ++i) {
     cuuint64_t dims[3], strides[2];
@@ -541,7 +558,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     if (e != cudaSuccess) return fail_cuda(e);
     goto combine;
   }
-  if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_U8) {
+  if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype)) {
     CUtensorMap maps[4];
     // Paged 16- / 32-token pages: blocks over groups of kv heads, one box per
     // page and head group (long contiguous runs of the pool).

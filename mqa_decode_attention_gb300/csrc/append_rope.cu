@@ -18,6 +18,7 @@
 // multiply-add), then rounded once to the cache dtype; the query is rotated
 // in fp32 and written as fp32.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/mqa_decode.h"
 #include "launch.h"
@@ -77,7 +78,28 @@ __device__ __forceinline__ uint32_t u8_code(float x, float2 sz) {
   return static_cast<uint32_t>(fminf(fmaxf(rintf(__fadd_rn(__fdiv_rn(x, sz.x), sz.y)), 0.0f), 255.0f));
 }
 
-template <typename T, bool QU8>
+// fp8 e5m2 code of x: 1 sign, 5 exponent (bias 15), 2 mantissa bits. x is
+// rounded once, to nearest with ties to even, at a quantum of 2 bits below
+// its leading bit (never below the subnormal quantum 2^-16); magnitudes past
+// the largest finite value 57344 saturate to it, NaN gives a NaN code. The
+// rounded value is an IEEE half whose low byte is zero: its high byte is the
+// code.
+__device__ __forceinline__ uint32_t e5m2_code(double x) {
+  uint32_t code = 0x7Fu;
+  if (!isnan(x)) {
+    const double ax = fabs(x);
+    double r = 57344.0;
+    if (ax < 57344.0) {
+      const int e = ax > 0.0 ? ilogb(ax) : -14;
+      const int qe = (e < -14 ? -14 : e) - 2;
+      r = fmin(ldexp(rint(ldexp(ax, -qe)), qe), 57344.0);
+    }
+    code = static_cast<uint32_t>(__half_as_ushort(__double2half(r))) >> 8;
+  }
+  return code | (signbit(x) ? 0x80u : 0u);
+}
+
+template <typename T, bool QU8, bool F8 = false>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const AppendParams p) {
   __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];
   __shared__ float s_red[kAppendThreads / 32][4];  // uint8 cache: per-warp k/v min and max
@@ -221,6 +243,30 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
     return;
   }
 
+  if constexpr (F8) {
+    // e5m2 cache: k from its fp64 rotation and v from its bf16 value, each
+    // rounded once to e5m2
+    const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
+    uint8_t* kc = static_cast<uint8_t*>(p.k_cache) + s_row;
+    uint8_t* vc = static_cast<uint8_t*>(p.v_cache) + s_row;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int idx = u == 0 ? i0 : i1;
+      if (idx >= n_pairs) continue;
+      const float2 x = u == 0 ? x0 : x1;
+      const int h = h_begin + idx / half, i = idx % half;
+      const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
+      const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
+      const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
+      const float2 vv = Elem<T>::load2(v + h * D + 2 * i);
+      *reinterpret_cast<uint16_t*>(kc + h * s_stride + 2 * i) =
+          static_cast<uint16_t>(e5m2_code(xr) | (e5m2_code(yr) << 8));
+      *reinterpret_cast<uint16_t*>(vc + h * s_stride + 2 * i) =
+          static_cast<uint16_t>(e5m2_code(vv.x) | (e5m2_code(vv.y) << 8));
+    }
+    return;
+  }
+
   // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
   const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
   T* kc = static_cast<T*>(p.k_cache) + s_row;
@@ -324,7 +370,7 @@ KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  if (p.cache_dtype != kDtypeU8 && static_cast<long long>(p.batch) * p.n_new >= 1024) {
+  if ((p.cache_dtype == kDtypeBf16 || p.cache_dtype == kDtypeF32) && static_cast<long long>(p.batch) * p.n_new >= 1024) {
     // enough tokens to fill the GPU with one block each
     cfg.gridDim = dim3(p.batch * p.n_new);
     cfg.blockDim = dim3(kAppendThreads);
@@ -338,6 +384,7 @@ cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   if (p.cache_dtype == kDtypeU8) return cudaLaunchKernelEx(&cfg, append_rope_kernel<__nv_bfloat16, true>, p);
+  if (p.cache_dtype == kDtypeF8) return cudaLaunchKernelEx(&cfg, append_rope_kernel<__nv_bfloat16, false, true>, p);
   if (p.cache_dtype == kDtypeBf16) return cudaLaunchKernelEx(&cfg, append_rope_kernel<__nv_bfloat16, false>, p);
   return cudaLaunchKernelEx(&cfg, append_rope_kernel<float, false>, p);
 }

@@ -16,6 +16,10 @@
 // reads its codes as whole 16-byte words (see the fragment notes below), and
 // the output's dims are put back in order when the block merges its warps.
 //
+// The same kernels read an fp8 e5m2 cache (template flag F8): an e5m2 value
+// is an IEEE half with its low byte zero, so a byte permute makes the exact
+// fp16 operand, and there is no scale, zero point or P' factor.
+//
 // Block = 4 consumer warps per head block of 16 query heads + 1 producer warp.
 // The producer streams 64-token tiles of codes (TMA, 128- or 64-byte swizzle)
 // and of the (scale, zero) rows, contiguous or page by page through the block
@@ -41,13 +45,13 @@ struct U8Stages {
   static constexpr int value = D == 128 ? 6 : 8;  // even: a tile's parity fixes its stages
 };
 
-template <int D, int HB, int STAGES>
+template <int D, int HB, int STAGES, bool F8 = false>
 struct U8Cfg {
   static constexpr int kConsumerWarps = 4 * HB;
   static constexpr int kConsumerThreads = 32 * kConsumerWarps;
   static constexpr int kThreads = kConsumerThreads + 32;
   static constexpr int kCodeBytes = kTile * D;  // codes of a K (or V) tile
-  static constexpr int kSzBytes = kTile * 8;    // (scale, zero) pairs of a tile
+  static constexpr int kSzBytes = F8 ? 0 : kTile * 8;  // (scale, zero) pairs of a tile
   static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSzBytes;
   static constexpr int kPipeBytes = STAGES * kStageBytes;
   static constexpr int kMergeStride = D + 4;
@@ -110,6 +114,10 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
 __device__ __forceinline__ uint32_t codes_f16(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x64u, sel); }
 constexpr uint32_t kSelLo = 0x4140u;
 constexpr uint32_t kSelHi = 0x4342u;
+// Two e5m2 codes of w (bytes 0, 1 / bytes 2, 3) as the fp16 pair whose high
+// bytes they are: exact.
+constexpr uint32_t kF8Lo = 0x1404u;
+constexpr uint32_t kF8Hi = 0x3424u;
 
 // One warp's share of the attention over a uint8 cache: up to 16 query heads
 // (MMA rows) against 32 consecutive tokens per step.
@@ -129,7 +137,7 @@ constexpr uint32_t kSelHi = 0x4342u;
 //   O   = sum_t p'_t (1024 + c_t) - sum_t p'_t (1024 + z_t),
 // the last sum being one more n8 MMA tile whose B column is 1024 + z_t, so it
 // sees exactly the fp16 P' the data columns see.
-template <int D>
+template <int D, bool F8 = false>
 struct WarpAttnU8 {
   uint32_t qa[D / 16][4];  // Q (fp16, log2-domain scale folded in), permuted dims
   float o[D / 8][4];       // O + zero-point terms: rows g (regs 0,1) and g + 8 (regs 2,3)
@@ -178,7 +186,10 @@ struct WarpAttnU8 {
   __device__ __forceinline__ void step(uint32_t kc, uint32_t vc, uint32_t ksz, uint32_t vsz, int trow0, int lo,
                                        int hi, int lane) {
     const int g = lane >> 2, c = lane & 3;
-    // ---- raw scores sum_d q_d (1024 + c_td): four n8 tiles, four independent MMA chains
+    auto lo2 = [](uint32_t x) { return F8 ? __byte_perm(x, 0u, kF8Lo) : codes_f16(x, kSelLo); };
+    auto hi2 = [](uint32_t x) { return F8 ? __byte_perm(x, 0u, kF8Hi) : codes_f16(x, kSelHi); };
+    // ---- raw scores sum_d q_d (1024 + c_td) (e5m2: sum_d q_d k_td): four n8
+    // tiles, four independent MMA chains
     float s[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -200,12 +211,13 @@ struct WarpAttnU8 {
       }
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_f16_16816(s[nt], qa[ks], codes_f16(w[ks], kSelLo), codes_f16(w[ks], kSelHi));
+        mma_f16_16816(s[nt], qa[ks], lo2(w[ks]), hi2(w[ks]));
     }
     // ---- scales and zero points of this lane's columns: tokens 8 nt + 2c + {0, 1}
     float sv[4][2], zv[4][2];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
+      if constexpr (F8) break;
       const float4 kq = lds_f4(ksz + sz_off<SBS>(trow0 + nt * 8 + 2 * c));
       const float4 vq = lds_f4(vsz + sz_off<SBS>(trow0 + nt * 8 + 2 * c));
       const float off0 = 1024.f + kq.y, off1 = 1024.f + kq.w;
@@ -218,7 +230,8 @@ struct WarpAttnU8 {
       sv[nt][1] = vq.z;
       zv[nt][1] = vq.w;
     }
-    if (lo > 0 || hi < 32) {  // a partial step: mask the rows outside [lo, hi)
+    const bool partial = lo > 0 || hi < 32;
+    if (partial) {  // a partial step: mask the rows outside [lo, hi)
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
@@ -233,8 +246,10 @@ struct WarpAttnU8 {
         }
       }
     }
+    if constexpr (!F8) {
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) vmax = fmaxf(vmax, fmaxf(sv[nt][0], sv[nt][1]));
+      for (int nt = 0; nt < 4; ++nt) vmax = fmaxf(vmax, fmaxf(sv[nt][0], sv[nt][1]));
+    }
     // ---- online softmax (log2 domain), rows g and g + 8
     float mx0 = fmaxf(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])),
                       fmaxf(fmaxf(s[2][0], s[2][1]), fmaxf(s[3][0], s[3][1])));
@@ -270,10 +285,12 @@ struct WarpAttnU8 {
         o[n][2] *= a1;
         o[n][3] *= a1;
       }
-      cz[0] *= a0;
-      cz[1] *= a0;
-      cz[2] *= a1;
-      cz[3] *= a1;
+      if constexpr (!F8) {
+        cz[0] *= a0;
+        cz[1] *= a0;
+        cz[2] *= a1;
+        cz[3] *= a1;
+      }
     }
     // ---- P' = p s^v kPScale and the zero-point column 1024 + z, packed to fp16
     // for both 16-token halves before the V codes are read
@@ -281,6 +298,13 @@ struct WarpAttnU8 {
 #pragma unroll
     for (int kh = 0; kh < 2; ++kh) {
       const int n0 = 2 * kh, n1 = 2 * kh + 1;
+      if constexpr (F8) {  // P as it is
+        pa[kh][0] = pack_f16x2(pr[n0][0], pr[n0][1]);
+        pa[kh][1] = pack_f16x2(pr[n0][2], pr[n0][3]);
+        pa[kh][2] = pack_f16x2(pr[n1][0], pr[n1][1]);
+        pa[kh][3] = pack_f16x2(pr[n1][2], pr[n1][3]);
+        continue;
+      }
       const float w00 = sv[n0][0] * kPScale, w01 = sv[n0][1] * kPScale;
       const float w10 = sv[n1][0] * kPScale, w11 = sv[n1][1] * kPScale;
       pa[kh][0] = pack_f16x2(pr[n0][0] * w00, pr[n0][1] * w01);
@@ -293,7 +317,7 @@ struct WarpAttnU8 {
     // ---- O += P' (1024 + V codes), cz += P' (1024 + z), per 16-token half
 #pragma unroll
     for (int kh = 0; kh < 2; ++kh) {
-      mma_f16_16816(cz, pa[kh], zb[kh][0], zb[kh][1]);
+      if constexpr (!F8) mma_f16_16816(cz, pa[kh], zb[kh][0], zb[kh][1]);
       const int r0 = trow0 + 16 * kh + 2 * c;
       // this lane's dims g (D/8) .. g (D/8) + D/8 - 1 of tokens 2c, 2c+1, 2c+8, 2c+9 of the half
       uint32_t ra[D / 32], rb[D / 32], rc[D / 32], rd[D / 32];
@@ -320,15 +344,31 @@ struct WarpAttnU8 {
         rc[0] = sw ? y3.x : y2.x; rc[1] = sw ? y3.y : y2.y;
         rd[0] = sw ? y2.x : y3.x; rd[1] = sw ? y2.y : y3.y;
       }
+      if constexpr (F8) {
+        // tokens outside [lo, hi) may hold any byte, NaN codes included: their
+        // P is 0, and 0 * NaN would still poison O, so their codes become 0
+        if (partial) {
+          const int t0 = 16 * kh + 2 * c;
+          const bool da = t0 < lo || t0 >= hi, db = t0 + 1 < lo || t0 + 1 >= hi;
+          const bool dc = t0 + 8 < lo || t0 + 8 >= hi, dd = t0 + 9 < lo || t0 + 9 >= hi;
+#pragma unroll
+          for (int wi = 0; wi < D / 32; ++wi) {
+            if (da) ra[wi] = 0u;
+            if (db) rb[wi] = 0u;
+            if (dc) rc[wi] = 0u;
+            if (dd) rd[wi] = 0u;
+          }
+        }
+      }
 #pragma unroll
       for (int wi = 0; wi < D / 32; ++wi) {
         // interleave the codes of tokens (2c, 2c+1) and (2c+8, 2c+9) byte by byte
         const uint32_t x01 = __byte_perm(ra[wi], rb[wi], 0x5140u), y01 = __byte_perm(ra[wi], rb[wi], 0x7362u);
         const uint32_t x89 = __byte_perm(rc[wi], rd[wi], 0x5140u), y89 = __byte_perm(rc[wi], rd[wi], 0x7362u);
-        mma_f16_16816(o[4 * wi + 0], pa[kh], codes_f16(x01, kSelLo), codes_f16(x89, kSelLo));
-        mma_f16_16816(o[4 * wi + 1], pa[kh], codes_f16(x01, kSelHi), codes_f16(x89, kSelHi));
-        mma_f16_16816(o[4 * wi + 2], pa[kh], codes_f16(y01, kSelLo), codes_f16(y89, kSelLo));
-        mma_f16_16816(o[4 * wi + 3], pa[kh], codes_f16(y01, kSelHi), codes_f16(y89, kSelHi));
+        mma_f16_16816(o[4 * wi + 0], pa[kh], lo2(x01), lo2(x89));
+        mma_f16_16816(o[4 * wi + 1], pa[kh], hi2(x01), hi2(x89));
+        mma_f16_16816(o[4 * wi + 2], pa[kh], lo2(y01), lo2(y89));
+        mma_f16_16816(o[4 * wi + 3], pa[kh], hi2(y01), hi2(y89));
       }
     }
   }
@@ -340,6 +380,7 @@ struct WarpAttnU8 {
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if constexpr (F8) return;
     constexpr float inv = 1.0f / kPScale;
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
@@ -351,12 +392,12 @@ struct WarpAttnU8 {
   }
 };
 
-template <int D, int HB, int STAGES>
-__global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 1)
+template <int D, int HB, int STAGES, bool F8>
+__global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 2 : 1)
     decode_u8_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                      const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
                      const DecodeParams p) {
-  using C = U8Cfg<D, HB, STAGES>;
+  using C = U8Cfg<D, HB, STAGES, F8>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -443,8 +484,10 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 
           const int row = b * p.h_kv + j;
           tma_load_3d(kc, &tm_kc, 0, t0, row, fb);
           tma_load_3d(vc, &tm_vc, 0, t0, row, fb);
-          tma_load_2d(ksd, &tm_ks, 2 * t0, row, fb);
-          tma_load_2d(vsd, &tm_vs, 2 * t0, row, fb);
+          if constexpr (!F8) {
+            tma_load_2d(ksd, &tm_ks, 2 * t0, row, fb);
+            tma_load_2d(vsd, &tm_vs, 2 * t0, row, fb);
+          }
         }
       } else {
         int pg[kTile / 16];
@@ -477,8 +520,10 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 
             const int page = pg[k] < 0 ? p.num_pages : pg[k];
             tma_load_4d(kc + k * rpc * D, &tm_kc, 0, r, j, page, fb);
             tma_load_4d(vc + k * rpc * D, &tm_vc, 0, r, j, page, fb);
-            tma_load_3d(ksd + k * rpc * 8, &tm_ks, 2 * r, j, page, fb);
-            tma_load_3d(vsd + k * rpc * 8, &tm_vs, 2 * r, j, page, fb);
+            if constexpr (!F8) {
+              tma_load_3d(ksd + k * rpc * 8, &tm_ks, 2 * r, j, page, fb);
+              tma_load_3d(vsd + k * rpc * 8, &tm_vs, 2 * r, j, page, fb);
+            }
           }
         }
       }
@@ -498,7 +543,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 
   const int ws = warp & 3;
   const int head0 = (hsb * HB + hb) * 16;
   if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
-  WarpAttnU8<D> wa;
+  WarpAttnU8<D, F8> wa;
   wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
 
   // warps 0, 1 of a head block take the even tiles, warps 2, 3 the odd
@@ -525,7 +570,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }
   wa.finish();
-  if (__any_sync(0xffffffffu, wa.vmax > kMaxVScale) && lane == 0)
+  if (!F8 && __any_sync(0xffffffffu, wa.vmax > kMaxVScale) && lane == 0)
     atomicOr(p.err, static_cast<int>(MQA_DEVERR_U8_SCALE));
 
   // ------------------------------------------- merge the 4 token slices
@@ -590,11 +635,11 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES>::kThreads, HB == 1 ? 2 : 
   }
 }
 
-template <int D, int HB>
+template <int D, int HB, bool F8>
 cudaError_t launch_u8_t(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
   constexpr int ST = U8Stages<D>::value;
-  using C = U8Cfg<D, HB, ST>;
-  auto kern = decode_u8_kernel<D, HB, ST>;
+  using C = U8Cfg<D, HB, ST, F8>;
+  auto kern = decode_u8_kernel<D, HB, ST, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -612,13 +657,13 @@ cudaError_t launch_u8_t(const DecodeParams& p, const CUtensorMap* maps, cudaStre
 
 // Blocks per SM as the occupancy calculator sees them (registers bound the
 // 288-thread blocks to one); 0 if there is no device to ask.
-template <int D, int HB>
+template <int D, int HB, bool F8>
 KernelShape shape_t() {
-  using C = U8Cfg<D, HB, U8Stages<D>::value>;
+  using C = U8Cfg<D, HB, U8Stages<D>::value, F8>;
   static std::atomic<int> occ{-1};
   int n = occ.load(std::memory_order_relaxed);
   if (n < 0) {
-    auto kern = decode_u8_kernel<D, HB, U8Stages<D>::value>;
+    auto kern = decode_u8_kernel<D, HB, U8Stages<D>::value, F8>;
     n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmemBytes) != cudaSuccess) {
@@ -640,14 +685,14 @@ KernelShape shape_t() {
 // 16-token pages or one 32-token page) of the HG heads. Consumer warp w owns
 // kv head jg HG + w and its G <= 16 query heads, runs its own online softmax
 // over the block's token range and writes its rows itself.
-template <int D, int HG, int PS, int STAGES>
+template <int D, int HG, int PS, int STAGES, bool F8 = false>
 struct U8HeadsCfg {
   static constexpr int kTokens = 32;                 // per stage
   static constexpr int kRows = PS < 32 ? PS : 32;    // rows of one box
   static constexpr int kBoxes = kTokens / kRows;     // pages per stage
   static constexpr int kThreads = 32 * (HG + 1);
   static constexpr int kCodeBytes = HG * kTokens * D;
-  static constexpr int kSzBytes = HG * kTokens * 8;
+  static constexpr int kSzBytes = F8 ? 0 : HG * kTokens * 8;
   static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSzBytes;
   static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8 + 1024;
   // byte strides in a stage: between heads, and between 16-row blocks of a head
@@ -659,12 +704,12 @@ struct U8HeadsCfg {
   static_assert(kStageBytes % 1024 == 0, "stages stay 1 KB aligned (swizzle atoms)");
 };
 
-template <int D, int HG, int PS, int STAGES>
-__global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES>::kThreads, HG <= 4 ? 2 : 1)
+template <int D, int HG, int PS, int STAGES, bool F8>
+__global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, HG <= 4 ? 2 : 1)
     decode_u8_heads_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                            const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
                            const DecodeParams p) {
-  using C = U8HeadsCfg<D, HG, PS, STAGES>;
+  using C = U8HeadsCfg<D, HG, PS, STAGES, F8>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -762,8 +807,10 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES>::kThreads, HG <=
         for (int k = 0; k < C::kBoxes; ++k) {
           tma_load_4d(kc + k * HG * C::kRows * D, &tm_kc, 0, 0, jg * HG, pg[k], fb);
           tma_load_4d(vc + k * HG * C::kRows * D, &tm_vc, 0, 0, jg * HG, pg[k], fb);
-          tma_load_3d(ksd + k * HG * C::kRows * 8, &tm_ks, 0, jg * HG, pg[k], fb);
-          tma_load_3d(vsd + k * HG * C::kRows * 8, &tm_vs, 0, jg * HG, pg[k], fb);
+          if constexpr (!F8) {
+            tma_load_3d(ksd + k * HG * C::kRows * 8, &tm_ks, 0, jg * HG, pg[k], fb);
+            tma_load_3d(vsd + k * HG * C::kRows * 8, &tm_vs, 0, jg * HG, pg[k], fb);
+          }
         }
       }
       __syncwarp();
@@ -779,7 +826,7 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES>::kThreads, HG <=
   // -------------------------------------------------------------- consumers
   const int j = jg * HG + warp;  // this warp's kv head
   if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
-  WarpAttnU8<D> wa;
+  WarpAttnU8<D, F8> wa;
   wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G) * D, G, p.scale_log2, lane);
   bool ok = true;
   for (int it = 0; it < n_steps; ++it) {
@@ -803,7 +850,7 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES>::kThreads, HG <=
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }
   wa.finish();
-  if (__any_sync(0xffffffffu, wa.vmax > kMaxVScale) && lane == 0)
+  if (!F8 && __any_sync(0xffffffffu, wa.vmax > kMaxVScale) && lane == 0)
     atomicOr(p.err, static_cast<int>(MQA_DEVERR_U8_SCALE));
   if (!ok) return;
 
@@ -859,11 +906,11 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES>::kThreads, HG <=
   }
 }
 
-template <int D, int HG, int PS>
+template <int D, int HG, int PS, bool F8>
 cudaError_t launch_u8_heads_t(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
   constexpr int ST = 3;
-  using C = U8HeadsCfg<D, HG, PS, ST>;
-  auto kern = decode_u8_heads_kernel<D, HG, PS, ST>;
+  using C = U8HeadsCfg<D, HG, PS, ST, F8>;
+  auto kern = decode_u8_heads_kernel<D, HG, PS, ST, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -883,10 +930,15 @@ int u8_hb(int group) { return group > 16 ? 2 : 1; }
 
 }  // namespace
 
-KernelShape decode_u8_shape(int head_dim, int group) {
+template <bool F8>
+KernelShape u8_shape(int head_dim, int group) {
   const bool two = u8_hb(group) == 2;
-  if (head_dim == 128) return two ? shape_t<128, 2>() : shape_t<128, 1>();
-  return two ? shape_t<64, 2>() : shape_t<64, 1>();
+  if (head_dim == 128) return two ? shape_t<128, 2, F8>() : shape_t<128, 1, F8>();
+  return two ? shape_t<64, 2, F8>() : shape_t<64, 1, F8>();
+}
+
+KernelShape decode_u8_shape(int head_dim, int group, bool f8) {
+  return f8 ? u8_shape<true>(head_dim, group) : u8_shape<false>(head_dim, group);
 }
 
 int decode_u8_heads_group(const DecodeParams& p) {
@@ -896,21 +948,32 @@ int decode_u8_heads_group(const DecodeParams& p) {
   return 0;
 }
 
-cudaError_t launch_decode_u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cudaStream_t stream) {
+template <bool F8>
+cudaError_t u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cudaStream_t stream) {
   if (p.head_dim == 128) {
-    if (p.page_size == 16) return hg == 4 ? launch_u8_heads_t<128, 4, 16>(p, maps, stream)
-                                          : launch_u8_heads_t<128, 2, 16>(p, maps, stream);
-    return hg == 4 ? launch_u8_heads_t<128, 4, 32>(p, maps, stream) : launch_u8_heads_t<128, 2, 32>(p, maps, stream);
+    if (p.page_size == 16) return hg == 4 ? launch_u8_heads_t<128, 4, 16, F8>(p, maps, stream)
+                                          : launch_u8_heads_t<128, 2, 16, F8>(p, maps, stream);
+    return hg == 4 ? launch_u8_heads_t<128, 4, 32, F8>(p, maps, stream)
+                   : launch_u8_heads_t<128, 2, 32, F8>(p, maps, stream);
   }
-  if (p.page_size == 16) return hg == 4 ? launch_u8_heads_t<64, 4, 16>(p, maps, stream)
-                                        : launch_u8_heads_t<64, 2, 16>(p, maps, stream);
-  return hg == 4 ? launch_u8_heads_t<64, 4, 32>(p, maps, stream) : launch_u8_heads_t<64, 2, 32>(p, maps, stream);
+  if (p.page_size == 16) return hg == 4 ? launch_u8_heads_t<64, 4, 16, F8>(p, maps, stream)
+                                        : launch_u8_heads_t<64, 2, 16, F8>(p, maps, stream);
+  return hg == 4 ? launch_u8_heads_t<64, 4, 32, F8>(p, maps, stream) : launch_u8_heads_t<64, 2, 32, F8>(p, maps, stream);
+}
+
+template <bool F8>
+cudaError_t u8_slices(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
+  const bool two = u8_hb(p.group) == 2;
+  if (p.head_dim == 128) return two ? launch_u8_t<128, 2, F8>(p, maps, stream) : launch_u8_t<128, 1, F8>(p, maps, stream);
+  return two ? launch_u8_t<64, 2, F8>(p, maps, stream) : launch_u8_t<64, 1, F8>(p, maps, stream);
+}
+
+cudaError_t launch_decode_u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cudaStream_t stream) {
+  return p.cache_dtype == kDtypeF8 ? u8_heads<true>(p, hg, maps, stream) : u8_heads<false>(p, hg, maps, stream);
 }
 
 cudaError_t launch_decode_u8(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
-  const bool two = u8_hb(p.group) == 2;
-  if (p.head_dim == 128) return two ? launch_u8_t<128, 2>(p, maps, stream) : launch_u8_t<128, 1>(p, maps, stream);
-  return two ? launch_u8_t<64, 2>(p, maps, stream) : launch_u8_t<64, 1>(p, maps, stream);
+  return p.cache_dtype == kDtypeF8 ? u8_slices<true>(p, maps, stream) : u8_slices<false>(p, maps, stream);
 }
 
 }  // namespace mqa

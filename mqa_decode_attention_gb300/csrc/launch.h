@@ -12,6 +12,7 @@ constexpr int kMaxHalfDim = 64;    // RoPE frequencies held in the append kernel
 constexpr int kDtypeBf16 = 0;
 constexpr int kDtypeF32 = 1;
 constexpr int kDtypeU8 = 2;  // cache only: uint8 codes + float2 (scale, zero point) per row
+constexpr int kDtypeF8 = 3;  // cache only: fp8 e5m2 values
 
 struct AppendParams {
   int batch, h_q, h_kv, head_dim, cache_dtype, paged;
@@ -139,8 +140,10 @@ cudaError_t launch_decode_mma_heads(const DecodeParams& p, int heads_per_block, 
                                     const CUtensorMap& tmap_v, cudaStream_t stream);
 
 // uint8 cache (codes + per-row scale and zero point), tensor cores; maps =
-// {K codes, V codes, K (scale, zero), V (scale, zero)}.
-KernelShape decode_u8_shape(int head_dim, int group);
+// {K codes, V codes, K (scale, zero), V (scale, zero)}. The same kernels read
+// an fp8 e5m2 cache (p.cache_dtype == kDtypeF8, f8): codes only, maps[2] and
+// maps[3] unused.
+KernelShape decode_u8_shape(int head_dim, int group, bool f8);
 cudaError_t launch_decode_u8(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream);
 // Paged 16- or 32-token pages, G <= 16: kv heads per block of the head-group
 // uint8 kernel (4 or 2), or 0 when it does not apply. Its maps box `hg` heads.

@@ -13,6 +13,7 @@ from .generate import (
     TinySequence,
     U8Cache,
     make_contiguous_case,
+    make_e5m2_cache,
     make_u8_cache,
     make_paged_case,
     make_tiny_sequence,
@@ -29,6 +30,7 @@ __all__ = [
     "TinySequence",
     "U8Cache",
     "make_contiguous_case",
+    "make_e5m2_cache",
     "make_u8_cache",
     "make_paged_case",
     "make_tiny_sequence",

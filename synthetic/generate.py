@@ -170,3 +170,18 @@ def make_u8_cache(shape_rows, head_dim: int, seed: int, device="cpu") -> U8Cache
         zp = torch.randint(100, 156, tuple(shape_rows), generator=g2, device=device).to(torch.float32)
         out += [codes, torch.stack([scale.to(torch.float32), zp], dim=-1).contiguous()]
     return U8Cache(*out)
+
+
+# fp8 e5m2 caches: streams of their own
+S_K8, S_V8 = 12, 13
+
+
+def make_e5m2_cache(shape_rows, head_dim: int, seed: int, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """K and V caches in torch.float8_e5m2: N(0, 1) values rounded by torch's
+    conversion. shape_rows: [B, H_kv, capacity] or [num_pages, H_kv, page_size]."""
+    out = []
+    for st in (S_K8, S_V8):
+        g = _generator(seed, st, device)
+        x = torch.randn(tuple(shape_rows) + (head_dim,), generator=g, device=device, dtype=torch.float32)
+        out.append(x.to(torch.float8_e5m2))
+    return out[0], out[1]

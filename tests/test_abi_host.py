@@ -106,6 +106,16 @@ def test_u8_layout_checks(lib):
         _abi.MQA_ERR_UNSUPPORTED
 
 
+def test_e5m2_layout_checks(lib):
+    """An fp8 e5m2 cache needs no scale arrays and no capacity rule; it is
+    read on tensor cores only, one new token per sequence."""
+    ok = dict(cache_dtype=_abi.MQA_FP8_E5M2)
+    assert _attn(lib, _layout(**ok), variant=_abi.MQA_VARIANT_CUDA_CORE) == _abi.MQA_ERR_UNSUPPORTED
+    assert _attn(lib, _layout(**dict(ok, capacity=255)), variant=_abi.MQA_VARIANT_CUDA_CORE) == \
+        _abi.MQA_ERR_UNSUPPORTED
+    assert _attn(lib, _layout(cache_dtype=4)) == _abi.MQA_ERR_UNSUPPORTED  # no such dtype
+
+
 def test_combine_rejects_bad_arguments(lib):
     assert lib.splitkv_combine(None, FAKE, 1, 1, 1, 128, FAKE, 0, None, None) == _abi.MQA_ERR_INVALID_ARG
     assert lib.splitkv_combine(FAKE, FAKE, 0, 1, 1, 128, FAKE, 0, None, None) == _abi.MQA_ERR_INVALID_ARG

@@ -1,0 +1,176 @@
+"""GPU parity of the fp8 e5m2 KV cache (MQA_FP8_E5M2) against the fp64 oracle.
+
+The oracle rounds the new token's fp64-rotated key and its bf16 value once to
+e5m2 and attends over the decoded cache in fp64. The append is byte work and
+must match exactly: the appended codes, and nothing else in the caches
+changes. Outputs are bf16, max |err| <= 2e-2 like the bf16 cache path.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, workload
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-2
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def m(built_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mqa_decode_attention_gb300 as mod
+
+    mod.library()
+    return mod
+
+
+def _np(t):
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def _codes(t):
+    return t.detach().cpu().view(torch.uint8).numpy()
+
+
+def run_f8(m, w, case, kc8, vc8, paged, splits=0, window=0, table=None, max_len=None):
+    kc, vc = kc8.to(DEV), vc8.to(DEV)
+    if paged:
+        bt = (case.block_table if table is None else table).to(DEV)
+        lay = m.layout_paged(kc, vc, bt, w.h_q, window=window)
+    else:
+        lay = m.layout_contiguous(kc, vc, w.h_q, window=window)
+    max_len = int(case.seq_lens.max()) if max_len is None else max_len
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=splits, device=DEV)
+    m.decode_step(lay, case.q_new.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV), case.pos.to(DEV),
+                  case.seq_lens.to(DEV), max_len, bufs, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                  num_splits=splits)
+    torch.cuda.synchronize()
+    return dict(out=_np(bufs.out), lse=_np(bufs.lse), q_rot=_np(bufs.q_rot), err=int(bufs.err.item()),
+                k_codes=_codes(kc), v_codes=_codes(vc))
+
+
+def _oracle(w, case, kc8, vc8, paged, window=0):
+    kw = dict(block_table=case.block_table, page_size=case.page_size) if paged else {}
+    return oracle.decode_step_e5m2(_codes(kc8), _codes(vc8), case.q_new, case.k_new, case.v_new, case.seq_lens,
+                                   w.rope_base, 1.0 / math.sqrt(w.head_dim), window=window, **kw)
+
+
+def check(got, ref):
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
+    for key in ("k_codes", "v_codes"):  # the appended rows bit for bit, every other row untouched
+        bad = np.argwhere(got[key] != ref[key])
+        assert bad.size == 0, (key, bad[:5])
+
+
+SHAPES = [
+    # B, h_q, h_kv, d, lens, capacity
+    (2, 32, 8, 128, [1000, 257], 1000),      # G=4, ragged tail
+    (3, 8, 8, 128, [64, 1, 129], 130),       # MHA
+    (1, 16, 1, 128, [777], 778),             # MQA, G=16
+    (2, 64, 2, 128, [300, 45], 300),         # G=32: two head blocks in one CTA
+    (1, 96, 1, 64, [200], 200),              # G=96, d=64
+    (2, 12, 3, 64, [513, 64], 514),          # d=64, G=4
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}d{s[3]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_e5m2_contiguous_matches_oracle(m, shape, splits):
+    B, hq, hkv, d, lens, cap = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, head_dim=d, seed=400 + hq + d)
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=cap)
+    kc8, vc8 = make_e5m2_cache((B, hkv, cap), d, seed=11 + d)
+    check(run_f8(m, w, c, kc8, vc8, paged=False, splits=splits), _oracle(w, c, kc8, vc8, paged=False))
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+@pytest.mark.parametrize("heads", [(16, 2, 128), (32, 8, 128), (12, 3, 128), (64, 2, 128), (16, 4, 64)],
+                         ids=lambda h: f"q{h[0]}kv{h[1]}d{h[2]}")
+def test_e5m2_paged_matches_oracle(m, page_size, heads):
+    """16- and 32-token pages with G <= 16 and an even kv head count take the
+    head-group kernel, the rest the token-slice kernel."""
+    w = workload("paged").with_(batch=5, h_q=heads[0], h_kv=heads[1], head_dim=heads[2], page_size=page_size,
+                                len_lo=1, len_hi=700, seed=29)
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor([1, 16, 17, 700, 333], dtype=torch.int32), spare_pages=2)
+    kc8, vc8 = make_e5m2_cache((pc.num_pages, w.h_kv, pc.page_size), w.head_dim, seed=31)
+    ref = _oracle(w, pc, kc8, vc8, paged=True)
+    for splits in (1, 3, 0):
+        check(run_f8(m, w, pc, kc8, vc8, paged=True, splits=splits), ref)
+
+
+@pytest.mark.parametrize("window", [1, 17, 100, 1000])
+def test_e5m2_sliding_window(m, window):
+    w = workload("gqa4k").with_(batch=3, h_q=16, h_kv=4, seed=81)
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor([700, 65, 3], dtype=torch.int32), capacity=704)
+    kc8, vc8 = make_e5m2_cache((3, 4, 704), 128, seed=12)
+    ref = _oracle(w, c, kc8, vc8, paged=False, window=window)
+    for splits in (1, 0):
+        got = run_f8(m, w, c, kc8, vc8, paged=False, splits=splits, window=window, max_len=700)
+        assert got["err"] == 0
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
+
+
+def test_e5m2_nan_codes_past_the_sequence(m):
+    """Rows at or past L hold NaN / infinity codes: the masked keys and values
+    contribute nothing (their V codes are cleared before the P V product)."""
+    w = workload("gqa4k").with_(batch=3, h_q=32, h_kv=8, seed=82)
+    lens = [100, 37, 64]
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=200)
+    kc8, vc8 = make_e5m2_cache((3, 8, 200), 128, seed=13)
+    for b, L in enumerate(lens):
+        kc8.view(torch.uint8)[b, :, L:] = 0x7F  # NaN
+        vc8.view(torch.uint8)[b, :, L:] = 0xFC  # -inf
+    ref = oracle.decode_step_e5m2(_codes(kc8)[:, :, :100], _codes(vc8)[:, :, :100], c.q_new, c.k_new, c.v_new,
+                                  c.seq_lens, w.rope_base, 1.0 / math.sqrt(128))
+    for splits in (1, 2):
+        got = run_f8(m, w, c, kc8, vc8, paged=False, splits=splits, max_len=100)
+        assert got["err"] == 0
+        assert np.all(np.isfinite(got["out"]))
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
+
+
+def test_e5m2_multi_token_is_refused(m):
+    w = workload("gqa4k").with_(batch=1, h_q=8, h_kv=2)
+    kc8, vc8 = make_e5m2_cache((1, 2, 64), 128, seed=14)
+    lay = m.layout_contiguous(kc8.to(DEV), vc8.to(DEV), 8)
+    q = torch.zeros(1, 2, 8, 128, device=DEV)
+    out = torch.empty(1, 2, 8, 128, dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    with pytest.raises(m.MqaError):
+        m.gqa_decode_attention_multi(lay, 2, q, torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1, 1, out,
+                                     err=err)
+
+
+def test_e5m2_full_size_sampled(m):
+    """The 4096-token GQA workload (batch 32, 32 query / 8 kv heads) over an
+    e5m2 cache: three (sequence, kv head) units against the oracle."""
+    w = workload("gqa4k")
+    L = w.seq_len
+    c = make_contiguous_case(w, DEV)
+    kc8, vc8 = make_e5m2_cache((w.batch, w.h_kv, L), w.head_dim, 15, device=DEV)
+    units = [(0, 0), (w.batch - 1, w.h_kv - 1), (13, 5)]
+    saved = {(b, j): (_codes(kc8[b, j]), _codes(vc8[b, j])) for b, j in units}
+    lay = m.layout_contiguous(kc8, vc8, w.h_q)
+    bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, device=DEV)
+    m.decode_step(lay, c.q_new, c.k_new, c.v_new, c.pos, c.seq_lens, L, bufs, w.rope_base,
+                  1.0 / math.sqrt(w.head_dim), num_splits=0)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    G = w.group
+    for b, j in units:
+        kc, vc = saved[(b, j)]
+        ref = oracle.decode_step_e5m2(kc[None, None], vc[None, None], c.q_new[b:b + 1, j * G:(j + 1) * G].cpu(),
+                                      c.k_new[b:b + 1, j:j + 1].cpu(), c.v_new[b:b + 1, j:j + 1].cpu(), [L],
+                                      w.rope_base, 1.0 / math.sqrt(w.head_dim))
+        assert np.max(np.abs(_np(bufs.out[b, j * G:(j + 1) * G]) - ref["out"][0])) <= BF16_TOL, (b, j)
+        assert np.array_equal(_codes(kc8[b, j, L - 1]), ref["k_codes"][0, 0, L - 1])
