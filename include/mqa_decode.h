@@ -26,6 +26,12 @@
  * Conventions for every call
  *  - All pointers to tensors are DEVICE pointers unless stated otherwise;
  *    the layout struct itself is a HOST pointer, read during the call only.
+ *    The new-token inputs (q_new, k_new, v_new, pos, seq_lens) and the
+ *    output `out` may instead be pinned host memory that the device reaches
+ *    through unified addressing (cudaHostAlloc / pinned tensors): the kernels
+ *    then read and write them across the CPU-GPU link, with no copy launch.
+ *    Caches, block tables, q_rot, workspaces and err_word stay in device
+ *    memory.
  *  - The caller owns every buffer. The library never allocates device memory,
  *    never synchronises, and keeps no pointer after a call returns.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
