@@ -109,8 +109,10 @@ def layout_contiguous(k_cache: torch.Tensor, v_cache: torch.Tensor, h_q: int, wi
     assert k_cache.shape == v_cache.shape and k_cache.dim() == 4
     assert k_cache.is_contiguous() and v_cache.is_contiguous()
     B, h_kv, cap, d = k_cache.shape
-    return KVLayout(_dtype_code(k_cache.dtype), B, h_q, h_kv, d, 0, k_cache.data_ptr(), v_cache.data_ptr(), cap,
-                    0, 0, 0, window, None, _ptr(k_scale_zero), _ptr(v_scale_zero))
+    lay = KVLayout(_dtype_code(k_cache.dtype), B, h_q, h_kv, d, 0, k_cache.data_ptr(), v_cache.data_ptr(), cap,
+                   0, 0, 0, window, None, _ptr(k_scale_zero), _ptr(v_scale_zero))
+    lay._tensors = (k_cache, v_cache, k_scale_zero, v_scale_zero)  # the struct holds raw pointers: keep them alive
+    return lay
 
 
 def layout_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor, h_q: int,
@@ -124,8 +126,10 @@ def layout_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.
     assert block_table.dtype == torch.int32 and block_table.is_contiguous()
     n, h_kv, ps, d = k_pool.shape
     B, mp = block_table.shape
-    return KVLayout(_dtype_code(k_pool.dtype), B, h_q, h_kv, d, 1, k_pool.data_ptr(), v_pool.data_ptr(), 0, ps, n,
-                    mp, window, block_table.data_ptr(), _ptr(k_scale_zero), _ptr(v_scale_zero))
+    lay = KVLayout(_dtype_code(k_pool.dtype), B, h_q, h_kv, d, 1, k_pool.data_ptr(), v_pool.data_ptr(), 0, ps, n,
+                   mp, window, block_table.data_ptr(), _ptr(k_scale_zero), _ptr(v_scale_zero))
+    lay._tensors = (k_pool, v_pool, block_table, k_scale_zero, v_scale_zero)  # keep the pointed-to tensors alive
+    return lay
 
 
 def kv_append_rope(layout: KVLayout, q_new, k_new, v_new, pos, rope_base: float, q_rot, err, stream=None) -> None:
