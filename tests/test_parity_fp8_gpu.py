@@ -174,3 +174,63 @@ def test_e5m2_full_size_sampled(m):
                                       w.rope_base, 1.0 / math.sqrt(w.head_dim))
         assert np.max(np.abs(_np(bufs.out[b, j * G:(j + 1) * G]) - ref["out"][0])) <= BF16_TOL, (b, j)
         assert np.array_equal(_codes(kc8[b, j, L - 1]), ref["k_codes"][0, 0, L - 1])
+
+
+MANY_HEADS = [
+    # B, h_q, h_kv, lens, capacity: 32 or more query heads per kv head (two or more 16-head blocks)
+    (3, 32, 1, [1000, 129, 1], 1000),   # MQA: 32 rows, 4 parts
+    (2, 64, 1, [700, 300], 704),        # 64 rows, 2 parts
+    (1, 128, 1, [300], 300),            # 128 rows, 1 part
+    (2, 64, 2, [513, 64], 514),         # two kv heads
+]
+
+
+@pytest.mark.parametrize("shape", MANY_HEADS, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_e5m2_many_heads_matches_oracle(m, shape, splits):
+    B, hq, hkv, lens, cap = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=420 + hq + hkv)
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=cap)
+    kc8, vc8 = make_e5m2_cache((B, hkv, cap), 128, seed=16 + hq)
+    check(run_f8(m, w, c, kc8, vc8, paged=False, splits=splits), _oracle(w, c, kc8, vc8, paged=False))
+
+
+@pytest.mark.parametrize("window", [1, 100, 1000])
+def test_e5m2_mqa_window_and_nan_tail(m, window):
+    """MQA over e5m2 with a window, and NaN / infinity codes in the rows past
+    each sequence (their codes are cleared before the P V product)."""
+    w = workload("gqa4k").with_(batch=3, h_q=32, h_kv=1, seed=431)
+    lens = [900, 200, 37]
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=1024)
+    kc8, vc8 = make_e5m2_cache((3, 1, 1024), 128, seed=17)
+    for b, L in enumerate(lens):
+        kc8.view(torch.uint8)[b, :, L:] = 0x7F
+        vc8.view(torch.uint8)[b, :, L:] = 0xFC
+    ref = oracle.decode_step_e5m2(_codes(kc8)[:, :, :900], _codes(vc8)[:, :, :900], c.q_new, c.k_new, c.v_new,
+                                  c.seq_lens, w.rope_base, 1.0 / math.sqrt(128), window=window)
+    for splits in (1, 2, 0):
+        got = run_f8(m, w, c, kc8, vc8, paged=False, splits=splits, window=window, max_len=900)
+        assert got["err"] == 0
+        assert np.all(np.isfinite(got["out"]))
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
+
+
+def test_e5m2_mqa_full_size_sampled(m):
+    """The MQA workload (64 sequences of 8192 tokens, 32 query heads on one kv
+    head) over an e5m2 cache: three sequences against the oracle."""
+    w = workload("mqa8k")
+    L = w.seq_len
+    c = make_contiguous_case(w, DEV)
+    kc8, vc8 = make_e5m2_cache((w.batch, 1, L), 128, 18, device=DEV)
+    seqs = [0, 31, 63]
+    saved = {b: (_codes(kc8[b, 0]), _codes(vc8[b, 0])) for b in seqs}
+    lay = m.layout_contiguous(kc8, vc8, w.h_q)
+    bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, device=DEV)
+    m.decode_step(lay, c.q_new, c.k_new, c.v_new, c.pos, c.seq_lens, L, bufs, w.rope_base, 1.0 / math.sqrt(128))
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    for b in seqs:
+        kc, vc = saved[b]
+        ref = oracle.decode_step_e5m2(kc[None, None], vc[None, None], c.q_new[b:b + 1].cpu(), c.k_new[b:b + 1].cpu(),
+                                      c.v_new[b:b + 1].cpu(), [L], w.rope_base, 1.0 / math.sqrt(128))
+        assert np.max(np.abs(_np(bufs.out[b]) - ref["out"][0])) <= BF16_TOL, b
