@@ -48,7 +48,8 @@ METRIC = "decode-attention HBM GB/s (fraction of GB300 peak) and µs/step at 1 G
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "gqa4k"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "attn_tc05.cu", "mma_warp.cuh", "tc05.cuh",
+KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "attn_tc05.cu", "attn_tc05_keys.cu",
+                  "mma_warp.cuh", "tc05.cuh",
                   "rope.cuh", "ptx.cuh", "launch.h"]
 
 
@@ -546,7 +547,10 @@ def bench_ours(args):
     peak, peak_src = measured_peak()
     if byte:
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
-        kernel_name = "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel"
+        # one new token and 32 query heads per kv head: keys on the MMA rows
+        keys_kernel = nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
+        kernel_name = ("attn_tc05_keys_kernel" if keys_kernel else
+                       "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel")
     elif tc05:
         kernel_name = "attn_tc05_kernel"
     elif variant in (0, 2) and w.dtype == "bf16":

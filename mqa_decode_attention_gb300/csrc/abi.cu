@@ -121,7 +121,8 @@ KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
   const int G = L->h_q / L->h_kv;
   if (use_tc05(L, variant, n_new)) return tc05_shape();
   if (variant == MQA_VARIANT_TENSOR_CORE && byte_cache(L->cache_dtype))
-    return decode_u8_shape(L->head_dim, G, L->cache_dtype == MQA_FP8_E5M2);
+    return tc05_keys_applies(G, n_new, L->head_dim, L->paged) ? tc05_keys_shape()
+                                                              : decode_u8_shape(L->head_dim, G, L->cache_dtype == MQA_FP8_E5M2);
   if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G * n_new);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
 }
@@ -558,7 +559,41 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     if (e != cudaSuccess) return fail_cuda(e);
     goto combine;
   }
-  if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype)) {
+  if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype) &&
+      tc05_keys_applies(p.group, n_new, layout->head_dim, layout->paged)) {
+    // one-byte MQA step: the tcgen05 kernel with the keys on the MMA rows
+    CUtensorMap maps[4];
+    if (!make_u8_maps(maps, layout, 128, 1)) {
+      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+      return MQA_ERR_CUDA;
+    }
+    Tc05Params t;
+    std::memset(&t, 0, sizeof(t));
+    t.batch = layout->batch;
+    t.h_q = layout->h_q;
+    t.h_kv = layout->h_kv;
+    t.group = p.group;
+    t.n_new = 1;
+    t.row_blocks = 1;
+    t.num_splits = splits;
+    t.chunk = chunk;
+    t.k_cache = layout->k_cache;
+    t.v_cache = layout->v_cache;
+    t.capacity = layout->capacity;
+    t.max_seq_len = max_seq_len;
+    t.seq_lens = seq_lens;
+    t.q_rot = q_rot;
+    t.scale_log2 = p.scale_log2;
+    t.window = layout->window;
+    t.out = out;
+    t.out_dtype = p.out_dtype;
+    t.lse_out = lse_out;
+    t.o_part = p.o_part;
+    t.lse_part = p.lse_part;
+    t.err = err_word;
+    t.early = early;
+    e = launch_tc05_keys_attention(t, layout->cache_dtype == MQA_U8 ? kDtypeU8 : kDtypeF8, maps, s);
+  } else if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype)) {
     CUtensorMap maps[4];
     // Paged 16- / 32-token pages: blocks over groups of kv heads, one box per
     // page and head group (long contiguous runs of the pool).

@@ -8,10 +8,10 @@
 //   shared memory descriptor (64 bit): start address >> 4 in bits 0-13,
 //   leading-dimension byte offset >> 4 in bits 16-29, stride-dimension byte
 //   offset >> 4 in bits 32-45, the fixed value 0b001 in bits 46-48, base
-//   offset 0 (every swizzle atom starts 1 KB aligned), swizzle mode in bits
-//   61-63 (2 = 128-byte swizzle).
+//   offset 0 (every swizzle atom starts aligned), swizzle mode in bits
+//   61-63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
 //   instruction descriptor for kind::f16 (32 bit): D format in bits 4-5
-//   (1 = f32), A / B format in bits 7-9 / 10-12 (1 = bf16), A / B major in
+//   (1 = f32), A / B format in bits 7-9 / 10-12 (0 = f16, 1 = bf16), A / B major in
 //   bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in
 //   bits 24-28.
 #pragma once
@@ -36,11 +36,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// 64-byte-swizzled operand tile: rows of 32 bf16 (64 B), 8-row atoms of 512 B
+// (16-byte chunk c of row r at c ^ ((r / 2) mod 4)); offsets as above.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // fixed 0b001
+  d |= 4ull << 61;  // 64-byte swizzle
+  return d;
+}
+
 // kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// kind::f16 instruction descriptor: f16 x f16 -> f32, M x N (A / B format 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Tensor-memory allocation: executed by one whole warp; the base address is

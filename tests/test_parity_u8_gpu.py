@@ -216,3 +216,86 @@ def test_u8_full_size_sampled(m):
         got = _np(bufs.out[b, j * G:(j + 1) * G])
         assert np.max(np.abs(got - ref["out"][0])) <= BF16_TOL, (b, j)
         assert np.array_equal(u.k_codes[b, j, L - 1].cpu().numpy(), ref["k_codes"][0, 0, L - 1])
+
+
+# One new token with 32 query heads per kv head (MQA) runs on the tcgen05
+# kernel that puts the keys on the MMA rows: codes widened to exact fp16
+# (c - z), K scale on the scores, V scale folded into P.
+MQA_SHAPES = [
+    # B, h_q, h_kv, lens, capacity
+    (9, 32, 1, [1, 2, 127, 128, 129, 255, 256, 257, 1000], 1000),  # tile edges, a single key
+    (2, 64, 2, [700, 77], 704),                                    # two kv heads
+]
+
+
+@pytest.mark.parametrize("shape", MQA_SHAPES, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}")
+@pytest.mark.parametrize("splits", [1, 2, 5, 0])
+def test_u8_mqa_matches_oracle(m, shape, splits):
+    B, hq, hkv, lens, cap = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=360 + hq)
+    c, u = _contiguous(w, lens, cap, seed=31)
+    ref = _oracle(w, c, u, paged=False)
+    got = run_u8(m, w, c, u, paged=False, splits=splits)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    check_u8_append(got, ref)
+
+
+@pytest.mark.parametrize("window", [1, 63, 64, 100, 1000])
+def test_u8_mqa_window_and_nan_rows_past_the_sequence(m, window):
+    """MQA over uint8 with a window; the rows past each sequence hold NaN
+    scales and zero points (their V rows are zeroed and their P is 0)."""
+    lens = [900, 200, 37]
+    w = workload("gqa4k").with_(batch=3, h_q=32, h_kv=1, seed=362)
+    c, u = _contiguous(w, lens, 1024, seed=32)
+    ref = _oracle(w, c, u, paged=False, window=window)
+    for b, L in enumerate(lens):
+        u.k_sz[b, :, L:] = float("nan")
+        u.v_sz[b, :, L:] = float("nan")
+    for splits in (1, 3, 0):
+        got = run_u8(m, w, c, u, paged=False, splits=splits, window=window, max_len=900)
+        assert got["err"] == 0
+        assert np.all(np.isfinite(got["out"]))
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (window, splits)
+
+
+def test_u8_mqa_large_v_scale_sets_error(m):
+    """MQA: a V scale above 1023 is reported (P' = p s^v / 4 would leave fp16)."""
+    w = workload("gqa4k").with_(batch=1, h_q=32, h_kv=1, seed=363)
+    c, u = _contiguous(w, [300], 300, seed=33)
+    u.v_sz[0, 0, 10, 0] = 2000.0
+    got = run_u8(m, w, c, u, paged=False, splits=1)
+    assert got["err"] & m.MQA_DEVERR_U8_SCALE
+
+
+def test_u8_mqa_full_size_sampled(m):
+    """The MQA workload (64 sequences of 8192 tokens, 32 query heads on one kv
+    head) over a uint8 cache: three sequences against the oracle."""
+    w = workload("mqa8k")
+    L = w.seq_len
+    c = make_contiguous_case(w, DEV)
+    u = make_u8_cache((w.batch, 1, L), w.head_dim, 34, device=DEV)
+    seqs = [0, 31, 63]
+    saved = {b: (u.k_codes[b, 0].cpu(), u.k_sz[b, 0].cpu(), u.v_codes[b, 0].cpu(), u.v_sz[b, 0].cpu()) for b in seqs}
+    lay = m.layout_contiguous(u.k_codes, u.v_codes, w.h_q, k_scale_zero=u.k_sz, v_scale_zero=u.v_sz)
+    bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, device=DEV)
+    m.decode_step(lay, c.q_new, c.k_new, c.v_new, c.pos, c.seq_lens, L, bufs, w.rope_base,
+                  1.0 / math.sqrt(w.head_dim), num_splits=0)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    for b in seqs:
+        kc, ks, vc, vs = saved[b]
+        sub = workload("gqa4k").with_(batch=1, h_q=32, h_kv=1)
+
+        class Case:
+            q_new = c.q_new[b:b + 1].cpu()
+            k_new = c.k_new[b:b + 1].cpu()
+            v_new = c.v_new[b:b + 1].cpu()
+            seq_lens = torch.tensor([L], dtype=torch.int32)
+
+        class Unit:
+            k_codes, k_sz, v_codes, v_sz = kc[None, None], ks[None, None], vc[None, None], vs[None, None]
+
+        ref = _oracle(sub, Case, Unit, paged=False)
+        assert np.max(np.abs(_np(bufs.out[b]) - ref["out"][0])) <= BF16_TOL, b
