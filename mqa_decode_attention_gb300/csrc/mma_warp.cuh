@@ -262,6 +262,18 @@ struct WarpAttn {
   __device__ __forceinline__ void init_rope(const __nv_bfloat16* q, int rows_valid, const float* cs,
                                             float scale_log2, int lane, float* q_rot_out) {
     const int r0 = lane >> 2, c2 = (lane & 3) * 2;
+    // every load first: interleaved with the q_rot stores (which the compiler
+    // must assume may alias q), each load would wait for the previous one
+    uint32_t raw[D / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        const int row = r0 + ((part & 1) ? 8 : 0);
+        const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
+        raw[ks][part] = row < rows_valid ? *reinterpret_cast<const uint32_t*>(q + row * D + col) : 0u;
+      }
+    }
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
@@ -270,8 +282,7 @@ struct WarpAttn {
         const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
         float2 v = make_float2(0.f, 0.f);
         if (row < rows_valid) {
-          const uint32_t raw = *reinterpret_cast<const uint32_t*>(q + row * D + col);
-          const float x = bf16lo_to_f32(raw), y = bf16hi_to_f32(raw);
+          const float x = bf16lo_to_f32(raw[ks][part]), y = bf16hi_to_f32(raw[ks][part]);
           const float c = cs[col >> 1], s = cs[D / 2 + (col >> 1)];
           v = make_float2(x * c - y * s, x * s + y * c);
           if (q_rot_out != nullptr) *reinterpret_cast<float2*>(q_rot_out + row * D + col) = v;
