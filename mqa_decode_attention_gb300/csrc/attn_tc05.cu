@@ -337,21 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_cs[kD / 2 + tid] = sf;
         } else if (writer) {
           // the new token's cache rows exactly as the append kernel writes
-          // them: k pair i turned in fp64 (round-to-nearest products, one
-          // rounding to bf16), v copied; a position outside the cache is
+          // them: k pair i turned and rounded once to bf16 (rope_k_bf16, equal
+          // to the fp64 rotation), v copied; a position outside the cache is
           // reported and nothing is written
           const int i = tid - kD / 2;
           if (apos >= 0 && apos < p.capacity) {
-            double c, sn;
-            sincos(reduce_two_pi(static_cast<double>(apos) * p.theta[i]), &sn, &c);
+            const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[i]);
             const long long row = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD + 2 * i;
             const long long src = (static_cast<long long>(b) * p.h_kv + j) * kD + 2 * i;
             const uint32_t kraw = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
-            const double x = bf16lo_to_f32(kraw), y = bf16hi_to_f32(kraw);
-            __nv_bfloat162 kr;
-            kr.x = __double2bfloat16(__dsub_rn(__dmul_rn(x, c), __dmul_rn(y, sn)));
-            kr.y = __double2bfloat16(__dadd_rn(__dmul_rn(x, sn), __dmul_rn(y, c)));
-            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + row) = kr;
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + row) =
+                rope_k_bf16(bf16lo_to_f32(kraw), bf16hi_to_f32(kraw), ang);
             *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + row) =
                 *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
           } else if (i == 0) {

@@ -10,7 +10,8 @@
 // the group:  S = Q K^T  (m16 x n8 x k16 steps over head_dim), then
 // O += P V with P rounded to bf16 (the fp32 softmax state stays in registers).
 //
-// Block = 4 consumer warps per head block of 16 heads + 1 producer warp. The
+// Block = 4 consumer warps per head block of 16 heads + 1 producer warp + 1
+// warp for the fused append (idle in other launches). The
 // producer streams 64-token K and V tiles with TMA tensor copies
 // (cp.async.bulk.tensor, 128-byte swizzle, one mbarrier pair per stage);
 // a paged cache is gathered page by page through the block table. Consumer
@@ -40,7 +41,11 @@ template <int D, int HB, int STAGES>
 struct MmaCfg {
   static constexpr int kConsumerWarps = 4 * HB;
   static constexpr int kConsumerThreads = 32 * kConsumerWarps;
-  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int kThreads = kConsumerThreads + 64;     // + producer warp + append warp
+  // one head block: as many blocks per SM as their stages fit in shared
+  // memory (two for d = 128, three for d = 64), so their registers must fit
+  // the SM's 64 K as well
+  static constexpr int kMinBlocks = HB == 1 ? (D == 128 ? 2 : 3) : 1;
   static constexpr int kHalfBytes = kTile * 128;             // 64 rows x 64 bf16 (one swizzle span)
   static constexpr int kTileBytes = (D / 64) * kHalfBytes;    // a K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
@@ -55,7 +60,7 @@ struct MmaCfg {
 // speculative decoding): the rows of a kv head are (new token i, query head
 // h) pairs, row = i G + h, and row i sees tokens [.., L - n + i] only.
 template <int D, int HB, int STAGES, bool MULTI>
-__global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
+__global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB, STAGES>::kMinBlocks)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const DecodeParams p) {
   using C = MmaCfg<D, HB, STAGES>;
@@ -119,6 +124,23 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
 
 
+  // the fused append (no append launch precedes this one): one block per
+  // sequence and kv head writes the new token's row
+  const int apos = p.fuse_append ? p.pos[b] : 0;
+  const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos - t_base, p.chunk, S);
+  if (warp == C::kConsumerWarps + 1) {
+    // --------------------------------------------------------- append warp
+    // writes the row, fences it for the async proxy and releases the
+    // producer, which waits (named barrier 3) only before the tile holding it
+    if (awaits) {
+      AppendRows<D, 1> ar;
+      ar.load(p, b, j, apos, lane);
+      ar.write(p, apos, lane);
+      ar.publish();
+      named_bar_arrive(3, 64);
+    }
+    return;
+  }
   if (warp == C::kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const int ps = p.page_size;
@@ -133,8 +155,6 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
     }
     int issued = 0;
     bool waited = !p.early;
-    const int apos = p.fuse_append ? p.pos[b] : 0;
-    const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos - t_base, p.chunk, S);
     bool appended = !awaits;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
@@ -153,8 +173,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
         grid_dependency_wait();
         waited = true;
       }
-      if (!appended && apos < t0 + kTile) {  // this block wrote that row itself: wait for it
-        named_bar_sync(3, D / 2 + 32);
+      if (!appended && apos < t0 + kTile) {  // this tile holds the row the append warp writes
+        named_bar_sync(3, 64);
         appended = true;
       }
       const uint32_t kdst = smem_u32(smem + stage * C::kStageBytes);
@@ -220,7 +240,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
       __syncwarp();
       issued = it + 1;
     }
-    if (!appended) named_bar_sync(3, D / 2 + 32);  // pair the writers' arrival
+    if (!appended) named_bar_sync(3, 64);  // pair the append warp's arrival
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
@@ -238,12 +258,13 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads)
   WarpAttn<D> wa;
   if (p.rope_q) {
     // rotate q_new here: nothing the consumers read comes from the append kernel
+    // (the q loads are issued before the cos / sin table is formed)
     __shared__ float s_cs[D];
-    const int pos = p.pos[b];
-    const bool writer = p.fuse_append && hsb == 0 && split == append_split(pos - t_base, p.chunk, S);
-    rope_table<D>(s_cs, p, b, pos, threadIdx.x, 2, C::kConsumerThreads, j, writer ? 1 : 0, 3);
     const long long qoff = (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
-    wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G - head0, s_cs, p.scale_log2, lane,
+    uint32_t qraw[D / 16][4];
+    WarpAttn<D>::load_q(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G - head0, lane, qraw);
+    rope_table<D>(s_cs, p, p.pos[b], threadIdx.x, 2, C::kConsumerThreads);
+    wa.init_rope(qraw, G - head0, s_cs, p.scale_log2, lane,
                  (p.fuse_append && split == 0 && ws == 0) ? p.q_rot_out + qoff : nullptr);
   } else if (MULTI) {
     if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel

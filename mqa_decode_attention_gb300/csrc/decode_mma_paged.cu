@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
   const int t_end = min(L, t_begin + p.chunk);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kPage - 1) / kPage : 0;
 
+  // the fused append (no append launch precedes this one): one block per
+  // sequence and group of kv heads writes the new token's rows
+  const int apos = p.fuse_append ? p.pos[b] : 0;
+  const bool awaits = p.fuse_append && split == append_split(apos - t_base, p.chunk, S);
   if (warp == C::kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const int32_t* trow = p.block_table + static_cast<long long>(b) * p.max_pages;
@@ -104,10 +108,18 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
     int wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
     int issued = 0;
     bool waited = !p.early;
-    const int apos = p.fuse_append ? p.pos[b] : 0;
-    bool appended = !(p.fuse_append && split == append_split(apos - t_base, p.chunk, S));
+    // the fused append, by this warp (a sixth warp for it measured slower
+    // here): its reads issued now, its rows written once the first pages are
+    // in flight, and fenced just before the page that holds them
+    AppendRows<D, HG> ar;
+    if (awaits) ar.load(p, b, jg * HG, apos, lane);
+    bool written = !awaits, published = !awaits;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
+      if (!written && it == STAGES) {
+        ar.write(p, apos, lane);
+        written = true;
+      }
       if (it >= STAGES) {
         if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
           if (lane == 0) {
@@ -123,9 +135,11 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
         grid_dependency_wait();
         waited = true;
       }
-      if (!appended && apos < t0 + kPage) {  // this block wrote that row itself: wait for it
-        named_bar_sync(3, D / 2 + 32);
-        appended = true;
+      if (!published && apos < t0 + kPage) {  // this page holds the rows this block appends
+        if (!written) ar.write(p, apos, lane);
+        written = true;
+        ar.publish();
+        published = true;
       }
       const int lp = t0 / kPage;  // < n_pages_seq since t0 < t_end <= L
       while (lp >= wbase + 32) {  // warp-uniform window advance
@@ -146,7 +160,7 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
       __syncwarp();
       issued = it + 1;
     }
-    if (!appended) named_bar_sync(3, D / 2 + 32);  // pair the writers' arrival
+    if (!written) ar.write(p, apos, lane);  // rows this block never reads
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
@@ -160,13 +174,13 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
   WarpAttn<D> wa;
   if (p.rope_q) {
     // rotate q_new here: nothing the consumers read comes from the append kernel
+    // (the q loads are issued before the cos / sin table is formed)
     __shared__ float s_cs[D];
-    const int pos = p.pos[b];
-    const bool writer = p.fuse_append && split == append_split(pos - t_base, p.chunk, S);
-    rope_table<D>(s_cs, p, b, pos, threadIdx.x, 2, C::kConsumerWarps * 32, jg * HG, writer ? HG : 0, 3);
     const long long qoff = (static_cast<long long>(b) * p.h_q + j * G) * D;
-    wa.init_rope(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G, s_cs, p.scale_log2, lane,
-                 (p.fuse_append && split == 0) ? p.q_rot_out + qoff : nullptr);
+    uint32_t qraw[D / 16][4];
+    WarpAttn<D>::load_q(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G, lane, qraw);
+    rope_table<D>(s_cs, p, p.pos[b], threadIdx.x, 2, C::kConsumerWarps * 32);
+    wa.init_rope(qraw, G, s_cs, p.scale_log2, lane, (p.fuse_append && split == 0) ? p.q_rot_out + qoff : nullptr);
   } else {
     if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
     wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G) * D, G, p.scale_log2, lane);

@@ -62,50 +62,74 @@ __device__ __forceinline__ int append_split(int pos, int chunk, int splits) {
 
 // Fill cs[0 .. D/2) with cos and cs[D/2 .. D) with sin of pos * theta_i for
 // rotating the query in fp32: the angle is formed and reduced in fp64, then
-// its fp32 sine/cosine taken. Called by all `count` consumer threads; the
-// first D/2 compute. With `append_heads` > 0 those threads also perform the
-// append of the new token for kv heads j0 .. j0 + append_heads - 1 exactly as
-// the append kernel does (fp64 sine/cosine, k rotated in fp64 with
-// round-to-nearest products and one rounding to bf16; v copied), fence the
-// rows for the block's own TMA loads and signal the producer on named barrier
-// `append_bar` (D/2 + 32 threads).
+// its fp32 sine/cosine taken. Called by all `count` consumer threads (named
+// barrier `bar`); the first D/2 compute.
 template <int D>
-__device__ __forceinline__ void rope_table(float* cs, const DecodeParams& p, int b, int pos, int tid, int bar,
-                                           int count, int j0, int append_heads, int append_bar) {
+__device__ __forceinline__ void rope_table(float* cs, const DecodeParams& p, int pos, int tid, int bar, int count) {
   if (tid < D / 2) {
     const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[tid]);
     float sf, cf;
     sincosf(static_cast<float>(ang), &sf, &cf);
     cs[tid] = cf;
     cs[D / 2 + tid] = sf;
-    if (append_heads > 0) {
-      double c, s;
-      sincos(ang, &s, &c);
-      for (int h = 0; h < append_heads; ++h) {
-        const int j = j0 + h;
-        const long long row = cache_row(p, b, j, pos, tid == 0 && h == 0);
-        if (row < 0) continue;
-        const long long src = (static_cast<long long>(b) * p.h_kv + j) * D + 2 * tid;
-        const uint32_t kraw = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
-        const double x = bf16lo_to_f32(kraw), y = bf16hi_to_f32(kraw);
-        const double xr = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
-        const double yr = __dadd_rn(__dmul_rn(x, s), __dmul_rn(y, c));
-        __nv_bfloat162 kv;
-        kv.x = __double2bfloat16(xr);
-        kv.y = __double2bfloat16(yr);
-        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + row + 2 * tid;
-        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + row + 2 * tid;
-        *reinterpret_cast<__nv_bfloat162*>(kc) = kv;
-        *reinterpret_cast<uint32_t*>(vc) =
-            *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
-      }
-      // the rows are read back by this block's TMA (async proxy)
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      asm volatile("bar.arrive %0, %1;" ::"r"(append_bar), "r"(D / 2 + 32) : "memory");
-    }
   }
   named_bar_sync(bar, count);
 }
+
+// The fused append of sequence b's new token for kv heads j0 .. j0 + H - 1,
+// by one whole warp (lane i owns rotation pairs i, i + 32, ...), with the
+// append kernel's result: k turned by the angle formed and reduced in fp64
+// and rounded once to bf16 (rope_k_bf16, equal to the fp64 rotation), v
+// copied. It comes in three parts so that its memory latencies overlap the
+// producer's other work: load() issues every global read, write() turns k and
+// stores both rows, publish() fences them for TMA loads (async proxy) that
+// this warp issues afterwards.
+template <int D, int H>
+struct AppendRows {
+  static constexpr int kPer = D / 64;  // rotation pairs per lane
+  uint32_t k[H][kPer], v[H][kPer];
+  double theta[kPer];
+  long long row[H];
+
+  __device__ __forceinline__ void load(const DecodeParams& p, int b, int j0, int pos, int lane) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) theta[i] = p.theta[lane + 32 * i];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const long long src = (static_cast<long long>(b) * p.h_kv + j0 + h) * D + 2 * (lane + 32 * i);
+        k[h][i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
+        v[h][i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < H; ++h) row[h] = cache_row(p, b, j0 + h, pos, lane == 0 && h == 0);
+  }
+
+  __device__ __forceinline__ void write(const DecodeParams& p, int pos, int lane) const {
+    double ang[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) ang[i] = reduce_two_pi(static_cast<double>(pos) * theta[i]);
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      if (row[h] < 0) continue;  // the same for every lane
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const long long e = row[h] + 2 * (lane + 32 * i);
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + e;
+        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + e;
+        *reinterpret_cast<__nv_bfloat162*>(kc) = rope_k_bf16(bf16lo_to_f32(k[h][i]), bf16hi_to_f32(k[h][i]), ang[i]);
+        *reinterpret_cast<uint32_t*>(vc) = v[h][i];
+      }
+    }
+  }
+
+  __device__ __forceinline__ static void publish() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+  }
+};
 
 template <int D>
 struct WarpAttn {
@@ -256,15 +280,13 @@ struct WarpAttn {
     }
   }
 
-  // Same as init, but rotates the raw bf16 query q_new first: pair i of a row
-  // turns by the angle whose fp32 cosine / sine are cs[i] / cs[D/2 + i], as the
-  // append kernel does for q_rot.
-  __device__ __forceinline__ void init_rope(const __nv_bfloat16* q, int rows_valid, const float* cs,
-                                            float scale_log2, int lane, float* q_rot_out) {
+  // Load this lane's fragment of the raw bf16 query q_new (q points at row 0
+  // of the warp's 16 query heads, [16][D], rows >= rows_valid read as zero).
+  // Kept apart from init_rope so the loads are in flight while the cos / sin
+  // table is formed.
+  __device__ __forceinline__ static void load_q(const __nv_bfloat16* q, int rows_valid, int lane,
+                                                uint32_t (&raw)[D / 16][4]) {
     const int r0 = lane >> 2, c2 = (lane & 3) * 2;
-    // every load first: interleaved with the q_rot stores (which the compiler
-    // must assume may alias q), each load would wait for the previous one
-    uint32_t raw[D / 16][4];
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
@@ -274,6 +296,15 @@ struct WarpAttn {
         raw[ks][part] = row < rows_valid ? *reinterpret_cast<const uint32_t*>(q + row * D + col) : 0u;
       }
     }
+  }
+
+  // Same as init, but from the raw bf16 query loaded by load_q, rotated first:
+  // pair i of a row turns by the angle whose fp32 cosine / sine are cs[i] /
+  // cs[D/2 + i], as the append kernel does for q_rot (written to q_rot_out, a
+  // [16][D] fp32 block like q, unless null).
+  __device__ __forceinline__ void init_rope(const uint32_t (&raw)[D / 16][4], int rows_valid, const float* cs,
+                                            float scale_log2, int lane, float* q_rot_out) {
+    const int r0 = lane >> 2, c2 = (lane & 3) * 2;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll

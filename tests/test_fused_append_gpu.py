@@ -1,0 +1,148 @@
+"""GPU: the new token's key row written by the fused decode step is bit for bit
+the row the standalone append kernel writes.
+
+The fused kernels turn each key pair in fp32 and redo it in fp64 only when the
+fp32 result could round to another bf16 than the fp64 rotation
+(rope_k_bf16). These tests feed them many rows whose values cover the cases
+that decide between the two: ordinary N(0,1) values, values scaled over most
+of the bf16 exponent range, zeros of both signs, bf16 subnormals, pairs with
+y = +-x or y = 0, infinities and NaN. Each comparison is against
+kv_append_rope, which rotates in fp64 throughout; both must also stay within
+one bf16 ulp of the oracle's rounding wherever the oracle's value is finite.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import make_contiguous_case, make_paged_case, workload
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def m(built_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mqa_decode_attention_gb300 as mod
+
+    mod.library()
+    return mod
+
+
+def hard_keys(shape, seed):
+    """bf16 key values mixing ordinary, scaled, zero, subnormal and special cases."""
+    gen = torch.Generator().manual_seed(seed)
+    k = torch.randn(shape, generator=gen, dtype=torch.float64)
+    flat = k.view(-1)
+    n = flat.numel()
+    kind = torch.randint(0, 100, (n,), generator=gen)
+    expo = torch.randint(-120, 121, (n,), generator=gen).to(torch.float64)
+    flat[:] = torch.where((kind >= 60) & (kind < 72), flat * torch.pow(2.0, expo), flat)
+    sub = torch.randint(-127, 128, (n,), generator=gen).to(torch.float64) * 2.0 ** -133  # bf16 subnormals
+    flat[:] = torch.where((kind >= 72) & (kind < 77), sub, flat)
+    flat[:] = torch.where(kind == 77, torch.zeros_like(flat), flat)
+    flat[:] = torch.where(kind == 78, -torch.zeros_like(flat), flat)
+    flat[:] = torch.where(kind == 79, torch.full_like(flat, math.inf), flat)
+    flat[:] = torch.where(kind == 80, torch.full_like(flat, -math.inf), flat)
+    flat[:] = torch.where(kind == 81, torch.full_like(flat, math.nan), flat)
+    kb = k.to(torch.bfloat16)
+    # pairs (x, y) = (x, +-x) and (x, 0) for some rotation pairs
+    pairs = kb.view(-1, 2)
+    pk = torch.randint(0, 10, (pairs.shape[0],), generator=gen)
+    pairs[pk == 0, 1] = pairs[pk == 0, 0]
+    pairs[pk == 1, 1] = -pairs[pk == 1, 0]
+    pairs[pk == 2, 1] = 0
+    return kb
+
+
+def bits(t):
+    return t.contiguous().view(torch.int16)
+
+
+def check_against_oracle(k_new, got_rows, pos, base):
+    """Each appended element whose oracle value is finite lies within one bf16
+    ulp of it (k_new, got_rows: [B, H_kv, d]; pos: [B])."""
+    for b in range(k_new.shape[0]):
+        with np.errstate(invalid="ignore", over="ignore"):
+            want = oracle.rope_rotate(k_new[b].to(torch.float64).numpy(), int(pos[b]), base)
+        got = got_rows[b].to(torch.float64).numpy()
+        fin = np.isfinite(want) & (np.abs(want) < 3.0e38)
+        e = np.floor(np.log2(np.maximum(np.abs(want[fin]), 2.0 ** -126)))
+        assert np.all(np.abs(got[fin] - want[fin]) <= 2.0 ** (e - 7)), b
+
+
+@pytest.mark.parametrize("base", [10000.0, 500000.0])
+def test_fused_append_warp_mma_contiguous(m, base):
+    w = workload("gqa4k").with_(batch=64, h_q=32, h_kv=8, seed=91)
+    lens = torch.randint(1, 2049, (w.batch,), generator=torch.Generator().manual_seed(92), dtype=torch.int32)
+    c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=2048)
+    k_new = hard_keys(c.k_new.shape, 93)
+    caches = []
+    for fused in (True, False):
+        kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+        lay = m.layout_contiguous(kc, vc, w.h_q)
+        bufs = m.DecodeBuffers.allocate(lay, 2048, num_splits=1, variant=2, device=DEV)
+        args = (c.q_new.to(DEV), k_new.to(DEV), c.v_new.to(DEV), c.pos.to(DEV), c.seq_lens.to(DEV))
+        if fused:
+            m.decode_step(lay, *args, 2048, bufs, base, 0.1, num_splits=1, variant=2)
+        else:
+            m.kv_append_rope(lay, args[0], args[1], args[2], args[3], base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        caches.append((kc.cpu(), vc.cpu()))
+    assert torch.equal(bits(caches[0][0]), bits(caches[1][0]))
+    assert torch.equal(bits(caches[0][1]), bits(caches[1][1]))
+    b_idx = torch.arange(w.batch)
+    rows = caches[0][0][b_idx, :, c.pos.long()]  # [B, H_kv, d]
+    check_against_oracle(k_new, rows, c.pos, base)
+
+
+def test_fused_append_paged_head_group(m):
+    w = workload("paged").with_(batch=48, seed=94)
+    lens = torch.randint(1, 1500, (w.batch,), generator=torch.Generator().manual_seed(95), dtype=torch.int32)
+    pc = make_paged_case(w, "cpu", seq_lens=lens)
+    k_new = hard_keys(pc.k_new.shape, 96)
+    pools = []
+    for fused in (True, False):
+        kp, vp, bt = pc.k_pool.to(DEV), pc.v_pool.to(DEV), pc.block_table.to(DEV)
+        lay = m.layout_paged(kp, vp, bt, w.h_q)
+        L = int(lens.max())
+        bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, variant=2, device=DEV)
+        args = (pc.q_new.to(DEV), k_new.to(DEV), pc.v_new.to(DEV), pc.pos.to(DEV), pc.seq_lens.to(DEV))
+        if fused:
+            m.decode_step(lay, *args, L, bufs, w.rope_base, 0.1, num_splits=0, variant=2)
+        else:
+            m.kv_append_rope(lay, args[0], args[1], args[2], args[3], w.rope_base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        pools.append((kp.cpu(), vp.cpu()))
+    assert torch.equal(bits(pools[0][0]), bits(pools[1][0]))
+    assert torch.equal(bits(pools[0][1]), bits(pools[1][1]))
+
+
+def test_fused_append_tc05_mqa(m):
+    w = workload("mqa8k").with_(batch=256, seed=97)
+    lens = torch.randint(1, 1025, (w.batch,), generator=torch.Generator().manual_seed(98), dtype=torch.int32)
+    c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=1024)
+    k_new = hard_keys(c.k_new.shape, 99)
+    caches = []
+    for fused in (True, False):
+        kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+        lay = m.layout_contiguous(kc, vc, w.h_q)
+        bufs = m.DecodeBuffers.allocate(lay, 1024, num_splits=0, variant=2, device=DEV)
+        args = (c.q_new.to(DEV), k_new.to(DEV), c.v_new.to(DEV), c.pos.to(DEV), c.seq_lens.to(DEV))
+        if fused:
+            m.decode_step(lay, *args, 1024, bufs, w.rope_base, 0.1, num_splits=0, variant=2)
+        else:
+            m.kv_append_rope(lay, args[0], args[1], args[2], args[3], w.rope_base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        caches.append((kc.cpu(), vc.cpu()))
+    assert torch.equal(bits(caches[0][0]), bits(caches[1][0]))
+    assert torch.equal(bits(caches[0][1]), bits(caches[1][1]))
