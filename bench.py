@@ -419,7 +419,10 @@ def bench_ours(args):
             and w.group * nn >= 32)
     fused = (not byte and nn == 1 and variant in (0, 2) and w.dtype == "bf16"
              and (w.group <= 128 if tc05 else w.group <= 32))
-    launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 else 0)
+    # two splits of at most 64 rows per kv head on the tcgen05 kernel: the two
+    # blocks of a kv head form a cluster and merge in shared memory (no combine)
+    merged = tc05 and splits_used == 2 and w.group * nn <= 64
+    launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 and not merged else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
     sampler = ClockSampler(gpu_index_for(local))
@@ -559,11 +562,11 @@ def bench_ours(args):
         kernel_name = "decode_mma_heads_kernel" if heads_kernel else "decode_mma_kernel"
     else:
         kernel_name = "decode_fma_kernel"
-    if fused and splits_used == 1:
+    if fused and (splits_used == 1 or merged):
         # the step is this one launch: its average duration over the timed
         # region is the step time, and it moves the whole step's bytes
         roof_bytes, roof_ms = sbytes, ms_per_step
-        roof_kernel = kernel_name + " (append fused)"
+        roof_kernel = kernel_name + " (append fused" + (", two-block clusters merging the splits)" if merged else ")")
         roof_time = "timed region: K back-to-back launches of this kernel, CUDA events at both ends"
     elif fused:
         roof_bytes, roof_ms = sbytes, step_call_ms
@@ -571,7 +574,7 @@ def bench_ours(args):
         roof_time = "events around each step call (decode + combine launches)"
     else:
         roof_bytes, roof_ms = abytes, attn_ms
-        roof_kernel = kernel_name + (" + combine_kernel" if splits_used > 1 else "")
+        roof_kernel = kernel_name + (" + combine_kernel" if splits_used > 1 and not merged else "")
         roof_time = "events around each standalone gqa_decode_attention call"
     achieved = roof_bytes / (roof_ms * 1e-3) / 1e9
     traffic = (ncu_traffic(args.workload + ("_" + args.cache if byte else "")) if kernel_name.startswith(("decode_mma", "decode_u8", "attn_tc05"))

@@ -460,6 +460,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   }
 
   const KernelShape ks = decode_shape(layout, v, n_new);
+  bool merged = false;  // the attention launch merged its splits itself: no combine
   DecodeParams p;
   std::memset(&p, 0, sizeof(p));
   p.n_new = n_new;
@@ -557,6 +558,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     }
     e = launch_tc05_attention(t, tk, tv, s);
     if (e != cudaSuccess) return fail_cuda(e);
+    merged = tc05_merges_splits(t);
     goto combine;
   }
   if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype) &&
@@ -630,7 +632,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   }
   if (e != cudaSuccess) return fail_cuda(e);
 combine:
-  if (splits > 1) {
+  if (splits > 1 && !merged) {
     CombineParams c;
     c.o_part = p.o_part;
     c.lse_part = p.lse_part;

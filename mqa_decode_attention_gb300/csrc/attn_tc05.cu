@@ -60,6 +60,11 @@ constexpr uint32_t kTmemCols = 512;                      // S0 .. S{kSBuf-1}, O
 constexpr uint32_t kColS = 0, kColO = kSBuf * 128;
 static_assert(kColO + kD <= kTmemCols, "S buffers and O exceed tensor memory");
 constexpr float kRescaleLog2 = 8.0f;
+// two-split cluster (CL): each block's normalised output rows (fp32) and their
+// lse, left in its V stages once its last PV is done
+constexpr int kXRows = 64;
+constexpr int kXOff = kVOff;
+static_assert((kXRows * (kD + 3)) * 4 <= kStages * kTileBytes, "cluster exchange area");
 
 // mbarriers (8 bytes each) at kBarOff
 constexpr int kQReady = 0;
@@ -84,10 +89,14 @@ __device__ __forceinline__ bool aborted(const Tc05Params& p) {
   return (*reinterpret_cast<volatile int32_t*>(p.err) & static_cast<int>(MQA_DEVERR_TIMEOUT)) != 0;
 }
 
-template <int PARTS, bool FUSE>
+// CL: the two splits of a (sequence, kv head) are one cluster of two blocks
+// that merge their partial results through distributed shared memory; block
+// 0 writes the output (no combine launch, no partials in global memory).
+template <int PARTS, bool FUSE, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const Tc05Params p) {
+  static_assert(!CL || PARTS > 1, "the cluster merge takes replicated rows (R <= 64)");
   constexpr int kRPad = kBM / PARTS;  // rows per part
   constexpr int kKW = kBN / PARTS;    // keys of a tile per thread
   extern __shared__ unsigned char smem_raw[];
@@ -102,14 +111,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group, n = p.n_new, R = G * n, S = p.num_splits;
   // block order: sequence fastest, then kv head, split, row block (row blocks
-  // with the longest key ranges -- the last tokens -- first)
+  // with the longest key ranges -- the last tokens -- first); CL: the split
+  // (the block's rank in its cluster) fastest
   int cta = blockIdx.x;
+  int cl_rank = 0;
+  if constexpr (CL) {
+    cl_rank = cta & 1;
+    cta >>= 1;
+  }
   const int b = cta % p.batch;
   cta /= p.batch;
   const int j = cta % p.h_kv;
   cta /= p.h_kv;
-  const int split = cta % S;
-  const int rb = p.row_blocks - 1 - cta / S;
+  const int split = CL ? cl_rank : cta % S;
+  const int rb = CL ? 0 : p.row_blocks - 1 - cta / S;
   const int g0 = rb * kBM;
   const int rows = min(kBM, R - g0);
 
@@ -122,9 +137,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && split == 0 && rb == 0 && j == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
     L = L < n ? n : static_cast<int>(limit);
   }
+  // CL: the exchange between the two blocks of the cluster. Every thread of
+  // both blocks runs it exactly once, on every path through the kernel (the
+  // cluster barriers have no timeout). Block 1 leaves (xo, xl) of its split
+  // in its shared memory; block 0 reads them, merges them with its own by
+  // their lse (as the combine does) and writes out and lse_out.
+  float* xo = reinterpret_cast<float*>(smem + kXOff);  // [kXRows][kD]
+  float* xl = xo + kXRows * kD;                         // [kXRows]
+  float* xw = xl + kXRows;                              // [2][kXRows] (block 0)
+  auto out_row = [&](int r) {
+    const int i = (g0 + r) / G;
+    return (static_cast<long long>(b) * n + i) * p.h_q + j * G + (g0 + r - i * G);
+  };
+  auto cl_exchange = [&]() {
+    grid_dependency_wait();  // out may still be read by the preceding launch
+    cluster_sync_all();
+    if (cl_rank == 0) {
+      const uint32_t peer = dsmem_map(smem_u32(xo), 1);
+      if (tid < rows) {
+        const float l0 = xl[tid], l1 = dsmem_ld_f32(peer + (kXRows * kD + tid) * 4);
+        const float m = fmaxf(l0, l1);
+        float w0 = 0.f, w1 = 0.f, lse = -INFINITY;
+        if (m != -INFINITY) {
+          w0 = expf(l0 - m);  // exp(-inf) = 0 for an empty split
+          w1 = expf(l1 - m);
+          lse = m + logf(w0 + w1);
+          const float inv = 1.f / (w0 + w1);
+          w0 *= inv;
+          w1 *= inv;
+        }
+        xw[tid] = w0;
+        xw[kXRows + tid] = w1;
+        if (p.lse_out != nullptr) p.lse_out[out_row(tid)] = lse;
+      }
+      __syncthreads();
+      // four elements per item; the peer's loads of a batch in flight together
+      constexpr int kBatch = 4;
+      const int items = rows * (kD / 4);
+      for (int i0 = tid; i0 < items; i0 += kBatch * kThreads) {
+        float4 pv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int it = i0 + u * kThreads;
+          pv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (it < items) pv[u] = dsmem_ld_f32x4(peer + it * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int it = i0 + u * kThreads;
+          if (it >= items) break;
+          const int r = it / (kD / 4), d = (it % (kD / 4)) * 4;
+          const float wa = xw[r], wb = xw[kXRows + r];
+          const float4 a = *reinterpret_cast<const float4*>(xo + r * kD + d);
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
+          if (wa > 0.f) {  // an empty or skipped split's rows are never read
+            v[0] = wa * a.x, v[1] = wa * a.y, v[2] = wa * a.z, v[3] = wa * a.w;
+          }
+          if (wb > 0.f) {
+            v[0] = fmaf(wb, pv[u].x, v[0]), v[1] = fmaf(wb, pv[u].y, v[1]);
+            v[2] = fmaf(wb, pv[u].z, v[2]), v[3] = fmaf(wb, pv[u].w, v[3]);
+          }
+          const long long o = out_row(r) * kD + d;
+          if (p.out_dtype == kDtypeBf16) {
+            uint2 w;
+            w.x = pack_bf16x2(v[0], v[1]);
+            w.y = pack_bf16x2(v[2], v[3]);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o) = w;
+          } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+        }
+      }
+    }
+    cluster_sync_all();  // block 1's shared memory is kept until block 0 has read it
+  };
+  auto cl_empty = [&]() {  // a split with no result: weight 0 in the merge
+    for (int r = tid; r < rows; r += kThreads) xl[r] = -INFINITY;
+  };
+
   if (tid == 0) s_skip = aborted(p) ? 1 : 0;  // an earlier block timed out: the result is invalid already
   __syncthreads();
-  if (s_skip) return;
+  if (s_skip) {
+    if constexpr (CL) {
+      cl_empty();
+      cl_exchange();
+    }
+    return;
+  }
   const int Lp = L - n;  // new token i sits at position Lp + i
   const int pos_first = Lp + g0 / G, pos_last = Lp + (g0 + rows - 1) / G;
   const int ka_first = p.window > 0 ? max(0, pos_first + 1 - p.window) : 0;
@@ -135,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kstart = max(t_begin, (ka_first / 64) * 64);
   const int kend = min(t_end, pos_last + 1);
   const int T = kend > kstart ? (kend - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
-  const bool split_out = S > 1;
+  const bool split_out = S > 1 && !CL;
   // fused step: the split whose token range holds the new token's position
   // (else split 0) appends its k / v row
   const int tbase = (t_lo / 64) * 64;
@@ -143,6 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (T == 0) {
     // no key of this split reaches these rows: an empty partial (weight 0 in the combine)
     grid_dependency_wait();
+    if constexpr (CL) {
+      cl_empty();
+      cl_exchange();
+      return;
+    }
     if (split_out) {
       for (int idx = tid; idx < rows * kD; idx += kThreads) {
         const int g = g0 + idx / kD, i = g / G;
@@ -622,7 +726,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const long long orow = (static_cast<long long>(b) * n + ti) * p.h_q + j * G + (g0 + r - ti * G);
           mrow[r] = orow;
           const float lse = den > 0.f ? (mx + log2f(den)) * 0.69314718055994530942f : -INFINITY;
-          if (split_out)
+          if constexpr (CL)
+            xl[r] = lse;
+          else if (split_out)
             p.lse_part[orow * S + split] = lse;
           else if (p.lse_out != nullptr)
             p.lse_out[orow] = lse;
@@ -638,7 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < PARTS; ++q)
               ov = fmaf(mw[q * kRPad + row], mo[(q * kRPad + row) * kStride + d], ov);
             const long long orow = mrow[row];
-            if (split_out) {
+            if constexpr (CL) {
+              xo[row * kD + d] = ov;
+            } else if (split_out) {
               p.o_part[(orow * S + split) * kD + d] = ov;
             } else if (p.out_dtype == kDtypeBf16) {
               static_cast<__nv_bfloat16*>(p.out)[orow * kD + d] = __float2bfloat16_rn(ov);
@@ -667,15 +775,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc05::fence_after_sync();
     tc05::tmem_dealloc(tmem, kTmemCols);
   }
+  if constexpr (CL) cl_exchange();
 }
 
 }  // namespace
 
 KernelShape tc05_shape() { return {kThreads, kSmemBytes, kBM, 1}; }
 
-template <int PARTS, bool FUSE>
+template <int PARTS, bool FUSE, bool CL>
 cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  auto kern = attn_tc05_kernel<PARTS, FUSE>;
+  auto kern = attn_tc05_kernel<PARTS, FUSE, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -683,24 +792,41 @@ cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUten
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (CL) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+template <int PARTS>
+cudaError_t launch_fuse(const Tc05Params& p, bool cl, const CUtensorMap& tk, const CUtensorMap& tv,
+                        cudaStream_t stream) {
+  if (cl) return p.fuse ? launch_parts<PARTS, true, true>(p, tk, tv, stream) : launch_parts<PARTS, false, true>(p, tk, tv, stream);
+  return p.fuse ? launch_parts<PARTS, true, false>(p, tk, tv, stream) : launch_parts<PARTS, false, false>(p, tk, tv, stream);
+}
+
+bool tc05_merges_splits(const Tc05Params& p) {
+  return p.num_splits == 2 && p.row_blocks == 1 && static_cast<long long>(p.group) * p.n_new <= 64;
 }
 
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
   // replicate few rows over the 128 MMA rows so that all four softmax warps work
   const long long rows = static_cast<long long>(p.group) * p.n_new;
+  const bool cl = tc05_merges_splits(p);
   // (a fused step has one row block: p.fuse implies row_blocks == 1)
-  if (p.row_blocks == 1 && rows <= 32)
-    return p.fuse ? launch_parts<4, true>(p, tk, tv, stream) : launch_parts<4, false>(p, tk, tv, stream);
-  if (p.row_blocks == 1 && rows <= 64)
-    return p.fuse ? launch_parts<2, true>(p, tk, tv, stream) : launch_parts<2, false>(p, tk, tv, stream);
-  return p.fuse ? launch_parts<1, true>(p, tk, tv, stream) : launch_parts<1, false>(p, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4>(p, cl, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2>(p, cl, tk, tv, stream);
+  return p.fuse ? launch_parts<1, true, false>(p, tk, tv, stream) : launch_parts<1, false, false>(p, tk, tv, stream);
 }
 
 }  // namespace mqa

@@ -164,5 +164,10 @@ cudaError_t launch_tc05_keys_attention(const Tc05Params& p, int cache_dtype, con
                                        cudaStream_t stream);
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                   cudaStream_t stream);
+// true when launch_tc05_attention merges the splits itself (two splits, R <=
+// 64 rows in one row block: each pair of split blocks is a two-block cluster
+// that writes out and lse_out directly): no combine follows, and o_part /
+// lse_part are not written
+bool tc05_merges_splits(const Tc05Params& p);
 
 }  // namespace mqa

@@ -86,7 +86,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}q{c[1]}kv{c[2]}n{c[3]}")
-@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("splits", [1, 2, 3, 0])
 def test_tc05_decode_matches_oracle(m, case, splits):
     B, hq, hkv, n, lens, cap = case
     w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=700 + hq + n)
@@ -160,6 +160,39 @@ def test_tc05_splits_with_garbage_workspace(m, standalone):
         got = _np(bufs.out).reshape(3, n, 32, -1)
         assert np.max(np.abs(got - ref["out"])) <= TOL
         assert np.max(np.abs(_np(bufs.lse).reshape(3, n, 32) - ref["lse"])) <= TOL
+
+
+@pytest.mark.parametrize("n, hq", [(1, 32), (1, 64), (2, 32)])
+def test_tc05_two_split_cluster_merge(m, n, hq):
+    """Two splits with at most 64 rows per kv head: the two blocks of a
+    (sequence, kv head) are one cluster and merge their results in shared
+    memory (no combine). Split 1 is empty for the short sequences (only split
+    0 holds keys), the fused step and the standalone call agree with the
+    oracle, in bf16 and fp32 output, on three calls in a row."""
+    w = workload("gqa4k").with_(batch=4, h_q=hq, h_kv=1, seed=760 + hq + n)
+    lens = [1000, 513, 512, max(n, 1)]
+    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=1000)
+    q, k, v = new_tokens(w, n)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, scale, "bf16")
+    check_step(run(m, w, n, c, q, k, v, lens, 2), ref)
+    # standalone attention over the appended cache, fp32 output
+    kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+    lay = m.layout_contiguous(kc, vc, w.h_q)
+    lens_d = torch.as_tensor(lens, dtype=torch.int32).to(DEV)
+    bufs = m.DecodeBuffers.allocate(lay, 1000, num_splits=2, device=DEV, n_new=n, out_dtype=torch.float32)
+    bufs.workspace.fill_(0x7F)
+    m.kv_append_rope_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, w.rope_base, bufs.q_rot, bufs.err)
+    for _ in range(3):
+        bufs.out.fill_(float("nan"))
+        m.gqa_decode_attention_multi(lay, n, bufs.q_rot, lens_d, 1000, scale, 2, bufs.out, bufs.lse,
+                                     bufs.workspace, err=bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        got = _np(bufs.out).reshape(4, n, hq, -1)
+        # (fp32 output of a tensor-core path: Q and P are bf16 MMA operands)
+        assert np.max(np.abs(got - ref["out"])) <= TOL
+        assert np.max(np.abs(_np(bufs.lse).reshape(4, n, hq) - ref["lse"])) <= TOL
 
 
 def test_tc05_many_short_splits(m):
