@@ -49,6 +49,7 @@ UNIT = "GB/s"
 DEFAULT_WORKLOAD = "gqa4k"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "attn_tc05.cu", "attn_tc05_keys.cu",
+                  "attn_tc05_widen.cu",
                   "mma_warp.cuh", "tc05.cuh",
                   "rope.cuh", "ptx.cuh", "launch.h"]
 
@@ -421,7 +422,10 @@ def bench_ours(args):
              and (w.group <= 128 if tc05 else w.group <= 32))
     # two splits of at most 64 rows per kv head on the tcgen05 kernel: the two
     # blocks of a kv head form a cluster and merge in shared memory (no combine)
-    merged = tc05 and splits_used == 2 and w.group * nn <= 64
+    # (likewise the e5m2 one-token MQA kernel with two splits)
+    widen = (byte and args.cache == "fp8" and nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
+             and variant in (0, 2))
+    merged = (tc05 and splits_used == 2 and w.group * nn <= 64) or (widen and splits_used == 2)
     launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 and not merged else 0)
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
@@ -550,9 +554,11 @@ def bench_ours(args):
     peak, peak_src = measured_peak()
     if byte:
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
-        # one new token and 32 query heads per kv head: keys on the MMA rows
+        # one new token and 32 query heads per kv head on tcgen05: uint8 with
+        # the keys on the MMA rows, e5m2 with the heads on the rows and the
+        # codes widened by converter warps
         keys_kernel = nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
-        kernel_name = ("attn_tc05_keys_kernel" if keys_kernel else
+        kernel_name = (("attn_tc05_keys_kernel" if args.cache == "u8" else "attn_tc05_widen_kernel") if keys_kernel else
                        "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel")
     elif tc05:
         kernel_name = "attn_tc05_kernel"

@@ -121,8 +121,9 @@ KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
   const int G = L->h_q / L->h_kv;
   if (use_tc05(L, variant, n_new)) return tc05_shape();
   if (variant == MQA_VARIANT_TENSOR_CORE && byte_cache(L->cache_dtype))
-    return tc05_keys_applies(G, n_new, L->head_dim, L->paged) ? tc05_keys_shape()
-                                                              : decode_u8_shape(L->head_dim, G, L->cache_dtype == MQA_FP8_E5M2);
+    return !tc05_keys_applies(G, n_new, L->head_dim, L->paged)
+               ? decode_u8_shape(L->head_dim, G, L->cache_dtype == MQA_FP8_E5M2)
+               : (L->cache_dtype == MQA_U8 ? tc05_keys_shape() : tc05_widen_shape());
   if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G * n_new);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
 }
@@ -563,7 +564,9 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   }
   if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype) &&
       tc05_keys_applies(p.group, n_new, layout->head_dim, layout->paged)) {
-    // one-byte MQA step: the tcgen05 kernel with the keys on the MMA rows
+    // one-byte MQA step on tcgen05. e5m2: the heads on the MMA rows, converter
+    // warps widening the code tiles (attn_tc05_widen.cu); uint8: the keys on
+    // the MMA rows (attn_tc05_keys.cu), measured faster for uint8
     CUtensorMap maps[4];
     if (!make_u8_maps(maps, layout, 128, 1)) {
       snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
@@ -594,7 +597,14 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     t.lse_part = p.lse_part;
     t.err = err_word;
     t.early = early;
-    e = launch_tc05_keys_attention(t, layout->cache_dtype == MQA_U8 ? kDtypeU8 : kDtypeF8, maps, s);
+    if (layout->cache_dtype == MQA_U8) {
+      e = launch_tc05_keys_attention(t, kDtypeU8, maps, s);
+    } else {
+      e = launch_tc05_widen_attention(t, maps[0], maps[1], s);
+      if (e != cudaSuccess) return fail_cuda(e);
+      merged = tc05_widen_merges_splits(t);
+      goto combine;
+    }
   } else if (v == MQA_VARIANT_TENSOR_CORE && byte_cache(layout->cache_dtype)) {
     CUtensorMap maps[4];
     // Paged 16- / 32-token pages: blocks over groups of kv heads, one box per

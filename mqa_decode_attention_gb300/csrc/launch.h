@@ -162,6 +162,14 @@ KernelShape tc05_keys_shape();
 bool tc05_keys_applies(int group, int n_new, int head_dim, bool paged);
 cudaError_t launch_tc05_keys_attention(const Tc05Params& p, int cache_dtype, const CUtensorMap* maps,
                                        cudaStream_t stream);
+// the same step over an e5m2 cache with the heads on the MMA rows
+// (attn_tc05_widen.cu): converter warps widen the code tiles. maps: the K and
+// V code maps of make_u8_maps. With two splits the two blocks of a kv head
+// merge in a cluster (no combine: tc05_widen_merges_splits).
+KernelShape tc05_widen_shape();
+bool tc05_widen_merges_splits(const Tc05Params& p);
+cudaError_t launch_tc05_widen_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                        cudaStream_t stream);
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                   cudaStream_t stream);
 // true when launch_tc05_attention merges the splits itself (two splits, R <=
