@@ -3,7 +3,8 @@
 // the MQA / GQA section; uint8 codes with a float32 (scale, zero point) per
 // cached row as in the QuantizedKVCache of "KV Cache 최적화 심층 분석", or fp8
 // e5m2 values) on the 5th-generation tensor cores, with the KEYS on the MMA's
-// row dimension.
+// row dimension. Launched for uint8 only: an e5m2 cache takes
+// attn_tc05_widen.cu (heads on the rows), measured faster for it.
 //
 // A decode step has only G = 32 query rows per kv head, a quarter of the 128
 // rows a tcgen05 MMA computes, so the products are taken transposed and a
@@ -737,7 +738,10 @@ bool tc05_keys_applies(int group, int n_new, int head_dim, bool paged) {
 
 cudaError_t launch_tc05_keys_attention(const Tc05Params& p, int cache_dtype, const CUtensorMap* maps,
                                        cudaStream_t stream) {
-  return cache_dtype == kDtypeU8 ? launch_keys<true>(p, maps, stream) : launch_keys<false>(p, maps, stream);
+  // an e5m2 cache takes attn_tc05_widen.cu (measured faster there); the
+  // kernel's e5m2 form (U8 = false) is kept compiled out
+  if (cache_dtype != kDtypeU8) return cudaErrorInvalidValue;
+  return launch_keys<true>(p, maps, stream);
 }
 
 }  // namespace mqa

@@ -154,10 +154,12 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // tmap_k / tmap_v: the merged-halves bf16 maps with 128-row boxes.
 KernelShape tc05_shape();
-// one-byte cache (uint8 or e5m2), one new token, 16 < G <= 32, contiguous,
-// head_dim 128: keys on the MMA rows (attn_tc05_keys.cu). maps: K codes, V
-// codes (128-row boxes), K and V (scale, zero) rows (uint8; e5m2 repeats the
-// code maps), as make_u8_maps builds them; Tc05Params without the fused fields.
+// uint8 cache, one new token, 16 < G <= 32, contiguous, head_dim 128: keys on
+// the MMA rows (attn_tc05_keys.cu; launched for uint8 only, an e5m2 cache
+// takes attn_tc05_widen.cu). maps: K codes, V codes (128-row boxes), K and V
+// (scale, zero) rows, as make_u8_maps builds them; Tc05Params without the
+// fused fields. tc05_keys_applies covers both byte caches (the shape both
+// MQA kernels take).
 KernelShape tc05_keys_shape();
 bool tc05_keys_applies(int group, int n_new, int head_dim, bool paged);
 cudaError_t launch_tc05_keys_attention(const Tc05Params& p, int cache_dtype, const CUtensorMap* maps,
