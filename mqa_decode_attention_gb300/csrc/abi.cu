@@ -426,9 +426,16 @@ struct RopeArgs {
 
 // The tensor-core kernels can take the append over when one block sees all
 // query heads of its kv head (warp-MMA kernels: G <= 32; tcgen05: one
-// 128-row block).
+// 128-row block). One-byte caches: the contiguous warp-MMA kernel
+// (decode_u8_kernel) only; the paged head-group and the MQA kernels keep the
+// append launch.
 bool fusable(const mqa_kv_layout* L, int variant) {
-  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16) return false;
+  if (variant != MQA_VARIANT_TENSOR_CORE) return false;
+  if (byte_cache(L->cache_dtype)) {
+    const int G = L->h_q / L->h_kv;
+    return !L->paged && !tc05_keys_applies(G, 1, L->head_dim, L->paged) && head_blocks(L, decode_shape(L, variant)) == 1;
+  }
+  if (L->cache_dtype != MQA_BF16) return false;
   if (use_tc05(L, variant, 1)) return L->h_q / L->h_kv <= 128;  // one row block
   return head_blocks(L, decode_shape(L, variant)) == 1;
 }
@@ -490,7 +497,9 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.head_blocks = head_blocks(layout, ks, n_new);
   p.window = layout->window;
   p.early = early;
-  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_BF16 && n_new == 1) {
+  // (one-byte caches: only in the fused step; otherwise q_rot comes from the append launch)
+  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE && n_new == 1 &&
+      (layout->cache_dtype == MQA_BF16 || (byte_cache(layout->cache_dtype) && rope->fuse_append))) {
     p.rope_q = 1;
     p.q_new = rope->q_new;
     p.pos = rope->pos;

@@ -32,7 +32,10 @@
 
 #include "../../include/mqa_decode.h"
 #include "launch.h"
+#include "mma_warp.cuh"
 #include "ptx.cuh"
+#include "quant.cuh"
+#include "rope.cuh"
 
 namespace mqa {
 namespace {
@@ -49,7 +52,7 @@ template <int D, int HB, int STAGES, bool F8 = false>
 struct U8Cfg {
   static constexpr int kConsumerWarps = 4 * HB;
   static constexpr int kConsumerThreads = 32 * kConsumerWarps;
-  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int kThreads = kConsumerThreads + 64;  // + producer warp + append warp (fused step)
   static constexpr int kCodeBytes = kTile * D;  // codes of a K (or V) tile
   static constexpr int kSzBytes = F8 ? 0 : kTile * 8;  // (scale, zero) pairs of a tile
   static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSzBytes;
@@ -148,14 +151,67 @@ struct WarpAttnU8 {
 
   __device__ __forceinline__ void init(const float* q, int rows_valid, float scale_log2, int lane) {
     const int g = lane >> 2, c = lane & 3;
-    qs0 = qs1 = 0.f;
+    init_from(
+        [&](int ks, int hi) {
+          const int row = g + 8 * hi;
+          return row < rows_valid ? *reinterpret_cast<const float4*>(q + row * D + (D / 4) * c + 4 * ks)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        },
+        scale_log2);
+  }
+
+  // This lane's raw bf16 q_new values (rows g, g + 8 of the warp's 16 heads;
+  // dims (D/4) c + 4 ks .. + 3: two rotation pairs), rows >= rows_valid zero.
+  // Kept apart from init_rope so the loads are in flight while the cos / sin
+  // table is formed.
+  __device__ __forceinline__ static void load_q(const __nv_bfloat16* q, int rows_valid, int lane,
+                                                uint2 (&raw)[D / 16][2]) {
+    const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
       for (int hi = 0; hi < 2; ++hi) {
         const int row = g + 8 * hi;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row < rows_valid) v = *reinterpret_cast<const float4*>(q + row * D + (D / 4) * c + 4 * ks);
+        raw[ks][hi] = row < rows_valid ? *reinterpret_cast<const uint2*>(q + row * D + (D / 4) * c + 4 * ks)
+                                       : make_uint2(0u, 0u);
+      }
+    }
+  }
+
+  // Same as init, from the raw q_new of load_q rotated first: pair i turns by
+  // the angle whose fp32 cosine / sine are cs[i] / cs[D/2 + i], as the other
+  // fused kernels form q_rot (written to q_rot_out, [16][D] fp32, unless null).
+  __device__ __forceinline__ void init_rope(const uint2 (&raw)[D / 16][2], int rows_valid, const float* cs,
+                                            float scale_log2, int lane, float* q_rot_out) {
+    const int g = lane >> 2, c = lane & 3;
+    init_from(
+        [&](int ks, int hi) {
+          const int row = g + 8 * hi;
+          const int col = (D / 4) * c + 4 * ks, i = col >> 1;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row < rows_valid) {
+            const uint2 w = raw[ks][hi];
+            const float x0 = bf16lo_to_f32(w.x), y0 = bf16hi_to_f32(w.x);
+            const float x1 = bf16lo_to_f32(w.y), y1 = bf16hi_to_f32(w.y);
+            const float c0 = cs[i], s0 = cs[D / 2 + i], c1 = cs[i + 1], s1 = cs[D / 2 + i + 1];
+            v = make_float4(x0 * c0 - y0 * s0, x0 * s0 + y0 * c0, x1 * c1 - y1 * s1, x1 * s1 + y1 * c1);
+            if (q_rot_out != nullptr) *reinterpret_cast<float4*>(q_rot_out + row * D + col) = v;
+          }
+          return v;
+        },
+        scale_log2);
+  }
+
+  // Q fragments from q4(ks, hi) = the lane's four fp32 values of row g + 8 hi
+  // (g = lane / 4), dims (D/4) c + 4 ks .. + 3; the other state reset.
+  template <class F>
+  __device__ __forceinline__ void init_from(F q4, float scale_log2) {
+    qs0 = qs1 = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const float4 v = q4(ks, hi);
         const __half2 h01 = __floats2half2_rn(v.x * scale_log2, v.y * scale_log2);
         const __half2 h23 = __floats2half2_rn(v.z * scale_log2, v.w * scale_log2);
         qa[ks][hi] = *reinterpret_cast<const uint32_t*>(&h01);
@@ -392,6 +448,94 @@ struct WarpAttnU8 {
   }
 };
 
+// The fused append of a one-byte cache: sequence b's new token at `pos`, kv
+// head j, by one whole warp (lane i owns rotation pairs i, i + 32, ...), with
+// the append kernel's bytes: k turned in fp64 by the fp64 sine and cosine of
+// the reduced angle (round-to-nearest products); uint8: k rounded to fp32 and
+// v taken as fp32, each row quantised with its own (scale, zero point) from
+// its minimum and maximum; e5m2: k (fp64) and v each rounded once to e5m2.
+// load() issues the global reads, write() does the rest and fences the rows
+// for TMA loads (async proxy) issued after the warp's arrival.
+template <int D, bool F8>
+struct AppendRowQ {
+  static constexpr int kPer = D / 64;  // rotation pairs per lane
+  uint32_t k[kPer], v[kPer];
+  double theta[kPer];
+  long long row;
+
+  __device__ __forceinline__ void load(const DecodeParams& p, int b, int j, int pos, int lane) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      theta[i] = p.theta[lane + 32 * i];
+      const long long src = (static_cast<long long>(b) * p.h_kv + j) * D + 2 * (lane + 32 * i);
+      k[i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
+      v[i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
+    }
+    row = cache_row(p, b, j, pos, lane == 0);
+  }
+
+  __device__ __forceinline__ void write(const DecodeParams& p, int pos, int lane) const {
+    if (row >= 0) {  // the same for every lane
+      double xr[kPer], yr[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        double c, sn;
+        sincos(reduce_two_pi(static_cast<double>(pos) * theta[i]), &sn, &c);
+        const double x = bf16lo_to_f32(k[i]), y = bf16hi_to_f32(k[i]);
+        xr[i] = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, sn));
+        yr[i] = __dadd_rn(__dmul_rn(x, sn), __dmul_rn(y, c));
+      }
+      uint8_t* kc = static_cast<uint8_t*>(const_cast<void*>(p.k_cache)) + row;
+      uint8_t* vc = static_cast<uint8_t*>(const_cast<void*>(p.v_cache)) + row;
+      if constexpr (F8) {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int t = lane + 32 * i;
+          *reinterpret_cast<uint16_t*>(kc + 2 * t) = static_cast<uint16_t>(e5m2_code(xr[i]) | (e5m2_code(yr[i]) << 8));
+          *reinterpret_cast<uint16_t*>(vc + 2 * t) = static_cast<uint16_t>(
+              e5m2_code(bf16lo_to_f32(v[i])) | (e5m2_code(bf16hi_to_f32(v[i])) << 8));
+        }
+      } else {
+        float kx[kPer], ky[kPer], vx[kPer], vy[kPer];
+        float kmn = INFINITY, kmx = -INFINITY, vmn = INFINITY, vmx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          kx[i] = __double2float_rn(xr[i]);
+          ky[i] = __double2float_rn(yr[i]);
+          vx[i] = bf16lo_to_f32(v[i]);
+          vy[i] = bf16hi_to_f32(v[i]);
+          kmn = fminf(kmn, fminf(kx[i], ky[i]));
+          kmx = fmaxf(kmx, fmaxf(kx[i], ky[i]));
+          vmn = fminf(vmn, fminf(vx[i], vy[i]));
+          vmx = fmaxf(vmx, fmaxf(vx[i], vy[i]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, off));
+          kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, off));
+          vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, off));
+          vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
+        }
+        const float2 ksz = u8_params(kmn, kmx), vsz = u8_params(vmn, vmx);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int t = lane + 32 * i;
+          *reinterpret_cast<uint16_t*>(kc + 2 * t) =
+              static_cast<uint16_t>(u8_code(kx[i], ksz) | (u8_code(ky[i], ksz) << 8));
+          *reinterpret_cast<uint16_t*>(vc + 2 * t) =
+              static_cast<uint16_t>(u8_code(vx[i], vsz) | (u8_code(vy[i], vsz) << 8));
+        }
+        if (lane == 0) {
+          const_cast<float2*>(p.k_sz)[row / D] = ksz;
+          const_cast<float2*>(p.v_sz)[row / D] = vsz;
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+  }
+};
+
 template <int D, int HB, int STAGES, bool F8>
 __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 2 : 1)
     decode_u8_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
@@ -442,6 +586,22 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   const int t_end = min(L, t_begin + p.chunk);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
 
+  // the fused append (no append launch precedes this one): one block per
+  // sequence and kv head quantises and writes the new token's rows
+  const int apos = p.fuse_append ? p.pos[b] : 0;
+  const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos - t_base, p.chunk, S);
+  if (warp == C::kConsumerWarps + 1) {
+    // --------------------------------------------------------- append warp
+    // writes the rows, fences them for the async proxy and releases the
+    // producer, which waits (named barrier 3) only before the tile holding them
+    if (awaits) {
+      AppendRowQ<D, F8> ar;
+      ar.load(p, b, j, apos, lane);
+      ar.write(p, apos, lane);
+      named_bar_arrive(3, 64);
+    }
+    return;
+  }
   if (warp == C::kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const int ps = p.page_size;
@@ -456,7 +616,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
       wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
     }
     int issued = 0;
-    bool waited = !p.early;
+    bool waited = !p.early, appended = !awaits;
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
@@ -473,6 +633,10 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
       if (!waited && L - 1 < t0 + kTile) {  // this tile holds the appended token
         grid_dependency_wait();
         waited = true;
+      }
+      if (!appended && apos < t0 + kTile) {  // this tile holds the rows the append warp writes
+        named_bar_sync(3, 64);
+        appended = true;
       }
       const uint32_t base = smem_u32(smem + stage * C::kStageBytes);
       const uint32_t kc = base, vc = base + C::kCodeBytes;
@@ -530,6 +694,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
       __syncwarp();
       issued = it + 1;
     }
+    if (!appended) named_bar_sync(3, 64);  // pair the append warp's arrival
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       // let the copies in flight land before the block exits
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
@@ -542,9 +707,21 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   const int hb = warp >> 2;
   const int ws = warp & 3;
   const int head0 = (hsb * HB + hb) * 16;
-  if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
   WarpAttnU8<D, F8> wa;
-  wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
+  if (p.rope_q) {
+    // fused step: q_new rotated here (its loads issued before the cos / sin
+    // table is formed)
+    __shared__ float s_cs[D];
+    const long long qoff = (static_cast<long long>(b) * p.h_q + j * G + head0) * D;
+    uint2 qraw[D / 16][2];
+    WarpAttnU8<D, F8>::load_q(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G - head0, lane, qraw);
+    rope_table<D>(s_cs, p, p.pos[b], threadIdx.x, 2, C::kConsumerThreads);
+    wa.init_rope(qraw, G - head0, s_cs, p.scale_log2, lane,
+                 (p.fuse_append && split == 0 && ws == 0) ? p.q_rot_out + qoff : nullptr);
+  } else {
+    if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
+    wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
+  }
 
   // warps 0, 1 of a head block take the even tiles, warps 2, 3 the odd
   // ones; each warp 32 tokens of its tiles

@@ -9,6 +9,9 @@ of the bf16 exponent range, zeros of both signs, bf16 subnormals, pairs with
 y = +-x or y = 0, infinities and NaN. Each comparison is against
 kv_append_rope, which rotates in fp64 throughout; both must also stay within
 one bf16 ulp of the oracle's rounding wherever the oracle's value is finite.
+One-byte caches (uint8 codes with per-row scale and zero point, fp8 e5m2):
+the fused step of the warp-MMA kernel quantises the new rows itself and must
+write the same bytes as the append kernel.
 """
 
 import math
@@ -18,7 +21,7 @@ import pytest
 import torch
 
 import oracle
-from synthetic import make_contiguous_case, make_paged_case, workload
+from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, make_u8_cache, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -146,3 +149,40 @@ def test_fused_append_tc05_mqa(m):
         caches.append((kc.cpu(), vc.cpu()))
     assert torch.equal(bits(caches[0][0]), bits(caches[1][0]))
     assert torch.equal(bits(caches[0][1]), bits(caches[1][1]))
+
+
+@pytest.mark.parametrize("cache", ["u8", "fp8"])
+def test_fused_append_byte_cache(m, cache):
+    w = workload("gqa4k").with_(batch=48, h_q=32, h_kv=8, seed=101)
+    cap = 1024
+    lens = torch.randint(1, cap + 1, (w.batch,), generator=torch.Generator().manual_seed(102), dtype=torch.int32)
+    c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=cap)
+    k_new = hard_keys(c.k_new.shape, 103)
+    if cache == "u8":
+        # finite keys over a wide range (a row's scale comes from its min and max)
+        k_new = torch.where(torch.isfinite(k_new.float()), k_new, torch.zeros_like(k_new))
+        u = make_u8_cache((w.batch, w.h_kv, cap), w.head_dim, 104)
+        tensors = (u.k_codes, u.v_codes, u.k_sz, u.v_sz)
+    else:
+        kc8, vc8 = make_e5m2_cache((w.batch, w.h_kv, cap), w.head_dim, seed=105)
+        tensors = (kc8, vc8)
+    results = []
+    for fused in (True, False):
+        t = [x.clone().to(DEV) for x in tensors]
+        if cache == "u8":
+            lay = m.layout_contiguous(t[0], t[1], w.h_q, k_scale_zero=t[2], v_scale_zero=t[3])
+        else:
+            lay = m.layout_contiguous(t[0], t[1], w.h_q)
+        bufs = m.DecodeBuffers.allocate(lay, cap, num_splits=1, variant=2, device=DEV)
+        args = (c.q_new.to(DEV), k_new.to(DEV), c.v_new.to(DEV), c.pos.to(DEV), c.seq_lens.to(DEV))
+        if fused:
+            m.decode_step(lay, *args, cap, bufs, w.rope_base, 0.1, num_splits=1, variant=2)
+        else:
+            m.kv_append_rope(lay, args[0], args[1], args[2], args[3], w.rope_base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) & ~int(m.MQA_DEVERR_U8_SCALE) == 0
+        results.append(([x.cpu() for x in t], bufs.q_rot.cpu()))
+    for a, b in zip(results[0][0], results[1][0]):
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+    qa, qb = results[0][1], results[1][1]
+    assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
