@@ -427,13 +427,15 @@ struct RopeArgs {
 // The tensor-core kernels can take the append over when one block sees all
 // query heads of its kv head (warp-MMA kernels: G <= 32; tcgen05: one
 // 128-row block). One-byte caches: the contiguous warp-MMA kernel
-// (decode_u8_kernel) only; the paged head-group and the MQA kernels keep the
-// append launch.
+// (decode_u8_kernel) and the e5m2 MQA kernel (attn_tc05_widen.cu); the paged
+// head-group kernel and the uint8 MQA kernel keep the append launch.
 bool fusable(const mqa_kv_layout* L, int variant) {
   if (variant != MQA_VARIANT_TENSOR_CORE) return false;
   if (byte_cache(L->cache_dtype)) {
     const int G = L->h_q / L->h_kv;
-    return !L->paged && !tc05_keys_applies(G, 1, L->head_dim, L->paged) && head_blocks(L, decode_shape(L, variant)) == 1;
+    if (L->paged) return false;
+    if (tc05_keys_applies(G, 1, L->head_dim, L->paged)) return L->cache_dtype == MQA_FP8_E5M2;
+    return head_blocks(L, decode_shape(L, variant)) == 1;
   }
   if (L->cache_dtype != MQA_BF16) return false;
   if (use_tc05(L, variant, 1)) return L->h_q / L->h_kv <= 128;  // one row block
@@ -609,6 +611,17 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     if (layout->cache_dtype == MQA_U8) {
       e = launch_tc05_keys_attention(t, kDtypeU8, maps, s);
     } else {
+      if (rope != nullptr && rope->fuse_append) {
+        // one launch: the kernel rotates q_new and encodes the new row itself
+        t.fuse = 1;
+        t.early = 0;
+        t.q_new = rope->q_new;
+        t.k_new = rope->k_new;
+        t.v_new = rope->v_new;
+        t.pos = rope->pos;
+        t.q_rot_out = rope->q_rot;
+        fill_theta(t.theta, layout->head_dim, rope->rope_base);
+      }
       e = launch_tc05_widen_attention(t, maps[0], maps[1], s);
       if (e != cudaSuccess) return fail_cuda(e);
       merged = tc05_widen_merges_splits(t);

@@ -27,15 +27,22 @@
 // keys-on-rows kernel (attn_tc05_keys.cu), measured faster there: its
 // per-key scales lengthen this layout's softmax chain.
 //
+// A one-token step is one launch (FUSE): the softmax warps rotate q_new and
+// write q_rot, warp 11 encodes the new k / v row to e5m2 with the append
+// kernel's encoder and the loaders wait for it only before the tile that holds
+// that row.
+//
 // Warps: 0-3 softmax and epilogue, 4 K loader, 5 V loader (TMA, 3 stages
 // each), 6 MMA issue (one thread) and tensor-memory allocation, 7-8 K
-// converters, 9-10 V converters.
+// converters, 9-10 V converters, 11 the fused step's append.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "../../include/mqa_decode.h"
 #include "launch.h"
 #include "ptx.cuh"
+#include "quant.cuh"
+#include "rope.cuh"
 #include "tc05.cuh"
 
 namespace mqa {
@@ -52,7 +59,7 @@ constexpr int kStages = 3;   // code tiles in flight (K and V each)
 // slower: the three code stages keep more bytes in flight)
 constexpr int kKOpB = 1;
 constexpr int kSBuf = 3;     // S / P buffers in tensor memory
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kCodeStage = kBN * kD;                 // 16 KB: [128 rows][128 B], 128-byte swizzle
 constexpr int kOpBytes = kBN * kD * 2;               // 32 KB fp16 tile: [2 halves][128 rows][128 B]
 constexpr int kQOff = 0;
@@ -91,11 +98,13 @@ constexpr int kSFull = kVOpEmpty + 1;        // [kSBuf]
 constexpr int kPFull = kSFull + kSBuf;       // [kSBuf]
 constexpr int kODone = kPFull + kSBuf;       // [kSBuf]
 constexpr int kDrain = kODone + kSBuf;
-constexpr int kNBars = kDrain + 1;
+constexpr int kAppended = kDrain + 1;        // fused step: the new k / v codes are in the cache
+constexpr int kNBars = kAppended + 1;
 static_assert(kNBars * 8 + 4 <= 512, "barrier area");
 
-// named barriers: 1 the softmax warps, 2 Q rows requested (softmax + loaders)
-constexpr int kBarSoftmax = 1, kBarQ = 2;
+// named barriers: 1 the softmax warps, 2 Q rows requested (softmax + loaders),
+// 3 the fused step's cos / sin table (softmax warps)
+constexpr int kBarSoftmax = 1, kBarQ = 2, kBarTable = 3;
 
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of 16-bit element (r, col) of a tile
   const int half = col >> 6, chunk = (col & 63) >> 3;
@@ -128,7 +137,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // CL: the two splits of a (sequence, kv head) are one cluster of two blocks
 // that merge their results through distributed shared memory; block 0 writes
 // the output (no combine launch, no partials in global memory).
-template <bool CL>
+template <bool FUSE, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_widen_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                            const Tc05Params p) {
@@ -160,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   long long limit = p.capacity < p.max_seq_len ? p.capacity : p.max_seq_len;
   int L = p.seq_lens[b];
+  const int apos = FUSE ? p.pos[b] : 0;  // fused step: the new token's position
   if (L < 1 || L > limit) {
     // reported; the rows are then unspecified
     if (tid == 0 && split == 0 && j == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
@@ -256,6 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = min(L, kstart + p.chunk);
   const int T = t_end > kstart ? (t_end - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
   const bool split_out = S > 1 && !CL;
+  // fused step: the split whose token range holds the new token's position
+  // (else split 0) appends its k / v row
+  const int tbase = (ka / 64) * 64;
+  const bool writer =
+      FUSE && split == ((apos - tbase >= 0 && (apos - tbase) / p.chunk < S) ? (apos - tbase) / p.chunk : 0);
   if (T == 0) {
     // no key of this split: an empty partial (weight 0 in the combine)
     grid_dependency_wait();
@@ -295,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kODone + s), 1);
     }
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kAppended), 1);  // the append warp
     fence_mbar_init();
   }
   if (warp == 6) {
@@ -347,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile loads the Q reads would wait microseconds
     named_bar_sync(kBarQ, kBM + 64);
     if (lane == 0) {
-      bool waited = !p.early;
+      bool waited = !p.early, appended = !writer;
       for (; it < T; ++it) {
         const int s = it % kStages;
         if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1)) {
@@ -358,6 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!waited && Lp < kstart + (it + 1) * kBN) {  // this tile holds the new token's row
           grid_dependency_wait();
           waited = true;
+        }
+        if (!appended && apos < kstart + (it + 1) * kBN) {  // ... written by this block's append warp
+          if (!mbar_wait(bar(kAppended), 0)) {
+            fail(1);
+            break;
+          }
+          appended = true;
         }
         issue(it);
       }
@@ -421,6 +444,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail(1);
     }
     __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------ append (fused step)
+    // the new token's cache row exactly as the append kernel writes it: k pair
+    // i turned in fp64 (fp64 sine and cosine of the reduced angle,
+    // round-to-nearest products) and v, each rounded once to e5m2; a position
+    // outside the cache is reported and nothing is written. Fenced for the
+    // loaders' TMA reads (async proxy), which wait for it only before the tile
+    // that holds the row.
+    if (writer) {
+      if (apos >= 0 && apos < p.capacity) {
+        const long long row0c = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD;
+        const long long src0 = (static_cast<long long>(b) * p.h_kv + j) * kD;
+        uint32_t kraw[kD / 64], vraw[kD / 64];
+#pragma unroll
+        for (int u = 0; u < kD / 64; ++u) {
+          const int i = lane + 32 * u;
+          kraw[u] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src0 + 2 * i);
+          vraw[u] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src0 + 2 * i);
+        }
+        uint8_t* kc = static_cast<uint8_t*>(const_cast<void*>(p.k_cache)) + row0c;
+        uint8_t* vc = static_cast<uint8_t*>(const_cast<void*>(p.v_cache)) + row0c;
+#pragma unroll
+        for (int u = 0; u < kD / 64; ++u) {
+          const int i = lane + 32 * u;
+          double c, sn;
+          sincos(reduce_two_pi(static_cast<double>(apos) * p.theta[i]), &sn, &c);
+          const double x = bf16lo_to_f32(kraw[u]), y = bf16hi_to_f32(kraw[u]);
+          const double xr = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, sn));
+          const double yr = __dadd_rn(__dmul_rn(x, sn), __dmul_rn(y, c));
+          *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(e5m2_code(xr) | (e5m2_code(yr) << 8));
+          *reinterpret_cast<uint16_t*>(vc + 2 * i) = static_cast<uint16_t>(
+              e5m2_code(bf16lo_to_f32(vraw[u])) | (e5m2_code(bf16hi_to_f32(vraw[u])) << 8));
+        }
+      } else if (lane == 0) {
+        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kAppended));
+    }
   } else if (warp >= 7) {
     // ------------------------------------------- converters: warps 7-8 K, 9-10 V
     // Each widens rows ct and ct + 64 of its tiles. K and V have their own
@@ -493,12 +556,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fp16 in the swizzled tile. The whole row is requested at once, and
       // the loaders are released only then: behind their burst of tile
       // requests these loads would wait microseconds.
-      if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
       float4 qv[kD / 4];
-      const float4* q = reinterpret_cast<const float4*>(p.q_rot + (row0 + gr) * kD);
+      if constexpr (FUSE) {
+        // fused step: q_new (bf16) rotated here, pair i by the fp32 cosine /
+        // sine of the fp64-reduced angle pos * theta_i, as the other fused
+        // kernels form q_rot
+        __shared__ float s_cs[kD];
+        const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_new) + (row0 + gr) * kD);
+        uint4 raw[kD / 8];
 #pragma unroll
-      for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-      named_bar_arrive(kBarQ, kBM + 64);
+        for (int c = 0; c < kD / 8; ++c) raw[c] = live ? qn[c] : make_uint4(0u, 0u, 0u, 0u);
+        named_bar_arrive(kBarQ, kBM + 64);
+        if (tid < kD / 2) {
+          const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[tid]);
+          float sf, cf;
+          sincosf(static_cast<float>(ang), &sf, &cf);
+          s_cs[tid] = cf;
+          s_cs[kD / 2 + tid] = sf;
+        }
+        named_bar_sync(kBarTable, kBM);
+#pragma unroll
+        for (int c = 0; c < kD / 8; ++c) {
+          const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+          float rv[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pi = 4 * c + e;  // pair (2 pi, 2 pi + 1)
+            const float x = bf16lo_to_f32(w4[e]), y = bf16hi_to_f32(w4[e]);
+            const float cs = s_cs[pi], sn = s_cs[kD / 2 + pi];
+            rv[2 * e] = x * cs - y * sn;
+            rv[2 * e + 1] = x * sn + y * cs;
+          }
+          qv[2 * c] = make_float4(rv[0], rv[1], rv[2], rv[3]);
+          qv[2 * c + 1] = make_float4(rv[4], rv[5], rv[6], rv[7]);
+        }
+        if (live && part == 0 && split == 0) {  // one copy of each row to q_rot
+          float4* qo = reinterpret_cast<float4*>(p.q_rot_out + (row0 + gr) * kD);
+#pragma unroll
+          for (int c = 0; c < kD / 4; ++c) qo[c] = qv[c];
+        }
+      } else {
+        if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
+        const float4* q = reinterpret_cast<const float4*>(p.q_rot + (row0 + gr) * kD);
+#pragma unroll
+        for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        named_bar_arrive(kBarQ, kBM + 64);
+      }
 #pragma unroll
       for (int c = 0; c < kD; c += 8) {
         const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
@@ -686,9 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (CL) cl_exchange();
 }
 
-template <bool CL>
+template <bool FUSE, bool CL>
 cudaError_t launch_widen(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  auto kern = attn_tc05_widen_kernel<CL>;
+  auto kern = attn_tc05_widen_kernel<FUSE, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -719,8 +822,9 @@ bool tc05_widen_merges_splits(const Tc05Params& p) { return p.num_splits == 2; }
 
 cudaError_t launch_tc05_widen_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                         cudaStream_t stream) {
-  return tc05_widen_merges_splits(p) ? launch_widen<true>(p, tmap_k, tmap_v, stream)
-                                     : launch_widen<false>(p, tmap_k, tmap_v, stream);
+  const bool cl = tc05_widen_merges_splits(p);
+  if (p.fuse) return cl ? launch_widen<true, true>(p, tmap_k, tmap_v, stream) : launch_widen<true, false>(p, tmap_k, tmap_v, stream);
+  return cl ? launch_widen<false, true>(p, tmap_k, tmap_v, stream) : launch_widen<false, false>(p, tmap_k, tmap_v, stream);
 }
 
 }  // namespace mqa

@@ -151,9 +151,10 @@ def test_fused_append_tc05_mqa(m):
     assert torch.equal(bits(caches[0][1]), bits(caches[1][1]))
 
 
-@pytest.mark.parametrize("cache", ["u8", "fp8"])
-def test_fused_append_byte_cache(m, cache):
-    w = workload("gqa4k").with_(batch=48, h_q=32, h_kv=8, seed=101)
+@pytest.mark.parametrize("cache, h_kv", [("u8", 8), ("fp8", 8), ("fp8", 1)])
+def test_fused_append_byte_cache(m, cache, h_kv):
+    """G = 4 (warp-MMA kernel) and, e5m2, G = 32 (MQA tcgen05 kernel)."""
+    w = workload("gqa4k").with_(batch=48 if h_kv > 1 else 192, h_q=32, h_kv=h_kv, seed=101)
     cap = 1024
     lens = torch.randint(1, cap + 1, (w.batch,), generator=torch.Generator().manual_seed(102), dtype=torch.int32)
     c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=cap)
