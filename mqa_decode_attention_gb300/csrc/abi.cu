@@ -427,14 +427,15 @@ struct RopeArgs {
 // The tensor-core kernels can take the append over when one block sees all
 // query heads of its kv head (warp-MMA kernels: G <= 32; tcgen05: one
 // 128-row block). One-byte caches: the contiguous warp-MMA kernel
-// (decode_u8_kernel) and the e5m2 MQA kernel (attn_tc05_widen.cu); the paged
-// head-group kernel and the uint8 MQA kernel keep the append launch.
+// (decode_u8_kernel) and the one-token MQA kernels (attn_tc05_keys.cu for
+// uint8, attn_tc05_widen.cu for e5m2); the paged head-group kernel keeps the
+// append launch.
 bool fusable(const mqa_kv_layout* L, int variant) {
   if (variant != MQA_VARIANT_TENSOR_CORE) return false;
   if (byte_cache(L->cache_dtype)) {
     const int G = L->h_q / L->h_kv;
     if (L->paged) return false;
-    if (tc05_keys_applies(G, 1, L->head_dim, L->paged)) return L->cache_dtype == MQA_FP8_E5M2;
+    if (tc05_keys_applies(G, 1, L->head_dim, L->paged)) return true;
     return head_blocks(L, decode_shape(L, variant)) == 1;
   }
   if (L->cache_dtype != MQA_BF16) return false;
@@ -608,20 +609,22 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     t.lse_part = p.lse_part;
     t.err = err_word;
     t.early = early;
+    if (rope != nullptr && rope->fuse_append) {
+      // one launch: the kernel rotates q_new and encodes the new row itself
+      t.fuse = 1;
+      t.early = 0;
+      t.q_new = rope->q_new;
+      t.k_new = rope->k_new;
+      t.v_new = rope->v_new;
+      t.pos = rope->pos;
+      t.q_rot_out = rope->q_rot;
+      t.k_sz = static_cast<float2*>(layout->k_scale_zero);
+      t.v_sz = static_cast<float2*>(layout->v_scale_zero);
+      fill_theta(t.theta, layout->head_dim, rope->rope_base);
+    }
     if (layout->cache_dtype == MQA_U8) {
       e = launch_tc05_keys_attention(t, kDtypeU8, maps, s);
     } else {
-      if (rope != nullptr && rope->fuse_append) {
-        // one launch: the kernel rotates q_new and encodes the new row itself
-        t.fuse = 1;
-        t.early = 0;
-        t.q_new = rope->q_new;
-        t.k_new = rope->k_new;
-        t.v_new = rope->v_new;
-        t.pos = rope->pos;
-        t.q_rot_out = rope->q_rot;
-        fill_theta(t.theta, layout->head_dim, rope->rope_base);
-      }
       e = launch_tc05_widen_attention(t, maps[0], maps[1], s);
       if (e != cudaSuccess) return fail_cuda(e);
       merged = tc05_widen_merges_splits(t);

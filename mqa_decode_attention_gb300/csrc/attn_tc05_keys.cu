@@ -38,12 +38,18 @@
 // uint8, the (scale, zero point) rows; 3 stages each), 6 MMA issue (one
 // thread) and tensor-memory allocation, 7-10 converters (warp w widens the
 // rows of tensor-memory lane quarter w mod 4).
+// In a one-token step the kernel is the only launch (FUSE): the softmax warps
+// rotate q_new and write q_rot, warp 11 quantises the new row with the append
+// kernel's encoder (append_row_q) and the loaders wait for it only before the
+// tile that holds it.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "../../include/mqa_decode.h"
 #include "launch.h"
 #include "ptx.cuh"
+#include "quant.cuh"
+#include "rope.cuh"
 #include "tc05.cuh"
 
 namespace mqa {
@@ -55,7 +61,7 @@ constexpr int kBN = 128;     // keys per tile (MMA M of S^T)
 constexpr int kStages = 3;   // code tiles in flight
 constexpr int kPB = 3;       // S^T buffers (tensor memory), P^T and scale buffers (shared memory)
 constexpr int kOpB = 2;      // widened K (tensor memory) and V (shared memory) buffers
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kCodeBytes = kBN * kD;                     // 16 KB: [128 rows][128 B], 128-byte swizzle
 constexpr int kSzBytes = kBN * 8;                        // 1 KB: (scale, zero point) per row
 constexpr int kCodeStage = kCodeBytes + kSzBytes;        // 17 KB (1 KB multiple)
@@ -102,13 +108,14 @@ constexpr int kODone = kPFull + kPB;         // [kPB]
 constexpr int kSclFull = kODone + kPB;       // [kPB] uint8: the tile's row scales for the softmax
 constexpr int kSclEmpty = kSclFull + kPB;    // [kPB]
 constexpr int kDrain = kSclEmpty + kPB;
-constexpr int kNBars = kDrain + 1;
+constexpr int kAppended = kDrain + 1;        // fused step: the new row's codes and scales are in the cache
+constexpr int kNBars = kAppended + 1;
 static_assert(kNBars * 8 + 4 <= 512, "barrier area");
 
 // named barriers: 1 the softmax warps (bar.sync), 2 Q rows requested
 // (softmax + loaders), 3 the softmax warps' votes (bar.red; never mixed with
-// bar.sync on one barrier)
-constexpr int kBarSoftmax = 1, kBarQ = 2, kBarVote = 3;
+// bar.sync on one barrier), 4 the fused step's cos / sin table
+constexpr int kBarSoftmax = 1, kBarQ = 2, kBarVote = 3, kBarTable = 4;
 
 __device__ __forceinline__ bool aborted(const Tc05Params& p) {
   return (*reinterpret_cast<volatile int32_t*>(p.err) & static_cast<int>(MQA_DEVERR_TIMEOUT)) != 0;
@@ -170,7 +177,7 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t zz, uint32_t& lo, ui
   }
 }
 
-template <bool U8>
+template <bool U8, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_keys_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                           const __grid_constant__ CUtensorMap tmap_ksz, const __grid_constant__ CUtensorMap tmap_vsz,
@@ -197,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   long long limit = p.capacity < p.max_seq_len ? p.capacity : p.max_seq_len;
   int L = p.seq_lens[b];
+  const int apos = FUSE ? p.pos[b] : 0;  // fused step: the new token's position
   if (L < 1 || L > limit) {
     // reported; the rows are then unspecified
     if (tid == 0 && split == 0 && j == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
@@ -213,6 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = t_end > kstart ? (t_end - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
   const bool split_out = S > 1;
   const long long row0 = static_cast<long long>(b) * p.h_q + j * G;  // output row of head 0 of the group
+  // fused step: the split whose token range holds the new token's position
+  // (else split 0) appends its row
+  const int tbase = (ka / 64) * 64;
+  const bool writer =
+      FUSE && split == ((apos - tbase >= 0 && (apos - tbase) / p.chunk < S) ? (apos - tbase) / p.chunk : 0);
   if (T == 0) {
     // no key of this split: an empty partial (weight 0 in the combine)
     grid_dependency_wait();
@@ -249,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kSclEmpty + s), 4);
     }
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kAppended), 1);  // the append warp
     fence_mbar_init();
   }
   if (warp == 6) {
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile loads the Q reads would wait microseconds
     named_bar_sync(kBarQ, 128 + 64);
     if (lane == 0) {
-      bool waited = !p.early;
+      bool waited = !p.early, appended = !writer;
       for (; it < T; ++it) {
         const int s = it % kStages;
         if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1)) {
@@ -314,6 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!waited && Lp < kstart + (it + 1) * kBN) {  // this tile holds the new token's row
           grid_dependency_wait();
           waited = true;
+        }
+        if (!appended && apos < kstart + (it + 1) * kBN) {  // ... written by this block's append warp
+          if (!mbar_wait(bar(kAppended), 0)) {
+            fail(1);
+            break;
+          }
+          appended = true;
         }
         issue(it);
       }
@@ -377,6 +398,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail(1);
     }
     __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------ append (fused step)
+    // the new token's codes and (scale, zero point) rows exactly as the append
+    // kernel writes them (append_row_q); a position outside the cache is
+    // reported and nothing is written. Fenced for the loaders' TMA reads, which
+    // wait for it only before the tile that holds the row.
+    if (writer) {
+      long long row = -1;
+      if (apos >= 0 && apos < p.capacity)
+        row = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD;
+      else if (lane == 0)
+        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+      append_row_q<kD, !U8>(p, b, j, apos, row, lane);
+      if (lane == 0) mbar_arrive(bar(kAppended));
+    }
   } else if (warp >= 7) {
     // ----------------------------------------------------- converters (row = key)
     const int ct = 32 * (warp & 3) + lane;
@@ -485,18 +521,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = t >> 2, qd = t & 3;
       const bool live = r < G;
       const long long grow = row0 + r;
-      if (p.early) grid_dependency_wait();
       float qv[32];
-      const float4* q = reinterpret_cast<const float4*>(p.q_rot + grow * kD + 32 * qd);
+      if constexpr (FUSE) {
+        // fused step: q_new (bf16) rotated here, pair i by the fp32 cosine /
+        // sine of the fp64-reduced angle pos * theta_i, as the other fused
+        // kernels form q_rot
+        __shared__ float s_cs[kD];
+        const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_new) + grow * kD + 32 * qd);
+        uint4 raw[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 v = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-        qv[4 * c] = v.x;
-        qv[4 * c + 1] = v.y;
-        qv[4 * c + 2] = v.z;
-        qv[4 * c + 3] = v.w;
+        for (int c = 0; c < 4; ++c) raw[c] = live ? qn[c] : make_uint4(0u, 0u, 0u, 0u);
+        named_bar_arrive(kBarQ, 128 + 64);
+        if (t < kD / 2) {
+          const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[t]);
+          float sf, cf;
+          sincosf(static_cast<float>(ang), &sf, &cf);
+          s_cs[t] = cf;
+          s_cs[kD / 2 + t] = sf;
+        }
+        named_bar_sync(kBarTable, 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pi = 16 * qd + 4 * c + e;  // pair (2 pi, 2 pi + 1)
+            const float x = bf16lo_to_f32(w4[e]), y = bf16hi_to_f32(w4[e]);
+            const float cs = s_cs[pi], sn = s_cs[kD / 2 + pi];
+            qv[8 * c + 2 * e] = x * cs - y * sn;
+            qv[8 * c + 2 * e + 1] = x * sn + y * cs;
+          }
+        }
+        if (live && split == 0) {  // one copy of each row to q_rot
+          float4* qo = reinterpret_cast<float4*>(p.q_rot_out + grow * kD + 32 * qd);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) qo[c] = make_float4(qv[4 * c], qv[4 * c + 1], qv[4 * c + 2], qv[4 * c + 3]);
+        }
+      } else {
+        if (p.early) grid_dependency_wait();
+        const float4* q = reinterpret_cast<const float4*>(p.q_rot + grow * kD + 32 * qd);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 v = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+          qv[4 * c] = v.x;
+          qv[4 * c + 1] = v.y;
+          qv[4 * c + 2] = v.z;
+          qv[4 * c + 3] = v.w;
+        }
+        named_bar_arrive(kBarQ, 128 + 64);
       }
-      named_bar_arrive(kBarQ, 128 + 64);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // 8 dims = one 16-byte chunk of the 128-byte row
         const int col = 32 * qd + 8 * c, half = col >> 6, chunk = (col & 63) >> 3;
@@ -710,9 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool U8>
+template <bool U8, bool FUSE>
 cudaError_t launch_keys(const Tc05Params& p, const CUtensorMap* maps, cudaStream_t stream) {
-  auto kern = attn_tc05_keys_kernel<U8>;
+  auto kern = attn_tc05_keys_kernel<U8, FUSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -741,7 +814,7 @@ cudaError_t launch_tc05_keys_attention(const Tc05Params& p, int cache_dtype, con
   // an e5m2 cache takes attn_tc05_widen.cu (measured faster there); the
   // kernel's e5m2 form (U8 = false) is kept compiled out
   if (cache_dtype != kDtypeU8) return cudaErrorInvalidValue;
-  return launch_keys<true>(p, maps, stream);
+  return p.fuse ? launch_keys<true, true>(p, maps, stream) : launch_keys<true, false>(p, maps, stream);
 }
 
 }  // namespace mqa

@@ -453,35 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loaders' TMA reads (async proxy), which wait for it only before the tile
     // that holds the row.
     if (writer) {
-      if (apos >= 0 && apos < p.capacity) {
-        const long long row0c = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD;
-        const long long src0 = (static_cast<long long>(b) * p.h_kv + j) * kD;
-        uint32_t kraw[kD / 64], vraw[kD / 64];
-#pragma unroll
-        for (int u = 0; u < kD / 64; ++u) {
-          const int i = lane + 32 * u;
-          kraw[u] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src0 + 2 * i);
-          vraw[u] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src0 + 2 * i);
-        }
-        uint8_t* kc = static_cast<uint8_t*>(const_cast<void*>(p.k_cache)) + row0c;
-        uint8_t* vc = static_cast<uint8_t*>(const_cast<void*>(p.v_cache)) + row0c;
-#pragma unroll
-        for (int u = 0; u < kD / 64; ++u) {
-          const int i = lane + 32 * u;
-          double c, sn;
-          sincos(reduce_two_pi(static_cast<double>(apos) * p.theta[i]), &sn, &c);
-          const double x = bf16lo_to_f32(kraw[u]), y = bf16hi_to_f32(kraw[u]);
-          const double xr = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, sn));
-          const double yr = __dadd_rn(__dmul_rn(x, sn), __dmul_rn(y, c));
-          *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(e5m2_code(xr) | (e5m2_code(yr) << 8));
-          *reinterpret_cast<uint16_t*>(vc + 2 * i) = static_cast<uint16_t>(
-              e5m2_code(bf16lo_to_f32(vraw[u])) | (e5m2_code(bf16hi_to_f32(vraw[u])) << 8));
-        }
-      } else if (lane == 0) {
+      long long row = -1;
+      if (apos >= 0 && apos < p.capacity)
+        row = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD;
+      else if (lane == 0)
         atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
-      }
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      __syncwarp();
+      append_row_q<kD, true>(p, b, j, apos, row, lane);
       if (lane == 0) mbar_arrive(bar(kAppended));
     }
   } else if (warp >= 7) {

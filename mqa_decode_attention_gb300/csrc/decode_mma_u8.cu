@@ -448,94 +448,6 @@ struct WarpAttnU8 {
   }
 };
 
-// The fused append of a one-byte cache: sequence b's new token at `pos`, kv
-// head j, by one whole warp (lane i owns rotation pairs i, i + 32, ...), with
-// the append kernel's bytes: k turned in fp64 by the fp64 sine and cosine of
-// the reduced angle (round-to-nearest products); uint8: k rounded to fp32 and
-// v taken as fp32, each row quantised with its own (scale, zero point) from
-// its minimum and maximum; e5m2: k (fp64) and v each rounded once to e5m2.
-// load() issues the global reads, write() does the rest and fences the rows
-// for TMA loads (async proxy) issued after the warp's arrival.
-template <int D, bool F8>
-struct AppendRowQ {
-  static constexpr int kPer = D / 64;  // rotation pairs per lane
-  uint32_t k[kPer], v[kPer];
-  double theta[kPer];
-  long long row;
-
-  __device__ __forceinline__ void load(const DecodeParams& p, int b, int j, int pos, int lane) {
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      theta[i] = p.theta[lane + 32 * i];
-      const long long src = (static_cast<long long>(b) * p.h_kv + j) * D + 2 * (lane + 32 * i);
-      k[i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
-      v[i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
-    }
-    row = cache_row(p, b, j, pos, lane == 0);
-  }
-
-  __device__ __forceinline__ void write(const DecodeParams& p, int pos, int lane) const {
-    if (row >= 0) {  // the same for every lane
-      double xr[kPer], yr[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        double c, sn;
-        sincos(reduce_two_pi(static_cast<double>(pos) * theta[i]), &sn, &c);
-        const double x = bf16lo_to_f32(k[i]), y = bf16hi_to_f32(k[i]);
-        xr[i] = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, sn));
-        yr[i] = __dadd_rn(__dmul_rn(x, sn), __dmul_rn(y, c));
-      }
-      uint8_t* kc = static_cast<uint8_t*>(const_cast<void*>(p.k_cache)) + row;
-      uint8_t* vc = static_cast<uint8_t*>(const_cast<void*>(p.v_cache)) + row;
-      if constexpr (F8) {
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int t = lane + 32 * i;
-          *reinterpret_cast<uint16_t*>(kc + 2 * t) = static_cast<uint16_t>(e5m2_code(xr[i]) | (e5m2_code(yr[i]) << 8));
-          *reinterpret_cast<uint16_t*>(vc + 2 * t) = static_cast<uint16_t>(
-              e5m2_code(bf16lo_to_f32(v[i])) | (e5m2_code(bf16hi_to_f32(v[i])) << 8));
-        }
-      } else {
-        float kx[kPer], ky[kPer], vx[kPer], vy[kPer];
-        float kmn = INFINITY, kmx = -INFINITY, vmn = INFINITY, vmx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          kx[i] = __double2float_rn(xr[i]);
-          ky[i] = __double2float_rn(yr[i]);
-          vx[i] = bf16lo_to_f32(v[i]);
-          vy[i] = bf16hi_to_f32(v[i]);
-          kmn = fminf(kmn, fminf(kx[i], ky[i]));
-          kmx = fmaxf(kmx, fmaxf(kx[i], ky[i]));
-          vmn = fminf(vmn, fminf(vx[i], vy[i]));
-          vmx = fmaxf(vmx, fmaxf(vx[i], vy[i]));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, off));
-          kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, off));
-          vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, off));
-          vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
-        }
-        const float2 ksz = u8_params(kmn, kmx), vsz = u8_params(vmn, vmx);
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int t = lane + 32 * i;
-          *reinterpret_cast<uint16_t*>(kc + 2 * t) =
-              static_cast<uint16_t>(u8_code(kx[i], ksz) | (u8_code(ky[i], ksz) << 8));
-          *reinterpret_cast<uint16_t*>(vc + 2 * t) =
-              static_cast<uint16_t>(u8_code(vx[i], vsz) | (u8_code(vy[i], vsz) << 8));
-        }
-        if (lane == 0) {
-          const_cast<float2*>(p.k_sz)[row / D] = ksz;
-          const_cast<float2*>(p.v_sz)[row / D] = vsz;
-        }
-      }
-    }
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    __syncwarp();
-  }
-};
-
 template <int D, int HB, int STAGES, bool F8>
 __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 2 : 1)
     decode_u8_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
@@ -595,9 +507,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
     // writes the rows, fences them for the async proxy and releases the
     // producer, which waits (named barrier 3) only before the tile holding them
     if (awaits) {
-      AppendRowQ<D, F8> ar;
-      ar.load(p, b, j, apos, lane);
-      ar.write(p, apos, lane);
+      append_row_q<D, F8>(p, b, j, apos, cache_row(p, b, j, apos, lane == 0), lane);
       named_bar_arrive(3, 64);
     }
     return;

@@ -100,6 +100,8 @@ struct Tc05Params {
   const void* v_new;
   const int32_t* pos;
   float* q_rot_out;  // RoPE(q_new) [B, H_q, 128] fp32
+  float2* k_sz;      // uint8 cache, fused step: where the new rows' (scale, zero point) go
+  float2* v_sz;
   double theta[kMaxHalfDim];
 };
 

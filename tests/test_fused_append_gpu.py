@@ -151,9 +151,9 @@ def test_fused_append_tc05_mqa(m):
     assert torch.equal(bits(caches[0][1]), bits(caches[1][1]))
 
 
-@pytest.mark.parametrize("cache, h_kv", [("u8", 8), ("fp8", 8), ("fp8", 1)])
+@pytest.mark.parametrize("cache, h_kv", [("u8", 8), ("fp8", 8), ("u8", 1), ("fp8", 1)])
 def test_fused_append_byte_cache(m, cache, h_kv):
-    """G = 4 (warp-MMA kernel) and, e5m2, G = 32 (MQA tcgen05 kernel)."""
+    """G = 4 (warp-MMA kernel) and G = 32 (the MQA tcgen05 kernels)."""
     w = workload("gqa4k").with_(batch=48 if h_kv > 1 else 192, h_q=32, h_kv=h_kv, seed=101)
     cap = 1024
     lens = torch.randint(1, cap + 1, (w.batch,), generator=torch.Generator().manual_seed(102), dtype=torch.int32)
