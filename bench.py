@@ -418,13 +418,12 @@ def bench_ours(args):
     # inside the attention kernel) when one block serves all of a kv head's heads
     tc05 = (not byte and variant in (0, 2) and w.dtype == "bf16" and not w.paged and w.head_dim == 128
             and w.group * nn >= 32)
-    # one-byte caches: the contiguous warp-MMA kernel and the one-token MQA
-    # kernels (not the paged head-group kernel) append the new token themselves
+    # one-byte caches: the warp-MMA kernels and the one-token MQA kernels
+    # append the new token themselves as well
     byte_mqa = byte and nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
     fused = nn == 1 and variant in (0, 2) and (
         (not byte and w.dtype == "bf16" and (w.group <= 128 if tc05 else w.group <= 32))
-        or (byte and not w.paged and not byte_mqa and w.group <= 32)
-        or byte_mqa)
+        or (byte and (w.group <= 32 or byte_mqa)))
     # two splits of at most 64 rows per kv head on the tcgen05 kernel: the two
     # blocks of a kv head form a cluster and merge in shared memory (no combine)
     # (likewise the e5m2 one-token MQA kernel with two splits)

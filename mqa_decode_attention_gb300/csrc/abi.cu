@@ -426,15 +426,13 @@ struct RopeArgs {
 
 // The tensor-core kernels can take the append over when one block sees all
 // query heads of its kv head (warp-MMA kernels: G <= 32; tcgen05: one
-// 128-row block). One-byte caches: the contiguous warp-MMA kernel
-// (decode_u8_kernel) and the one-token MQA kernels (attn_tc05_keys.cu for
-// uint8, attn_tc05_widen.cu for e5m2); the paged head-group kernel keeps the
-// append launch.
+// 128-row block). One-byte caches: the warp-MMA kernels (decode_u8_kernel
+// with one head block, the paged head-group kernel) and the one-token MQA
+// kernels (attn_tc05_keys.cu for uint8, attn_tc05_widen.cu for e5m2).
 bool fusable(const mqa_kv_layout* L, int variant) {
   if (variant != MQA_VARIANT_TENSOR_CORE) return false;
   if (byte_cache(L->cache_dtype)) {
     const int G = L->h_q / L->h_kv;
-    if (L->paged) return false;
     if (tc05_keys_applies(G, 1, L->head_dim, L->paged)) return true;
     return head_blocks(L, decode_shape(L, variant)) == 1;
   }

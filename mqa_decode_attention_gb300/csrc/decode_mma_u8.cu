@@ -849,8 +849,21 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
     int wnxt = (wbase + 32 + lane < n_pages_seq) ? __ldg(trow + wbase + 32 + lane) : -1;
     int issued = 0;
     bool waited = !p.early;
+    // the fused append of the group's HG rows (no append launch precedes this
+    // one), by this warp: once the first stages are in flight, or before the
+    // stage that holds the rows if that comes sooner
+    const int apos = p.fuse_append ? p.pos[b] : 0;
+    bool appended = !(p.fuse_append && split == append_split(apos - t_base, p.chunk, S));
+    auto append = [&]() {
+      for (int h = 0; h < HG; ++h) {
+        const int jj = jg * HG + h;
+        append_row_q<D, F8>(p, b, jj, apos, cache_row(p, b, jj, apos, lane == 0 && h == 0), lane);
+      }
+      appended = true;
+    };
     for (int it = 0; it < n_steps; ++it) {
       const int stage = it % STAGES;
+      if (!appended && it == STAGES) append();
       if (it >= STAGES) {
         if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
           if (lane == 0) {
@@ -866,6 +879,7 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
         grid_dependency_wait();
         waited = true;
       }
+      if (!appended && apos < t0 + C::kTokens) append();  // this stage holds the rows this block appends
       int pg[C::kBoxes];
 #pragma unroll
       for (int k = 0; k < C::kBoxes; ++k) {
@@ -903,6 +917,7 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
       __syncwarp();
       issued = it + 1;
     }
+    if (!appended) append();  // rows this block never reads
     if (*reinterpret_cast<volatile int*>(&s_abort)) {
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
@@ -912,9 +927,20 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
 
   // -------------------------------------------------------------- consumers
   const int j = jg * HG + warp;  // this warp's kv head
-  if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
   WarpAttnU8<D, F8> wa;
-  wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G) * D, G, p.scale_log2, lane);
+  if (p.rope_q) {
+    // fused step: q_new rotated here (its loads issued before the cos / sin
+    // table is formed)
+    __shared__ float s_cs[D];
+    const long long qoff = (static_cast<long long>(b) * p.h_q + j * G) * D;
+    uint2 qraw[D / 16][2];
+    WarpAttnU8<D, F8>::load_q(static_cast<const __nv_bfloat16*>(p.q_new) + qoff, G, lane, qraw);
+    rope_table<D>(s_cs, p, p.pos[b], threadIdx.x, 2, HG * 32);
+    wa.init_rope(qraw, G, s_cs, p.scale_log2, lane, (p.fuse_append && split == 0) ? p.q_rot_out + qoff : nullptr);
+  } else {
+    if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
+    wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G) * D, G, p.scale_log2, lane);
+  }
   bool ok = true;
   for (int it = 0; it < n_steps; ++it) {
     const int stage = it % STAGES;

@@ -187,3 +187,42 @@ def test_fused_append_byte_cache(m, cache, h_kv):
         assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
     qa, qb = results[0][1], results[1][1]
     assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
+
+
+@pytest.mark.parametrize("cache", ["u8", "fp8"])
+def test_fused_append_byte_cache_paged(m, cache):
+    """Paged one-byte pools (16-token pages, G = 8: the head-group kernel,
+    whose producer warp appends the group's rows)."""
+    w = workload("paged").with_(batch=40, seed=111)
+    lens = torch.randint(1, 1500, (w.batch,), generator=torch.Generator().manual_seed(112), dtype=torch.int32)
+    pc = make_paged_case(w, "cpu", seq_lens=lens)
+    k_new = hard_keys(pc.k_new.shape, 113)
+    rows = (pc.num_pages, w.h_kv, pc.page_size)
+    if cache == "u8":
+        k_new = torch.where(torch.isfinite(k_new.float()), k_new, torch.zeros_like(k_new))
+        u = make_u8_cache(rows, w.head_dim, 114)
+        tensors = (u.k_codes, u.v_codes, u.k_sz, u.v_sz)
+    else:
+        tensors = make_e5m2_cache(rows, w.head_dim, seed=115)
+    L = int(lens.max())
+    results = []
+    for fused in (True, False):
+        t = [x.clone().to(DEV) for x in tensors]
+        bt = pc.block_table.to(DEV)
+        if cache == "u8":
+            lay = m.layout_paged(t[0], t[1], bt, w.h_q, k_scale_zero=t[2], v_scale_zero=t[3])
+        else:
+            lay = m.layout_paged(t[0], t[1], bt, w.h_q)
+        bufs = m.DecodeBuffers.allocate(lay, L, num_splits=0, variant=2, device=DEV)
+        args = (pc.q_new.to(DEV), k_new.to(DEV), pc.v_new.to(DEV), pc.pos.to(DEV), pc.seq_lens.to(DEV))
+        if fused:
+            m.decode_step(lay, *args, L, bufs, w.rope_base, 0.1, num_splits=0, variant=2)
+        else:
+            m.kv_append_rope(lay, args[0], args[1], args[2], args[3], w.rope_base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) & ~int(m.MQA_DEVERR_U8_SCALE) == 0
+        results.append(([x.cpu() for x in t], bufs.q_rot.cpu()))
+    for a, b in zip(results[0][0], results[1][0]):
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+    qa, qb = results[0][1], results[1][1]
+    assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
