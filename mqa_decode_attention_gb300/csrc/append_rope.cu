@@ -336,8 +336,11 @@ KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  if ((p.cache_dtype == kDtypeBf16 || p.cache_dtype == kDtypeF32) && static_cast<long long>(p.batch) * p.n_new >= 1024) {
-    // enough tokens to fill the GPU with one block each
+  if ((p.cache_dtype == kDtypeBf16 || p.cache_dtype == kDtypeF32) && static_cast<long long>(p.batch) * p.n_new >= 256) {
+    // one block per token forms its fp64 table once for all heads: from a few
+    // hundred tokens the per-head-block tables' fp64 work costs more than the
+    // parallelism they buy (measured, gqa4k shapes: 256 tokens 21.6 -> 17.3 µs;
+    // at 64 and 128 tokens the per-head-block grid stays faster)
     cfg.gridDim = dim3(p.batch * p.n_new);
     cfg.blockDim = dim3(kAppendThreads);
     cfg.stream = stream;
