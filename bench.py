@@ -50,7 +50,7 @@ DEFAULT_WORKLOAD = "gqa4k"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu", "attn_tc05.cu", "attn_tc05_keys.cu",
                   "attn_tc05_widen.cu",
-                  "mma_warp.cuh", "tc05.cuh",
+                  "mma_warp.cuh", "tc05.cuh", "quant.cuh",
                   "rope.cuh", "ptx.cuh", "launch.h"]
 
 

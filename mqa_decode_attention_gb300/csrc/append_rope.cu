@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "../../include/mqa_decode.h"
 #include "launch.h"
 #include "ptx.cuh"
@@ -67,7 +69,14 @@ struct Elem<float> {
 
 template <typename T, bool QU8, bool F8 = false>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const AppendParams p) {
-  __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];
+  // bf16 cache: no fp64 sine / cosine table. q turns by the fp32 sine / cosine
+  // of the fp64-reduced angle (as the fused decode kernels form q_rot) and k
+  // by rope_k_bf16 (bit for bit the fp64 rotation rounded once to bf16); the
+  // fp32 and one-byte caches, whose stored values depend on the exact fp32 /
+  // fp64 rotation, keep the fp64 table.
+  constexpr bool kFast = std::is_same<T, __nv_bfloat16>::value && !QU8 && !F8;
+  __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];  // fp64 cos / sin; kFast: s_cos holds the angle
+  __shared__ float s_cf[kMaxHalfDim], s_sf[kMaxHalfDim];    // kFast: fp32 cos / sin of the angle
   __shared__ float s_red[kAppendThreads / 32][4];  // uint8 cache: per-warp k/v min and max
   __shared__ long long s_row;     // element offset of the slot row of kv head 0
   __shared__ long long s_stride;  // element distance between kv heads at that slot
@@ -103,10 +112,19 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   if (i1 < n_pairs) x1 = Elem<T>::load2(src + (h_begin + i1 / half) * D + 2 * (i1 % half));
 
   if (threadIdx.x < half) {
-    double cs, sn;
-    rope_cos_sin(pos, p.theta[threadIdx.x], &cs, &sn);
-    s_cos[threadIdx.x] = cs;
-    s_sin[threadIdx.x] = sn;
+    if constexpr (kFast) {
+      const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]);
+      float sf, cf;
+      sincosf(static_cast<float>(ang), &sf, &cf);
+      s_cos[threadIdx.x] = ang;
+      s_cf[threadIdx.x] = cf;
+      s_sf[threadIdx.x] = sf;
+    } else {
+      double cs, sn;
+      rope_cos_sin(pos, p.theta[threadIdx.x], &cs, &sn);
+      s_cos[threadIdx.x] = cs;
+      s_sin[threadIdx.x] = sn;
+    }
   }
   if (threadIdx.x == 0 && kv_block) {
     int ok = 1;
@@ -151,7 +169,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
       if (idx >= n_pairs) continue;
       const float2 x = u == 0 ? x0 : x1;
       const int h = h_begin + idx / half, i = idx % half;
-      const float c = static_cast<float>(s_cos[i]), s = static_cast<float>(s_sin[i]);
+      const float c = kFast ? s_cf[i] : static_cast<float>(s_cos[i]);
+      const float s = kFast ? s_sf[i] : static_cast<float>(s_sin[i]);
       *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
     }
     return;
@@ -244,10 +263,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
     if (idx >= n_pairs) continue;
     const float2 x = u == 0 ? x0 : x1;
     const int h = h_begin + idx / half, i = idx % half;
-    const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
-    const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
-    const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
-    Elem<T>::store2_from_f64(kc + h * stride + 2 * i, xr, yr);
+    if constexpr (kFast) {
+      *reinterpret_cast<__nv_bfloat162*>(kc + h * stride + 2 * i) = rope_k_bf16(x.x, x.y, s_cos[i]);
+    } else {
+      const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
+      const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
+      const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
+      Elem<T>::store2_from_f64(kc + h * stride + 2 * i, xr, yr);
+    }
     Elem<T>::copy2(vc + h * stride + 2 * i, v + h * D + 2 * i);
   }
 }
@@ -258,7 +281,9 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 // per-head-block grid would evaluate the same fp64 table once per head block).
 template <typename T>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(const AppendParams p) {
-  __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];
+  constexpr bool kFast = std::is_same<T, __nv_bfloat16>::value;  // as in append_rope_kernel
+  __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];  // fp64 cos / sin; kFast: s_cos holds the angle
+  __shared__ float s_cf[kMaxHalfDim], s_sf[kMaxHalfDim];    // kFast: fp32 cos / sin of the angle
   __shared__ long long s_row, s_stride;
   __shared__ int s_ok;
   grid_dependents_launch();
@@ -267,10 +292,19 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   const int D = p.head_dim, half = D >> 1;
   const int pos = p.pos[b] + (bt - b * p.n_new);
   if (threadIdx.x < half) {
-    double cs, sn;
-    rope_cos_sin(pos, p.theta[threadIdx.x], &cs, &sn);
-    s_cos[threadIdx.x] = cs;
-    s_sin[threadIdx.x] = sn;
+    if constexpr (kFast) {
+      const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]);
+      float sf, cf;
+      sincosf(static_cast<float>(ang), &sf, &cf);
+      s_cos[threadIdx.x] = ang;
+      s_cf[threadIdx.x] = cf;
+      s_sf[threadIdx.x] = sf;
+    } else {
+      double cs, sn;
+      rope_cos_sin(pos, p.theta[threadIdx.x], &cs, &sn);
+      s_cos[threadIdx.x] = cs;
+      s_sin[threadIdx.x] = sn;
+    }
   }
   if (threadIdx.x == 0) {
     int ok = 1;
@@ -310,7 +344,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   for (int idx = threadIdx.x; idx < p.h_q * half; idx += kAppendThreads) {
     const int h = idx / half, i = idx - h * half;
     const float2 x = Elem<T>::load2(qs + h * D + 2 * i);
-    const float c = static_cast<float>(s_cos[i]), s = static_cast<float>(s_sin[i]);
+    const float c = kFast ? s_cf[i] : static_cast<float>(s_cos[i]);
+    const float s = kFast ? s_sf[i] : static_cast<float>(s_sin[i]);
     *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
   }
   if (!s_ok) return;
@@ -322,10 +357,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   for (int idx = threadIdx.x; idx < p.h_kv * half; idx += kAppendThreads) {
     const int h = idx / half, i = idx - h * half;
     const float2 x = Elem<T>::load2(ks + h * D + 2 * i);
-    const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
-    const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
-    const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
-    Elem<T>::store2_from_f64(kc + h * s_stride + 2 * i, xr, yr);
+    if constexpr (kFast) {
+      *reinterpret_cast<__nv_bfloat162*>(kc + h * s_stride + 2 * i) = rope_k_bf16(x.x, x.y, s_cos[i]);
+    } else {
+      const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
+      const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
+      const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
+      Elem<T>::store2_from_f64(kc + h * s_stride + 2 * i, xr, yr);
+    }
     Elem<T>::copy2(vc + h * s_stride + 2 * i, vs + h * D + 2 * i);
   }
 }
