@@ -230,8 +230,9 @@ MQA_API mqa_status splitkv_combine(const float* o_part, const float* lse_part, i
  * fp32 [batch, h_q, head_dim] scratch that carries the rotated query from the
  * first launch to the second. Every argument of both calls is checked before
  * the first launch. On the tensor-core path the step is ONE launch (plus the
- * combine when it splits; two splits of the tcgen05 one-token kernels merge
- * inside the launch) when one block serves all query heads of a kv head -- at
+ * combine when it splits; two splits of the bf16 and e5m2 tcgen05 one-token
+ * kernels merge inside the launch) when one block serves all query heads of a
+ * kv head -- at
  * most 32 of them on the warp-MMA kernels, 32 to 128 on the bf16 tcgen05
  * kernel (contiguous cache, head_dim 128), 17 to 32 on the one-byte-cache
  * tcgen05 kernels: the attention kernel rotates q and k_new itself, writes the
