@@ -232,17 +232,15 @@ MQA_API mqa_status splitkv_combine(const float* o_part, const float* lse_part, i
  * the first launch. On the tensor-core path the step is ONE launch (plus the
  * combine when it splits; two splits of the bf16 and e5m2 tcgen05 one-token
  * kernels merge inside the launch) when one block serves all query heads of a
- * kv head -- at
- * most 32 of them on the warp-MMA kernels, 32 to 128 on the bf16 tcgen05
- * kernel (contiguous cache, head_dim 128), 17 to 32 on the one-byte-cache
- * tcgen05 kernels: the attention kernel rotates q and k_new itself, writes the
- * new token's slot (quantised, for a uint8 or e5m2 cache, exactly as
- * kv_append_rope writes it) and q_rot, and then reads that slot back.
- * Otherwise the attention launch directly follows the
- * append launch and is allowed to start while the append is still running:
- * it streams every cached row except the appended one, the lengths and the
- * block table early, and waits for the append before it reads q_rot or the
- * new token's row.
+ * kv head -- at most 32 of them on the warp-MMA kernels, 32 to 128 on the bf16
+ * tcgen05 kernel (contiguous cache, head_dim 128), 17 to 32 on the
+ * one-byte-cache tcgen05 kernels: the attention kernel rotates q and k_new
+ * itself, writes the new token's slot (quantised, for a uint8 or e5m2 cache,
+ * exactly as kv_append_rope writes it) and q_rot, and then reads that slot
+ * back. Otherwise the attention launch directly follows the append launch and
+ * is allowed to start while the append is still running: it streams every
+ * cached row except the appended one, the lengths and the block table early,
+ * and waits for the append before it reads q_rot or the new token's row.
  */
 MQA_API mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_new, const void* k_new,
                                    const void* v_new, const int32_t* pos, const int32_t* seq_lens,
