@@ -186,7 +186,7 @@ MANY_HEADS = [
 
 
 @pytest.mark.parametrize("shape", MANY_HEADS, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}")
-@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("splits", [1, 2, 3, 0])
 def test_e5m2_many_heads_matches_oracle(m, shape, splits):
     B, hq, hkv, lens, cap = shape
     w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=420 + hq + hkv)
