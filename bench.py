@@ -421,9 +421,11 @@ def bench_ours(args):
     # one-byte caches: the warp-MMA kernels and the one-token MQA kernels
     # append the new token themselves as well
     byte_mqa = byte and nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
-    fused = nn == 1 and variant in (0, 2) and (
-        (not byte and w.dtype == "bf16" and (w.group <= 128 if tc05 else w.group <= 32))
-        or (byte and (w.group <= 32 or byte_mqa)))
+    fused = variant in (0, 2) and (
+        (nn == 1 and not byte and w.dtype == "bf16" and (w.group <= 128 if tc05 else w.group <= 32))
+        or (nn == 1 and byte and (w.group <= 32 or byte_mqa))
+        # several new tokens: the warp-MMA kernel (not tcgen05) for up to 8 of them
+        or (1 < nn <= 8 and not byte and w.dtype == "bf16" and not tc05 and w.group * nn <= 32))
     # two splits of at most 64 rows per kv head on the tcgen05 kernel: the two
     # blocks of a kv head form a cluster and merge in shared memory (no combine)
     # (likewise the e5m2 one-token MQA kernel with two splits)

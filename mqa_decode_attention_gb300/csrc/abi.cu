@@ -441,6 +441,15 @@ bool fusable(const mqa_kv_layout* L, int variant) {
   return head_blocks(L, decode_shape(L, variant)) == 1;
 }
 
+// Several new tokens per sequence (bf16 cache): the warp-MMA kernel takes the
+// appends over when one block sees all (token, head) rows of its kv head and
+// the tokens' cos / sin tables fit (at most kMaxFusedNewTokens).
+bool fusable_multi(const mqa_kv_layout* L, int variant, int n_new) {
+  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16) return false;
+  if (n_new < 2 || n_new > kMaxFusedNewTokens || use_tc05(L, variant, n_new)) return false;
+  return head_blocks(L, decode_shape(L, variant, n_new), n_new) == 1;
+}
+
 mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens, int32_t max_seq_len,
                           float scale, int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
                           void* workspace, size_t workspace_bytes, int32_t variant, int32_t* err_word,
@@ -498,9 +507,11 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.head_blocks = head_blocks(layout, ks, n_new);
   p.window = layout->window;
   p.early = early;
-  // (one-byte caches: only in the fused step; otherwise q_rot comes from the append launch)
-  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE && n_new == 1 &&
-      (layout->cache_dtype == MQA_BF16 || (byte_cache(layout->cache_dtype) && rope->fuse_append))) {
+  // (one-byte caches and several new tokens: only in the fused step;
+  // otherwise q_rot comes from the append launch)
+  if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE &&
+      ((n_new == 1 && (layout->cache_dtype == MQA_BF16 || (byte_cache(layout->cache_dtype) && rope->fuse_append))) ||
+       (n_new > 1 && rope->fuse_append))) {
     p.rope_q = 1;
     p.q_new = rope->q_new;
     p.pos = rope->pos;
@@ -884,11 +895,11 @@ mqa_status step_impl(const mqa_kv_layout* layout, int n_new, const void* q_new, 
   }
   const mqa_status ca = check_append_args(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word);
   if (ca != MQA_OK) return ca;
-  if (n_new == 1 && fusable(layout, v)) {
-    // one launch: the attention kernel appends the new token itself
+  if ((n_new == 1 && fusable(layout, v)) || fusable_multi(layout, v, n_new)) {
+    // one launch: the attention kernel appends the new token(s) itself
     const RopeArgs rope{q_new, pos, rope_base, 1, k_new, v_new, q_rot};
     return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, num_splits, out, out_dtype, lse_out,
-                          workspace, workspace_bytes, variant, err_word, stream, /*early=*/0, &rope);
+                          workspace, workspace_bytes, variant, err_word, stream, /*early=*/0, &rope, n_new);
   }
   const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);
   if (a != MQA_OK) return a;

@@ -124,19 +124,30 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
 
 
-  // the fused append (no append launch precedes this one): one block per
-  // sequence and kv head writes the new token's row
+  // the fused append (no append launch precedes this one): new token i
+  // (at apos + i) is written by the head-block-0 block of the split whose
+  // token range holds it (else split 0), so that no block reads a row that
+  // another block writes; a_first is this block's first such row
   const int apos = p.fuse_append ? p.pos[b] : 0;
-  const bool awaits = p.fuse_append && hsb == 0 && split == append_split(apos - t_base, p.chunk, S);
+  int a_first = -1;
+  if (p.fuse_append && hsb == 0) {
+    for (int i = nq - 1; i >= 0; --i)
+      if (split == append_split(apos + i - t_base, p.chunk, S)) a_first = i;
+  }
+  const bool awaits = a_first >= 0;
   if (warp == C::kConsumerWarps + 1) {
     // --------------------------------------------------------- append warp
-    // writes the row, fences it for the async proxy and releases the
-    // producer, which waits (named barrier 3) only before the tile holding it
+    // writes the rows, fences them for the async proxy and releases the
+    // producer, which waits (named barrier 3) only before the first tile
+    // holding one of them
     if (awaits) {
-      AppendRows<D, 1> ar;
-      ar.load(p, b, j, apos, lane);
-      ar.write(p, apos, lane);
-      ar.publish();
+      for (int i = a_first; i < nq; ++i) {
+        if (split != append_split(apos + i - t_base, p.chunk, S)) continue;
+        AppendRows<D, 1> ar;
+        ar.load(p, b, j, apos + i, lane, i, nq);
+        ar.write(p, apos + i, lane);
+      }
+      AppendRows<D, 1>::publish();
       named_bar_arrive(3, 64);
     }
     return;
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
         grid_dependency_wait();
         waited = true;
       }
-      if (!appended && apos < t0 + kTile) {  // this tile holds the row the append warp writes
+      if (!appended && apos + a_first < t0 + kTile) {  // this tile holds a row the append warp writes
         named_bar_sync(3, 64);
         appended = true;
       }
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
   const int c2 = (lane & 3) * 2;      // fragment column pair
 
   WarpAttn<D> wa;
-  if (p.rope_q) {
+  if (p.rope_q && !MULTI) {
     // rotate q_new here: nothing the consumers read comes from the append kernel
     // (the q loads are issued before the cos / sin table is formed)
     __shared__ float s_cs[D];
@@ -266,6 +277,36 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
     rope_table<D>(s_cs, p, p.pos[b], threadIdx.x, 2, C::kConsumerThreads);
     wa.init_rope(qraw, G - head0, s_cs, p.scale_log2, lane,
                  (p.fuse_append && split == 0 && ws == 0) ? p.q_rot_out + qoff : nullptr);
+  } else if (MULTI && p.fuse_append) {
+    // fused multi-token step: q_new [B, n, H_q, D] rotated here, row (i, h)
+    // by the table of position pos + i (fp32 cos / sin of the fp64-reduced
+    // angle, one table per new token); the rows' loads are issued first
+    __shared__ float s_csm[kMaxFusedNewTokens][D];
+    auto qnew = [&](int r) -> const __nv_bfloat16* {
+      if (r >= R) return nullptr;
+      const int i = r / G;
+      return static_cast<const __nv_bfloat16*>(p.q_new) +
+             ((static_cast<long long>(b) * nq + i) * p.h_q + j * G + (r - i * G)) * D;
+    };
+    auto qout = [&](int r) -> float* {
+      if (r >= R || split != 0 || ws != 0) return nullptr;
+      const int i = r / G;
+      return p.q_rot_out + ((static_cast<long long>(b) * nq + i) * p.h_q + j * G + (r - i * G)) * D;
+    };
+    const int ra = head0 + (lane >> 2), rb = ra + 8;
+    uint32_t qraw[D / 16][4];
+    WarpAttn<D>::load_q2(qnew(ra), qnew(rb), lane, qraw);
+    for (int idx = threadIdx.x; idx < nq * (D / 2); idx += C::kConsumerThreads) {
+      const int i = idx / (D / 2), t = idx - i * (D / 2);
+      const double ang = reduce_two_pi(static_cast<double>(apos + i) * p.theta[t]);
+      float sf, cf;
+      sincosf(static_cast<float>(ang), &sf, &cf);
+      s_csm[i][t] = cf;
+      s_csm[i][D / 2 + t] = sf;
+    }
+    named_bar_sync(2, C::kConsumerThreads);
+    wa.init2_rope(qraw, ra < R, rb < R, s_csm[min(ra, R - 1) / G], s_csm[min(rb, R - 1) / G], p.scale_log2, lane,
+                  qout(ra), qout(rb));
   } else if (MULTI) {
     if (p.early) grid_dependency_wait();  // q_rot comes from the append kernel
     auto qrow = [&](int r) -> const float* {

@@ -8,6 +8,7 @@
 namespace mqa {
 
 constexpr int kTile = 64;          // tokens per pipeline stage of the decode kernels
+constexpr int kMaxFusedNewTokens = 8;  // new tokens per sequence a fused multi-token step takes
 constexpr int kMaxHalfDim = 64;    // RoPE frequencies held in the append kernel's parameters
 constexpr int kDtypeBf16 = 0;
 constexpr int kDtypeF32 = 1;

@@ -91,14 +91,18 @@ struct AppendRows {
   double theta[kPer];
   long long row[H];
 
-  __device__ __forceinline__ void load(const DecodeParams& p, int b, int j0, int pos, int lane) {
+  // tok / n_tok: the new token's index among the sequence's n_tok new tokens
+  // (k_new / v_new [B, n_tok, H_kv, D])
+  __device__ __forceinline__ void load(const DecodeParams& p, int b, int j0, int pos, int lane, int tok = 0,
+                                       int n_tok = 1) {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) theta[i] = p.theta[lane + 32 * i];
 #pragma unroll
     for (int h = 0; h < H; ++h) {
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        const long long src = (static_cast<long long>(b) * p.h_kv + j0 + h) * D + 2 * (lane + 32 * i);
+        const long long src =
+            ((static_cast<long long>(b) * n_tok + tok) * p.h_kv + j0 + h) * D + 2 * (lane + 32 * i);
         k[h][i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
         v[h][i] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
       }
@@ -317,6 +321,55 @@ struct WarpAttn {
           const float c = cs[col >> 1], s = cs[D / 2 + (col >> 1)];
           v = make_float2(x * c - y * s, x * s + y * c);
           if (q_rot_out != nullptr) *reinterpret_cast<float2*>(q_rot_out + row * D + col) = v;
+        }
+        qa[ks][part] = pack_bf16x2(v.x * scale_log2, v.y * scale_log2);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  }
+
+  // Two rows of raw bf16 q_new for init2_rope: q0 is row r0 = lane / 4 of the
+  // warp's 16, q1 row r0 + 8 (each bf16 [D], or null for padding); this
+  // lane's columns of both.
+  __device__ __forceinline__ static void load_q2(const __nv_bfloat16* q0, const __nv_bfloat16* q1, int lane,
+                                                 uint32_t (&raw)[D / 16][4]) {
+    const int c2 = (lane & 3) * 2;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        const __nv_bfloat16* q = (part & 1) ? q1 : q0;
+        const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
+        raw[ks][part] = q != nullptr ? *reinterpret_cast<const uint32_t*>(q + col) : 0u;
+      }
+    }
+  }
+
+  // Same as init2, from the raw rows of load_q2 rotated first, row r0 by the
+  // fp32 cos / sin table cs0 (cs[i], cs[D/2 + i] for pair i) and row r0 + 8 by
+  // cs1 (rows of different new tokens turn by different positions); the
+  // rotated rows also go to out0 / out1 (fp32 [D]) unless null.
+  __device__ __forceinline__ void init2_rope(const uint32_t (&raw)[D / 16][4], bool valid0, bool valid1,
+                                             const float* cs0, const float* cs1, float scale_log2, int lane,
+                                             float* out0, float* out1) {
+    const int c2 = (lane & 3) * 2;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        const bool hi = (part & 1) != 0;
+        const int col = ks * 16 + c2 + ((part & 2) ? 8 : 0);
+        const float* cs = hi ? cs1 : cs0;
+        float* out = hi ? out1 : out0;
+        float2 v = make_float2(0.f, 0.f);
+        if (hi ? valid1 : valid0) {
+          const float x = bf16lo_to_f32(raw[ks][part]), y = bf16hi_to_f32(raw[ks][part]);
+          const float c = cs[col >> 1], sn = cs[D / 2 + (col >> 1)];
+          v = make_float2(x * c - y * sn, x * sn + y * c);
+          if (out != nullptr) *reinterpret_cast<float2*>(out + col) = v;
         }
         qa[ks][part] = pack_bf16x2(v.x * scale_log2, v.y * scale_log2);
       }

@@ -226,3 +226,38 @@ def test_fused_append_byte_cache_paged(m, cache):
         assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
     qa, qb = results[0][1], results[1][1]
     assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
+
+
+@pytest.mark.parametrize("n", [2, 4, 7])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fused_append_multi_token(m, n, splits):
+    """Several new tokens per sequence on the warp-MMA kernel: each split's
+    block appends the new rows inside its own token range, so sequences whose
+    new rows straddle a split boundary (lengths 705.., 1409..) are written by
+    two blocks; the cache must equal the append kernel's bit for bit."""
+    w = workload("gqa4k").with_(batch=12, h_q=32, h_kv=8, seed=121 + n)
+    cap = 2048
+    lens = torch.tensor([705, 706, 707, 1409, 1410, 2048, n, 64 + n - 1, 1000, 129, 700, 1500], dtype=torch.int32)
+    c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=cap)
+    gen = torch.Generator().manual_seed(122 + n)
+    q = torch.randn((w.batch, n, w.h_q, w.head_dim), generator=gen).to(torch.bfloat16)
+    k = hard_keys((w.batch, n, w.h_kv, w.head_dim), 123 + n)
+    v = torch.randn((w.batch, n, w.h_kv, w.head_dim), generator=gen).to(torch.bfloat16)
+    pos = (lens - n).to(torch.int32)
+    results = []
+    for fused in (True, False):
+        kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+        lay = m.layout_contiguous(kc, vc, w.h_q)
+        bufs = m.DecodeBuffers.allocate(lay, cap, num_splits=splits, variant=2, device=DEV, n_new=n)
+        args = (q.to(DEV), k.to(DEV), v.to(DEV), pos.to(DEV))
+        if fused:
+            m.decode_step_multi(lay, n, *args, lens.to(DEV), cap, bufs, w.rope_base, 0.1, num_splits=splits, variant=2)
+        else:
+            m.kv_append_rope_multi(lay, n, *args, w.rope_base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        results.append((kc.cpu(), vc.cpu(), bufs.q_rot.cpu()))
+    assert torch.equal(bits(results[0][0]), bits(results[1][0]))
+    assert torch.equal(bits(results[0][1]), bits(results[1][1]))
+    qa, qb = results[0][2], results[1][2]
+    assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
