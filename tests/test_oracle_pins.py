@@ -480,18 +480,82 @@ def test_sliding_window_decode_pins():
 
 
 # ---------------------------------------------------------- uint8 cache
-def test_u8_quantisation_pins():
-    """QuantizedKVCache (youngju.dev): codes in [0, 255]; the round trip is
-    within half a step (scale / 2) of the input; values already on the grid
-    come back exactly; the row min and max land on codes 0 and 255 when the
-    zero point needs no clamping; a constant row takes scale 1."""
+def listing_quantize_torch(x):
+    """QuantizedKVCache.quantize ("KV Cache 최적화 심층 분석", youngju.dev) run as the
+    listing states it, in torch float32: the row's min and max over the last
+    axis, scale = (max - min) / 255, zero point = round(-min / scale) clamped to
+    [0, 255], code = round(x / scale + zero point) clamped and cast to uint8;
+    torch.round rounds half to even. The one reading added is the constant
+    row, whose scale the listing leaves at 0 (a division by zero): scale 1.
+    This route shares nothing with the oracle's numpy code."""
+    t = torch.as_tensor(np.asarray(x, np.float32))
+    lo = t.min(dim=-1, keepdim=True)[0]
+    hi = t.max(dim=-1, keepdim=True)[0]
+    step = (hi - lo) / 255.0
+    step = torch.where(step == 0, torch.ones_like(step), step)
+    zero = (-lo / step).round().clamp(0, 255)
+    codes = ((t / step) + zero).round().clamp(0, 255).to(torch.uint8)
+    return codes.numpy(), step[..., 0].numpy(), zero[..., 0].numpy()
+
+
+def _u8_rows(rng):
+    """Rows that separate the plausible readings of the listing: N(0,1) rows of
+    mixed scales; rows with a positive minimum (zero point clamped to 0) and a
+    negative maximum (clamped to 255); rows whose -min / scale is far from an
+    integer (the order of the offset matters); and tie rows, where
+    x / scale + zero point lands exactly on c + 1/2."""
+    rows = [rng.standard_normal((40, 128)).astype(np.float32) * rng.uniform(0.05, 20, (40, 1)).astype(np.float32)]
+    rows.append(rng.uniform(1.0, 3.0, (8, 128)).astype(np.float32))
+    rows.append(rng.uniform(-5.0, -0.5, (8, 128)).astype(np.float32))
+    # min = -100.4 s, max = 154.6 s: scale ~s, -min / scale ~100.4 -> zero point 100; values
+    # (c - 99.7) s: x / scale + 100 ~ c + 0.3 (code c), (x - min) / scale ~ c + 0.7 (code c + 1)
+    s = np.float32(2.0 ** -6)
+    off = np.tile(np.arange(255, dtype=np.float32) - np.float32(99.7), (4, 1))
+    off[:, 0], off[:, 1] = np.float32(-100.4), np.float32(154.6)
+    rows.append(off * s)
+    return rows
+
+
+def check_u8_quantise(fn):
     rng = np.random.default_rng(31)
-    x = rng.standard_normal((50, 128)).astype(np.float32) * rng.uniform(0.1, 10, (50, 1)).astype(np.float32)
-    codes, scale, zp = oracle.quantize_u8(x)
-    assert codes.dtype == np.uint8 and scale.dtype == np.float32
-    back = oracle.dequantize_u8(codes, scale, zp)
-    assert np.all(np.abs(back - x) <= scale[:, None].astype(np.float64) * (0.5 + 1e-5) + 1e-7)
-    # grid values survive exactly
+    for x in _u8_rows(rng):
+        codes, scale, zp = fn(x)
+        rc, rs, rz = listing_quantize_torch(x)
+        assert codes.dtype == np.uint8 and scale.dtype == np.float32
+        assert np.array_equal(scale, rs) and np.array_equal(zp, rz) and np.array_equal(codes, rc)
+        back = (codes.astype(np.float64) - zp.astype(np.float64)[:, None]) * scale.astype(np.float64)[:, None]
+        inside = (x >= -zp[:, None] * scale[:, None]) & (x <= (255 - zp[:, None]) * scale[:, None])
+        assert np.all(np.abs(back - x)[inside] <= (scale[:, None] * (0.5 + 1e-5) + 1e-7)[np.nonzero(inside)[0], 0])
+    # ties: scale 2^-5 exactly (min -100 s, max 155 s), x = (c - 100 + 1/2) s gives
+    # x / scale + zp = c + 1/2 exactly: half to even picks c for even c, c + 1 for odd
+    s = np.float32(2.0 ** -5)
+    c = np.arange(0, 255)
+    row = np.concatenate([[-100.0, 155.0], c - 100 + 0.5]).astype(np.float32) * s
+    codes, scale, zp = fn(row[None])
+    assert scale[0] == s and zp[0] == 100
+    assert np.array_equal(codes[0, 2:].astype(np.int64), c + (c % 2))
+    assert codes[0, 0] == 0 and codes[0, 1] == 255
+    # the zero point itself on a tie: -min / scale = 100.5 -> 100, 101.5 -> 102
+    for lo, want in ((-100.5, 100), (-101.5, 102)):
+        r = np.array([[lo, lo + 255.0]], np.float32) * s
+        _, sc, z = fn(r)
+        assert sc[0] == s and z[0] == want
+    # clamped zero points: a positive minimum gives 0, a negative maximum 255
+    _, _, z = fn(np.array([[1.0, 2.0, 3.0], [-3.0, -2.0, -1.0]], np.float32))
+    assert z[0] == 0 and z[1] == 255
+    # a constant row takes scale 1 and dequantises to 0 (its value is lost, as the listing's formula would lose it)
+    c3, s3, z3 = fn(np.full((1, 8), 0.5, np.float32))
+    assert s3[0] == 1.0 and np.all(c3.astype(np.float64) - z3[0] == 0.0)
+
+
+def test_u8_quantisation_pins():
+    """QuantizedKVCache (youngju.dev): the oracle's quantiser equals the listing
+    run in torch float32 (codes, scales and zero points identical) on rows that
+    separate the readings, rounds exact ties to even, clamps the zero point,
+    and round-trips within half a step. Values already on the grid come back
+    exactly; the row min and max land on codes 0 and 255."""
+    check_u8_quantise(oracle.quantize_u8)
+    rng = np.random.default_rng(33)
     s = np.float32(0.03125)
     grid = ((rng.integers(0, 256, (4, 64)) - 100) * s).astype(np.float32)
     grid[:, 0] = -100 * s
@@ -500,9 +564,75 @@ def test_u8_quantisation_pins():
     assert np.all(s2 == s) and np.all(z2 == 100)
     assert np.array_equal(oracle.dequantize_u8(c2, s2, z2), grid.astype(np.float64))
     assert np.all(c2[:, 0] == 0) and np.all(c2[:, 1] == 255)
-    # constant row
-    c3, s3, z3 = oracle.quantize_u8(np.full((1, 8), 0.5, np.float32))
-    assert s3[0] == 1.0 and np.all(oracle.dequantize_u8(c3, s3, z3) == 0.0)
+
+
+def test_u8_planted_mistakes_are_caught():
+    """Plausible misreadings of the quantiser each fail a pin: rounding half up,
+    offsetting before the division ((x - min) / scale, no rounded zero point),
+    and an unclamped zero point."""
+    def quantise(x, rnd=np.rint, offset_first=False, clamp_zp=True):
+        x = np.asarray(x, np.float32)
+        mn, mx = x.min(axis=-1), x.max(axis=-1)
+        scale = ((mx - mn) / np.float32(255.0)).astype(np.float32)
+        scale = np.where(scale == 0, np.float32(1.0), scale).astype(np.float32)
+        zp = rnd((-mn) / scale)
+        zp = (np.clip(zp, 0, 255) if clamp_zp else zp).astype(np.float32)
+        if offset_first:
+            v = (x - mn[..., None]) / scale[..., None]
+        else:
+            v = x / scale[..., None] + zp[..., None]
+        return np.clip(rnd(v), 0, 255).astype(np.uint8), scale, zp
+
+    def half_up(v):
+        return np.floor(np.asarray(v) + np.float32(0.5))
+
+    assert not _fails(check_u8_quantise, quantise)  # the restatement itself passes
+    assert _fails(check_u8_quantise, lambda x: quantise(x, rnd=half_up))
+    assert _fails(check_u8_quantise, lambda x: quantise(x, offset_first=True))
+    assert _fails(check_u8_quantise, lambda x: quantise(x, clamp_zp=False))
+
+
+def test_u8_step_matches_listing_and_library():
+    """The uint8 decode step against a route that shares nothing with the oracle:
+    RoPE in complex form (torch), the new key rounded to float32 and quantised
+    by the listing in torch float32, the value likewise, the cache dequantised
+    as the listing's dequantize does ((code - zero point) * scale, here in
+    float64), and torch's fp64 scaled_dot_product_attention over it."""
+    rng = np.random.default_rng(34)
+    B, h_q, h_kv, d, cap, base, sc = 2, 8, 2, 64, 40, 10000.0, 0.125
+    kc = rng.integers(0, 256, (B, h_kv, cap, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, (B, h_kv, cap, d)).astype(np.uint8)
+    ks = np.stack([rng.uniform(0.01, 0.03, (B, h_kv, cap)), rng.integers(100, 156, (B, h_kv, cap))], -1)
+    vs = np.stack([rng.uniform(0.01, 0.03, (B, h_kv, cap)), rng.integers(100, 156, (B, h_kv, cap))], -1)
+    ks, vs = ks.astype(np.float32), vs.astype(np.float32)
+    q = oracle.round_bf16(rng.standard_normal((B, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, h_kv, d)))
+    lens = np.array([40, 13])
+    r = oracle.decode_step_u8(kc, ks, vc, vs, q, k, v, lens, base, sc)
+    theta = torch.pow(torch.tensor(base, dtype=torch.float64), -torch.arange(0, d, 2, dtype=torch.float64) / d)
+
+    def turn(x, pos):
+        z = torch.view_as_complex(torch.from_numpy(np.ascontiguousarray(x)).reshape(*x.shape[:-1], d // 2, 2))
+        return torch.view_as_real(z * torch.polar(torch.ones_like(theta), pos * theta)).reshape(x.shape).numpy()
+
+    for b in range(B):
+        L = int(lens[b])
+        kq, kss, kz = listing_quantize_torch(turn(k[b], L - 1).astype(np.float32))
+        vq, vss, vz = listing_quantize_torch(v[b].astype(np.float32))
+        assert np.array_equal(r["k_codes"][b, :, L - 1], kq) and np.array_equal(r["v_codes"][b, :, L - 1], vq)
+        assert np.array_equal(r["k_sz"][b, :, L - 1], np.stack([kss, kz], -1))
+        assert np.array_equal(r["v_sz"][b, :, L - 1], np.stack([vss, vz], -1))
+        Kc, Vc = kc[b, :, :L].copy(), vc[b, :, :L].copy()
+        Ks, Vs = ks[b, :, :L].copy(), vs[b, :, :L].copy()
+        Kc[:, L - 1], Vc[:, L - 1] = kq, vq
+        Ks[:, L - 1], Vs[:, L - 1] = np.stack([kss, kz], -1), np.stack([vss, vz], -1)
+        Kd = (torch.from_numpy(Kc).double() - torch.from_numpy(Ks[..., 1:]).double()) * torch.from_numpy(Ks[..., :1]).double()
+        Vd = (torch.from_numpy(Vc).double() - torch.from_numpy(Vs[..., 1:]).double()) * torch.from_numpy(Vs[..., :1]).double()
+        qr = torch.from_numpy(turn(q[b], L - 1))
+        ref = F.scaled_dot_product_attention(qr[None, :, None], Kd[None], Vd[None], scale=sc,
+                                             enable_gqa=True)[0, :, 0].numpy()
+        assert np.allclose(r["out"][b], ref, rtol=0, atol=1e-12)
 
 
 def test_u8_decode_step_pins():
