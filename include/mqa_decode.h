@@ -264,8 +264,11 @@ MQA_API mqa_status mqa_decode_step(const mqa_kv_layout* layout, const void* q_ne
  * Arguments as in gqa_decode_attention, without workspace. Returns
  * MQA_ERR_WORKSPACE when mqa_workspace_size(layout, max_seq_len, num_splits,
  * variant) exceeds 32 MiB.
- * The first call on a device looks up the scratch's device address with that
- * device current; make that first call before any stream capture.
+ * The first call in each CUDA context (per device; again after the context is
+ * destroyed and created anew, e.g. by cudaDeviceReset) looks up the scratch's
+ * device address with that device current; make that first call before any
+ * stream capture. A failed lookup returns MQA_ERR_CUDA with its text in
+ * mqa_last_cuda_error.
  * All calls share the one scratch array and it keeps the last call's
  * contents; nothing in it needs clearing, since every call rewrites each
  * partial result it reads. Calls whose work overlaps on the GPU (two streams,

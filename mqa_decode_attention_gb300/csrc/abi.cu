@@ -14,13 +14,19 @@
 #include "launch.h"
 
 namespace {
+thread_local char g_cuda_error[256] = "";
+}  // namespace
+
+void mqa::record_cuda_error(cudaError_t e) {
+  snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+namespace {
 
 using namespace mqa;
 
-thread_local char g_cuda_error[256] = "";
-
 mqa_status fail_cuda(cudaError_t e) {
-  snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  record_cuda_error(e);
   return MQA_ERR_CUDA;
 }
 

@@ -53,6 +53,9 @@ struct MmaCfg {
   static constexpr int kMergeBytes = kConsumerWarps * 16 * (kMergeStride + 2) * 4;
   static constexpr int kBodyBytes = (STAGES * kStageBytes > kMergeBytes) ? STAGES * kStageBytes : kMergeBytes;
   static constexpr int kSmemBytes = kBodyBytes + 2 * STAGES * 8 + 1024;  // + alignment slack
+  // the fused multi-token step's cos / sin tables (one per new token), placed
+  // after the barriers and requested only by that launch
+  static constexpr int kMultiTableBytes = kMaxFusedNewTokens * D * 4;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
     // fused multi-token step: q_new [B, n, H_q, D] rotated here, row (i, h)
     // by the table of position pos + i (fp32 cos / sin of the fp64-reduced
     // angle, one table per new token); the rows' loads are issued first
-    __shared__ float s_csm[kMaxFusedNewTokens][D];
+    float(*s_csm)[D] = reinterpret_cast<float(*)[D]>(smem + C::kBodyBytes + 2 * STAGES * 8);
     auto qnew = [&](int r) -> const __nv_bfloat16* {
       if (r >= R) return nullptr;
       const int i = r / G;
@@ -437,12 +440,14 @@ cudaError_t launch_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUt
   constexpr int ST = mma_stages<D, HB>();
   using C = MmaCfg<D, HB, ST>;
   auto kern = decode_mma_kernel<D, HB, ST, MULTI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  const int smem = C::kSmemBytes + ((MULTI && p.fuse_append) ? C::kMultiTableBytes : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes + (MULTI ? C::kMultiTableBytes : 0));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.h_kv * p.head_blocks * p.num_splits);
   cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -7,6 +7,10 @@
 
 namespace mqa {
 
+// Records `e` as the calling thread's last CUDA error (the text
+// mqa_last_cuda_error returns).
+void record_cuda_error(cudaError_t e);
+
 constexpr int kTile = 64;          // tokens per pipeline stage of the decode kernels
 constexpr int kMaxFusedNewTokens = 8;  // new tokens per sequence a fused multi-token step takes
 constexpr int kMaxHalfDim = 64;    // RoPE frequencies held in the append kernel's parameters

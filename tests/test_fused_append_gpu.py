@@ -21,6 +21,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse
 from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, make_u8_cache, workload
 
 pytestmark = pytest.mark.gpu
@@ -261,3 +262,21 @@ def test_fused_append_multi_token(m, n, splits):
     assert torch.equal(bits(results[0][1]), bits(results[1][1]))
     qa, qb = results[0][2], results[1][2]
     assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
+    # the attention of the fused launch on these boundary cases, with ordinary
+    # keys, against the oracle: a block must see the rows that another block
+    # appended inside its own token range before it reads them
+    k = torch.randn((w.batch, n, w.h_kv, w.head_dim), generator=gen).to(torch.bfloat16)
+    kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
+    lay = m.layout_contiguous(kc, vc, w.h_q)
+    bufs = m.DecodeBuffers.allocate(lay, cap, num_splits=splits, variant=2, device=DEV, n_new=n)
+    m.decode_step_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), pos.to(DEV), lens.to(DEV), cap, bufs, w.rope_base,
+                        1.0 / math.sqrt(w.head_dim), num_splits=splits, variant=2)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16")
+    out = bufs.out.double().cpu().numpy().reshape(ref["out"].shape)
+    lse = bufs.lse.double().cpu().numpy().reshape(ref["lse"].shape)
+    assert np.max(np.abs(out - ref["out"])) <= 2e-2
+    assert np.max(np.abs(lse - ref["lse"])) <= 2e-2
+    assert_lse(lse, ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(w.head_dim), "bf16")

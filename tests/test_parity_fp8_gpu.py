@@ -3,7 +3,9 @@
 The oracle rounds the new token's fp64-rotated key and its bf16 value once to
 e5m2 and attends over the decoded cache in fp64. The append is byte work and
 must match exactly: the appended codes, and nothing else in the caches
-changes. Outputs are bf16, max |err| <= 2e-2 like the bf16 cache path.
+changes. Outputs are bf16, max |err| <= 2e-2 like the bf16 cache path; the
+fp32 lse is held to 1e-4 of the log-sum-exp over the scores the kernels form
+(their fp16 query operand, tests/lse_model.py).
 """
 
 import math
@@ -13,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse, paged_keys
 from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, workload
 
 pytestmark = pytest.mark.gpu
@@ -62,10 +65,18 @@ def _oracle(w, case, kc8, vc8, paged, window=0):
                                    w.rope_base, 1.0 / math.sqrt(w.head_dim), window=window, **kw)
 
 
-def check(got, ref):
+def _keys(ref, case, paged):
+    """The logical keys after the append, decoded from the oracle's codes."""
+    k = oracle.dequantize_e5m2(ref["k_codes"])
+    return paged_keys(k, case.block_table, case.seq_lens, case.page_size) if paged else k
+
+
+def check(got, ref, case, paged=False, window=0):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    assert_lse(got["lse"], ref["q_rot"], _keys(ref, case, paged), case.seq_lens, 1.0 / math.sqrt(case.q_new.shape[-1]),
+               "f16", window=window)
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
     for key in ("k_codes", "v_codes"):  # the appended rows bit for bit, every other row untouched
         bad = np.argwhere(got[key] != ref[key])
@@ -90,7 +101,7 @@ def test_e5m2_contiguous_matches_oracle(m, shape, splits):
     w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, head_dim=d, seed=400 + hq + d)
     c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=cap)
     kc8, vc8 = make_e5m2_cache((B, hkv, cap), d, seed=11 + d)
-    check(run_f8(m, w, c, kc8, vc8, paged=False, splits=splits), _oracle(w, c, kc8, vc8, paged=False))
+    check(run_f8(m, w, c, kc8, vc8, paged=False, splits=splits), _oracle(w, c, kc8, vc8, paged=False), c)
 
 
 @pytest.mark.parametrize("page_size", [16, 32, 64])
@@ -105,7 +116,7 @@ def test_e5m2_paged_matches_oracle(m, page_size, heads):
     kc8, vc8 = make_e5m2_cache((pc.num_pages, w.h_kv, pc.page_size), w.head_dim, seed=31)
     ref = _oracle(w, pc, kc8, vc8, paged=True)
     for splits in (1, 3, 0):
-        check(run_f8(m, w, pc, kc8, vc8, paged=True, splits=splits), ref)
+        check(run_f8(m, w, pc, kc8, vc8, paged=True, splits=splits), ref, pc, paged=True)
 
 
 @pytest.mark.parametrize("window", [1, 17, 100, 1000])
@@ -118,6 +129,8 @@ def test_e5m2_sliding_window(m, window):
         got = run_f8(m, w, c, kc8, vc8, paged=False, splits=splits, window=window, max_len=700)
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
+        assert_lse(got["lse"], ref["q_rot"], _keys(ref, c, False), c.seq_lens, 1.0 / math.sqrt(128), "f16",
+                   window=window, what=splits)
 
 
 def test_e5m2_nan_codes_past_the_sequence(m):
@@ -192,7 +205,7 @@ def test_e5m2_many_heads_matches_oracle(m, shape, splits):
     w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=420 + hq + hkv)
     c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=cap)
     kc8, vc8 = make_e5m2_cache((B, hkv, cap), 128, seed=16 + hq)
-    check(run_f8(m, w, c, kc8, vc8, paged=False, splits=splits), _oracle(w, c, kc8, vc8, paged=False))
+    check(run_f8(m, w, c, kc8, vc8, paged=False, splits=splits), _oracle(w, c, kc8, vc8, paged=False), c)
 
 
 @pytest.mark.parametrize("window", [1, 100, 1000])
@@ -213,6 +226,8 @@ def test_e5m2_mqa_window_and_nan_tail(m, window):
         assert got["err"] == 0
         assert np.all(np.isfinite(got["out"]))
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
+        assert_lse(got["lse"], ref["q_rot"], _keys(ref, c, False), c.seq_lens, 1.0 / math.sqrt(128), "f16",
+                   window=window, what=splits)
 
 
 def test_e5m2_mqa_full_size_sampled(m):

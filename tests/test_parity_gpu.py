@@ -1,6 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
 Tolerances: bf16 outputs max |err| <= 2e-2, fp32 (debug) outputs <= 1e-4.
+The fp32 lse outputs: <= 1e-4 of the oracle's log-sum-exp over the scores the
+kernel forms (its query rounded to the MMA operand type, tests/lse_model.py),
+and <= 2e-2 of the oracle's exact lse.
 Cache-append placement is bit-exact (the set of changed elements is exactly
 the oracle's target slots, V slices are byte copies); an appended K element
 may differ from round-to-nearest of the fp64 RoPE by at most one bf16 ulp.
@@ -13,6 +16,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse, paged_keys
 from synthetic import (make_contiguous_case, make_paged_case, make_tiny_sequence, workload)
 
 pytestmark = pytest.mark.gpu
@@ -20,6 +24,7 @@ pytestmark = pytest.mark.gpu
 BF16_TOL = 2e-2
 F32_TOL = 1e-4
 VARIANTS = {"tc": 2, "cc": 1}
+Q_FMT = {"tc": "bf16", "cc": "f32", 2: "bf16", 1: "f32", 0: "bf16"}  # the query operand of each bf16-cache path
 
 
 @pytest.fixture(scope="module")
@@ -110,6 +115,7 @@ def test_contiguous_matches_oracle(m, variant, shape, splits):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], c.seq_lens, 1.0 / math.sqrt(d), Q_FMT[variant])
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
     check_append(c.k_cache, c.v_cache, got["k"], got["v"], ref["k_cache"], ref["v_cache"], "bf16")
 
@@ -129,11 +135,14 @@ def test_paged_matches_oracle(m, variant, page_size, heads):
     pc = make_paged_case(w, "cpu", seq_lens=lens, spare_pages=3)
     ref = oracle.decode_step_paged(pc.k_pool, pc.v_pool, pc.block_table, pc.q_new, pc.k_new, pc.v_new,
                                    pc.seq_lens, pc.page_size, w.rope_base, 1.0 / math.sqrt(w.head_dim), "bf16")
+    keys = paged_keys(ref["k_pool"], pc.block_table, pc.seq_lens, pc.page_size)
     for splits in (1, 3, 0):
         got = run_paged(m, pc, w, splits=splits, variant=VARIANTS[variant])
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
         assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+        assert_lse(got["lse"], ref["q_rot"], keys, pc.seq_lens, 1.0 / math.sqrt(w.head_dim), Q_FMT[variant],
+                   what=splits)
         check_append(pc.k_pool, pc.v_pool, got["k"], got["v"], ref["k_pool"], ref["v_pool"], "bf16")
 
 
@@ -161,6 +170,7 @@ def test_fp32_output_mode_tight(m):
                                         1.0 / math.sqrt(w.head_dim), "bf16")
     got = run_contiguous(m, c, w, splits=2, variant=1, out_dtype=torch.float32)
     assert np.max(np.abs(got["out"] - ref["out"])) <= F32_TOL
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= F32_TOL
 
 
 # ----------------------------------------------------- fp32 debug sequence
@@ -309,6 +319,11 @@ def _full_contiguous(m, name, n_samples=6):
                                         1.0 / math.sqrt(w.head_dim), "bf16")
         assert np.max(np.abs(_np(bufs.out[b, j * G:(j + 1) * G]) - ro)) <= BF16_TOL, (b, j)
         assert np.max(np.abs(_np(bufs.lse[b, j * G:(j + 1) * G]) - rl)) <= BF16_TOL, (b, j)
+        keys = _np(Ku)[None, None].copy()
+        keys[0, 0, L - 1] = ks
+        assert_lse(_np(bufs.lse[b, j * G:(j + 1) * G])[None],
+                   oracle.rope_rotate(_np(q_new[b, j * G:(j + 1) * G]), L - 1, w.rope_base)[None], keys, [L],
+                   1.0 / math.sqrt(w.head_dim), "bf16", what=(b, j))
         got_k = _np(c.k_cache[b, j, L - 1])
         assert np.all(np.abs(got_k - ks) <= ulp_bf16(ks))
         assert torch.equal(c.v_cache[b, j, L - 1].cpu(), v_new[b, j])
@@ -359,6 +374,10 @@ def test_full_size_paged_sampled(m):
                                      k_new[b:b + 1, j:j + 1], v_new[b:b + 1, j:j + 1], lens[b:b + 1], w.page_size,
                                      w.rope_base, 1.0 / math.sqrt(w.head_dim), "bf16")
         assert np.max(np.abs(_np(bufs.out[b, j * G:(j + 1) * G]) - r["out"][0])) <= BF16_TOL, (b, j)
+        assert np.max(np.abs(_np(bufs.lse[b, j * G:(j + 1) * G]) - r["lse"][0])) <= BF16_TOL, (b, j)
+        assert_lse(_np(bufs.lse[b, j * G:(j + 1) * G])[None], r["q_rot"],
+                   paged_keys(r["k_pool"], rank[None], lens[b:b + 1], w.page_size), lens[b:b + 1],
+                   1.0 / math.sqrt(w.head_dim), "bf16", what=(b, j))
         p = int(lens[b]) - 1
         page = int(table[b, p // w.page_size])
         got_k = _np(pc.k_pool[page, j, p % w.page_size])
@@ -422,6 +441,8 @@ def test_sliding_window_contiguous(m, variant, window):
         assert int(bufs.err.item()) == 0
         assert np.max(np.abs(_np(bufs.out) - ref["out"])) <= BF16_TOL, (splits, window)
         assert np.max(np.abs(_np(bufs.lse) - ref["lse"])) <= BF16_TOL
+        assert_lse(_np(bufs.lse), ref["q_rot"], ref["k_cache"], c.seq_lens, 1.0 / math.sqrt(w.head_dim),
+                   Q_FMT[variant], window=window, what=splits)
 
 
 @pytest.mark.parametrize("variant", [2, 1])
@@ -435,6 +456,7 @@ def test_sliding_window_paged_with_released_pages(m, variant, h_kv, window):
     pc = make_paged_case(w, "cpu", seq_lens=lens)
     ref = oracle.decode_step_paged(pc.k_pool, pc.v_pool, pc.block_table, pc.q_new, pc.k_new, pc.v_new, pc.seq_lens,
                                    pc.page_size, w.rope_base, 1.0 / math.sqrt(w.head_dim), "bf16", window=window)
+    keys = paged_keys(ref["k_pool"], pc.block_table, pc.seq_lens, pc.page_size)
     table = pc.block_table.clone()
     for b in range(w.batch):
         t_lo = max(0, int(lens[b]) - window)
@@ -449,6 +471,8 @@ def test_sliding_window_paged_with_released_pages(m, variant, h_kv, window):
         torch.cuda.synchronize()
         assert int(bufs.err.item()) == 0, (splits, int(bufs.err.item()))
         assert np.max(np.abs(_np(bufs.out) - ref["out"])) <= BF16_TOL, (splits, window)
+        assert_lse(_np(bufs.lse), ref["q_rot"], keys, pc.seq_lens, 1.0 / math.sqrt(w.head_dim), Q_FMT[variant],
+                   window=window, what=splits)
 
 
 def test_sliding_window_full_size_long(m):

@@ -2,7 +2,9 @@
 decoding: n new tokens per sequence, causal among them) against the fp64
 oracle's ``decode_step_multi``.
 
-Tolerances as for single-token decode: bf16 outputs and lse max |err| <= 2e-2;
+Tolerances as for single-token decode: bf16 outputs and lse max |err| <= 2e-2,
+and lse <= 1e-4 of the log-sum-exp over the scores the kernel forms (its bf16
+query operand, tests/lse_model.py);
 the append is placement-exact (only the n target slots of each sequence
 change, V slices are byte copies, K within one bf16 ulp of the fp64 RoPE).
 """
@@ -14,6 +16,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse, paged_keys
 from synthetic import make_contiguous_case, make_paged_case, normal, workload
 
 pytestmark = pytest.mark.gpu
@@ -104,6 +107,7 @@ def test_multi_contiguous_matches_oracle(m, shape, splits):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(d), "bf16")
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
     check_cache(c.k_cache, got["k"], ref["k_cache"], v_cache=False)
     check_cache(c.v_cache, got["v"], ref["v_cache"], v_cache=True)
@@ -118,11 +122,14 @@ def test_multi_paged_matches_oracle(m, page_size, n):
     q, k, v = new_tokens(w, n)
     ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
                                    "bf16", block_table=pc.block_table, page_size=page_size)
+    keys = paged_keys(ref["k_pool"], pc.block_table, lens, page_size)
     for splits in (1, 3, 0):
         got = run_multi(m, w, n, pc.k_pool, pc.v_pool, q, k, v, lens, splits=splits, table=pc.block_table,
                         page_size=page_size)
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, splits
+        assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL, splits
+        assert_lse(got["lse"], ref["q_rot"], keys, lens, 1.0 / math.sqrt(w.head_dim), "bf16", what=splits)
         check_cache(pc.k_pool, got["k"], ref["k_pool"], v_cache=False)
         check_cache(pc.v_pool, got["v"], ref["v_pool"], v_cache=True)
 
@@ -142,6 +149,8 @@ def test_multi_sliding_window(m, window):
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
         assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+        assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(w.head_dim), "bf16",
+                   window=window, what=splits)
 
 
 def test_multi_with_one_token_is_the_single_token_step(m):

@@ -4,8 +4,10 @@ in one pass, on the tcgen05 tensor cores) against the fp64 oracle's
 length.
 
 Tolerances: bf16 outputs and lse max |err| <= 2e-2, fp32 outputs <= 2e-2
-(the scores and P pass through bf16 on the tensor cores); the appended cache
-rows are placement-exact (V byte copies, K within one bf16 ulp).
+(the scores and P pass through bf16 on the tensor cores), lse <= 1e-4 of the
+log-sum-exp over the scores the kernel forms (its bf16 query operand,
+tests/lse_model.py); the appended cache rows are placement-exact (V byte
+copies, K within one bf16 ulp).
 """
 
 import math
@@ -15,6 +17,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse
 from synthetic import make_contiguous_case, make_paged_case, normal, workload
 
 pytestmark = pytest.mark.gpu
@@ -92,6 +95,7 @@ def test_prefill_matches_oracle(m, case):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= TOL
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(w.head_dim), "bf16")
     # appended rows: V byte copies, K within one bf16 ulp, nothing else touched
     bk, ak = _np(c.k_cache), _np(got["k"])
     assert np.array_equal(np.any(ak != bk, axis=-1), np.any(ref["k_cache"] != bk, axis=-1))
@@ -111,6 +115,7 @@ def test_prefill_sliding_window(m, window):
     got = run_prefill(m, w, n, c, q, k, v, lens, window=window)
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= TOL, window
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(w.head_dim), "bf16", window=window)
 
 
 def test_prefill_f32_output_and_unequal_rows(m):

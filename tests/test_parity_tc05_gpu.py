@@ -1,7 +1,9 @@
 """GPU parity of decode steps that run on the tensor-memory (tcgen05) kernel:
 32 or more query rows per kv head (MQA's G = 32; several new tokens per
 sequence), contiguous bf16 cache, head_dim 128. Checked against the fp64
-oracle like every other decode path: outputs and lse <= 2e-2.
+oracle like every other decode path: outputs and lse <= 2e-2, and lse <= 1e-4
+of the log-sum-exp over the scores the kernel forms (its bf16 query operand,
+tests/lse_model.py).
 """
 
 import math
@@ -11,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse
 from synthetic import make_contiguous_case, normal, workload
 
 pytestmark = pytest.mark.gpu
@@ -63,12 +66,14 @@ def ulp_bf16(x):
     return 2.0 ** (e - 7)
 
 
-def check_step(got, ref):
-    """Outputs within the bf16 tolerance, q_rot within fp32 rounding, the
-    appended rows placement-exact (V bytes, K within one bf16 ulp)."""
+def check_step(got, ref, lens):
+    """Outputs within the bf16 tolerance, lse within fp32 rounding of the
+    scores the kernel forms, q_rot within fp32 rounding, the appended rows
+    placement-exact (V bytes, K within one bf16 ulp)."""
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= TOL
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(128), "bf16")
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
     assert np.array_equal(_np(got["v"]), ref["v_cache"])
     k = _np(got["k"])
@@ -95,7 +100,7 @@ def test_tc05_decode_matches_oracle(m, case, splits):
     ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
                                    "bf16")
     got = run(m, w, n, c, q, k, v, lens, splits)
-    check_step(got, ref)
+    check_step(got, ref, lens)
 
 
 @pytest.mark.parametrize("window", [1, 100, 1000])
@@ -110,6 +115,8 @@ def test_tc05_decode_sliding_window(m, window):
         got = run(m, w, n, c, q, k, v, lens, splits, window=window)
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= TOL, (splits, window)
+        assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(128), "bf16", window=window,
+                   what=splits)
 
 
 def test_tc05_mqa_full_size_sampled(m):
@@ -160,6 +167,7 @@ def test_tc05_splits_with_garbage_workspace(m, standalone):
         got = _np(bufs.out).reshape(3, n, 32, -1)
         assert np.max(np.abs(got - ref["out"])) <= TOL
         assert np.max(np.abs(_np(bufs.lse).reshape(3, n, 32) - ref["lse"])) <= TOL
+        assert_lse(_np(bufs.lse).reshape(3, n, 32), ref["q_rot"], ref["k_cache"], lens, scale, "bf16")
 
 
 @pytest.mark.parametrize("n, hq", [(1, 32), (1, 64), (2, 32)])
@@ -175,7 +183,7 @@ def test_tc05_two_split_cluster_merge(m, n, hq):
     q, k, v = new_tokens(w, n)
     scale = 1.0 / math.sqrt(w.head_dim)
     ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, scale, "bf16")
-    check_step(run(m, w, n, c, q, k, v, lens, 2), ref)
+    check_step(run(m, w, n, c, q, k, v, lens, 2), ref, lens)
     # standalone attention over the appended cache, fp32 output
     kc, vc = c.k_cache.to(DEV), c.v_cache.to(DEV)
     lay = m.layout_contiguous(kc, vc, w.h_q)
@@ -193,6 +201,7 @@ def test_tc05_two_split_cluster_merge(m, n, hq):
         # (fp32 output of a tensor-core path: Q and P are bf16 MMA operands)
         assert np.max(np.abs(got - ref["out"])) <= TOL
         assert np.max(np.abs(_np(bufs.lse).reshape(4, n, hq) - ref["lse"])) <= TOL
+        assert_lse(_np(bufs.lse).reshape(4, n, hq), ref["q_rot"], ref["k_cache"], lens, scale, "bf16")
 
 
 def test_tc05_many_short_splits(m):
@@ -208,6 +217,7 @@ def test_tc05_many_short_splits(m):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= TOL
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(128), "bf16")
 
 
 def test_tc05_fused_step_new_slot_holds_nan(m):
@@ -226,7 +236,7 @@ def test_tc05_fused_step_new_slot_holds_nan(m):
     for splits in (3, 1, 0):
         got = run(m, w, 1, c, q, k, v, lens, splits)
         assert np.all(np.isfinite(got["out"]))
-        check_step(got, ref)
+        check_step(got, ref, lens)
 
 
 def test_tc05_fused_step_position_out_of_range(m):

@@ -1,8 +1,9 @@
 """GPU parity of the one-token decode step with 32 query heads per kv head
 (MQA) over a bf16 cache, on the tcgen05 kernel (the 32 query rows replicated
 over the MMA's 128 rows, each copy a quarter of every key tile). Checked
-against the fp64 oracle: outputs and lse <= 2e-2, the appended rows
-placement-exact.
+against the fp64 oracle: outputs and lse <= 2e-2, lse <= 1e-4 of the
+log-sum-exp over the scores the kernel forms (its bf16 query operand,
+tests/lse_model.py), the appended rows placement-exact.
 
 Cases: lengths at the 128-key tile edges and below one tile, sliding windows
 (a block's first tile starts up to 63 keys before the window), several kv
@@ -18,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse
 from synthetic import make_contiguous_case, normal, workload
 
 pytestmark = pytest.mark.gpu
@@ -67,10 +69,12 @@ def step(m, w, c, q, k, v, lens, splits, window=0):
                 q_rot=_np(bufs.q_rot).reshape(B, 1, hq, -1), k=_np(kc), v=_np(vc), err=int(bufs.err.item()))
 
 
-def check(got, ref, what):
+def check(got, ref, what, lens, window=0):
     assert got["err"] == 0, what
     assert np.max(np.abs(got["out"] - ref["out"])) <= TOL, what
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= TOL, what
+    assert_lse(got["lse"], ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(128), "bf16", window=window,
+               what=what)
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"]))), what
     assert np.array_equal(got["v"], ref["v_cache"]), what
     assert np.all(np.abs(got["k"] - ref["k_cache"]) <= ulp_bf16(ref["k_cache"]) + 1e-30), what
@@ -86,7 +90,7 @@ def test_keys_kernel_tile_edges(m, splits):
     q, k, v = new_token(w)
     ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
                                    "bf16")
-    check(step(m, w, c, q, k, v, lens, splits), ref, splits)
+    check(step(m, w, c, q, k, v, lens, splits), ref, splits, lens)
 
 
 @pytest.mark.parametrize("window", [1, 63, 64, 100, 129, 1000])
@@ -98,7 +102,7 @@ def test_keys_kernel_sliding_window(m, window):
     ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
                                    "bf16", window=window)
     for splits in (1, 3, 0):
-        check(step(m, w, c, q, k, v, lens, splits, window=window), ref, (window, splits))
+        check(step(m, w, c, q, k, v, lens, splits, window=window), ref, (window, splits), lens, window)
 
 
 def test_keys_kernel_two_kv_heads(m):
@@ -110,7 +114,7 @@ def test_keys_kernel_two_kv_heads(m):
     ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
                                    "bf16")
     for splits in (1, 4, 0):
-        check(step(m, w, c, q, k, v, lens, splits), ref, splits)
+        check(step(m, w, c, q, k, v, lens, splits), ref, splits, lens)
 
 
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
@@ -138,6 +142,7 @@ def test_keys_kernel_standalone_attention(m, out_dtype):
         assert int(bufs.err.item()) == 0
         assert np.max(np.abs(_np(out) - ref["out"][:, 0])) <= TOL, splits
         assert np.max(np.abs(_np(lse) - ref["lse"][:, 0])) <= TOL, splits
+        assert_lse(_np(lse), ref["q_rot"][:, 0], ref["k_cache"], lens, scale, "bf16", what=splits)
 
 
 def test_keys_kernel_growing_scores_rescale(m):
@@ -162,4 +167,4 @@ def test_keys_kernel_growing_scores_rescale(m):
     s = (qr @ kf[:1280].T) / math.sqrt(w.head_dim) / math.log(2)
     assert int(((s[:, 384:].amax(1) - s[:, :384].amax(1)) > 8).sum()) >= 16
     for splits in (1, 3, 0):
-        check(step(m, w, c, q, k, v, lens, splits), ref, splits)
+        check(step(m, w, c, q, k, v, lens, splits), ref, splits, lens)

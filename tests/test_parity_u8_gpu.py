@@ -4,7 +4,10 @@ The oracle quantises the new token's rotated key and its value in float32 (the
 pages' QuantizedKVCache) and attends over the dequantised cache in fp64. The
 append is integer / byte work and must match exactly: codes, scale and zero
 point of the appended rows, and nothing else in the caches changes. Outputs
-are bf16, max |err| <= 2e-2 like the bf16 cache path.
+are bf16, max |err| <= 2e-2 like the bf16 cache path. The fp32 lse is held to
+the log-sum-exp over the scores the kernels form (their fp16 query operand)
+within 1e-4 plus a bound on the zero-point cancellation of the warp-MMA
+kernel's score form (tests/lse_model.py).
 """
 
 import math
@@ -14,6 +17,7 @@ import pytest
 import torch
 
 import oracle
+from lse_model import assert_lse, paged_keys
 from synthetic import make_contiguous_case, make_paged_case, make_u8_cache, workload
 
 pytestmark = pytest.mark.gpu
@@ -76,6 +80,18 @@ def _oracle(w, case, u, paged, window=0):
                                  case.seq_lens, w.rope_base, 1.0 / math.sqrt(w.head_dim), window=window)
 
 
+def check_u8_lse(got, ref, case, paged=False, window=0, what=None):
+    """lse against the model over the dequantised keys the kernel reads."""
+    kd = oracle.dequantize_u8(ref["k_codes"], ref["k_sz"][..., 0], ref["k_sz"][..., 1])
+    ks = np.asarray(ref["k_sz"][..., :1], np.float64)
+    if paged:
+        kd = paged_keys(kd, case.block_table, case.seq_lens, case.page_size)
+        ks = paged_keys(ks, case.block_table, case.seq_lens, case.page_size)
+    d = case.q_new.shape[-1]
+    assert_lse(got["lse"], ref["q_rot"], kd, case.seq_lens, 1.0 / math.sqrt(d), "f16", window=window, what=what,
+               key_scales=ks[..., 0])
+
+
 def check_u8_append(got, ref):
     """Codes and (scale, zero) pairs equal the oracle's everywhere: the appended
     rows bit for bit, every other row untouched."""
@@ -108,6 +124,7 @@ def test_u8_contiguous_matches_oracle(m, shape, splits):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    check_u8_lse(got, ref, c)
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
     check_u8_append(got, ref)
 
@@ -128,6 +145,7 @@ def test_u8_paged_matches_oracle(m, page_size, heads):
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, splits
         assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+        check_u8_lse(got, ref, pc, paged=True, what=splits)
         check_u8_append(got, ref)
 
 
@@ -239,6 +257,7 @@ def test_u8_mqa_matches_oracle(m, shape, splits):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
+    check_u8_lse(got, ref, c)
     check_u8_append(got, ref)
 
 

@@ -5,15 +5,20 @@ framework already holds the device memory, or a loop that must not take
 cudaMalloc's device synchronisation); this entry point keeps its split
 scratch in a fixed array inside the library. The test calls it through the
 C ABI twice in a row and checks each result against gqa_decode_attention
-with a caller-allocated workspace. This file is collected last.
+with a caller-allocated workspace, and the first one also directly against
+the fp64 oracle (outputs <= 2e-2, lse <= 1e-4 of the log-sum-exp over the
+scores the kernel forms). This file is collected last.
 """
 
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
+from lse_model import assert_lse, paged_keys
 from mqa_decode_attention_gb300 import _abi
 from synthetic import make_contiguous_case, make_paged_case, workload
 
@@ -51,6 +56,22 @@ def _case(paged: bool, seed: int):
     return w, c, lay, q_rot
 
 
+def _oracle(w, c, paged, q_rot, scale):
+    """Attention of the given q_rot over each sequence's logical cache (fp64)."""
+    lens = c.seq_lens.cpu().numpy()
+    if paged:
+        keys = paged_keys(c.k_pool.cpu().double().numpy(), c.block_table.cpu(), lens, c.page_size)
+        vals = paged_keys(c.v_pool.cpu().double().numpy(), c.block_table.cpu(), lens, c.page_size)
+    else:
+        keys, vals = c.k_cache.cpu().double().numpy(), c.v_cache.cpu().double().numpy()
+    q = q_rot.cpu().double().numpy()
+    out = np.empty(q.shape)
+    lse = np.empty(q.shape[:2])
+    for b, L in enumerate(lens):
+        out[b], lse[b] = oracle.gqa_attention(q[b], keys[b, :, :L], vals[b, :, :L], scale)
+    return out, lse, keys
+
+
 @pytest.mark.parametrize("paged", [False, True])
 @pytest.mark.parametrize("variant", [1, 2])
 def test_noalloc_matches_workspace_call(lib, paged, variant):
@@ -81,6 +102,12 @@ def test_noalloc_matches_workspace_call(lib, paged, variant):
         assert torch.isfinite(got.float()).all()
         assert (got.float() - ref.float()).abs().max().item() <= TOL
         assert (got_lse - ref_lse).abs().max().item() <= TOL
+        if call == 0:
+            o, l, keys = _oracle(w, c, paged, qr, scale)
+            assert np.max(np.abs(got.double().cpu().numpy() - o)) <= TOL
+            assert np.max(np.abs(got_lse.double().cpu().numpy() - l)) <= TOL
+            assert_lse(got_lse.double().cpu().numpy(), qr.double().cpu().numpy(), keys, c.seq_lens.cpu().numpy(),
+                       scale, "bf16" if variant == 2 else "f32")
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(lib):
