@@ -288,53 +288,237 @@ def unit_inputs(w, case, units):
     return out
 
 
+def numpy_units(w, units, out_esize, cache: str, n_new: int, window: int):
+    """The units as numpy arrays for oracle.cores: bf16 values as their 16-bit
+    patterns (fp32 values as float32), byte caches as stored, and each unit's
+    algorithmic bytes."""
+    import numpy as np
+
+    span = (window + n_new - 1) if window else 1 << 30
+    out = []
+    for u in units:
+        v = {"L": np.array(u["L"]), "n": np.array(u["n"]),
+             "bytes": np.array(unit_bytes(w, min(u["L"], span), out_esize, cache, n_new))}
+        for key, t in u.items():
+            if not isinstance(t, torch.Tensor):
+                continue
+            if t.dtype == torch.bfloat16:
+                v[key] = t.contiguous().view(torch.int16).numpy().view(np.uint16)
+            elif t.dtype == torch.float32:
+                v[key] = t.numpy()
+            else:
+                v[key] = t.numpy()
+        out.append(v)
+    return out
+
+
+def oracle_meta(w, window: int) -> dict:
+    return {"scale": 1.0 / math.sqrt(w.head_dim), "rope_base": w.rope_base, "window": window, "dtype": w.dtype,
+            "bf16_bits": w.dtype == "bf16"}
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_baseline(w, units, out_esize, cache: str, n_new: int, window: int, seconds: float, runs: int = 3):
+    """The oracle's decode step timed on the host cores over a sample of units:
+    single-threaded in this process and on every core (one process per core,
+    oracle.cores), each the median of `runs` runs of about `seconds` seconds.
+    Returns (single, all_cores, outputs of the distinct units)."""
+    import subprocess
+    import tempfile
+
+    from oracle import cores  # test infrastructure: the CPU-baseline leg only
+
+    nu = numpy_units(w, units, out_esize, cache, n_new, window)
+    meta = oracle_meta(w, window)
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "units.npz")
+        cores.save_units(path, nu, meta)
+        loaded, _ = cores.load_units(path)
+        outs = [cores.run_unit(u, meta) for u in loaded]  # also the warm-up
+        single = []
+        for _ in range(runs):
+            nb, nd, secs = cores.run_for(loaded, meta, seconds)
+            single.append({"bytes": nb, "units": nd, "wall_s": secs})
+        del loaded
+        procs = host_cores()
+        r = subprocess.run([sys.executable, "-m", "oracle.cores", path, "--seconds", str(seconds), "--runs",
+                            str(runs), "--procs", str(procs)], cwd=ROOT, capture_output=True, text=True,
+                           timeout=600)
+        if r.returncode != 0:
+            raise RuntimeError("oracle.cores failed: " + r.stderr[-2000:])
+        multi = json.loads(r.stdout.strip().splitlines()[-1])
+
+    def med(rs):
+        rates = sorted(x["bytes"] / x["wall_s"] / 1e9 for x in rs)
+        return rates[len(rates) // 2], rates
+
+    s_med, s_all = med(single)
+    m_med, m_all = med(multi["runs"])
+    return ({"value": s_med, "runs_gbs": s_all, "cores": 1, "seconds_per_run": seconds},
+            {"value": m_med, "runs_gbs": m_all, "cores": multi["procs"], "seconds_per_run": seconds}, outs)
+
+
 def unit_bytes(w, L, out_esize, cache: str = "native", n_new: int = 1):
     es = w.esize
     return (2 * L * row_bytes(w, cache) + n_new * w.group * w.head_dim * (es + out_esize)
             + 2 * n_new * (w.head_dim * es + row_bytes(w, cache)))
 
 
-def oracle_unit(w, u, window: int = 0):
-    """The oracle's decode step for one (sequence, kv head) unit: its output rows."""
-    import oracle  # test infrastructure: the CPU-baseline and reference legs only
-
-    scale = 1.0 / math.sqrt(w.head_dim)
-    if "K8" in u:
-        r = oracle.decode_step_e5m2(u["K8"][None, None].numpy(), u["V8"][None, None].numpy(), u["q"][None],
-                                    u["k"][None, None], u["v"][None, None], [u["L"]], w.rope_base, scale,
-                                    window=window)
-        return r["out"][0]
-    if "Kc" in u:
-        L = u["L"]
-        r = oracle.decode_step_u8(u["Kc"][None, None], u["Ks"][None, None], u["Vc"][None, None], u["Vs"][None, None],
-                                  u["q"][None], u["k"][None, None], u["v"][None, None], [L], w.rope_base, scale,
-                                  window=window)
-        return r["out"][0]
-    if u["n"] > 1:
-        r = oracle.decode_step_multi(u["K"][None, None], u["V"][None, None], u["q"][None], u["k"][None, :, None],
-                                     u["v"][None, :, None], [u["L"]], w.rope_base, scale, w.dtype, window=window)
-        return r["out"][0]
-    o, _, _ = oracle.decode_unit(u["q"], u["k"], u["v"], u["K"], u["V"], u["L"], w.rope_base, scale, w.dtype,
-                                 window=window)
-    return o
+# ------------------------------------------------ every workload, L2-controlled
+SWEEP = ["gqa4k", "mqa8k", "paged", "long"]
 
 
-def run_oracle_units(w, inputs, budget_s: float, min_units: int = 2, window: int = 0):
-    """Time the oracle's decode step over the units, cycling through them,
-    until the budget is spent. Returns the first result of each unit and the totals."""
-    results = {}
-    done = 0
-    t0 = time.perf_counter()
-    i = 0
+def percentiles(xs):
+    xs = sorted(xs)
+    q = statistics.quantiles(xs, n=10, method="inclusive")
+    return {"median": round(statistics.median(xs), 6), "p10": round(q[0], 6), "p90": round(q[-1], 6)}
+
+
+def layout_for(m, w, case, window: int = 0):
+    if w.paged:
+        return m.layout_paged(case.k_pool, case.v_pool, case.block_table, w.h_q, window=window)
+    return m.layout_contiguous(case.k_cache, case.v_cache, w.h_q, window=window)
+
+
+def measure_workload(m, name, dev, stream, n_timed, n_warm, flush, sampler, l2_bytes, peak):
+    """One workload's decode step (mqa_decode_step: RoPE, append, attention,
+    the combine when it splits) at its own split count, two ways:
+    isolated -- each step preceded by an L2 flush (a read of a buffer twice
+    the L2 size), CUDA events around the step alone: median, p10, p90;
+    back to back -- steps one after another over enough identical copies of
+    the cache that at least 4x the L2 size streams between two reads of the
+    same copy. Returns the entry for the bench line."""
+    w = workload(name)
+    lens = None
+    copies = []
+    one = None
     while True:
-        u = inputs[i % len(inputs)]
-        o = oracle_unit(w, u, window)
-        results.setdefault(i % len(inputs), (u, o))
-        done += 1
-        i += 1
-        if done >= min_units and time.perf_counter() - t0 > budget_s:
+        case = build_case(w, dev)
+        lay = layout_for(m, w, case)
+        lens = case.seq_lens.cpu()
+        max_len = int(lens.max())
+        bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=w.num_splits, device=dev)
+        copies.append((case, lay, bufs))
+        if one is None:
+            one = step_bytes(w, lens, bufs.out.element_size())
+        if len(copies) * one >= 4 * l2_bytes:
             break
-    return list(results.values()), done, time.perf_counter() - t0
+    scale = 1.0 / math.sqrt(w.head_dim)
+    splits = w.num_splits if w.num_splits > 0 else m.choose_splits(copies[0][1], max_len, 0, 1)
+
+    def step(i):
+        case, lay, bufs = copies[i % len(copies)]
+        m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs, w.rope_base,
+                      scale, w.num_splits, 0, stream)
+
+    for i in range(n_warm):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
+    for i in range(n_timed):
+        flush()
+        e0[i].record(stream)
+        step(i)
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    iso = [e0[i].elapsed_time(e1[i]) for i in range(n_timed)]
+    # back to back for at least half a second, so that the clock sampler sees this workload
+    n_b2b = max(n_timed, int(0.5e3 / statistics.median(iso)))
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for i in range(n_b2b):
+        step(i)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    b2b = b0.elapsed_time(b1) / n_b2b
+    for _, _, bufs in copies:
+        err = int(bufs.err.item())
+        if err != 0:
+            raise RuntimeError(f"{name}: device error word {err:#x}")
+    pc = percentiles(iso)
+    gbs = one / (pc["median"] * 1e-3) / 1e9
+    traffic = ncu_traffic(name)
+    entry = {
+        "shape": (f"batch {w.batch}, H_q {w.h_q}, H_kv {w.h_kv}, head_dim {w.head_dim}, "
+                  + (f"{w.page_size}-token pages, lengths U[{w.len_lo},{w.len_hi}]" if w.paged
+                     else f"{w.seq_len} tokens/seq")),
+        "num_splits": splits,
+        "bytes_per_step": one,
+        "ms_per_step": pc,
+        "gbs": round(gbs, 2),
+        "frac_of_measured": round(gbs / peak, 4),
+        "frac_of_8000": round(gbs / 8000.0, 4),
+        "back_to_back": {"ms_per_step": round(b2b, 6), "gbs": round(one / (b2b * 1e-3) / 1e9, 2),
+                         "frac_of_measured": round(one / (b2b * 1e-3) / 1e9 / peak, 4),
+                         "cache_copies": len(copies), "steps": n_b2b},
+        "ncu_traffic_ratio": round(traffic / one, 4) if traffic else None,
+        "steps": n_timed,
+        "clocks": sampler.summary(t0, t1),
+        "l2": (f"isolated: L2 flushed before each step (read of {2 * l2_bytes / 1e6:.0f} MB); back to back: "
+               f"{len(copies)} cache cop{'y' if len(copies) == 1 else 'ies'}, {len(copies) * one / 1e6:.0f} MB "
+               f"streamed between reads of a copy ({l2_bytes / 1e6:.0f} MB L2)"),
+    }
+    del copies
+    torch.cuda.empty_cache()
+    return entry
+
+
+def measure_workloads(m, dev, stream, n_timed, sampler, peak):
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
+    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.sum()
+
+    out = {}
+    for name in SWEEP:
+        out[name] = measure_workload(m, name, dev, stream, n_timed, 10, flush, sampler, l2, peak)
+    del flush_buf
+    torch.cuda.empty_cache()
+    return out
+
+
+def tiny_parity(m, dev):
+    """The tiny workload (fp32, batch 1, 4 / 2 heads, head_dim 64, a 5-token
+    prompt then decoding until 16 attention evaluations) token by token
+    through the library, against the oracle's cached sequence."""
+    import numpy as np
+
+    import oracle  # test infrastructure: the CPU-baseline leg only
+    from synthetic import make_tiny_sequence
+
+    w = workload("tiny")
+    seq = make_tiny_sequence(w)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    n = seq.prompt_len + seq.decode_evals - 1
+    ref, _, _, _ = oracle.run_cached_sequence(seq.q, seq.k, seq.v, seq.prompt_len, seq.decode_evals, w.rope_base,
+                                              scale, "f32")
+    kc = torch.zeros(w.batch, w.h_kv, n, w.head_dim, dtype=torch.float32, device=dev)
+    vc = torch.zeros_like(kc)
+    lay = m.layout_contiguous(kc, vc, w.h_q)
+    bufs = m.DecodeBuffers.allocate(lay, n, num_splits=1, variant=1, device=dev)
+    outs = []
+    for p in range(n):
+        lens = torch.full((w.batch,), p + 1, dtype=torch.int32, device=dev)
+        m.decode_step(lay, seq.q[p].to(dev), seq.k[p].to(dev), seq.v[p].to(dev), lens - 1, lens, p + 1, bufs,
+                      w.rope_base, scale, num_splits=1, variant=1)
+        if p >= seq.prompt_len - 1:
+            outs.append(bufs.out.double().cpu().numpy())
+    torch.cuda.synchronize()
+    if int(bufs.err.item()) != 0:
+        raise RuntimeError("tiny: device error word")
+    err = float(np.max(np.abs(np.stack(outs) - ref)))
+    return {"shape": "batch 1, H_q 4, H_kv 2, head_dim 64, fp32, prompt 5 then 16 attention evaluations",
+            "max_abs_err": err, "tolerance": 1e-4, "path": "CUDA-core kernel, fp32 cache and output"}
 
 
 # --------------------------------------------------------------- our arm
@@ -394,7 +578,8 @@ def bench_ours(args):
     if do_cpu:
         g = torch.Generator().manual_seed(w.seed)
         perm = torch.randperm(w.batch * w.h_kv, generator=g).tolist()
-        units = unit_inputs(w, case, [(u // w.h_kv, u % w.h_kv) for u in perm[:args.cpu_units or len(perm)]])
+        n_units = args.cpu_units or min(len(perm), max(2 * host_cores(), 16))
+        units = unit_inputs(w, case, [(u // w.h_kv, u % w.h_kv) for u in perm[:n_units]])
 
     def append():
         m.kv_append_rope_multi(lay, nn, case.q_new, case.k_new, case.v_new, case.pos, w.rope_base, bufs.q_rot,
@@ -473,7 +658,6 @@ def bench_ours(args):
         step()
         ev_e[i].record(stream)
     torch.cuda.synchronize()
-    sampler.stop()
     step_call_ms = statistics.fmean(ev_s[i].elapsed_time(ev_e[i]) for i in range(K))
     # the standalone calls, for reference (not part of the step)
     n_alone = min(K, 500)
@@ -586,6 +770,10 @@ def bench_ours(args):
     bufs.out = dev_out
 
     peak, peak_src = measured_peak()
+    sweep = (world == 1 and args.workload == DEFAULT_WORKLOAD and args.cache == "native" and nn == 1
+             and args.window == 0 and args.variant == 0 and not args.no_workloads)
+    workloads = measure_workloads(m, dev, stream, max(50, K), sampler, peak) if sweep else None
+    sampler.stop()
     if byte:
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
         # one new token and 32 query heads per kv head on tcgen05: uint8 with
@@ -688,25 +876,37 @@ def bench_ours(args):
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
     }
+    if workloads is not None:
+        line["workloads"] = workloads
 
     if do_cpu:
-        results, n_done, secs = run_oracle_units(w, units, args.cpu_seconds, window=args.window)
-        by_unit = {(u["b"], u["j"]): u for u, _ in results}
-        span = (args.window + nn - 1) if args.window else 1 << 30
-        done = sum(unit_bytes(w, min(units[i % len(units)]["L"], span), out_es, args.cache, nn) for i in range(n_done))
+        single, multi, outs = oracle_baseline(w, units, out_es, args.cache, nn, args.window, args.cpu_seconds)
         out_host = bufs.out.float().cpu().numpy()
         G = w.group
         if nn > 1:
-            errs = [float(np.max(np.abs(out_host[u["b"], :, u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
+            errs = [float(np.max(np.abs(out_host[u["b"], :, u["j"] * G:(u["j"] + 1) * G] - o)))
+                    for u, o in zip(units, outs)]
         else:
-            errs = [float(np.max(np.abs(out_host[u["b"], u["j"] * G:(u["j"] + 1) * G] - o))) for u, o in results]
+            errs = [float(np.max(np.abs(out_host[u["b"], u["j"] * G:(u["j"] + 1) * G] - o)))
+                    for u, o in zip(units, outs)]
+        per_unit_ms = 1e3 * statistics.fmean(unit_bytes(w, u["L"], out_es, args.cache, nn) for u in units) / (
+            multi["value"] * 1e9)
         line["cpu_baseline"] = {
-            "value": round(done / secs / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n_done} (sequence, kv head) units of the step ({len(by_unit)} distinct of "
-                      f"{w.batch * w.h_kv}), fp64 numpy, single thread, {secs:.1f} s",
-            "ms_per_step_extrapolated": round(secs / n_done * w.batch * w.h_kv * 1e3, 1),
+            "value": round(multi["value"], 6), "unit": UNIT, "cores": multi["cores"], "kind": "oracle",
+            "sample": f"{len(units)} distinct (sequence, kv head) units of the step (of {w.batch * w.h_kv}), "
+                      f"fp64 numpy, one single-threaded process per host core cycling over its share of them; "
+                      f"median of {len(multi['runs_gbs'])} runs of {args.cpu_seconds:.1f} s",
+            "runs_gbs": [round(x, 6) for x in multi["runs_gbs"]],
+            "single_thread": {"value": round(single["value"], 6), "unit": UNIT, "cores": 1,
+                              "runs_gbs": [round(x, 6) for x in single["runs_gbs"]],
+                              "sample": f"the same units in one thread, median of {len(single['runs_gbs'])} runs "
+                                        f"of {args.cpu_seconds:.1f} s"},
+            "ms_per_step_extrapolated": round(sbytes / (multi["value"] * 1e9) * 1e3, 1),
+            "ms_per_unit_all_cores": round(per_unit_ms, 3),
         }
-        line["parity_sample"] = {"units": len(results), "max_abs_err": max(errs), "tolerance": 2e-2}
+        line["parity_sample"] = {"units": len(units), "max_abs_err": max(errs), "tolerance": 2e-2}
+        if workloads is not None:
+            line["workloads"]["tiny"] = tiny_parity(m, dev)
 
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -811,6 +1011,8 @@ def bench_prefill(args):
 
 # ---------------------------------------------------------- reference arm
 def bench_reference(args):
+    from oracle import cores  # test infrastructure: the reference (oracle) arm only
+
     world, rank, _ = dist_env()
     if rank != 0:
         return
@@ -820,18 +1022,15 @@ def bench_reference(args):
     n_units = w.batch * w.h_kv
     order = [(u // w.h_kv, u % w.h_kv) for u in range(n_units)]
     out_es = 4 if w.dtype == "f32" else 2
-
-    def one(i):
-        u = unit_inputs(w, case, [order[i % n_units]])
-        return u
-
-    inputs = [one(i)[0] for i in range(min(n_units, args.warmup + args.steps))]
+    meta = oracle_meta(w, args.window)
+    picked = order[:min(n_units, args.warmup + args.steps)]
+    inputs = [cores.widen(u, meta) for u in numpy_units(w, unit_inputs(w, case, picked), out_es, args.cache,
+                                                        args.n_new, args.window)]
 
     def run(i):
         u = inputs[i % len(inputs)]
-        oracle_unit(w, u, args.window)
-        span = (args.window + args.n_new - 1) if args.window else 1 << 30
-        return unit_bytes(w, min(u["L"], span), out_es, args.cache, args.n_new)
+        cores.run_unit(u, meta)
+        return int(u["bytes"])
 
     for i in range(args.warmup):
         run(i)
@@ -868,6 +1067,8 @@ def main():
     ap.add_argument("--splits", type=int, default=None, help="override the workload's split count (0 = auto)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the L2-controlled pass over every workload (the default bench line carries it)")
     ap.add_argument("--warm-seconds", type=float, default=1.0,
                     help="minimum warm-up time, so the clock sampler sees the load (0 for profiler runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (smaller profiling cases)")
@@ -878,7 +1079,7 @@ def main():
                     help="new tokens per sequence (the verification pass of speculative decoding)")
     ap.add_argument("--cache", choices=["native", "u8", "fp8"], default="native",
                     help="cache type: the workload's own (bf16 / fp32) or uint8 codes with per-row scale / zero point")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=3.0, help="seconds per oracle timing run (3 runs each)")
     ap.add_argument("--cpu-units", type=int, default=0, help="distinct units in the CPU sample (0 = all)")
     args = ap.parse_args()
     if args.warmup < 3:
