@@ -130,6 +130,19 @@ typedef enum mqa_variant {
  * it. q_new, k_new and v_new are bf16; attention on tensor cores only, one
  * new token per sequence.
  *
+ * Bounded waits: inside the attention kernels every wait for another warp's
+ * progress (a tile landing, a tile freed, a product done) gives up after
+ * wait_limit_ns nanoseconds (0 selects the default, one second). The kernel
+ * then ORs MQA_DEVERR_TIMEOUT into err_word, lets its own copies and tensor
+ * core products still in flight complete (those waits keep the one-second
+ * limit), releases what it holds and returns; its outputs are then invalid,
+ * and the next call on the stream runs normally. A healthy wait lasts
+ * microseconds: a short limit only serves to exercise this path (below one
+ * second the waits poll instead of letting the hardware suspend the warp,
+ * which could outlast the limit). (The
+ * one-token MQA kernels over a one-byte cache -- 16 < G <= 32 over MQA_U8
+ * or MQA_FP8_E5M2, contiguous, head_dim 128 -- always use one second.)
+ *
  * window: 0 = the attention reads every cached token [0, L); W > 0 = a
  * sliding window: only the last W tokens [max(0, L - W), L) are read
  * ("KV Cache 최적화 심층 분석", SlidingWindowAttention keeps the cache's last
@@ -153,6 +166,7 @@ typedef struct mqa_kv_layout {
   const int32_t* block_table;
   void* k_scale_zero; /* MQA_U8 only: float32 (scale, zero_point) per cached row of K */
   void* v_scale_zero; /* MQA_U8 only: same for V */
+  uint64_t wait_limit_ns; /* 0: 1 s; see "Bounded waits" above */
 } mqa_kv_layout;
 
 /*

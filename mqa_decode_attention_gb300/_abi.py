@@ -55,6 +55,7 @@ class KVLayout(ctypes.Structure):
         ("block_table", c_vp),
         ("k_scale_zero", c_vp),
         ("v_scale_zero", c_vp),
+        ("wait_limit_ns", ctypes.c_uint64),
     ]
 
 

@@ -30,6 +30,10 @@ mqa_status fail_cuda(cudaError_t e) {
   return MQA_ERR_CUDA;
 }
 
+unsigned long long wait_limit(const mqa_kv_layout* L) {
+  return L->wait_limit_ns > 0 ? static_cast<unsigned long long>(L->wait_limit_ns) : kWaitLimitNs;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool is_pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -513,6 +517,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
   p.head_blocks = head_blocks(layout, ks, n_new);
   p.window = layout->window;
   p.early = early;
+  p.wait_ns = wait_limit(layout);
   // (one-byte caches and several new tokens: only in the fused step;
   // otherwise q_rot comes from the append launch)
   if (rope != nullptr && v == MQA_VARIANT_TENSOR_CORE &&
@@ -568,6 +573,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     t.lse_part = p.lse_part;
     t.err = err_word;
     t.early = early;
+    t.wait_ns = p.wait_ns;
     if (rope != nullptr && rope->fuse_append && n_new == 1) {
       t.fuse = 1;
       t.early = 0;  // nothing of this step precedes the launch
@@ -624,6 +630,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     t.lse_part = p.lse_part;
     t.err = err_word;
     t.early = early;
+    t.wait_ns = p.wait_ns;
     if (rope != nullptr && rope->fuse_append) {
       // one launch: the kernel rotates q_new and encodes the new row itself
       t.fuse = 1;
@@ -741,6 +748,7 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
   p.lse_out = lse_out;
   p.err = err_word;
   p.early = early;
+  p.wait_ns = wait_limit(layout);
   CUtensorMap tk, tv;
   if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
       !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool waited = !p.early, appended = !writer;
       for (; it < T; ++it) {
         const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1)) {
+        if (it >= kStages && !mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1, p.wait_ns)) {
           fail(1);
           break;
         }
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           waited = true;
         }
         if (!appended && apos < kstart + (it + 1) * kBN) {  // ... written by this block's softmax warps
-          if (!mbar_wait(bar(kAppended), 0)) {
+          if (!mbar_wait(bar(kAppended), 0, p.wait_ns)) {
             fail(1);
             break;
           }
@@ -346,6 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issue(it);
       }
+      // every tile this warp issued (it of them) lands before the block can
+      // exit: after a timeout nothing else may wait for them
+      for (int k = it > kStages ? it - kStages : 0; k < it; ++k)
+        (void)mbar_wait(bar(full + k % kStages), (k / kStages) & 1, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 6) {
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = tc05::idesc_bf16_f32(kBM, kBN, false, false);
       const uint32_t id_o = tc05::idesc_bf16_f32(kBM, kD, false, true);
       const uint32_t q_s = sbase + kQOff;
-      bool ok = mbar_wait(bar(kQReady), 0);
+      bool ok = mbar_wait(bar(kQReady), 0, p.wait_ns);
       // S of tile it into buffer it % kSBuf. That buffer last held P of tile
       // it - kSBuf, whose PV was issued before: MMAs of this thread execute in order.
       auto issue_s = [&](int it) {
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (progress) {
           t_idle = global_timer_ns();
-        } else if (stop() || global_timer_ns() - t_idle > kWaitLimitNs) {
+        } else if (stop() || global_timer_ns() - t_idle > p.wait_ns) {
           ok = false;
         } else {
           __nanosleep(32);  // leave the issue slots to the softmax warp sharing this scheduler
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = 0; it < T; ++it) {
       const int sb = it % kSBuf;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + sb), (it / kSBuf) & 1) && !stop());
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + sb), (it / kSBuf) & 1, p.wait_ns) && !stop());
       if (!ok) break;
       tc05::fence_after_sync();
       float s[kKW];
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // new token's, being written by another block of a fused step. P = 0
         // there, and 0 * NaN would still poison O: zero the V row of this
         // thread's key once that tile has landed
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + it % kStages), (it / kStages) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + it % kStages), (it / kStages) & 1, p.wait_ns));
         if (!ok) break;
         if (key0 + r >= t_end) {
           unsigned char* vrow = smem + kVOff + (it % kStages) * kTileBytes + r * 128;
@@ -563,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = grow ? mt : m_ref;
       if (it > 0 && __any_sync(0xffffffffu, grow && m_ref != -INFINITY)) {
         // O is rescaled: PV of the previous tile must be done first
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + (it - 1) % kSBuf), ((it - 1) / kSBuf) & 1) && !stop());
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(kODone + (it - 1) % kSBuf), ((it - 1) / kSBuf) & 1, p.wait_ns) && !stop());
         if (!ok) break;
         tc05::fence_after_sync();
         const float alpha = (grow && m_ref != -INFINITY) ? fast_exp2(m_ref - m_new) : 1.f;
@@ -633,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kPFull + sb));
     }
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + (T - 1) % kSBuf), ((T - 1) / kSBuf) & 1));
+    if (ok && T > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kODone + (T - 1) % kSBuf), ((T - 1) / kSBuf) & 1, p.wait_ns));
     if (!ok && lane == 0) fail(1);
     if (ok) tc05::fence_after_sync();
     {
@@ -768,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the columns are released
       if (lane == 0) {
         tc05::commit(bar(kDrain));
-        (void)mbar_wait(bar(kDrain), 0);
+        (void)mbar_wait(bar(kDrain), 0, kWaitLimitNs);
       }
       __syncwarp();
     }

@@ -121,20 +121,6 @@ __device__ __forceinline__ bool aborted(const Tc05Params& p) {
   return (*reinterpret_cast<volatile int32_t*>(p.err) & static_cast<int>(MQA_DEVERR_TIMEOUT)) != 0;
 }
 
-// Barrier over `count` threads that returns whether `pred` held on any of them.
-__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 // Butterfly over the warp: on return v[0] of lane h is op over the 32 lanes of
 // the values they held for head h (the other entries are spent).
 template <bool MAX>

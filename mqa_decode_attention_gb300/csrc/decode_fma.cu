@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
-        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
+        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1, p.wait_ns)) {
           if (lane == 0) {
             s_abort = 1;
             atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -223,11 +223,10 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
       __syncwarp();
       issued = it + 1;
     }
-    // On an abort, let the copies already in flight land before the block exits.
-    if (*reinterpret_cast<volatile int*>(&s_abort)) {
-      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
-    }
+    // every copy this warp issued lands before the block can exit: after a
+    // timeout the consumers may have stopped waiting for them
+    for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+      (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, kWaitLimitNs);
     return;
   }
 
@@ -259,7 +258,7 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
   bool ok = true;
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it % STAGES;
-    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
+    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1, p.wait_ns)) {
       if (lane == 0) {
         s_abort = 1;
         atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -340,8 +339,9 @@ __global__ void __launch_bounds__(FmaCfg<T, D, HBLK, STAGES>::kThreads)
   }
 
   // ----------------------------------------------- merge the token groups
-  named_bar_sync(1, C::kConsumerThreads);
-  if (*reinterpret_cast<volatile int*>(&s_abort) || !ok) return;
+  // one decision for every consumer warp (the producer may time out and set
+  // s_abort at any moment); the barrier also ends their reads of the stages
+  if (bar_any(2, C::kConsumerThreads, *reinterpret_cast<volatile int*>(&s_abort) || !ok)) return;
   float* mo = reinterpret_cast<float*>(smem);                       // [groups][HBLK][stride]
   float* mm = mo + C::kGroups * HBLK * C::kMergeStride;             // [groups][HBLK]
   float* ml = mm + C::kGroups * HBLK;                               // [groups][HBLK]

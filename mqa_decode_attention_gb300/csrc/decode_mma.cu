@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
-        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
+        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1, p.wait_ns)) {
           if (lane == 0) {
             s_abort = 1;
             atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -255,10 +255,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
       issued = it + 1;
     }
     if (!appended) named_bar_sync(3, 64);  // pair the append warp's arrival
-    if (*reinterpret_cast<volatile int*>(&s_abort)) {
-      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
-    }
+    // every copy this warp issued lands before the block can exit: after a
+    // timeout the consumers may have stopped waiting for them
+    for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+      (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, kWaitLimitNs);
     return;
   }
 
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
   const int lg_rpb = 31 - __clz(rpb);
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it % STAGES;
-    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
+    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1, p.wait_ns)) {
       if (lane == 0) {
         s_abort = 1;
         atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -367,8 +367,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, STAGES>::kThreads, MmaCfg<D, HB,
   }
   wa.finish_sums();
   // ------------------------------------------- merge the 4 token slices
-  named_bar_sync(1, C::kConsumerThreads);
-  if (*reinterpret_cast<volatile int*>(&s_abort) || !ok) return;
+  // one decision for every consumer warp (the producer may time out and set
+  // s_abort at any moment); the barrier also ends their reads of the stages
+  if (bar_any(4, C::kConsumerThreads, *reinterpret_cast<volatile int*>(&s_abort) || !ok)) return;
   float* mo = reinterpret_cast<float*>(smem);            // [warps][16][stride]
   float* mm = mo + C::kConsumerWarps * 16 * C::kMergeStride;  // [warps][16]
   float* ml = mm + C::kConsumerWarps * 16;                     // [warps][16]

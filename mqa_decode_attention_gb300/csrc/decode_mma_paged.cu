@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
         written = true;
       }
       if (it >= STAGES) {
-        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
+        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1, p.wait_ns)) {
           if (lane == 0) {
             s_abort = 1;
             atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -161,10 +161,10 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
       issued = it + 1;
     }
     if (!written) ar.write(p, apos, lane);  // rows this block never reads
-    if (*reinterpret_cast<volatile int*>(&s_abort)) {
-      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
-    }
+    // every copy this warp issued lands before the block can exit: after a
+    // timeout the consumers may have stopped waiting for them
+    for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+      (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, kWaitLimitNs);
     return;
   }
 
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(HeadsCfg<HG, STAGES>::kThreads)
   bool ok = true;
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it % STAGES;
-    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
+    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1, p.wait_ns)) {
       if (lane == 0) {
         s_abort = 1;
         atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));

@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
     for (int it = 0; it < n_tiles; ++it) {
       const int stage = it % STAGES;
       if (it >= STAGES) {
-        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
+        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1, p.wait_ns)) {
           if (lane == 0) {
             s_abort = 1;
             atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -605,11 +605,10 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
       issued = it + 1;
     }
     if (!appended) named_bar_sync(3, 64);  // pair the append warp's arrival
-    if (*reinterpret_cast<volatile int*>(&s_abort)) {
-      // let the copies in flight land before the block exits
-      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
-    }
+    // every copy this warp issued lands before the block can exit: after a
+    // timeout the consumers may have stopped waiting for them
+    for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+      (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, kWaitLimitNs);
     return;
   }
 
@@ -639,7 +638,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   bool ok = true;
   for (int it = ws >> 1; it < n_tiles; it += 2) {
     const int stage = it % STAGES;
-    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
+    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1, p.wait_ns)) {
       if (lane == 0) {
         s_abort = 1;
         atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -661,8 +660,9 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
     atomicOr(p.err, static_cast<int>(MQA_DEVERR_U8_SCALE));
 
   // ------------------------------------------- merge the 4 token slices
-  named_bar_sync(1, C::kConsumerThreads);
-  if (*reinterpret_cast<volatile int*>(&s_abort) || !ok) return;
+  // one decision for every consumer warp (the producer may time out and set
+  // s_abort at any moment); the barrier also ends their reads of the stages
+  if (bar_any(4, C::kConsumerThreads, *reinterpret_cast<volatile int*>(&s_abort) || !ok)) return;
   float* mo = reinterpret_cast<float*>(smem);  // [warp][16][kMergeStride], columns in fragment order
   float* mm = mo + C::kConsumerWarps * 16 * C::kMergeStride;
   float* ml = mm + C::kConsumerWarps * 16;
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
       const int stage = it % STAGES;
       if (!appended && it == STAGES) append();
       if (it >= STAGES) {
-        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1)) {
+        if (!mbar_wait(smem_u32(&empty[stage]), ((it / STAGES) + 1) & 1, p.wait_ns)) {
           if (lane == 0) {
             s_abort = 1;
             atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));
@@ -918,10 +918,10 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
       issued = it + 1;
     }
     if (!appended) append();  // rows this block never reads
-    if (*reinterpret_cast<volatile int*>(&s_abort)) {
-      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1);
-    }
+    // every copy this warp issued lands before the block can exit: after a
+    // timeout the consumers may have stopped waiting for them
+    for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+      (void)mbar_wait(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, kWaitLimitNs);
     return;
   }
 
@@ -944,7 +944,7 @@ __global__ void __launch_bounds__(U8HeadsCfg<D, HG, PS, STAGES, F8>::kThreads, H
   bool ok = true;
   for (int it = 0; it < n_steps; ++it) {
     const int stage = it % STAGES;
-    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1)) {
+    if (!mbar_wait(smem_u32(&full[stage]), (it / STAGES) & 1, p.wait_ns)) {
       if (lane == 0) {
         s_abort = 1;
         atomicOr(p.err, static_cast<int>(MQA_DEVERR_TIMEOUT));

@@ -7,6 +7,13 @@
 
 namespace mqa {
 
+// A spin on an mbarrier gives up after a limit (the kernel then sets
+// MQA_DEVERR_TIMEOUT and winds down). The limit of the waits for progress is
+// a launch parameter (the layout's wait_limit_ns, by default this constant);
+// the waits that let a kernel's own copies and MMAs in flight land before it
+// exits always use this constant. A healthy wait lasts microseconds.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
 // Records `e` as the calling thread's last CUDA error (the text
 // mqa_last_cuda_error returns).
 void record_cuda_error(cudaError_t e);
@@ -57,6 +64,7 @@ struct DecodeParams {
   int head_blocks;   // blocks of query heads a (sequence, kv head) is cut into
   int window;        // 0: all tokens; W > 0: only tokens [max(0, L - W), L)
   int early;         // 1: the preceding launch is the append kernel; stream K/V before waiting for it
+  unsigned long long wait_ns;  // limit of the waits for progress (the drains use kWaitLimitNs)
   int merged_halves; // tensor-core path: one TMA box carries both 64-column halves of a row block
   int rope_q;        // 1: rotate q_new (bf16) in the kernel instead of reading q_rot (fused step)
   int fuse_append;   // 1: the kernel also performs the append of the new token (single-launch step)
@@ -97,6 +105,7 @@ struct Tc05Params {
   float* lse_part;  // [B, n_new, H_q, num_splits]
   int32_t* err;
   int early;  // 1: the preceding launch is the append kernel; stream K/V before waiting for it
+  unsigned long long wait_ns;  // limit of the waits for progress (the drains use kWaitLimitNs)
   // 1: single-launch step (one new token, one row block): the kernel rotates
   // q_new itself and the block whose split holds pos appends the k / v row
   int fuse;

@@ -6,11 +6,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-namespace mqa {
+#include "launch.h"
 
-// Every spin on an mbarrier gives up after this long (the kernel then sets
-// MQA_DEVERR_TIMEOUT and winds down). A healthy wait lasts microseconds.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+namespace mqa {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,13 +63,24 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once `limit_ns`
+// has passed. try_wait may suspend the thread for a time the hardware
+// chooses, longer than a short limit: a limit below the default polls with
+// the non-blocking test_wait instead (a short limit only exercises the
+// timeout path).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns < kWaitLimitNs) {
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_test(bar, parity))
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -176,6 +185,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 // arrive at a named barrier without waiting for it
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Barrier over `count` threads that returns whether `pred` held on any of them
+// (one answer for all: a decision every participant takes alike). A barrier
+// id used here is never also used with bar.sync / bar.arrive.
+__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------- thread-block clusters
