@@ -32,7 +32,8 @@
 // Warps: 0-3 softmax and epilogue (row = thread), 4 K loader, 5 V loader
 // (TMA, 3 stages each; a K stage is released when its S is computed, a V
 // stage when its PV is), 6 MMA issue (one thread) and tensor-memory
-// allocation.
+// allocation, 7 the fused step's append (its own warp, so that the block
+// that writes the new row publishes Q as early as the others).
 #include <cuda_bf16.h>
 
 #include "../../include/mqa_decode.h"
@@ -48,7 +49,7 @@ constexpr int kD = 128;       // head_dim
 constexpr int kBM = 128;      // query rows (tokens of one head) per block
 constexpr int kBN = 128;      // keys per tile
 constexpr int kStages = 3;    // K tiles and V tiles in flight
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr int kTileBytes = kBN * kD * 2;                 // 32 KB: [2 halves][128 rows][128 B]
 constexpr int kQOff = 0;
 constexpr int kKOff = kTileBytes;                        // K stages
@@ -60,6 +61,12 @@ constexpr uint32_t kTmemCols = 512;                      // S0 .. S{kSBuf-1}, O
 constexpr uint32_t kColS = 0, kColO = kSBuf * 128;
 static_assert(kColO + kD <= kTmemCols, "S buffers and O exceed tensor memory");
 constexpr float kRescaleLog2 = 8.0f;
+// In the fused step the loaders request this many tiles before the Q rows
+// have landed, the rest after (other steps: before the Q rows are requested): a full ring of tile requests ahead of the Q reads delays them by
+// microseconds, none at all leaves the memory idle meanwhile (mqa8k, same-box
+// A/B: 2 tiles then Q 53.3 / 48.0 us isolated / back to back, 3 tiles with Q
+// requested 53.3 / 48.1, no tile 55.5 / 49.4).
+constexpr int kPreTiles = 2;
 // two-split cluster (CL): each block's normalised output rows (fp32) and their
 // lse, left in its V stages once its last PV is done
 constexpr int kXRows = 64;
@@ -83,10 +90,6 @@ static_assert(kNBars * 8 + 4 <= 256, "barrier area");
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
   const int half = col >> 6, chunk = (col & 63) >> 3;
   return half * 16384 + r * 128 + ((chunk ^ (r & 7)) << 4) + (col & 7) * 2;
-}
-
-__device__ __forceinline__ bool aborted(const Tc05Params& p) {
-  return (*reinterpret_cast<volatile int32_t*>(p.err) & static_cast<int>(MQA_DEVERR_TIMEOUT)) != 0;
 }
 
 // CL: the two splits of a (sequence, kv head) are one cluster of two blocks
@@ -129,8 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = min(kBM, R - g0);
 
   long long limit = p.capacity < p.max_seq_len ? p.capacity : p.max_seq_len;
+  // the length, the new position and the error word, requested together
   int L = p.seq_lens[b];
   const int apos = FUSE ? p.pos[b] : 0;  // fused step: the new token's position
+  const int err0 = tid == 0 ? *reinterpret_cast<volatile int32_t*>(p.err) : 0;
   if (L < n || L > limit) {
     // reported; these rows are then unspecified, but the block still runs (a
     // fused step's append and q_rot land as they would without the error)
@@ -215,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = tid; r < rows; r += kThreads) xl[r] = -INFINITY;
   };
 
-  if (tid == 0) s_skip = aborted(p) ? 1 : 0;  // an earlier block timed out: the result is invalid already
+  // an earlier block timed out: the result is invalid already
+  if (tid == 0) s_skip = (err0 & static_cast<int>(MQA_DEVERR_TIMEOUT)) ? 1 : 0;
   __syncthreads();
   if (s_skip) {
     if constexpr (CL) {
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kODone + s), 1);
     }
     mbar_init(bar(kDrain), 1);
-    mbar_init(bar(kAppended), 2);  // the two writer warps
+    mbar_init(bar(kAppended), 1);  // the append warp
     fence_mbar_init();
   }
   if (warp == 6) {
@@ -315,14 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(dst0 + s * kTileBytes, map, 0, kstart + it * kBN, 0, row, bar(full + s));
     };
     int it = 0;
-    if (p.early) {
-      // while the append kernel runs: the ring's first fill, tiles wholly
-      // before the new tokens
-      for (; it < T && it < kStages && kstart + (it + 1) * kBN <= Lp; ++it)
+    {
+      // the first tiles before the Q rows are in (while the append kernel
+      // runs, the ring's first fill), none holding a row that the preceding
+      // launch or this block's append writes
+      const int npre = p.early ? kStages : kPreTiles;
+      const int lim = p.early ? Lp : (writer ? apos : 0x7fffffff);
+      for (; it < T && it < npre && kstart + (it + 1) * kBN <= lim; ++it)
         if (lane == 0) issue(it);
     }
-    // the rest only once the Q rows have been requested: behind a burst of
-    // tile loads the Q reads would wait microseconds
+    // the rest only once the Q rows are in
     named_bar_sync(2, kBM + 64);
     if (lane == 0) {
       bool waited = !p.early, appended = !writer;
@@ -412,6 +420,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail(1);
     }
     __syncwarp();
+  } else if (warp == 7) {
+    // ---------------------------------------------- append (fused step only)
+    // the new token's cache rows exactly as the append kernel writes them: k
+    // pair i turned and rounded once to bf16 (rope_k_bf16, equal to the fp64
+    // rotation), v copied; a position outside the cache is reported and
+    // nothing is written. The loaders wait for it only before the tile that
+    // holds the row.
+    if (FUSE && writer) {
+      if (apos >= 0 && apos < p.capacity) {
+        const long long src = (static_cast<long long>(b) * p.h_kv + j) * kD;
+        const long long dst = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD;
+        uint32_t kraw[kD / 64], vraw[kD / 64];
+#pragma unroll
+        for (int h = 0; h < kD / 64; ++h) {  // pairs lane, lane + 32
+          const int i = lane + 32 * h;
+          kraw[h] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src + 2 * i);
+          vraw[h] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src + 2 * i);
+        }
+#pragma unroll
+        for (int h = 0; h < kD / 64; ++h) {
+          const int i = lane + 32 * h;
+          const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[i]);
+          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + dst + 2 * i) =
+              rope_k_bf16(bf16lo_to_f32(kraw[h]), bf16hi_to_f32(kraw[h]), ang);
+          *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + dst + 2 * i) =
+              vraw[h];
+        }
+      } else if (lane == 0) {
+        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+      }
+      // this block's TMA loads (async proxy) read the rows back
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kAppended));
+    }
   } else {
     // --------------------------------------------------- softmax (row = tid)
     const int r = tid;
@@ -436,35 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 raw[kD / 8];
 #pragma unroll
         for (int c = 0; c < kD / 8; ++c) raw[c] = live ? qn[c] : make_uint4(0u, 0u, 0u, 0u);
-        named_bar_arrive(2, kBM + 64);
         if (tid < kD / 2) {
           const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[tid]);
           float sf, cf;
           sincosf(static_cast<float>(ang), &sf, &cf);
           s_cs[tid] = cf;
           s_cs[kD / 2 + tid] = sf;
-        } else if (writer) {
-          // the new token's cache rows exactly as the append kernel writes
-          // them: k pair i turned and rounded once to bf16 (rope_k_bf16, equal
-          // to the fp64 rotation), v copied; a position outside the cache is
-          // reported and nothing is written
-          const int i = tid - kD / 2;
-          if (apos >= 0 && apos < p.capacity) {
-            const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[i]);
-            const long long row = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD + 2 * i;
-            const long long src = (static_cast<long long>(b) * p.h_kv + j) * kD + 2 * i;
-            const uint32_t kraw = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
-            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + row) =
-                rope_k_bf16(bf16lo_to_f32(kraw), bf16hi_to_f32(kraw), ang);
-            *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + row) =
-                *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
-          } else if (i == 0) {
-            atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
-          }
-          // this block's TMA loads (async proxy) read the rows back
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kAppended));
         }
         named_bar_sync(3, kBM);  // the cos / sin table
 #pragma unroll
@@ -491,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* q = reinterpret_cast<const float4*>(p.q_rot + grow_row * kD);
 #pragma unroll
         for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-        named_bar_arrive(2, kBM + 64);
+        named_bar_arrive(2, kBM + 64);  // (prefill and multi-token steps: the Q rows requested)
       }
 #pragma unroll
       for (int c = 0; c < kD; c += 8) {
@@ -503,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.w = pack_bf16x2(bq.z * p.scale_log2, bq.w * p.scale_log2);
         *reinterpret_cast<uint4*>(smem + kQOff + sw128(r, c)) = v;
       }
+      if constexpr (FUSE) named_bar_arrive(2, kBM + 64);  // the Q rows have landed: the loaders may go on
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kQReady));
