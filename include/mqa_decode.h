@@ -127,8 +127,13 @@ typedef enum mqa_variant {
  * 2 mantissa bits, no scale; k_scale_zero / v_scale_zero are unused.
  * kv_append_rope rounds the new row to nearest (ties to even) -- the key
  * once, from its fp64 rotation -- and saturates magnitudes beyond 57344 to
- * it. q_new, k_new and v_new are bf16; attention on tensor cores only, one
- * new token per sequence.
+ * it. q_new, k_new and v_new are bf16; attention on tensor cores only. One
+ * new token per sequence runs on the warp-MMA kernels (codes widened to fp16,
+ * fp16 query). Several new tokens (multi-token calls, prefill) run on the
+ * tcgen05 kernel's fp8 form: the code tiles are the MMA's B operand as they
+ * sit in memory, the query and the probabilities enter as two e4m3 parts
+ * each (hi + lo, the query scaled by 64 first), so q and P keep about 8
+ * significant bits of precision beyond a single e4m3 rounding.
  *
  * Bounded waits: inside the attention kernels every wait for another warp's
  * progress (a tile landing, a tile freed, a product done) gives up after
@@ -315,8 +320,10 @@ MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, con
  * mqa_decode_step_multi: the two calls on one stream, pos[b] = L - n_new.
  * 1 <= n_new <= 32 for the attention (kv_append_rope_multi takes any n_new;
  * longer runs of new tokens go to gqa_prefill_attention). n_new > 1 runs on
- * tensor cores over a bf16 cache only (MQA_ERR_UNSUPPORTED otherwise); n_new
- * = 1 is exactly the single-token call.
+ * tensor cores over a bf16 cache, or over a MQA_FP8_E5M2 cache that is
+ * contiguous with head_dim 128 and at least 32 query rows per kv head
+ * ((h_q / h_kv) * n_new >= 32; the tcgen05 kernel's fp8 form), and
+ * MQA_ERR_UNSUPPORTED otherwise; n_new = 1 is exactly the single-token call.
  */
 MQA_API mqa_status kv_append_rope_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new,
                                         const void* k_new, const void* v_new, const int32_t* pos, double rope_base,
@@ -355,8 +362,9 @@ MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_n
  *   lse_out optional [batch, n_new, h_q].
  * mqa_prefill_step: kv_append_rope_multi (pos[b] = L - n_new), then
  *   gqa_prefill_attention, on one stream.
- * Contiguous bf16 cache with head_dim 128 only (MQA_ERR_UNSUPPORTED
- * otherwise); no workspace. A bounded wait that runs out sets
+ * Contiguous bf16 or MQA_FP8_E5M2 cache with head_dim 128 only
+ * (MQA_ERR_UNSUPPORTED otherwise; e5m2 on the kernel's fp8 form described
+ * with MQA_FP8_E5M2); no workspace. A bounded wait that runs out sets
  * MQA_DEVERR_TIMEOUT and every later block of the launch returns at once.
  */
 MQA_API mqa_status gqa_prefill_attention(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,

@@ -121,10 +121,15 @@ DeviceInfo device_info(int dev) {
 // (MQA's G = 32, several new tokens per sequence).
 constexpr int kTc05MinRows = 32;
 
+// bf16 caches, and fp8 e5m2 caches with several new tokens per sequence (the
+// kernel's fp8 form: the code tiles enter the MMAs as they are; a one-token
+// e5m2 MQA step takes attn_tc05_widen.cu, measured faster there).
 bool use_tc05(const mqa_kv_layout* L, int variant, int n_new) {
-  return variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16 && !L->paged && L->head_dim == 128 &&
+  return variant == MQA_VARIANT_TENSOR_CORE && !L->paged && L->head_dim == 128 &&
+         (L->cache_dtype == MQA_BF16 || (L->cache_dtype == MQA_FP8_E5M2 && n_new > 1)) &&
          (L->h_q / L->h_kv) * n_new >= kTc05MinRows;
 }
+
 
 // n_new: query tokens per sequence; a kv head then has G x n_new query rows.
 KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
@@ -147,7 +152,8 @@ constexpr int kMaxNewTokens = 32;
 
 // Multi-token decode runs on the bf16 tensor-core kernel only.
 bool multi_supported(const mqa_kv_layout* L, int variant, int n_new) {
-  return n_new == 1 || (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16);
+  return n_new == 1 || (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16) ||
+         use_tc05(L, variant, n_new);
 }
 
 // Tokens one (sequence, kv head) may need read: the bound, or with a sliding
@@ -365,6 +371,20 @@ bool make_u8_maps(CUtensorMap* maps, const mqa_kv_layout* L, int rows_in, int he
       return false;
   }
   return true;
+}
+
+// Tensor maps of the tcgen05 kernel's K / V tiles: bf16 tiles, or the fp8
+// kernel's code tiles (t->f8 set).
+bool tc05_maps(const mqa_kv_layout* L, Tc05Params* t, CUtensorMap* tk, CUtensorMap* tv) {
+  if (L->cache_dtype == MQA_FP8_E5M2) {
+    CUtensorMap maps[4];
+    if (!make_u8_maps(maps, L, tc05_f8_box_rows(), 1)) return false;
+    *tk = maps[0];
+    *tv = maps[1];
+    t->f8 = 1;
+    return true;
+  }
+  return make_tensor_map(tk, L->k_cache, L, true, 1, 128) && make_tensor_map(tv, L->v_cache, L, true, 1, 128);
 }
 
 void fill_theta(double* theta, int head_dim, double base) {
@@ -585,8 +605,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
       fill_theta(t.theta, layout->head_dim, rope->rope_base);
     }
     CUtensorMap tk, tv;
-    if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
-        !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {
+    if (!tc05_maps(layout, &t, &tk, &tv)) {
       snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
       return MQA_ERR_CUDA;
     }
@@ -713,7 +732,9 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
                         int32_t* err_word, mqa_stream_t stream, int early) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if (layout->cache_dtype != MQA_BF16 || layout->paged || layout->head_dim != 128) return MQA_ERR_UNSUPPORTED;
+  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) || layout->paged ||
+      layout->head_dim != 128)
+    return MQA_ERR_UNSUPPORTED;
   if (n_new < 1 || static_cast<long long>(layout->batch) * n_new > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
   if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
   if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
@@ -750,8 +771,7 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
   p.early = early;
   p.wait_ns = wait_limit(layout);
   CUtensorMap tk, tv;
-  if (!make_tensor_map(&tk, layout->k_cache, layout, true, 1, 128) ||
-      !make_tensor_map(&tv, layout->v_cache, layout, true, 1, 128)) {
+  if (!tc05_maps(layout, &p, &tk, &tv)) {
     snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
     return MQA_ERR_CUDA;
   }
@@ -779,7 +799,9 @@ mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const vo
   // the attention's own checks first, so nothing is launched for a call that fails
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if (layout->cache_dtype != MQA_BF16 || layout->paged || layout->head_dim != 128) return MQA_ERR_UNSUPPORTED;
+  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) || layout->paged ||
+      layout->head_dim != 128)
+    return MQA_ERR_UNSUPPORTED;
   if (!seq_lens || !out || max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);

@@ -48,14 +48,7 @@ namespace {
 constexpr int kD = 128;       // head_dim
 constexpr int kBM = 128;      // query rows (tokens of one head) per block
 constexpr int kBN = 128;      // keys per tile
-constexpr int kStages = 3;    // K tiles and V tiles in flight
 constexpr int kThreads = 256;
-constexpr int kTileBytes = kBN * kD * 2;                 // 32 KB: [2 halves][128 rows][128 B]
-constexpr int kQOff = 0;
-constexpr int kKOff = kTileBytes;                        // K stages
-constexpr int kVOff = kKOff + kStages * kTileBytes;      // V stages
-constexpr int kBarOff = kVOff + kStages * kTileBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;
 constexpr int kSBuf = 3;                                 // S / P buffers in tensor memory
 constexpr uint32_t kTmemCols = 512;                      // S0 .. S{kSBuf-1}, O
 constexpr uint32_t kColS = 0, kColO = kSBuf * 128;
@@ -70,22 +63,52 @@ constexpr int kPreTiles = 2;
 // two-split cluster (CL): each block's normalised output rows (fp32) and their
 // lse, left in its V stages once its last PV is done
 constexpr int kXRows = 64;
-constexpr int kXOff = kVOff;
-static_assert((kXRows * (kD + 3)) * 4 <= kStages * kTileBytes, "cluster exchange area");
+// F8 (fp8 e5m2 cache): Q and P enter the MMAs as e4m3 pairs hi + lo, Q scaled
+// by 2^6 first (its values then sit in e4m3's normal range); the scores come
+// out 2^6 too large and are scaled back exactly
+constexpr float kQScaleF8 = 64.f;
 
-// mbarriers (8 bytes each) at kBarOff
-constexpr int kQReady = 0;
-constexpr int kKFull = 1;                   // [kStages]
-constexpr int kKEmpty = kKFull + kStages;   // [kStages]
-constexpr int kVFull = kKEmpty + kStages;   // [kStages]
-constexpr int kVEmpty = kVFull + kStages;   // [kStages]
-constexpr int kSFull = kVEmpty + kStages;   // [kSBuf]
-constexpr int kPFull = kSFull + kSBuf;      // [kSBuf]
-constexpr int kODone = kPFull + kSBuf;      // [kSBuf]
-constexpr int kDrain = kODone + kSBuf;
-constexpr int kAppended = kDrain + 1;       // fused step: the new k / v row is in the cache
-constexpr int kNBars = kAppended + 1;
-static_assert(kNBars * 8 + 4 <= 256, "barrier area");
+// Shared memory and mbarriers. bf16 cache: Q [2 halves][128 rows][128 B], K
+// and V tiles of 32 KB, three stages each. fp8 e5m2 cache (F8): Q as two
+// 16 KB e4m3 tiles (hi, lo) [128 rows][128 B], K and V code tiles of 16 KB
+// (128 keys x 128 one-byte values, as TMA lands them), six stages each: the
+// same bytes in flight.
+template <bool F8>
+struct Lay {
+  static constexpr int kStages = F8 ? 6 : 3;
+  static constexpr int kTileBytes = F8 ? kBN * kD : kBN * kD * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = 32768;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;
+  static constexpr int kXOff = kVOff;
+  // mbarriers (8 bytes each) at kBarOff
+  static constexpr int kQReady = 0;
+  static constexpr int kKFull = 1;                   // [kStages]
+  static constexpr int kKEmpty = kKFull + kStages;   // [kStages]
+  static constexpr int kVFull = kKEmpty + kStages;   // [kStages]
+  static constexpr int kVEmpty = kVFull + kStages;   // [kStages]
+  static constexpr int kSFull = kVEmpty + kStages;   // [kSBuf]
+  static constexpr int kPFull = kSFull + kSBuf;      // [kSBuf]
+  static constexpr int kODone = kPFull + kSBuf;      // [kSBuf]
+  static constexpr int kDrain = kODone + kSBuf;
+  static constexpr int kAppended = kDrain + 1;       // fused step: the new k / v row is in the cache
+  static constexpr int kNBars = kAppended + 1;
+  static_assert(kNBars * 8 + 4 <= 512, "barrier area");
+  static_assert((kXRows * (kD + 3)) * 4 <= kStages * kTileBytes, "cluster exchange area");
+  static_assert((kBM * (kD + 4) + 3 * kBM) * 4 <= kStages * kTileBytes, "replica merge area (the K stages)");
+  static_assert(kKOff >= kD * kBM * 2, "Q area");
+};
+static_assert(Lay<true>::kSmemBytes <= Lay<false>::kSmemBytes, "the bf16 layout is the larger one");
+
+// e4m3_split4 out of line: the Q rows are split once per launch, and 32
+// inlined copies of the code would only be cold instruction-cache misses.
+__device__ __noinline__ uint2 e4m3_split4_once(float a, float b, float c, float d) {
+  uint2 r;
+  tc05::e4m3_split4(a, b, c, d, r.x, r.y);
+  return r;
+}
 
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
   const int half = col >> 6, chunk = (col & 63) >> 3;
@@ -95,11 +118,19 @@ __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of b
 // CL: the two splits of a (sequence, kv head) are one cluster of two blocks
 // that merge their partial results through distributed shared memory; block
 // 0 writes the output (no combine launch, no partials in global memory).
-template <int PARTS, bool FUSE, bool CL>
+// F8: fp8 e5m2 cache (the tensor maps describe the one-byte code tiles).
+template <int PARTS, bool FUSE, bool CL, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const Tc05Params p) {
   static_assert(!CL || PARTS > 1, "the cluster merge takes replicated rows (R <= 64)");
+  static_assert(!(FUSE && F8), "the fused one-token step is bf16 only");
+  using Y = Lay<F8>;
+  constexpr int kStages = Y::kStages, kTileBytes = Y::kTileBytes, kQOff = Y::kQOff, kKOff = Y::kKOff,
+                kVOff = Y::kVOff, kBarOff = Y::kBarOff, kXOff = Y::kXOff;
+  constexpr int kQReady = Y::kQReady, kKFull = Y::kKFull, kKEmpty = Y::kKEmpty, kVFull = Y::kVFull,
+                kVEmpty = Y::kVEmpty, kSFull = Y::kSFull, kPFull = Y::kPFull, kODone = Y::kODone,
+                kDrain = Y::kDrain, kAppended = Y::kAppended, kNBars = Y::kNBars;
   constexpr int kRPad = kBM / PARTS;  // rows per part
   constexpr int kKW = kBN / PARTS;    // keys of a tile per thread
   extern __shared__ unsigned char smem_raw[];
@@ -240,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kstart = max(t_begin, (ka_first / 64) * 64);
   const int kend = min(t_end, pos_last + 1);
   const int T = kend > kstart ? (kend - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
+  auto tile_key0 = [&](int it) { return kstart + it * kBN; };
   const bool split_out = S > 1 && !CL;
   // fused step: the split whose token range holds the new token's position
   // (else split 0) appends its k / v row
@@ -318,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue = [&](int it) {
       const int s = it % kStages;
       mbar_arrive_expect_tx(bar(full + s), kTileBytes);
-      tma_load_4d(dst0 + s * kTileBytes, map, 0, kstart + it * kBN, 0, row, bar(full + s));
+      if constexpr (F8)
+        tma_load_3d(dst0 + s * kTileBytes, map, 0, tile_key0(it), row, bar(full + s));
+      else
+        tma_load_4d(dst0 + s * kTileBytes, map, 0, tile_key0(it), 0, row, bar(full + s));
     };
     int it = 0;
     {
@@ -327,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // launch or this block's append writes
       const int npre = p.early ? kStages : kPreTiles;
       const int lim = p.early ? Lp : (writer ? apos : 0x7fffffff);
-      for (; it < T && it < npre && kstart + (it + 1) * kBN <= lim; ++it)
+      for (; it < T && it < npre && tile_key0(it) + kBN <= lim; ++it)
         if (lane == 0) issue(it);
     }
     // the rest only once the Q rows are in
@@ -341,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (stop()) break;
-        if (!waited && Lp < kstart + (it + 1) * kBN) {  // this tile holds a new token's row
+        if (!waited && Lp < tile_key0(it) + kBN) {  // this tile holds a new token's row
           grid_dependency_wait();
           waited = true;
         }
-        if (!appended && apos < kstart + (it + 1) * kBN) {  // ... written by this block's softmax warps
+        if (!appended && apos < tile_key0(it) + kBN) {  // ... written by this block's append warp
           if (!mbar_wait(bar(kAppended), 0, p.wait_ns)) {
             fail(1);
             break;
@@ -363,8 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 6) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      const uint32_t id_s = tc05::idesc_bf16_f32(kBM, kBN, false, false);
-      const uint32_t id_o = tc05::idesc_bf16_f32(kBM, kD, false, true);
+      const uint32_t id_s = F8 ? tc05::idesc_e4m3_e5m2_f32(kBM, kBN, false, false)
+                               : tc05::idesc_bf16_f32(kBM, kBN, false, false);
+      const uint32_t id_o = F8 ? tc05::idesc_e4m3_e5m2_f32(kBM, kD, false, true)
+                               : tc05::idesc_bf16_f32(kBM, kD, false, true);
       const uint32_t q_s = sbase + kQOff;
       bool ok = mbar_wait(bar(kQReady), 0, p.wait_ns);
       // S of tile it into buffer it % kSBuf. That buffer last held P of tile
@@ -373,11 +410,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % kStages, sb = it % kSBuf;
         tc05::fence_after_sync();
         const uint32_t k_s = sbase + kKOff + s * kTileBytes;
+        if constexpr (F8) {
+          // S = Q_hi K^T + Q_lo K^T, 32 head dims per MMA (K-major 8-bit rows)
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc05::mma_bf16(tmem + kColS + sb * 128, tc05::smem_desc_sw128(q_s + off, 16, 1024),
-                         tc05::smem_desc_sw128(k_s + off, 16, 1024), id_s, ks > 0);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < kD / 32; ++ks)
+              tc05::mma_f8(tmem + kColS + sb * 128, tc05::smem_desc_sw128(q_s + part * 16384 + ks * 32, 16, 1024),
+                           tc05::smem_desc_sw128(k_s + ks * 32, 16, 1024), id_s, part > 0 || ks > 0);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            tc05::mma_bf16(tmem + kColS + sb * 128, tc05::smem_desc_sw128(q_s + off, 16, 1024),
+                           tc05::smem_desc_sw128(k_s + off, 16, 1024), id_s, ks > 0);
+          }
         }
         tc05::commit(bar(kSFull + sb));
         tc05::commit(bar(kKEmpty + s));
@@ -386,10 +433,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % kStages, pb = it % kSBuf;
         tc05::fence_after_sync();
         const uint32_t v_s = sbase + kVOff + s * kTileBytes;
+        if constexpr (F8) {
+          // O += P_hi V + P_lo V, 32 keys per MMA: P from tensor memory (hi in
+          // the buffer's columns 0-31, lo in 32-63), V MN-major (8-bit rows of
+          // 128 dims, 8-key groups 1 KB apart)
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          tc05::mma_bf16_ta(tmem + kColO, tmem + kColS + pb * 128 + ks * 8,
-                            tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, it > 0 || ks > 0);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < kBN / 32; ++ks)
+              tc05::mma_f8_ta(tmem + kColO, tmem + kColS + pb * 128 + part * 32 + ks * 8,
+                              tc05::smem_desc_sw128(v_s + ks * 4096, 16384, 1024), id_o,
+                              it > 0 || part > 0 || ks > 0);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            tc05::mma_bf16_ta(tmem + kColO, tmem + kColS + pb * 128 + ks * 8,
+                              tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, it > 0 || ks > 0);
+        }
         tc05::commit(bar(kODone + pb));
         tc05::commit(bar(kVEmpty + s));
       };
@@ -513,15 +573,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kD / 4; ++c) qv[c] = live ? q[c] : make_float4(0.f, 0.f, 0.f, 0.f);
         named_bar_arrive(2, kBM + 64);  // (prefill and multi-token steps: the Q rows requested)
       }
+      if constexpr (F8) {
+        // e4m3 hi + lo of q * scale * log2(e) * 2^6: 16 dims per 16-byte chunk,
+        // chunk c of row r at c ^ (r mod 8) (128-byte swizzle)
+        const float qs = p.scale_log2 * kQScaleF8;
 #pragma unroll
-      for (int c = 0; c < kD; c += 8) {
-        const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
-        uint4 v;
-        v.x = pack_bf16x2(a.x * p.scale_log2, a.y * p.scale_log2);
-        v.y = pack_bf16x2(a.z * p.scale_log2, a.w * p.scale_log2);
-        v.z = pack_bf16x2(bq.x * p.scale_log2, bq.y * p.scale_log2);
-        v.w = pack_bf16x2(bq.z * p.scale_log2, bq.w * p.scale_log2);
-        *reinterpret_cast<uint4*>(smem + kQOff + sw128(r, c)) = v;
+        for (int c = 0; c < kD / 16; ++c) {
+          uint4 hi, lo;
+          uint32_t* h = &hi.x;
+          uint32_t* o = &lo.x;
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            const float4 a = qv[4 * c + w4];
+            const uint2 hl = e4m3_split4_once(a.x * qs, a.y * qs, a.z * qs, a.w * qs);
+            h[w4] = hl.x;
+            o[w4] = hl.y;
+          }
+          const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(smem + kQOff + off) = hi;
+          *reinterpret_cast<uint4*>(smem + kQOff + 16384 + off) = lo;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kD; c += 8) {
+          const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
+          uint4 v;
+          v.x = pack_bf16x2(a.x * p.scale_log2, a.y * p.scale_log2);
+          v.y = pack_bf16x2(a.z * p.scale_log2, a.w * p.scale_log2);
+          v.z = pack_bf16x2(bq.x * p.scale_log2, bq.y * p.scale_log2);
+          v.w = pack_bf16x2(bq.z * p.scale_log2, bq.w * p.scale_log2);
+          *reinterpret_cast<uint4*>(smem + kQOff + sw128(r, c)) = v;
+        }
       }
       if constexpr (FUSE) named_bar_arrive(2, kBM + 64);  // the Q rows have landed: the loaders may go on
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -547,8 +629,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc05::wait_ld();
 #pragma unroll
       for (int c = 0; c < kKW; c += 32) tc05::reg_fence(*reinterpret_cast<float(*)[32]>(&s[c]));
+      if constexpr (F8) {
+#pragma unroll
+        for (int c = 0; c < kKW; ++c) s[c] *= 1.f / kQScaleF8;  // exact: a power of two
+      }
       // keys of this tile outside [ka, pos] are masked
-      const int key0 = kstart + it * kBN;
+      const int key0 = tile_key0(it);
       if (key0 + kBN > t_end) {
         // rows past the split may hold anything: past the sequence any bit
         // pattern (NaN included), and the next split's first rows may be the
@@ -562,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (!F8) *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
@@ -611,7 +697,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P of this thread's keys as bf16 pairs over its own S columns; the
       // other parts' columns of this row carry zeros
       const uint32_t prow = tmem + lane_base + kColS + sb * 128;
-      if constexpr (PARTS == 1) {
+      if constexpr (F8) {
+        // P as e4m3 hi + lo, four keys per column: hi over the buffer's columns
+        // 0-31, lo over 32-63; this thread's keys at its part's columns, zeros
+        // over the other parts'
+        if constexpr (PARTS == 1) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t ph[16], pl[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float pv[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                pv[k] = fast_exp2(s[64 * half + 4 * i + k] - e);
+                sm8[(4 * i + k) & 7] += pv[k];
+              }
+              tc05::e4m3_split4(pv[0], pv[1], pv[2], pv[3], ph[i], pl[i]);
+            }
+            tc05::st_32x32b_x16_u(prow + 16 * half, ph);
+            tc05::st_32x32b_x16_u(prow + 32 + 16 * half, pl);
+          }
+        } else {
+          constexpr int kW8 = kKW / 4;  // columns of this thread's P_hi (and of its P_lo)
+          uint32_t ph[kW8], pl[kW8], z[kW8];
+#pragma unroll
+          for (int i = 0; i < kW8; ++i) {
+            float pv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              pv[k] = fast_exp2(s[4 * i + k] - e);
+              sm8[(4 * i + k) & 7] += pv[k];
+            }
+            tc05::e4m3_split4(pv[0], pv[1], pv[2], pv[3], ph[i], pl[i]);
+            z[i] = 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < PARTS; ++q) {
+            if constexpr (PARTS == 4) {
+              tc05::st_32x32b_x8_u(prow + 8 * q, q == part ? ph : z);
+              tc05::st_32x32b_x8_u(prow + 32 + 8 * q, q == part ? pl : z);
+            } else {
+              tc05::st_32x32b_x16_u(prow + 16 * q, q == part ? ph : z);
+              tc05::st_32x32b_x16_u(prow + 32 + 16 * q, q == part ? pl : z);
+            }
+          }
+        }
+      } else if constexpr (PARTS == 1) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
@@ -807,17 +939,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-KernelShape tc05_shape() { return {kThreads, kSmemBytes, kBM, 1}; }
+KernelShape tc05_shape() { return {kThreads, Lay<false>::kSmemBytes, kBM, 1}; }
 
-template <int PARTS, bool FUSE, bool CL>
+int tc05_f8_box_rows() { return kBN; }
+
+template <int PARTS, bool FUSE, bool CL, bool F8>
 cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  auto kern = attn_tc05_kernel<PARTS, FUSE, CL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = attn_tc05_kernel<PARTS, FUSE, CL, F8>;
+  constexpr int smem = Lay<F8>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.h_kv * p.num_splits * p.row_blocks);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -834,11 +969,34 @@ cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUten
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-template <int PARTS>
+template <int PARTS, bool F8>
 cudaError_t launch_fuse(const Tc05Params& p, bool cl, const CUtensorMap& tk, const CUtensorMap& tv,
                         cudaStream_t stream) {
-  if (cl) return p.fuse ? launch_parts<PARTS, true, true>(p, tk, tv, stream) : launch_parts<PARTS, false, true>(p, tk, tv, stream);
-  return p.fuse ? launch_parts<PARTS, true, false>(p, tk, tv, stream) : launch_parts<PARTS, false, false>(p, tk, tv, stream);
+  if constexpr (F8) {  // (several new tokens: never fused)
+    return cl ? launch_parts<PARTS, false, true, true>(p, tk, tv, stream)
+              : launch_parts<PARTS, false, false, true>(p, tk, tv, stream);
+  } else {
+    if (cl)
+      return p.fuse ? launch_parts<PARTS, true, true, false>(p, tk, tv, stream)
+                    : launch_parts<PARTS, false, true, false>(p, tk, tv, stream);
+    return p.fuse ? launch_parts<PARTS, true, false, false>(p, tk, tv, stream)
+                  : launch_parts<PARTS, false, false, false>(p, tk, tv, stream);
+  }
+}
+
+template <bool F8>
+cudaError_t launch_rows(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  // replicate few rows over the 128 MMA rows so that all four softmax warps work
+  const long long rows = static_cast<long long>(p.group) * p.n_new;
+  const bool cl = tc05_merges_splits(p);
+  // (a fused step has one row block: p.fuse implies row_blocks == 1)
+  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4, F8>(p, cl, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2, F8>(p, cl, tk, tv, stream);
+  if constexpr (F8)
+    return launch_parts<1, false, false, true>(p, tk, tv, stream);
+  else
+    return p.fuse ? launch_parts<1, true, false, false>(p, tk, tv, stream)
+                  : launch_parts<1, false, false, false>(p, tk, tv, stream);
 }
 
 bool tc05_merges_splits(const Tc05Params& p) {
@@ -847,13 +1005,7 @@ bool tc05_merges_splits(const Tc05Params& p) {
 
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
-  // replicate few rows over the 128 MMA rows so that all four softmax warps work
-  const long long rows = static_cast<long long>(p.group) * p.n_new;
-  const bool cl = tc05_merges_splits(p);
-  // (a fused step has one row block: p.fuse implies row_blocks == 1)
-  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4>(p, cl, tk, tv, stream);
-  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2>(p, cl, tk, tv, stream);
-  return p.fuse ? launch_parts<1, true, false>(p, tk, tv, stream) : launch_parts<1, false, false>(p, tk, tv, stream);
+  return p.f8 ? launch_rows<true>(p, tk, tv, stream) : launch_rows<false>(p, tk, tv, stream);
 }
 
 }  // namespace mqa

@@ -88,6 +88,7 @@ struct DecodeParams {
 struct Tc05Params {
   int batch, h_q, h_kv, group, n_new;
   int row_blocks;  // ceil(group * n_new / 128)
+  int f8;          // attn_tc05: 1 = fp8 e5m2 cache (code tiles), 0 = bf16
   int num_splits;  // token-axis splits; 1 = write `out` directly
   int chunk;       // tokens per split, a multiple of 64
   const void* k_cache;
@@ -195,5 +196,8 @@ cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k
 // that writes out and lse_out directly): no combine follows, and o_part /
 // lse_part are not written
 bool tc05_merges_splits(const Tc05Params& p);
+// rows of the TMA box (keys per load) the tcgen05 kernel expects for an fp8
+// e5m2 cache
+int tc05_f8_box_rows();
 
 }  // namespace mqa

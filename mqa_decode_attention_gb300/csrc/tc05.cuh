@@ -10,10 +10,13 @@
 //   offset >> 4 in bits 32-45, the fixed value 0b001 in bits 46-48, base
 //   offset 0 (every swizzle atom starts aligned), swizzle mode in bits
 //   61-63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
-//   instruction descriptor for kind::f16 (32 bit): D format in bits 4-5
-//   (1 = f32), A / B format in bits 7-9 / 10-12 (0 = f16, 1 = bf16), A / B major in
-//   bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in
-//   bits 24-28.
+//   instruction descriptor for kind::f16 and kind::f8f6f4 (32 bit): D format
+//   in bits 4-5 (1 = f32), A / B format in bits 7-9 / 10-12 (kind::f16: 0 =
+//   f16, 1 = bf16; kind::f8f6f4: 0 = e4m3, 1 = e5m2), A / B major in bits 15 /
+//   16 (0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits
+//   24-28.
+//   8-bit operands use the same 128-byte-swizzled layouts with 128 elements
+//   per 128-byte row; one kind::f8f6f4 MMA takes K = 32.
 #pragma once
 
 #include <stdint.h>
@@ -61,6 +64,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::f8f6f4 instruction descriptor: e4m3 A x e5m2 B -> f32, M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_e5m2_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+         (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Tensor-memory allocation: executed by one whole warp; the base address is
 // written to shared memory at `dst`. ncols a power of two >= 32.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -96,6 +106,29 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, 8-bit operands (kind::f8f6f4), one thread.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], 8-bit operands: A's M rows in lanes,
+// K-major, four elements per 32-bit column (lowest K in the low byte).
+__device__ __forceinline__ void mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
       : "memory");
 }
@@ -162,6 +195,38 @@ __device__ __forceinline__ void st_32x32b_x16_u(uint32_t taddr, const uint32_t (
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
+}
+
+// 8 consecutive 32-bit columns of this thread's lane from registers.
+__device__ __forceinline__ void st_32x32b_x8_u(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Four fp32 values (a, b, c, d in K order) as e4m3 pairs hi + lo with
+// hi = e4m3(x), lo = e4m3(x - hi), rounded to nearest, saturating at 448;
+// packed four per word, the first value in the low byte.
+__device__ __forceinline__ void e4m3_split4(float a, float b, float c, float d, uint32_t& hi, uint32_t& lo) {
+  uint32_t h01, h23, l01, l23;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(h01) : "f"(b), "f"(a));
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(h23) : "f"(d), "f"(c));
+  uint32_t f01, f23;  // the hi values back as f16 pairs (exact)
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(f01) : "r"(h01));
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(f23) : "r"(h23));
+  float fa, fb, fc, fd;
+  asm("{\n\t.reg .f16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\tcvt.f32.f16 %1, y;\n\t}"
+      : "=f"(fa), "=f"(fb) : "r"(f01));
+  asm("{\n\t.reg .f16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\tcvt.f32.f16 %1, y;\n\t}"
+      : "=f"(fc), "=f"(fd) : "r"(f23));
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(l01) : "f"(b - fb), "f"(a - fa));
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(l23) : "f"(d - fd), "f"(c - fc));
+  hi = h01 | (h23 << 16);
+  lo = l01 | (l23 << 16);
 }
 
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

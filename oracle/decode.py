@@ -497,6 +497,49 @@ def decode_step_multi(k_cache, v_cache, q_new, k_new, v_new, seq_lens, rope_base
     return res
 
 
+def decode_step_multi_e5m2(k_codes, v_codes, q_new, k_new, v_new, seq_lens, rope_base: float, scale: float,
+                           block_table=None, page_size: int = 0, window: int = 0):
+    """n new tokens per sequence in one pass (the verification of drafted
+    tokens, "Arsitektur Inferensi LLM", section 7) over an fp8 e5m2 cache:
+    decode_step_multi's steps with decode_step_e5m2's storage. New token i of
+    sequence b sits at p = L_b - n + i; its q and k are rotated by p in fp64,
+    its key is rounded once to e5m2 and its value (bf16 input) likewise, both
+    stored at p; query i then attends to [window_start(p + 1, W), p + 1) of
+    the decoded cache.
+    Returns dict(out [B,n,H_q,d], lse [B,n,H_q], q_rot [B,n,H_q,d], k_codes,
+    v_codes) with the codes as updated copies."""
+    Kc, Vc = np.array(k_codes, dtype=np.uint8, copy=True), np.array(v_codes, dtype=np.uint8, copy=True)
+    q_new, k_new, v_new = _f64(q_new), _f64(k_new), _f64(v_new)
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    table = None if block_table is None else np.asarray(_f64(block_table), dtype=np.int64)
+    B, n, h_q, d = q_new.shape
+    out = np.empty((B, n, h_q, d), F64)
+    lse = np.empty((B, n, h_q), F64)
+    q_rot = np.empty((B, n, h_q, d), F64)
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(n):
+            p = L - n + i
+            q_rot[b, i] = rope_rotate(q_new[b, i], p, rope_base)
+            kq = quantize_e5m2(rope_rotate(k_new[b, i], p, rope_base))
+            vq = quantize_e5m2(v_new[b, i])
+            if table is None:
+                Kc[b, :, p], Vc[b, :, p] = kq, vq
+            else:
+                page, off = page_slot(table[b], p, page_size)
+                Kc[page, :, off], Vc[page, :, off] = kq, vq
+        if table is None:
+            Kd, Vd = dequantize_e5m2(Kc[b, :, :L]), dequantize_e5m2(Vc[b, :, :L])
+        else:
+            Kd = dequantize_e5m2(gather_paged(Kc, table[b], L, page_size))
+            Vd = dequantize_e5m2(gather_paged(Vc, table[b], L, page_size))
+        for i in range(n):
+            p = L - n + i
+            t0 = window_start(p + 1, window)
+            out[b, i], lse[b, i] = gqa_attention(q_rot[b, i], Kd[:, t0:p + 1], Vd[:, t0:p + 1], scale)
+    return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "v_codes": Vc}
+
+
 def decode_unit(q_group, k_row, v_row, K_unit, V_unit, seq_len: int, rope_base: float, scale: float,
                 cache_dtype: str, window: int = 0):
     """The decode step for ONE (sequence, KV head) unit, for sampled checks at

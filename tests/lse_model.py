@@ -4,8 +4,10 @@ fp32 accuracy instead of the bf16 output tolerance.
 
 Every kernel multiplies q_rot by c = fp32(scale * log2 e) in fp32 and rounds
 the product to its MMA operand type before the scores are formed: bf16 on the
-bf16-cache tensor-core kernels (warp MMA and tcgen05), fp16 on the e5m2-cache
-kernels, none on the CUDA-core (fp32) path. That one rounding moves a score by
+bf16-cache tensor-core kernels (warp MMA and tcgen05), fp16 on the warp-MMA
+e5m2-cache kernels, none on the CUDA-core (fp32) path; the tcgen05 e5m2-cache
+kernel takes x = q c 2^6 as two e4m3 values hi = e4m3(x), lo = e4m3(x - hi)
+(fmt "e4m3x2"). That one rounding moves a score by
 up to 2^-8 of the sum of its terms' magnitudes for bf16 (about 1e-3 on N(0,1)
 data at d = 128), far more than everything after it: fp32 accumulation, the
 ex2 approximation, the split combine. The model applies the same rounding to
@@ -15,8 +17,8 @@ fp64, so what remains between it and the GPU is fp32 arithmetic: LSE_TOL.
 The GPU's own q_rot comes from an fp32 rotation (relative error below 1e-6 of
 the fp64 one), so an element of q * c lying within that distance of a rounding
 boundary may round the other way on the GPU. Such elements widen their row's
-tolerance by what one operand spacing can move the log-sum-exp (it is
-1-Lipschitz in the largest score change): ln 2 * spacing * max_t |k_t,i|.
+tolerance by what that change of the operand can move the log-sum-exp (it is
+1-Lipschitz in the largest score change): ln 2 * |change| * max_t |k_t,i|.
 """
 
 import math
@@ -31,7 +33,18 @@ _LOG2E = np.float32(1.4426950408889634)
 _AMBIGUOUS = 2e-6  # relative distance to a rounding boundary that the fp32 rotation may cross
 
 
+def _e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to e4m3 (nearest, ties to even), saturating at 448."""
+    t = torch.from_numpy(np.clip(np.ascontiguousarray(x, np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).to(torch.float32).numpy()
+
+
 def _round(x32: np.ndarray, fmt: str) -> np.ndarray:
+    if fmt == "e4m3x2":
+        x = x32.astype(np.float32) * np.float32(64.0)
+        hi = _e4m3(x)
+        lo = _e4m3((x - hi).astype(np.float32))
+        return (hi.astype(np.float64) + lo.astype(np.float64)) / 64.0
     if fmt == "bf16":
         return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16).to(torch.float64).numpy()
     if fmt == "f16":
@@ -39,12 +52,6 @@ def _round(x32: np.ndarray, fmt: str) -> np.ndarray:
     if fmt == "f32":
         return x32.astype(np.float64)
     raise ValueError(fmt)
-
-
-def _spacing(x: np.ndarray, fmt: str) -> np.ndarray:
-    bits = {"bf16": 7, "f16": 10}[fmt]
-    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
-    return 2.0 ** (e - bits)
 
 
 def model_lse(q_rot, keys, lens, scale: float, fmt: str, window: int = 0, key_scales=None):
@@ -69,9 +76,10 @@ def model_lse(q_rot, keys, lens, scale: float, fmt: str, window: int = 0, key_sc
     if fmt == "f32":
         spread = np.zeros_like(qr)
     else:
+        # how far the operand moves when q c moves by the fp32 rotation's error
         lo = _round((qs.astype(np.float64) * (1 - _AMBIGUOUS)).astype(np.float32), fmt)
         hi = _round((qs.astype(np.float64) * (1 + _AMBIGUOUS)).astype(np.float32), fmt)
-        spread = np.where((lo != qr) | (hi != qr), _spacing(qs.astype(np.float64), fmt), 0.0)
+        spread = np.maximum(np.abs(lo - qr), np.abs(hi - qr))
     lse = np.empty((B, n, h_q))
     tol = np.empty((B, n, h_q))
     for b in range(B):

@@ -781,6 +781,52 @@ def check_multi_step(fn):
         assert np.array_equal(K, r["k_cache"]) and np.array_equal(V, r["v_cache"])
 
 
+def check_multi_e5m2(fn):
+    """n new tokens over an e5m2 cache in one pass equal n single-token e5m2
+    steps in order (each sees the codes the earlier ones stored), contiguous
+    and with a window; the stored codes are identical."""
+    rng = np.random.default_rng(61)
+    B, h_q, h_kv, d, cap, n = 2, 8, 2, 32, 40, 4
+    Kc = oracle.quantize_e5m2(rng.standard_normal((B, h_kv, cap, d)))
+    Vc = oracle.quantize_e5m2(rng.standard_normal((B, h_kv, cap, d)))
+    q = oracle.round_bf16(rng.standard_normal((B, n, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    lens = np.array([40, 9])
+    for window in (0, 5):
+        r = fn(Kc, Vc, q, k, v, lens, 10000.0, 0.2, window=window)
+        kc, vc = Kc.copy(), Vc.copy()
+        for i in range(n):
+            one = oracle.decode_step_e5m2(kc, vc, q[:, i], k[:, i], v[:, i], lens - n + i + 1, 10000.0, 0.2,
+                                          window=window)
+            kc, vc = one["k_codes"], one["v_codes"]
+            assert np.allclose(r["out"][:, i], one["out"], rtol=0, atol=1e-12)
+            assert np.allclose(r["lse"][:, i], one["lse"], rtol=0, atol=1e-12)
+        assert np.array_equal(r["k_codes"], kc) and np.array_equal(r["v_codes"], vc)
+
+
+def test_multi_token_e5m2_pins():
+    check_multi_e5m2(oracle.decode_step_multi_e5m2)
+
+
+def test_multi_token_e5m2_planted_mistake_is_caught():
+    """Without the causal mask among the new tokens (every query sees all n
+    new rows) the pin fails."""
+    def no_causal(k_codes, v_codes, q_new, k_new, v_new, seq_lens, rope_base, scale, window=0):
+        r = oracle.decode_step_multi_e5m2(k_codes, v_codes, q_new, k_new, v_new, seq_lens, rope_base, scale,
+                                          window=window)
+        n = q_new.shape[1]
+        for b, L in enumerate(np.asarray(seq_lens)):
+            Kd = oracle.dequantize_e5m2(r["k_codes"][b, :, :L])
+            Vd = oracle.dequantize_e5m2(r["v_codes"][b, :, :L])
+            for i in range(n):
+                t0 = oracle.window_start(L, window)
+                r["out"][b, i], r["lse"][b, i] = oracle.gqa_attention(r["q_rot"][b, i], Kd[:, t0:], Vd[:, t0:], scale)
+        return r
+
+    assert _fails(check_multi_e5m2, no_causal)
+
+
 def test_multi_token_decode_pins(golden_dir):
     check_multi_step(oracle.decode_step_multi)
     # n = 1 is the single-token step

@@ -5,7 +5,8 @@ e5m2 and attends over the decoded cache in fp64. The append is byte work and
 must match exactly: the appended codes, and nothing else in the caches
 changes. Outputs are bf16, max |err| <= 2e-2 like the bf16 cache path; the
 fp32 lse is held to 1e-4 of the log-sum-exp over the scores the kernels form
-(their fp16 query operand, tests/lse_model.py).
+(tests/lse_model.py): an fp16 query operand on the one-token kernels, e4m3 hi +
+lo on the tcgen05 kernel that serves several new tokens.
 """
 
 import math
@@ -16,7 +17,7 @@ import torch
 
 import oracle
 from lse_model import assert_lse, paged_keys
-from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, workload
+from synthetic import make_contiguous_case, make_e5m2_cache, make_paged_case, normal, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -71,12 +72,19 @@ def _keys(ref, case, paged):
     return paged_keys(k, case.block_table, case.seq_lens, case.page_size) if paged else k
 
 
+def q_fmt(case, paged=False):
+    """The query operand of the kernel that serves a one-token step over an
+    e5m2 cache: the warp-MMA kernels, fp16 (the tcgen05 kernel's fp8 form,
+    e4m3 hi + lo, serves only several new tokens)."""
+    return "f16"
+
+
 def check(got, ref, case, paged=False, window=0):
     assert got["err"] == 0
     assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
     assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL
     assert_lse(got["lse"], ref["q_rot"], _keys(ref, case, paged), case.seq_lens, 1.0 / math.sqrt(case.q_new.shape[-1]),
-               "f16", window=window)
+               q_fmt(case, paged), window=window)
     assert np.max(np.abs(got["q_rot"] - ref["q_rot"])) <= 1e-5 * (1 + np.max(np.abs(ref["q_rot"])))
     for key in ("k_codes", "v_codes"):  # the appended rows bit for bit, every other row untouched
         bad = np.argwhere(got[key] != ref[key])
@@ -129,7 +137,7 @@ def test_e5m2_sliding_window(m, window):
         got = run_f8(m, w, c, kc8, vc8, paged=False, splits=splits, window=window, max_len=700)
         assert got["err"] == 0
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
-        assert_lse(got["lse"], ref["q_rot"], _keys(ref, c, False), c.seq_lens, 1.0 / math.sqrt(128), "f16",
+        assert_lse(got["lse"], ref["q_rot"], _keys(ref, c, False), c.seq_lens, 1.0 / math.sqrt(128), q_fmt(c),
                    window=window, what=splits)
 
 
@@ -153,6 +161,8 @@ def test_e5m2_nan_codes_past_the_sequence(m):
 
 
 def test_e5m2_multi_token_is_refused(m):
+    """Several new tokens with fewer than 32 query rows per kv head (G x n):
+    no kernel takes them over an e5m2 cache."""
     w = workload("gqa4k").with_(batch=1, h_q=8, h_kv=2)
     kc8, vc8 = make_e5m2_cache((1, 2, 64), 128, seed=14)
     lay = m.layout_contiguous(kc8.to(DEV), vc8.to(DEV), 8)
@@ -162,6 +172,107 @@ def test_e5m2_multi_token_is_refused(m):
     with pytest.raises(m.MqaError):
         m.gqa_decode_attention_multi(lay, 2, q, torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1, 1, out,
                                      err=err)
+
+
+def _new_tokens(w, n, seed):
+    q = normal((w.batch, n, w.h_q, w.head_dim), seed, 21)
+    k = normal((w.batch, n, w.h_kv, w.head_dim), seed, 22)
+    v = normal((w.batch, n, w.h_kv, w.head_dim), seed, 23)
+    return q, k, v
+
+
+def _check_multi(got_out, got_lse, kc8, vc8, ref, lens, w, n, window=0, what=None):
+    assert np.max(np.abs(got_out.reshape(ref["out"].shape) - ref["out"])) <= BF16_TOL, what
+    assert np.max(np.abs(got_lse.reshape(ref["lse"].shape) - ref["lse"])) <= BF16_TOL, what
+    assert_lse(got_lse.reshape(ref["lse"].shape), ref["q_rot"], oracle.dequantize_e5m2(ref["k_codes"]), lens,
+               1.0 / math.sqrt(w.head_dim), "e4m3x2", window=window, what=what)
+    assert np.array_equal(_codes(kc8), ref["k_codes"]) and np.array_equal(_codes(vc8), ref["v_codes"]), what
+
+
+MULTI = [
+    # B, h_q, h_kv, lens, capacity, n: 32 or more query rows (G x n) per kv head
+    (2, 32, 8, [1000, 257], 1000, 8),    # G = 4 x 8 tokens
+    (2, 32, 1, [700, 2], 704, 2),        # MQA, G = 32 x 2
+    (3, 16, 2, [300, 129, 4], 300, 4),   # G = 8 x 4
+    (1, 32, 1, [260], 260, 5),           # 160 rows: two row blocks
+]
+
+
+@pytest.mark.parametrize("shape", MULTI, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}n{s[5]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_e5m2_multi_token_matches_oracle(m, shape, splits):
+    """Several new tokens per sequence (the verification pass) over an e5m2
+    cache, on the tcgen05 kernel's fp8 form: the appended codes bit for bit,
+    outputs and lse against the oracle's decode_step_multi_e5m2."""
+    B, hq, hkv, lens, cap, n = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=470 + hq + n)
+    kc8, vc8 = make_e5m2_cache((B, hkv, cap), 128, seed=19 + n)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_e5m2(_codes(kc8), _codes(vc8), q, k, v, lens, w.rope_base,
+                                        1.0 / math.sqrt(w.head_dim))
+    kd, vd = kc8.to(DEV), vc8.to(DEV)
+    lay = m.layout_contiguous(kd, vd, hq)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=splits, device=DEV, n_new=n)
+    m.decode_step_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, max(lens), bufs, w.rope_base,
+                        1.0 / math.sqrt(w.head_dim), num_splits=splits)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    _check_multi(_np(bufs.out), _np(bufs.lse), kd, vd, ref, lens, w, n, what=splits)
+
+
+@pytest.mark.parametrize("window", [1, 100])
+def test_e5m2_multi_token_window(m, window):
+    n, lens = 3, [900, 50]
+    w = workload("gqa4k").with_(batch=2, h_q=32, h_kv=1, seed=481)
+    kc8, vc8 = make_e5m2_cache((2, 1, 900), 128, seed=23)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_e5m2(_codes(kc8), _codes(vc8), q, k, v, lens, w.rope_base,
+                                        1.0 / math.sqrt(128), window=window)
+    kd, vd = kc8.to(DEV), vc8.to(DEV)
+    lay = m.layout_contiguous(kd, vd, 32, window=window)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    for splits in (1, 4, 0):
+        bufs = m.DecodeBuffers.allocate(lay, 900, num_splits=splits, device=DEV, n_new=n)
+        kd.copy_(kc8.to(DEV))
+        vd.copy_(vc8.to(DEV))
+        m.decode_step_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, 900, bufs, w.rope_base,
+                            1.0 / math.sqrt(128), num_splits=splits)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        _check_multi(_np(bufs.out), _np(bufs.lse), kd, vd, ref, lens, w, n, window=window, what=(window, splits))
+
+
+PREFILL = [
+    # B, h_q, h_kv, n (prompt), prefix, capacity
+    (2, 8, 2, 5, 0, 8),
+    (2, 8, 2, 129, 0, 140),
+    (2, 8, 2, 200, 57, 260),
+    (1, 16, 1, 140, 10, 150),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL, ids=lambda c: f"B{c[0]}q{c[1]}kv{c[2]}n{c[3]}pre{c[4]}")
+def test_e5m2_prefill_matches_oracle(m, case):
+    """A prompt appended and attended causally in one pass over an e5m2 cache
+    (with and without a cached prefix): prefill is the multi-token step with n
+    = prompt length."""
+    B, hq, hkv, n, pre, cap = case
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=560 + n + pre)
+    lens = [pre + n] * B
+    kc8, vc8 = make_e5m2_cache((B, hkv, cap), 128, seed=29 + n)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_e5m2(_codes(kc8), _codes(vc8), q, k, v, lens, w.rope_base,
+                                        1.0 / math.sqrt(128))
+    kd, vd = kc8.to(DEV), vc8.to(DEV)
+    lay = m.layout_contiguous(kd, vd, hq)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=1, device=DEV, n_new=n)
+    m.prefill_step(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, max(lens), bufs, w.rope_base,
+                   1.0 / math.sqrt(128))
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    _check_multi(_np(bufs.out), _np(bufs.lse), kd, vd, ref, lens, w, n)
 
 
 def test_e5m2_full_size_sampled(m):
@@ -226,7 +337,7 @@ def test_e5m2_mqa_window_and_nan_tail(m, window):
         assert got["err"] == 0
         assert np.all(np.isfinite(got["out"]))
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (splits, window)
-        assert_lse(got["lse"], ref["q_rot"], _keys(ref, c, False), c.seq_lens, 1.0 / math.sqrt(128), "f16",
+        assert_lse(got["lse"], ref["q_rot"], _keys(ref, c, False), c.seq_lens, 1.0 / math.sqrt(128), q_fmt(c),
                    window=window, what=splits)
 
 
