@@ -597,27 +597,17 @@ def bench_ours(args):
             m.decode_step(lay, case.q_new, case.k_new, case.v_new, case.pos, case.seq_lens, max_len, bufs,
                           w.rope_base, scale, w.num_splits, variant, stream)
 
-    # the library's routing: 32 or more query rows per kv head (G x n_new) on a
-    # contiguous bf16 cache with head_dim 128 run on the tcgen05 kernel, the
-    # rest on the warp-MMA kernels; a one-token step is one launch (the append
-    # inside the attention kernel) when one block serves all of a kv head's heads
-    tc05 = (not byte and variant in (0, 2) and w.dtype == "bf16" and not w.paged and w.head_dim == 128
-            and w.group * nn >= 32)
-    # one-byte caches: the warp-MMA kernels and the one-token MQA kernels
-    # append the new token themselves as well
-    byte_mqa = byte and nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
-    fused = variant in (0, 2) and (
-        (nn == 1 and not byte and w.dtype == "bf16" and (w.group <= 128 if tc05 else w.group <= 32))
-        or (nn == 1 and byte and (w.group <= 32 or byte_mqa))
-        # several new tokens: the warp-MMA kernel (not tcgen05) for up to 8 of them
-        or (1 < nn <= 8 and not byte and w.dtype == "bf16" and not tc05 and w.group * nn <= 32))
-    # two splits of at most 64 rows per kv head on the tcgen05 kernel: the two
-    # blocks of a kv head form a cluster and merge in shared memory (no combine)
-    # (likewise the e5m2 one-token MQA kernel with two splits)
-    widen = (byte and args.cache == "fp8" and nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
-             and variant in (0, 2))
-    merged = (tc05 and splits_used == 2 and w.group * nn <= 64) or (widen and splits_used == 2)
-    launches_per_step = (1 if fused else 2) + (1 if splits_used > 1 and not merged else 0)
+    # the library's routing, as it reports it: the launches of one step and
+    # whether the append runs inside the attention launch; a split step with
+    # one launch fewer than append + attention + combine merged its splits
+    # inside the attention launch
+    launches_per_step, fused = m.step_launches(lay, max_len, w.num_splits, variant, nn)
+    assert launches_per_step > 0, "the library refuses this step"
+    merged = splits_used > 1 and launches_per_step == (1 if fused else 2)
+    # 32 or more query rows per kv head (G x n_new) on a contiguous cache with
+    # head_dim 128 run on the tcgen05 kernel (bf16; e5m2 with several tokens)
+    tc05 = (variant in (0, 2) and not w.paged and w.head_dim == 128 and w.group * nn >= 32
+            and (w.dtype == "bf16" and not byte or args.cache == "fp8" and nn > 1))
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
     sampler = ClockSampler(gpu_index_for(local))
@@ -774,7 +764,9 @@ def bench_ours(args):
              and args.window == 0 and args.variant == 0 and not args.no_workloads)
     workloads = measure_workloads(m, dev, stream, max(50, K), sampler, peak) if sweep else None
     sampler.stop()
-    if byte:
+    if tc05:
+        kernel_name = "attn_tc05_kernel"
+    elif byte:
         heads_kernel = w.paged and w.page_size in (16, 32) and w.group <= 16 and w.h_kv % 2 == 0
         # one new token and 32 query heads per kv head on tcgen05: uint8 with
         # the keys on the MMA rows, e5m2 with the heads on the rows and the
@@ -782,8 +774,6 @@ def bench_ours(args):
         keys_kernel = nn == 1 and 16 < w.group <= 32 and not w.paged and w.head_dim == 128
         kernel_name = (("attn_tc05_keys_kernel" if args.cache == "u8" else "attn_tc05_widen_kernel") if keys_kernel else
                        "decode_u8_heads_kernel" if heads_kernel else "decode_u8_kernel")
-    elif tc05:
-        kernel_name = "attn_tc05_kernel"
     elif variant in (0, 2) and w.dtype == "bf16":
         heads_kernel = (w.paged and w.page_size == 16 and w.head_dim == 128 and w.group <= 16 and w.h_kv % 2 == 0
                         and nn == 1)

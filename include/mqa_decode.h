@@ -317,7 +317,12 @@ MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, con
  *   MQA_DEVERR_SEQ_LEN. The (token, query head) pairs of a kv head are the
  *   rows of one MMA tile set, so the K/V bytes are read once for all n_new
  *   tokens.
- * mqa_decode_step_multi: the two calls on one stream, pos[b] = L - n_new.
+ * mqa_decode_step_multi: the two calls on one stream, pos[b] = L - n_new; ONE
+ *   launch (plus the combine when it splits and does not merge in a cluster)
+ *   when the attention kernel takes the append over -- bf16 cache, one block
+ *   for all (token, head) rows of a kv head: the warp-MMA kernel with n_new
+ *   <= 8 and G n_new <= 32, the tcgen05 kernel with n_new <= 16 and G n_new
+ *   <= 128 -- with the cache rows bit for bit those of the two calls.
  * 1 <= n_new <= 32 for the attention (kv_append_rope_multi takes any n_new;
  * longer runs of new tokens go to gqa_prefill_attention). n_new > 1 runs on
  * tensor cores over a bf16 cache, or over a MQA_FP8_E5M2 cache that is
@@ -383,6 +388,16 @@ MQA_API int32_t mqa_choose_splits(const mqa_kv_layout* layout, int32_t max_seq_l
  * count (num_splits = 0: the count mqa_choose_splits returns); 0 when the call
  * does not split. */
 MQA_API size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t num_splits, int32_t variant);
+
+/* Kernel launches one mqa_decode_step_multi call (n_new = 1: mqa_decode_step)
+ * makes for these arguments: 1 when the attention kernel appends the new
+ * tokens itself and needs no combine, 2 for append + attention or attention +
+ * combine, 3 for all three; -1 when the call would be refused. If
+ * fused_append is not NULL it receives 1 when the append runs inside the
+ * attention launch. Host only, no device work. (The library's own routing,
+ * not an operation of the pages.) */
+MQA_API int32_t mqa_step_launches(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len, int32_t num_splits,
+                                  int32_t variant, int32_t* fused_append);
 
 /* Static description of a status code. */
 MQA_API const char* mqa_status_string(mqa_status status);

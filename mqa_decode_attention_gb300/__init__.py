@@ -44,6 +44,7 @@ __all__ = [
     "splitkv_combine",
     "choose_splits",
     "workspace_size",
+    "step_launches",
     "decode_step",
     "decode_step_multi",
     "kv_append_rope_multi",
@@ -192,6 +193,17 @@ def workspace_size(layout: KVLayout, max_seq_len: int, num_splits: int, variant:
                    n_new: int = 1) -> int:
     return int(library().mqa_workspace_size_multi(ctypes.byref(layout), int(n_new), int(max_seq_len),
                                                   int(num_splits), int(variant)))
+
+
+def step_launches(layout: KVLayout, max_seq_len: int, num_splits: int = 0, variant: int = MQA_VARIANT_AUTO,
+                  n_new: int = 1) -> tuple[int, bool]:
+    """(kernel launches of one decode step, whether the append runs inside the
+    attention launch) through ``mqa_step_launches``; (-1, False) when the step
+    would be refused."""
+    fused = ctypes.c_int32(0)
+    n = int(library().mqa_step_launches(ctypes.byref(layout), int(n_new), int(max_seq_len), int(num_splits),
+                                        int(variant), ctypes.byref(fused)))
+    return n, bool(fused.value)
 
 
 @dataclass

@@ -93,6 +93,7 @@ _PROTOTYPES = {
     ),
     "mqa_choose_splits_multi": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32]),
     "mqa_workspace_size_multi": (ctypes.c_size_t, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32, c_i32]),
+    "mqa_step_launches": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32)]),
     "mqa_choose_splits": (c_i32, [ctypes.POINTER(KVLayout), c_i32, c_i32]),
     "mqa_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(KVLayout), c_i32, c_i32, c_i32]),
     "mqa_status_string": (ctypes.c_char_p, [c_i32]),

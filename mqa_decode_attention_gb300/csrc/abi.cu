@@ -148,7 +148,6 @@ int head_blocks(const mqa_kv_layout* L, const KernelShape& ks, int n_new = 1) {
   return (rows + ks.heads_per_cta - 1) / ks.heads_per_cta;
 }
 
-constexpr int kMaxNewTokens = 32;
 
 // Multi-token decode runs on the bf16 tensor-core kernel only.
 bool multi_supported(const mqa_kv_layout* L, int variant, int n_new) {
@@ -471,12 +470,19 @@ bool fusable(const mqa_kv_layout* L, int variant) {
   return head_blocks(L, decode_shape(L, variant)) == 1;
 }
 
-// Several new tokens per sequence (bf16 cache): the warp-MMA kernel takes the
-// appends over when one block sees all (token, head) rows of its kv head and
-// the tokens' cos / sin tables fit (at most kMaxFusedNewTokens).
+// Several new tokens per sequence (bf16 cache): the attention kernel takes the
+// appends over when one block sees all (token, head) rows of its kv head --
+// tcgen05: at most 128 rows; warp-MMA: one head block, and the tokens' cos /
+// sin tables fit (at most kMaxFusedNewTokens).
 bool fusable_multi(const mqa_kv_layout* L, int variant, int n_new) {
-  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16) return false;
-  if (n_new < 2 || n_new > kMaxFusedNewTokens || use_tc05(L, variant, n_new)) return false;
+  if (variant != MQA_VARIANT_TENSOR_CORE || L->cache_dtype != MQA_BF16 || n_new < 2) return false;
+  // tcgen05: one row block of 128 (token, head) rows, and at most
+  // kMaxFusedNewTokensTc05 tokens: the block's append warp turns every new
+  // key pair with an fp64-reduced angle, which past that outlasts the stream
+  // of keys it hides behind (gqa4k, step vs append + attention: n = 8 90.8 vs
+  // 100.0 us, n = 16 100.4 vs 106.4, n = 32 148 vs 113.6)
+  if (use_tc05(L, variant, n_new)) return (L->h_q / L->h_kv) * n_new <= 128 && n_new <= kMaxFusedNewTokensTc05;
+  if (n_new > kMaxFusedNewTokens) return false;
   return head_blocks(L, decode_shape(L, variant, n_new), n_new) == 1;
 }
 
@@ -594,7 +600,7 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
     t.err = err_word;
     t.early = early;
     t.wait_ns = p.wait_ns;
-    if (rope != nullptr && rope->fuse_append && n_new == 1) {
+    if (rope != nullptr && rope->fuse_append) {  // (fusable: one row block)
       t.fuse = 1;
       t.early = 0;  // nothing of this step precedes the launch
       t.q_new = rope->q_new;
@@ -855,6 +861,37 @@ size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_new, int3
 
 size_t mqa_workspace_size(const mqa_kv_layout* layout, int32_t max_seq_len, int32_t num_splits, int32_t variant) {
   return mqa_workspace_size_multi(layout, 1, max_seq_len, num_splits, variant);
+}
+
+int32_t mqa_step_launches(const mqa_kv_layout* layout, int32_t n_new, int32_t max_seq_len, int32_t num_splits,
+                          int32_t variant, int32_t* fused_append) {
+  if (check_layout(layout) != MQA_OK || max_seq_len < 1 || max_seq_len > token_limit(layout) || num_splits < 0)
+    return -1;
+  if (variant < MQA_VARIANT_AUTO || variant > MQA_VARIANT_TENSOR_CORE) return -1;
+  if (n_new < 1 || n_new > kMaxNewTokens || max_seq_len < n_new) return -1;
+  const int v = resolve_variant(layout, variant);
+  if (!variant_supports(v, layout->cache_dtype) || !multi_supported(layout, v, n_new)) return -1;
+  const int req = num_splits == 0 ? choose_splits(layout, max_seq_len, v, n_new) : num_splits;
+  int splits, chunk;
+  split_plan(req, read_span(layout, max_seq_len, n_new), &splits, &chunk);
+  // the decisions step_impl and attention_impl take
+  const bool fused = (n_new == 1 && fusable(layout, v)) || fusable_multi(layout, v, n_new);
+  bool merged = false;
+  if (splits > 1) {
+    Tc05Params t;
+    std::memset(&t, 0, sizeof(t));
+    t.group = layout->h_q / layout->h_kv;
+    t.n_new = n_new;
+    t.num_splits = splits;
+    t.row_blocks = (t.group * n_new + 127) / 128;
+    if (use_tc05(layout, v, n_new))
+      merged = tc05_merges_splits(t);
+    else if (v == MQA_VARIANT_TENSOR_CORE && layout->cache_dtype == MQA_FP8_E5M2 &&
+             tc05_keys_applies(t.group, n_new, layout->head_dim, layout->paged))
+      merged = tc05_widen_merges_splits(t);
+  }
+  if (fused_append) *fused_append = fused ? 1 : 0;
+  return (fused ? 1 : 2) + (splits > 1 && !merged ? 1 : 0);
 }
 
 mqa_status splitkv_combine(const float* o_part, const float* lse_part, int32_t batch, int32_t h_q,

@@ -33,7 +33,7 @@
 // (TMA, 3 stages each; a K stage is released when its S is computed, a V
 // stage when its PV is), 6 MMA issue (one thread) and tensor-memory
 // allocation, 7 the fused step's append (its own warp, so that the block
-// that writes the new row publishes Q as early as the others).
+// that writes the new rows publishes Q as early as the others).
 #include <cuda_bf16.h>
 
 #include "../../include/mqa_decode.h"
@@ -110,6 +110,26 @@ __device__ __noinline__ uint2 e4m3_split4_once(float a, float b, float c, float 
   return r;
 }
 
+// The two stages of rope_k_bf16 for one packed bf16 pair, out of line: the
+// fused step's append runs them a few times per block, and inlined copies
+// would sit as cold code beside the softmax loop. The fp32 stage returns
+// false when it leaves the rounding to the fp64 stage.
+__device__ __noinline__ bool rope_k_packed_fast(uint32_t kp, double ang, uint32_t* out) {
+  const float x = bf16lo_to_f32(kp), y = bf16hi_to_f32(kp);
+  const float s = fabsf(x) + fabsf(y);
+  if (!(s >= 0x1p-100f && s <= 1e37f)) return false;
+  float sf, cf;
+  sincosf(static_cast<float>(ang), &sf, &cf);
+  __nv_bfloat162 r;
+  if (!rope_k_bf16_fast(x, y, cf, sf, &r)) return false;
+  *out = *reinterpret_cast<const uint32_t*>(&r);
+  return true;
+}
+__device__ __noinline__ uint32_t rope_k_packed_fp64(uint32_t kp, double ang) {
+  const __nv_bfloat162 r = rope_k_bf16_fp64(bf16lo_to_f32(kp), bf16hi_to_f32(kp), ang);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of bf16 element (r, col) of a tile
   const int half = col >> 6, chunk = (col & 63) >> 3;
   return half * 16384 + r * 128 + ((chunk ^ (r & 7)) << 4) + (col & 7) * 2;
@@ -124,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const Tc05Params p) {
   static_assert(!CL || PARTS > 1, "the cluster merge takes replicated rows (R <= 64)");
-  static_assert(!(FUSE && F8), "the fused one-token step is bf16 only");
+  static_assert(!(FUSE && F8), "the fused step is bf16 only");
   using Y = Lay<F8>;
   constexpr int kStages = Y::kStages, kTileBytes = Y::kTileBytes, kQOff = Y::kQOff, kKOff = Y::kKOff,
                 kVOff = Y::kVOff, kBarOff = Y::kBarOff, kXOff = Y::kXOff;
@@ -273,12 +293,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = kend > kstart ? (kend - kstart + kBN - 1) / kBN : 0;  // key tiles of this block
   auto tile_key0 = [&](int it) { return kstart + it * kBN; };
   const bool split_out = S > 1 && !CL;
-  // fused step: the split whose token range holds the new token's position
-  // (else split 0) appends its k / v row
+  // fused step: new token i (position apos + i) is appended by the split whose
+  // token range holds it (else split 0), so that no block reads a row another
+  // block writes (a fused step has one row block); a_first is this block's
+  // first such token, a_pos its position
   const int tbase = (t_lo / 64) * 64;
-  const bool writer = FUSE && split == ((apos - tbase >= 0 && (apos - tbase) / p.chunk < S) ? (apos - tbase) / p.chunk : 0);
+  auto owner = [&](int i) {
+    const int o = apos + i - tbase;
+    return (o >= 0 && o / p.chunk < S) ? o / p.chunk : 0;
+  };
+  int a_first = -1;
+  if constexpr (FUSE) {
+    for (int i = n - 1; i >= 0; --i)
+      if (owner(i) == split) a_first = i;
+  }
+  const bool writer = a_first >= 0;
+  const int a_pos = apos + (writer ? a_first : 0);
+  // the new tokens' cache rows exactly as the append kernel writes them: k
+  // pair i turned and rounded once to bf16 (rope_k_bf16, equal to the fp64
+  // rotation), v copied; a position outside the cache is reported and nothing
+  // is written there. Then fenced for this block's TMA loads (async proxy).
+  // The rows of kU tokens are requested together (one memory round trip per
+  // kU tokens, not per token), and the pairs the fp32 stage of rope_k_bf16
+  // leaves open are collected and finished in fp64 at the end, every lane at
+  // once: a lane's open pair no longer stalls the whole warp on its own.
+  auto append_rows = [&]() {
+    constexpr int kU = 2;  // (mqa8k, same-box A/B: 2 tokens 56.1 / 48.4 us isolated / back to back, 4: 61.4 / 49.3)
+    __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache));
+    __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache));
+    const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(p.k_new);
+    const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(p.v_new);
+    bool bad_pos = false;
+    static_assert(2 * kMaxNewTokens <= 64, "the open-pair mask");
+    uint64_t open = 0;  // bit 2 i + h: pair lane + 32 h of new token i left to the fp64 stage
+    auto dst_of = [&](int i) { return ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos + i) * kD; };
+    auto src_of = [&](int i) { return ((static_cast<long long>(b) * n + i) * p.h_kv + j) * kD; };
+    for (int i0 = a_first; i0 < n; i0 += kU) {
+      uint32_t kraw[kU][kD / 64], vraw[kU][kD / 64];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u;
+        if (i >= n || owner(i) != split || apos + i < 0 || apos + i >= p.capacity) continue;
+        const long long src = src_of(i);
+#pragma unroll
+        for (int h = 0; h < kD / 64; ++h) {  // pairs lane, lane + 32
+          const int pi = lane + 32 * h;
+          kraw[u][h] = *reinterpret_cast<const uint32_t*>(kn + src + 2 * pi);
+          vraw[u][h] = *reinterpret_cast<const uint32_t*>(vn + src + 2 * pi);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u, ap = apos + i;
+        if (i >= n || owner(i) != split) continue;
+        if (ap < 0 || ap >= p.capacity) {
+          bad_pos = true;
+          continue;
+        }
+        const long long dst = dst_of(i);
+#pragma unroll
+        for (int h = 0; h < kD / 64; ++h) {
+          const int pi = lane + 32 * h;
+          const double ang = reduce_two_pi(static_cast<double>(ap) * p.theta[pi]);
+          uint32_t kr;
+          if (rope_k_packed_fast(kraw[u][h], ang, &kr))
+            *reinterpret_cast<uint32_t*>(kc + dst + 2 * pi) = kr;
+          else
+            open |= 1ull << (2 * i + h);
+          *reinterpret_cast<uint32_t*>(vc + dst + 2 * pi) = vraw[u][h];
+        }
+      }
+    }
+    while (__any_sync(0xffffffffu, open != 0)) {
+      if (open != 0) {
+        const int bit = __ffsll(static_cast<long long>(open)) - 1;
+        open &= open - 1;
+        const int i = bit >> 1, pi = lane + 32 * (bit & 1);
+        const uint32_t kp = *reinterpret_cast<const uint32_t*>(kn + src_of(i) + 2 * pi);
+        const double ang = reduce_two_pi(static_cast<double>(apos + i) * p.theta[pi]);
+        *reinterpret_cast<uint32_t*>(kc + dst_of(i) + 2 * pi) = rope_k_packed_fp64(kp, ang);
+      }
+    }
+    if (bad_pos && lane == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+  };
   if (T == 0) {
-    // no key of this split reaches these rows: an empty partial (weight 0 in the combine)
+    // no key of this split reaches these rows: an empty partial (weight 0 in
+    // the combine); a fused step's rows owned by this split are still written
+    if (FUSE && writer && warp == 7) append_rows();
     grid_dependency_wait();
     if constexpr (CL) {
       cl_empty();
@@ -361,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // runs, the ring's first fill), none holding a row that the preceding
       // launch or this block's append writes
       const int npre = p.early ? kStages : kPreTiles;
-      const int lim = p.early ? Lp : (writer ? apos : 0x7fffffff);
+      const int lim = p.early ? Lp : (writer ? a_pos : 0x7fffffff);
       for (; it < T && it < npre && tile_key0(it) + kBN <= lim; ++it)
         if (lane == 0) issue(it);
     }
@@ -380,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           grid_dependency_wait();
           waited = true;
         }
-        if (!appended && apos < tile_key0(it) + kBN) {  // ... written by this block's append warp
+        if (!appended && a_pos < tile_key0(it) + kBN) {  // ... written by this block's append warp
           if (!mbar_wait(bar(kAppended), 0, p.wait_ns)) {
             fail(1);
             break;
@@ -482,37 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 7) {
     // ---------------------------------------------- append (fused step only)
-    // the new token's cache rows exactly as the append kernel writes them: k
-    // pair i turned and rounded once to bf16 (rope_k_bf16, equal to the fp64
-    // rotation), v copied; a position outside the cache is reported and
-    // nothing is written. The loaders wait for it only before the tile that
-    // holds the row.
+    // The loaders wait for it only before the first tile that holds one of
+    // this block's rows.
     if (FUSE && writer) {
-      if (apos >= 0 && apos < p.capacity) {
-        const long long src = (static_cast<long long>(b) * p.h_kv + j) * kD;
-        const long long dst = ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos) * kD;
-        uint32_t kraw[kD / 64], vraw[kD / 64];
-#pragma unroll
-        for (int h = 0; h < kD / 64; ++h) {  // pairs lane, lane + 32
-          const int i = lane + 32 * h;
-          kraw[h] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.k_new) + src + 2 * i);
-          vraw[h] = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.v_new) + src + 2 * i);
-        }
-#pragma unroll
-        for (int h = 0; h < kD / 64; ++h) {
-          const int i = lane + 32 * h;
-          const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[i]);
-          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + dst + 2 * i) =
-              rope_k_bf16(bf16lo_to_f32(kraw[h]), bf16hi_to_f32(kraw[h]), ang);
-          *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + dst + 2 * i) =
-              vraw[h];
-        }
-      } else if (lane == 0) {
-        atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
-      }
-      // this block's TMA loads (async proxy) read the rows back
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      __syncwarp();
+      append_rows();
       if (lane == 0) mbar_arrive(bar(kAppended));
     }
   } else {
@@ -531,22 +607,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.early) grid_dependency_wait();
       float4 qv[kD / 4];
       if constexpr (FUSE) {
-        // fused step: q_new (bf16) rotated here, pair i by the fp32 cosine /
-        // sine of the fp64-reduced angle pos * theta_i, as the append kernel
-        // forms q_rot
-        __shared__ float s_cs[kD];
+        // fused step: q_new (bf16) rotated here, pair i of new token t by the
+        // fp32 cosine / sine of the fp64-reduced angle (apos + t) theta_i, as
+        // the append kernel forms q_rot. The tokens' tables [n][cos | sin]
+        // (row stride kD + 1: the rows of a warp read different banks) sit in
+        // the last K stage, which no tile request reaches before the Q rows
+        // have landed (named barrier 2).
+        static_assert(kPreTiles < kStages && kMaxNewTokens * (kD + 1) * 4 <= kTileBytes, "fused cos / sin tables");
+        float* cst = reinterpret_cast<float*>(smem + kKOff + (kStages - 1) * kTileBytes);
         const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_new) + grow_row * kD);
         uint4 raw[kD / 8];
 #pragma unroll
         for (int c = 0; c < kD / 8; ++c) raw[c] = live ? qn[c] : make_uint4(0u, 0u, 0u, 0u);
-        if (tid < kD / 2) {
-          const double ang = reduce_two_pi(static_cast<double>(apos) * p.theta[tid]);
+        for (int e = tid; e < n * (kD / 2); e += kBM) {
+          const int t = e / (kD / 2), pi = e - t * (kD / 2);
+          const double ang = reduce_two_pi(static_cast<double>(apos + t) * p.theta[pi]);
           float sf, cf;
           sincosf(static_cast<float>(ang), &sf, &cf);
-          s_cs[tid] = cf;
-          s_cs[kD / 2 + tid] = sf;
+          cst[t * (kD + 1) + pi] = cf;
+          cst[t * (kD + 1) + kD / 2 + pi] = sf;
         }
-        named_bar_sync(3, kBM);  // the cos / sin table
+        named_bar_sync(3, kBM);  // the cos / sin tables
+        const float* tcs = cst + min(gi, n - 1) * (kD + 1);  // this row's token
 #pragma unroll
         for (int c = 0; c < kD / 8; ++c) {
           const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
@@ -555,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             const int pi = 4 * c + e;  // pair (2 pi, 2 pi + 1)
             const float x = bf16lo_to_f32(w4[e]), y = bf16hi_to_f32(w4[e]);
-            const float cs = s_cs[pi], sn = s_cs[kD / 2 + pi];
+            const float cs = tcs[pi], sn = tcs[kD / 2 + pi];
             rv[2 * e] = x * cs - y * sn;
             rv[2 * e + 1] = x * sn + y * cs;
           }

@@ -19,7 +19,9 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 void record_cuda_error(cudaError_t e);
 
 constexpr int kTile = 64;          // tokens per pipeline stage of the decode kernels
-constexpr int kMaxFusedNewTokens = 8;  // new tokens per sequence a fused multi-token step takes
+constexpr int kMaxNewTokens = 32;      // new tokens per sequence the multi-token attention takes
+constexpr int kMaxFusedNewTokens = 8;  // new tokens per sequence a fused warp-MMA multi-token step takes
+constexpr int kMaxFusedNewTokensTc05 = 16;  // ... a fused tcgen05 multi-token step takes
 constexpr int kMaxHalfDim = 64;    // RoPE frequencies held in the append kernel's parameters
 constexpr int kDtypeBf16 = 0;
 constexpr int kDtypeF32 = 1;

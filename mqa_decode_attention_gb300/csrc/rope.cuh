@@ -43,23 +43,26 @@ __device__ __forceinline__ void rope_cos_sin(int pos, double theta, double* c, d
 // arithmetic < 4e-16 s: |r32 - r64| < 4.8e-7 s. The bound used is 8e-7 s.
 // Rounding to nearest is monotonic, so when r32 - bound and r32 + bound
 // (each rounded outward) round to the same bf16, r64 rounds to it as well.
-__device__ __forceinline__ __nv_bfloat162 rope_k_bf16(float x, float y, double ang) {
+//
+// rope_k_bf16_fast is the fp32 stage alone, given cf / sf = the fp32 cosine /
+// sine of the reduced angle rounded to fp32: true, with *r set, when it
+// decides the rounding; rope_k_bf16_fp64 the fp64 stage; rope_k_bf16 both.
+__device__ __forceinline__ bool rope_k_bf16_fast(float x, float y, float cf, float sf, __nv_bfloat162* r) {
   const float s = fabsf(x) + fabsf(y);
-  if (s >= 0x1p-100f && s <= 1e37f) {
-    float sf, cf;
-    sincosf(static_cast<float>(ang), &sf, &cf);
-    const float xr = fmaf(x, cf, -(y * sf));
-    const float yr = fmaf(x, sf, y * cf);
-    const float e = s * 8e-7f;
-    const __nv_bfloat16 xl = __float2bfloat16_rn(__fsub_rd(xr, e)), xh = __float2bfloat16_rn(__fadd_ru(xr, e));
-    const __nv_bfloat16 yl = __float2bfloat16_rn(__fsub_rd(yr, e)), yh = __float2bfloat16_rn(__fadd_ru(yr, e));
-    if (__bfloat16_as_ushort(xl) == __bfloat16_as_ushort(xh) && __bfloat16_as_ushort(yl) == __bfloat16_as_ushort(yh)) {
-      __nv_bfloat162 r;
-      r.x = xl;
-      r.y = yl;
-      return r;
-    }
-  }
+  if (!(s >= 0x1p-100f && s <= 1e37f)) return false;
+  const float xr = fmaf(x, cf, -(y * sf));
+  const float yr = fmaf(x, sf, y * cf);
+  const float e = s * 8e-7f;
+  const __nv_bfloat16 xl = __float2bfloat16_rn(__fsub_rd(xr, e)), xh = __float2bfloat16_rn(__fadd_ru(xr, e));
+  const __nv_bfloat16 yl = __float2bfloat16_rn(__fsub_rd(yr, e)), yh = __float2bfloat16_rn(__fadd_ru(yr, e));
+  if (__bfloat16_as_ushort(xl) != __bfloat16_as_ushort(xh) || __bfloat16_as_ushort(yl) != __bfloat16_as_ushort(yh))
+    return false;
+  r->x = xl;
+  r->y = yl;
+  return true;
+}
+
+__device__ __forceinline__ __nv_bfloat162 rope_k_bf16_fp64(float x, float y, double ang) {
   double c, sn;
   sincos(ang, &sn, &c);
   const double xd = x, yd = y;
@@ -67,6 +70,17 @@ __device__ __forceinline__ __nv_bfloat162 rope_k_bf16(float x, float y, double a
   r.x = __double2bfloat16(__dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, sn)));
   r.y = __double2bfloat16(__dadd_rn(__dmul_rn(xd, sn), __dmul_rn(yd, c)));
   return r;
+}
+
+__device__ __forceinline__ __nv_bfloat162 rope_k_bf16(float x, float y, double ang) {
+  __nv_bfloat162 r;
+  const float s = fabsf(x) + fabsf(y);
+  if (s >= 0x1p-100f && s <= 1e37f) {
+    float sf, cf;
+    sincosf(static_cast<float>(ang), &sf, &cf);
+    if (rope_k_bf16_fast(x, y, cf, sf, &r)) return r;
+  }
+  return rope_k_bf16_fp64(x, y, ang);
 }
 
 }  // namespace mqa

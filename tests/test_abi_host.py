@@ -144,3 +144,36 @@ def test_invalid_layout_queries(lib):
     assert lib.mqa_choose_splits(None, 10, 0) == -1
     assert lib.mqa_choose_splits(ctypes.byref(_layout(h_kv=3)), 10, 0) == -1
     assert lib.mqa_workspace_size(ctypes.byref(_layout()), 0, 1, 0) == 0
+
+
+@pytest.mark.parametrize("hq,hkv,n,splits,expect,fused", [
+    (32, 8, 1, 1, 1, True),     # G = 4, one token: warp-MMA, append inside
+    (32, 8, 1, 3, 2, True),     # ... plus the combine
+    (32, 1, 1, 2, 1, True),     # MQA on tcgen05: two splits merged in a cluster
+    (32, 1, 1, 3, 2, True),
+    (32, 8, 8, 1, 1, True),     # 32 (token, head) rows: tcgen05, append inside
+    (32, 8, 8, 2, 1, True),     # ... two splits merged
+    (32, 8, 8, 4, 2, True),
+    (32, 8, 16, 2, 1, True),    # 64 rows, two splits merged
+    (32, 8, 32, 1, 2, False),   # 128 rows, but 32 tokens: the append launch is faster
+    (64, 8, 32, 1, 2, False),   # 256 rows: two row blocks, separate append
+    (64, 8, 32, 3, 3, False),
+    (32, 8, 2, 1, 1, True),     # 8 rows: warp-MMA fused multi-token
+    (32, 8, 16, 1, 1, True),
+    (64, 8, 16, 1, 1, True),    # 128 rows, 16 tokens
+])
+def test_step_launches(lib, hq, hkv, n, splits, expect, fused):
+    """The launch count of one step follows the routing the header states."""
+    lay = _layout(batch=2, h_q=hq, h_kv=hkv, capacity=4096)
+    f = ctypes.c_int32(-1)
+    assert lib.mqa_step_launches(ctypes.byref(lay), n, 4096, splits, 2, ctypes.byref(f)) == expect
+    assert bool(f.value) == fused
+
+
+def test_step_launches_refused(lib):
+    f = ctypes.c_int32(0)
+    assert lib.mqa_step_launches(None, 1, 10, 1, 2, ctypes.byref(f)) == -1
+    assert lib.mqa_step_launches(ctypes.byref(_layout()), 33, 4096, 1, 2, None) == -1
+    assert lib.mqa_step_launches(ctypes.byref(_layout(capacity=4096)), 2, 4096, 1, 1, None) == -1  # CUDA cores, n > 1
+    u8 = _layout(cache_dtype=_abi.MQA_U8, k_scale_zero=FAKE, v_scale_zero=FAKE, capacity=4096)
+    assert lib.mqa_step_launches(ctypes.byref(u8), 2, 4096, 1, 2, None) == -1  # several tokens over uint8

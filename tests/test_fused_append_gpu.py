@@ -229,20 +229,17 @@ def test_fused_append_byte_cache_paged(m, cache):
     assert (qa - qb).abs().max().item() <= 1e-5 * (1 + qb.abs().max().item())
 
 
-@pytest.mark.parametrize("n", [2, 4, 7])
-@pytest.mark.parametrize("splits", [1, 3])
-def test_fused_append_multi_token(m, n, splits):
-    """Several new tokens per sequence on the warp-MMA kernel: each split's
-    block appends the new rows inside its own token range, so sequences whose
-    new rows straddle a split boundary (lengths 705.., 1409..) are written by
-    two blocks; the cache must equal the append kernel's bit for bit."""
-    w = workload("gqa4k").with_(batch=12, h_q=32, h_kv=8, seed=121 + n)
+def fused_multi_case(m, h_q, h_kv, n, splits, seed):
+    """The fused multi-token step against the separate append (cache bits,
+    q_rot) and then against the oracle. Sequences whose new rows straddle a
+    split boundary (lengths 705.., 1409..) are written by two blocks."""
+    w = workload("gqa4k").with_(batch=12, h_q=h_q, h_kv=h_kv, seed=seed)
     cap = 2048
     lens = torch.tensor([705, 706, 707, 1409, 1410, 2048, n, 64 + n - 1, 1000, 129, 700, 1500], dtype=torch.int32)
     c = make_contiguous_case(w, "cpu", seq_lens=lens, capacity=cap)
-    gen = torch.Generator().manual_seed(122 + n)
+    gen = torch.Generator().manual_seed(seed + 1)
     q = torch.randn((w.batch, n, w.h_q, w.head_dim), generator=gen).to(torch.bfloat16)
-    k = hard_keys((w.batch, n, w.h_kv, w.head_dim), 123 + n)
+    k = hard_keys((w.batch, n, w.h_kv, w.head_dim), seed + 2)
     v = torch.randn((w.batch, n, w.h_kv, w.head_dim), generator=gen).to(torch.bfloat16)
     pos = (lens - n).to(torch.int32)
     results = []
@@ -280,3 +277,20 @@ def test_fused_append_multi_token(m, n, splits):
     assert np.max(np.abs(out - ref["out"])) <= 2e-2
     assert np.max(np.abs(lse - ref["lse"])) <= 2e-2
     assert_lse(lse, ref["q_rot"], ref["k_cache"], lens, 1.0 / math.sqrt(w.head_dim), "bf16")
+
+
+@pytest.mark.parametrize("n", [2, 4, 7])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fused_append_multi_token(m, n, splits):
+    """Several new tokens per sequence on the warp-MMA kernel (G n < 32)."""
+    fused_multi_case(m, 32, 8, n, splits, 121 + n)
+
+
+@pytest.mark.parametrize("h_q, h_kv, n", [(32, 8, 8), (32, 8, 16), (64, 8, 16), (32, 1, 2), (32, 1, 4)],
+                         ids=lambda v: str(v))
+@pytest.mark.parametrize("splits", [1, 2, 3])
+def test_fused_append_multi_token_tc05(m, h_q, h_kv, n, splits):
+    """Several new tokens per sequence on the tcgen05 kernel (32 <= G n <=
+    128, n <= 16: one launch, the kernel's append warp writing the rows of its
+    split; G n <= 64 at two splits merges them in a two-block cluster)."""
+    fused_multi_case(m, h_q, h_kv, n, splits, 131 + n + h_q)
