@@ -604,10 +604,12 @@ def bench_ours(args):
     launches_per_step, fused = m.step_launches(lay, max_len, w.num_splits, variant, nn)
     assert launches_per_step > 0, "the library refuses this step"
     merged = splits_used > 1 and launches_per_step == (1 if fused else 2)
-    # 32 or more query rows per kv head (G x n_new) on a contiguous cache with
-    # head_dim 128 run on the tcgen05 kernel (bf16; e5m2 with several tokens)
-    tc05 = (variant in (0, 2) and not w.paged and w.head_dim == 128 and w.group * nn >= 32
-            and (w.dtype == "bf16" and not byte or args.cache == "fp8" and nn > 1))
+    # 32 or more query rows per kv head (G x n_new) with head_dim 128 run on the
+    # tcgen05 kernel: contiguous bf16, paged bf16 with several tokens,
+    # contiguous e5m2 with several tokens
+    tc05 = (variant in (0, 2) and w.head_dim == 128 and w.group * nn >= 32
+            and ((w.dtype == "bf16" and not byte and (not w.paged or nn > 1))
+                 or (args.cache == "fp8" and not w.paged and nn > 1)))
 
     # warm-up (at least W steps and at least ~1 s, so the clock sampler sees load)
     sampler = ClockSampler(gpu_index_for(local))
@@ -924,13 +926,19 @@ def bench_prefill(args):
     torch.cuda.set_device(dev)
     n = args.prefill
     w = workload(args.workload).with_(batch=args.batch or 8)
-    case = make_contiguous_case(w, dev, seq_lens=torch.full((w.batch,), n, dtype=torch.int32), capacity=n)
+    full = torch.full((w.batch,), n, dtype=torch.int32)
+    if w.paged:  # the prompt's rows go to the pages the (permuted) block table names
+        pc = make_paged_case(w, dev, seq_lens=full)
+        lay = m.layout_paged(pc.k_pool, pc.v_pool, pc.block_table, w.h_q)
+        lens = pc.seq_lens
+    else:
+        case = make_contiguous_case(w, dev, seq_lens=full, capacity=n)
+        lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q)
+        lens = case.seq_lens
     q = normal((w.batch, n, w.h_q, w.head_dim), w.seed, S_QM, w.dtype, dev)
     k = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_KM, w.dtype, dev)
     v = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_VM, w.dtype, dev)
-    lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q)
     bufs = m.DecodeBuffers.allocate(lay, n, num_splits=1, device=dev, n_new=n)
-    lens = case.seq_lens
     pos = (lens - n).to(torch.int32)
     scale = 1.0 / math.sqrt(w.head_dim)
     stream = torch.cuda.current_stream()
@@ -986,7 +994,9 @@ def bench_prefill(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v; empty cache before the prompt)",
         "config": {"workload": f"prefill: batch {w.batch}, {n}-token prompts, H_q {w.h_q}, H_kv {w.h_kv}, "
-                               f"head_dim {w.head_dim}, causal, RoPE base 10000",
+                               f"head_dim {w.head_dim}, causal, RoPE base 10000, "
+                               + (f"paged bf16 pool (page_size {w.page_size}, pages dealt by a seeded permutation)"
+                                  if w.paged else "contiguous bf16 cache"),
                    "flops_per_step": flops},
         "kernels_ms": {"mqa_prefill_step": round(ms_step, 6), "standalone_gqa_prefill_attention": round(attn_ms, 6)},
         "roofline": {"bound": "tensor", "kernel": "attn_tc05_kernel (prefill)", "achieved": round(achieved, 1),

@@ -325,7 +325,9 @@ MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, con
  *   <= 128 -- with the cache rows bit for bit those of the two calls.
  * 1 <= n_new <= 32 for the attention (kv_append_rope_multi takes any n_new;
  * longer runs of new tokens go to gqa_prefill_attention). n_new > 1 runs on
- * tensor cores over a bf16 cache, or over a MQA_FP8_E5M2 cache that is
+ * tensor cores over a bf16 cache, contiguous or paged (32 or more query rows
+ * per kv head on the tcgen05 kernel, which gathers a paged key tile page by
+ * page), or over a MQA_FP8_E5M2 cache that is
  * contiguous with head_dim 128 and at least 32 query rows per kv head
  * ((h_q / h_kv) * n_new >= 32; the tcgen05 kernel's fp8 form), and
  * MQA_ERR_UNSUPPORTED otherwise; n_new = 1 is exactly the single-token call.
@@ -358,8 +360,8 @@ MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_n
  * compute-bound). The arithmetic is that of the multi-token calls above --
  * query token i of sequence b (position L - n_new + i) attends to the keys
  * [0, L - n_new + i] (or the last W of them) -- on the tensor-memory tensor
- * cores (tcgen05): one block per (sequence, query head, 128 tokens), S and O
- * accumulated in tensor memory.
+ * cores (tcgen05): one block per (sequence, kv head, 128 (token, query head)
+ * rows), S and O accumulated in tensor memory.
  *
  * gqa_prefill_attention: q_rot [batch, n_new, h_q, 128] fp32 (from
  *   kv_append_rope_multi), seq_lens[b] = L after the append (>= n_new; L > n_new
@@ -367,9 +369,13 @@ MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_n
  *   lse_out optional [batch, n_new, h_q].
  * mqa_prefill_step: kv_append_rope_multi (pos[b] = L - n_new), then
  *   gqa_prefill_attention, on one stream.
- * Contiguous bf16 or MQA_FP8_E5M2 cache with head_dim 128 only
- * (MQA_ERR_UNSUPPORTED otherwise; e5m2 on the kernel's fp8 form described
- * with MQA_FP8_E5M2); no workspace. A bounded wait that runs out sets
+ * head_dim 128 with a bf16 cache, contiguous or paged (a key tile gathered
+ * page by page from the pool the block table names, the prompt's rows
+ * appended into its pages), or a contiguous MQA_FP8_E5M2 cache (the kernel's
+ * fp8 form described with MQA_FP8_E5M2); MQA_ERR_UNSUPPORTED otherwise. No
+ * workspace. A block-table entry outside the pool for a page the prompt
+ * attends or is appended to sets MQA_DEVERR_PAGE_RANGE (that page reads as
+ * zeros). A bounded wait that runs out sets
  * MQA_DEVERR_TIMEOUT and every later block of the launch returns at once.
  */
 MQA_API mqa_status gqa_prefill_attention(const mqa_kv_layout* layout, int32_t n_new, const float* q_rot,

@@ -121,13 +121,16 @@ DeviceInfo device_info(int dev) {
 // (MQA's G = 32, several new tokens per sequence).
 constexpr int kTc05MinRows = 32;
 
-// bf16 caches, and fp8 e5m2 caches with several new tokens per sequence (the
-// kernel's fp8 form: the code tiles enter the MMAs as they are; a one-token
-// e5m2 MQA step takes attn_tc05_widen.cu, measured faster there).
+// Contiguous bf16 caches; paged bf16 pools with several new tokens per
+// sequence (a one-token paged step keeps the warp-MMA kernels); contiguous fp8
+// e5m2 caches with several new tokens per sequence (the kernel's fp8 form: the
+// code tiles enter the MMAs as they are; a one-token e5m2 MQA step takes
+// attn_tc05_widen.cu, measured faster there).
 bool use_tc05(const mqa_kv_layout* L, int variant, int n_new) {
-  return variant == MQA_VARIANT_TENSOR_CORE && !L->paged && L->head_dim == 128 &&
-         (L->cache_dtype == MQA_BF16 || (L->cache_dtype == MQA_FP8_E5M2 && n_new > 1)) &&
-         (L->h_q / L->h_kv) * n_new >= kTc05MinRows;
+  if (variant != MQA_VARIANT_TENSOR_CORE || L->head_dim != 128) return false;
+  if ((L->h_q / L->h_kv) * n_new < kTc05MinRows) return false;
+  if (L->cache_dtype == MQA_BF16) return !L->paged || n_new > 1;
+  return L->cache_dtype == MQA_FP8_E5M2 && !L->paged && n_new > 1;
 }
 
 
@@ -374,7 +377,34 @@ bool make_u8_maps(CUtensorMap* maps, const mqa_kv_layout* L, int rows_in, int he
 
 // Tensor maps of the tcgen05 kernel's K / V tiles: bf16 tiles, or the fp8
 // kernel's code tiles (t->f8 set).
+// TMA descriptor of a paged bf16 pool for the tcgen05 kernel: dims (64 dims,
+// page rows, the two 64-dim halves, kv heads, pages), box 64 x rp x 1 x 1 x 1
+// with rp = min(page_size, 64), 128-byte swizzle: one copy per (page run,
+// half), landing at the tile's half and row offset.
+bool make_tc05_paged_map(CUtensorMap* map, void* base, const mqa_kv_layout* L) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t row_bytes = 256, ps = static_cast<cuuint64_t>(L->page_size);
+  const cuuint64_t dims[5] = {64, ps, 2, static_cast<cuuint64_t>(L->h_kv), static_cast<cuuint64_t>(L->num_pages)};
+  const cuuint64_t strides[4] = {row_bytes, 128, ps * row_bytes, static_cast<cuuint64_t>(L->h_kv) * ps * row_bytes};
+  const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(L->page_size < 64 ? L->page_size : 64), 1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool tc05_maps(const mqa_kv_layout* L, Tc05Params* t, CUtensorMap* tk, CUtensorMap* tv) {
+  if (L->paged) {
+    t->paged = 1;
+    t->page_size = L->page_size;
+    t->max_pages = L->max_pages_per_seq;
+    t->num_pages = L->num_pages;
+    t->block_table = L->block_table;
+    t->capacity = token_limit(L);
+    return make_tc05_paged_map(tk, L->k_cache, L) && make_tc05_paged_map(tv, L->v_cache, L);
+  }
   if (L->cache_dtype == MQA_FP8_E5M2) {
     CUtensorMap maps[4];
     if (!make_u8_maps(maps, L, tc05_f8_box_rows(), 1)) return false;
@@ -738,8 +768,8 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
                         int32_t* err_word, mqa_stream_t stream, int early) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) || layout->paged ||
-      layout->head_dim != 128)
+  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) ||
+      (layout->paged && layout->cache_dtype != MQA_BF16) || layout->head_dim != 128)
     return MQA_ERR_UNSUPPORTED;
   if (n_new < 1 || static_cast<long long>(layout->batch) * n_new > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
   if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
@@ -805,8 +835,8 @@ mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const vo
   // the attention's own checks first, so nothing is launched for a call that fails
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) || layout->paged ||
-      layout->head_dim != 128)
+  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) ||
+      (layout->paged && layout->cache_dtype != MQA_BF16) || layout->head_dim != 128)
     return MQA_ERR_UNSUPPORTED;
   if (!seq_lens || !out || max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;

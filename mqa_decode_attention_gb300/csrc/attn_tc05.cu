@@ -139,12 +139,17 @@ __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of b
 // that merge their partial results through distributed shared memory; block
 // 0 writes the output (no combine launch, no partials in global memory).
 // F8: fp8 e5m2 cache (the tensor maps describe the one-byte code tiles).
-template <int PARTS, bool FUSE, bool CL, bool F8>
+// PG: paged bf16 cache (PagedAttention, "Arsitektur Inferensi LLM", section
+// 4): pages [num_pages, h_kv, page_size, 128] through the block table; a key
+// tile is gathered page by page (rp = min(page_size, 64) rows per copy: the
+// tiles start on multiples of 64, so a 64-key half never straddles a page).
+template <int PARTS, bool FUSE, bool CL, bool F8, bool PG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const Tc05Params p) {
   static_assert(!CL || PARTS > 1, "the cluster merge takes replicated rows (R <= 64)");
   static_assert(!(FUSE && F8), "the fused step is bf16 only");
+  static_assert(!(PG && F8), "paged caches: bf16 only");
   using Y = Lay<F8>;
   constexpr int kStages = Y::kStages, kTileBytes = Y::kTileBytes, kQOff = Y::kQOff, kKOff = Y::kKOff,
                 kVOff = Y::kVOff, kBarOff = Y::kBarOff, kXOff = Y::kXOff;
@@ -317,23 +322,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kU tokens, not per token), and the pairs the fp32 stage of rope_k_bf16
   // leaves open are collected and finished in fp64 at the end, every lane at
   // once: a lane's open pair no longer stalls the whole warp on its own.
+  const int32_t* trow = PG ? p.block_table + static_cast<long long>(b) * p.max_pages : nullptr;
   auto append_rows = [&]() {
     constexpr int kU = 2;  // (mqa8k, same-box A/B: 2 tokens 56.1 / 48.4 us isolated / back to back, 4: 61.4 / 49.3)
     __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache));
     __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache));
     const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(p.k_new);
     const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(p.v_new);
-    bool bad_pos = false;
+    bool bad_pos = false, bad_page = false;
     static_assert(2 * kMaxNewTokens <= 64, "the open-pair mask");
     uint64_t open = 0;  // bit 2 i + h: pair lane + 32 h of new token i left to the fp64 stage
-    auto dst_of = [&](int i) { return ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + apos + i) * kD; };
+    // the page of position ap (paged; entry checked by the caller)
+    auto page_at = [&](int ap) { return PG ? __ldg(trow + ap / p.page_size) : 0; };
+    auto dst_of = [&](int i, int page) -> long long {  // element offset of new token i's cache row
+      const int ap = apos + i;
+      if constexpr (PG)
+        return ((static_cast<long long>(page) * p.h_kv + j) * p.page_size + (ap & (p.page_size - 1))) * kD;
+      else
+        return ((static_cast<long long>(b) * p.h_kv + j) * p.capacity + ap) * kD;
+    };
     auto src_of = [&](int i) { return ((static_cast<long long>(b) * n + i) * p.h_kv + j) * kD; };
     for (int i0 = a_first; i0 < n; i0 += kU) {
       uint32_t kraw[kU][kD / 64], vraw[kU][kD / 64];
+      int pg[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int i = i0 + u;
         if (i >= n || owner(i) != split || apos + i < 0 || apos + i >= p.capacity) continue;
+        pg[u] = page_at(apos + i);
         const long long src = src_of(i);
 #pragma unroll
         for (int h = 0; h < kD / 64; ++h) {  // pairs lane, lane + 32
@@ -350,7 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bad_pos = true;
           continue;
         }
-        const long long dst = dst_of(i);
+        if (PG && (pg[u] < 0 || pg[u] >= p.num_pages)) {
+          bad_page = true;
+          continue;
+        }
+        const long long dst = dst_of(i, pg[u]);
 #pragma unroll
         for (int h = 0; h < kD / 64; ++h) {
           const int pi = lane + 32 * h;
@@ -371,10 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = bit >> 1, pi = lane + 32 * (bit & 1);
         const uint32_t kp = *reinterpret_cast<const uint32_t*>(kn + src_of(i) + 2 * pi);
         const double ang = reduce_two_pi(static_cast<double>(apos + i) * p.theta[pi]);
-        *reinterpret_cast<uint32_t*>(kc + dst_of(i) + 2 * pi) = rope_k_packed_fp64(kp, ang);
+        *reinterpret_cast<uint32_t*>(kc + dst_of(i, page_at(apos + i)) + 2 * pi) = rope_k_packed_fp64(kp, ang);
       }
     }
     if (bad_pos && lane == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_POS_RANGE));
+    if (bad_page && lane == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
   };
@@ -443,7 +464,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto stop = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
 
-  if (warp == 4 || warp == 5) {
+  if (PG && (warp == 4 || warp == 5)) {
+    // ------------------------------------ K (warp 4) / V (warp 5) loaders, paged
+    // Lane c issues copy c of a tile (its rp rows, in two 64-dim halves at the
+    // tile's two 16 KB halves). The page ids of the block's key range are held
+    // 32 at a time, one per lane (wcur: pages wbase .., wnxt: the next 32). A
+    // copy past the last page holding a key the block reads, or before the
+    // first, loads nothing (page coordinate -1: the copy lands zeros) and its
+    // entry is not read; an entry that a read needs and that is outside the
+    // pool sets MQA_DEVERR_PAGE_RANGE, and its rows land as zeros.
+    const bool is_k = warp == 4;
+    const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+    const int full = is_k ? kKFull : kVFull, empty = is_k ? kKEmpty : kVEmpty;
+    const uint32_t dst0 = sbase + (is_k ? kKOff : kVOff);
+    const int ps = p.page_size, rp = ps < 64 ? ps : 64, copies = kBN / rp;
+    const int lp_end = (kend + ps - 1) / ps, lp_first = ka_first / ps;
+    auto entry = [&](int lp) { return (lp >= lp_first && lp < lp_end) ? __ldg(trow + lp) : -1; };
+    int wbase = kstart / ps;
+    int wcur = entry(wbase + lane), wnxt = entry(wbase + 32 + lane);
+    bool bad = false;
+    auto issue = [&](int it) {  // every lane
+      const int s = it % kStages, key0 = tile_key0(it);
+      while (key0 / ps - wbase >= 32) {
+        wcur = wnxt;
+        wbase += 32;
+        wnxt = entry(wbase + 32 + lane);
+      }
+      const int k = key0 + lane * rp, lp = k / ps, off = lp - wbase;  // off < 32 + 8
+      const int pc = __shfl_sync(0xffffffffu, wcur, off & 31), pn = __shfl_sync(0xffffffffu, wnxt, off & 31);
+      int page = off < 32 ? pc : pn;
+      const bool needed = lane < copies && lp >= lp_first && lp < lp_end;
+      if (needed && (page < 0 || page >= p.num_pages)) bad = true;
+      if (!needed || page < 0 || page >= p.num_pages) page = -1;
+      if (lane == 0) mbar_arrive_expect_tx(bar(full + s), kTileBytes);
+      __syncwarp();
+      if (lane < copies) {
+        const uint32_t d = dst0 + s * kTileBytes + lane * rp * 128;
+        tma_load_5d(d, map, 0, k & (ps - 1), 0, j, page, bar(full + s));
+        tma_load_5d(d + 16384, map, 0, k & (ps - 1), 1, j, page, bar(full + s));
+      }
+    };
+    int it = 0;
+    {
+      const int npre = p.early ? kStages : kPreTiles;
+      const int lim = p.early ? Lp : (writer ? a_pos : 0x7fffffff);
+      for (; it < T && it < npre && tile_key0(it) + kBN <= lim; ++it) issue(it);
+    }
+    named_bar_sync(2, kBM + 64);
+    bool waited = !p.early, appended = !writer;
+    for (; it < T; ++it) {
+      const int s = it % kStages;
+      bool ok = true;
+      if (lane == 0) {
+        if (it >= kStages) ok = mbar_wait(bar(empty + s), ((it - kStages) / kStages) & 1, p.wait_ns);
+        if (ok && !appended && a_pos < tile_key0(it) + kBN) ok = mbar_wait(bar(kAppended), 0, p.wait_ns);
+        if (!ok) fail(1);
+        if (stop()) ok = false;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (!appended && a_pos < tile_key0(it) + kBN) appended = true;
+      if (!waited && Lp < tile_key0(it) + kBN) {  // this tile holds a new token's row
+        grid_dependency_wait();
+        waited = true;
+      }
+      issue(it);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
+    // every tile this warp issued lands before the block can exit
+    if (lane == 0)
+      for (int k = it > kStages ? it - kStages : 0; k < it; ++k)
+        (void)mbar_wait(bar(full + k % kStages), (k / kStages) & 1, kWaitLimitNs);
+    __syncwarp();
+  } else if (warp == 4 || warp == 5) {
     // ------------------------------------------------- K (warp 4) / V (warp 5) loaders
     const bool is_k = warp == 4;
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
@@ -1025,9 +1117,9 @@ KernelShape tc05_shape() { return {kThreads, Lay<false>::kSmemBytes, kBM, 1}; }
 
 int tc05_f8_box_rows() { return kBN; }
 
-template <int PARTS, bool FUSE, bool CL, bool F8>
+template <int PARTS, bool FUSE, bool CL, bool F8, bool PG>
 cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  auto kern = attn_tc05_kernel<PARTS, FUSE, CL, F8>;
+  auto kern = attn_tc05_kernel<PARTS, FUSE, CL, F8, PG>;
   constexpr int smem = Lay<F8>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1051,34 +1143,34 @@ cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUten
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-template <int PARTS, bool F8>
+template <int PARTS, bool F8, bool PG>
 cudaError_t launch_fuse(const Tc05Params& p, bool cl, const CUtensorMap& tk, const CUtensorMap& tv,
                         cudaStream_t stream) {
   if constexpr (F8) {  // (several new tokens: never fused)
-    return cl ? launch_parts<PARTS, false, true, true>(p, tk, tv, stream)
-              : launch_parts<PARTS, false, false, true>(p, tk, tv, stream);
+    return cl ? launch_parts<PARTS, false, true, true, false>(p, tk, tv, stream)
+              : launch_parts<PARTS, false, false, true, false>(p, tk, tv, stream);
   } else {
     if (cl)
-      return p.fuse ? launch_parts<PARTS, true, true, false>(p, tk, tv, stream)
-                    : launch_parts<PARTS, false, true, false>(p, tk, tv, stream);
-    return p.fuse ? launch_parts<PARTS, true, false, false>(p, tk, tv, stream)
-                  : launch_parts<PARTS, false, false, false>(p, tk, tv, stream);
+      return p.fuse ? launch_parts<PARTS, true, true, false, PG>(p, tk, tv, stream)
+                    : launch_parts<PARTS, false, true, false, PG>(p, tk, tv, stream);
+    return p.fuse ? launch_parts<PARTS, true, false, false, PG>(p, tk, tv, stream)
+                  : launch_parts<PARTS, false, false, false, PG>(p, tk, tv, stream);
   }
 }
 
-template <bool F8>
+template <bool F8, bool PG>
 cudaError_t launch_rows(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   // replicate few rows over the 128 MMA rows so that all four softmax warps work
   const long long rows = static_cast<long long>(p.group) * p.n_new;
   const bool cl = tc05_merges_splits(p);
   // (a fused step has one row block: p.fuse implies row_blocks == 1)
-  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4, F8>(p, cl, tk, tv, stream);
-  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2, F8>(p, cl, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4, F8, PG>(p, cl, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2, F8, PG>(p, cl, tk, tv, stream);
   if constexpr (F8)
-    return launch_parts<1, false, false, true>(p, tk, tv, stream);
+    return launch_parts<1, false, false, true, false>(p, tk, tv, stream);
   else
-    return p.fuse ? launch_parts<1, true, false, false>(p, tk, tv, stream)
-                  : launch_parts<1, false, false, false>(p, tk, tv, stream);
+    return p.fuse ? launch_parts<1, true, false, false, PG>(p, tk, tv, stream)
+                  : launch_parts<1, false, false, false, PG>(p, tk, tv, stream);
 }
 
 bool tc05_merges_splits(const Tc05Params& p) {
@@ -1087,7 +1179,8 @@ bool tc05_merges_splits(const Tc05Params& p) {
 
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
-  return p.f8 ? launch_rows<true>(p, tk, tv, stream) : launch_rows<false>(p, tk, tv, stream);
+  if (p.f8) return launch_rows<true, false>(p, tk, tv, stream);
+  return p.paged ? launch_rows<false, true>(p, tk, tv, stream) : launch_rows<false, false>(p, tk, tv, stream);
 }
 
 }  // namespace mqa

@@ -85,17 +85,20 @@ struct DecodeParams {
 };
 
 // Attention on tcgen05 over blocks of 128 (new token, query head) rows of
-// one kv head: prefill, MQA decode, multi-token decode. Contiguous bf16
-// cache, head_dim 128.
+// one kv head: prefill, MQA decode, multi-token decode. head_dim 128; bf16
+// cache (contiguous or paged) or contiguous fp8 e5m2 cache.
 struct Tc05Params {
   int batch, h_q, h_kv, group, n_new;
   int row_blocks;  // ceil(group * n_new / 128)
   int f8;          // attn_tc05: 1 = fp8 e5m2 cache (code tiles), 0 = bf16
+  int paged;       // attn_tc05: 1 = paged bf16 cache [num_pages, h_kv, page_size, 128] through block_table
+  int page_size, max_pages, num_pages;
+  const int32_t* block_table;  // [batch, max_pages] (paged)
   int num_splits;  // token-axis splits; 1 = write `out` directly
   int chunk;       // tokens per split, a multiple of 64
   const void* k_cache;
   const void* v_cache;
-  long long capacity;
+  long long capacity;  // tokens a sequence can hold (paged: max_pages * page_size)
   int max_seq_len;
   const int32_t* seq_lens;
   const float* q_rot;  // [B, n_new, H_q, 128] fp32
@@ -109,14 +112,15 @@ struct Tc05Params {
   int32_t* err;
   int early;  // 1: the preceding launch is the append kernel; stream K/V before waiting for it
   unsigned long long wait_ns;  // limit of the waits for progress (the drains use kWaitLimitNs)
-  // 1: single-launch step (one new token, one row block): the kernel rotates
-  // q_new itself and the block whose split holds pos appends the k / v row
+  // 1: single-launch step (one row block): the kernel rotates q_new itself
+  // and the block whose split holds a new token's position appends its k / v
+  // rows
   int fuse;
-  const void* q_new;  // [B, H_q, 128] bf16
-  const void* k_new;  // [B, H_kv, 128] bf16
+  const void* q_new;  // [B, n_new, H_q, 128] bf16
+  const void* k_new;  // [B, n_new, H_kv, 128] bf16
   const void* v_new;
   const int32_t* pos;
-  float* q_rot_out;  // RoPE(q_new) [B, H_q, 128] fp32
+  float* q_rot_out;  // RoPE(q_new) [B, n_new, H_q, 128] fp32
   float2* k_sz;      // uint8 cache, fused step: where the new rows' (scale, zero point) go
   float2* v_sz;
   double theta[kMaxHalfDim];

@@ -294,3 +294,38 @@ def test_fused_append_multi_token_tc05(m, h_q, h_kv, n, splits):
     128, n <= 16: one launch, the kernel's append warp writing the rows of its
     split; G n <= 64 at two splits merges them in a two-block cluster)."""
     fused_multi_case(m, h_q, h_kv, n, splits, 131 + n + h_q)
+
+
+@pytest.mark.parametrize("page_size, n, splits", [(16, 8, 1), (16, 8, 3), (32, 16, 2), (256, 4, 3), (64, 2, 2)])
+def test_fused_append_multi_token_tc05_paged(m, page_size, n, splits):
+    """The fused multi-token step over a paged pool (tcgen05 kernel): every
+    pool byte equals what kv_append_rope_multi writes, new rows crossing page
+    and split boundaries alike."""
+    h_q, h_kv = (32, 1) if n <= 4 else (32, 8)
+    w = workload("paged").with_(batch=6, h_q=h_q, h_kv=h_kv, page_size=page_size, seed=141 + n + page_size)
+    lens = torch.tensor([705, 706, 1409, n, 64 + n - 1, 1000], dtype=torch.int32)
+    pc = make_paged_case(w, "cpu", seq_lens=lens, spare_pages=2)
+    gen = torch.Generator().manual_seed(142 + n)
+    q = torch.randn((w.batch, n, w.h_q, w.head_dim), generator=gen).to(torch.bfloat16)
+    k = hard_keys((w.batch, n, w.h_kv, w.head_dim), 143 + n)
+    v = torch.randn((w.batch, n, w.h_kv, w.head_dim), generator=gen).to(torch.bfloat16)
+    pos = (lens - n).to(torch.int32)
+    bt = pc.block_table.to(DEV)
+    cap = int(lens.max())
+    results = []
+    for fused in (True, False):
+        kp, vp = pc.k_pool.to(DEV), pc.v_pool.to(DEV)
+        lay = m.layout_paged(kp, vp, bt, w.h_q)
+        if fused:
+            assert m.step_launches(lay, cap, splits, 2, n)[1], "the step should append inside the attention launch"
+        bufs = m.DecodeBuffers.allocate(lay, cap, num_splits=splits, variant=2, device=DEV, n_new=n)
+        args = (q.to(DEV), k.to(DEV), v.to(DEV), pos.to(DEV))
+        if fused:
+            m.decode_step_multi(lay, n, *args, lens.to(DEV), cap, bufs, w.rope_base, 0.1, num_splits=splits, variant=2)
+        else:
+            m.kv_append_rope_multi(lay, n, *args, w.rope_base, bufs.q_rot, bufs.err)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0
+        results.append((kp.cpu(), vp.cpu()))
+    assert torch.equal(bits(results[0][0]), bits(results[1][0]))
+    assert torch.equal(bits(results[0][1]), bits(results[1][1]))

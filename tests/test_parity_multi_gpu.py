@@ -134,6 +134,78 @@ def test_multi_paged_matches_oracle(m, page_size, n):
         check_cache(pc.v_pool, got["v"], ref["v_pool"], v_cache=True)
 
 
+@pytest.mark.parametrize("page_size", [16, 32, 128, 256])
+@pytest.mark.parametrize("shape", [(32, 8, 8), (32, 1, 2), (64, 8, 16), (32, 8, 32), (64, 8, 32)],
+                         ids=lambda s: f"q{s[0]}kv{s[1]}n{s[2]}")
+def test_multi_paged_tc05_matches_oracle(m, page_size, shape):
+    """32 or more (token, head) rows per kv head over a paged pool: the
+    tcgen05 kernel gathering each key tile page by page -- with the append
+    inside the launch (n <= 16, one row block) or after the append launch (n =
+    32; 256 rows: two row blocks)."""
+    hq, hkv, n = shape
+    w = workload("paged").with_(batch=4, h_q=hq, h_kv=hkv, page_size=page_size, seed=41 + n + hq + page_size)
+    lens = [700, n, 129 + n, 300]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=2)
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", block_table=pc.block_table, page_size=page_size)
+    keys = paged_keys(ref["k_pool"], pc.block_table, lens, page_size)
+    for splits in (1, 2, 3, 0):
+        got = run_multi(m, w, n, pc.k_pool, pc.v_pool, q, k, v, lens, splits=splits, table=pc.block_table,
+                        page_size=page_size)
+        assert got["err"] == 0
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, splits
+        assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL, splits
+        assert_lse(got["lse"], ref["q_rot"], keys, lens, 1.0 / math.sqrt(w.head_dim), "bf16", what=splits)
+        check_cache(pc.k_pool, got["k"], ref["k_pool"], v_cache=False)
+        check_cache(pc.v_pool, got["v"], ref["v_pool"], v_cache=True)
+
+
+@pytest.mark.parametrize("window", [1, 50, 300])
+def test_multi_paged_tc05_window_released_pages(m, window):
+    """Sliding window over a paged pool on the tcgen05 kernel: pages wholly
+    before the first new token's window are released (-1) and never read."""
+    n, ps = 8, 16
+    w = workload("paged").with_(batch=3, h_q=32, h_kv=8, page_size=ps, seed=51 + window)
+    lens = [900, 400, n]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+    table = pc.block_table.clone()
+    for b, L in enumerate(lens):
+        table[b, :max(0, L - n + 1 - window) // ps] = -1
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", block_table=pc.block_table, page_size=ps, window=window)
+    keys = paged_keys(ref["k_pool"], pc.block_table, lens, ps)
+    for splits in (1, 3, 0):
+        got = run_multi(m, w, n, pc.k_pool, pc.v_pool, q, k, v, lens, splits=splits, table=table, page_size=ps,
+                        window=window)
+        assert got["err"] == 0, (window, splits)
+        assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL, (window, splits)
+        assert_lse(got["lse"], ref["q_rot"], keys, lens, 1.0 / math.sqrt(w.head_dim), "bf16", window=window,
+                   what=splits)
+
+
+def test_multi_paged_tc05_bad_page_is_reported(m):
+    """A table entry outside the pool for a page the new tokens attend, and
+    one for the page a new token is appended to: both reported as
+    MQA_DEVERR_PAGE_RANGE; the other sequences match the oracle."""
+    n, ps = 8, 16
+    w = workload("paged").with_(batch=3, h_q=32, h_kv=8, page_size=ps, seed=61)
+    lens = [300, 200, 100]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+    table = pc.block_table.clone()
+    table[0, 3] = pc.num_pages  # attended, cached page of sequence 0
+    table[1, (lens[1] - 1) // ps] = -5  # the page sequence 1's last new token goes to
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", block_table=pc.block_table, page_size=ps)
+    for splits in (1, 3):
+        got = run_multi(m, w, n, pc.k_pool, pc.v_pool, q, k, v, lens, splits=splits, table=table, page_size=ps)
+        assert got["err"] & m.MQA_DEVERR_PAGE_RANGE, splits
+        out = got["out"].reshape(ref["out"].shape)
+        assert np.max(np.abs(out[2] - ref["out"][2])) <= BF16_TOL, splits
+
+
 @pytest.mark.parametrize("window", [1, 3, 17, 100])
 def test_multi_sliding_window(m, window):
     """Query token i sees the last W tokens up to its own position."""

@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from lse_model import assert_lse
+from lse_model import assert_lse, paged_keys
 from synthetic import make_contiguous_case, make_paged_case, normal, workload
 
 pytestmark = pytest.mark.gpu
@@ -148,9 +148,11 @@ def test_prefill_errors_and_refusals(m):
     wp = workload("paged").with_(batch=1, h_q=8, h_kv=2, seed=614)
     pc = make_paged_case(wp, "cpu", seq_lens=torch.tensor([64], dtype=torch.int32))
     bt = pc.block_table.to(DEV)
-    lay_p = m.layout_paged(pc.k_pool.to(DEV), pc.v_pool.to(DEV), bt, 8)
-    with pytest.raises(m.MqaError):  # paged pools: decode and multi-token calls only
-        m.gqa_prefill_attention(lay_p, n, q_rot[:1], torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1,
+    codes = torch.zeros(pc.k_pool.shape, dtype=torch.uint8, device=DEV)
+    sz = torch.ones(pc.k_pool.shape[:-1] + (2,), dtype=torch.float32, device=DEV)
+    lay_u8 = m.layout_paged(codes, codes.clone(), bt, 8, k_scale_zero=sz, v_scale_zero=sz.clone())
+    with pytest.raises(m.MqaError):  # paged pools: bf16 only
+        m.gqa_prefill_attention(lay_u8, n, q_rot[:1], torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1,
                                 out[:1], err=err)
 
 
@@ -193,3 +195,93 @@ def test_prefill_ignores_garbage_past_the_sequence(m):
     assert got["err"] == 0
     assert np.all(np.isfinite(got["out"]))
     assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
+
+
+def run_prefill_paged(m, w, n, pc, q, k, v, lens, window=0, table=None):
+    kp, vp = pc.k_pool.to(DEV), pc.v_pool.to(DEV)
+    bt = (pc.block_table if table is None else table).to(DEV)
+    lay = m.layout_paged(kp, vp, bt, w.h_q, window=window)
+    lens_d = torch.as_tensor(lens, dtype=torch.int32).to(DEV)
+    max_len = int(max(lens))
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=1, device=DEV, n_new=n)
+    m.prefill_step(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), (lens_d - n).to(torch.int32), lens_d, max_len, bufs,
+                   w.rope_base, 1.0 / math.sqrt(w.head_dim))
+    torch.cuda.synchronize()
+    B, hq = w.batch, w.h_q
+    return dict(out=_np(bufs.out).reshape(B, n, hq, -1), lse=_np(bufs.lse).reshape(B, n, hq), k=kp.cpu(),
+                v=vp.cpu(), err=int(bufs.err.item()))
+
+
+PAGED_CASES = [
+    # B, h_q, h_kv, n (prompt), prefixes, page_size
+    (2, 8, 2, 5, [0, 0], 16),
+    (2, 8, 2, 129, [0, 3], 16),
+    (2, 8, 2, 200, [57, 0], 32),
+    (2, 8, 2, 300, [0, 64], 64),
+    (1, 8, 2, 250, [100], 128),
+    (2, 16, 1, 140, [10, 300], 256),   # MQA, prefix longer than a page
+    (1, 4, 4, 190, [70], 64),          # MHA
+]
+
+
+@pytest.mark.parametrize("case", PAGED_CASES, ids=lambda c: f"B{c[0]}q{c[1]}kv{c[2]}n{c[3]}ps{c[5]}")
+def test_prefill_paged_matches_oracle(m, case):
+    """Prefill over a paged pool (PagedAttention, "Arsitektur Inferensi LLM",
+    section 4): the prompt's rows land in the pages the block table names and
+    the key tiles are gathered page by page."""
+    B, hq, hkv, n, pre, ps = case
+    w = workload("paged").with_(batch=B, h_q=hq, h_kv=hkv, page_size=ps, seed=700 + n + ps + hq)
+    lens = [p_ + n for p_ in pre]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=2)
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", block_table=pc.block_table, page_size=ps)
+    got = run_prefill_paged(m, w, n, pc, q, k, v, lens)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= TOL
+    keys = paged_keys(ref["k_pool"], pc.block_table, lens, ps)
+    assert_lse(got["lse"], ref["q_rot"], keys, lens, 1.0 / math.sqrt(w.head_dim), "bf16")
+    bk, ak = _np(pc.k_pool), _np(got["k"])
+    assert np.array_equal(np.any(ak != bk, axis=-1), np.any(ref["k_pool"] != bk, axis=-1))
+    assert np.all(np.abs(ak - ref["k_pool"]) <= ulp_bf16(ref["k_pool"]) + 1e-30)
+    assert np.array_equal(_np(got["v"]), ref["v_pool"])
+
+
+@pytest.mark.parametrize("window, ps", [(1, 16), (64, 16), (200, 64), (100, 256)])
+def test_prefill_paged_window_released_pages(m, window, ps):
+    """A sliding window over a paged pool: the pages wholly before the first
+    prompt token's window are released (table entry -1) and never read."""
+    w = workload("paged").with_(batch=2, h_q=8, h_kv=2, page_size=ps, seed=720 + window)
+    n, pre = 300, 600
+    lens = [pre + n, pre + n - 50]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+    table = pc.block_table.clone()
+    for b, L in enumerate(lens):
+        first = max(0, L - n + 1 - window)  # the first key the first prompt token attends
+        table[b, :first // ps] = -1
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", block_table=pc.block_table, page_size=ps, window=window)
+    got = run_prefill_paged(m, w, n, pc, q, k, v, lens, window=window, table=table)
+    assert got["err"] == 0
+    assert np.max(np.abs(got["out"] - ref["out"])) <= TOL
+    keys = paged_keys(ref["k_pool"], pc.block_table, lens, ps)
+    assert_lse(got["lse"], ref["q_rot"], keys, lens, 1.0 / math.sqrt(w.head_dim), "bf16", window=window)
+
+
+def test_prefill_paged_bad_page_is_reported(m):
+    """A table entry outside the pool, for a page the prompt attends: the call
+    reports MQA_DEVERR_PAGE_RANGE (the page reads as zeros) and the other
+    sequence's rows are unaffected."""
+    w = workload("paged").with_(batch=2, h_q=8, h_kv=2, page_size=16, seed=731)
+    n, lens = 40, [40 + 80, 40 + 80]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+    table = pc.block_table.clone()
+    table[0, 1] = pc.num_pages + 7  # a cached prefix page of sequence 0
+    q, k, v = new_tokens(w, n)
+    ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, 1.0 / math.sqrt(w.head_dim),
+                                   "bf16", block_table=pc.block_table, page_size=16)
+    got = run_prefill_paged(m, w, n, pc, q, k, v, lens, table=table)
+    assert got["err"] & m.MQA_DEVERR_PAGE_RANGE
+    assert np.max(np.abs(got["out"][1] - ref["out"][1])) <= TOL
