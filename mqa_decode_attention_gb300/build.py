@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 LIB_NAME = "libmqa_decode.so"
 SOURCES = ["abi.cu", "append_rope.cu", "combine.cu", "decode_fma.cu", "decode_mma.cu", "decode_mma_paged.cu", "decode_mma_u8.cu",
-           "noalloc.cu", "attn_tc05.cu", "attn_tc05_keys.cu", "attn_tc05_widen.cu"]
+           "noalloc.cu", "attn_tc05.cu", "attn_tc05_keys.cu", "attn_tc05_widen.cu",
+           "attn_tc05_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-diag-suppress", "177"]

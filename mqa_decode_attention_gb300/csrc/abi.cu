@@ -811,7 +811,15 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
     snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
     return MQA_ERR_CUDA;
   }
-  const cudaError_t e = launch_tc05_attention(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (p.f8) {
+    e = launch_tc05_attention(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    // bf16: two 128-row query tiles per block sharing every K / V tile
+    const int rpb = tc05_prefill_rows_per_block();
+    p.row_blocks = static_cast<int>((static_cast<long long>(p.group) * n_new + rpb - 1) / rpb);
+    e = launch_tc05_prefill(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return fail_cuda(e);
   const cudaError_t e2 = cudaGetLastError();
   return e2 == cudaSuccess ? MQA_OK : fail_cuda(e2);

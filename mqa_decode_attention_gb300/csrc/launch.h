@@ -197,6 +197,12 @@ cudaError_t launch_tc05_widen_attention(const Tc05Params& p, const CUtensorMap& 
                                         cudaStream_t stream);
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                   cudaStream_t stream);
+// Prefill over a bf16 cache (contiguous or paged): blocks of
+// tc05_prefill_rows_per_block() rows (two 128-row query tiles); p.row_blocks
+// counts those blocks.
+int tc05_prefill_rows_per_block();
+cudaError_t launch_tc05_prefill(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                cudaStream_t stream);
 // true when launch_tc05_attention merges the splits itself (two splits, R <=
 // 64 rows in one row block: each pair of split blocks is a two-block cluster
 // that writes out and lse_out directly): no combine follows, and o_part /

@@ -12,7 +12,8 @@ same stream, matches the oracle.
 
 Kernels covered: the warp-MMA kernel (fused one-launch step; split with the
 combine), the paged head-group kernel, the tcgen05 MQA kernel (one split and
-a two-block cluster), the CUDA-core kernel and the uint8 warp-MMA kernel.
+a two-block cluster), the CUDA-core kernel, the uint8 warp-MMA kernel and the
+prefill kernel (contiguous and paged).
 """
 
 import math
@@ -103,3 +104,50 @@ def test_timeout_then_normal_call(m, name):
     assert int(bufs.err.item()) == 0, name
     assert np.max(np.abs(_np(bufs.out) - ref["out"])) <= TOL, name
     assert np.max(np.abs(_np(bufs.lse) - ref["lse"])) <= TOL, name
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_prefill_timeout_then_normal_call(m, paged):
+    """The prefill kernel (two query tiles per block, contiguous and paged)
+    takes the same timeout path."""
+    n, B, hq, hkv = 300, 2, 8, 2
+    lens = [n + 40, n]
+    L = torch.tensor(lens, dtype=torch.int32)
+    scale = 1.0 / math.sqrt(128)
+    gen = torch.Generator().manual_seed(911)
+    q = torch.randn((B, n, hq, 128), generator=gen).to(torch.bfloat16)
+    k = torch.randn((B, n, hkv, 128), generator=gen).to(torch.bfloat16)
+    v = torch.randn((B, n, hkv, 128), generator=gen).to(torch.bfloat16)
+    if paged:
+        w = workload("paged").with_(batch=B, h_q=hq, h_kv=hkv, page_size=32, seed=912)
+        c = make_paged_case(w, "cpu", seq_lens=L, spare_pages=1)
+        pools = (c.k_pool.to(DEV), c.v_pool.to(DEV))
+        bt = c.block_table.to(DEV)
+        lay = m.layout_paged(pools[0], pools[1], bt, hq)
+        ref = oracle.decode_step_multi(c.k_pool, c.v_pool, q, k, v, lens, 10000.0, scale, "bf16",
+                                       block_table=c.block_table, page_size=32)
+    else:
+        w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=912)
+        c = make_contiguous_case(w, "cpu", seq_lens=L, capacity=n + 40)
+        caches = (c.k_cache.to(DEV), c.v_cache.to(DEV))
+        lay = m.layout_contiguous(caches[0], caches[1], hq)
+        ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, 10000.0, scale, "bf16")
+    bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=1, device=DEV, n_new=n)
+    Ld = L.to(DEV)
+    args = (q.to(DEV), k.to(DEV), v.to(DEV), (Ld - n).to(torch.int32), Ld, max(lens), bufs, 10000.0, scale)
+
+    lay.wait_limit_ns = 1
+    bufs.err.zero_()
+    m.prefill_step(lay, n, *args)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) & m.MQA_DEVERR_TIMEOUT, hex(int(bufs.err.item()))
+
+    # the default limit, same inputs (the append wrote the same rows): the oracle
+    lay.wait_limit_ns = 0
+    bufs.err.zero_()
+    bufs.out.fill_(float("nan"))
+    m.prefill_step(lay, n, *args)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    out = _np(bufs.out).reshape(ref["out"].shape)
+    assert np.max(np.abs(out - ref["out"])) <= TOL
