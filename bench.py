@@ -999,7 +999,7 @@ def bench_prefill(args):
                                   if w.paged else "contiguous bf16 cache"),
                    "flops_per_step": flops},
         "kernels_ms": {"mqa_prefill_step": round(ms_step, 6), "standalone_gqa_prefill_attention": round(attn_ms, 6)},
-        "roofline": {"bound": "tensor", "kernel": "attn_tc05_kernel (prefill)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": ("attn_tc05_prefill_kernel" if w.dtype == "bf16" else "attn_tc05_kernel"), "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)" if peaks else "fallback"},
         "gpu_launches": 2 * K,

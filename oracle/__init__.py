@@ -18,6 +18,7 @@ from .decode import (
     decode_step_contiguous,
     decode_step_multi,
     decode_step_multi_e5m2,
+    decode_step_multi_u8,
     decode_step_paged,
     decode_step_e5m2,
     decode_step_u8,

@@ -540,6 +540,58 @@ def decode_step_multi_e5m2(k_codes, v_codes, q_new, k_new, v_new, seq_lens, rope
     return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "v_codes": Vc}
 
 
+def decode_step_multi_u8(k_codes, k_sz, v_codes, v_sz, q_new, k_new, v_new, seq_lens, rope_base: float,
+                         scale: float, block_table=None, page_size: int = 0, window: int = 0):
+    """n new tokens per sequence in one pass (the verification of drafted
+    tokens, "Arsitektur Inferensi LLM", section 7) over a uint8 cache (the
+    QuantizedKVCache of "KV Cache 최적화 심층 분석"): decode_step_multi's steps
+    with decode_step_u8's storage. New token i of sequence b sits at
+    p = L_b - n + i; its q and k are rotated by p in fp64, its key (rounded to
+    fp32) and its value (bf16 input) are quantised row by row and stored at p
+    with their (scale, zero point); query i then attends to
+    [window_start(p + 1, W), p + 1) of the dequantised cache.
+    Returns dict(out [B,n,H_q,d], lse [B,n,H_q], q_rot [B,n,H_q,d], k_codes,
+    k_sz, v_codes, v_sz) with the cache as updated copies."""
+    Kc, Vc = np.array(k_codes, copy=True), np.array(v_codes, copy=True)
+    Ks, Vs = np.array(k_sz, dtype=np.float32, copy=True), np.array(v_sz, dtype=np.float32, copy=True)
+    q_new, k_new, v_new = _f64(q_new), _f64(k_new), _f64(v_new)
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    table = None if block_table is None else np.asarray(_f64(block_table), dtype=np.int64)
+    B, n, h_q, d = q_new.shape
+    out = np.empty((B, n, h_q, d), F64)
+    lse = np.empty((B, n, h_q), F64)
+    q_rot = np.empty((B, n, h_q, d), F64)
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(n):
+            p = L - n + i
+            q_rot[b, i] = rope_rotate(q_new[b, i], p, rope_base)
+            kq, ks, kz = quantize_u8(rope_rotate(k_new[b, i], p, rope_base))
+            vq, vs, vz = quantize_u8(v_new[b, i])
+            if table is None:
+                Kc[b, :, p], Vc[b, :, p] = kq, vq
+                Ks[b, :, p] = np.stack([ks, kz], -1)
+                Vs[b, :, p] = np.stack([vs, vz], -1)
+            else:
+                page, off = page_slot(table[b], p, page_size)
+                Kc[page, :, off], Vc[page, :, off] = kq, vq
+                Ks[page, :, off] = np.stack([ks, kz], -1)
+                Vs[page, :, off] = np.stack([vs, vz], -1)
+        if table is None:
+            Kd = dequantize_u8(Kc[b, :, :L], Ks[b, :, :L, 0], Ks[b, :, :L, 1])
+            Vd = dequantize_u8(Vc[b, :, :L], Vs[b, :, :L, 0], Vs[b, :, :L, 1])
+        else:
+            ksz = gather_paged(Ks, table[b], L, page_size)
+            vsz = gather_paged(Vs, table[b], L, page_size)
+            Kd = dequantize_u8(gather_paged(Kc, table[b], L, page_size), ksz[..., 0], ksz[..., 1])
+            Vd = dequantize_u8(gather_paged(Vc, table[b], L, page_size), vsz[..., 0], vsz[..., 1])
+        for i in range(n):
+            p = L - n + i
+            t0 = window_start(p + 1, window)
+            out[b, i], lse[b, i] = gqa_attention(q_rot[b, i], Kd[:, t0:p + 1], Vd[:, t0:p + 1], scale)
+    return {"out": out, "lse": lse, "q_rot": q_rot, "k_codes": Kc, "k_sz": Ks, "v_codes": Vc, "v_sz": Vs}
+
+
 def decode_unit(q_group, k_row, v_row, K_unit, V_unit, seq_len: int, rope_base: float, scale: float,
                 cache_dtype: str, window: int = 0):
     """The decode step for ONE (sequence, KV head) unit, for sampled checks at

@@ -783,8 +783,9 @@ def check_multi_step(fn):
 
 def check_multi_e5m2(fn):
     """n new tokens over an e5m2 cache in one pass equal n single-token e5m2
-    steps in order (each sees the codes the earlier ones stored), contiguous
-    and with a window; the stored codes are identical."""
+    steps in order (each sees the codes the earlier ones stored), with and
+    without a window; the stored codes are identical; a paged pool holding the
+    same logical cache gives the same result."""
     rng = np.random.default_rng(61)
     B, h_q, h_kv, d, cap, n = 2, 8, 2, 32, 40, 4
     Kc = oracle.quantize_e5m2(rng.standard_normal((B, h_kv, cap, d)))
@@ -803,6 +804,85 @@ def check_multi_e5m2(fn):
             assert np.allclose(r["out"][:, i], one["out"], rtol=0, atol=1e-12)
             assert np.allclose(r["lse"][:, i], one["lse"], rtol=0, atol=1e-12)
         assert np.array_equal(r["k_codes"], kc) and np.array_equal(r["v_codes"], vc)
+    # paged: the same logical cache dealt into permuted 8-token pages
+    ps = 8
+    npg = cap // ps
+    perm = rng.permutation(B * npg)
+    table = perm.reshape(B, npg)
+    Kp = np.zeros((B * npg, h_kv, ps, d), np.uint8)
+    Vp = np.zeros_like(Kp)
+    for b in range(B):
+        for lp in range(npg):
+            Kp[table[b, lp]] = Kc[b, :, lp * ps:(lp + 1) * ps]
+            Vp[table[b, lp]] = Vc[b, :, lp * ps:(lp + 1) * ps]
+    r = fn(Kc, Vc, q, k, v, lens, 10000.0, 0.2)
+    rp = fn(Kp, Vp, q, k, v, lens, 10000.0, 0.2, block_table=table, page_size=ps)
+    assert np.allclose(rp["out"], r["out"], rtol=0, atol=1e-12)
+    for b in range(B):
+        for lp in range(npg):
+            assert np.array_equal(rp["k_codes"][table[b, lp]], r["k_codes"][b, :, lp * ps:(lp + 1) * ps])
+
+
+def check_multi_u8(fn):
+    """n new tokens over a uint8 cache in one pass equal n single-token uint8
+    steps in order (each sees the codes, scales and zero points the earlier
+    ones stored), with and without a window; a paged pool holding the same
+    logical cache gives the same result."""
+    rng = np.random.default_rng(67)
+    B, h_q, h_kv, d, cap, n = 2, 8, 2, 32, 40, 4
+    Kc, Ks, Kz = oracle.quantize_u8(rng.standard_normal((B, h_kv, cap, d)))
+    Vc, Vs, Vz = oracle.quantize_u8(rng.standard_normal((B, h_kv, cap, d)))
+    Ksz = np.stack([Ks, Kz], -1).astype(np.float32)
+    Vsz = np.stack([Vs, Vz], -1).astype(np.float32)
+    q = oracle.round_bf16(rng.standard_normal((B, n, h_q, d)))
+    k = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    v = oracle.round_bf16(rng.standard_normal((B, n, h_kv, d)))
+    lens = np.array([40, 9])
+    for window in (0, 5):
+        r = fn(Kc, Ksz, Vc, Vsz, q, k, v, lens, 10000.0, 0.2, window=window)
+        kc, ksz, vc, vsz = Kc.copy(), Ksz.copy(), Vc.copy(), Vsz.copy()
+        for i in range(n):
+            one = oracle.decode_step_u8(kc, ksz, vc, vsz, q[:, i], k[:, i], v[:, i], lens - n + i + 1, 10000.0, 0.2,
+                                        window=window)
+            kc, ksz, vc, vsz = one["k_codes"], one["k_sz"], one["v_codes"], one["v_sz"]
+            assert np.allclose(r["out"][:, i], one["out"], rtol=0, atol=1e-12)
+            assert np.allclose(r["lse"][:, i], one["lse"], rtol=0, atol=1e-12)
+        for key, ref in (("k_codes", kc), ("k_sz", ksz), ("v_codes", vc), ("v_sz", vsz)):
+            assert np.array_equal(r[key], ref), key
+    ps = 8
+    npg = cap // ps
+    table = rng.permutation(B * npg).reshape(B, npg)
+    pools = []
+    for a in (Kc, Ksz, Vc, Vsz):
+        pool = np.zeros((B * npg, h_kv, ps) + a.shape[3:], a.dtype)
+        for b in range(B):
+            for lp in range(npg):
+                pool[table[b, lp]] = a[b, :, lp * ps:(lp + 1) * ps]
+        pools.append(pool)
+    r = fn(Kc, Ksz, Vc, Vsz, q, k, v, lens, 10000.0, 0.2)
+    rp = fn(*pools, q, k, v, lens, 10000.0, 0.2, block_table=table, page_size=ps)
+    assert np.allclose(rp["out"], r["out"], rtol=0, atol=1e-12)
+    for b in range(B):
+        for lp in range(npg):
+            assert np.array_equal(rp["k_codes"][table[b, lp]], r["k_codes"][b, :, lp * ps:(lp + 1) * ps])
+            assert np.array_equal(rp["v_sz"][table[b, lp]], r["v_sz"][b, :, lp * ps:(lp + 1) * ps])
+
+
+def test_multi_token_u8_pins():
+    check_multi_u8(oracle.decode_step_multi_u8)
+
+
+def test_multi_token_u8_planted_mistake_is_caught():
+    """Quantising the key before it is rotated (rotating the dequantised
+    codes) fails the pin."""
+    def quantise_first(k_codes, k_sz, v_codes, v_sz, q_new, k_new, v_new, seq_lens, rope_base, scale,
+                       block_table=None, page_size=0, window=0):
+        kc, ks, kz = oracle.quantize_u8(np.asarray(k_new, np.float64))
+        k_pre = oracle.dequantize_u8(kc, ks, kz)
+        return oracle.decode_step_multi_u8(k_codes, k_sz, v_codes, v_sz, q_new, k_pre, v_new, seq_lens, rope_base,
+                                           scale, block_table=block_table, page_size=page_size, window=window)
+    with pytest.raises(AssertionError):
+        check_multi_u8(quantise_first)
 
 
 def test_multi_token_e5m2_pins():
