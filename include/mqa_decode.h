@@ -129,11 +129,14 @@ typedef enum mqa_variant {
  * once, from its fp64 rotation -- and saturates magnitudes beyond 57344 to
  * it. q_new, k_new and v_new are bf16; attention on tensor cores only. One
  * new token per sequence runs on the warp-MMA kernels (codes widened to fp16,
- * fp16 query). Several new tokens (multi-token calls, prefill) run on the
- * tcgen05 kernel's fp8 form: the code tiles are the MMA's B operand as they
- * sit in memory, the query and the probabilities enter as two e4m3 parts
- * each (hi + lo, the query scaled by 64 first), so q and P keep about 8
- * significant bits of precision beyond a single e4m3 rounding.
+ * fp16 query) or, for 16 < G <= 32 contiguous at head_dim 128, the MQA
+ * tcgen05 kernel. Several new tokens with 32 or more query rows per kv head
+ * over a contiguous cache at head_dim 128 (multi-token calls, prefill) run
+ * on the tcgen05 kernel's fp8 form: the code tiles are the MMA's B operand as
+ * they sit in memory, the query and the probabilities enter as two e4m3
+ * parts each (hi + lo, the query scaled by 64 first), so q and P keep about 8
+ * significant bits of precision beyond a single e4m3 rounding; fewer rows, or
+ * a paged pool, take the warp-MMA kernels.
  *
  * Bounded waits: inside the attention kernels every wait for another warp's
  * progress (a tile landing, a tile freed, a product done) gives up after
@@ -325,12 +328,14 @@ MQA_API mqa_status gqa_decode_attention_noalloc(const mqa_kv_layout* layout, con
  *   <= 128 -- with the cache rows bit for bit those of the two calls.
  * 1 <= n_new <= 32 for the attention (kv_append_rope_multi takes any n_new;
  * longer runs of new tokens go to gqa_prefill_attention). n_new > 1 runs on
- * tensor cores over a bf16 cache, contiguous or paged (32 or more query rows
- * per kv head on the tcgen05 kernel, which gathers a paged key tile page by
- * page), or over a MQA_FP8_E5M2 cache that is
- * contiguous with head_dim 128 and at least 32 query rows per kv head
- * ((h_q / h_kv) * n_new >= 32; the tcgen05 kernel's fp8 form), and
- * MQA_ERR_UNSUPPORTED otherwise; n_new = 1 is exactly the single-token call.
+ * tensor cores only (MQA_ERR_UNSUPPORTED on CUDA cores): over a bf16 cache,
+ * contiguous or paged (32 or more query rows per kv head on the tcgen05
+ * kernel, which gathers a paged key tile page by page); over a MQA_FP8_E5M2
+ * cache (contiguous with head_dim 128 and (h_q / h_kv) * n_new >= 32: the
+ * tcgen05 kernel's fp8 form; otherwise the one-byte warp-MMA kernel); over a
+ * MQA_U8 cache (the one-byte warp-MMA kernel, contiguous or paged). Over a
+ * one-byte cache the append is always its own launch. n_new = 1 is exactly
+ * the single-token call.
  */
 MQA_API mqa_status kv_append_rope_multi(const mqa_kv_layout* layout, int32_t n_new, const void* q_new,
                                         const void* k_new, const void* v_new, const int32_t* pos, double rope_base,

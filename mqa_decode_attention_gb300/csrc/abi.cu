@@ -140,7 +140,7 @@ KernelShape decode_shape(const mqa_kv_layout* L, int variant, int n_new = 1) {
   if (use_tc05(L, variant, n_new)) return tc05_shape();
   if (variant == MQA_VARIANT_TENSOR_CORE && byte_cache(L->cache_dtype))
     return !tc05_keys_applies(G, n_new, L->head_dim, L->paged)
-               ? decode_u8_shape(L->head_dim, G, L->cache_dtype == MQA_FP8_E5M2)
+               ? decode_u8_shape(L->head_dim, G * n_new, L->cache_dtype == MQA_FP8_E5M2)
                : (L->cache_dtype == MQA_U8 ? tc05_keys_shape() : tc05_widen_shape());
   if (variant == MQA_VARIANT_TENSOR_CORE) return decode_mma_shape(L->head_dim, G * n_new);
   return decode_fma_shape(L->cache_dtype == MQA_BF16 ? kDtypeBf16 : kDtypeF32, L->head_dim, G);
@@ -152,10 +152,12 @@ int head_blocks(const mqa_kv_layout* L, const KernelShape& ks, int n_new = 1) {
 }
 
 
-// Multi-token decode runs on the bf16 tensor-core kernel only.
+// Multi-token decode runs on the tensor-core kernels: bf16 (warp-MMA or
+// tcgen05), uint8 and e5m2 (the one-byte warp-MMA kernel, or the tcgen05
+// kernel's fp8 form for 32 or more rows per kv head over a contiguous e5m2
+// cache).
 bool multi_supported(const mqa_kv_layout* L, int variant, int n_new) {
-  return n_new == 1 || (variant == MQA_VARIANT_TENSOR_CORE && L->cache_dtype == MQA_BF16) ||
-         use_tc05(L, variant, n_new);
+  return n_new == 1 || (variant == MQA_VARIANT_TENSOR_CORE && (L->cache_dtype == MQA_BF16 || byte_cache(L->cache_dtype)));
 }
 
 // Tokens one (sequence, kv head) may need read: the bound, or with a sliding

@@ -160,6 +160,19 @@ struct WarpAttnU8 {
         scale_log2);
   }
 
+  // Rows g and g + 8 from two row pointers (several new tokens: the warp's 16
+  // rows are (token, head) pairs, not consecutive heads); null = zeros.
+  __device__ __forceinline__ void init_rows(const float* qa, const float* qb, float scale_log2, int lane) {
+    const int c = lane & 3;
+    init_from(
+        [&](int ks, int hi) {
+          const float* q = hi ? qb : qa;
+          return q != nullptr ? *reinterpret_cast<const float4*>(q + (D / 4) * c + 4 * ks)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        },
+        scale_log2);
+  }
+
   // This lane's raw bf16 q_new values (rows g, g + 8 of the warp's 16 heads;
   // dims (D/4) c + 4 ks .. + 3: two rotation pairs), rows >= rows_valid zero.
   // Kept apart from init_rope so the loads are in flight while the cos / sin
@@ -237,10 +250,12 @@ struct WarpAttnU8 {
   // (16-row blocks CBS bytes apart) and of the (scale, zero) rows at ksz / vsz
   // (16-row blocks SBS bytes apart); only rows lo .. hi-1 of the 32 are real
   // tokens. The others may hold anything (NaN scales included): their scores
-  // are masked and their P' and zero points forced to 0.
-  template <uint32_t CBS, uint32_t SBS>
+  // are masked and their P' and zero points forced to 0. MULTI: row g sees
+  // only tokens [lo0, hi0) and row g + 8 only [lo1, hi1) (within [lo, hi)),
+  // and a row that has seen no token yet keeps a -inf maximum.
+  template <uint32_t CBS, uint32_t SBS, bool MULTI = false>
   __device__ __forceinline__ void step(uint32_t kc, uint32_t vc, uint32_t ksz, uint32_t vsz, int trow0, int lo,
-                                       int hi, int lane) {
+                                       int hi, int lane, int lo0 = 0, int hi0 = 32, int lo1 = 0, int hi1 = 32) {
     const int g = lane >> 2, c = lane & 3;
     auto lo2 = [](uint32_t x) { return F8 ? __byte_perm(x, 0u, kF8Lo) : codes_f16(x, kSelLo); };
     auto hi2 = [](uint32_t x) { return F8 ? __byte_perm(x, 0u, kF8Hi) : codes_f16(x, kSelHi); };
@@ -302,6 +317,17 @@ struct WarpAttnU8 {
         }
       }
     }
+    if constexpr (MULTI) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = nt * 8 + 2 * c + e;
+          if (t < lo0 || t >= hi0) s[nt][e] = -INFINITY;
+          if (t < lo1 || t >= hi1) s[nt][2 + e] = -INFINITY;
+        }
+      }
+    }
     if constexpr (!F8) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) vmax = fmaxf(vmax, fmaxf(sv[nt][0], sv[nt][1]));
@@ -317,17 +343,19 @@ struct WarpAttnU8 {
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     const bool moved = (mn0 != m0) || (mn1 != m1);
-    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+    // (MULTI: a row with no token yet subtracts 0 instead of its -inf maximum)
+    const float e0 = (MULTI && mn0 == -INFINITY) ? 0.f : mn0, e1 = (MULTI && mn1 == -INFINITY) ? 0.f : mn1;
+    const float a0 = fast_exp2(m0 - e0), a1 = fast_exp2(m1 - e1);
     m0 = mn0;
     m1 = mn1;
     float pr[4][4];
     float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      pr[nt][0] = fast_exp2(s[nt][0] - mn0);
-      pr[nt][1] = fast_exp2(s[nt][1] - mn0);
-      pr[nt][2] = fast_exp2(s[nt][2] - mn1);
-      pr[nt][3] = fast_exp2(s[nt][3] - mn1);
+      pr[nt][0] = fast_exp2(s[nt][0] - e0);
+      pr[nt][1] = fast_exp2(s[nt][1] - e0);
+      pr[nt][2] = fast_exp2(s[nt][2] - e1);
+      pr[nt][3] = fast_exp2(s[nt][3] - e1);
       sum0 += pr[nt][0] + pr[nt][1];
       sum1 += pr[nt][2] + pr[nt][3];
     }
@@ -448,7 +476,11 @@ struct WarpAttnU8 {
   }
 };
 
-template <int D, int HB, int STAGES, bool F8>
+// MULTI: n_new > 1 new tokens per sequence (the verification of drafted
+// tokens): the rows of a kv head are (new token i, query head h) pairs, row =
+// i G + h, and row i sees the tokens up to L - n + i only (the bf16 warp-MMA
+// kernel's scheme). The new rows come from a preceding append launch.
+template <int D, int HB, int STAGES, bool F8, bool MULTI>
 __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 2 : 1)
     decode_u8_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                      const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
@@ -471,6 +503,8 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   const int j = cta % p.h_kv;
   const int b = cta / p.h_kv;
   const int G = p.group;
+  const int nq = MULTI ? p.n_new : 1;  // new tokens (query rows per head) of each sequence
+  const int R = G * nq;                // query rows of this kv head
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -488,11 +522,12 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   long long limit = p.paged ? static_cast<long long>(p.max_pages) * p.page_size : p.capacity;
   if (limit > p.max_seq_len) limit = p.max_seq_len;
   int L = p.seq_lens[b];
-  if (L < 1 || L > limit) {
+  if (L < nq || L > limit) {
     if (threadIdx.x == 0 && split == 0 && hsb == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_SEQ_LEN));
-    L = L < 0 ? 0 : static_cast<int>(L > limit ? limit : L);
+    L = L < nq ? (L < 0 ? 0 : L) : static_cast<int>(limit);
   }
-  const int t_lo = p.window > 0 ? max(0, L - p.window) : 0;
+  // sliding window: tokens [t_lo, L) (t_lo of the first new token, the lowest)
+  const int t_lo = p.window > 0 ? max(0, L - nq + 1 - p.window) : 0;
   const int t_base = (t_lo / kTile) * kTile;
   const int t_begin = t_base + split * p.chunk;
   const int t_end = min(L, t_begin + p.chunk);
@@ -540,7 +575,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
       }
       if (*reinterpret_cast<volatile int*>(&s_abort)) break;
       const int t0 = t_begin + it * kTile;
-      if (!waited && L - 1 < t0 + kTile) {  // this tile holds the appended token
+      if (!waited && L - nq < t0 + kTile) {  // this tile holds an appended token
         grid_dependency_wait();
         waited = true;
       }
@@ -627,9 +662,27 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
     rope_table<D>(s_cs, p, p.pos[b], threadIdx.x, 2, C::kConsumerThreads);
     wa.init_rope(qraw, G - head0, s_cs, p.scale_log2, lane,
                  (p.fuse_append && split == 0 && ws == 0) ? p.q_rot_out + qoff : nullptr);
+  } else if (MULTI) {
+    if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
+    auto qrow = [&](int r) -> const float* {
+      if (r >= R) return nullptr;
+      const int i = r / G;
+      return p.q_rot + ((static_cast<long long>(b) * nq + i) * p.h_q + j * G + (r - i * G)) * D;
+    };
+    wa.init_rows(qrow(head0 + (lane >> 2)), qrow(head0 + (lane >> 2) + 8), p.scale_log2, lane);
   } else {
     if (p.early) grid_dependency_wait();  // q_rot is written by the append kernel
     wa.init(p.q_rot + (static_cast<long long>(b) * p.h_q + j * G + head0) * D, G - head0, p.scale_log2, lane);
+  }
+  // MULTI: the key range [ka, ke) of this lane's rows g and g + 8 (row of new
+  // token i: ends after position L - n + i; a window of W before that)
+  int ka0 = 0, ke0 = L, ka1 = 0, ke1 = L;
+  if (MULTI) {
+    const int i0 = min(head0 + (lane >> 2), R - 1) / G, i1 = min(head0 + (lane >> 2) + 8, R - 1) / G;
+    ke0 = L - nq + i0 + 1;
+    ke1 = L - nq + i1 + 1;
+    ka0 = p.window > 0 ? max(0, ke0 - p.window) : 0;
+    ka1 = p.window > 0 ? max(0, ke1 - p.window) : 0;
   }
 
   // warps 0, 1 of a head block take the even tiles, warps 2, 3 the odd
@@ -649,9 +702,16 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
     const uint32_t st = smem_u32(smem + stage * C::kStageBytes);
     const int tt = t_begin + it * kTile + trow0;
     const int lo = max(0, t_lo - tt), hi = min(32, t_end - tt);
-    if (lo < hi)
-      wa.template step<16 * D, 128>(st, st + C::kCodeBytes, st + 2 * C::kCodeBytes,
-                                    st + 2 * C::kCodeBytes + C::kSzBytes, trow0, lo, hi, lane);
+    if (lo < hi) {
+      if constexpr (MULTI)
+        wa.template step<16 * D, 128, true>(st, st + C::kCodeBytes, st + 2 * C::kCodeBytes,
+                                            st + 2 * C::kCodeBytes + C::kSzBytes, trow0, lo, hi, lane,
+                                            max(0, ka0 - tt), min(32, min(ke0, t_end) - tt), max(0, ka1 - tt),
+                                            min(32, min(ke1, t_end) - tt));
+      else
+        wa.template step<16 * D, 128>(st, st + C::kCodeBytes, st + 2 * C::kCodeBytes,
+                                      st + 2 * C::kCodeBytes + C::kSzBytes, trow0, lo, hi, lane);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
   }
@@ -688,7 +748,7 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   const int tid = threadIdx.x;
   for (int hbi = 0; hbi < HB; ++hbi) {
     const int hh0 = (hsb * HB + hbi) * 16;
-    const int n_rows = min(16, G - hh0);
+    const int n_rows = min(16, R - hh0);
     for (int idx = tid; idx < n_rows * D; idx += C::kConsumerThreads) {
       const int r = idx / D, d = idx - r * D;
       const int pc = (d % (D / 8)) * 8 + d / (D / 8);  // head dim d = column (D/8) + dim tile
@@ -707,7 +767,11 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
       }
       const float ov = den > 0.f ? num / den : 0.f;
       const float lse = den > 0.f ? (mx + log2f(den)) * 0.69314718055994530942f : -INFINITY;
-      const long long grow = static_cast<long long>(b) * p.h_q + j * G + hh0 + r;
+      long long grow = static_cast<long long>(b) * p.h_q + j * G + hh0 + r;  // output row [B, (n,) H_q]
+      if (MULTI) {
+        const int i = (hh0 + r) / G;
+        grow = (static_cast<long long>(b) * nq + i) * p.h_q + j * G + (hh0 + r - i * G);
+      }
       if (split_out) {
         p.o_part[(grow * S + split) * D + d] = ov;
         if (d == 0) p.lse_part[grow * S + split] = lse;
@@ -722,11 +786,11 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   }
 }
 
-template <int D, int HB, bool F8>
+template <int D, int HB, bool F8, bool MULTI>
 cudaError_t launch_u8_t(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
   constexpr int ST = U8Stages<D>::value;
   using C = U8Cfg<D, HB, ST, F8>;
-  auto kern = decode_u8_kernel<D, HB, ST, F8>;
+  auto kern = decode_u8_kernel<D, HB, ST, F8, MULTI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -750,7 +814,7 @@ KernelShape shape_t() {
   static std::atomic<int> occ{-1};
   int n = occ.load(std::memory_order_relaxed);
   if (n < 0) {
-    auto kern = decode_u8_kernel<D, HB, U8Stages<D>::value, F8>;
+    auto kern = decode_u8_kernel<D, HB, U8Stages<D>::value, F8, false>;
     n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmemBytes) != cudaSuccess) {
@@ -1055,7 +1119,7 @@ KernelShape decode_u8_shape(int head_dim, int group, bool f8) {
 }
 
 int decode_u8_heads_group(const DecodeParams& p) {
-  if (!p.paged || (p.page_size != 16 && p.page_size != 32) || p.group > 16) return 0;
+  if (!p.paged || (p.page_size != 16 && p.page_size != 32) || p.group > 16 || p.n_new > 1) return 0;
   if (p.h_kv % 4 == 0) return 4;
   if (p.h_kv % 2 == 0) return 2;
   return 0;
@@ -1074,11 +1138,17 @@ cudaError_t u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cud
   return hg == 4 ? launch_u8_heads_t<64, 4, 32, F8>(p, maps, stream) : launch_u8_heads_t<64, 2, 32, F8>(p, maps, stream);
 }
 
+template <bool F8, bool MULTI>
+cudaError_t u8_slices_m(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
+  const bool two = u8_hb(p.group * (MULTI ? p.n_new : 1)) == 2;
+  if (p.head_dim == 128)
+    return two ? launch_u8_t<128, 2, F8, MULTI>(p, maps, stream) : launch_u8_t<128, 1, F8, MULTI>(p, maps, stream);
+  return two ? launch_u8_t<64, 2, F8, MULTI>(p, maps, stream) : launch_u8_t<64, 1, F8, MULTI>(p, maps, stream);
+}
+
 template <bool F8>
 cudaError_t u8_slices(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
-  const bool two = u8_hb(p.group) == 2;
-  if (p.head_dim == 128) return two ? launch_u8_t<128, 2, F8>(p, maps, stream) : launch_u8_t<128, 1, F8>(p, maps, stream);
-  return two ? launch_u8_t<64, 2, F8>(p, maps, stream) : launch_u8_t<64, 1, F8>(p, maps, stream);
+  return p.n_new > 1 ? u8_slices_m<F8, true>(p, maps, stream) : u8_slices_m<F8, false>(p, maps, stream);
 }
 
 cudaError_t launch_decode_u8_heads(const DecodeParams& p, int hg, const CUtensorMap* maps, cudaStream_t stream) {

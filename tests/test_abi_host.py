@@ -176,4 +176,4 @@ def test_step_launches_refused(lib):
     assert lib.mqa_step_launches(ctypes.byref(_layout()), 33, 4096, 1, 2, None) == -1
     assert lib.mqa_step_launches(ctypes.byref(_layout(capacity=4096)), 2, 4096, 1, 1, None) == -1  # CUDA cores, n > 1
     u8 = _layout(cache_dtype=_abi.MQA_U8, k_scale_zero=FAKE, v_scale_zero=FAKE, capacity=4096)
-    assert lib.mqa_step_launches(ctypes.byref(u8), 2, 4096, 1, 2, None) == -1  # several tokens over uint8
+    assert lib.mqa_step_launches(ctypes.byref(u8), 2, 4096, 1, 2, None) == 2  # uint8: append launch + attention

@@ -160,20 +160,6 @@ def test_e5m2_nan_codes_past_the_sequence(m):
         assert np.max(np.abs(got["out"] - ref["out"])) <= BF16_TOL
 
 
-def test_e5m2_multi_token_is_refused(m):
-    """Several new tokens with fewer than 32 query rows per kv head (G x n):
-    no kernel takes them over an e5m2 cache."""
-    w = workload("gqa4k").with_(batch=1, h_q=8, h_kv=2)
-    kc8, vc8 = make_e5m2_cache((1, 2, 64), 128, seed=14)
-    lay = m.layout_contiguous(kc8.to(DEV), vc8.to(DEV), 8)
-    q = torch.zeros(1, 2, 8, 128, device=DEV)
-    out = torch.empty(1, 2, 8, 128, dtype=torch.bfloat16, device=DEV)
-    err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    with pytest.raises(m.MqaError):
-        m.gqa_decode_attention_multi(lay, 2, q, torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1, 1, out,
-                                     err=err)
-
-
 def _new_tokens(w, n, seed):
     q = normal((w.batch, n, w.h_q, w.head_dim), seed, 21)
     k = normal((w.batch, n, w.h_kv, w.head_dim), seed, 22)
@@ -360,3 +346,71 @@ def test_e5m2_mqa_full_size_sampled(m):
         ref = oracle.decode_step_e5m2(kc[None, None], vc[None, None], c.q_new[b:b + 1].cpu(), c.k_new[b:b + 1].cpu(),
                                       c.v_new[b:b + 1].cpu(), [L], w.rope_base, 1.0 / math.sqrt(128))
         assert np.max(np.abs(_np(bufs.out[b]) - ref["out"][0])) <= BF16_TOL, b
+
+
+SMALL_MULTI = [
+    # B, h_q, h_kv, lens, capacity, n: fewer than 32 (token, head) rows per kv
+    # head, on the warp-MMA one-byte kernel (fp16 query operand)
+    (2, 8, 2, [300, 64], 300, 2),     # G = 4 x 2
+    (2, 32, 8, [1000, 9], 1000, 4),   # G = 4 x 4
+    (1, 16, 2, [129], 129, 3),        # G = 8 x 3
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_MULTI, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}n{s[5]}")
+@pytest.mark.parametrize("splits", [1, 3])
+def test_e5m2_multi_token_small_groups(m, shape, splits):
+    """Several new tokens with fewer than 32 rows per kv head over an e5m2
+    cache (the one-byte warp-MMA kernel's multi-token form) against
+    decode_step_multi_e5m2."""
+    B, hq, hkv, lens, cap, n = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, seed=590 + hq + n)
+    kc8, vc8 = make_e5m2_cache((B, hkv, cap), 128, seed=31 + n)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_e5m2(_codes(kc8), _codes(vc8), q, k, v, lens, w.rope_base,
+                                        1.0 / math.sqrt(w.head_dim))
+    kd, vd = kc8.to(DEV), vc8.to(DEV)
+    lay = m.layout_contiguous(kd, vd, hq)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=splits, device=DEV, n_new=n)
+    m.decode_step_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, max(lens), bufs, w.rope_base,
+                        1.0 / math.sqrt(w.head_dim), num_splits=splits)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    got_out, got_lse = _np(bufs.out), _np(bufs.lse)
+    assert np.max(np.abs(got_out.reshape(ref["out"].shape) - ref["out"])) <= BF16_TOL
+    assert np.max(np.abs(got_lse.reshape(ref["lse"].shape) - ref["lse"])) <= BF16_TOL
+    assert_lse(got_lse.reshape(ref["lse"].shape), ref["q_rot"], oracle.dequantize_e5m2(ref["k_codes"]), lens,
+               1.0 / math.sqrt(w.head_dim), "f16")
+    assert np.array_equal(_codes(kd), ref["k_codes"]) and np.array_equal(_codes(vd), ref["v_codes"])
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_e5m2_multi_token_paged(m, page_size):
+    """Several new tokens over a paged e5m2 pool (the one-byte warp-MMA kernel
+    for every row count: the tcgen05 fp8 form reads contiguous caches only)."""
+    n = 8
+    w = workload("paged").with_(batch=3, h_q=32, h_kv=8, page_size=page_size, seed=600 + page_size)
+    lens = [700, n, 130]
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=2)
+    kc8, vc8 = make_e5m2_cache((pc.num_pages, w.h_kv, page_size), 128, seed=37)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_e5m2(_codes(kc8), _codes(vc8), q, k, v, lens, w.rope_base,
+                                        1.0 / math.sqrt(w.head_dim), block_table=pc.block_table,
+                                        page_size=page_size)
+    for splits in (1, 3):
+        kd, vd = kc8.to(DEV), vc8.to(DEV)
+        bt = pc.block_table.to(DEV)
+        lay = m.layout_paged(kd, vd, bt, w.h_q)
+        lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+        bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=splits, device=DEV, n_new=n)
+        m.decode_step_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, max(lens), bufs,
+                            w.rope_base, 1.0 / math.sqrt(w.head_dim), num_splits=splits)
+        torch.cuda.synchronize()
+        assert int(bufs.err.item()) == 0, splits
+        got_out, got_lse = _np(bufs.out), _np(bufs.lse)
+        assert np.max(np.abs(got_out.reshape(ref["out"].shape) - ref["out"])) <= BF16_TOL, splits
+        keys = paged_keys(oracle.dequantize_e5m2(ref["k_codes"]), pc.block_table, lens, page_size)
+        assert_lse(got_lse.reshape(ref["lse"].shape), ref["q_rot"], keys, lens, 1.0 / math.sqrt(w.head_dim), "f16",
+                   what=splits)
+        assert np.array_equal(_codes(kd), ref["k_codes"]) and np.array_equal(_codes(vd), ref["v_codes"])

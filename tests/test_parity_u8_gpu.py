@@ -318,3 +318,97 @@ def test_u8_mqa_full_size_sampled(m):
 
         ref = _oracle(sub, Case, Unit, paged=False)
         assert np.max(np.abs(_np(bufs.out[b]) - ref["out"][0])) <= BF16_TOL, b
+
+
+# ------------------------------------------------------------ several new tokens
+def run_u8_multi(m, w, n, u, q, k, v, lens, splits=0, window=0, table=None, page_size=0):
+    kc, vc = u.k_codes.to(DEV), u.v_codes.to(DEV)
+    ks, vs = u.k_sz.to(DEV), u.v_sz.to(DEV)
+    if table is not None:
+        bt = table.to(DEV)
+        lay = m.layout_paged(kc, vc, bt, w.h_q, window=window, k_scale_zero=ks, v_scale_zero=vs)
+    else:
+        lay = m.layout_contiguous(kc, vc, w.h_q, window=window, k_scale_zero=ks, v_scale_zero=vs)
+    lens_d = torch.as_tensor(lens, dtype=torch.int32).to(DEV)
+    max_len = int(max(lens))
+    bufs = m.DecodeBuffers.allocate(lay, max_len, num_splits=splits, device=DEV, n_new=n)
+    m.decode_step_multi(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), (lens_d - n).to(torch.int32), lens_d, max_len,
+                        bufs, w.rope_base, 1.0 / math.sqrt(w.head_dim), num_splits=splits)
+    torch.cuda.synchronize()
+    return dict(out=_np(bufs.out), lse=_np(bufs.lse), q_rot=_np(bufs.q_rot), err=int(bufs.err.item()),
+                k_codes=kc.cpu().numpy(), v_codes=vc.cpu().numpy(), k_sz=ks.cpu().numpy(), v_sz=vs.cpu().numpy())
+
+
+def _new_tokens(w, n, seed):
+    from synthetic import normal
+    return (normal((w.batch, n, w.h_q, w.head_dim), seed, 21), normal((w.batch, n, w.h_kv, w.head_dim), seed, 22),
+            normal((w.batch, n, w.h_kv, w.head_dim), seed, 23))
+
+
+def check_multi(got, ref, lens, w, paged_table=None, page_size=0, window=0, what=None):
+    assert got["err"] == 0, what
+    assert np.max(np.abs(got["out"].reshape(ref["out"].shape) - ref["out"])) <= BF16_TOL, what
+    assert np.max(np.abs(got["lse"].reshape(ref["lse"].shape) - ref["lse"])) <= BF16_TOL, what
+    check_u8_append(got, ref)
+    kd = oracle.dequantize_u8(ref["k_codes"], ref["k_sz"][..., 0], ref["k_sz"][..., 1])
+    ks = np.asarray(ref["k_sz"][..., :1], np.float64)
+    if paged_table is not None:
+        kd = paged_keys(kd, paged_table, lens, page_size)
+        ks = paged_keys(ks, paged_table, lens, page_size)
+    assert_lse(got["lse"].reshape(ref["lse"].shape), ref["q_rot"], kd, lens, 1.0 / math.sqrt(w.head_dim), "f16",
+               window=window, what=what, key_scales=ks[..., 0])
+
+
+MULTI = [
+    # B, h_q, h_kv, d, lens, capacity, n
+    (2, 32, 8, 128, [1000, 257], 1000, 4),   # G = 4 x 4 tokens: one 16-row block
+    (2, 32, 8, 128, [300, 6], 300, 6),       # 24 rows, L = n
+    (3, 16, 2, 128, [129, 64, 65], 130, 2),  # G = 8 x 2
+    (1, 32, 1, 128, [500], 500, 3),          # MQA: 96 rows, three CTAs of 32
+    (2, 12, 3, 64, [200, 33], 200, 8),       # d = 64, G = 4 x 8
+]
+
+
+@pytest.mark.parametrize("shape", MULTI, ids=lambda s: f"B{s[0]}q{s[1]}kv{s[2]}d{s[3]}n{s[6]}")
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_u8_multi_token_matches_oracle(m, shape, splits):
+    """Several new tokens per sequence over a uint8 cache (the warp-MMA uint8
+    kernel, rows = (token, head) pairs with per-row key limits) against the
+    oracle's decode_step_multi_u8: the appended rows (codes, scales, zero
+    points) bit for bit, outputs within 2e-2, lse against the model."""
+    B, hq, hkv, d, lens, cap, n = shape
+    w = workload("gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, head_dim=d, seed=820 + hq + d + n)
+    u = make_u8_cache((B, hkv, cap), d, 83 + n)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, q, k, v, lens, w.rope_base,
+                                      1.0 / math.sqrt(d))
+    got = run_u8_multi(m, w, n, u, q, k, v, lens, splits=splits)
+    check_multi(got, ref, lens, w, what=splits)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+def test_u8_multi_token_paged(m, page_size):
+    n = 5
+    w = workload("paged").with_(batch=4, h_q=16, h_kv=4, page_size=page_size, seed=840 + page_size)
+    lens = [700, n, 17, 64]
+    pc, u = _paged(w, lens, 85)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, q, k, v, lens, w.rope_base,
+                                      1.0 / math.sqrt(w.head_dim), block_table=pc.block_table, page_size=page_size)
+    for splits in (1, 3, 0):
+        got = run_u8_multi(m, w, n, u, q, k, v, lens, splits=splits, table=pc.block_table, page_size=page_size)
+        check_multi(got, ref, lens, w, paged_table=pc.block_table, page_size=page_size, what=splits)
+
+
+@pytest.mark.parametrize("window", [1, 3, 100])
+def test_u8_multi_token_window(m, window):
+    n = 5
+    w = workload("gqa4k").with_(batch=3, h_q=16, h_kv=4, seed=851)
+    lens = [700, 70, 5]
+    u = make_u8_cache((3, 4, 704), 128, 86)
+    q, k, v = _new_tokens(w, n, w.seed)
+    ref = oracle.decode_step_multi_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, q, k, v, lens, w.rope_base,
+                                      1.0 / math.sqrt(128), window=window)
+    for splits in (1, 3, 0):
+        got = run_u8_multi(m, w, n, u, q, k, v, lens, splits=splits, window=window)
+        check_multi(got, ref, lens, w, window=window, what=(window, splits))
