@@ -90,18 +90,28 @@ def test_paged_step_graph(m):
     assert np.max(np.abs(go.double().numpy() - ref["out"])) <= TOL
 
 
-def test_multi_token_step_graph(m):
-    """Four new tokens per sequence on the tcgen05 kernel (G x n = 32 rows): the
-    append launch and the attention launch that starts while it runs."""
-    w = workload("gqa4k").with_(batch=2, h_q=32, h_kv=4, seed=970)
-    n, lens = 4, [400, 33]
-    c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=400)
-    q = normal((2, n, 32, 128), w.seed, 21, "bf16")
-    k = normal((2, n, 4, 128), w.seed, 22, "bf16")
-    v = normal((2, n, 4, 128), w.seed, 23, "bf16")
+@pytest.mark.parametrize("hq,hkv,n,paged", [(32, 4, 4, False), (32, 8, 32, False), (32, 8, 8, True)],
+                         ids=["tc05_fused", "tc05_append_launch", "tc05_paged_fused"])
+def test_multi_token_step_graph(m, hq, hkv, n, paged):
+    """Several new tokens per sequence on the tcgen05 kernel: one launch (the
+    kernel appends), or the append launch and the attention launch that
+    starts while it runs; contiguous and paged."""
+    w = workload("paged" if paged else "gqa4k").with_(batch=2, h_q=hq, h_kv=hkv, page_size=32, seed=970 + n)
+    lens = [400, n + 33]
+    q = normal((2, n, hq, 128), w.seed, 21, "bf16")
+    k = normal((2, n, hkv, 128), w.seed, 22, "bf16")
+    v = normal((2, n, hkv, 128), w.seed, 23, "bf16")
     scale = 1.0 / math.sqrt(128)
-    ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, scale, "bf16")
-    lay = m.layout_contiguous(c.k_cache.to(DEV), c.v_cache.to(DEV), w.h_q)
+    if paged:
+        pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+        ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, scale, "bf16",
+                                       block_table=pc.block_table, page_size=32)
+        bt = pc.block_table.to(DEV)
+        lay = m.layout_paged(pc.k_pool.to(DEV), pc.v_pool.to(DEV), bt, hq)
+    else:
+        c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=400)
+        ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, scale, "bf16")
+        lay = m.layout_contiguous(c.k_cache.to(DEV), c.v_cache.to(DEV), hq)
     bufs = m.DecodeBuffers.allocate(lay, 400, num_splits=0, device=DEV, n_new=n)
     lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
@@ -110,4 +120,35 @@ def test_multi_token_step_graph(m):
     (eo, ee), (go, ge) = _capture_and_replay(step)
     assert ee == 0 and ge == 0
     assert torch.equal(eo, go)
-    assert np.max(np.abs(go.double().numpy().reshape(2, n, 32, 128) - ref["out"])) <= TOL
+    assert np.max(np.abs(go.double().numpy().reshape(2, n, hq, 128) - ref["out"])) <= TOL
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_prefill_step_graph(m, paged):
+    """The prefill step (append launch + the two-query-tile prefill kernel)."""
+    n, pre = 300, 20
+    w = workload("paged" if paged else "gqa4k").with_(batch=2, h_q=8, h_kv=2, page_size=64, seed=980)
+    lens = [pre + n, n]
+    q = normal((2, n, 8, 128), w.seed, 21, "bf16")
+    k = normal((2, n, 2, 128), w.seed, 22, "bf16")
+    v = normal((2, n, 2, 128), w.seed, 23, "bf16")
+    scale = 1.0 / math.sqrt(128)
+    if paged:
+        pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+        ref = oracle.decode_step_multi(pc.k_pool, pc.v_pool, q, k, v, lens, w.rope_base, scale, "bf16",
+                                       block_table=pc.block_table, page_size=64)
+        bt = pc.block_table.to(DEV)
+        lay = m.layout_paged(pc.k_pool.to(DEV), pc.v_pool.to(DEV), bt, 8)
+    else:
+        c = make_contiguous_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), capacity=pre + n)
+        ref = oracle.decode_step_multi(c.k_cache, c.v_cache, q, k, v, lens, w.rope_base, scale, "bf16")
+        lay = m.layout_contiguous(c.k_cache.to(DEV), c.v_cache.to(DEV), 8)
+    bufs = m.DecodeBuffers.allocate(lay, pre + n, num_splits=1, device=DEV, n_new=n)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    step = Step(lambda: m.prefill_step(lay, n, qd, kd, vd, lens_d - n, lens_d, pre + n, bufs, w.rope_base, scale),
+                bufs)
+    (eo, ee), (go, ge) = _capture_and_replay(step)
+    assert ee == 0 and ge == 0
+    assert torch.equal(eo, go)
+    assert np.max(np.abs(go.double().numpy().reshape(2, n, 8, 128) - ref["out"])) <= TOL
