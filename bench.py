@@ -974,12 +974,21 @@ def bench_prefill(args):
     full = torch.full((w.batch,), n, dtype=torch.int32)
     if w.paged:  # the prompt's rows go to the pages the (permuted) block table names
         pc = make_paged_case(w, dev, seq_lens=full)
-        lay = m.layout_paged(pc.k_pool, pc.v_pool, pc.block_table, w.h_q)
-        lens = pc.seq_lens
+        rows_shape, lens, table = (pc.num_pages, w.h_kv, pc.page_size), pc.seq_lens, pc.block_table
+        kb, vb = pc.k_pool, pc.v_pool
     else:
         case = make_contiguous_case(w, dev, seq_lens=full, capacity=n)
-        lay = m.layout_contiguous(case.k_cache, case.v_cache, w.h_q)
-        lens = case.seq_lens
+        rows_shape, lens, table = (w.batch, w.h_kv, n), case.seq_lens, None
+        kb, vb = case.k_cache, case.v_cache
+    extra = {}
+    if args.cache == "u8":  # codes with per-row (scale, zero point)
+        u = make_u8_cache(rows_shape, w.head_dim, w.seed + 5, dev)
+        kb, vb = u.k_codes, u.v_codes
+        extra = dict(k_scale_zero=u.k_sz, v_scale_zero=u.v_sz)
+    elif args.cache == "fp8":
+        kb, vb = make_e5m2_cache(rows_shape, w.head_dim, w.seed + 5, dev)
+    lay = (m.layout_paged(kb, vb, table, w.h_q, **extra) if w.paged else
+           m.layout_contiguous(kb, vb, w.h_q, **extra))
     q = normal((w.batch, n, w.h_q, w.head_dim), w.seed, S_QM, w.dtype, dev)
     k = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_KM, w.dtype, dev)
     v = normal((w.batch, n, w.h_kv, w.head_dim), w.seed, S_VM, w.dtype, dev)
@@ -1036,15 +1045,21 @@ def bench_prefill(args):
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 6),
         "higher_is_better": True,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 q/k/v; empty cache before the prompt)",
+        "dtype": {"native": "bf16", "u8": "u8", "fp8": "fp8_e5m2"}[args.cache],
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v; " + {"native": "bf16", "u8": "uint8", "fp8": "fp8 e5m2"}[args.cache]
+                + " cache, empty before the prompt)",
         "config": {"workload": f"prefill: batch {w.batch}, {n}-token prompts, H_q {w.h_q}, H_kv {w.h_kv}, "
                                f"head_dim {w.head_dim}, causal, RoPE base 10000, "
-                               + (f"paged bf16 pool (page_size {w.page_size}, pages dealt by a seeded permutation)"
-                                  if w.paged else "contiguous bf16 cache"),
+                               + (f"paged pool (page_size {w.page_size}, pages dealt by a seeded permutation)"
+                                  if w.paged else "contiguous cache")
+                               + {"native": ", bf16", "u8": ", uint8 codes + (scale, zero point)", "fp8": ", fp8 e5m2"}[args.cache],
                    "flops_per_step": flops},
         "kernels_ms": {"mqa_prefill_step": round(ms_step, 6), "standalone_gqa_prefill_attention": round(attn_ms, 6)},
-        "roofline": {"bound": "tensor", "kernel": ("attn_tc05_prefill_kernel" if w.dtype == "bf16" else "attn_tc05_kernel"), "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor",
+                     "kernel": ("attn_tc05_prefill_kernel" if args.cache == "native" else
+                                "decode_u8_kernel (multi-token form)" if args.cache == "u8" or w.paged else
+                                "attn_tc05_kernel (fp8 form)"),
+                     "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)" if peaks else "fallback"},
         "gpu_launches": 2 * K,

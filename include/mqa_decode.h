@@ -377,7 +377,10 @@ MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_n
  * head_dim 128 with a bf16 cache, contiguous or paged (a key tile gathered
  * page by page from the pool the block table names, the prompt's rows
  * appended into its pages), or a contiguous MQA_FP8_E5M2 cache (the kernel's
- * fp8 form described with MQA_FP8_E5M2); MQA_ERR_UNSUPPORTED otherwise. No
+ * fp8 form described with MQA_FP8_E5M2). A MQA_U8 cache (contiguous or paged)
+ * and a paged MQA_FP8_E5M2 pool, head_dim 64 or 128, take the one-byte
+ * warp-MMA kernel's multi-token form over the whole prompt instead (32 rows per
+ * block; correct, not tuned for prompts). MQA_ERR_UNSUPPORTED otherwise. No
  * workspace. A block-table entry outside the pool for a page the prompt
  * attends or is appended to sets MQA_DEVERR_PAGE_RANGE (that page reads as
  * zeros). A bounded wait that runs out sets

@@ -521,10 +521,12 @@ bool fusable_multi(const mqa_kv_layout* L, int variant, int n_new) {
 mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const int32_t* seq_lens, int32_t max_seq_len,
                           float scale, int32_t num_splits, void* out, int32_t out_dtype, float* lse_out,
                           void* workspace, size_t workspace_bytes, int32_t variant, int32_t* err_word,
-                          mqa_stream_t stream, int early, const RopeArgs* rope, int n_new = 1) {
+                          mqa_stream_t stream, int early, const RopeArgs* rope, int n_new = 1, int prefill = 0) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if (n_new < 1 || n_new > kMaxNewTokens) return MQA_ERR_INVALID_ARG;
+  // (prefill over a one-byte cache takes this path with the whole prompt)
+  if (n_new < 1 || (!prefill && n_new > kMaxNewTokens)) return MQA_ERR_INVALID_ARG;
+  if (static_cast<long long>(layout->batch) * n_new * layout->h_q > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
   if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
   if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
       (lse_out && !aligned(lse_out, 4)))
@@ -765,14 +767,29 @@ combine:
 
 // Causal attention of the last n_new tokens of every sequence on tcgen05
 // (prefill): contiguous bf16 cache, head_dim 128.
+// Prefill over a uint8 cache, or a paged e5m2 pool: the one-byte warp-MMA
+// kernel's multi-token form over the whole prompt (rows = (token, head) pairs,
+// 32 per block; every block streams the keys up to its last row).
+bool prefill_on_byte_kernel(const mqa_kv_layout* L) {
+  return L->cache_dtype == MQA_U8 || (L->cache_dtype == MQA_FP8_E5M2 && L->paged);
+}
+
+// The cache types and shapes gqa_prefill_attention takes.
+bool prefill_supported(const mqa_kv_layout* L) {
+  if (prefill_on_byte_kernel(L)) return L->head_dim == 64 || L->head_dim == 128;
+  return (L->cache_dtype == MQA_BF16 || L->cache_dtype == MQA_FP8_E5M2) && L->head_dim == 128;
+}
+
 mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_rot, const int32_t* seq_lens,
                         int32_t max_seq_len, float scale, void* out, int32_t out_dtype, float* lse_out,
                         int32_t* err_word, mqa_stream_t stream, int early) {
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) ||
-      (layout->paged && layout->cache_dtype != MQA_BF16) || layout->head_dim != 128)
-    return MQA_ERR_UNSUPPORTED;
+  if (!prefill_supported(layout)) return MQA_ERR_UNSUPPORTED;
+  if (prefill_on_byte_kernel(layout))
+    return attention_impl(layout, q_rot, seq_lens, max_seq_len, scale, /*num_splits=*/1, out, out_dtype, lse_out,
+                          nullptr, 0, MQA_VARIANT_TENSOR_CORE, err_word, stream, early, nullptr, n_new,
+                          /*prefill=*/1);
   if (n_new < 1 || static_cast<long long>(layout->batch) * n_new > (1ll << 31) - 1) return MQA_ERR_INVALID_ARG;
   if (!q_rot || !seq_lens || !out || !err_word) return MQA_ERR_INVALID_ARG;
   if (!aligned(q_rot, 16) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(err_word, 4) ||
@@ -845,9 +862,7 @@ mqa_status mqa_prefill_step(const mqa_kv_layout* layout, int32_t n_new, const vo
   // the attention's own checks first, so nothing is launched for a call that fails
   const mqa_status st = check_layout(layout);
   if (st != MQA_OK) return st;
-  if ((layout->cache_dtype != MQA_BF16 && layout->cache_dtype != MQA_FP8_E5M2) ||
-      (layout->paged && layout->cache_dtype != MQA_BF16) || layout->head_dim != 128)
-    return MQA_ERR_UNSUPPORTED;
+  if (!prefill_supported(layout)) return MQA_ERR_UNSUPPORTED;
   if (!seq_lens || !out || max_seq_len < n_new || max_seq_len > token_limit(layout)) return MQA_ERR_INVALID_ARG;
   if (out_dtype != MQA_BF16 && out_dtype != MQA_F32) return MQA_ERR_UNSUPPORTED;
   const mqa_status a = append_impl(layout, q_new, k_new, v_new, pos, rope_base, q_rot, err_word, stream, n_new);

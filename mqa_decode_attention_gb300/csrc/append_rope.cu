@@ -279,9 +279,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 // that forms the token's d/2 fp64 sines and cosines once and rotates every
 // query and kv head of it, with the arithmetic of append_rope_kernel (the
 // per-head-block grid would evaluate the same fp64 table once per head block).
-template <typename T>
+// BYTE: a uint8 (1) or e5m2 (2) cache: one warp per kv head row rotates k in
+// fp64 and quantises the row as append_rope_kernel does (uint8: the row's
+// minimum and maximum over a warp reduction, the same set of values, so the
+// same scale and zero point).
+template <typename T, int BYTE = 0>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(const AppendParams p) {
-  constexpr bool kFast = std::is_same<T, __nv_bfloat16>::value;  // as in append_rope_kernel
+  constexpr bool kFast = std::is_same<T, __nv_bfloat16>::value && BYTE == 0;  // as in append_rope_kernel
   __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];  // fp64 cos / sin; kFast: s_cos holds the angle
   __shared__ float s_cf[kMaxHalfDim], s_sf[kMaxHalfDim];    // kFast: fp32 cos / sin of the angle
   __shared__ long long s_row, s_stride;
@@ -349,9 +353,63 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
     *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
   }
   if (!s_ok) return;
-  // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
   const T* ks = static_cast<const T*>(p.k_new) + static_cast<long long>(bt) * p.h_kv * D;
   const T* vs = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
+  if constexpr (BYTE != 0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int h = warp; h < p.h_kv; h += kAppendThreads / 32) {
+      const long long row = s_row + static_cast<long long>(h) * s_stride;  // element (byte) offset of the row
+      uint8_t* kc = static_cast<uint8_t*>(p.k_cache) + row;
+      uint8_t* vc = static_cast<uint8_t*>(p.v_cache) + row;
+      float kmn = INFINITY, kmx = -INFINITY, vmn = INFINITY, vmx = -INFINITY;
+      double xr[2], yr[2];
+      float2 vv[2];
+      for (int u = 0; u < 2; ++u) {
+        const int i = lane + 32 * u;
+        if (i >= half) break;
+        const float2 x = Elem<T>::load2(ks + h * D + 2 * i);
+        vv[u] = Elem<T>::load2(vs + h * D + 2 * i);
+        const double xd = x.x, yd = x.y, c = s_cos[i], sn = s_sin[i];
+        xr[u] = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, sn));
+        yr[u] = __dadd_rn(__dmul_rn(xd, sn), __dmul_rn(yd, c));
+        if constexpr (BYTE == 2) {
+          *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(e5m2_code(xr[u]) | (e5m2_code(yr[u]) << 8));
+          *reinterpret_cast<uint16_t*>(vc + 2 * i) =
+              static_cast<uint16_t>(e5m2_code(vv[u].x) | (e5m2_code(vv[u].y) << 8));
+        } else {
+          const float kx = __double2float_rn(xr[u]), ky = __double2float_rn(yr[u]);
+          kmn = fminf(kmn, fminf(kx, ky));
+          kmx = fmaxf(kmx, fmaxf(kx, ky));
+          vmn = fminf(vmn, fminf(vv[u].x, vv[u].y));
+          vmx = fmaxf(vmx, fmaxf(vv[u].x, vv[u].y));
+        }
+      }
+      if constexpr (BYTE == 1) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, off));
+          kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, off));
+          vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, off));
+          vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
+        }
+        const float2 ksz = u8_params(kmn, kmx), vsz = u8_params(vmn, vmx);
+        for (int u = 0; u < 2; ++u) {
+          const int i = lane + 32 * u;
+          if (i >= half) break;
+          const float kx = __double2float_rn(xr[u]), ky = __double2float_rn(yr[u]);
+          *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(u8_code(kx, ksz) | (u8_code(ky, ksz) << 8));
+          *reinterpret_cast<uint16_t*>(vc + 2 * i) =
+              static_cast<uint16_t>(u8_code(vv[u].x, vsz) | (u8_code(vv[u].y, vsz) << 8));
+        }
+        if (lane == 0) {
+          p.k_sz[row / D] = ksz;
+          p.v_sz[row / D] = vsz;
+        }
+      }
+    }
+    return;
+  }
+  // k: fp64 rotation, one rounding to the cache dtype; v: bit copy
   T* kc = static_cast<T*>(p.k_cache) + s_row;
   T* vc = static_cast<T*>(p.v_cache) + s_row;
   for (int idx = threadIdx.x; idx < p.h_kv * half; idx += kAppendThreads) {
@@ -375,14 +433,18 @@ KernelShape append_rope_shape() { return {kAppendThreads, 0, 0, 0}; }
 
 cudaError_t launch_append_rope(const AppendParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  if ((p.cache_dtype == kDtypeBf16 || p.cache_dtype == kDtypeF32) && static_cast<long long>(p.batch) * p.n_new >= 256) {
+  if (static_cast<long long>(p.batch) * p.n_new >= 256) {
     // one block per token forms its fp64 table once for all heads: from a few
     // hundred tokens the per-head-block tables' fp64 work costs more than the
     // parallelism they buy (measured, gqa4k shapes: 256 tokens 21.6 -> 17.3 µs;
-    // at 64 and 128 tokens the per-head-block grid stays faster)
+    // at 64 and 128 tokens the per-head-block grid stays faster; one-byte
+    // caches, whose tables are fp64 sines and cosines: 8 x 4096 tokens e5m2
+    // 3.3 ms on the per-head-block grid)
     cfg.gridDim = dim3(p.batch * p.n_new);
     cfg.blockDim = dim3(kAppendThreads);
     cfg.stream = stream;
+    if (p.cache_dtype == kDtypeU8) return cudaLaunchKernelEx(&cfg, append_rope_tokens_kernel<__nv_bfloat16, 1>, p);
+    if (p.cache_dtype == kDtypeF8) return cudaLaunchKernelEx(&cfg, append_rope_tokens_kernel<__nv_bfloat16, 2>, p);
     if (p.cache_dtype == kDtypeBf16) return cudaLaunchKernelEx(&cfg, append_rope_tokens_kernel<__nv_bfloat16>, p);
     return cudaLaunchKernelEx(&cfg, append_rope_tokens_kernel<float>, p);
   }

@@ -530,7 +530,13 @@ __global__ void __launch_bounds__(U8Cfg<D, HB, STAGES, F8>::kThreads, HB == 1 ? 
   const int t_lo = p.window > 0 ? max(0, L - nq + 1 - p.window) : 0;
   const int t_base = (t_lo / kTile) * kTile;
   const int t_begin = t_base + split * p.chunk;
-  const int t_end = min(L, t_begin + p.chunk);
+  int t_end = min(L, t_begin + p.chunk);
+  if (MULTI) {
+    // keys past this block's last row are masked for all of its rows (a
+    // prompt's early rows read only the early keys)
+    const int last_row = min(R, (hsb + 1) * HB * 16) - 1;
+    t_end = min(t_end, L - nq + last_row / G + 1);
+  }
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
 
   // the fused append (no append launch precedes this one): one block per

@@ -148,11 +148,9 @@ def test_prefill_errors_and_refusals(m):
     wp = workload("paged").with_(batch=1, h_q=8, h_kv=2, seed=614)
     pc = make_paged_case(wp, "cpu", seq_lens=torch.tensor([64], dtype=torch.int32))
     bt = pc.block_table.to(DEV)
-    codes = torch.zeros(pc.k_pool.shape, dtype=torch.uint8, device=DEV)
-    sz = torch.ones(pc.k_pool.shape[:-1] + (2,), dtype=torch.float32, device=DEV)
-    lay_u8 = m.layout_paged(codes, codes.clone(), bt, 8, k_scale_zero=sz, v_scale_zero=sz.clone())
-    with pytest.raises(m.MqaError):  # paged pools: bf16 only
-        m.gqa_prefill_attention(lay_u8, n, q_rot[:1], torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1,
+    lay_f32 = m.layout_paged(pc.k_pool.float().to(DEV), pc.v_pool.float().to(DEV), bt, 8)
+    with pytest.raises(m.MqaError):  # an fp32 (debug) cache has no prefill
+        m.gqa_prefill_attention(lay_f32, n, q_rot[:1], torch.tensor([64], dtype=torch.int32, device=DEV), 64, 0.1,
                                 out[:1], err=err)
 
 
@@ -285,3 +283,67 @@ def test_prefill_paged_bad_page_is_reported(m):
     got = run_prefill_paged(m, w, n, pc, q, k, v, lens, table=table)
     assert got["err"] & m.MQA_DEVERR_PAGE_RANGE
     assert np.max(np.abs(got["out"][1] - ref["out"][1])) <= TOL
+
+
+# ------------------------------------------------------- one-byte caches
+@pytest.mark.parametrize("paged, pre", [(False, 0), (False, 70), (True, 0), (True, 45)],
+                         ids=["contiguous", "contiguous_prefix", "paged", "paged_prefix"])
+def test_prefill_u8_matches_oracle(m, paged, pre):
+    """Prefill over a uint8 cache (the one-byte warp-MMA kernel's multi-token
+    form over the whole prompt) against decode_step_multi_u8: the prompt's
+    codes, scales and zero points bit for bit, outputs within 2e-2."""
+    from synthetic import make_u8_cache
+    n, B, hq, hkv = 150, 2, 8, 2
+    lens = [pre + n, n]
+    w = workload("paged" if paged else "gqa4k").with_(batch=B, h_q=hq, h_kv=hkv, page_size=32, seed=760 + pre)
+    q, k, v = new_tokens(w, n)
+    scale = 1.0 / math.sqrt(128)
+    if paged:
+        pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+        u = make_u8_cache((pc.num_pages, hkv, 32), 128, 77)
+        ref = oracle.decode_step_multi_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, q, k, v, lens, w.rope_base, scale,
+                                          block_table=pc.block_table, page_size=32)
+        bt = pc.block_table.to(DEV)
+    else:
+        u = make_u8_cache((B, hkv, pre + n), 128, 77)
+        ref = oracle.decode_step_multi_u8(u.k_codes, u.k_sz, u.v_codes, u.v_sz, q, k, v, lens, w.rope_base, scale)
+    kc, vc, ks, vs = u.k_codes.to(DEV), u.v_codes.to(DEV), u.k_sz.to(DEV), u.v_sz.to(DEV)
+    lay = (m.layout_paged(kc, vc, bt, hq, k_scale_zero=ks, v_scale_zero=vs) if paged else
+           m.layout_contiguous(kc, vc, hq, k_scale_zero=ks, v_scale_zero=vs))
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=1, device=DEV, n_new=n)
+    m.prefill_step(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, max(lens), bufs, w.rope_base, scale)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    out = _np(bufs.out).reshape(ref["out"].shape)
+    assert np.max(np.abs(out - ref["out"])) <= TOL
+    assert np.max(np.abs(_np(bufs.lse).reshape(ref["lse"].shape) - ref["lse"])) <= TOL
+    assert np.array_equal(kc.cpu().numpy(), ref["k_codes"]) and np.array_equal(vc.cpu().numpy(), ref["v_codes"])
+    for got, want in ((ks, ref["k_sz"]), (vs, ref["v_sz"])):
+        assert np.array_equal(got.cpu().numpy().view(np.uint32), np.asarray(want, np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("pre", [0, 40])
+def test_prefill_e5m2_paged_matches_oracle(m, pre):
+    """Prefill over a paged e5m2 pool (the one-byte warp-MMA kernel) against
+    decode_step_multi_e5m2."""
+    from synthetic import make_e5m2_cache
+    n, B, hq, hkv = 140, 2, 16, 2
+    lens = [pre + n, n + 5]
+    w = workload("paged").with_(batch=B, h_q=hq, h_kv=hkv, page_size=16, seed=780 + pre)
+    pc = make_paged_case(w, "cpu", seq_lens=torch.tensor(lens, dtype=torch.int32), spare_pages=1)
+    kc8, vc8 = make_e5m2_cache((pc.num_pages, hkv, 16), 128, seed=79)
+    q, k, v = new_tokens(w, n)
+    scale = 1.0 / math.sqrt(128)
+    codes = lambda t: t.detach().cpu().view(torch.uint8).numpy()
+    ref = oracle.decode_step_multi_e5m2(codes(kc8), codes(vc8), q, k, v, lens, w.rope_base, scale,
+                                        block_table=pc.block_table, page_size=16)
+    kd, vd, bt = kc8.to(DEV), vc8.to(DEV), pc.block_table.to(DEV)
+    lay = m.layout_paged(kd, vd, bt, hq)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    bufs = m.DecodeBuffers.allocate(lay, max(lens), num_splits=1, device=DEV, n_new=n)
+    m.prefill_step(lay, n, q.to(DEV), k.to(DEV), v.to(DEV), lens_d - n, lens_d, max(lens), bufs, w.rope_base, scale)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    assert np.max(np.abs(_np(bufs.out).reshape(ref["out"].shape) - ref["out"])) <= TOL
+    assert np.array_equal(codes(kd), ref["k_codes"]) and np.array_equal(codes(vd), ref["v_codes"])
