@@ -226,6 +226,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// q_rot [batch n_new tokens][h_q][128] fp32 for the prefill kernel: a box is
+// `rows` consecutive rows (group) of one kv head, i.e. rows / group tokens x
+// the group's heads x 128 dims, unswizzled (512-byte rows).
+bool make_q_map(CUtensorMap* map, const float* q_rot, int batch, int n_new, int h_q, int group, int rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(h_q), static_cast<cuuint64_t>(batch) * n_new};
+  const cuuint64_t strides[2] = {128 * 4, static_cast<cuuint64_t>(h_q) * 128 * 4};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(rows / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(q_rot), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // TMA descriptors for the tensor-core path: 128-byte swizzled boxes of
 // 64 columns, kTile rows (contiguous) or one page (paged, pages shorter than
 // a tile). With `merged`, head_dim 128 is described as 64 columns x 2 halves
@@ -837,7 +853,17 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
     // bf16: two 128-row query tiles per block sharing every K / V tile
     const int rpb = tc05_prefill_rows_per_block();
     p.row_blocks = static_cast<int>((static_cast<long long>(p.group) * n_new + rpb - 1) / rpb);
-    e = launch_tc05_prefill(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+    // a block's rows are whole tokens when the group divides them: then they
+    // come as one TMA box ([tokens][heads][128] fp32)
+    CUtensorMap tq = tk;
+    if (p.group <= 256 && (p.group & (p.group - 1)) == 0) {
+      if (!make_q_map(&tq, q_rot, layout->batch, n_new, layout->h_q, p.group, rpb)) {
+        snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+        return MQA_ERR_CUDA;
+      }
+      p.q_tma = 1;
+    }
+    e = launch_tc05_prefill(p, tk, tv, tq, reinterpret_cast<cudaStream_t>(stream));
   }
   if (e != cudaSuccess) return fail_cuda(e);
   const cudaError_t e2 = cudaGetLastError();

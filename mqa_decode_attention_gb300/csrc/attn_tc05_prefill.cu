@@ -31,6 +31,13 @@
 // S_1(t), V(t) after PV_1(t)). Warp 8 loads (TMA), warp 9 issues the MMAs
 // (one thread) and owns the tensor memory; warps 10 and 11 only complete the
 // third warpgroup.
+//
+// The block's 256 query rows (fp32 q_rot, 128 KB) arrive as one TMA box in
+// ring slots 1-4 while K(0) lands in slot 0; the softmax warps scale them into
+// the bf16 query tiles, and only then does the ring take V(0) and the rest.
+// Read with plain loads instead (still done when the group is not a power of
+// two), the rows took 8-9 us per block: a block's 8192 outstanding 16-byte
+// misses drain a few hundred at a time.
 #include <cuda_bf16.h>
 
 #include "../../include/mqa_decode.h"
@@ -71,7 +78,10 @@ constexpr int kSFull = kEmpty + kSlots;   // [kQT]
 constexpr int kPFull = kSFull + kQT;      // [kQT] (4 warps)
 constexpr int kODone = kPFull + kQT;      // every product done (committed once)
 constexpr int kDrain = kODone + 1;
-constexpr int kNBars = kDrain + 1;
+constexpr int kQStage = kDrain + 1;       // the query rows' box landed (ring slots 1-4)
+constexpr int kNBars = kQStage + 1;
+constexpr int kQStageBytes = kQT * kBM * kD * 4;
+static_assert(kSlots >= 5 && 4 * kTileBytes == kQStageBytes, "query box in ring slots 1-4");
 static_assert(kNBars * 8 + 4 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -87,7 +97,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of b
 template <bool PG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                             const Tc05Params p) {
+                             const __grid_constant__ CUtensorMap tmap_q, const Tc05Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
@@ -139,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kODone), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kQStage), 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -213,12 +224,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     bool waited = !p.early;
+    const bool q_tma = p.q_tma != 0;
+    if (q_tma) {
+      // the query rows (written by the preceding launch): 256 / G tokens x G
+      // heads x 128 dims, block row r at row r of the box
+      if (!waited) {
+        grid_dependency_wait();
+        waited = true;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(kQStage), kQStageBytes);
+        tma_load_3d(sbase + kRingOff + kTileBytes, &tmap_q, 0, j * G, b * n + g0 / G, bar(kQStage));
+      }
+    }
     int u = 0;
     for (; u < 2 * T; ++u) {
       const int slot = u % kSlots;
       bool ok = true;
       if (lane == 0) {
-        if (u >= kSlots) ok = mbar_wait(bar(kEmpty + slot), ((u / kSlots) - 1) & 1, p.wait_ns);
+        if (u >= kSlots)
+          ok = mbar_wait(bar(kEmpty + slot), ((u / kSlots) - 1) & 1, p.wait_ns);
+        else if (q_tma && u == 1)  // slots 1-4 are free once both query tiles are built
+          ok = mbar_wait(bar(kQReady + 0), 0, p.wait_ns) && mbar_wait(bar(kQReady + 1), 0, p.wait_ns);
         if (!ok) fail(1);
         if (stop()) ok = false;
       }
@@ -231,9 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (PG && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, static_cast<int>(MQA_DEVERR_PAGE_RANGE));
     // every copy this warp issued lands before the block can exit
-    if (lane == 0)
+    if (lane == 0) {
+      if (q_tma) (void)mbar_wait(bar(kQStage), 0, kWaitLimitNs);
       for (int k = u > kSlots ? u - kSlots : 0; k < u; ++k)
         (void)mbar_wait(bar(kFull + k % kSlots), (k / kSlots) & 1, kWaitLimitNs);
+    }
     __syncwarp();
   } else if (warp == 9) {
     regs_aux();
@@ -311,7 +340,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hh = j * G + (g0 + gr - gi * G);   // its query head
     const long long grow_row = (static_cast<long long>(b) * n + gi) * p.h_q + hh;
     unsigned char* qtile = smem + kQOff + q * kQBytes;
-    {
+    bool qok = true;
+    if (p.q_tma) {
+      // this warp's 32 rows of query tile q from the landed box, pre-scaled
+      // into the log2 domain, as bf16 in the swizzled tile (rows past the
+      // block's rows zero): lane l takes dims 4 l .. 4 l + 3 of one row at a
+      // time, so a warp reads 512 contiguous bytes per row
+      qok = __all_sync(0xffffffffu, mbar_wait(bar(kQStage), 0, p.wait_ns));
+      if (qok) {
+        const unsigned char* stage = smem + kRingOff + kTileBytes;
+        const int rbase = (warp & 3) * 32;
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+          const int rr = rbase + i;
+          float4 v = *reinterpret_cast<const float4*>(stage + (q * kBM + rr) * (kD * 4) + lane * 16);
+          if (q * kBM + rr >= rows) v = make_float4(0.f, 0.f, 0.f, 0.f);
+          uint2 w;
+          w.x = pack_bf16x2(v.x * p.scale_log2, v.y * p.scale_log2);
+          w.y = pack_bf16x2(v.z * p.scale_log2, v.w * p.scale_log2);
+          *reinterpret_cast<uint2*>(qtile + sw128(rr, 4 * lane)) = w;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kQReady + q));
+      } else if (lane == 0) {
+        fail(1);
+      }
+    } else {
       // Q row, pre-scaled into the log2 domain, as bf16 in the swizzled tile
       if (p.early) grid_dependency_wait();
       const float4* qs = reinterpret_cast<const float4*>(p.q_rot + grow_row * kD);
@@ -337,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t scol = tmem + lane_base + kColS + q * 128, ocol = tmem + lane_base + kColO + q * 128;
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    bool ok = qok;
+    for (int t = 0; ok && t < T; ++t) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + q), t & 1, p.wait_ns) && !stop());
       if (!ok) break;
       tc05::fence_after_sync();
@@ -479,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool PG>
-cudaError_t launch_prefill_t(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+cudaError_t launch_prefill_t(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                             cudaStream_t stream) {
   auto kern = attn_tc05_prefill_kernel<PG>;
   // the register split holds only for the launch count it was made for: a
   // build that launches with fewer registers would leave setmaxnreg.inc
@@ -504,7 +560,7 @@ cudaError_t launch_prefill_t(const Tc05Params& p, const CUtensorMap& tk, const C
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, tq, p);
 }
 
 }  // namespace
@@ -512,8 +568,8 @@ cudaError_t launch_prefill_t(const Tc05Params& p, const CUtensorMap& tk, const C
 int tc05_prefill_rows_per_block() { return kQT * kBM; }
 
 cudaError_t launch_tc05_prefill(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                cudaStream_t stream) {
-  return p.paged ? launch_prefill_t<true>(p, tk, tv, stream) : launch_prefill_t<false>(p, tk, tv, stream);
+                                const CUtensorMap& tq, cudaStream_t stream) {
+  return p.paged ? launch_prefill_t<true>(p, tk, tv, tq, stream) : launch_prefill_t<false>(p, tk, tv, tq, stream);
 }
 
 }  // namespace mqa

@@ -112,6 +112,9 @@ struct Tc05Params {
   int32_t* err;
   int early;  // 1: the preceding launch is the append kernel; stream K/V before waiting for it
   unsigned long long wait_ns;  // limit of the waits for progress (the drains use kWaitLimitNs)
+  // prefill (attn_tc05_prefill): 1 = the block's query rows arrive as one TMA
+  // box through the q_rot tensor map (group a power of two <= 256)
+  int q_tma;
   // 1: single-launch step (one row block): the kernel rotates q_new itself
   // and the block whose split holds a new token's position appends its k / v
   // rows
@@ -201,8 +204,10 @@ cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k
 // tc05_prefill_rows_per_block() rows (two 128-row query tiles); p.row_blocks
 // counts those blocks.
 int tc05_prefill_rows_per_block();
+// tmap_q: q_rot as [B n_new tokens][H_q][128] fp32, box 128 x group x
+// (256 / group), used when p.q_tma is set.
 cudaError_t launch_tc05_prefill(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                cudaStream_t stream);
+                                const CUtensorMap& tmap_q, cudaStream_t stream);
 // true when launch_tc05_attention merges the splits itself (two splits, R <=
 // 64 rows in one row block: each pair of split blocks is a two-block cluster
 // that writes out and lse_out directly): no combine follows, and o_part /
