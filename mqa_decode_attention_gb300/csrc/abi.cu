@@ -242,6 +242,20 @@ bool make_q_map(CUtensorMap* map, const float* q_rot, int batch, int n_new, int 
   return r == CUDA_SUCCESS;
 }
 
+// attn_tc05_kernel reading q_rot (not a fused step) with full 128-row blocks
+// (prefill, many new tokens): when the group divides 64, a block's rows come
+// as two boxes of 64 rows (p->q_tma set); else, and for fewer rows, the
+// kernel reads them with plain loads. False only if the encoder fails.
+bool tc05_q_map(Tc05Params* p, CUtensorMap* tq) {
+  p->q_tma = 0;
+  if (p->fuse || p->q_rot == nullptr || p->group > 64 || (p->group & (p->group - 1)) != 0 ||
+      static_cast<long long>(p->group) * p->n_new < 128)
+    return true;
+  if (!make_q_map(tq, p->q_rot, p->batch, p->n_new, p->h_q, p->group, 64)) return false;
+  p->q_tma = 1;
+  return true;
+}
+
 // TMA descriptors for the tensor-core path: 128-byte swizzled boxes of
 // 64 columns, kTile rows (contiguous) or one page (paged, pages shorter than
 // a tile). With `merged`, head_dim 128 is described as 64 columns x 2 halves
@@ -660,12 +674,12 @@ mqa_status attention_impl(const mqa_kv_layout* layout, const float* q_rot, const
       t.q_rot_out = rope->q_rot;
       fill_theta(t.theta, layout->head_dim, rope->rope_base);
     }
-    CUtensorMap tk, tv;
-    if (!tc05_maps(layout, &t, &tk, &tv)) {
+    CUtensorMap tk, tv, tq;
+    if (!tc05_maps(layout, &t, &tk, &tv) || !tc05_q_map(&t, &tq)) {
       snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
       return MQA_ERR_CUDA;
     }
-    e = launch_tc05_attention(t, tk, tv, s);
+    e = launch_tc05_attention(t, tk, tv, &tq, s);
     if (e != cudaSuccess) return fail_cuda(e);
     merged = tc05_merges_splits(t);
     goto combine;
@@ -848,7 +862,12 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
   }
   cudaError_t e;
   if (p.f8) {
-    e = launch_tc05_attention(p, tk, tv, reinterpret_cast<cudaStream_t>(stream));
+    CUtensorMap tq;
+    if (!tc05_q_map(&p, &tq)) {
+      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
+      return MQA_ERR_CUDA;
+    }
+    e = launch_tc05_attention(p, tk, tv, &tq, reinterpret_cast<cudaStream_t>(stream));
   } else {
     // bf16: two 128-row query tiles per block sharing every K / V tile
     const int rpb = tc05_prefill_rows_per_block();

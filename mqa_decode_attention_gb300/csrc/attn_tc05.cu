@@ -94,7 +94,8 @@ struct Lay {
   static constexpr int kODone = kPFull + kSBuf;      // [kSBuf]
   static constexpr int kDrain = kODone + kSBuf;
   static constexpr int kAppended = kDrain + 1;       // fused step: the new k / v row is in the cache
-  static constexpr int kNBars = kAppended + 1;
+  static constexpr int kQStage = kAppended + 1;      // q_tma: the query rows' two boxes landed
+  static constexpr int kNBars = kQStage + 1;
   static_assert(kNBars * 8 + 4 <= 512, "barrier area");
   static_assert((kXRows * (kD + 3)) * 4 <= kStages * kTileBytes, "cluster exchange area");
   static_assert((kBM * (kD + 4) + 3 * kBM) * 4 <= kStages * kTileBytes, "replica merge area (the K stages)");
@@ -146,7 +147,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of b
 template <int PARTS, bool FUSE, bool CL, bool F8, bool PG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                     const Tc05Params p) {
+                     const __grid_constant__ CUtensorMap tmap_q, const Tc05Params p) {
   static_assert(!CL || PARTS > 1, "the cluster merge takes replicated rows (R <= 64)");
   static_assert(!(FUSE && F8), "the fused step is bf16 only");
   static_assert(!(PG && F8), "paged caches: bf16 only");
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kVOff = Y::kVOff, kBarOff = Y::kBarOff, kXOff = Y::kXOff;
   constexpr int kQReady = Y::kQReady, kKFull = Y::kKFull, kKEmpty = Y::kKEmpty, kVFull = Y::kVFull,
                 kVEmpty = Y::kVEmpty, kSFull = Y::kSFull, kPFull = Y::kPFull, kODone = Y::kODone,
-                kDrain = Y::kDrain, kAppended = Y::kAppended, kNBars = Y::kNBars;
+                kDrain = Y::kDrain, kAppended = Y::kAppended, kQStage = Y::kQStage, kNBars = Y::kNBars;
   constexpr int kRPad = kBM / PARTS;  // rows per part
   constexpr int kKW = kBN / PARTS;    // keys of a tile per thread
   extern __shared__ unsigned char smem_raw[];
@@ -436,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kAppended), 1);  // the append warp
+    mbar_init(bar(kQStage), 1);
     fence_mbar_init();
   }
   if (warp == 6) {
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int it = 0;
     {
-      const int npre = p.early ? kStages : kPreTiles;
+      const int npre = p.early && !p.q_tma ? kStages : kPreTiles;  // (q_tma: the query rows use stage kPreTiles on)
       const int lim = p.early ? Lp : (writer ? a_pos : 0x7fffffff);
       for (; it < T && it < npre && tile_key0(it) + kBN <= lim; ++it) issue(it);
     }
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the first tiles before the Q rows are in (while the append kernel
       // runs, the ring's first fill), none holding a row that the preceding
       // launch or this block's append writes
-      const int npre = p.early ? kStages : kPreTiles;
+      const int npre = p.early && !p.q_tma ? kStages : kPreTiles;  // (q_tma: the query rows use stage kPreTiles on)
       const int lim = p.early ? Lp : (writer ? a_pos : 0x7fffffff);
       for (; it < T && it < npre && tile_key0(it) + kBN <= lim; ++it)
         if (lane == 0) issue(it);
@@ -691,7 +693,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int gi = (g0 + gr) / G;                      // new token of this row
     const int hh = j * G + (g0 + gr - gi * G);         // its query head
     const long long grow_row = (static_cast<long long>(b) * n + gi) * p.h_q + hh;  // output row [B, n, H_q]
-    {
+    if (!FUSE && p.q_tma) {
+      // The block's 128 rows of q_rot as two TMA boxes of 64 rows (64 / G
+      // tokens x G heads x 128 fp32 dims) into stages the first tile
+      // requests leave free (bf16: K and V stage kPreTiles; fp8: K stages
+      // kPreTiles .. kPreTiles + 3); a warp then builds its 32 rows of the Q
+      // tile, lane l taking dims 4 l .. 4 l + 3 (a warp reads 512 contiguous
+      // bytes per row), and only then are the loaders released. Read with
+      // plain loads, a block's 4096 outstanding 16-byte misses drain a few
+      // hundred at a time.
+      if (p.early) grid_dependency_wait();
+      const int qa = kKOff + kPreTiles * kTileBytes;
+      const int qb = F8 ? qa + 32768 : kVOff + kPreTiles * kTileBytes;
+      static_assert(F8 ? (kPreTiles + 4) * kTileBytes <= kStages * kTileBytes : kTileBytes >= 64 * kD * 4,
+                    "query boxes in the free stages");
+      if (tid == 0) {
+        mbar_arrive_expect_tx(bar(kQStage), 2 * 64 * kD * 4);
+        tma_load_3d(sbase + qa, &tmap_q, 0, j * G, b * n + g0 / G, bar(kQStage));
+        tma_load_3d(sbase + qb, &tmap_q, 0, j * G, b * n + (g0 + 64) / G, bar(kQStage));
+      }
+      const bool landed = __all_sync(0xffffffffu, mbar_wait(bar(kQStage), 0, p.wait_ns));
+      if (landed) {
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+          const int rq = 32 * warp + i;                       // row of the Q tile
+          const int gq = rq - (rq / kRPad) * kRPad;           // its row of the block
+          float4 v = *reinterpret_cast<const float4*>(smem + (gq < 64 ? qa : qb) + (gq & 63) * (kD * 4) + lane * 16);
+          if (gq >= rows) v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (F8) {
+            const float qs = p.scale_log2 * kQScaleF8;
+            const uint2 hl = e4m3_split4_once(v.x * qs, v.y * qs, v.z * qs, v.w * qs);
+            const uint32_t off = rq * 128 + (((lane >> 2) ^ (rq & 7)) << 4) + (lane & 3) * 4;
+            *reinterpret_cast<uint32_t*>(smem + kQOff + off) = hl.x;
+            *reinterpret_cast<uint32_t*>(smem + kQOff + 16384 + off) = hl.y;
+          } else {
+            uint2 w;
+            w.x = pack_bf16x2(v.x * p.scale_log2, v.y * p.scale_log2);
+            w.y = pack_bf16x2(v.z * p.scale_log2, v.w * p.scale_log2);
+            *reinterpret_cast<uint2*>(smem + kQOff + sw128(rq, 4 * lane)) = w;
+          }
+        }
+      } else {
+        if (lane == 0) fail(1);
+        if (tid == 0) (void)mbar_wait(bar(kQStage), 0, kWaitLimitNs);  // the boxes land before the block exits
+      }
+      named_bar_arrive(2, kBM + 64);  // the boxes are read: the loaders may go on
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (landed && lane == 0) mbar_arrive(bar(kQReady));
+    } else {
       // Q row, pre-scaled into the log2 domain, as bf16 in the swizzled tile.
       // The whole row is requested at once (one memory round trip), and the
       // K / V loaders are released only then: behind their burst of tile
@@ -1118,7 +1168,8 @@ KernelShape tc05_shape() { return {kThreads, Lay<false>::kSmemBytes, kBM, 1}; }
 int tc05_f8_box_rows() { return kBN; }
 
 template <int PARTS, bool FUSE, bool CL, bool F8, bool PG>
-cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                         cudaStream_t stream) {
   auto kern = attn_tc05_kernel<PARTS, FUSE, CL, F8, PG>;
   constexpr int smem = Lay<F8>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1140,37 +1191,38 @@ cudaError_t launch_parts(const Tc05Params& p, const CUtensorMap& tk, const CUten
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, tq, p);
 }
 
 template <int PARTS, bool F8, bool PG>
 cudaError_t launch_fuse(const Tc05Params& p, bool cl, const CUtensorMap& tk, const CUtensorMap& tv,
-                        cudaStream_t stream) {
+                        const CUtensorMap& tq, cudaStream_t stream) {
   if constexpr (F8) {  // (several new tokens: never fused)
-    return cl ? launch_parts<PARTS, false, true, true, false>(p, tk, tv, stream)
-              : launch_parts<PARTS, false, false, true, false>(p, tk, tv, stream);
+    return cl ? launch_parts<PARTS, false, true, true, false>(p, tk, tv, tq, stream)
+              : launch_parts<PARTS, false, false, true, false>(p, tk, tv, tq, stream);
   } else {
     if (cl)
-      return p.fuse ? launch_parts<PARTS, true, true, false, PG>(p, tk, tv, stream)
-                    : launch_parts<PARTS, false, true, false, PG>(p, tk, tv, stream);
-    return p.fuse ? launch_parts<PARTS, true, false, false, PG>(p, tk, tv, stream)
-                  : launch_parts<PARTS, false, false, false, PG>(p, tk, tv, stream);
+      return p.fuse ? launch_parts<PARTS, true, true, false, PG>(p, tk, tv, tq, stream)
+                    : launch_parts<PARTS, false, true, false, PG>(p, tk, tv, tq, stream);
+    return p.fuse ? launch_parts<PARTS, true, false, false, PG>(p, tk, tv, tq, stream)
+                  : launch_parts<PARTS, false, false, false, PG>(p, tk, tv, tq, stream);
   }
 }
 
 template <bool F8, bool PG>
-cudaError_t launch_rows(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+cudaError_t launch_rows(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                        cudaStream_t stream) {
   // replicate few rows over the 128 MMA rows so that all four softmax warps work
   const long long rows = static_cast<long long>(p.group) * p.n_new;
   const bool cl = tc05_merges_splits(p);
   // (a fused step has one row block: p.fuse implies row_blocks == 1)
-  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4, F8, PG>(p, cl, tk, tv, stream);
-  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2, F8, PG>(p, cl, tk, tv, stream);
+  if (p.row_blocks == 1 && rows <= 32) return launch_fuse<4, F8, PG>(p, cl, tk, tv, tq, stream);
+  if (p.row_blocks == 1 && rows <= 64) return launch_fuse<2, F8, PG>(p, cl, tk, tv, tq, stream);
   if constexpr (F8)
-    return launch_parts<1, false, false, true, false>(p, tk, tv, stream);
+    return launch_parts<1, false, false, true, false>(p, tk, tv, tq, stream);
   else
-    return p.fuse ? launch_parts<1, true, false, false, PG>(p, tk, tv, stream)
-                  : launch_parts<1, false, false, false, PG>(p, tk, tv, stream);
+    return p.fuse ? launch_parts<1, true, false, false, PG>(p, tk, tv, tq, stream)
+                  : launch_parts<1, false, false, false, PG>(p, tk, tv, tq, stream);
 }
 
 bool tc05_merges_splits(const Tc05Params& p) {
@@ -1178,9 +1230,11 @@ bool tc05_merges_splits(const Tc05Params& p) {
 }
 
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                  cudaStream_t stream) {
-  if (p.f8) return launch_rows<true, false>(p, tk, tv, stream);
-  return p.paged ? launch_rows<false, true>(p, tk, tv, stream) : launch_rows<false, false>(p, tk, tv, stream);
+                                  const CUtensorMap* tq, cudaStream_t stream) {
+  if (p.q_tma && tq == nullptr) return cudaErrorInvalidValue;
+  const CUtensorMap& q = tq ? *tq : tk;  // (unused unless p.q_tma)
+  if (p.f8) return launch_rows<true, false>(p, tk, tv, q, stream);
+  return p.paged ? launch_rows<false, true>(p, tk, tv, q, stream) : launch_rows<false, false>(p, tk, tv, q, stream);
 }
 
 }  // namespace mqa

@@ -112,8 +112,10 @@ struct Tc05Params {
   int32_t* err;
   int early;  // 1: the preceding launch is the append kernel; stream K/V before waiting for it
   unsigned long long wait_ns;  // limit of the waits for progress (the drains use kWaitLimitNs)
-  // prefill (attn_tc05_prefill): 1 = the block's query rows arrive as one TMA
-  // box through the q_rot tensor map (group a power of two <= 256)
+  // 1 = the block's query rows arrive as TMA boxes through the q_rot tensor
+  // map (prefill kernel: one box of 256 rows, group a power of two <= 256;
+  // attn_tc05 without a fused append: two boxes of 64 rows, group a power of
+  // two <= 64)
   int q_tma;
   // 1: single-launch step (one row block): the kernel rotates q_new itself
   // and the block whose split holds a new token's position appends its k / v
@@ -198,8 +200,10 @@ KernelShape tc05_widen_shape();
 bool tc05_widen_merges_splits(const Tc05Params& p);
 cudaError_t launch_tc05_widen_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                         cudaStream_t stream);
+// tmap_q (used when p.q_tma is set): q_rot as [B n_new tokens][H_q][128]
+// fp32, box 128 x group x (64 / group).
 cudaError_t launch_tc05_attention(const Tc05Params& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                  cudaStream_t stream);
+                                  const CUtensorMap* tmap_q, cudaStream_t stream);
 // Prefill over a bf16 cache (contiguous or paged): blocks of
 // tc05_prefill_rows_per_block() rows (two 128-row query tiles); p.row_blocks
 // counts those blocks.
