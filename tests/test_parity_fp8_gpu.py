@@ -235,6 +235,7 @@ PREFILL = [
     (2, 8, 2, 129, 0, 140),
     (2, 8, 2, 200, 57, 260),
     (1, 16, 1, 140, 10, 150),
+    (2, 12, 4, 129, 0, 140),   # G = 3: query rows by plain loads
 ]
 
 

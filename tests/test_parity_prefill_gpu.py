@@ -79,6 +79,8 @@ CASES = [
     (2, 8, 2, 200, 57, 260),   # cached prefix of 57 tokens
     (1, 4, 4, 150, 300, 450),  # MHA, prefix longer than the prompt
     (1, 16, 1, 140, 10, 150),  # MQA
+    (2, 12, 4, 150, 20, 180),  # G = 3: a block's rows are not whole tokens (query rows by plain loads)
+    (1, 6, 1, 100, 0, 100),    # G = 6
 ]
 
 
@@ -219,6 +221,7 @@ PAGED_CASES = [
     (1, 8, 2, 250, [100], 128),
     (2, 16, 1, 140, [10, 300], 256),   # MQA, prefix longer than a page
     (1, 4, 4, 190, [70], 64),          # MHA
+    (2, 12, 4, 130, [0, 17], 32),      # G = 3 (query rows by plain loads)
 ]
 
 

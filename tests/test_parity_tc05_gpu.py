@@ -87,6 +87,8 @@ CASES = [
     (2, 32, 4, 4, [400, 33], 400),          # G = 8 x 4 tokens = 32 rows
     (2, 32, 8, 8, [300, 8], 300),           # G = 4 x 8 tokens, L = n
     (1, 32, 1, 5, [260], 260),              # G = 32 x 5 = 160 rows: two row blocks
+    (2, 32, 8, 32, [300, 40], 300),         # G = 4 x 32 = 128 rows: query rows as two TMA boxes
+    (1, 10, 2, 32, [250], 250),             # G = 5 x 32 = 160 rows: a group that does not divide 64 (plain loads)
 ]
 
 
