@@ -16,7 +16,10 @@
 // with fused multiply-adds) and takes their sine and cosine in fp64. The key
 // is rotated in fp64 with explicit round-to-nearest products (no fused
 // multiply-add), then rounded once to the cache dtype; the query is rotated
-// in fp32 and written as fp32.
+// in fp32 and written as fp32. bf16 and e5m2 caches keep the reduced angle
+// and its fp32 cosine / sine instead: the key's rounding is decided from its
+// fp32 rotation wherever an error bound settles it (the same bits as the
+// fp64 path), the fp64 rotation taken only for the rest.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,6 +33,57 @@
 
 namespace mqa {
 namespace {
+
+// e5m2_code of a float, in float arithmetic: every step is exact for a float
+// input (scalings by powers of two, one rint), so the code equals
+// e5m2_code(double(x)) without fp64 work.
+__device__ __forceinline__ uint32_t e5m2_code_f(float x) {
+  uint32_t code = 0x7Fu;
+  if (!isnan(x)) {
+    const float ax = fabsf(x);
+    float r = 57344.0f;
+    if (ax < 57344.0f) {
+      const int e = ax > 0.0f ? ilogbf(ax) : -14;
+      const int qe = (e < -14 ? -14 : e) - 2;
+      r = fminf(ldexpf(rintf(ldexpf(ax, -qe)), qe), 57344.0f);
+    }
+    code = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(r))) >> 8;
+  }
+  return code | (signbit(x) ? 0x80u : 0u);
+}
+
+// The key pair (x, y) turned by the reduced angle and rounded once to e5m2,
+// decided in fp32 as rope_k_bf16_fast decides a bf16 rounding: the rotation
+// from the fp32 cosine / sine cf, sf of the angle is within 8e-7 (|x| + |y|)
+// of the fp64 rotation, and e5m2 rounding is monotonic, so when both ends of
+// that interval (rounded outward) give one code the fp64 rotation gives it
+// too. True with the codes in *codes (x in bits 0-7, y in 8-15); false
+// leaves the pair to the fp64 rotation (e5m2_pair_fp64).
+__device__ __forceinline__ bool rope_k_e5m2_fast(float x, float y, float cf, float sf, uint32_t* codes) {
+  const float s = fabsf(x) + fabsf(y);
+  if (!(s >= 0x1p-100f && s <= 1e37f)) return false;
+  const float xr = fmaf(x, cf, -(y * sf));
+  const float yr = fmaf(x, sf, y * cf);
+  const float e = s * 8e-7f;
+  const uint32_t xl = e5m2_code_f(__fsub_rd(xr, e)), xh = e5m2_code_f(__fadd_ru(xr, e));
+  const uint32_t yl = e5m2_code_f(__fsub_rd(yr, e)), yh = e5m2_code_f(__fadd_ru(yr, e));
+  if (xl != xh || yl != yh) return false;
+  *codes = xl | (yl << 8);
+  return true;
+}
+
+// The same pair from the fp64 rotation (fp64 sine and cosine of ang,
+// round-to-nearest products and sum; the fused steps' append_row_q forms
+// every pair this way), out of line: it runs only for the pairs whose fp32
+// interval holds an e5m2 rounding boundary.
+__device__ __noinline__ uint32_t e5m2_pair_fp64(float x, float y, double ang) {
+  double c, sn;
+  sincos(ang, &sn, &c);
+  const double xd = x, yd = y;
+  const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, sn));
+  const double yr = __dadd_rn(__dmul_rn(xd, sn), __dmul_rn(yd, c));
+  return e5m2_code(xr) | (e5m2_code(yr) << 8);
+}
 
 constexpr int kAppendThreads = 256;
 constexpr int kQHeadsPerBlock = 8;   // 8 heads x 64 pairs = 2 pairs per thread at d = 128
@@ -69,12 +123,16 @@ struct Elem<float> {
 
 template <typename T, bool QU8, bool F8 = false>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const AppendParams p) {
-  // bf16 cache: no fp64 sine / cosine table. q turns by the fp32 sine / cosine
-  // of the fp64-reduced angle (as the fused decode kernels form q_rot) and k
-  // by rope_k_bf16 (bit for bit the fp64 rotation rounded once to bf16); the
-  // fp32 and one-byte caches, whose stored values depend on the exact fp32 /
-  // fp64 rotation, keep the fp64 table.
+  // bf16 and e5m2 caches: no fp64 sine / cosine table. q turns by the fp32
+  // sine / cosine of the fp64-reduced angle (as the fused decode kernels form
+  // q_rot) and k by rope_k_bf16 / rope_k_e5m2_fast (bit for bit the fp64
+  // rotation rounded once); the fp32 and uint8 caches, whose stored values
+  // depend on the exact fp32 rounding of the fp64 rotation, keep the fp64
+  // table.
   constexpr bool kFast = std::is_same<T, __nv_bfloat16>::value && !QU8 && !F8;
+  // the angle table (s_cos = the reduced angle, s_cf / s_sf its fp32 cosine /
+  // sine): bf16 and e5m2 caches, whose keys take the fp32 stage first
+  constexpr bool kAngle = kFast || F8;
   __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];  // fp64 cos / sin; kFast: s_cos holds the angle
   __shared__ float s_cf[kMaxHalfDim], s_sf[kMaxHalfDim];    // kFast: fp32 cos / sin of the angle
   __shared__ float s_red[kAppendThreads / 32][4];  // uint8 cache: per-warp k/v min and max
@@ -112,7 +170,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   if (i1 < n_pairs) x1 = Elem<T>::load2(src + (h_begin + i1 / half) * D + 2 * (i1 % half));
 
   if (threadIdx.x < half) {
-    if constexpr (kFast) {
+    if constexpr (kAngle) {
       const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]);
       float sf, cf;
       sincosf(static_cast<float>(ang), &sf, &cf);
@@ -169,8 +227,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
       if (idx >= n_pairs) continue;
       const float2 x = u == 0 ? x0 : x1;
       const int h = h_begin + idx / half, i = idx % half;
-      const float c = kFast ? s_cf[i] : static_cast<float>(s_cos[i]);
-      const float s = kFast ? s_sf[i] : static_cast<float>(s_sin[i]);
+      const float c = kAngle ? s_cf[i] : static_cast<float>(s_cos[i]);
+      const float s = kAngle ? s_sf[i] : static_cast<float>(s_sin[i]);
       *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
     }
     return;
@@ -229,8 +287,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
 
   if constexpr (F8) {
-    // e5m2 cache: k from its fp64 rotation and v from its bf16 value, each
-    // rounded once to e5m2
+    // e5m2 cache: k from its rotation (rope_k_e5m2_fast, else the fp64 one)
+    // and v from its bf16 value, each rounded once to e5m2
     const T* v = static_cast<const T*>(p.v_new) + static_cast<long long>(bt) * p.h_kv * D;
     uint8_t* kc = static_cast<uint8_t*>(p.k_cache) + s_row;
     uint8_t* vc = static_cast<uint8_t*>(p.v_cache) + s_row;
@@ -240,14 +298,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
       if (idx >= n_pairs) continue;
       const float2 x = u == 0 ? x0 : x1;
       const int h = h_begin + idx / half, i = idx % half;
-      const double xd = x.x, yd = x.y, c = s_cos[i], s = s_sin[i];
-      const double xr = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, s));
-      const double yr = __dadd_rn(__dmul_rn(xd, s), __dmul_rn(yd, c));
+      uint32_t kk;
+      if (!rope_k_e5m2_fast(x.x, x.y, s_cf[i], s_sf[i], &kk)) kk = e5m2_pair_fp64(x.x, x.y, s_cos[i]);
       const float2 vv = Elem<T>::load2(v + h * D + 2 * i);
-      *reinterpret_cast<uint16_t*>(kc + h * s_stride + 2 * i) =
-          static_cast<uint16_t>(e5m2_code(xr) | (e5m2_code(yr) << 8));
+      *reinterpret_cast<uint16_t*>(kc + h * s_stride + 2 * i) = static_cast<uint16_t>(kk);
       *reinterpret_cast<uint16_t*>(vc + h * s_stride + 2 * i) =
-          static_cast<uint16_t>(e5m2_code(vv.x) | (e5m2_code(vv.y) << 8));
+          static_cast<uint16_t>(e5m2_code_f(vv.x) | (e5m2_code_f(vv.y) << 8));
     }
     return;
   }
@@ -286,6 +342,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 template <typename T, int BYTE = 0>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(const AppendParams p) {
   constexpr bool kFast = std::is_same<T, __nv_bfloat16>::value && BYTE == 0;  // as in append_rope_kernel
+  constexpr bool kAngle = kFast || BYTE == 2;
   __shared__ double s_cos[kMaxHalfDim], s_sin[kMaxHalfDim];  // fp64 cos / sin; kFast: s_cos holds the angle
   __shared__ float s_cf[kMaxHalfDim], s_sf[kMaxHalfDim];    // kFast: fp32 cos / sin of the angle
   __shared__ long long s_row, s_stride;
@@ -296,7 +353,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   const int D = p.head_dim, half = D >> 1;
   const int pos = p.pos[b] + (bt - b * p.n_new);
   if (threadIdx.x < half) {
-    if constexpr (kFast) {
+    if constexpr (kAngle) {
       const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]);
       float sf, cf;
       sincosf(static_cast<float>(ang), &sf, &cf);
@@ -348,8 +405,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   for (int idx = threadIdx.x; idx < p.h_q * half; idx += kAppendThreads) {
     const int h = idx / half, i = idx - h * half;
     const float2 x = Elem<T>::load2(qs + h * D + 2 * i);
-    const float c = kFast ? s_cf[i] : static_cast<float>(s_cos[i]);
-    const float s = kFast ? s_sf[i] : static_cast<float>(s_sin[i]);
+    const float c = kAngle ? s_cf[i] : static_cast<float>(s_cos[i]);
+    const float s = kAngle ? s_sf[i] : static_cast<float>(s_sin[i]);
     *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
   }
   if (!s_ok) return;
@@ -369,14 +426,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
         if (i >= half) break;
         const float2 x = Elem<T>::load2(ks + h * D + 2 * i);
         vv[u] = Elem<T>::load2(vs + h * D + 2 * i);
-        const double xd = x.x, yd = x.y, c = s_cos[i], sn = s_sin[i];
-        xr[u] = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, sn));
-        yr[u] = __dadd_rn(__dmul_rn(xd, sn), __dmul_rn(yd, c));
         if constexpr (BYTE == 2) {
-          *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(e5m2_code(xr[u]) | (e5m2_code(yr[u]) << 8));
+          uint32_t kk;
+          if (!rope_k_e5m2_fast(x.x, x.y, s_cf[i], s_sf[i], &kk)) kk = e5m2_pair_fp64(x.x, x.y, s_cos[i]);
+          *reinterpret_cast<uint16_t*>(kc + 2 * i) = static_cast<uint16_t>(kk);
           *reinterpret_cast<uint16_t*>(vc + 2 * i) =
-              static_cast<uint16_t>(e5m2_code(vv[u].x) | (e5m2_code(vv[u].y) << 8));
+              static_cast<uint16_t>(e5m2_code_f(vv[u].x) | (e5m2_code_f(vv[u].y) << 8));
         } else {
+          const double xd = x.x, yd = x.y, c = s_cos[i], sn = s_sin[i];
+          xr[u] = __dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, sn));
+          yr[u] = __dadd_rn(__dmul_rn(xd, sn), __dmul_rn(yd, c));
           const float kx = __double2float_rn(xr[u]), ky = __double2float_rn(yr[u]);
           kmn = fminf(kmn, fminf(kx, ky));
           kmx = fmaxf(kmx, fmaxf(kx, ky));
