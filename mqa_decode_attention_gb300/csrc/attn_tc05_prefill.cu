@@ -94,6 +94,38 @@ __device__ __forceinline__ uint32_t sw128(int r, int col) {  // byte offset of b
 // table; a key tile is gathered page by page (rp = min(page_size, 64) rows per
 // copy: tiles start on multiples of 64, so a 64-key half never straddles a
 // page).
+// The softmax's fp32 arithmetic on the sm_100 family's packed and
+// three-input forms: two subtractions or additions per instruction (each
+// rounded as the scalar one), and a maximum of three values (exact). The
+// results are those of the scalar code; the instruction count of a row's
+// softmax drops by about a fifth (8 x 4096 prefill step 1221 -> 1178 us with
+// the packed pairs).
+__device__ __forceinline__ float2 sub2(float2 a, float b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "sub.rn.f32x2 rr, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rr, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 template <bool PG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -427,13 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (key0 + c < ka || key0 + c > pos) s[c] = -INFINITY;
       }
-      float mx8[8];  // eight independent chains
+      float mx8[8];  // eight independent chains, two new scores per step
+      static_assert(kBN % 16 == 0, "max chains");
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[8 + i]);
 #pragma unroll
-      for (int c = 8; c < kBN; c += 8) {
+      for (int c = 16; c < kBN; c += 16) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
+        for (int i = 0; i < 8; ++i) mx8[i] = max3(mx8[i], s[c + i], s[c + 8 + i]);
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -458,20 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m_ref = m_new;
       const float e = m_ref == -INFINITY ? 0.f : m_ref;
-      float sm8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float2 sm4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = fast_exp2(s[64 * half + 2 * i] - e), p1 = fast_exp2(s[64 * half + 2 * i + 1] - e);
-          sm8[(2 * i) & 7] += p0;
-          sm8[(2 * i + 1) & 7] += p1;
+          const float2 dd = sub2(make_float2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), e);
+          const float p0 = fast_exp2(dd.x), p1 = fast_exp2(dd.y);
+          sm4[i & 3] = add2(sm4[i & 3], make_float2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tc05::st_32x32b_x32_u(scol + 32 * half, pk);
       }
-      l += ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+      l += ((sm4[0].x + sm4[0].y) + (sm4[1].x + sm4[1].y)) + ((sm4[2].x + sm4[2].y) + (sm4[3].x + sm4[3].y));
       tc05::wait_st();
       tc05::fence_before_sync();
       __syncwarp();
