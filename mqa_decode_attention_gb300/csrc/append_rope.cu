@@ -352,6 +352,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   const int b = bt / p.n_new;
   const int D = p.head_dim, half = D >> 1;
   const int pos = p.pos[b] + (bt - b * p.n_new);
+  // bf16 q rows: 16-byte units of four rotation pairs; a thread's first two
+  // units are requested before the table is formed, so that their latency
+  // and the table's overlap
+  constexpr bool kVec = std::is_same<T, __nv_bfloat16>::value;
+  const int n_units = kVec ? p.h_q * D / 8 : 0;
+  const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q_new) + static_cast<long long>(bt) * p.h_q * D);
+  uint4 qpre0 = make_uint4(0u, 0u, 0u, 0u), qpre1 = make_uint4(0u, 0u, 0u, 0u);
+  if (kVec && static_cast<int>(threadIdx.x) < n_units) qpre0 = qsrc[threadIdx.x];
+  if (kVec && static_cast<int>(threadIdx.x) + kAppendThreads < n_units) qpre1 = qsrc[threadIdx.x + kAppendThreads];
   if (threadIdx.x < half) {
     if constexpr (kAngle) {
       const double ang = reduce_two_pi(static_cast<double>(pos) * p.theta[threadIdx.x]);
@@ -402,12 +411,33 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_tokens_kernel(cons
   // q: fp32 rotation, fp32 output
   const T* qs = static_cast<const T*>(p.q_new) + static_cast<long long>(bt) * p.h_q * D;
   float* qr = p.q_rot + static_cast<long long>(bt) * p.h_q * D;
-  for (int idx = threadIdx.x; idx < p.h_q * half; idx += kAppendThreads) {
-    const int h = idx / half, i = idx - h * half;
-    const float2 x = Elem<T>::load2(qs + h * D + 2 * i);
-    const float c = kAngle ? s_cf[i] : static_cast<float>(s_cos[i]);
-    const float s = kAngle ? s_sf[i] : static_cast<float>(s_sin[i]);
-    *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
+  if constexpr (kVec) {
+    auto rot_unit = [&](int w, uint4 raw) {  // elements 8 w .. 8 w + 7 (one head: D % 8 == 0)
+      const int e0 = 8 * w, i0 = (e0 % D) >> 1;
+      const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+      float o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x = bf16lo_to_f32(wd[k]), y = bf16hi_to_f32(wd[k]);
+        const float c = kAngle ? s_cf[i0 + k] : static_cast<float>(s_cos[i0 + k]);
+        const float s = kAngle ? s_sf[i0 + k] : static_cast<float>(s_sin[i0 + k]);
+        o[2 * k] = x * c - y * s;
+        o[2 * k + 1] = x * s + y * c;
+      }
+      *reinterpret_cast<float4*>(qr + e0) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(qr + e0 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    };
+    if (static_cast<int>(threadIdx.x) < n_units) rot_unit(threadIdx.x, qpre0);
+    if (static_cast<int>(threadIdx.x) + kAppendThreads < n_units) rot_unit(threadIdx.x + kAppendThreads, qpre1);
+    for (int w = threadIdx.x + 2 * kAppendThreads; w < n_units; w += kAppendThreads) rot_unit(w, qsrc[w]);
+  } else {
+    for (int idx = threadIdx.x; idx < p.h_q * half; idx += kAppendThreads) {
+      const int h = idx / half, i = idx - h * half;
+      const float2 x = Elem<T>::load2(qs + h * D + 2 * i);
+      const float c = kAngle ? s_cf[i] : static_cast<float>(s_cos[i]);
+      const float s = kAngle ? s_sf[i] : static_cast<float>(s_sin[i]);
+      *reinterpret_cast<float2*>(qr + h * D + 2 * i) = make_float2(x.x * c - x.y * s, x.x * s + x.y * c);
+    }
   }
   if (!s_ok) return;
   const T* ks = static_cast<const T*>(p.k_new) + static_cast<long long>(bt) * p.h_kv * D;
