@@ -1058,7 +1058,7 @@ def bench_prefill(args):
         "roofline": {"bound": "tensor",
                      "kernel": ("attn_tc05_prefill_kernel" if args.cache == "native" else
                                 "decode_u8_kernel (multi-token form)" if args.cache == "u8" or w.paged else
-                                "attn_tc05_kernel (fp8 form)"),
+                                "attn_tc05_prefill_kernel (fp8 form)"),
                      "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)" if peaks else "fallback"},

@@ -366,8 +366,7 @@ MQA_API size_t mqa_workspace_size_multi(const mqa_kv_layout* layout, int32_t n_n
  * query token i of sequence b (position L - n_new + i) attends to the keys
  * [0, L - n_new + i] (or the last W of them) -- on the tensor-memory tensor
  * cores (tcgen05): one block per (sequence, kv head, 256 (token, query head)
- * rows as two 128-row query tiles; 128 rows over an e5m2 cache), S and O
- * accumulated in tensor memory.
+ * rows as two 128-row query tiles), S and O accumulated in tensor memory.
  *
  * gqa_prefill_attention: q_rot [batch, n_new, h_q, 128] fp32 (from
  *   kv_append_rope_multi), seq_lens[b] = L after the append (>= n_new; L > n_new

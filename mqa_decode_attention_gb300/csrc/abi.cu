@@ -861,15 +861,9 @@ mqa_status prefill_impl(const mqa_kv_layout* layout, int n_new, const float* q_r
     return MQA_ERR_CUDA;
   }
   cudaError_t e;
-  if (p.f8) {
-    CUtensorMap tq;
-    if (!tc05_q_map(&p, &tq)) {
-      snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed or is unavailable");
-      return MQA_ERR_CUDA;
-    }
-    e = launch_tc05_attention(p, tk, tv, &tq, reinterpret_cast<cudaStream_t>(stream));
-  } else {
-    // bf16: two 128-row query tiles per block sharing every K / V tile
+  {
+    // two 128-row query tiles per block sharing every K / V tile (bf16, or
+    // e5m2 code tiles in the kernel's fp8 form)
     const int rpb = tc05_prefill_rows_per_block();
     p.row_blocks = static_cast<int>((static_cast<long long>(p.group) * n_new + rpb - 1) / rpb);
     // a block's rows are whole tokens when the group divides them: then they

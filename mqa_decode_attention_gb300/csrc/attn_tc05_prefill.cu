@@ -72,6 +72,9 @@ constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + 1 KB alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;  // S/P of tile q at 128 q, O of tile q at 256 + 128 q
 constexpr float kRescaleLog2 = 8.0f;
+// F8: Q enters scaled by 2^6 (its values then sit in e4m3's normal range); the
+// scores come out 2^6 too large and are scaled back exactly
+constexpr float kQScaleF8 = 64.f;
 // mbarriers (8 bytes each) at kBarOff
 constexpr int kQReady = 0;                // [kQT] the query tile is in shared memory (4 warps)
 constexpr int kFull = kQReady + kQT;      // [kSlots]
@@ -129,7 +132,13 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return r;
 }
 
-template <bool PG>
+// F8: contiguous fp8 e5m2 cache. K and V code tiles (16 KB, one per ring
+// slot) are the MMAs' B operands as TMA lands them (kind::f8f6f4, K = 32 per
+// instruction); Q (scaled by 2^6 into e4m3's normal range) and P each enter
+// as two e4m3 parts, hi = e4m3(x) and lo = e4m3(x - hi), as in the fp8 form
+// of attn_tc05_kernel, so the scores and outputs equal that kernel's up to the
+// order of fp32 accumulation.
+template <bool PG, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const __grid_constant__ CUtensorMap tmap_q, const Tc05Params p) {
@@ -140,6 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort, s_skip;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+  static_assert(!(PG && F8), "e5m2: contiguous caches only");
+  constexpr int kLoadBytes = F8 ? kBN * kD : kTileBytes;  // bytes of one K / V tile (a ring slot holds one)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group, n = p.n_new, R = G * n;
   // block order: sequence fastest, then kv head, then row pair (the pairs with
@@ -255,8 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_5d(d + 16384, map, 0, k & (ps - 1), 1, j, page, bar(kFull + slot));
         }
       } else if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kFull + slot), kTileBytes);
-        tma_load_4d(dst, map, 0, tile_key0(t), 0, row, bar(kFull + slot));
+        mbar_arrive_expect_tx(bar(kFull + slot), kLoadBytes);
+        if constexpr (F8)
+          tma_load_3d(dst, map, 0, tile_key0(t), row, bar(kFull + slot));
+        else
+          tma_load_4d(dst, map, 0, tile_key0(t), 0, row, bar(kFull + slot));
       }
     };
     bool waited = !p.early;
@@ -304,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_aux();
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t id_s = tc05::idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t id_o = tc05::idesc_bf16_f32(kBM, kD, false, true);
+      constexpr uint32_t id_s = F8 ? tc05::idesc_e4m3_e5m2_f32(kBM, kBN, false, false)
+                                   : tc05::idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t id_o = F8 ? tc05::idesc_e4m3_e5m2_f32(kBM, kD, false, true)
+                                   : tc05::idesc_bf16_f32(kBM, kD, false, true);
       // waits poll (test_wait): a suspended try_wait woke a third of a
       // microsecond after the phase completed, once per product group
       // (8 x 4096: 1608 -> 1532 us per step)
@@ -318,21 +334,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [&](int q, int t) {  // S_q = Q_q K(t)^T
         const uint32_t q_s = sbase + kQOff + q * kQBytes, k_s = sbase + kRingOff + ((2 * t) % kSlots) * kTileBytes;
         tc05::fence_after_sync();
+        if constexpr (F8) {
+          // S = Q_hi K^T + Q_lo K^T, 32 head dims per product (K-major 8-bit rows)
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc05::mma_bf16(tmem + kColS + q * 128, tc05::smem_desc_sw128(q_s + off, 16, 1024),
-                         tc05::smem_desc_sw128(k_s + off, 16, 1024), id_s, ks > 0);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < kD / 32; ++ks)
+              tc05::mma_f8(tmem + kColS + q * 128, tc05::smem_desc_sw128(q_s + part * 16384 + ks * 32, 16, 1024),
+                           tc05::smem_desc_sw128(k_s + ks * 32, 16, 1024), id_s, part > 0 || ks > 0);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            tc05::mma_bf16(tmem + kColS + q * 128, tc05::smem_desc_sw128(q_s + off, 16, 1024),
+                           tc05::smem_desc_sw128(k_s + off, 16, 1024), id_s, ks > 0);
+          }
         }
         tc05::commit(bar(kSFull + q));
       };
       auto issue_pv = [&](int q, int t, int h) {  // O_q += P_q V(t), keys 64 h .. 64 h + 63
         const uint32_t v_s = sbase + kRingOff + ((2 * t + 1) % kSlots) * kTileBytes;
         tc05::fence_after_sync();
+        if constexpr (F8) {
+          // O += P_hi V + P_lo V, 32 keys per product: P from tensor memory
+          // (hi in the buffer's columns 0-31, lo in 32-63, four keys a
+          // column), V MN-major (8-bit rows of 128 dims)
 #pragma unroll
-        for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-          tc05::mma_bf16_ta(tmem + kColO + q * 128, tmem + kColS + q * 128 + ks * 8,
-                            tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, t > 0 || ks > 0);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 2 * h; ks < 2 * h + 2; ++ks)
+              tc05::mma_f8_ta(tmem + kColO + q * 128, tmem + kColS + q * 128 + part * 32 + ks * 8,
+                              tc05::smem_desc_sw128(v_s + ks * 4096, 16384, 1024), id_o, t > 0 || h > 0 || part > 0 || ks > 0);
+        } else {
+#pragma unroll
+          for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
+            tc05::mma_bf16_ta(tmem + kColO + q * 128, tmem + kColS + q * 128 + ks * 8,
+                              tc05::smem_desc_sw128(v_s + ks * 2048, 16384, 1024), id_o, t > 0 || ks > 0);
+        }
       };
       auto full = [&](int u) { return wait(kFull + u % kSlots, (u / kSlots) & 1); };
       bool ok = wait(kQReady + 0, 0) && wait(kQReady + 1, 0) && full(0);
@@ -398,10 +436,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rr = rbase + i;
           float4 v = *reinterpret_cast<const float4*>(stage + (q * kBM + rr) * (kD * 4) + lane * 16);
           if (q * kBM + rr >= rows) v = make_float4(0.f, 0.f, 0.f, 0.f);
-          uint2 w;
-          w.x = pack_bf16x2(v.x * p.scale_log2, v.y * p.scale_log2);
-          w.y = pack_bf16x2(v.z * p.scale_log2, v.w * p.scale_log2);
-          *reinterpret_cast<uint2*>(qtile + sw128(rr, 4 * lane)) = w;
+          if constexpr (F8) {
+            // e4m3 hi + lo of q * scale * log2(e) * 2^6, chunk c of row rr at c ^ (rr mod 8)
+            const float qs = p.scale_log2 * kQScaleF8;
+            uint32_t hi, lo;
+            tc05::e4m3_split4(v.x * qs, v.y * qs, v.z * qs, v.w * qs, hi, lo);
+            const uint32_t off = rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + (lane & 3) * 4;
+            *reinterpret_cast<uint32_t*>(qtile + off) = hi;
+            *reinterpret_cast<uint32_t*>(qtile + 16384 + off) = lo;
+          } else {
+            uint2 w;
+            w.x = pack_bf16x2(v.x * p.scale_log2, v.y * p.scale_log2);
+            w.y = pack_bf16x2(v.z * p.scale_log2, v.w * p.scale_log2);
+            *reinterpret_cast<uint2*>(qtile + sw128(rr, 4 * lane)) = w;
+          }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -416,15 +464,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4 qv[kD / 4];
 #pragma unroll
       for (int c = 0; c < kD / 4; ++c) qv[c] = live ? qs[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (F8) {
+        const float qs = p.scale_log2 * kQScaleF8;
 #pragma unroll
-      for (int c = 0; c < kD; c += 8) {
-        const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
-        uint4 v;
-        v.x = pack_bf16x2(a.x * p.scale_log2, a.y * p.scale_log2);
-        v.y = pack_bf16x2(a.z * p.scale_log2, a.w * p.scale_log2);
-        v.z = pack_bf16x2(bq.x * p.scale_log2, bq.y * p.scale_log2);
-        v.w = pack_bf16x2(bq.z * p.scale_log2, bq.w * p.scale_log2);
-        *reinterpret_cast<uint4*>(qtile + sw128(r, c)) = v;
+        for (int c = 0; c < kD / 16; ++c) {  // 16 dims per 16-byte chunk
+          uint4 hi, lo;
+          uint32_t* h4 = &hi.x;
+          uint32_t* l4 = &lo.x;
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            const float4 a = qv[4 * c + w4];
+            tc05::e4m3_split4(a.x * qs, a.y * qs, a.z * qs, a.w * qs, h4[w4], l4[w4]);
+          }
+          const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(qtile + off) = hi;
+          *reinterpret_cast<uint4*>(qtile + 16384 + off) = lo;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kD; c += 8) {
+          const float4 a = qv[c / 4], bq = qv[c / 4 + 1];
+          uint4 v;
+          v.x = pack_bf16x2(a.x * p.scale_log2, a.y * p.scale_log2);
+          v.y = pack_bf16x2(a.z * p.scale_log2, a.w * p.scale_log2);
+          v.z = pack_bf16x2(bq.x * p.scale_log2, bq.y * p.scale_log2);
+          v.w = pack_bf16x2(bq.z * p.scale_log2, bq.w * p.scale_log2);
+          *reinterpret_cast<uint4*>(qtile + sw128(r, c)) = v;
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -446,6 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc05::wait_ld();
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) tc05::reg_fence(*reinterpret_cast<float(*)[32]>(&s[c]));
+      if constexpr (F8) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) s[c] *= 1.f / kQScaleF8;  // exact: a power of two
+      }
       const int key0 = tile_key0(t);
       if (q == 0 && key0 + kBN > L) {
         // rows at or past L may hold anything (NaN included); P = 0 there, and
@@ -459,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (!F8) *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
@@ -505,15 +575,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 sm4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+        if constexpr (F8) {
+          // P as e4m3 hi + lo, four keys per column: hi over columns 0-31,
+          // lo over 32-63 (this half: 16 + 16 of them)
+          uint32_t ph[16], pl[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 dd = sub2(make_float2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), e);
-          const float p0 = fast_exp2(dd.x), p1 = fast_exp2(dd.y);
-          sm4[i & 3] = add2(sm4[i & 3], make_float2(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 16; ++i) {
+            const int k0 = 64 * half + 4 * i;
+            const float2 d0 = sub2(make_float2(s[k0], s[k0 + 1]), e), d1 = sub2(make_float2(s[k0 + 2], s[k0 + 3]), e);
+            const float p0 = fast_exp2(d0.x), p1 = fast_exp2(d0.y), p2 = fast_exp2(d1.x), p3 = fast_exp2(d1.y);
+            sm4[(2 * i) & 3] = add2(sm4[(2 * i) & 3], make_float2(p0, p1));
+            sm4[(2 * i + 1) & 3] = add2(sm4[(2 * i + 1) & 3], make_float2(p2, p3));
+            tc05::e4m3_split4(p0, p1, p2, p3, ph[i], pl[i]);
+          }
+          tc05::st_32x32b_x16_u(scol + 16 * half, ph);
+          tc05::st_32x32b_x16_u(scol + 32 + 16 * half, pl);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 dd = sub2(make_float2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), e);
+            const float p0 = fast_exp2(dd.x), p1 = fast_exp2(dd.y);
+            sm4[i & 3] = add2(sm4[i & 3], make_float2(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tc05::st_32x32b_x32_u(scol + 32 * half, pk);
         }
-        tc05::st_32x32b_x32_u(scol + 32 * half, pk);
         // this half of P is in tensor memory: its products may start
         tc05::wait_st();
         tc05::fence_before_sync();
@@ -578,10 +665,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool PG>
+template <bool PG, bool F8>
 cudaError_t launch_prefill_t(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                              cudaStream_t stream) {
-  auto kern = attn_tc05_prefill_kernel<PG>;
+  auto kern = attn_tc05_prefill_kernel<PG, F8>;
   // the register split holds only for the launch count it was made for: a
   // build that launches with fewer registers would leave setmaxnreg.inc
   // waiting for registers that never come, so such a build is not launched
@@ -614,7 +701,8 @@ int tc05_prefill_rows_per_block() { return kQT * kBM; }
 
 cudaError_t launch_tc05_prefill(const Tc05Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tq, cudaStream_t stream) {
-  return p.paged ? launch_prefill_t<true>(p, tk, tv, tq, stream) : launch_prefill_t<false>(p, tk, tv, tq, stream);
+  if (p.f8) return p.paged ? cudaErrorInvalidValue : launch_prefill_t<false, true>(p, tk, tv, tq, stream);
+  return p.paged ? launch_prefill_t<true, false>(p, tk, tv, tq, stream) : launch_prefill_t<false, false>(p, tk, tv, tq, stream);
 }
 
 }  // namespace mqa
